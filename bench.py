@@ -1,0 +1,469 @@
+"""Benchmark: causal linear-attention tokens/s and fraction of the GB300 roofline.
+
+A step is one causal forward + backward (la_forward then la_backward, the whole
+training-direction hot path) over the B=4, H=8, N=16384, D=M=64 bf16 batch
+resident in HBM. `value` is tokens/s over all ranks (a token is one sequence
+position across all H heads). The JSON line also carries the forward-only,
+non-causal and decode parts, the dominant kernel's roofline, the end-to-end
+number through the C ABI with host buffers, and the fp64 oracle's CPU time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal linear-attention tokens/s (fwd, fwd+bwd, decode) and % of GB300 roofline"
+MAIN = "causal_fwdbwd_b4h8n16384d64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    except Exception:
+        return dict(FALLBACK_PEAKS)
+
+
+# Algorithmic bytes per token-head (bf16 inputs, float32 gradients).
+def fwd_bytes(w):
+    return 2 * (2 * w.D + 2 * w.M)                     # q, k, v read + out written
+
+
+def bwd_bytes(w):
+    return 2 * (2 * w.D + 2 * w.M) + 4 * (2 * w.D + w.M)  # q,k,v,dout read; dq,dk,dv written
+
+
+def decode_bytes(w):
+    return 8 * w.D * w.M + 8 * w.D + 2 * (2 * w.D + 2 * w.M)  # S, Z read+write; q,k,v,out
+
+
+class Clocks:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return self
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="la_clocks_", suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            [exe, "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+             "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-parts", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def device_inputs(w, device, dout=False):
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    q = inputs.torch_normal(g, (w.B, w.H, w.N, w.D), w.scale, w.dtype, device)
+    k = inputs.torch_normal(g, (w.B, w.H, w.N, w.D), w.scale, w.dtype, device)
+    v = inputs.torch_normal(g, (w.B, w.H, w.N, w.M), w.scale, w.dtype, device)
+    if dout:
+        d = inputs.torch_normal(g, (w.B, w.H, w.N, w.M), w.scale, w.dtype, device)
+        return q, k, v, d, g
+    return q, k, v, g
+
+
+def l2_flush_buffer(device):
+    import torch
+    return torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+
+def time_calls(fn, reps, warm, flush=None):
+    """Per-call CUDA-event times (ms) on the current stream; optional L2 flush between calls."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def run_parts(la, device, peaks, reps=10):
+    """Forward-only, non-causal and decode throughput on their own workloads."""
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    parts = {}
+    flush = l2_flush_buffer(device)
+    hbm = peaks["hbm_gbs"]
+    for name in ("causal_fwdbwd_b4h8n16384d64", "causal_fwd_b8h8n3072d64",
+                 "noncausal_fwd_b4h8n4096d64"):
+        w = inputs.WORKLOADS[name]
+        q, k, v, _ = device_inputs(w, device)
+        out = torch.empty((w.B, w.H, w.N, w.M), dtype=q.dtype, device=device)
+        ws = torch.empty(la.la_forward_workspace_bytes(w.B, w.H, w.N, w.D, w.M, w.causal),
+                         dtype=torch.uint8, device=device)
+        t = time_calls(lambda: la.la_forward(q, k, v, w.causal, out, ws), reps, 3, flush)
+        ms = statistics.median(t)
+        th = w.B * w.H * w.N
+        gbs = th * fwd_bytes(w) / (ms * 1e-3) / 1e9
+        key = ("causal_fwd_b4h8n16384d64" if name == MAIN else name)
+        parts[key] = {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms": ms,
+                      "hbm_gbs": gbs, "roofline_frac": gbs / hbm, "l2": "flushed between calls"}
+        del q, k, v, out
+    # decode: prefill, then the per-token steps replayed from a CUDA graph
+    w = inputs.WORKLOADS["decode_s256h8d64_prefill1024_steps3072"]
+    q, k, v, g = device_inputs(w, device)
+    T = w.steps
+    sq = inputs.torch_normal(g, (T, w.B, w.H, w.D), w.scale, w.dtype, device)
+    sk = inputs.torch_normal(g, (T, w.B, w.H, w.D), w.scale, w.dtype, device)
+    sv = inputs.torch_normal(g, (T, w.B, w.H, w.M), w.scale, w.dtype, device)
+    outs = torch.empty((T, w.B, w.H, w.M), dtype=q.dtype, device=device)
+    _, S, Z = la.la_prefill(q, k, v)
+    S0, Z0 = S.clone(), Z.clone()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for t in range(3):
+            la.la_decode_step(sq[t], sk[t], sv[t], S, Z, out=outs[t])
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(T):
+            la.la_decode_step(sq[t], sk[t], sv[t], S, Z, out=outs[t])
+
+    def replay():
+        S.copy_(S0)
+        Z.copy_(Z0)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    replay()
+    ms = statistics.median([replay() for _ in range(3)])
+    per_step = ms / T
+    gbs = w.B * w.H * decode_bytes(w) / (per_step * 1e-3) / 1e9
+    parts["decode_s256h8d64_prefill1024_steps3072"] = {
+        "tokens_per_s": w.B * T / (ms * 1e-3), "ms_per_step": per_step, "hbm_gbs": gbs,
+        "roofline_frac": gbs / hbm, "steps": T, "launch": "CUDA graph of 3072 la_decode_step calls",
+        "l2": "S/Z state (33.5 MB) fits in L2; fraction can exceed 1"}
+    return parts
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import kernelized_causal_self_gb300 as la
+    from kernelized_causal_self_gb300 import build as labuild
+    from kernelized_causal_self_gb300 import inputs
+
+    labuild.build()
+    la.load_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    w = inputs.WORKLOADS[MAIN]
+    q, k, v, dout, _ = device_inputs(w, device, dout=True)
+    out = torch.empty((w.B, w.H, w.N, w.M), dtype=q.dtype, device=device)
+    f32 = torch.float32
+    dq = torch.empty((w.B, w.H, w.N, w.D), dtype=f32, device=device)
+    dk = torch.empty((w.B, w.H, w.N, w.D), dtype=f32, device=device)
+    dv = torch.empty((w.B, w.H, w.N, w.M), dtype=f32, device=device)
+    wsf = torch.empty(la.la_forward_workspace_bytes(w.B, w.H, w.N, w.D, w.M, True),
+                      dtype=torch.uint8, device=device)
+    wsb = torch.empty(la.la_backward_workspace_bytes(w.B, w.H, w.N, w.D, w.M, True),
+                      dtype=torch.uint8, device=device)
+    st = torch.cuda.current_stream(device)
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def step(i=None):
+        if i is not None:
+            ev[i][0].record(st)
+        la.la_forward(q, k, v, True, out, wsf)
+        if i is not None:
+            ev[i][1].record(st)
+        la.la_backward(q, k, v, dout, True, dq, dk, dv, wsb)
+        if i is not None:
+            ev[i][2].record(st)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    n0 = la.la_kernel_launches()
+    with Clocks(torch.cuda.current_device() if local == 0 else local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(st)
+        for i in range(K):
+            step(i)
+        t_end.record(st)
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = la.la_kernel_launches() - n0
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, device)
+    ms_step = ms_total / K
+    tokens = w.B * w.N * world
+    value = tokens / (ms_step * 1e-3)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    th = w.B * w.H * w.N
+    hbm = peaks["hbm_gbs"]
+    cand = {"la_backward": (bwd_ms, th * bwd_bytes(w), bwd_bytes(w)),
+            "la_forward": (fwd_ms, th * fwd_bytes(w), fwd_bytes(w))}
+    dom = max(cand, key=lambda n: cand[n][0])
+    d_ms, d_bytes, per_unit = cand[dom]
+    achieved = d_bytes / (d_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "peak_source": peaks.get("source"),
+                "algorithmic_bytes_per_token_head": per_unit, "token_heads_per_launch": th,
+                "launch_ms": d_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
+                   "step": "la_forward + la_backward (causal)", "grads": "float32",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs+outputs 470 MB per step > 129 MB L2 (no flush needed)"},
+        "roofline": roofline, "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(la, w, q, k, v, dout, device, K=max(2, min(K, 5)))
+    if not args.no_parts:
+        del q, k, v, dout, dq, dk, dv, out
+        torch.cuda.empty_cache()
+        result["parts"] = run_parts(la, device, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(la, w, q, k, v, dout, device, K):
+    """Same step through the C ABI with pinned host buffers: H2D of q, k, v, dout, then
+    forward + backward, then D2H of out, dq, dk, dv, all inside the timed region."""
+    import torch
+    hq, hk, hv, hd = (t.cpu().pin_memory() for t in (q, k, v, dout))
+    f32 = torch.float32
+    ho = torch.empty(tuple(q.shape[:3]) + (w.M,), dtype=q.dtype).pin_memory()
+    hdq = torch.empty(q.shape, dtype=f32).pin_memory()
+    hdk = torch.empty(q.shape, dtype=f32).pin_memory()
+    hdv = torch.empty(tuple(q.shape[:3]) + (w.M,), dtype=f32).pin_memory()
+    dq_, dk_, dv_ = (torch.empty_like(x) for x in (q, k, v))
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dout.copy_(hd, non_blocking=True)
+        o = la.la_forward(q, k, v, True)
+        gq, gk, gv = la.la_backward(q, k, v, dout, True)
+        ho.copy_(o, non_blocking=True)
+        hdq.copy_(gq, non_blocking=True)
+        hdk.copy_(gk, non_blocking=True)
+        hdv.copy_(gv, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    b.synchronize()
+    ms = a.elapsed_time(b) / K
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hd))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
+    del dq_, dk_, dv_
+    return {"value": w.B * w.N / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device, la_forward + la_backward, device -> pinned host"}
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """fp64 oracle (as it stands) on host cores: causal forward + backward of one (b, h)
+    sequence per sample, as many samples as fit in ~budget_s."""
+    import numpy as np
+    import oracle
+    from kernelized_causal_self_gb300 import inputs
+    n = w.N
+    q, k, v = inputs.qkv(w.seed, 1, 1, n, w.D, w.M, w.scale, w.dtype)
+    g = inputs.upstream_grad(w.seed, 1, 1, n, w.M, w.scale, w.dtype)
+    q, k, v, g = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        oracle.forward(q, k, v, True)
+        oracle.backward(q, k, v, g, True)
+        done += 1
+        if time.perf_counter() - t0 > budget_s or done >= 4:
+            break
+    sec = time.perf_counter() - t0
+    tokens = done * n / w.H           # one head of N positions = N/H token-equivalents
+    return {"value": tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} x (one (b,h) sequence, N={n}, causal fwd + bwd, float64 NumPy, "
+                      f"single thread), {sec:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 oracle on the host, a bounded sample per step."""
+    if rank != 0:
+        return
+    from kernelized_causal_self_gb300 import inputs
+    import oracle
+    w = inputs.WORKLOADS[MAIN]
+    n = 2048   # first 2048 positions of one (b, h) sequence per step
+    q, k, v = inputs.qkv(w.seed, 1, 1, n, w.D, w.M, w.scale, w.dtype)
+    g = inputs.upstream_grad(w.seed, 1, 1, n, w.M, w.scale, w.dtype)
+    q, k, v, g = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
+
+    def step():
+        oracle.forward(q, k, v, True)
+        oracle.backward(q, k, v, g, True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = (time.perf_counter() - t0) / args.steps
+    value = (n / w.H) / sec
+    sample = (f"per step: causal fwd + bwd of the first {n} positions of one (b,h) sequence "
+              f"of {MAIN}, float64 NumPy oracle, single thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
+                   "sample_positions": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) kernelized linear-attention library.
+ *
+ * Method: "Transformers are RNNs: Fast Autoregressive Transformers with
+ * Linear Attention" (Katharopoulos et al., ICML 2020), as summarised on the
+ * pages cited per entry point below:
+ *   [review]  "[Paper Review] Transformers are RNNs ..." (nubint.ai), "Proposed method"
+ *   [summary] "Transformers are RNNs: Fast Autoregressive Transformers with
+ *             Linear Attention" (paperlayer.ai), paper sections 3.1-3.4, App. A
+ *   [deck]    "Transformers are RNNs ... 解读" (zhengyuhong.cn), slides 3-4
+ *
+ * phi(x) = elu(x) + 1 (ELU alpha = 1): x + 1 for x > 0, exp(x) otherwise.
+ * No 1/sqrt(D) scale and no epsilon are applied inside the operator.
+ *
+ * Layouts (all row-major, contiguous, no padding):
+ *   q, k        [B][H][N][D]      element type `dtype`
+ *   v, out      [B][H][N][M]      element type `dtype`
+ *   dout        [B][H][N][M]      element type `dtype`
+ *   dq, dk      [B][H][N][D]      float32
+ *   dv          [B][H][N][M]      float32
+ *   S           [B][H][D][M]      float32  (attention memory, S[d][m])
+ *   Z           [B][H][D]         float32  (normalizer memory)
+ *   decode q,k  [n_streams][H][D], decode v,out [n_streams][H][M]
+ *
+ * Ownership and threading: every pointer is device memory owned by the
+ * caller; the library never allocates, frees or synchronises. All calls are
+ * asynchronous on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ * default stream). The only process-wide state is an atomic count of kernel
+ * launches (la_kernel_launches), so calls from several host threads are safe.
+ * Outputs must not alias inputs (S and Z of la_decode_step are updated in
+ * place by design).
+ *
+ * Supported shapes: B, H >= 1; N >= 0 (N == 0 is a no-op); D and M multiples
+ * of 8 in [8, 128]; pointers 16-byte aligned. dtype is LA_F32 or LA_BF16;
+ * accumulation and carried state are always float32. Shapes outside this
+ * set return LA_ERR_INVALID_ARG before anything is launched.
+ *
+ * Errors: every entry point returns an int status and never throws.
+ * la_status_string() maps it to a message.
+ */
+#ifndef LA_H_
+#define LA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum la_status {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1, /* null pointer, bad dimension, unsupported D/M, misaligned pointer */
+  LA_ERR_WORKSPACE = 2,   /* workspace missing or smaller than the *_workspace_bytes() size */
+  LA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  LA_ERR_TIMEOUT = 4      /* a bounded cross-CTA wait expired (see la_workspace_status) */
+};
+
+enum la_dtype { LA_F32 = 0, LA_BF16 = 1 };
+
+/* Human-readable text for a status code; never NULL. */
+const char* la_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int la_version(void);
+
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all entry points, all threads; memsets are not counted). */
+unsigned long long la_kernel_launches(void);
+
+/*
+ * Scratch needed by la_forward / la_prefill for this shape, in bytes (0 if
+ * none). The caller allocates it (16-byte aligned, contents irrelevant) and
+ * passes it in; it must not be shared by calls that may run concurrently.
+ */
+size_t la_forward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype);
+
+/*
+ * la_forward -- kernelized attention forward, out = V'.
+ *
+ * causal != 0: [deck slide 4], [summary §3.3]:
+ *   S_i = S_{i-1} + phi(K_i) V_i^T,  Z_i = Z_{i-1} + phi(K_i),
+ *   out_i = phi(Q_i)^T S_i / (phi(Q_i)^T Z_i)      (inclusive mask j <= i)
+ * causal == 0: [review, "Proposed method"], [deck slide 3]:
+ *   S = sum_j phi(K_j) V_j^T, Z = sum_j phi(K_j), out_i = phi(Q_i)^T S / phi(Q_i)^T Z
+ *
+ * q, k, v: inputs (see layouts); out: output, same dtype as the inputs.
+ * workspace/workspace_bytes: caller scratch of la_forward_workspace_bytes().
+ * Returns LA_OK, LA_ERR_INVALID_ARG, LA_ERR_WORKSPACE or LA_ERR_CUDA.
+ */
+int la_forward(const void* q, const void* k, const void* v, void* out,
+               int B, int H, int N, int D, int M, int causal, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * la_prefill -- causal forward that also writes the final recurrent state.
+ *
+ * [summary §3.4], [review, "Proposed method"]: a causally masked layer is an
+ * RNN with attention memory s and normalizer memory z. Writes out as
+ * la_forward(causal=1) and S[b][h] = S_N, Z[b][h] = Z_N (float32), which
+ * la_decode_step then continues. B plays the role of independent streams.
+ * Workspace: la_forward_workspace_bytes(B, H, N, D, M, 1, dtype).
+ * N == 0 writes S = 0, Z = 0.
+ */
+int la_prefill(const void* q, const void* k, const void* v, void* out, float* S, float* Z,
+               int B, int H, int N, int D, int M, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch needed by la_backward for this shape, in bytes. */
+size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype);
+
+/*
+ * la_backward -- gradients of sum(dout * out) w.r.t. q, k, v.
+ *
+ * [summary §3.3.1, App. A]: cumulative-sum gradients, never storing every S_i;
+ * the phi(Q) gradient is a forward-direction scan over (S_i, Z_i), the phi(K)
+ * and V gradients a reverse-direction scan over R_j = sum_{i>=j} phi(Q_i) gN_i^T
+ * and r_j = sum_{i>=j} gd_i phi(Q_i), with gN_i = dout_i / den_i and
+ * gd_i = -(dout_i . out_i) / den_i (the normalizer's quotient-rule terms):
+ *   dphiQ_i = S_i gN_i + gd_i Z_i,  dphiK_j = R_j V_j + r_j,  dV_j = R_j^T phi(K_j),
+ *   dq = dphiQ * phi'(q),  dk = dphiK * phi'(k).
+ * Non-causal uses the full sums in both directions. The forward quantities are
+ * recomputed, not read from a saved forward.
+ *
+ * q, k, v, dout: inputs in `dtype`; dq, dk, dv: float32 outputs.
+ */
+int la_backward(const void* q, const void* k, const void* v, const void* dout,
+                float* dq, float* dk, float* dv,
+                int B, int H, int N, int D, int M, int causal, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * la_decode_step -- one recurrent generation step per (stream, head).
+ *
+ * [deck slide 4], [summary §3.3.2, §3.4]: update, then read out:
+ *   S <- S + phi(k) v^T,  Z <- Z + phi(k),  out = phi(q)^T S / phi(q)^T Z.
+ * q, k: [n_streams][H][D]; v, out: [n_streams][H][M] in `dtype`;
+ * S [n_streams][H][D][M] and Z [n_streams][H][D] float32, updated in place.
+ * Needs no workspace.
+ */
+int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
+                   int n_streams, int H, int D, int M, int dtype, void* stream);
+
+/*
+ * la_workspace_status -- synchronises `stream` and reads the status word a
+ * previous la_forward / la_prefill / la_backward left in `workspace`:
+ * LA_OK, or LA_ERR_TIMEOUT if a bounded cross-CTA wait gave up (the outputs
+ * of that call are then invalid). Clears the word. Debug / test use.
+ */
+int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H_ */

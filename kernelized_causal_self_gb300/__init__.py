@@ -1,0 +1,210 @@
+"""Thin Python binding over the C ABI in ``include/la.h``.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their ``data_ptr()`` and the current CUDA stream are handed to the
+shared library, and outputs/workspaces are allocated with PyTorch (the caller's
+allocator). Every step of the computation runs in the library's CUDA kernels;
+there is no fallback. If the library is missing the calls raise.
+"""
+
+import ctypes
+import os
+
+__all__ = [
+    "la_forward", "la_prefill", "la_backward", "la_decode_step",
+    "la_forward_workspace_bytes", "la_backward_workspace_bytes",
+    "la_workspace_status", "la_status_string", "la_kernel_launches", "library_path",
+    "load_library",
+    "LAError", "LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_WORKSPACE", "LA_ERR_CUDA",
+    "LA_ERR_TIMEOUT", "LA_F32", "LA_BF16",
+]
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LA_F32, LA_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "liblagb300.so")
+_lib = None
+
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+_SIGNATURES = {
+    "la_status_string": (ctypes.c_char_p, [_c_int]),
+    "la_version": (_c_int, []),
+    "la_kernel_launches": (ctypes.c_ulonglong, []),
+    "la_forward_workspace_bytes": (_c_size, [_c_int] * 7),
+    "la_backward_workspace_bytes": (_c_size, [_c_int] * 7),
+    "la_forward": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
+    "la_prefill": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_backward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
+    "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
+    "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
+}
+
+
+class LAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {la_status_string(status)} (status {status})")
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the shared library (ctypes); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library not built: {_LIB_PATH} is missing "
+                "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def la_status_string(status):
+    return load_library().la_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != LA_OK:
+        raise LAError(fn, status)
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _stream_ptr(device):
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _workspace(nbytes, device, workspace):
+    import torch
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def la_kernel_launches():
+    """Kernels launched by the library in this process so far."""
+    return int(load_library().la_kernel_launches())
+
+
+def la_forward_workspace_bytes(B, H, N, D, M, causal=True, dtype=LA_BF16):
+    return load_library().la_forward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dtype)
+
+
+def la_backward_workspace_bytes(B, H, N, D, M, causal=True, dtype=LA_BF16):
+    return load_library().la_backward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dtype)
+
+
+def la_forward(q, k, v, causal=True, out=None, workspace=None):
+    """out[B,H,N,M] = kernelized attention of q, k [B,H,N,D] and v [B,H,N,M]."""
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v shapes/dtypes do not match")
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _need_cuda(out)
+    nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
+    ws = _workspace(nbytes, q.device, workspace)
+    st = lib.la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D, M,
+                        int(bool(causal)), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                        _stream_ptr(q.device))
+    _check("la_forward", st)
+    return out
+
+
+def la_prefill(q, k, v, out=None, S=None, Z=None, workspace=None):
+    """Causal forward plus the final float32 state S [B,H,D,M], Z [B,H,D]."""
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dev = q.device
+    out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
+    S = torch.empty((B, H, D, M), dtype=torch.float32, device=dev) if S is None else S
+    Z = torch.empty((B, H, D), dtype=torch.float32, device=dev) if Z is None else Z
+    _need_cuda(out, S, Z)
+    nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.la_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S.data_ptr(),
+                        Z.data_ptr(), B, H, N, D, M, dt, ws.data_ptr(),
+                        ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check("la_prefill", st)
+    return out, S, Z
+
+
+def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace=None):
+    """float32 gradients (dq, dk, dv) of sum(dout * la_forward(q, k, v))."""
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v, dout)
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dev = q.device
+    f32 = torch.float32
+    dq = torch.empty((B, H, N, D), dtype=f32, device=dev) if dq is None else dq
+    dk = torch.empty((B, H, N, D), dtype=f32, device=dev) if dk is None else dk
+    dv = torch.empty((B, H, N, M), dtype=f32, device=dev) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    nbytes = lib.la_backward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                         dk.data_ptr(), dv.data_ptr(), B, H, N, D, M, int(bool(causal)), dt,
+                         ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check("la_backward", st)
+    return dq, dk, dv
+
+
+def la_decode_step(q, k, v, S, Z, out=None):
+    """One recurrent step: q, k [S,H,D], v [S,H,M]; S, Z updated in place; returns out."""
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v, S, Z)
+    n, H, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty((n, H, M), dtype=q.dtype, device=q.device) if out is None else out
+    st = lib.la_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), S.data_ptr(), Z.data_ptr(),
+                            out.data_ptr(), n, H, D, M, dt, _stream_ptr(q.device))
+    _check("la_decode_step", st)
+    return out
+
+
+def la_workspace_status(workspace):
+    """Synchronise and read (then clear) the status word a call left in `workspace`."""
+    lib = load_library()
+    return lib.la_workspace_status(workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   _stream_ptr(workspace.device))

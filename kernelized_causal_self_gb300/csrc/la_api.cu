@@ -1,0 +1,164 @@
+// C-ABI entry points: argument validation and kernel selection.
+//
+// Every entry point validates its arguments on the host, launches on the
+// caller's stream and returns a status; nothing is allocated, synchronised or
+// thrown across the boundary.
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <initializer_list>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace la
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dims(int B, int H, int N, int D, int M) {
+  if (B < 1 || H < 1 || N < 0) return false;
+  if (D < 8 || D > 128 || (D % 8) != 0) return false;
+  if (M < 8 || M > 128 || (M % 8) != 0) return false;
+  // element offsets are formed in 64-bit; keep B*H inside a grid dimension
+  if ((long long)B * H > 0x7fffffffLL) return false;
+  return true;
+}
+
+bool valid_dtype(int dtype) { return dtype == LA_F32 || dtype == LA_BF16; }
+
+bool ptrs_ok(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr || !aligned16(p)) return false;
+  return true;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// The caller's workspace arrives with arbitrary contents: clear its header
+// (status word, work counters) on the stream before any kernel reads it.
+cudaError_t clear_header(void* ws, cudaStream_t st) {
+  return cudaMemsetAsync(ws, 0, la::kHeaderBytes, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* la_status_string(int status) {
+  switch (status) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARG:
+      return "invalid argument (null or misaligned pointer, bad dimension, or unsupported D/M/dtype)";
+    case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LA_ERR_CUDA: return "CUDA runtime error";
+    case LA_ERR_TIMEOUT: return "a bounded cross-CTA wait expired; outputs are invalid";
+    default: return "unknown status";
+  }
+}
+
+int la_version(void) { return 100; }
+
+unsigned long long la_kernel_launches(void) {
+  return la::g_launches.load(std::memory_order_relaxed);
+}
+
+size_t la_forward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
+  (void)B; (void)H; (void)N; (void)D; (void)M; (void)causal; (void)dtype;
+  return la::kHeaderBytes;
+}
+
+int la_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int N, int D,
+               int M, int causal, int dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = clear_header(workspace, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::simt_forward(q, k, v, out, nullptr, nullptr, B * H, N, D, M, causal != 0,
+                                    dtype, st));
+}
+
+int la_prefill(const void* q, const void* k, const void* v, void* out, float* S, float* Z, int B,
+               int H, int N, int D, int M, int dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S, Z})) return LA_ERR_INVALID_ARG;
+  if (N == 0) {
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)B * H * D * M, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(Z, 0, sizeof(float) * (size_t)B * H * D, st);
+    return from_cuda(e);
+  }
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = clear_header(workspace, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::simt_forward(q, k, v, out, S, Z, B * H, N, D, M, true, dtype, st));
+}
+
+size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
+  (void)D; (void)M; (void)causal; (void)dtype;
+  if (B < 1 || H < 1 || N < 0) return la::kHeaderBytes;
+  return la::simt_backward_workspace(B * H, N);
+}
+
+int la_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                float* dk, float* dv, int B, int H, int N, int D, int M, int causal, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, dout, dq, dk, dv})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_backward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = clear_header(workspace, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::simt_backward(q, k, v, dout, dq, dk, dv, B * H, N, D, M, causal != 0,
+                                     dtype, workspace, st));
+}
+
+int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
+                   int n_streams, int H, int D, int M, int dtype, void* stream) {
+  if (!valid_dims(n_streams, H, 1, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({q, k, v, S, Z, out})) return LA_ERR_INVALID_ARG;
+  return from_cuda(la::decode_step(q, k, v, S, Z, out, n_streams * H, D, M, dtype,
+                                   as_stream(stream)));
+}
+
+int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || workspace_bytes < la::kHeaderBytes) return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  la::WorkspaceHeader h;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (h.status != LA_OK) {
+    const int zero = 0;
+    e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return LA_ERR_CUDA;
+    return h.status == LA_ERR_TIMEOUT ? LA_ERR_TIMEOUT : LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,25 @@
+// Launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace la {
+
+// Adds n to the process-wide kernel launch count reported by la_kernel_launches().
+void count_launches(unsigned n);
+
+// ---- general-shape CUDA-core path (any dtype, D and M multiples of 8 up to 128)
+cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
+                         float* Z_out, int BH, int N, int D, int M, bool causal, int dtype,
+                         cudaStream_t st);
+size_t simt_backward_workspace(int BH, int N);
+cudaError_t simt_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                          float* dk, float* dv, int BH, int N, int D, int M, bool causal,
+                          int dtype, void* ws, cudaStream_t st);
+
+// ---- decode step (memory-bound CUDA-core kernel)
+cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
+                        int n_sh, int D, int M, int dtype, cudaStream_t st);
+
+}  // namespace la

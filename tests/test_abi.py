@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every symbol include/la.h declares, and rejects bad arguments on the
+host before anything is launched."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import kernelized_causal_self_gb300 as la
+from kernelized_causal_self_gb300 import build as labuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+FAKE = 0x10000      # 16-byte aligned, never dereferenced: every call below returns first
+ODD = 0x10008       # 8-byte aligned only
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(la_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    labuild.build()
+    return la.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill",
+              "la_forward_workspace_bytes", "la_backward_workspace_bytes",
+              "la_status_string", "la_workspace_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", la.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (la_\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_binding_mirrors_the_abi_names():
+    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill",
+              "la_forward_workspace_bytes", "la_backward_workspace_bytes",
+              "la_status_string", "la_workspace_status"):
+        assert callable(getattr(la, n))
+
+
+def test_status_strings(lib):
+    for code in range(0, 6):
+        s = lib.la_status_string(code)
+        assert s and len(s) > 1
+    assert lib.la_status_string(0) == b"ok"
+    assert lib.la_version() >= 100
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, H=1, N=16, D=64, M=64, causal=1, dtype=1,
+         ws=FAKE, wsb=1 << 20):
+    return lib.la_forward(q, k, v, out, B, H, N, D, M, causal, dtype, ws, wsb, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert _fwd(lib, q=0) == la.LA_ERR_INVALID_ARG
+    assert _fwd(lib, out=ODD) == la.LA_ERR_INVALID_ARG
+    for D, M in ((0, 64), (12, 64), (64, 7), (136, 64), (64, 256)):
+        assert _fwd(lib, D=D, M=M) == la.LA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == la.LA_ERR_INVALID_ARG
+    assert _fwd(lib, N=-1) == la.LA_ERR_INVALID_ARG
+    assert _fwd(lib, dtype=7) == la.LA_ERR_INVALID_ARG
+    assert _fwd(lib, ws=0) == la.LA_ERR_WORKSPACE
+    assert _fwd(lib, ws=ODD) == la.LA_ERR_WORKSPACE
+    assert _fwd(lib, wsb=16) == la.LA_ERR_WORKSPACE
+
+
+def test_empty_sequence_is_a_noop(lib):
+    assert _fwd(lib, q=0, k=0, v=0, out=0, N=0) == la.LA_OK
+    assert lib.la_backward(0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 64, 64, 1, 1, 0, 0, None) == la.LA_OK
+
+
+def test_backward_and_decode_reject_bad_arguments(lib):
+    ws = lib.la_backward_workspace_bytes(1, 1, 16, 64, 64, 1, 1)
+    args = [FAKE] * 7 + [1, 1, 16, 64, 64, 1, 1, FAKE, ws, None]
+    assert lib.la_backward(*args[:6], 0, *args[7:]) == la.LA_ERR_INVALID_ARG
+    assert lib.la_backward(*args[:14], FAKE, ws - 1, None) == la.LA_ERR_WORKSPACE
+    assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 8, 64, 64, 1, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 60, 64, 1, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 64, 64, 1, None) == \
+        la.LA_ERR_INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    for causal in (0, 1):
+        a = lib.la_forward_workspace_bytes(4, 8, 1024, 64, 64, causal, 1)
+        b = lib.la_forward_workspace_bytes(4, 8, 16384, 64, 64, causal, 1)
+        assert 256 <= a <= b
+        c = lib.la_backward_workspace_bytes(4, 8, 1024, 64, 64, causal, 1)
+        d = lib.la_backward_workspace_bytes(4, 8, 16384, 64, 64, causal, 1)
+        assert 256 <= c <= d
+        assert a % 16 == 0 and c % 16 == 0

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases span several chunks/tiles with ragged tails and the degenerate
+shapes (N = 1, D != M, tiny D/M); the named workloads run at full size with a
+sample of their sequences checked one by one against the oracle. Tolerances
+(max relative error with a 1e-3*max|ref| floor): 1e-4 for float32 inputs,
+2e-2 for bfloat16 inputs (float32 accumulation).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from kernelized_causal_self_gb300 import inputs
+from tests.helpers import TOL, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def la():
+    from kernelized_causal_self_gb300 import build
+    build.build()
+    import kernelized_causal_self_gb300 as pkg
+    pkg.load_library()
+    return pkg
+
+
+DEV = "cuda:0"
+
+
+def _t(x, dtype):
+    return inputs.to_torch(x, dtype, DEV)
+
+
+def _fwd_case(la, seed, B, H, N, D, M, dtype, causal, scale):
+    q, k, v = inputs.qkv(seed, B, H, N, D, M, scale, dtype)
+    out = la.la_forward(_t(q, dtype), _t(k, dtype), _t(v, dtype), causal=causal)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), (q, k, v)
+
+
+# ------------------------------------------------------------------ forward
+
+def test_forward_f32_b1h1n64d32_both_forms(la):
+    got, (q, k, v) = _fwd_case(la, 0, 1, 1, 64, 32, 32, inputs.F32, True, 1.0)
+    assert max_rel_err(got, oracle.masked_attention(q, k, v, causal=True)) < TOL["f32"]
+    assert max_rel_err(got, oracle.recurrent_attention(q, k, v)[0]) < TOL["f32"]
+
+
+SMALL = [
+    (1, 1, 1, 64, 64), (2, 3, 5, 64, 64), (2, 2, 127, 64, 64), (1, 2, 128, 64, 64),
+    (2, 1, 129, 64, 64), (1, 2, 300, 64, 64), (1, 1, 1000, 64, 64), (3, 1, 257, 32, 16),
+    (1, 2, 200, 16, 128), (1, 1, 70, 8, 8), (1, 1, 333, 128, 128), (1, 1, 64, 64, 32),
+]
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F32])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "b%dh%dn%dd%dm%d" % s)
+def test_forward_small(la, shape, dtype, causal):
+    B, H, N, D, M = shape
+    scale = 0.125 if dtype == inputs.BF16 else 1.0
+    got, (q, k, v) = _fwd_case(la, 100 + N, B, H, N, D, M, dtype, causal, scale)
+    want = oracle.forward(q, k, v, causal)
+    assert max_rel_err(got, want) < TOL[dtype]
+
+
+def test_forward_constant_v(la):
+    # out_i = c exactly for constant V (normalisation); bf16 output rounding only
+    B, H, N, D, M = 2, 2, 517, 64, 64
+    q, k, _ = inputs.qkv(7, B, H, N, D, M, 0.125, inputs.BF16)
+    c = inputs.bf16_round(np.linspace(-1.0, 1.0, M, dtype=np.float32))
+    v = np.broadcast_to(c, (B, H, N, M)).copy()
+    for causal in (True, False):
+        out = la.la_forward(_t(q, inputs.BF16), _t(k, inputs.BF16), _t(v, inputs.BF16), causal)
+        got = out.float().cpu().numpy()
+        assert max_rel_err(got, np.broadcast_to(c, got.shape)) < 8e-3
+
+
+def test_forward_large_magnitude_inputs(la):
+    # N(0,1) bf16 inputs (no 1/8 scale): phi spans exp(-4)..5
+    got, (q, k, v) = _fwd_case(la, 9, 2, 2, 640, 64, 64, inputs.BF16, True, 1.0)
+    assert max_rel_err(got, oracle.forward(q, k, v, True)) < TOL["bf16"]
+
+
+# ----------------------------------------------------------------- backward
+
+BWD = [
+    (1, 2, 100, 32, 32, inputs.F32), (2, 1, 129, 64, 64, inputs.F32),
+    (2, 2, 300, 64, 64, inputs.BF16), (1, 1, 1, 64, 64, inputs.BF16),
+    (1, 2, 257, 32, 64, inputs.BF16), (1, 1, 517, 64, 64, inputs.BF16),
+]
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("case", BWD, ids=lambda s: "b%dh%dn%dd%dm%d-%s" % s)
+def test_backward_small(la, case, causal):
+    B, H, N, D, M, dtype = case
+    scale = 0.125 if dtype == inputs.BF16 else 1.0
+    q, k, v = inputs.qkv(200 + N, B, H, N, D, M, scale, dtype)
+    g = inputs.upstream_grad(200 + N, B, H, N, M, scale, dtype)
+    dq, dk, dv = la.la_backward(_t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, dtype), causal)
+    torch.cuda.synchronize()
+    wq, wk, wv = oracle.backward(q, k, v, g, causal)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        err = max_rel_err(got.cpu().numpy(), want)
+        assert err < TOL[dtype], (name, err)
+
+
+# ------------------------------------------------------------ prefill/decode
+
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F32])
+def test_prefill_then_decode_matches_forward(la, dtype):
+    S_, H, P, T, D, M = 5, 3, 130, 6, 64, 64
+    scale = 0.125 if dtype == inputs.BF16 else 1.0
+    q, k, v = inputs.qkv(300, S_, H, P + T, D, M, scale, dtype)
+    want = oracle.forward(q, k, v, True)
+    tq, tk, tv = _t(q, dtype), _t(k, dtype), _t(v, dtype)
+    out, S, Z = la.la_prefill(tq[:, :, :P].contiguous(), tk[:, :, :P].contiguous(),
+                              tv[:, :, :P].contiguous())
+    torch.cuda.synchronize()
+    assert max_rel_err(out.float().cpu().numpy(), want[:, :, :P]) < TOL[dtype]
+    _, S_ref, Z_ref = oracle.prefill(q[:, :, :P], k[:, :, :P], v[:, :, :P])
+    assert max_rel_err(S.cpu().numpy(), S_ref) < 1e-4
+    assert max_rel_err(Z.cpu().numpy(), Z_ref) < 1e-5
+    for t in range(P, P + T):
+        o = la.la_decode_step(tq[:, :, t].contiguous(), tk[:, :, t].contiguous(),
+                              tv[:, :, t].contiguous(), S, Z)
+        torch.cuda.synchronize()
+        assert max_rel_err(o.float().cpu().numpy(), want[:, :, t]) < TOL[dtype]
+
+
+def test_decode_step_odd_shapes(la):
+    for D, M in ((8, 8), (32, 16), (128, 128), (16, 120)):
+        n, H = 3, 2
+        q = inputs.normal(1, (n, H, D), 1.0, inputs.F32, 0)
+        k = inputs.normal(1, (n, H, D), 1.0, inputs.F32, 1)
+        v = inputs.normal(1, (n, H, M), 1.0, inputs.F32, 2)
+        S0 = np.abs(inputs.normal(1, (n, H, D, M), 1.0, inputs.F32, 3))
+        Z0 = np.abs(inputs.normal(1, (n, H, D), 1.0, inputs.F32, 4)) + 1.0
+        tS, tZ = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+        o = la.la_decode_step(_t(q, inputs.F32), _t(k, inputs.F32), _t(v, inputs.F32), tS, tZ)
+        torch.cuda.synchronize()
+        wo, wS, wZ = oracle.decode_step(q, k, v, S0, Z0)
+        assert max_rel_err(o.cpu().numpy(), wo) < 1e-4
+        assert max_rel_err(tS.cpu().numpy(), wS) < 1e-5
+        assert max_rel_err(tZ.cpu().numpy(), wZ) < 1e-6
+
+
+def test_prefill_empty_sequence_zeroes_state(la):
+    S = torch.full((2, 2, 64, 64), 7.0, device=DEV)
+    Z = torch.full((2, 2, 64), 7.0, device=DEV)
+    e = torch.empty((2, 2, 0, 64), dtype=torch.bfloat16, device=DEV)
+    la.la_prefill(e, e, e, out=torch.empty((2, 2, 0, 64), dtype=torch.bfloat16, device=DEV),
+                  S=S, Z=Z)
+    torch.cuda.synchronize()
+    assert float(S.abs().max()) == 0.0 and float(Z.abs().max()) == 0.0
+
+
+# ------------------------------------------------- full-size named workloads
+
+def _device_inputs(w, seed_offset=0):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(w.seed + seed_offset)
+    shp_qk, shp_v = (w.B, w.H, w.N, w.D), (w.B, w.H, w.N, w.M)
+    q = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, DEV)
+    k = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, DEV)
+    v = inputs.torch_normal(g, shp_v, w.scale, w.dtype, DEV)
+    return q, k, v, g
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+SAMPLE_BH = [(0, 0), (-1, -1)]
+
+
+@pytest.mark.parametrize("name", ["noncausal_fwd_b4h8n4096d64", "causal_fwd_b8h8n3072d64",
+                                  "causal_fwdbwd_b4h8n16384d64"])
+def test_full_size_forward_sampled(la, name):
+    w = inputs.WORKLOADS[name]
+    q, k, v, _ = _device_inputs(w)
+    out = la.la_forward(q, k, v, causal=w.causal)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    for b, h in SAMPLE_BH:
+        want = oracle.forward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), w.causal)
+        assert max_rel_err(_np(out[b, h]), want) < TOL[w.dtype], (b, h)
+
+
+def test_full_size_backward_sampled(la):
+    w = inputs.WORKLOADS["causal_fwdbwd_b4h8n16384d64"]
+    q, k, v, g = _device_inputs(w)
+    dout = inputs.torch_normal(g, (w.B, w.H, w.N, w.M), w.scale, w.dtype, DEV)
+    dq, dk, dv = la.la_backward(q, k, v, dout, causal=True)
+    torch.cuda.synchronize()
+    for b, h in SAMPLE_BH:
+        wq, wk, wv = oracle.backward(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(dout[b, h]), True)
+        for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+            err = max_rel_err(_np(got[b, h]), want)
+            assert err < TOL[w.dtype], (name, b, h, err)
+
+
+def test_full_size_decode_sampled(la):
+    w = inputs.WORKLOADS["decode_s256h8d64_prefill1024_steps3072"]
+    q, k, v, g = _device_inputs(w)
+    _, S, Z = la.la_prefill(q, k, v)
+    T = w.steps
+    shp_qk, shp_v = (T, w.B, w.H, w.D), (T, w.B, w.H, w.M)
+    sq = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, DEV)
+    sk = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, DEV)
+    sv = inputs.torch_normal(g, shp_v, w.scale, w.dtype, DEV)
+    outs = torch.empty((T, w.B, w.H, w.M), dtype=torch.bfloat16, device=DEV)
+    for t in range(T):
+        la.la_decode_step(sq[t], sk[t], sv[t], S, Z, out=outs[t])
+    torch.cuda.synchronize()
+    for s, h in ((0, 0), (w.B - 1, w.H - 1), (77, 3)):
+        fq = np.concatenate([_np(q[s, h]), _np(sq[:, s, h])])
+        fk = np.concatenate([_np(k[s, h]), _np(sk[:, s, h])])
+        fv = np.concatenate([_np(v[s, h]), _np(sv[:, s, h])])
+        want = oracle.forward(fq, fk, fv, True)[w.N:]
+        assert max_rel_err(_np(outs[:, s, h]), want) < TOL[w.dtype], (s, h)
