@@ -73,7 +73,9 @@ unsigned long long la_kernel_launches(void) {
 }
 
 size_t la_forward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
-  (void)B; (void)H; (void)N; (void)D; (void)M; (void)causal; (void)dtype;
+  (void)causal;
+  if (B < 1 || H < 1 || N < 0) return la::kHeaderBytes;
+  if (la::tc_forward_supported(D, M, dtype)) return la::tc_forward_workspace(B * H, N);
   return la::kHeaderBytes;
 }
 
@@ -89,6 +91,9 @@ int la_forward(const void* q, const void* k, const void* v, void* out, int B, in
   cudaStream_t st = as_stream(stream);
   cudaError_t e = clear_header(workspace, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_forward(q, k, v, out, nullptr, nullptr, B * H, N, causal != 0,
+                                    workspace, st));
   return from_cuda(la::simt_forward(q, k, v, out, nullptr, nullptr, B * H, N, D, M, causal != 0,
                                     dtype, st));
 }
@@ -111,6 +116,8 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
   cudaStream_t st = as_stream(stream);
   cudaError_t e = clear_header(workspace, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_forward(q, k, v, out, S, Z, B * H, N, true, workspace, st));
   return from_cuda(la::simt_forward(q, k, v, out, S, Z, B * H, N, D, M, true, dtype, st));
 }
 

@@ -18,6 +18,12 @@ cudaError_t simt_backward(const void* q, const void* k, const void* v, const voi
                           float* dk, float* dv, int BH, int N, int D, int M, bool causal,
                           int dtype, void* ws, cudaStream_t st);
 
+// ---- tensor-core path (bf16, D = M = 64): tcgen05 + TMEM + TMA
+bool tc_forward_supported(int D, int M, int dtype);
+size_t tc_forward_workspace(int BH, int N);
+cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
+                       float* Z_out, int BH, int N, bool causal, void* ws, cudaStream_t st);
+
 // ---- decode step (memory-bound CUDA-core kernel)
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
                         int n_sh, int D, int M, int dtype, cudaStream_t st);

@@ -146,24 +146,53 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 }
 
 // ---------------------------------------------------- backward: dq (forward scan)
+//
+// The gradient of phi(Q_i) is S_i gN_i + gd_i Z_i, and the two terms cancel
+// strongly (exactly at i = 0, where out_0 = v_0 whatever q_0 is). The backward
+// kernels therefore carry state and form these combinations in the accumulator
+// type Acc: double for float32 inputs (so the result keeps float32 accuracy
+// relative to its own size), float for bfloat16 inputs.
+
+template <typename Acc>
+__device__ __forceinline__ void accumulate_state_acc(Acc* S, Acc* Z, const float* fk,
+                                                     const float* vv, int D, int M) {
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) {
+    const int d = e / M, m = e % M;
+    Acc acc = 0;
+#pragma unroll 8
+    for (int j = 0; j < kChunk; ++j) acc += (Acc)fk[j * D + d] * (Acc)vv[j * M + m];
+    S[e] += acc;
+  }
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    Acc acc = 0;
+    for (int j = 0; j < kChunk; ++j) acc += (Acc)fk[j * D + d];
+    Z[d] += acc;
+  }
+}
+
+template <typename Acc>
+__device__ __forceinline__ Acc warp_sum(Acc x) {
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
 
 // Writes dq and, per token, den_i and gd_i = -(dout_i . out_i) / den_i.
-template <typename T, bool CAUSAL>
+template <typename T, typename Acc, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const T* __restrict__ dout, float* __restrict__ dq,
-                   float* __restrict__ ws_den, float* __restrict__ ws_gd, int N, int D, int M) {
-  extern __shared__ float sm[];
-  float* S = sm;                    // D*M
-  float* Z = S + D * M;             // D
-  float* fq = Z + D;                // kChunk*D
-  float* fk = fq + kChunk * D;      // kChunk*D
-  float* vv = fk + kChunk * D;      // kChunk*M
-  float* g = vv + kChunk * M;       // kChunk*M   (dout, then gN)
-  float* A = g + kChunk * M;        // kChunk*kChunk
-  float* Tm = A + kChunk * kChunk;  // kChunk*kChunk
-  float* den = Tm + kChunk * kChunk;  // kChunk
-  float* gd = den + kChunk;         // kChunk
+                   Acc* __restrict__ ws_den, Acc* __restrict__ ws_gd, int N, int D, int M) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  Acc* S = reinterpret_cast<Acc*>(smraw);  // D*M
+  Acc* Z = S + D * M;                       // D
+  Acc* A = Z + D;                           // kChunk*kChunk  phi(q_i).phi(k_j), j <= i
+  Acc* Tm = A + kChunk * kChunk;            // kChunk*kChunk  v_j.gN_i + gd_i, j <= i
+  Acc* den = Tm + kChunk * kChunk;          // kChunk
+  Acc* gd = den + kChunk;                   // kChunk
+  Acc* g = gd + kChunk;                     // kChunk*M   (dout, then gN)
+  float* fq = reinterpret_cast<float*>(g + kChunk * M);  // kChunk*D
+  float* fk = fq + kChunk * D;                           // kChunk*D
+  float* vv = fk + kChunk * D;                           // kChunk*M
 
   const size_t bh = blockIdx.x;
   q += bh * (size_t)N * D;
@@ -175,8 +204,8 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   ws_gd += bh * (size_t)N;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = 0.f;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = 0.f;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = 0;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = 0;
   __syncthreads();
   if (!CAUSAL) {
     for (int t0 = 0; t0 < N; t0 += kChunk) {
@@ -184,7 +213,7 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
       load_rows<T>(k + (size_t)t0 * D, nv, D, fk, true);
       load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
       __syncthreads();
-      accumulate_state(S, Z, fk, vv, D, M);
+      accumulate_state_acc<Acc>(S, Z, fk, vv, D, M);
       __syncthreads();
     }
   }
@@ -192,34 +221,43 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   for (int t0 = 0; t0 < N; t0 += kChunk) {
     const int nv = min(kChunk, N - t0);
     load_rows<T>(q + (size_t)t0 * D, nv, D, fq, true);
-    load_rows<T>(dout + (size_t)t0 * M, nv, M, g, false);
+    for (int e = threadIdx.x; e < kChunk * M; e += blockDim.x)
+      g[e] = (e / M) < nv ? (Acc)to_f32<T>(dout[(size_t)t0 * M + e]) : (Acc)0;
     if (CAUSAL) {
       load_rows<T>(k + (size_t)t0 * D, nv, D, fk, true);
       load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
     }
     __syncthreads();
-    if (CAUSAL) pair_dots<true, false>(fq, fk, D, nv, A);
+    if (CAUSAL) {
+      for (int e = threadIdx.x; e < kChunk * kChunk; e += blockDim.x) {
+        const int i = e / kChunk, j = e % kChunk;
+        Acc acc = 0;
+        if (i < nv && j <= i)
+          for (int d = 0; d < D; ++d) acc += (Acc)fq[i * D + d] * (Acc)fk[j * D + d];
+        A[e] = acc;
+      }
+    }
     __syncthreads();
     // one warp per row: den_i, out_i (on the fly) and gd_i
     for (int i = warp; i < kChunk; i += kWarps) {
-      float dsum = 0.f;
-      for (int d = lane; d < D; d += 32) dsum += fq[i * D + d] * Z[d];
+      Acc dsum = 0;
+      for (int d = lane; d < D; d += 32) dsum += (Acc)fq[i * D + d] * Z[d];
       if (CAUSAL)
         for (int j = lane; j <= i; j += 32) dsum += A[i * kChunk + j];
-      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-      float go = 0.f;
+      dsum = warp_sum(dsum);
+      Acc go = 0;
       for (int m = lane; m < M; m += 32) {
-        float num = 0.f;
-        for (int d = 0; d < D; ++d) num += fq[i * D + d] * S[d * M + m];
+        Acc num = 0;
+        for (int d = 0; d < D; ++d) num += (Acc)fq[i * D + d] * S[d * M + m];
         if (CAUSAL)
-          for (int j = 0; j <= i; ++j) num += A[i * kChunk + j] * vv[j * M + m];
+          for (int j = 0; j <= i; ++j) num += A[i * kChunk + j] * (Acc)vv[j * M + m];
         go += g[i * M + m] * (num / dsum);
       }
-      for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
+      go = warp_sum(go);
       if (lane == 0) {
         const bool valid = i < nv;
-        den[i] = valid ? dsum : 1.f;
-        gd[i] = valid ? -go / dsum : 0.f;
+        den[i] = valid ? dsum : (Acc)1;
+        gd[i] = valid ? -go / dsum : (Acc)0;
         if (valid) {
           ws_den[t0 + i] = dsum;
           ws_gd[t0 + i] = -go / dsum;
@@ -232,9 +270,9 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     if (CAUSAL) {  // Tm[i][j] = v_j . gN_i + gd_i for j <= i
       for (int e = threadIdx.x; e < kChunk * kChunk; e += blockDim.x) {
         const int i = e / kChunk, j = e % kChunk;
-        float acc = 0.f;
+        Acc acc = 0;
         if (i < nv && j <= i) {
-          for (int m = 0; m < M; ++m) acc += vv[j * M + m] * g[i * M + m];
+          for (int m = 0; m < M; ++m) acc += (Acc)vv[j * M + m] * g[i * M + m];
           acc += gd[i];
         }
         Tm[e] = acc;
@@ -243,15 +281,15 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     }
     for (int e = threadIdx.x; e < nv * D; e += blockDim.x) {
       const int i = e / D, d = e % D;
-      float acc = gd[i] * Z[d];
+      Acc acc = gd[i] * Z[d];
       for (int m = 0; m < M; ++m) acc += S[d * M + m] * g[i * M + m];
       if (CAUSAL)
-        for (int j = 0; j <= i; ++j) acc += Tm[i * kChunk + j] * fk[j * D + d];
-      dq[(size_t)t0 * D + e] = acc * phi_grad_from_phi(fq[e]);
+        for (int j = 0; j <= i; ++j) acc += Tm[i * kChunk + j] * (Acc)fk[j * D + d];
+      dq[(size_t)t0 * D + e] = (float)(acc * (Acc)phi_grad_from_phi(fq[e]));
     }
     __syncthreads();
     if (CAUSAL) {
-      accumulate_state(S, Z, fk, vv, D, M);
+      accumulate_state_acc<Acc>(S, Z, fk, vv, D, M);
       __syncthreads();
     }
   }
@@ -259,51 +297,52 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 
 // ------------------------------------------------ backward: dk, dv (reverse scan)
 
-template <typename T>
-__device__ __forceinline__ void load_gN(const T* __restrict__ dout, const float* __restrict__ den_g,
-                                        const float* __restrict__ gd_g, int nv, int M, float* g,
-                                        float* gd) {
-  for (int e = threadIdx.x; e < kChunk * M; e += blockDim.x) {
-    const int r = e / M;
-    g[e] = r < nv ? to_f32<T>(dout[e]) / den_g[r] : 0.f;
-  }
-  for (int r = threadIdx.x; r < kChunk; r += blockDim.x) gd[r] = r < nv ? gd_g[r] : 0.f;
-}
-
 // R[d][m] += sum_i fq[i][d] gN[i][m];  r[d] += sum_i gd[i] fq[i][d]
-__device__ __forceinline__ void accumulate_reverse_state(float* R, float* r, const float* fq,
-                                                         const float* g, const float* gd, int D,
+template <typename Acc>
+__device__ __forceinline__ void accumulate_reverse_state(Acc* R, Acc* r, const float* fq,
+                                                         const Acc* g, const Acc* gd, int D,
                                                          int M) {
   for (int e = threadIdx.x; e < D * M; e += blockDim.x) {
     const int d = e / M, m = e % M;
-    float acc = 0.f;
+    Acc acc = 0;
 #pragma unroll 8
-    for (int i = 0; i < kChunk; ++i) acc += fq[i * D + d] * g[i * M + m];
+    for (int i = 0; i < kChunk; ++i) acc += (Acc)fq[i * D + d] * g[i * M + m];
     R[e] += acc;
   }
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    for (int i = 0; i < kChunk; ++i) acc += gd[i] * fq[i * D + d];
+    Acc acc = 0;
+    for (int i = 0; i < kChunk; ++i) acc += gd[i] * (Acc)fq[i * D + d];
     r[d] += acc;
   }
 }
 
-template <typename T, bool CAUSAL>
+template <typename T, typename Acc>
+__device__ __forceinline__ void load_gN(const T* __restrict__ dout, const Acc* __restrict__ den_g,
+                                        const Acc* __restrict__ gd_g, int nv, int M, Acc* g,
+                                        Acc* gd) {
+  for (int e = threadIdx.x; e < kChunk * M; e += blockDim.x) {
+    const int r = e / M;
+    g[e] = r < nv ? (Acc)to_f32<T>(dout[e]) / den_g[r] : (Acc)0;
+  }
+  for (int r = threadIdx.x; r < kChunk; r += blockDim.x) gd[r] = r < nv ? gd_g[r] : (Acc)0;
+}
+
+template <typename T, typename Acc, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      const T* __restrict__ dout, float* __restrict__ dk, float* __restrict__ dv,
-                     const float* __restrict__ ws_den, const float* __restrict__ ws_gd, int N,
-                     int D, int M) {
-  extern __shared__ float sm[];
-  float* R = sm;                    // D*M
-  float* r = R + D * M;             // D
-  float* fq = r + D;                // kChunk*D
-  float* fk = fq + kChunk * D;      // kChunk*D
-  float* vv = fk + kChunk * D;      // kChunk*M
-  float* g = vv + kChunk * M;       // kChunk*M  (gN)
-  float* Pm = g + kChunk * M;       // kChunk*kChunk  Pm[i][j] = fq_i . fk_j  (i >= j)
-  float* Um = Pm + kChunk * kChunk; // kChunk*kChunk  Um[i][j] = v_j . gN_i + gd_i (i >= j)
-  float* gd = Um + kChunk * kChunk; // kChunk
+                     const Acc* __restrict__ ws_den, const Acc* __restrict__ ws_gd, int N, int D,
+                     int M) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  Acc* R = reinterpret_cast<Acc*>(smraw);  // D*M
+  Acc* r = R + D * M;                       // D
+  Acc* Pm = r + D;                          // kChunk*kChunk  phi(q_i).phi(k_j), i >= j
+  Acc* Um = Pm + kChunk * kChunk;           // kChunk*kChunk  v_j.gN_i + gd_i,  i >= j
+  Acc* gd = Um + kChunk * kChunk;           // kChunk
+  Acc* g = gd + kChunk;                     // kChunk*M  (gN)
+  float* fq = reinterpret_cast<float*>(g + kChunk * M);  // kChunk*D
+  float* fk = fq + kChunk * D;                           // kChunk*D
+  float* vv = fk + kChunk * D;                           // kChunk*M
 
   const size_t bh = blockIdx.x;
   q += bh * (size_t)N * D;
@@ -315,17 +354,17 @@ simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   ws_den += bh * (size_t)N;
   ws_gd += bh * (size_t)N;
 
-  for (int e = threadIdx.x; e < D * M; e += blockDim.x) R[e] = 0.f;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) r[e] = 0.f;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) R[e] = 0;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) r[e] = 0;
   __syncthreads();
   const int n_chunks = (N + kChunk - 1) / kChunk;
   if (!CAUSAL) {
     for (int c = 0; c < n_chunks; ++c) {
       const int t0 = c * kChunk, nv = min(kChunk, N - t0);
       load_rows<T>(q + (size_t)t0 * D, nv, D, fq, true);
-      load_gN<T>(dout + (size_t)t0 * M, ws_den + t0, ws_gd + t0, nv, M, g, gd);
+      load_gN<T, Acc>(dout + (size_t)t0 * M, ws_den + t0, ws_gd + t0, nv, M, g, gd);
       __syncthreads();
-      accumulate_reverse_state(R, r, fq, g, gd, D, M);
+      accumulate_reverse_state<Acc>(R, r, fq, g, gd, D, M);
       __syncthreads();
     }
   }
@@ -336,41 +375,42 @@ simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
     if (CAUSAL) {
       load_rows<T>(q + (size_t)t0 * D, nv, D, fq, true);
-      load_gN<T>(dout + (size_t)t0 * M, ws_den + t0, ws_gd + t0, nv, M, g, gd);
+      load_gN<T, Acc>(dout + (size_t)t0 * M, ws_den + t0, ws_gd + t0, nv, M, g, gd);
     }
     __syncthreads();
     if (CAUSAL) {
-      pair_dots<true, false>(fq, fk, D, nv, Pm);
       for (int e = threadIdx.x; e < kChunk * kChunk; e += blockDim.x) {
         const int i = e / kChunk, j = e % kChunk;
-        float acc = 0.f;
+        Acc p = 0, u = 0;
         if (i < nv && j <= i) {
-          for (int m = 0; m < M; ++m) acc += vv[j * M + m] * g[i * M + m];
-          acc += gd[i];
+          for (int d = 0; d < D; ++d) p += (Acc)fq[i * D + d] * (Acc)fk[j * D + d];
+          for (int m = 0; m < M; ++m) u += (Acc)vv[j * M + m] * g[i * M + m];
+          u += gd[i];
         }
-        Um[e] = acc;
+        Pm[e] = p;
+        Um[e] = u;
       }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < nv * D; e += blockDim.x) {
       const int j = e / D, d = e % D;
-      float acc = r[d];
-      for (int m = 0; m < M; ++m) acc += R[d * M + m] * vv[j * M + m];
+      Acc acc = r[d];
+      for (int m = 0; m < M; ++m) acc += R[d * M + m] * (Acc)vv[j * M + m];
       if (CAUSAL)
-        for (int i = j; i < nv; ++i) acc += Um[i * kChunk + j] * fq[i * D + d];
-      dk[(size_t)t0 * D + e] = acc * phi_grad_from_phi(fk[e]);
+        for (int i = j; i < nv; ++i) acc += Um[i * kChunk + j] * (Acc)fq[i * D + d];
+      dk[(size_t)t0 * D + e] = (float)(acc * (Acc)phi_grad_from_phi(fk[e]));
     }
     for (int e = threadIdx.x; e < nv * M; e += blockDim.x) {
       const int j = e / M, m = e % M;
-      float acc = 0.f;
-      for (int d = 0; d < D; ++d) acc += R[d * M + m] * fk[j * D + d];
+      Acc acc = 0;
+      for (int d = 0; d < D; ++d) acc += R[d * M + m] * (Acc)fk[j * D + d];
       if (CAUSAL)
         for (int i = j; i < nv; ++i) acc += Pm[i * kChunk + j] * g[i * M + m];
-      dv[(size_t)t0 * M + e] = acc;
+      dv[(size_t)t0 * M + e] = (float)acc;
     }
     __syncthreads();
     if (CAUSAL) {
-      accumulate_reverse_state(R, r, fq, g, gd, D, M);
+      accumulate_reverse_state<Acc>(R, r, fq, g, gd, D, M);
       __syncthreads();
     }
   }
@@ -379,13 +419,15 @@ simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 size_t fwd_smem(int D, int M) {
   return sizeof(float) * ((size_t)D * M + D + 2 * kChunk * D + kChunk * M + kChunk * kChunk + kChunk);
 }
+template <typename Acc>
 size_t dq_smem(int D, int M) {
-  return sizeof(float) *
-         ((size_t)D * M + D + 2 * kChunk * D + 2 * kChunk * M + 2 * kChunk * kChunk + 2 * kChunk);
+  return sizeof(Acc) * ((size_t)D * M + D + 2 * kChunk * kChunk + 2 * kChunk + kChunk * M) +
+         sizeof(float) * (2 * kChunk * D + kChunk * M);
 }
+template <typename Acc>
 size_t dkdv_smem(int D, int M) {
-  return sizeof(float) *
-         ((size_t)D * M + D + 2 * kChunk * D + 2 * kChunk * M + 2 * kChunk * kChunk + kChunk);
+  return sizeof(Acc) * ((size_t)D * M + D + 2 * kChunk * kChunk + kChunk + kChunk * M) +
+         sizeof(float) * (2 * kChunk * D + kChunk * M);
 }
 
 template <typename K, typename... Args>
@@ -408,27 +450,27 @@ cudaError_t forward_t(const void* q, const void* k, const void* v, void* out, fl
   return causal ? args(simt_forward_kernel<T, true>) : args(simt_forward_kernel<T, false>);
 }
 
-template <typename T>
+template <typename T, typename Acc>
 cudaError_t backward_t(const void* q, const void* k, const void* v, const void* dout, float* dq,
                        float* dk, float* dv, int BH, int N, int D, int M, bool causal, void* ws,
                        cudaStream_t st) {
-  float* den = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
-  float* gd = den + (size_t)BH * N;
+  Acc* den = reinterpret_cast<Acc*>(static_cast<char*>(ws) + kHeaderBytes);
+  Acc* gd = den + (size_t)BH * N;
   cudaError_t err;
   if (causal)
-    err = launch(simt_bwd_dq_kernel<T, true>, BH, dq_smem(D, M), st, (const T*)q, (const T*)k,
-                 (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
+    err = launch(simt_bwd_dq_kernel<T, Acc, true>, BH, dq_smem<Acc>(D, M), st, (const T*)q,
+                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
   else
-    err = launch(simt_bwd_dq_kernel<T, false>, BH, dq_smem(D, M), st, (const T*)q, (const T*)k,
-                 (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
+    err = launch(simt_bwd_dq_kernel<T, Acc, false>, BH, dq_smem<Acc>(D, M), st, (const T*)q,
+                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
   if (err != cudaSuccess) return err;
   if (causal)
-    return launch(simt_bwd_dkdv_kernel<T, true>, BH, dkdv_smem(D, M), st, (const T*)q,
-                  (const T*)k, (const T*)v, (const T*)dout, dk, dv, (const float*)den,
-                  (const float*)gd, N, D, M);
-  return launch(simt_bwd_dkdv_kernel<T, false>, BH, dkdv_smem(D, M), st, (const T*)q, (const T*)k,
-                (const T*)v, (const T*)dout, dk, dv, (const float*)den, (const float*)gd, N, D,
-                M);
+    return launch(simt_bwd_dkdv_kernel<T, Acc, true>, BH, dkdv_smem<Acc>(D, M), st, (const T*)q,
+                  (const T*)k, (const T*)v, (const T*)dout, dk, dv, (const Acc*)den,
+                  (const Acc*)gd, N, D, M);
+  return launch(simt_bwd_dkdv_kernel<T, Acc, false>, BH, dkdv_smem<Acc>(D, M), st, (const T*)q,
+                (const T*)k, (const T*)v, (const T*)dout, dk, dv, (const Acc*)den,
+                (const Acc*)gd, N, D, M);
 }
 
 }  // namespace
@@ -441,15 +483,16 @@ cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out,
 }
 
 size_t simt_backward_workspace(int BH, int N) {
-  return kHeaderBytes + align_up(2 * sizeof(float) * (size_t)BH * N, 256);
+  return kHeaderBytes + align_up(2 * sizeof(double) * (size_t)BH * N, 256);
 }
 
 cudaError_t simt_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                           float* dk, float* dv, int BH, int N, int D, int M, bool causal,
                           int dtype, void* ws, cudaStream_t st) {
   if (dtype == LA_F32)
-    return backward_t<float>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws, st);
-  return backward_t<__nv_bfloat16>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws, st);
+    return backward_t<float, double>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws, st);
+  return backward_t<__nv_bfloat16, float>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws,
+                                          st);
 }
 
 }  // namespace la

@@ -1,0 +1,693 @@
+// Tensor-core (tcgen05 + TMEM + TMA) forward for bf16 inputs with D = M = 64.
+//
+// The sequence of each (batch, head) is cut into chunks of C = 128 tokens and
+// the chunks into segments. Three kernels:
+//
+//  1. tc_state_kernel: per segment, the state increment
+//       dS^T = V^T phi(K)  (tcgen05, M=64 x N=64, K = tokens), dZ = sum_t phi(K_t)
+//     ("Transformers are RNNs": S = sum_j phi(K_j) V_j^T, Z = sum_j phi(K_j);
+//     nubint.ai review, "Proposed method"; zhengyuhong.cn deck, slide 3).
+//  2. state_scan_kernel: exclusive prefix over segments (causal; deck slide 4:
+//     S_i = S_{i-1} + phi(K_i) V_i^T) or the full sum (non-causal), in float32;
+//     optionally the final state for prefill.
+//  3. tc_attend_kernel: per chunk, with S_prev / Z_prev the state before it,
+//       causal:     num = (phi(Q) phi(K)^T (.) L) V + phi(Q) S_prev,
+//                   den = rowsum((phi(Q) phi(K)^T) (.) L) + phi(Q) Z_prev
+//       non-causal: num = phi(Q) S, den = phi(Q) Z
+//     out = num / den. L is the inclusive lower-triangular mask (j <= i). The
+//     chunk form is the parallel reading of the S/Z recurrence (paperlayer.ai
+//     summary §3.3.2: training stays parallel); it equals it up to rounding.
+//
+// phi is applied in shared memory right after each TMA tile lands (bf16 in,
+// float32 math, bf16 out). The carried state is float32; it enters the
+// tensor cores as a bf16 hi + lo pair, so the inter-chunk term keeps ~16 bits.
+#include <cuda_bf16.h>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "la_tc.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;            // tokens per chunk
+constexpr int kDim = 64;           // D = M
+constexpr int kTile = kC * kDim * 2;  // 16 KB bf16 tile
+constexpr int kThreadsTC = 128;
+constexpr int kStateFloats = kDim * kDim + kDim;  // S^T [m][d] then Z [d]
+
+// ------------------------------------------------------------------ helpers
+
+struct Geometry {
+  int BH, N, n_chunks, seg_chunks, n_seg;
+  __host__ __device__ int n_items() const { return BH * n_seg; }
+  // item -> (bh, seg): segment-major so that a segment's predecessors were
+  // scheduled earlier
+  __host__ __device__ int bh_of(int item) const { return item % BH; }
+  __host__ __device__ int seg_of(int item) const { return item / BH; }
+  __host__ __device__ int chunk_begin(int item) const { return seg_of(item) * seg_chunks; }
+  __host__ __device__ int chunk_end(int item) const {
+    return min(chunk_begin(item) + seg_chunks, n_chunks);
+  }
+};
+
+// Walks (item, chunk) pairs of this CTA in processing order.
+struct Cursor {
+  int item, chunk;
+  __device__ void start(const Geometry& g) {
+    item = blockIdx.x;
+    chunk = item < g.n_items() ? g.chunk_begin(item) : 0;
+  }
+  __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
+  __device__ void advance(const Geometry& g) {
+    if (++chunk >= g.chunk_end(item)) {
+      item += gridDim.x;
+      if (item < g.n_items()) chunk = g.chunk_begin(item);
+    }
+  }
+};
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ void record_timeout(WorkspaceHeader* hdr, int site) {
+  atomicExch(&hdr->status, (int)LA_ERR_TIMEOUT);
+  atomicExch(&hdr->wait_site, site);
+}
+
+// phi on one 128 x 64 bf16 tile row (row = tid), in place in the swizzled
+// layout; rows >= nvalid become 0. If zsum != nullptr the float32 values are
+// returned in z[64] for the column sums.
+template <bool KEEP>
+__device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, float (&z)[64]) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int lc = 0; lc < 8; ++lc) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, lc * 16));
+    uint4 w = *p;
+    uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float a = valid ? phi(bf16_lo_f(u[h])) : 0.f;
+      float b = valid ? phi(bf16_hi_f(u[h])) : 0.f;
+      u[h] = pack_bf16(a, b);
+      if (KEEP) {
+        z[lc * 8 + 2 * h] = bf16_lo_f(u[h]);
+        z[lc * 8 + 2 * h + 1] = bf16_hi_f(u[h]);
+      }
+    }
+    *p = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
+// Sum z[64] over the 32 lanes of a warp; lane l ends with columns 2l, 2l+1.
+__device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool up = lane & 16;
+    const float mine = up ? z[32 + j] : z[j];
+    const float other = up ? z[j] : z[32 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool up = lane & 8;
+    const float mine = up ? z[16 + j] : z[j];
+    const float other = up ? z[j] : z[16 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool up = lane & 4;
+    const float mine = up ? z[8 + j] : z[j];
+    const float other = up ? z[j] : z[8 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool up = lane & 2;
+    const float mine = up ? z[4 + j] : z[j];
+    const float other = up ? z[j] : z[4 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool up = lane & 1;
+    const float mine = up ? z[2 + j] : z[j];
+    const float other = up ? z[j] : z[2 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
+  }
+  return make_float2(z[0], z[1]);
+}
+
+// Block-uniform bounded wait: every thread waits, then all agree on the outcome
+// (a timeout seen by any thread ends the loop for the whole CTA together).
+__device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, WorkspaceHeader* hdr,
+                                             int site) {
+  const bool all = __syncthreads_and(mbar_wait(bar, parity) ? 1 : 0) != 0;
+  if (!all && threadIdx.x == 0) record_timeout(hdr, site);
+  return all;
+}
+
+__device__ __forceinline__ uint32_t lane_base(uint32_t tbase) {
+  return tbase + ((uint32_t)((threadIdx.x / 32) % 4 * 32) << 16);
+}
+
+// ------------------------------------------------------- 1. segment states
+
+constexpr int kStateStages = 3;
+constexpr int kStateSmem = 1024 + kStateStages * 2 * kTile + 2048;
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = sm;  // [stage][K tile | V tile]
+  uint8_t* misc = sm + kStateStages * 2 * kTile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // kStateStages
+  uint64_t* mma_bar = full + kStateStages;                      // 1
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  float* dz = reinterpret_cast<float*>(misc + 128);             // [4][64]
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (tid == 0) {
+    for (int s = 0; s < kStateStages; ++s) mbar_init(&full[s], 1);
+    mbar_init(mma_bar, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 64);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+
+  Cursor cc, cp;
+  cc.start(g);
+  cp.start(g);
+  long long issued = 0;
+  auto issue = [&](Cursor& c) {
+    const int s = issued % kStateStages;
+    uint8_t* st = stages + s * 2 * kTile;
+    mbar_arrive_expect_tx(&full[s], 2 * kTile);
+    tma_load_3d(st, &tm_k, &full[s], 0, c.chunk * kC, g.bh_of(c.item));
+    tma_load_3d(st + kTile, &tm_v, &full[s], 0, c.chunk * kC, g.bh_of(c.item));
+    ++issued;
+    c.advance(g);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kStateStages - 1 && cp.valid(g); ++i) issue(cp);
+
+  bool ok = true;
+  long long consumed = 0;
+  uint32_t mma_phase = 0;
+  float zrun0 = 0.f, zrun1 = 0.f;  // this thread's share of dZ: columns 2*lane, 2*lane+1 (warp 0 only)
+  float zacc[64];
+  while (cc.valid(g) && ok) {
+    const int item = cc.item;
+    const int bh = g.bh_of(item);
+    const bool first = cc.chunk == g.chunk_begin(item);
+    const int nvalid = min(kC, g.N - cc.chunk * kC);
+    const bool last = cc.chunk + 1 == g.chunk_end(item);
+    if (tid == 0 && cp.valid(g)) issue(cp);
+    const int s = consumed % kStateStages;
+    uint8_t* kt = stages + s * 2 * kTile;
+    uint8_t* vt = kt + kTile;
+    if (!wait_uniform(&full[s], (consumed / kStateStages) & 1, hdr, 1)) {
+      ok = false;
+      break;
+    }
+    phi_row<true>(kt, tid, nvalid, zacc);
+    float2 cs = warp_column_sums(zacc);
+    dz[warp * 64 + 2 * lane] = cs.x;
+    dz[warp * 64 + 2 * lane + 1] = cs.y;
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t va = smem_u32(vt), ka = smem_u32(kt);
+      const uint32_t id = idesc_bf16(64, 64, true, true);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024), id,
+               (first && k == 0) ? 0u : 1u);
+      mma_commit(mma_bar);
+    }
+    if (warp == 0) {
+      const float a = dz[2 * lane] + dz[64 + 2 * lane] + dz[128 + 2 * lane] + dz[192 + 2 * lane];
+      const float b = dz[2 * lane + 1] + dz[64 + 2 * lane + 1] + dz[128 + 2 * lane + 1] +
+                      dz[192 + 2 * lane + 1];
+      zrun0 = first ? a : zrun0 + a;
+      zrun1 = first ? b : zrun1 + b;
+    }
+    // the tile stage and dz are reused only after the MMA has consumed them
+    if (!wait_uniform(mma_bar, mma_phase, hdr, 2)) {
+      ok = false;
+      break;
+    }
+    mma_phase ^= 1;
+    fence_after_sync();
+    if (last) {
+      float* dst = partial + (size_t)item * kStateFloats;
+      // M = 64 accumulator: row r sits in TMEM lane 32 * (r / 16) + r % 16
+      uint32_t r[32];
+      const int row = warp * 16 + lane;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(lane_base(tbase) + half * 32, r);
+        if (lane < 16) {
+          float4* d4 = reinterpret_cast<float4*>(dst + row * kDim + half * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (warp == 0) {
+        dst[kDim * kDim + 2 * lane] = zrun0;
+        dst[kDim * kDim + 2 * lane + 1] = zrun1;
+      }
+      (void)bh;
+    }
+    fence_before_sync();
+    __syncthreads();
+    ++consumed;
+    cc.advance(g);
+  }
+  // drain: every issued load must land before the CTA exits
+  if (tid == 0) {
+    while (consumed < issued) {
+      const int s = consumed % kStateStages;
+      if (!mbar_wait(&full[s], (consumed / kStateStages) & 1)) record_timeout(hdr, 3);
+      ++consumed;
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 64);
+}
+
+// ----------------------------------------------------------- 2. segment scan
+
+// prefix[bh][seg] = sum_{s < seg} partial[bh][s]  (causal)
+// prefix[bh][0]   = sum_s partial[bh][s]           (non-causal)
+// S_out[bh][d][m], Z_out[bh][d] = full sum when requested.
+__global__ void state_scan_kernel(const float* __restrict__ partial, float* __restrict__ prefix,
+                                  int BH, int n_seg, int causal, float* __restrict__ S_out,
+                                  float* __restrict__ Z_out) {
+  const int bh = blockIdx.x;
+  for (int e = threadIdx.x; e < kStateFloats; e += blockDim.x) {
+    float run = 0.f;
+    for (int s = 0; s < n_seg; ++s) {
+      const size_t idx = ((size_t)s * BH + bh) * kStateFloats + e;
+      if (causal) prefix[idx] = run;
+      run += partial[idx];
+    }
+    if (!causal) prefix[(size_t)bh * kStateFloats + e] = run;
+    if (S_out != nullptr) {
+      if (e < kDim * kDim) {
+        const int m = e / kDim, d = e % kDim;
+        S_out[(size_t)bh * kDim * kDim + d * kDim + m] = run;
+      } else {
+        Z_out[(size_t)bh * kDim + (e - kDim * kDim)] = run;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------- 3. chunk attention
+
+constexpr int kAttStages = 3;
+constexpr int kSnapBytes = 2 * kDim * 128 + 16 * 128;  // S_hi, S_lo (64 rows each), Z rows (16)
+constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
+
+// TMEM columns
+constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T, then bf16 P in [0, 64)
+constexpr uint32_t kColO = 128;   // 64: numerator
+constexpr uint32_t kColOz = 192;  // 16: phi(Q) . [Z_hi, Z_lo]
+constexpr uint32_t kColS = 256;   // 64: dS^T (M = 64 layout)
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 Geometry g, const float* __restrict__ prefix, WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = sm;  // [stage][Q | K | V]
+  uint8_t* snap = sm + kAttStages * 3 * kTile;
+  uint8_t* s_hi = snap;
+  uint8_t* s_lo = snap + kDim * 128;
+  uint8_t* zrow = snap + 2 * kDim * 128;
+  uint8_t* misc = snap + kSnapBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
+  uint64_t* mma_bar = full + kAttStages;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  float* dz = reinterpret_cast<float*>(misc + 128);  // [4][64]
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (tid == 0) {
+    for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
+    mbar_init(mma_bar, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_o);
+    if (CAUSAL) {
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+    }
+  }
+  // Z rows 2..15 of the [Z_hi; Z_lo; 0...] operand stay zero
+  for (int e = tid; e < 16 * 128 / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(zrow)[e] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tl = lane_base(tbase);
+
+  const uint32_t tx_bytes = CAUSAL ? 3 * kTile : kTile;
+  Cursor cc, cp;
+  cc.start(g);
+  cp.start(g);
+  long long issued = 0;
+  auto issue = [&](Cursor& c) {
+    const int s = issued % kAttStages;
+    uint8_t* st = stages + s * 3 * kTile;
+    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    mbar_arrive_expect_tx(&full[s], tx_bytes);
+    tma_load_3d(st, &tm_q, &full[s], 0, t0, bh);
+    if (CAUSAL) {
+      tma_load_3d(st + kTile, &tm_k, &full[s], 0, t0, bh);
+      tma_load_3d(st + 2 * kTile, &tm_v, &full[s], 0, t0, bh);
+    }
+    ++issued;
+    c.advance(g);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
+
+  // running state: S^T row m (threads with lane < 16: m = 16 * warp + lane) and
+  // Z[d] (threads 0..63: d = tid)
+  float srun[64];
+  float zrun = 0.f;
+  const int srow = warp * 16 + lane;
+  const bool sthread = lane < 16;
+
+  bool ok = true;
+  long long consumed = 0;
+  uint32_t mma_phase = 0;
+  float zacc[64];
+  while (cc.valid(g) && ok) {
+    const int item = cc.item;
+    const int bh = g.bh_of(item);
+    const int t0 = cc.chunk * kC;
+    const bool first = cc.chunk == g.chunk_begin(item);
+    const int nvalid = min(kC, g.N - t0);
+    if (tid == 0 && cp.valid(g)) {
+      bulk_wait_read<0>();  // the stage being refilled was last read by an output store
+      issue(cp);
+    }
+    if (first) {  // state before this segment
+      const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+      if (sthread) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 x = s4[j];
+          srun[4 * j] = x.x;
+          srun[4 * j + 1] = x.y;
+          srun[4 * j + 2] = x.z;
+          srun[4 * j + 3] = x.w;
+        }
+      }
+      if (tid < kDim) zrun = src[kDim * kDim + tid];
+    }
+    const int s = consumed % kAttStages;
+    uint8_t* qt = stages + s * 3 * kTile;
+    uint8_t* kt = qt + kTile;
+    uint8_t* vt = qt + 2 * kTile;
+    // snapshot of the state before this chunk: bf16 hi + lo, K-major rows
+    if ((CAUSAL || first) && sthread) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float a = srun[8 * c + 2 * h], b = srun[8 * c + 2 * h + 1];
+          hi[h] = pack_bf16(a, b);
+          lo[h] = pack_bf16(a - bf16_lo_f(hi[h]), b - bf16_hi_f(hi[h]));
+        }
+        *reinterpret_cast<uint4*>(s_hi + sw128(srow, c * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(s_lo + sw128(srow, c * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    if ((CAUSAL || first) && tid < kDim) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(zrun);
+      const __nv_bfloat16 l = __float2bfloat16_rn(zrun - __bfloat162float(h));
+      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * tid)) = h;
+      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(1, 2 * tid)) = l;
+    }
+    if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
+      ok = false;
+      break;
+    }
+    phi_row<false>(qt, tid, kC, zacc);  // padded query rows are never stored
+    if (CAUSAL) {
+      phi_row<true>(kt, tid, nvalid, zacc);
+      const float2 cs = warp_column_sums(zacc);
+      dz[warp * 64 + 2 * lane] = cs.x;
+      dz[warp * 64 + 2 * lane + 1] = cs.y;
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t ha = smem_u32(s_hi), la = smem_u32(s_lo), za = smem_u32(zrow);
+      if (CAUSAL) {
+        const uint32_t idP = idesc_bf16(128, 128, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kColP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
+        const uint32_t idS = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kColS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
+                 idS, k);
+      }
+      const uint32_t idO = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
+      const uint32_t idZ = idesc_bf16(128, 16, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+      mma_commit(mma_bar);
+    }
+    if (!wait_uniform(mma_bar, mma_phase, hdr, 12)) {
+      ok = false;
+      break;
+    }
+    mma_phase ^= 1;
+    fence_after_sync();
+
+    float rowsum = 0.f;
+    if (CAUSAL) {
+      // masked P row -> bf16, written back over the first 64 TMEM columns
+      const int i = tid;  // query row within the chunk
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        uint32_t pk[16];
+        if (sl <= warp) {  // warp-uniform: slices past the diagonal are all zero
+          uint32_t r[32];
+          tmem_ld32(tl + kColP + 32 * sl, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int j0 = 32 * sl + 2 * c;
+            const float a = j0 <= i ? __uint_as_float(r[2 * c]) : 0.f;
+            const float b = j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f;
+            pk[c] = pack_bf16(a, b);
+            rowsum += bf16_lo_f(pk[c]) + bf16_hi_f(pk[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        }
+        tmem_st16(tl + kColP + 16 * sl, pk);
+      }
+      // state update: S^T += dS^T (rows of the M = 64 accumulator), Z += dZ
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tl + kColS + 32 * half, r);
+          if (sthread) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) srun[32 * half + j] += __uint_as_float(r[j]);
+          }
+        }
+      }
+      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t va = smem_u32(vt);
+        const uint32_t idPV = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kColO, tbase + kColP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
+        mma_commit(mma_bar);
+      }
+      if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
+        ok = false;
+        break;
+      }
+      mma_phase ^= 1;
+      fence_after_sync();
+    }
+
+    // out = num / den -> bf16, staged in the Q slot (all MMAs reading it are done)
+    {
+      uint32_t oz[16];
+      tmem_ld16(tl + kColOz, oz);
+      const float den = rowsum + __uint_as_float(oz[0]) + __uint_as_float(oz[1]);
+      const float inv = 1.f / den;
+      uint32_t r[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + kColO + 32 * half, r);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            o[h] = pack_bf16(__uint_as_float(r[8 * c + 2 * h]) * inv,
+                             __uint_as_float(r[8 * c + 2 * h + 1]) * inv);
+          *reinterpret_cast<uint4*>(qt + sw128(tid, (half * 4 + c) * 16)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      tma_store_3d(&tm_o, qt, 0, t0, bh);
+      bulk_commit();
+    }
+    ++consumed;
+    cc.advance(g);
+  }
+  if (tid == 0) {
+    while (consumed < issued) {  // loads still in flight after an early exit
+      const int s = consumed % kAttStages;
+      if (!mbar_wait(&full[s], (consumed / kAttStages) & 1)) record_timeout(hdr, 14);
+      ++consumed;
+    }
+    bulk_wait_all<0>();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+int sm_count() {
+  static int n = [] {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v > 0 ? v : 148;
+  }();
+  return n;
+}
+
+Geometry make_geometry(int BH, int N) {
+  Geometry g;
+  g.BH = BH;
+  g.N = N;
+  g.n_chunks = (N + kC - 1) / kC;
+  // segments: aim for >= 4 items per SM while keeping segments >= 2 chunks
+  const int target_items = 4 * sm_count();
+  int seg_chunks = (int)(((long long)BH * g.n_chunks + target_items - 1) / target_items);
+  seg_chunks = max(2, seg_chunks);
+  g.seg_chunks = min(seg_chunks, g.n_chunks);
+  g.n_seg = (g.n_chunks + g.seg_chunks - 1) / g.seg_chunks;
+  return g;
+}
+
+}  // namespace
+
+bool tc_forward_supported(int D, int M, int dtype) { return dtype == LA_BF16 && D == 64 && M == 64; }
+
+size_t tc_forward_workspace(int BH, int N) {
+  const Geometry g = make_geometry(BH, N);
+  return kHeaderBytes + 2 * align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256);
+}
+
+cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
+                       float* Z_out, int BH, int N, bool causal, void* ws, cudaStream_t st) {
+  const Geometry g = make_geometry(BH, N);
+  WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
+  float* prefix = partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;
+  CUtensorMap tq, tk, tv, to;
+  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
+  if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
+    return cudaErrorInvalidValue;
+
+  const int sms = sm_count();
+  cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStateSmem);
+  if (e != cudaSuccess) return e;
+  tc_state_kernel<<<min(g.n_items(), sms), kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  state_scan_kernel<<<BH, 256, 0, st>>>(partial, prefix, BH, g.n_seg, causal ? 1 : 0, S_out, Z_out);
+  count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  // non-causal: one item per chunk range of the readout, all reading prefix[bh]
+  if (causal) {
+    e = cudaFuncSetAttribute(tc_attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kAttSmem);
+    if (e != cudaSuccess) return e;
+    tc_attend_kernel<true><<<min(g.n_items(), sms), kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g,
+                                                                                prefix, hdr);
+  } else {
+    e = cudaFuncSetAttribute(tc_attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kAttSmem);
+    if (e != cudaSuccess) return e;
+    tc_attend_kernel<false><<<min(g.n_items(), sms), kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g,
+                                                                                 prefix, hdr);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace la
