@@ -116,6 +116,9 @@ def parse():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--part", default=None,
+                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode"],
+                    help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
 
@@ -451,8 +454,42 @@ def run_reference(args, world, rank):
     }), flush=True)
 
 
+def run_part(args):
+    """One entry point on one workload, W + K calls; prints per-call CUDA-event times."""
+    import torch
+    import kernelized_causal_self_gb300 as la
+    from kernelized_causal_self_gb300 import build as labuild
+    from kernelized_causal_self_gb300 import inputs
+    labuild.build()
+    la.load_library()
+    device = torch.device("cuda", 0)
+    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "fwd3072": "causal_fwd_b8h8n3072d64",
+            "noncausal": "noncausal_fwd_b4h8n4096d64",
+            "decode": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
+    w = inputs.WORKLOADS[name]
+    q, k, v, dout, g = device_inputs(w, device, dout=True)
+    if args.part == "decode":
+        _, S, Z = la.la_prefill(q, k, v)
+        sq = inputs.torch_normal(g, (w.B, w.H, w.D), w.scale, w.dtype, device)
+        sk = inputs.torch_normal(g, (w.B, w.H, w.D), w.scale, w.dtype, device)
+        sv = inputs.torch_normal(g, (w.B, w.H, w.M), w.scale, w.dtype, device)
+        fn = lambda: la.la_decode_step(sq, sk, sv, S, Z)
+    elif args.part == "bwd":
+        fn = lambda: la.la_backward(q, k, v, dout, True)
+    elif args.part == "fwdbwd":
+        fn = lambda: (la.la_forward(q, k, v, True), la.la_backward(q, k, v, dout, True))
+    else:
+        fn = lambda: la.la_forward(q, k, v, w.causal)
+    t = time_calls(fn, args.steps, args.warmup)
+    print(json.dumps({"part": args.part, "workload": name, "ms": t,
+                      "median_ms": statistics.median(t)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.part is not None:
+        run_part(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

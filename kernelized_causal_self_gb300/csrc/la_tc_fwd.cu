@@ -77,8 +77,15 @@ __device__ __forceinline__ void record_timeout(WorkspaceHeader* hdr, int site) {
   atomicExch(&hdr->wait_site, site);
 }
 
+// phi(x) = exp(min(x, 0)) + max(x, 0): the elu + 1 map without a branch, with
+// the hardware exp2 (its few-ulp float32 error vanishes in the bf16 rounding
+// of the result).
+__device__ __forceinline__ float phi_fast(float x) {
+  return __expf(fminf(x, 0.f)) + fmaxf(x, 0.f);
+}
+
 // phi on one 128 x 64 bf16 tile row (row = tid), in place in the swizzled
-// layout; rows >= nvalid become 0. If zsum != nullptr the float32 values are
+// layout; rows >= nvalid become 0. With KEEP the rounded values are also
 // returned in z[64] for the column sums.
 template <bool KEEP>
 __device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, float (&z)[64]) {
@@ -90,8 +97,8 @@ __device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, floa
     uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      float a = valid ? phi(bf16_lo_f(u[h])) : 0.f;
-      float b = valid ? phi(bf16_hi_f(u[h])) : 0.f;
+      float a = valid ? phi_fast(bf16_lo_f(u[h])) : 0.f;
+      float b = valid ? phi_fast(bf16_hi_f(u[h])) : 0.f;
       u[h] = pack_bf16(a, b);
       if (KEEP) {
         z[lc * 8 + 2 * h] = bf16_lo_f(u[h]);
@@ -302,25 +309,37 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // prefix[bh][seg] = sum_{s < seg} partial[bh][s]  (causal)
 // prefix[bh][0]   = sum_s partial[bh][s]           (non-causal)
 // S_out[bh][d][m], Z_out[bh][d] = full sum when requested.
-__global__ void state_scan_kernel(const float* __restrict__ partial, float* __restrict__ prefix,
-                                  int BH, int n_seg, int causal, float* __restrict__ S_out,
-                                  float* __restrict__ Z_out) {
-  const int bh = blockIdx.x;
-  for (int e = threadIdx.x; e < kStateFloats; e += blockDim.x) {
-    float run = 0.f;
-    for (int s = 0; s < n_seg; ++s) {
-      const size_t idx = ((size_t)s * BH + bh) * kStateFloats + e;
-      if (causal) prefix[idx] = run;
-      run += partial[idx];
-    }
-    if (!causal) prefix[(size_t)bh * kStateFloats + e] = run;
-    if (S_out != nullptr) {
-      if (e < kDim * kDim) {
-        const int m = e / kDim, d = e % kDim;
-        S_out[(size_t)bh * kDim * kDim + d * kDim + m] = run;
-      } else {
-        Z_out[(size_t)bh * kDim + (e - kDim * kDim)] = run;
+// One thread per state element; the segment loads are issued in batches of 8
+// so the walk over segments is not a chain of dependent global loads.
+constexpr int kScanThreads = 128;
+
+__global__ void __launch_bounds__(kScanThreads)
+state_scan_kernel(const float* __restrict__ partial, float* __restrict__ prefix, int BH, int n_seg,
+                  int causal, float* __restrict__ S_out, float* __restrict__ Z_out) {
+  const int bh = blockIdx.y;
+  const int e = blockIdx.x * kScanThreads + threadIdx.x;
+  if (e >= kStateFloats) return;
+  float run = 0.f;
+  for (int s0 = 0; s0 < n_seg; s0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      x[j] = s0 + j < n_seg ? partial[((size_t)(s0 + j) * BH + bh) * kStateFloats + e] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < n_seg) {
+        if (causal) prefix[((size_t)(s0 + j) * BH + bh) * kStateFloats + e] = run;
+        run += x[j];
       }
+    }
+  }
+  if (!causal) prefix[(size_t)bh * kStateFloats + e] = run;
+  if (S_out != nullptr) {
+    if (e < kDim * kDim) {
+      const int m = e / kDim, d = e % kDim;
+      S_out[(size_t)bh * kDim * kDim + d * kDim + m] = run;
+    } else {
+      Z_out[(size_t)bh * kDim + (e - kDim * kDim)] = run;
     }
   }
 }
@@ -668,7 +687,9 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
   tc_state_kernel<<<min(g.n_items(), sms), kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  state_scan_kernel<<<BH, 256, 0, st>>>(partial, prefix, BH, g.n_seg, causal ? 1 : 0, S_out, Z_out);
+  const dim3 scan_grid((kStateFloats + kScanThreads - 1) / kScanThreads, BH);
+  state_scan_kernel<<<scan_grid, kScanThreads, 0, st>>>(partial, prefix, BH, g.n_seg, causal ? 1 : 0,
+                                                        S_out, Z_out);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
