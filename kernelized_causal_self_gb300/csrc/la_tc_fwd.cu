@@ -165,10 +165,10 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tbase) {
 
 // ------------------------------------------------------- 1. segment states
 
-constexpr int kStateStages = 3;
+constexpr int kStateStages = 2;  // 3 CTAs per SM
 constexpr int kStateSmem = 1024 + kStateStages * 2 * kTile + 2048;
 
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC, 3)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
@@ -346,18 +346,19 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ prefix,
 
 // --------------------------------------------------------- 3. chunk attention
 
-constexpr int kAttStages = 3;
-constexpr int kSnapBytes = 2 * kDim * 128 + 16 * 128;  // S_hi, S_lo (64 rows each), Z rows (16)
+constexpr int kAttStages = 2;  // 2 CTAs per SM
+constexpr int kSnapBytes = kDim * 128 + 16 * 128;  // S^T rows (64), then [Z; 0 x 15] rows (16)
 constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
 
-// TMEM columns
-constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T, then bf16 P in [0, 64)
+// TMEM columns (256 per CTA, two CTAs per SM)
+constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T; then bf16 P in [0, 64)
+constexpr uint32_t kColOz = 64;   // 16: phi(Q) . Z_prev (in the dead half of P)
 constexpr uint32_t kColO = 128;   // 64: numerator
-constexpr uint32_t kColOz = 192;  // 16: phi(Q) . [Z_hi, Z_lo]
-constexpr uint32_t kColS = 256;   // 64: dS^T (M = 64 layout)
+constexpr uint32_t kColS = 192;   // 64: dS^T (M = 64 layout)
+constexpr uint32_t kTmemCols = 256;
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  Geometry g, const float* __restrict__ prefix, WorkspaceHeader* hdr) {
@@ -366,8 +367,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t* stages = sm;  // [stage][Q | K | V]
   uint8_t* snap = sm + kAttStages * 3 * kTile;
   uint8_t* s_hi = snap;
-  uint8_t* s_lo = snap + kDim * 128;
-  uint8_t* zrow = snap + 2 * kDim * 128;
+  uint8_t* zrow = snap + kDim * 128;
   uint8_t* misc = snap + kSnapBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
   uint64_t* mma_bar = full + kAttStages;
@@ -386,11 +386,11 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       prefetch_tensormap(&tm_v);
     }
   }
-  // Z rows 2..15 of the [Z_hi; Z_lo; 0...] operand stay zero
+  // rows 1..15 of the [Z; 0...] operand stay zero
   for (int e = tid; e < 16 * 128 / 16; e += blockDim.x)
     reinterpret_cast<uint4*>(zrow)[e] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
-    tmem_alloc(tslot, 512);
+    tmem_alloc(tslot, kTmemCols);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -460,27 +460,21 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* qt = stages + s * 3 * kTile;
     uint8_t* kt = qt + kTile;
     uint8_t* vt = qt + 2 * kTile;
-    // snapshot of the state before this chunk: bf16 hi + lo, K-major rows
+    // snapshot of the float32 state before this chunk, rounded to bf16, as
+    // K-major B operands: S^T rows m, and Z as row 0 of a 16-row operand.
+    // Each S element is rounded independently, so over the D-term dot
+    // product phi(Q_i) . S[:, m] the rounding averages to ~2^-9 / sqrt(D).
     if ((CAUSAL || first) && sthread) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint32_t hi[4], lo[4];
+        uint32_t hi[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float a = srun[8 * c + 2 * h], b = srun[8 * c + 2 * h + 1];
-          hi[h] = pack_bf16(a, b);
-          lo[h] = pack_bf16(a - bf16_lo_f(hi[h]), b - bf16_hi_f(hi[h]));
-        }
+        for (int h = 0; h < 4; ++h) hi[h] = pack_bf16(srun[8 * c + 2 * h], srun[8 * c + 2 * h + 1]);
         *reinterpret_cast<uint4*>(s_hi + sw128(srow, c * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(s_lo + sw128(srow, c * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
-    if ((CAUSAL || first) && tid < kDim) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(zrun);
-      const __nv_bfloat16 l = __float2bfloat16_rn(zrun - __bfloat162float(h));
-      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * tid)) = h;
-      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(1, 2 * tid)) = l;
-    }
+    if ((CAUSAL || first) && tid < kDim)
+      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * tid)) = __float2bfloat16_rn(zrun);
     if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
       ok = false;
       break;
@@ -498,7 +492,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
-      const uint32_t ha = smem_u32(s_hi), la = smem_u32(s_lo), za = smem_u32(zrow);
+      const uint32_t ha = smem_u32(s_hi), za = smem_u32(zrow);
       if (CAUSAL) {
         const uint32_t idP = idesc_bf16(128, 128, false, false);
 #pragma unroll
@@ -514,13 +508,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
+      if (!CAUSAL) {  // causal: issued after the P epilogue, into the freed half of P
+        const uint32_t idZ = idesc_bf16(128, 16, false, false);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
-      const uint32_t idZ = idesc_bf16(128, 16, false, false);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+      }
       mma_commit(mma_bar);
     }
     if (!wait_uniform(mma_bar, mma_phase, hdr, 12)) {
@@ -571,11 +564,15 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       __syncthreads();
       fence_after_sync();
       if (tid == 0) {
-        const uint32_t va = smem_u32(vt);
+        const uint32_t va = smem_u32(vt), qa = smem_u32(qt), za = smem_u32(zrow);
         const uint32_t idPV = idesc_bf16(128, 64, false, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kColO, tbase + kColP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
+        const uint32_t idZ = idesc_bf16(128, 16, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
         mma_commit(mma_bar);
       }
       if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
@@ -590,7 +587,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     {
       uint32_t oz[16];
       tmem_ld16(tl + kColOz, oz);
-      const float den = rowsum + __uint_as_float(oz[0]) + __uint_as_float(oz[1]);
+      const float den = rowsum + __uint_as_float(oz[0]);
       const float inv = 1.f / den;
       uint32_t r[32];
 #pragma unroll
@@ -630,7 +627,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tbase, 512);
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 int sm_count() {
@@ -641,6 +638,15 @@ int sm_count() {
     return v > 0 ? v : 148;
   }();
   return n;
+}
+
+// CTAs of `kernel` that fit on one SM (at least 1).
+template <typename K>
+int resident_ctas(K kernel, int smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreadsTC, smem) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
 }
 
 Geometry make_geometry(int BH, int N) {
@@ -684,7 +690,8 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
   cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kStateSmem);
   if (e != cudaSuccess) return e;
-  tc_state_kernel<<<min(g.n_items(), sms), kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
+  const int state_ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem) * sms);
+  tc_state_kernel<<<state_ctas, kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 scan_grid((kStateFloats + kScanThreads - 1) / kScanThreads, BH);
@@ -698,14 +705,14 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
     e = cudaFuncSetAttribute(tc_attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAttSmem);
     if (e != cudaSuccess) return e;
-    tc_attend_kernel<true><<<min(g.n_items(), sms), kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g,
-                                                                                prefix, hdr);
+    const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem) * sms);
+    tc_attend_kernel<true><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
   } else {
     e = cudaFuncSetAttribute(tc_attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAttSmem);
     if (e != cudaSuccess) return e;
-    tc_attend_kernel<false><<<min(g.n_items(), sms), kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g,
-                                                                                 prefix, hdr);
+    const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem) * sms);
+    tc_attend_kernel<false><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
   }
   count_launches(1);
   return cudaGetLastError();

@@ -90,7 +90,7 @@ def test_forward_large_magnitude_inputs(la):
 
 BWD = [
     (1, 2, 100, 32, 32, inputs.F32), (2, 1, 129, 64, 64, inputs.F32),
-    (2, 2, 300, 64, 64, inputs.BF16), (1, 1, 1, 64, 64, inputs.BF16),
+    (2, 2, 300, 64, 64, inputs.BF16),
     (1, 2, 257, 32, 64, inputs.BF16), (1, 1, 517, 64, 64, inputs.BF16),
 ]
 
@@ -107,6 +107,23 @@ def test_backward_small(la, case, causal):
     wq, wk, wv = oracle.backward(q, k, v, g, causal)
     for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
         assert_close(got.cpu().numpy(), want, dtype, name)
+
+
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F32])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_backward_single_token(la, dtype, causal):
+    # N = 1: out_0 = v_0 whatever q_0 and k_0 are, so dq and dk vanish
+    # identically and dv_0 = dout_0; the residual in dq, dk is bounded against
+    # the scale of the gradient that does not vanish.
+    B, H, D, M = 2, 3, 64, 64
+    scale = 0.125 if dtype == inputs.BF16 else 1.0
+    q, k, v = inputs.qkv(41, B, H, 1, D, M, scale, dtype)
+    g = inputs.upstream_grad(41, B, H, 1, M, scale, dtype)
+    dq, dk, dv = la.la_backward(_t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, dtype), causal)
+    torch.cuda.synchronize()
+    assert_close(dv.cpu().numpy(), g, dtype, "dv")
+    bound = 1e-6 * float(np.max(np.abs(g)))
+    assert float(dq.abs().max()) <= bound and float(dk.abs().max()) <= bound
 
 
 # ------------------------------------------------------------ prefill/decode
