@@ -640,6 +640,16 @@ int sm_count() {
   return n;
 }
 
+// Opt in to the dynamic shared memory `kernel` needs and to the largest
+// shared-memory carveout (so several CTAs fit per SM).
+template <typename K>
+cudaError_t configure(K kernel, int smem) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // CTAs of `kernel` that fit on one SM (at least 1).
 template <typename K>
 int resident_ctas(K kernel, int smem) {
@@ -687,8 +697,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
     return cudaErrorInvalidValue;
 
   const int sms = sm_count();
-  cudaError_t e = cudaFuncSetAttribute(tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStateSmem);
+  cudaError_t e = configure(tc_state_kernel, kStateSmem);
   if (e != cudaSuccess) return e;
   const int state_ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem) * sms);
   tc_state_kernel<<<state_ctas, kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
@@ -702,14 +711,12 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
 
   // non-causal: one item per chunk range of the readout, all reading prefix[bh]
   if (causal) {
-    e = cudaFuncSetAttribute(tc_attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kAttSmem);
+    e = configure(tc_attend_kernel<true>, kAttSmem);
     if (e != cudaSuccess) return e;
     const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem) * sms);
     tc_attend_kernel<true><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
   } else {
-    e = cudaFuncSetAttribute(tc_attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kAttSmem);
+    e = configure(tc_attend_kernel<false>, kAttSmem);
     if (e != cudaSuccess) return e;
     const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem) * sms);
     tc_attend_kernel<false><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
