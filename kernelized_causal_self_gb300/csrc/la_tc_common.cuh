@@ -1,0 +1,190 @@
+// Shared pieces of the tensor-core kernels (forward and backward): chunk
+// geometry, the per-CTA work cursor, phi on swizzled tiles, warp column sums
+// and block-uniform bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "la_tc.cuh"
+
+namespace la {
+namespace tcx {
+
+using namespace tc;
+
+constexpr int kC = 128;            // tokens per chunk
+constexpr int kDim = 64;           // D = M
+constexpr int kTile = kC * kDim * 2;  // 16 KB bf16 tile
+constexpr int kThreadsTC = 128;
+constexpr int kStateFloats = kDim * kDim + kDim;  // S^T [m][d] then Z [d]
+
+// ------------------------------------------------------------------ helpers
+
+struct Geometry {
+  int BH, N, n_chunks, seg_chunks, n_seg;
+  __host__ __device__ int n_items() const { return BH * n_seg; }
+  // item -> (bh, seg): segment-major so that a segment's predecessors were
+  // scheduled earlier
+  __host__ __device__ int bh_of(int item) const { return item % BH; }
+  __host__ __device__ int seg_of(int item) const { return item / BH; }
+  __host__ __device__ int chunk_begin(int item) const { return seg_of(item) * seg_chunks; }
+  __host__ __device__ int chunk_end(int item) const {
+    return min(chunk_begin(item) + seg_chunks, n_chunks);
+  }
+};
+
+// Walks (item, chunk) pairs of this CTA in processing order.
+struct Cursor {
+  int item, chunk;
+  __device__ void start(const Geometry& g) {
+    item = blockIdx.x;
+    chunk = item < g.n_items() ? g.chunk_begin(item) : 0;
+  }
+  __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
+  __device__ void advance(const Geometry& g) {
+    if (++chunk >= g.chunk_end(item)) {
+      item += gridDim.x;
+      if (item < g.n_items()) chunk = g.chunk_begin(item);
+    }
+  }
+};
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ void record_timeout(WorkspaceHeader* hdr, int site) {
+  atomicExch(&hdr->status, (int)LA_ERR_TIMEOUT);
+  atomicExch(&hdr->wait_site, site);
+}
+
+// phi(x) = exp(min(x, 0)) + max(x, 0): the elu + 1 map without a branch, with
+// the hardware exp2 (its few-ulp float32 error vanishes in the bf16 rounding
+// of the result).
+__device__ __forceinline__ float phi_fast(float x) {
+  return __expf(fminf(x, 0.f)) + fmaxf(x, 0.f);
+}
+
+// phi on one 128 x 64 bf16 tile row (row = tid), in place in the swizzled
+// layout; rows >= nvalid become 0. With KEEP the rounded values are also
+// returned in z[64] for the column sums.
+template <bool KEEP>
+__device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, float (&z)[64]) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int lc = 0; lc < 8; ++lc) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, lc * 16));
+    uint4 w = *p;
+    uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float a = valid ? phi_fast(bf16_lo_f(u[h])) : 0.f;
+      float b = valid ? phi_fast(bf16_hi_f(u[h])) : 0.f;
+      u[h] = pack_bf16(a, b);
+      if (KEEP) {
+        z[lc * 8 + 2 * h] = bf16_lo_f(u[h]);
+        z[lc * 8 + 2 * h + 1] = bf16_hi_f(u[h]);
+      }
+    }
+    *p = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
+// Sum z[64] over the 32 lanes of a warp; lane l ends with columns 2l, 2l+1.
+__device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool up = lane & 16;
+    const float mine = up ? z[32 + j] : z[j];
+    const float other = up ? z[j] : z[32 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool up = lane & 8;
+    const float mine = up ? z[16 + j] : z[j];
+    const float other = up ? z[j] : z[16 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool up = lane & 4;
+    const float mine = up ? z[8 + j] : z[j];
+    const float other = up ? z[j] : z[8 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool up = lane & 2;
+    const float mine = up ? z[4 + j] : z[j];
+    const float other = up ? z[j] : z[4 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool up = lane & 1;
+    const float mine = up ? z[2 + j] : z[j];
+    const float other = up ? z[j] : z[2 + j];
+    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
+  }
+  return make_float2(z[0], z[1]);
+}
+
+// Block-uniform bounded wait: every thread waits, then all agree on the outcome
+// (a timeout seen by any thread ends the loop for the whole CTA together).
+__device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, WorkspaceHeader* hdr,
+                                             int site) {
+  const bool all = __syncthreads_and(mbar_wait(bar, parity) ? 1 : 0) != 0;
+  if (!all && threadIdx.x == 0) record_timeout(hdr, site);
+  return all;
+}
+
+__device__ __forceinline__ uint32_t lane_base(uint32_t tbase) {
+  return tbase + ((uint32_t)((threadIdx.x / 32) % 4 * 32) << 16);
+}
+
+
+// Opt in to the dynamic shared memory `kernel` needs and to the largest
+// shared-memory carveout (so several CTAs fit per SM).
+template <typename K>
+inline cudaError_t configure(K kernel, int smem) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// CTAs of `kernel` that fit on one SM (at least 1): the larger of the runtime's
+// occupancy answer and a count from the kernel's registers and shared memory
+// against the SM's register file and shared memory (1 KB reserved per CTA).
+template <typename K>
+inline int resident_ctas(K kernel, int smem) {
+  int api = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api, kernel, kThreadsTC, smem) != cudaSuccess)
+    api = 0;
+  int dev = 0, smem_sm = 0, regs_sm = 0;
+  cudaFuncAttributes fa;
+  int manual = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) ==
+          cudaSuccess &&
+      cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
+    const int regs_warp = ((fa.numRegs + 7) / 8 * 8) * 32;
+    const int regs_cta = regs_warp * (kThreadsTC / 32);
+    const int by_smem = smem_sm / (smem + (int)fa.sharedSizeBytes + 1024);
+    const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
+    manual = by_smem < by_regs ? by_smem : by_regs;
+  }
+  const int n = api > manual ? api : manual;
+  return n > 0 ? n : 1;
+}
+
+int sm_count();
+Geometry make_geometry(int BH, int N);
+
+}  // namespace tcx
+}  // namespace la
