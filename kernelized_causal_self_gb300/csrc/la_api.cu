@@ -122,8 +122,9 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
 }
 
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
-  (void)D; (void)M; (void)causal; (void)dtype;
+  (void)causal;
   if (B < 1 || H < 1 || N < 0) return la::kHeaderBytes;
+  if (la::tc_forward_supported(D, M, dtype)) return la::tc_backward_workspace(B * H, N);
   return la::simt_backward_workspace(B * H, N);
 }
 
@@ -139,6 +140,9 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout, f
   cudaStream_t st = as_stream(stream);
   cudaError_t e = clear_header(workspace, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_backward(q, k, v, dout, dq, dk, dv, B * H, N, causal != 0, workspace,
+                                     st));
   return from_cuda(la::simt_backward(q, k, v, dout, dq, dk, dv, B * H, N, D, M, causal != 0,
                                      dtype, workspace, st));
 }

@@ -23,6 +23,10 @@ bool tc_forward_supported(int D, int M, int dtype);
 size_t tc_forward_workspace(int BH, int N);
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
                        float* Z_out, int BH, int N, bool causal, void* ws, cudaStream_t st);
+size_t tc_backward_workspace(int BH, int N);
+cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                        float* dk, float* dv, int BH, int N, bool causal, void* ws,
+                        cudaStream_t st);
 
 // ---- decode step (memory-bound CUDA-core kernel)
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,

@@ -1,0 +1,848 @@
+// Tensor-core backward for bf16 inputs with D = M = 64: cumulative-sum
+// gradients ("Transformers are RNNs", paperlayer.ai summary §3.3.1 and
+// App. A), chunked like the forward.
+//
+// With G = dout, den_i = phi(Q_i)^T Z_i, out_i = num_i / den_i:
+//   gN_i = G_i / den_i,  gd_i = -(G_i . out_i) / den_i,
+//   T_ij = V_j . gN_i + gd_i,
+//   dphiQ_i = sum_{j<=i} T_ij phi(K_j)            (forward-direction sums)
+//   dphiK_j = sum_{i>=j} T_ij phi(Q_i)            (reverse-direction sums)
+//   dV_j    = sum_{i>=j} (phi(Q_i) . phi(K_j)) gN_i
+// and dq = dphiQ * phi'(q), dk = dphiK * phi'(k). Per chunk of C = 128 tokens
+// the sums split into an intra-chunk part with the masked C x C matrices
+// P_L = (phi(Q) phi(K)^T) (.) L and T_L, and a state part: S_prev, Z_prev
+// (state before the chunk) for dq, R_next = sum_{i after the chunk} phi(Q_i)
+// gN_i^T and r_next = sum gd_i phi(Q_i) for dk and dv:
+//   dphiQ = T_L phi(K) + gN S_prev^T + gd Z_prev^T
+//   dphiK = T_L^T phi(Q) + V R_next^T + r_next
+//   dV    = P_L^T gN + phi(K) R_next
+//
+// Kernels: the forward's segment-state kernel and scan give S_prev per
+// segment; tc_bwd_q_kernel (forward direction) recomputes num/den, writes dq,
+// den_i, gd_i and each segment's sum of phi(Q)^T gN and gd phi(Q); a suffix
+// scan gives R_next per segment; tc_bwd_kv_kernel walks each segment's chunks
+// from last to first and writes dk, dv.
+//
+// Precision: T_ij and S gN + gd Z cancel strongly (exactly at i = j = 0), so
+// gN enters the tensor cores as a bf16 hi + lo pair, the carried states as hi
+// + lo pairs, and gd is added in float32; the cancelled results are only then
+// rounded to bf16 (T_L) or kept in float32.
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace tcx {
+namespace {
+
+constexpr int kBwdStages = 2;
+constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows each
+constexpr int kZRows = 16 * 128;        // [Z_hi; Z_lo; 0 ...]
+constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
+constexpr int kArr = 4096;              // small float arrays
+constexpr int kBwdSmem = 1024 + kBwdStages * 4 * kTile + kSnapB + kZRows + kGnB + kArr + 2048;
+
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(a, b);
+  lo = pack_bf16(a - bf16_lo_f(hi), b - bf16_hi_f(hi));
+}
+
+// Writes the float32 row `x` (64 values) as bf16 hi and lo rows of two
+// 128-byte-swizzled operand buffers.
+__device__ __forceinline__ void store_split_row(uint8_t* hi_buf, uint8_t* lo_buf, int row,
+                                                const float* x) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) split_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1], h[q], l[q]);
+    *reinterpret_cast<uint4*>(hi_buf + sw128(row, c * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_buf + sw128(row, c * 16)) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// 16 consecutive bf16 of row `row`, logical 16-byte chunks c0, c0+1 -> float.
+__device__ __forceinline__ void load_row16(const uint8_t* tile, int row, int c0, float* out) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128(row, (c0 + c) * 16));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      out[8 * c + 2 * q] = bf16_lo_f(u[q]);
+      out[8 * c + 2 * q + 1] = bf16_hi_f(u[q]);
+    }
+  }
+}
+
+struct BwdSmem {
+  uint8_t* stages;
+  uint8_t* s_hi;
+  uint8_t* s_lo;
+  uint8_t* zrows;
+  uint8_t* gn_hi;
+  uint8_t* gn_lo;
+  float* arr;
+  uint64_t* full;
+  uint64_t* mma_bar;
+  uint32_t* tslot;
+  __device__ explicit BwdSmem(uint8_t* raw) {
+    uint8_t* sm =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    stages = sm;
+    s_hi = sm + kBwdStages * 4 * kTile;
+    s_lo = s_hi + kDim * 128;
+    zrows = s_lo + kDim * 128;
+    gn_hi = zrows + kZRows;
+    gn_lo = gn_hi + kTile;
+    arr = reinterpret_cast<float*>(gn_lo + kTile);
+    uint8_t* misc = reinterpret_cast<uint8_t*>(arr) + kArr;
+    full = reinterpret_cast<uint64_t*>(misc);
+    mma_bar = full + kBwdStages;
+    tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  }
+  __device__ uint8_t* tile(int stage, int which) { return stages + (stage * 4 + which) * kTile; }
+};
+
+enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
+
+// --------------------------------------------------- forward direction: dq
+
+// TMEM columns
+constexpr uint32_t kFP = 0;     // 128: P, then bf16 P_L in [0,64); then T, bf16 T_L in [0,64)
+constexpr uint32_t kFO = 128;   // 64: numerator
+constexpr uint32_t kFOz = 192;  // 16: phi(Q) . [Z_hi, Z_lo]
+constexpr uint32_t kFQ = 256;   // 64: dphiQ
+constexpr uint32_t kFS = 320;   // 64: dS^T (M = 64 layout)
+constexpr uint32_t kFR = 384;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                Geometry g, const float* __restrict__ sprefix, float* __restrict__ rpartial,
+                float* __restrict__ dq, float* __restrict__ den_out, float* __restrict__ gd_out,
+                WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  BwdSmem sm(smraw);
+  float* zsnap = sm.arr;          // 64: Z before the chunk (float32)
+  float* gds = sm.arr + 64;       // 128: gd per row
+  float* dz = sm.arr + 192;       // [4][64]: warp column sums
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  if (tid == 0) {
+    for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
+    mbar_init(sm.mma_bar, 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < kZRows / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(sm.zrows)[e] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    tmem_alloc(sm.tslot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *sm.tslot;
+  const uint32_t tl = lane_base(tbase);
+
+  const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
+  Cursor cc, cp;
+  cc.start(g);
+  cp.start(g);
+  long long issued = 0;
+  auto issue = [&](Cursor& c) {
+    const int s = issued % kBwdStages;
+    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    mbar_arrive_expect_tx(&sm.full[s], tx);
+    tma_load_3d(sm.tile(s, kQ), &tm_q, &sm.full[s], 0, t0, bh);
+    tma_load_3d(sm.tile(s, kG), &tm_g, &sm.full[s], 0, t0, bh);
+    if (CAUSAL) {
+      tma_load_3d(sm.tile(s, kK), &tm_k, &sm.full[s], 0, t0, bh);
+      tma_load_3d(sm.tile(s, kV), &tm_v, &sm.full[s], 0, t0, bh);
+    }
+    ++issued;
+    c.advance(g);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
+
+  float srun[64];
+  float zrun = 0.f, r0 = 0.f, r1 = 0.f;
+  const int srow = warp * 16 + lane;
+  const bool sthread = lane < 16;
+  long long consumed = 0;
+  uint32_t ph = 0;
+  float z[64];
+
+  while (cc.valid(g)) {
+    const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
+    const bool first = cc.chunk == g.chunk_begin(item);
+    const bool last = cc.chunk + 1 == g.chunk_end(item);
+    const int nvalid = min(kC, g.N - t0);
+    const int i = tid;  // query row of this thread
+    if (tid == 0 && cp.valid(g)) issue(cp);
+    if (first) {
+      const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+      if (sthread) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float4 x = s4[j];
+          srun[4 * j] = x.x;
+          srun[4 * j + 1] = x.y;
+          srun[4 * j + 2] = x.z;
+          srun[4 * j + 3] = x.w;
+        }
+      }
+      if (tid < kDim) zrun = src[kDim * kDim + tid];
+      r0 = r1 = 0.f;
+    }
+    if ((CAUSAL || first) && sthread) store_split_row(sm.s_hi, sm.s_lo, srow, srun);
+    if (tid < kDim) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(zrun);
+      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(0, 2 * tid)) = h;
+      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(1, 2 * tid)) =
+          __float2bfloat16_rn(zrun - __bfloat162float(h));
+      zsnap[tid] = zrun;
+    }
+    const int s = consumed % kBwdStages;
+    uint8_t* qt = sm.tile(s, kQ);
+    uint8_t* kt = sm.tile(s, kK);
+    uint8_t* vt = sm.tile(s, kV);
+    uint8_t* gt = sm.tile(s, kG);
+    if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 21)) break;
+    phi_row<false>(qt, tid, kC, z);
+    if (CAUSAL) {
+      phi_row<true>(kt, tid, nvalid, z);
+      const float2 cs = warp_column_sums(z);
+      dz[warp * 64 + 2 * lane] = cs.x;
+      dz[warp * 64 + 2 * lane + 1] = cs.y;
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo), za = smem_u32(sm.zrows);
+      if (CAUSAL) {
+        const uint32_t idP = idesc_bf16(128, 128, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
+        const uint32_t idS = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
+                 idS, k);
+      }
+      const uint32_t idO = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
+      const uint32_t idZ = idesc_bf16(128, 16, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+      mma_commit(sm.mma_bar);
+    }
+    if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
+    ph ^= 1;
+    fence_after_sync();
+
+    float rowsum = 0.f;
+    if (CAUSAL) {
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        uint32_t pk[16];
+        if (sl <= warp) {
+          uint32_t r[32];
+          tmem_ld32(tl + kFP + 32 * sl, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int j0 = 32 * sl + 2 * c;
+            pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) : 0.f,
+                              j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f);
+            rowsum += bf16_lo_f(pk[c]) + bf16_hi_f(pk[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        }
+        tmem_st16(tl + kFP + 16 * sl, pk);
+      }
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tl + kFS + 32 * half, r);
+          if (sthread) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) srun[32 * half + j] += __uint_as_float(r[j]);
+          }
+        }
+      }
+      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t va = smem_u32(vt);
+        const uint32_t idPV = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFO, tbase + kFP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
+        mma_commit(sm.mma_bar);
+      }
+      if (!wait_uniform(sm.mma_bar, ph, hdr, 23)) break;
+      ph ^= 1;
+      fence_after_sync();
+    }
+
+    // den, out, gN = G / den, gd = -(G . out) / den
+    float gd;
+    {
+      uint32_t oz[16];
+      tmem_ld16(tl + kFOz, oz);
+      const float den = rowsum + __uint_as_float(oz[0]) + __uint_as_float(oz[1]);
+      const float inv = 1.f / den;
+      float go = 0.f;
+      float gn[64];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(tl + kFO + 32 * half, r);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float gv[16];
+          load_row16(gt, i, half * 4 + 2 * c, gv);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float out = __uint_as_float(r[16 * c + q]) * inv;
+            go += gv[q] * out;
+            gn[32 * half + 16 * c + q] = gv[q] * inv;
+          }
+        }
+      }
+      gd = -go * inv;
+      store_split_row(sm.gn_hi, sm.gn_lo, i, gn);
+      gds[i] = gd;
+      if (i < nvalid) {
+        den_out[(size_t)bh * g.N + t0 + i] = den;
+        gd_out[(size_t)bh * g.N + t0 + i] = gd;
+      }
+      // this chunk's share of r = sum_i gd_i phi(Q_i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float qv[16];
+        load_row16(qt, i, 2 * c, qv);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) z[16 * c + q] = gd * qv[q];
+      }
+      const float2 cs = warp_column_sums(z);
+      dz[warp * 64 + 2 * lane] = cs.x;
+      dz[warp * 64 + 2 * lane + 1] = cs.y;
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 0) {
+      r0 += dz[2 * lane] + dz[64 + 2 * lane] + dz[128 + 2 * lane] + dz[192 + 2 * lane];
+      r1 += dz[2 * lane + 1] + dz[65 + 2 * lane] + dz[129 + 2 * lane] + dz[193 + 2 * lane];
+    }
+    if (tid == 0) {
+      const uint32_t qa = smem_u32(qt), va = smem_u32(vt);
+      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
+      if (CAUSAL) {  // T = gN V^T (hi + lo)
+        const uint32_t idT = idesc_bf16(128, 128, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kFP, sdesc(gha + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), idT, k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kFP, sdesc(gla + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), idT, 1);
+      }
+      // dphiQ = gN S_prev^T: B is the S^T snapshot read MN-major (rows m, d contiguous)
+      const uint32_t idQ = idesc_bf16(128, 64, false, true);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idQ, 1);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, 1);
+      // segment sum of phi(Q)^T gN (hi + lo)
+      const uint32_t idR = idesc_bf16(64, 64, true, true);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
+               (first && k == 0) ? 0u : 1u);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
+               1);
+      mma_commit(sm.mma_bar);
+    }
+    if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
+    ph ^= 1;
+    fence_after_sync();
+
+    if (CAUSAL) {  // T_L = (T + gd_i) masked to j <= i, bf16, for the TMEM A operand
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        uint32_t pk[16];
+        if (sl <= warp) {
+          uint32_t r[32];
+          tmem_ld32(tl + kFP + 32 * sl, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int j0 = 32 * sl + 2 * c;
+            pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) + gd : 0.f,
+                              j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) + gd : 0.f);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        }
+        tmem_st16(tl + kFP + 16 * sl, pk);
+      }
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t ka = smem_u32(kt);
+        const uint32_t idTK = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFP + k * 8, sdesc(ka + k * 2048, 1024, 1024), idTK, 1);
+        mma_commit(sm.mma_bar);
+      }
+      if (!wait_uniform(sm.mma_bar, ph, hdr, 25)) break;
+      ph ^= 1;
+      fence_after_sync();
+    }
+
+    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      tmem_ld32(tl + kFQ + 32 * half, r);
+      if (i < nvalid) {
+        float4* dst = reinterpret_cast<float4*>(dq + ((size_t)bh * g.N + t0 + i) * kDim + 32 * half);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float qv[16];
+          load_row16(qt, i, half * 4 + 2 * c, qv);
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int d = 32 * half + 16 * c + q + u;
+              o[u] = (__uint_as_float(r[16 * c + q + u]) + gd * zsnap[d]) * fminf(qv[q + u], 1.f);
+            }
+            dst[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+
+    if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
+      float* dst = rpartial + (size_t)item * kStateFloats;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(tl + kFR + 32 * half, r);
+        if (sthread) {
+          float4* d4 = reinterpret_cast<float4*>(dst + srow * kDim + 32 * half);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (warp == 0) {
+        dst[kDim * kDim + 2 * lane] = r0;
+        dst[kDim * kDim + 2 * lane + 1] = r1;
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    ++consumed;
+    cc.advance(g);
+  }
+  if (tid == 0) {
+    while (consumed < issued) {
+      const int s = consumed % kBwdStages;
+      if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 26);
+      ++consumed;
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// --------------------------------------------------- reverse direction: dk, dv
+
+constexpr uint32_t kRP = 0;     // 128: P^T (rows keys), then bf16 P_L^T in [0, 64)
+constexpr uint32_t kRT = 128;   // 128: T^T, then bf16 T_L^T in [128, 192)
+constexpr uint32_t kRV = 256;   // 64: dV
+constexpr uint32_t kRK = 320;   // 64: dphiK
+constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                 Geometry g, const float* __restrict__ rsuffix, const float* __restrict__ den_in,
+                 const float* __restrict__ gd_in, float* __restrict__ dk, float* __restrict__ dv,
+                 WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  BwdSmem sm(smraw);
+  // the state snapshot buffers hold R rows d (m contiguous)
+  float* rsnap = sm.arr;         // 64: r before the chunk
+  float* gds = sm.arr + 64;      // 128
+  float* dens = sm.arr + 192;    // 128
+  float* dz = sm.arr + 320;      // [4][64]
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  if (tid == 0) {
+    for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
+    mbar_init(sm.mma_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sm.tslot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *sm.tslot;
+  const uint32_t tl = lane_base(tbase);
+
+  const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
+  RevCursor cc, cp;
+  cc.start(g);
+  cp.start(g);
+  long long issued = 0;
+  auto issue = [&](RevCursor& c) {
+    const int s = issued % kBwdStages;
+    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    mbar_arrive_expect_tx(&sm.full[s], tx);
+    tma_load_3d(sm.tile(s, kK), &tm_k, &sm.full[s], 0, t0, bh);
+    tma_load_3d(sm.tile(s, kV), &tm_v, &sm.full[s], 0, t0, bh);
+    if (CAUSAL) {
+      tma_load_3d(sm.tile(s, kQ), &tm_q, &sm.full[s], 0, t0, bh);
+      tma_load_3d(sm.tile(s, kG), &tm_g, &sm.full[s], 0, t0, bh);
+    }
+    ++issued;
+    c.advance(g);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
+
+  float rrun[64];
+  float rr = 0.f;  // r[d] for d = tid < 64
+  const int srow = warp * 16 + lane;
+  const bool sthread = lane < 16;
+  long long consumed = 0;
+  uint32_t ph = 0;
+  float z[64];
+
+  while (cc.valid(g)) {
+    const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
+    const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
+    const int nvalid = min(kC, g.N - t0);
+    const int j = tid;  // key row of this thread (also the query row it prepares)
+    if (tid == 0 && cp.valid(g)) issue(cp);
+    if (first) {
+      const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+      if (sthread) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 x = s4[q];
+          rrun[4 * q] = x.x;
+          rrun[4 * q + 1] = x.y;
+          rrun[4 * q + 2] = x.z;
+          rrun[4 * q + 3] = x.w;
+        }
+      }
+      if (tid < kDim) rr = src[kDim * kDim + tid];
+    }
+    if ((CAUSAL || first) && sthread) store_split_row(sm.s_hi, sm.s_lo, srow, rrun);
+    if (tid < kDim) rsnap[tid] = rr;
+    if (CAUSAL) {
+      const bool valid = tid < nvalid;
+      dens[tid] = valid ? den_in[(size_t)bh * g.N + t0 + tid] : 1.f;
+      gds[tid] = valid ? gd_in[(size_t)bh * g.N + t0 + tid] : 0.f;
+    }
+    const int s = consumed % kBwdStages;
+    uint8_t* qt = sm.tile(s, kQ);
+    uint8_t* kt = sm.tile(s, kK);
+    uint8_t* vt = sm.tile(s, kV);
+    uint8_t* gt = sm.tile(s, kG);
+    if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 31)) break;
+    phi_row<false>(kt, tid, nvalid, z);
+    if (CAUSAL) {
+      phi_row<false>(qt, tid, kC, z);
+      // gN row (query row = tid) and this chunk's share of r
+      const float inv = 1.f / dens[tid];
+      float gn[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float gv[16], qv[16];
+        load_row16(gt, tid, 2 * c, gv);
+        load_row16(qt, tid, 2 * c, qv);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          gn[16 * c + q] = gv[q] * inv;
+          z[16 * c + q] = gds[tid] * qv[q];
+        }
+      }
+      store_split_row(sm.gn_hi, sm.gn_lo, tid, gn);
+      const float2 cs = warp_column_sums(z);
+      dz[warp * 64 + 2 * lane] = cs.x;
+      dz[warp * 64 + 2 * lane + 1] = cs.y;
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
+      if (CAUSAL) {
+        const uint32_t idP = idesc_bf16(128, 128, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // P^T = phi(K) phi(Q)^T
+          mma_ss(tbase + kRP, sdesc(ka + k * 32, 16, 1024), sdesc(qa + k * 32, 16, 1024), idP, k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // T^T = V gN^T (hi + lo)
+          mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(gha + k * 32, 16, 1024), idP, k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(gla + k * 32, 16, 1024), idP, 1);
+        const uint32_t idR = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+                 idR, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
+                 idR, 1);
+      }
+      // dV = phi(K) R_next: B = R rows d read MN-major (n = m contiguous)
+      const uint32_t idVn = idesc_bf16(128, 64, false, true);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idVn, k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idVn, 1);
+      // dphiK = V R_next^T: B = R rows d read K-major (k = m contiguous)
+      const uint32_t idKn = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idKn, k);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idKn, 1);
+      mma_commit(sm.mma_bar);
+    }
+    if (!wait_uniform(sm.mma_bar, ph, hdr, 32)) break;
+    ph ^= 1;
+    fence_after_sync();
+
+    if (CAUSAL) {
+      // key row j keeps query columns i >= j
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        uint32_t pp[16], pt[16];
+        if (sl >= warp) {
+          uint32_t r[32];
+          tmem_ld32(tl + kRP + 32 * sl, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int i0 = 32 * sl + 2 * c;
+            pp[c] = pack_bf16(i0 >= j ? __uint_as_float(r[2 * c]) : 0.f,
+                              i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) : 0.f);
+          }
+          tmem_ld32(tl + kRT + 32 * sl, r);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int i0 = 32 * sl + 2 * c;
+            pt[c] = pack_bf16(i0 >= j ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
+                              i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pp[c] = pt[c] = 0u;
+        }
+        tmem_st16(tl + kRP + 16 * sl, pp);
+        tmem_st16(tl + kRT + 16 * sl, pt);
+      }
+      {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
+        uint32_t r[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tl + kRR + 32 * half, r);
+          if (sthread) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) rrun[32 * half + q] += __uint_as_float(r[q]);
+          }
+        }
+      }
+      if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t qa = smem_u32(qt);
+        const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+        const uint32_t idV = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T gN
+          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gha + k * 2048, 1024, 1024), idV, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gla + k * 2048, 1024, 1024), idV, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_L^T phi(Q)
+          mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
+        mma_commit(sm.mma_bar);
+      }
+      if (!wait_uniform(sm.mma_bar, ph, hdr, 33)) break;
+      ph ^= 1;
+      fence_after_sync();
+    }
+
+    // dk = (dphiK + r_next) * phi'(k), dv
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      tmem_ld32(tl + kRK + 32 * half, r);
+      uint32_t w[32];
+      tmem_ld32(tl + kRV + 32 * half, w);
+      if (j < nvalid) {
+        const size_t row = (size_t)bh * g.N + t0 + j;
+        float4* dkp = reinterpret_cast<float4*>(dk + row * kDim + 32 * half);
+        float4* dvp = reinterpret_cast<float4*>(dv + row * kDim + 32 * half);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float kv[16];
+          load_row16(kt, j, half * 4 + 2 * c, kv);
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            float o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int d = 32 * half + 16 * c + q + u;
+              o[u] = (__uint_as_float(r[16 * c + q + u]) + rsnap[d]) * fminf(kv[q + u], 1.f);
+            }
+            dkp[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
+            dvp[(16 * c + q) / 4] =
+                make_float4(__uint_as_float(w[16 * c + q]), __uint_as_float(w[16 * c + q + 1]),
+                            __uint_as_float(w[16 * c + q + 2]), __uint_as_float(w[16 * c + q + 3]));
+          }
+        }
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    ++consumed;
+    cc.advance(g);
+  }
+  if (tid == 0) {
+    while (consumed < issued) {
+      const int s = consumed % kBwdStages;
+      if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 36);
+      ++consumed;
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+size_t states_bytes(const Geometry& g) {
+  return align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256);
+}
+
+}  // namespace
+}  // namespace tcx
+
+using namespace tcx;
+
+size_t tc_backward_workspace(int BH, int N) {
+  const Geometry g = make_geometry(BH, N);
+  return kHeaderBytes + 4 * states_bytes(g) + 2 * align_up(sizeof(float) * (size_t)BH * N, 256);
+}
+
+cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                        float* dk, float* dv, int BH, int N, bool causal, void* ws,
+                        cudaStream_t st) {
+  const Geometry g = make_geometry(BH, N);
+  WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
+  char* base = static_cast<char*>(ws) + kHeaderBytes;
+  const size_t sb = states_bytes(g);
+  float* spartial = reinterpret_cast<float*>(base);
+  float* sprefix = reinterpret_cast<float*>(base + sb);
+  float* rpartial = reinterpret_cast<float*>(base + 2 * sb);
+  float* rsuffix = reinterpret_cast<float*>(base + 3 * sb);
+  float* den = reinterpret_cast<float*>(base + 4 * sb);
+  float* gd = den + align_up(sizeof(float) * (size_t)BH * N, 256) / sizeof(float);
+
+  CUtensorMap tq, tk, tv, tg;
+  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
+  if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1))
+    return cudaErrorInvalidValue;
+
+  cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, st);
+  if (e != cudaSuccess) return e;
+  e = launch_scan(spartial, sprefix, g, causal ? kScanPrefix : kScanTotal, nullptr, nullptr, st);
+  if (e != cudaSuccess) return e;
+
+  const int sms = sm_count();
+  auto run_q = [&](auto kern) {
+    cudaError_t err = configure(kern, kBwdSmem);
+    if (err != cudaSuccess) return err;
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem) * sms);
+    kern<<<ctas, kThreadsTC, kBwdSmem, st>>>(tq, tk, tv, tg, g, sprefix, rpartial, dq, den, gd, hdr);
+    count_launches(1);
+    return cudaGetLastError();
+  };
+  e = causal ? run_q(tc_bwd_q_kernel<true>) : run_q(tc_bwd_q_kernel<false>);
+  if (e != cudaSuccess) return e;
+  e = launch_scan(rpartial, rsuffix, g, causal ? kScanSuffix : kScanTotal, nullptr, nullptr, st);
+  if (e != cudaSuccess) return e;
+  auto run_kv = [&](auto kern) {
+    cudaError_t err = configure(kern, kBwdSmem);
+    if (err != cudaSuccess) return err;
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem) * sms);
+    kern<<<ctas, kThreadsTC, kBwdSmem, st>>>(tq, tk, tv, tg, g, rsuffix, den, gd, dk, dv, hdr);
+    count_launches(1);
+    return cudaGetLastError();
+  };
+  return causal ? run_kv(tc_bwd_kv_kernel<true>) : run_kv(tc_bwd_kv_kernel<false>);
+}
+
+}  // namespace la

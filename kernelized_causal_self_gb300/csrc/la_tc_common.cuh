@@ -51,6 +51,22 @@ struct Cursor {
   }
 };
 
+// Same items as Cursor, but each item's chunks from last to first.
+struct RevCursor {
+  int item, chunk;
+  __device__ void start(const Geometry& g) {
+    item = blockIdx.x;
+    chunk = item < g.n_items() ? g.chunk_end(item) - 1 : 0;
+  }
+  __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
+  __device__ void advance(const Geometry& g) {
+    if (--chunk < g.chunk_begin(item)) {
+      item += gridDim.x;
+      if (item < g.n_items()) chunk = g.chunk_end(item) - 1;
+    }
+  }
+};
+
 __device__ __forceinline__ float bf16_lo_f(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
@@ -185,6 +201,15 @@ inline int resident_ctas(K kernel, int smem) {
 
 int sm_count();
 Geometry make_geometry(int BH, int N);
+
+enum ScanMode { kScanPrefix = 0, kScanTotal = 1, kScanSuffix = 2 };
+
+// Segment increments dS^T = V^T phi(K), dZ = sum phi(K) into partial[item].
+cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st);
+// Prefix / total / suffix of the per-segment states (see ScanMode).
+cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
+                        float* Z_out, cudaStream_t st);
 
 }  // namespace tcx
 }  // namespace la

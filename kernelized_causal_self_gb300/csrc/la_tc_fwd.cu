@@ -171,34 +171,39 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // ----------------------------------------------------------- 2. segment scan
 
-// prefix[bh][seg] = sum_{s < seg} partial[bh][s]  (causal)
-// prefix[bh][0]   = sum_s partial[bh][s]           (non-causal)
-// S_out[bh][d][m], Z_out[bh][d] = full sum when requested.
+// mode kScanPrefix:  out[seg][bh] = sum_{s < seg} partial[s][bh]  (causal, forward)
+// mode kScanTotal:   out[bh]      = sum_s partial[s][bh]          (non-causal)
+// mode kScanSuffix:  out[seg][bh] = sum_{s > seg} partial[s][bh]  (causal, reverse)
+// S_out[bh][d][m], Z_out[bh][d] = full sum when requested (prefill).
 // One thread per state element; the segment loads are issued in batches of 8
 // so the walk over segments is not a chain of dependent global loads.
 constexpr int kScanThreads = 128;
 
 __global__ void __launch_bounds__(kScanThreads)
-state_scan_kernel(const float* __restrict__ partial, float* __restrict__ prefix, int BH, int n_seg,
-                  int causal, float* __restrict__ S_out, float* __restrict__ Z_out) {
+state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, int BH, int n_seg,
+                  int mode, float* __restrict__ S_out, float* __restrict__ Z_out) {
   const int bh = blockIdx.y;
   const int e = blockIdx.x * kScanThreads + threadIdx.x;
   if (e >= kStateFloats) return;
   float run = 0.f;
+  const bool rev = mode == kScanSuffix;
   for (int s0 = 0; s0 < n_seg; s0 += 8) {
     float x[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      x[j] = s0 + j < n_seg ? partial[((size_t)(s0 + j) * BH + bh) * kStateFloats + e] : 0.f;
+    for (int j = 0; j < 8; ++j) {
+      const int sg = rev ? n_seg - 1 - (s0 + j) : s0 + j;
+      x[j] = s0 + j < n_seg ? partial[((size_t)sg * BH + bh) * kStateFloats + e] : 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (s0 + j < n_seg) {
-        if (causal) prefix[((size_t)(s0 + j) * BH + bh) * kStateFloats + e] = run;
+        const int sg = rev ? n_seg - 1 - (s0 + j) : s0 + j;
+        if (mode != kScanTotal) out[((size_t)sg * BH + bh) * kStateFloats + e] = run;
         run += x[j];
       }
     }
   }
-  if (!causal) prefix[(size_t)bh * kStateFloats + e] = run;
+  if (mode == kScanTotal) out[(size_t)bh * kStateFloats + e] = run;
   if (S_out != nullptr) {
     if (e < kDim * kDim) {
       const int m = e / kDim, d = e % kDim;
@@ -519,6 +524,24 @@ Geometry make_geometry(int BH, int N) {
   return g;
 }
 
+cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st) {
+  cudaError_t e = configure(tc_state_kernel, kStateSmem);
+  if (e != cudaSuccess) return e;
+  const int ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem) * sm_count());
+  tc_state_kernel<<<ctas, kThreadsTC, kStateSmem, st>>>(*tk, *tv, g, partial, hdr);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
+                        float* Z_out, cudaStream_t st) {
+  const dim3 grid((kStateFloats + kScanThreads - 1) / kScanThreads, g.BH);
+  state_scan_kernel<<<grid, kScanThreads, 0, st>>>(partial, out, g.BH, g.n_seg, mode, S_out, Z_out);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace tcx
 
 using namespace tcx;
@@ -544,18 +567,11 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
       !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
 
-  const int sms = sm_count();
-  cudaError_t e = configure(tc_state_kernel, kStateSmem);
+  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, st);
   if (e != cudaSuccess) return e;
-  const int state_ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem) * sms);
-  tc_state_kernel<<<state_ctas, kThreadsTC, kStateSmem, st>>>(tk, tv, g, partial, hdr);
-  count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 scan_grid((kStateFloats + kScanThreads - 1) / kScanThreads, BH);
-  state_scan_kernel<<<scan_grid, kScanThreads, 0, st>>>(partial, prefix, BH, g.n_seg, causal ? 1 : 0,
-                                                        S_out, Z_out);
-  count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, S_out, Z_out, st);
+  if (e != cudaSuccess) return e;
+  const int sms = sm_count();
 
   // non-causal: one item per chunk range of the readout, all reading prefix[bh]
   if (causal) {
