@@ -23,10 +23,14 @@
 // scan gives R_next per segment; tc_bwd_kv_kernel walks each segment's chunks
 // from last to first and writes dk, dv.
 //
-// Precision: T_ij and S gN + gd Z cancel strongly (exactly at i = j = 0), so
-// gN enters the tensor cores as a bf16 hi + lo pair, the carried states as hi
-// + lo pairs, and gd is added in float32; the cancelled results are only then
-// rounded to bf16 (T_L) or kept in float32.
+// Precision: phi(k) = 1 + k for small k, and dq = sum_j T_ij phi(K_j) cancels
+// the constant part (sum_j T_ij ~ 0; exactly 0 at i = j = 0). What is left is
+// carried by k, so bf16 rounding of phi(K) (2^-9 absolute at 1.0) would cost
+// dq ~2% normwise and ~10% on its significant elements; likewise phi(Q) for dk
+// and P_L, T_L for dq. Every operand that feeds such a sum therefore enters the
+// tensor cores as a bf16 hi + lo pair (phi(K) and P_L in the forward-direction
+// kernel and the prefix states, phi(Q) in both kernels' R sums and T_L^T phi(Q),
+// T_L / T_L^T, gN, and the carried states), and gd is added in float32.
 #include "la_tc_common.cuh"
 
 namespace la {
@@ -38,7 +42,9 @@ constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows ea
 constexpr int kZRows = 16 * 128;        // [Z_hi; Z_lo; 0 ...]
 constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
 constexpr int kArr = 4096;              // small float arrays
-constexpr int kBwdSmem = 1024 + kBwdStages * 4 * kTile + kSnapB + kZRows + kGnB + kArr + 2048;
+constexpr int kLoB = 2 * kTile;         // phi(Q), phi(K) lo parts
+constexpr int kBwdSmem =
+    1024 + kBwdStages * 4 * kTile + kSnapB + kZRows + kGnB + kLoB + kArr + 2048;
 
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
@@ -80,6 +86,8 @@ struct BwdSmem {
   uint8_t* zrows;
   uint8_t* gn_hi;
   uint8_t* gn_lo;
+  uint8_t* qlo;
+  uint8_t* klo;
   float* arr;
   uint64_t* full;
   uint64_t* mma_bar;
@@ -93,7 +101,9 @@ struct BwdSmem {
     zrows = s_lo + kDim * 128;
     gn_hi = zrows + kZRows;
     gn_lo = gn_hi + kTile;
-    arr = reinterpret_cast<float*>(gn_lo + kTile);
+    qlo = gn_lo + kTile;
+    klo = qlo + kTile;
+    arr = reinterpret_cast<float*>(klo + kTile);
     uint8_t* misc = reinterpret_cast<uint8_t*>(arr) + kArr;
     full = reinterpret_cast<uint64_t*>(misc);
     mma_bar = full + kBwdStages;
@@ -113,6 +123,7 @@ constexpr uint32_t kFOz = 192;  // 16: phi(Q) . [Z_hi, Z_lo]
 constexpr uint32_t kFQ = 256;   // 64: dphiQ
 constexpr uint32_t kFS = 320;   // 64: dS^T (M = 64 layout)
 constexpr uint32_t kFR = 384;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
+constexpr uint32_t kFL = 448;   // 64: bf16 lo parts of P_L, then of T_L
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -211,9 +222,9 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 21)) break;
-    phi_row<false>(qt, tid, kC, z);
+    phi_row_split(qt, sm.qlo, tid, kC, z);
     if (CAUSAL) {
-      phi_row<true>(kt, tid, nvalid, z);
+      phi_row_split(kt, sm.klo, tid, nvalid, z);
       const float2 cs = warp_column_sums(z);
       dz[warp * 64 + 2 * lane] = cs.x;
       dz[warp * 64 + 2 * lane + 1] = cs.y;
@@ -224,17 +235,25 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     fence_after_sync();
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t kl = smem_u32(sm.klo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo), za = smem_u32(sm.zrows);
       if (CAUSAL) {
         const uint32_t idP = idesc_bf16(128, 128, false, false);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(kl + k * 32, 16, 1024), idP, 1);
         const uint32_t idS = idesc_bf16(64, 64, true, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
                  idS, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024),
+                 idS, 1);
       }
       const uint32_t idO = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -257,22 +276,24 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (CAUSAL) {
 #pragma unroll
       for (int sl = 0; sl < 4; ++sl) {
-        uint32_t pk[16];
+        uint32_t ph16[16], pl16[16];
         if (sl <= warp) {
           uint32_t r[32];
           tmem_ld32(tl + kFP + 32 * sl, r);
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int j0 = 32 * sl + 2 * c;
-            pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) : 0.f,
-                              j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f);
-            rowsum += bf16_lo_f(pk[c]) + bf16_hi_f(pk[c]);
+            const float a = j0 <= i ? __uint_as_float(r[2 * c]) : 0.f;
+            const float b = j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f;
+            split_bf16(a, b, ph16[c], pl16[c]);
+            rowsum += a + b;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+          for (int c = 0; c < 16; ++c) ph16[c] = pl16[c] = 0u;
         }
-        tmem_st16(tl + kFP + 16 * sl, pk);
+        tmem_st16(tl + kFP + 16 * sl, ph16);
+        tmem_st16(tl + kFL + 16 * sl, pl16);
       }
       {
         uint32_t r[32];
@@ -295,6 +316,9 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kFO, tbase + kFP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFO, tbase + kFL + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
         mma_commit(sm.mma_bar);
       }
       if (!wait_uniform(sm.mma_bar, ph, hdr, 23)) break;
@@ -337,10 +361,11 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // this chunk's share of r = sum_i gd_i phi(Q_i)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float qv[16];
+        float qv[16], ql[16];
         load_row16(qt, i, 2 * c, qv);
+        load_row16(sm.qlo, i, 2 * c, ql);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) z[16 * c + q] = gd * qv[q];
+        for (int q = 0; q < 16; ++q) z[16 * c + q] = gd * (qv[q] + ql[q]);
       }
       const float2 cs = warp_column_sums(z);
       dz[warp * 64 + 2 * lane] = cs.x;
@@ -355,7 +380,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       r1 += dz[2 * lane + 1] + dz[65 + 2 * lane] + dz[129 + 2 * lane] + dz[193 + 2 * lane];
     }
     if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), va = smem_u32(vt);
+      const uint32_t qa = smem_u32(qt), va = smem_u32(vt), ql = smem_u32(sm.qlo);
       const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
       if (CAUSAL) {  // T = gN V^T (hi + lo)
@@ -388,40 +413,51 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < kC / 16; ++k)
         mma_ss(tbase + kFR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
                1);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + kFR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
+               1);
       mma_commit(sm.mma_bar);
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
     ph ^= 1;
     fence_after_sync();
 
-    if (CAUSAL) {  // T_L = (T + gd_i) masked to j <= i, bf16, for the TMEM A operand
+    if (CAUSAL) {  // T_L = (T + gd_i) masked to j <= i, bf16 hi + lo, TMEM A operands
 #pragma unroll
       for (int sl = 0; sl < 4; ++sl) {
-        uint32_t pk[16];
+        uint32_t th[16], tlo[16];
         if (sl <= warp) {
           uint32_t r[32];
           tmem_ld32(tl + kFP + 32 * sl, r);
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int j0 = 32 * sl + 2 * c;
-            pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) + gd : 0.f,
-                              j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) + gd : 0.f);
+            split_bf16(j0 <= i ? __uint_as_float(r[2 * c]) + gd : 0.f,
+                       j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) + gd : 0.f, th[c], tlo[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+          for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
         }
-        tmem_st16(tl + kFP + 16 * sl, pk);
+        tmem_st16(tl + kFP + 16 * sl, th);
+        tmem_st16(tl + kFL + 16 * sl, tlo);
       }
       fence_before_sync();
       __syncthreads();
       fence_after_sync();
       if (tid == 0) {
-        const uint32_t ka = smem_u32(kt);
+        const uint32_t ka = smem_u32(kt), kl = smem_u32(sm.klo);
         const uint32_t idTK = idesc_bf16(128, 64, false, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kFQ, tbase + kFP + k * 8, sdesc(ka + k * 2048, 1024, 1024), idTK, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFP + k * 8, sdesc(kl + k * 2048, 1024, 1024), idTK, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFL + k * 8, sdesc(ka + k * 2048, 1024, 1024), idTK, 1);
         mma_commit(sm.mma_bar);
       }
       if (!wait_uniform(sm.mma_bar, ph, hdr, 25)) break;
@@ -499,6 +535,7 @@ constexpr uint32_t kRT = 128;   // 128: T^T, then bf16 T_L^T in [128, 192)
 constexpr uint32_t kRV = 256;   // 64: dV
 constexpr uint32_t kRK = 320;   // 64: dphiK
 constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
+constexpr uint32_t kRL = 448;   // 64: bf16 lo part of T_L^T
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -596,19 +633,18 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 31)) break;
     phi_row<false>(kt, tid, nvalid, z);
     if (CAUSAL) {
-      phi_row<false>(qt, tid, kC, z);
+      phi_row_split(qt, sm.qlo, tid, kC, z);
       // gN row (query row = tid) and this chunk's share of r
       const float inv = 1.f / dens[tid];
       float gn[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float gv[16], qv[16];
+        float gv[16];
         load_row16(gt, tid, 2 * c, gv);
-        load_row16(qt, tid, 2 * c, qv);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           gn[16 * c + q] = gv[q] * inv;
-          z[16 * c + q] = gds[tid] * qv[q];
+          z[16 * c + q] *= gds[tid];
         }
       }
       store_split_row(sm.gn_hi, sm.gn_lo, tid, gn);
@@ -644,6 +680,11 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
                  idR, 1);
+        const uint32_t ql = smem_u32(sm.qlo);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+                 idR, 1);
       }
       // dV = phi(K) R_next: B = R rows d read MN-major (n = m contiguous)
       const uint32_t idVn = idesc_bf16(128, 64, false, true);
@@ -671,7 +712,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // key row j keeps query columns i >= j
 #pragma unroll
       for (int sl = 0; sl < 4; ++sl) {
-        uint32_t pp[16], pt[16];
+        uint32_t pp[16], pt[16], ptl[16];
         if (sl >= warp) {
           uint32_t r[32];
           tmem_ld32(tl + kRP + 32 * sl, r);
@@ -685,15 +726,17 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int i0 = 32 * sl + 2 * c;
-            pt[c] = pack_bf16(i0 >= j ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
-                              i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f);
+            split_bf16(i0 >= j ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
+                       i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f, pt[c],
+                       ptl[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pp[c] = pt[c] = 0u;
+          for (int c = 0; c < 16; ++c) pp[c] = pt[c] = ptl[c] = 0u;
         }
         tmem_st16(tl + kRP + 16 * sl, pp);
         tmem_st16(tl + kRT + 16 * sl, pt);
+        tmem_st16(tl + kRL + 16 * sl, ptl);
       }
       {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
         uint32_t r[32];
@@ -720,9 +763,16 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gla + k * 2048, 1024, 1024), idV, 1);
+        const uint32_t ql = smem_u32(sm.qlo);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_L^T phi(Q)
+        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_L^T phi(Q): hi*hi + hi*lo + lo*hi
           mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(ql + k * 2048, 1024, 1024), idV, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
         mma_commit(sm.mma_bar);
       }
       if (!wait_uniform(sm.mma_bar, ph, hdr, 33)) break;
@@ -816,7 +866,7 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
       !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, st);
+  cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, true, st);
   if (e != cudaSuccess) return e;
   e = launch_scan(spartial, sprefix, g, causal ? kScanPrefix : kScanTotal, nullptr, nullptr, st);
   if (e != cudaSuccess) return e;

@@ -107,6 +107,33 @@ __device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, floa
   }
 }
 
+// phi on one tile row, split into a bf16 hi part (written in place) and the
+// bf16 of the remainder phi - hi (written at the same swizzled position of
+// `lo`), so hi + lo carries ~16 bits; rows >= nvalid become 0. z receives the
+// float32 values of phi (for column sums).
+__device__ __forceinline__ void phi_row_split(uint8_t* tile, uint8_t* lo, int row, int nvalid,
+                                              float (&z)[64]) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int lc = 0; lc < 8; ++lc) {
+    const uint32_t off = sw128(row, lc * 16);
+    uint4* p = reinterpret_cast<uint4*>(tile + off);
+    const uint4 w = *p;
+    uint32_t u[4] = {w.x, w.y, w.z, w.w}, l[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float a = valid ? phi_fast(bf16_lo_f(u[h])) : 0.f;
+      const float b = valid ? phi_fast(bf16_hi_f(u[h])) : 0.f;
+      u[h] = pack_bf16(a, b);
+      l[h] = pack_bf16(a - bf16_lo_f(u[h]), b - bf16_hi_f(u[h]));
+      z[lc * 8 + 2 * h] = a;
+      z[lc * 8 + 2 * h + 1] = b;
+    }
+    *p = make_uint4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
 // Sum z[64] over the 32 lanes of a warp; lane l ends with columns 2l, 2l+1.
 __device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
   const int lane = threadIdx.x & 31;
@@ -206,7 +233,8 @@ enum ScanMode { kScanPrefix = 0, kScanTotal = 1, kScanSuffix = 2 };
 
 // Segment increments dS^T = V^T phi(K), dZ = sum phi(K) into partial[item].
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st);
+                                  float* partial, WorkspaceHeader* hdr, bool precise,
+                                  cudaStream_t st);
 // Prefix / total / suffix of the per-segment states (see ScanMode).
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
                         float* Z_out, cudaStream_t st);

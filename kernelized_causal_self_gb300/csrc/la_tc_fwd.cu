@@ -30,16 +30,23 @@ namespace tcx {
 
 // ------------------------------------------------------- 1. segment states
 
-constexpr int kStateStages = 2;  // 3 CTAs per SM
-constexpr int kStateSmem = 1024 + kStateStages * 2 * kTile + 2048;
+constexpr int kStateStages = 2;  // 3 CTAs per SM (2 with the precise variant)
+template <bool PRECISE>
+constexpr int state_smem() {
+  return 1024 + kStateStages * 2 * kTile + (PRECISE ? kTile : 0) + 2048;
+}
 
-__global__ void __launch_bounds__(kThreadsTC, 3)
+// PRECISE: phi(K) enters the MMA as a bf16 hi + lo pair and dZ sums the
+// float32 phi values (used by the backward, whose dq needs phi(K) beyond bf16).
+template <bool PRECISE>
+__global__ void __launch_bounds__(kThreadsTC, PRECISE ? 2 : 3)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = sm;  // [stage][K tile | V tile]
-  uint8_t* misc = sm + kStateStages * 2 * kTile;
+  uint8_t* klo = sm + kStateStages * 2 * kTile;  // phi(K) lo part (PRECISE)
+  uint8_t* misc = klo + (PRECISE ? kTile : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // kStateStages
   uint64_t* mma_bar = full + kStateStages;                      // 1
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
@@ -97,7 +104,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       ok = false;
       break;
     }
-    phi_row<true>(kt, tid, nvalid, zacc);
+    if (PRECISE)
+      phi_row_split(kt, klo, tid, nvalid, zacc);
+    else
+      phi_row<true>(kt, tid, nvalid, zacc);
     float2 cs = warp_column_sums(zacc);
     dz[warp * 64 + 2 * lane] = cs.x;
     dz[warp * 64 + 2 * lane + 1] = cs.y;
@@ -106,12 +116,17 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     __syncthreads();
     fence_after_sync();
     if (tid == 0) {
-      const uint32_t va = smem_u32(vt), ka = smem_u32(kt);
+      const uint32_t va = smem_u32(vt), ka = smem_u32(kt), kl = smem_u32(klo);
       const uint32_t id = idesc_bf16(64, 64, true, true);
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
         mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024), id,
                (first && k == 0) ? 0u : 1u);
+      if (PRECISE) {
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024), id, 1);
+      }
       mma_commit(mma_bar);
     }
     if (warp == 0) {
@@ -525,13 +540,18 @@ Geometry make_geometry(int BH, int N) {
 }
 
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st) {
-  cudaError_t e = configure(tc_state_kernel, kStateSmem);
-  if (e != cudaSuccess) return e;
-  const int ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem) * sm_count());
-  tc_state_kernel<<<ctas, kThreadsTC, kStateSmem, st>>>(*tk, *tv, g, partial, hdr);
-  count_launches(1);
-  return cudaGetLastError();
+                                  float* partial, WorkspaceHeader* hdr, bool precise,
+                                  cudaStream_t st) {
+  auto run = [&](auto kern, int smem) {
+    cudaError_t e = configure(kern, smem);
+    if (e != cudaSuccess) return e;
+    const int ctas = min(g.n_items(), resident_ctas(kern, smem) * sm_count());
+    kern<<<ctas, kThreadsTC, smem, st>>>(*tk, *tv, g, partial, hdr);
+    count_launches(1);
+    return cudaGetLastError();
+  };
+  return precise ? run(tc_state_kernel<true>, state_smem<true>())
+                 : run(tc_state_kernel<false>, state_smem<false>());
 }
 
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
@@ -567,7 +587,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
       !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, st);
+  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
   if (e != cudaSuccess) return e;
   e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, S_out, Z_out, st);
   if (e != cudaSuccess) return e;
