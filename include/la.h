@@ -52,7 +52,8 @@ enum la_status {
   LA_ERR_INVALID_ARG = 1, /* null pointer, bad dimension, unsupported D/M, misaligned pointer */
   LA_ERR_WORKSPACE = 2,   /* workspace missing or smaller than the *_workspace_bytes() size */
   LA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-  LA_ERR_TIMEOUT = 4      /* a bounded cross-CTA wait expired (see la_workspace_status) */
+  LA_ERR_TIMEOUT = 4,     /* a bounded cross-CTA wait expired (see la_workspace_status) */
+  LA_ERR_TOO_LARGE = 5    /* the problem needs more scratch than la_forward_noalloc holds */
 };
 
 enum la_dtype { LA_F32 = 0, LA_BF16 = 1 };
@@ -139,6 +140,33 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout,
  */
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
                    int n_streams, int H, int D, int M, int dtype, void* stream);
+
+/*
+ * la_forward_noalloc -- la_forward for callers that cannot allocate device
+ * memory: code that only receives device pointers for its inputs and outputs
+ * from a host application or framework that owns the allocator (and exposes
+ * none to it), or that runs where a cudaMalloc is not permitted. The paper has
+ * no counterpart; this is a deployment variant of la_forward.
+ *
+ * Same arguments, layouts, results and status codes as la_forward, without
+ * the workspace: the scratch is a fixed array of LA_NOALLOC_SCRATCH_BYTES in
+ * the library's own device memory. Every GPU that loads the library holds
+ * that array until the process exits. Nothing is allocated or freed by this
+ * call (no cudaMalloc/cudaFree or allocating library routine).
+ *
+ * - The first call on each device looks up the array's device address with
+ *   that device current (the caller's current device must be the one its
+ *   pointers and stream belong to). Make that first call before any stream
+ *   capture.
+ * - Returns LA_ERR_TOO_LARGE, launching nothing, when the shape needs more
+ *   scratch than the array holds (la_forward_workspace_bytes() > capacity).
+ * - All calls share the one array and it keeps the previous call's contents
+ *   (each call clears what must start at zero). Calls that overlap on the GPU,
+ *   from any stream or host thread, race on it: serialise them.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
+                       int B, int H, int N, int D, int M, int causal, int dtype, void* stream);
 
 /*
  * la_workspace_status -- synchronises `stream` and reads the status word a

@@ -16,10 +16,11 @@ __all__ = [
     "la_workspace_status", "la_status_string", "la_kernel_launches", "library_path",
     "load_library",
     "LAError", "LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_WORKSPACE", "LA_ERR_CUDA",
-    "LA_ERR_TIMEOUT", "LA_F32", "LA_BF16",
+    "LA_ERR_TIMEOUT", "LA_ERR_TOO_LARGE", "LA_F32", "LA_BF16", "la_forward_noalloc",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+LA_ERR_TOO_LARGE = 5
 LA_F32, LA_BF16 = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +40,7 @@ _SIGNATURES = {
     "la_backward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
+    "la_forward_noalloc": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp]),
 }
 
 
@@ -140,6 +142,28 @@ def la_forward(q, k, v, causal=True, out=None, workspace=None):
                         int(bool(causal)), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
                         _stream_ptr(q.device))
     _check("la_forward", st)
+    return out
+
+
+def la_forward_noalloc(q, k, v, causal=True, out=None):
+    """la_forward without a workspace: the library's fixed device scratch array is used.
+
+    For callers that cannot allocate device memory. Calls that overlap on the
+    GPU share that array and race; the first call on a device must not be
+    made during stream capture.
+    """
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _need_cuda(out)
+    st = lib.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
+                                D, M, int(bool(causal)), dt, _stream_ptr(q.device))
+    _check("la_forward_noalloc", st)
     return out
 
 

@@ -62,6 +62,8 @@ const char* la_status_string(int status) {
     case LA_ERR_WORKSPACE: return "workspace missing or too small";
     case LA_ERR_CUDA: return "CUDA runtime error";
     case LA_ERR_TIMEOUT: return "a bounded cross-CTA wait expired; outputs are invalid";
+    case LA_ERR_TOO_LARGE:
+      return "problem needs more scratch than la_forward_noalloc's fixed array holds";
     default: return "unknown status";
   }
 }
