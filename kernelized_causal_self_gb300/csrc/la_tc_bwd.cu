@@ -51,20 +51,6 @@ __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint3
   lo = pack_bf16(a - bf16_lo_f(hi), b - bf16_hi_f(hi));
 }
 
-// Writes the float32 row `x` (64 values) as bf16 hi and lo rows of two
-// 128-byte-swizzled operand buffers.
-__device__ __forceinline__ void store_split_row(uint8_t* hi_buf, uint8_t* lo_buf, int row,
-                                                const float* x) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) split_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1], h[q], l[q]);
-    *reinterpret_cast<uint4*>(hi_buf + sw128(row, c * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_buf + sw128(row, c * 16)) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
 // 16 consecutive bf16 of row `row`, logical 16-byte chunks c0, c0+1 -> float.
 __device__ __forceinline__ void load_row16(const uint8_t* tile, int row, int c0, float* out) {
 #pragma unroll
@@ -114,6 +100,32 @@ struct BwdSmem {
 
 enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 
+// Both kernels run 256 threads: warp w covers TMEM lane quarter w % 4 (rows
+// 32 (w % 4) .. + 31) and half h = w / 4 of each row's columns, so every row is
+// handled by two threads. Where a TMEM region is compacted in place (fp32 P
+// into bf16 P_L), all reads finish before a barrier and the writes follow it.
+constexpr int kBT = 256;
+
+// Half-row store of x[32] (columns [32h, 32h + 32)) as bf16 hi and lo rows.
+__device__ __forceinline__ void store_split_half(uint8_t* hi_buf, uint8_t* lo_buf, int row, int h,
+                                                 const float* x) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t hh[4], ll[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) split_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1], hh[q], ll[q]);
+    const uint32_t off = sw128(row, (4 * h + c) * 16);
+    *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+    *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+  }
+}
+
+__device__ __forceinline__ void sync_tc() {
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+}
+
 // --------------------------------------------------- forward direction: dq
 
 // TMEM columns
@@ -125,8 +137,44 @@ constexpr uint32_t kFS = 320;   // 64: dS^T (M = 64 layout)
 constexpr uint32_t kFR = 384;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 constexpr uint32_t kFL = 448;   // 64: bf16 lo parts of P_L, then of T_L
 
+// Masked row slices sl of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs.
+// keep(j) decides which columns survive; `add` is added to kept values.
+template <bool LOWER>
+__device__ __forceinline__ void masked_split_slices(uint32_t taddr, int h, int q4, int row,
+                                                    float add, uint32_t (&hi)[2][16],
+                                                    uint32_t (&lo)[2][16], float& sum) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int sl = 2 * h + t;
+    // LOWER (query rows, keep j <= row): slices past the diagonal are all zero.
+    // upper (key rows, keep i >= row): slices before the diagonal are all zero.
+    const bool any = LOWER ? sl <= q4 : sl >= q4;
+    if (any) {
+      uint32_t r[32];
+      tmem_ld32(taddr + 32 * sl, r);
+      const bool diag = sl == q4;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int j0 = 32 * sl + 2 * c;
+        bool k0 = true, k1 = true;
+        if (diag) {
+          k0 = LOWER ? j0 <= row : j0 >= row;
+          k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
+        }
+        const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
+        const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
+        split_bf16(a, b, hi[t][c], lo[t][c]);
+        sum += a + b;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) hi[t][c] = lo[t][c] = 0u;
+    }
+  }
+}
+
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kBT, 1)
 tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                 Geometry g, const float* __restrict__ sprefix, float* __restrict__ rpartial,
@@ -134,10 +182,15 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   BwdSmem sm(smraw);
-  float* zsnap = sm.arr;          // 64: Z before the chunk (float32)
-  float* gds = sm.arr + 64;       // 128: gd per row
-  float* dz = sm.arr + 192;       // [4][64]: warp column sums
+  float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
+  float* dz = sm.arr + 64;       // [4][64]: warp column sums
+  float* rsum = sm.arr + 320;    // [2][128]: half-row sums of P_L
+  float* gout = sm.arr + 576;    // [2][128]: half-row G . out
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int q4 = warp & 3, h = warp >> 2;
+  const int row = q4 * 32 + lane;  // query row of this thread
+  const int srow = q4 * 16 + lane;  // state row (M = 64 layout), valid for lane < 16
+  const bool sthread = lane < 16;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -150,9 +203,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tmem_alloc(sm.tslot, 512);
     tmem_relinquish();
   }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  sync_tc();
   const uint32_t tbase = *sm.tslot;
   const uint32_t tl = lane_base(tbase);
 
@@ -177,27 +228,24 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float srun[64];
-  float zrun = 0.f, r0 = 0.f, r1 = 0.f;
-  const int srow = warp * 16 + lane;
-  const bool sthread = lane < 16;
+  float srun[32];             // S^T row srow, columns [32h, 32h + 32)
+  float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0;
-  float z[64];
+  float z[32];
 
   while (cc.valid(g)) {
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_begin(item);
     const bool last = cc.chunk + 1 == g.chunk_end(item);
     const int nvalid = min(kC, g.N - t0);
-    const int i = tid;  // query row of this thread
     if (tid == 0 && cp.valid(g)) issue(cp);
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
           const float4 x = s4[j];
           srun[4 * j] = x.x;
           srun[4 * j + 1] = x.y;
@@ -205,15 +253,17 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           srun[4 * j + 3] = x.w;
         }
       }
-      if (tid < kDim) zrun = src[kDim * kDim + tid];
-      r0 = r1 = 0.f;
+      if (tid < kDim) {
+        zrun = src[kDim * kDim + tid];
+        rr = 0.f;
+      }
     }
-    if ((CAUSAL || first) && sthread) store_split_row(sm.s_hi, sm.s_lo, srow, srun);
+    if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, srun);
     if (tid < kDim) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(zrun);
-      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(0, 2 * tid)) = h;
+      const __nv_bfloat16 hb = __float2bfloat16_rn(zrun);
+      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(0, 2 * tid)) = hb;
       *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(1, 2 * tid)) =
-          __float2bfloat16_rn(zrun - __bfloat162float(h));
+          __float2bfloat16_rn(zrun - __bfloat162float(hb));
       zsnap[tid] = zrun;
     }
     const int s = consumed % kBwdStages;
@@ -222,17 +272,13 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 21)) break;
-    phi_row_split(qt, sm.qlo, tid, kC, z);
+    phi_half_split(qt, sm.qlo, row, h, kC, z);
     if (CAUSAL) {
-      phi_row_split(kt, sm.klo, tid, nvalid, z);
-      const float2 cs = warp_column_sums(z);
-      dz[warp * 64 + 2 * lane] = cs.x;
-      dz[warp * 64 + 2 * lane + 1] = cs.y;
+      phi_half_split(kt, sm.klo, row, h, nvalid, z);
+      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
     }
     fence_proxy_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+    sync_tc();
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
       const uint32_t kl = smem_u32(sm.klo);
@@ -272,44 +318,27 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     ph ^= 1;
     fence_after_sync();
 
-    float rowsum = 0.f;
     if (CAUSAL) {
-#pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        uint32_t ph16[16], pl16[16];
-        if (sl <= warp) {
-          uint32_t r[32];
-          tmem_ld32(tl + kFP + 32 * sl, r);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int j0 = 32 * sl + 2 * c;
-            const float a = j0 <= i ? __uint_as_float(r[2 * c]) : 0.f;
-            const float b = j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f;
-            split_bf16(a, b, ph16[c], pl16[c]);
-            rowsum += a + b;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) ph16[c] = pl16[c] = 0u;
-        }
-        tmem_st16(tl + kFP + 16 * sl, ph16);
-        tmem_st16(tl + kFL + 16 * sl, pl16);
-      }
+      uint32_t phv[2][16], plv[2][16];
+      float part = 0.f;
+      masked_split_slices<true>(tl + kFP, h, q4, row, 0.f, phv, plv, part);
+      rsum[h * 128 + row] = part;
       {
         uint32_t r[32];
+        tmem_ld32(tl + kFS + 32 * h, r);
+        if (sthread) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tl + kFS + 32 * half, r);
-          if (sthread) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) srun[32 * half + j] += __uint_as_float(r[j]);
-          }
+          for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
         }
       }
       if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-      fence_before_sync();
-      __syncthreads();
-      fence_after_sync();
+      sync_tc();  // every read of fp32 P is done before P_L overwrites it
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        tmem_st16(tl + kFP + 16 * (2 * h + t), phv[t]);
+        tmem_st16(tl + kFL + 16 * (2 * h + t), plv[t]);
+      }
+      sync_tc();
       if (tid == 0) {
         const uint32_t va = smem_u32(vt);
         const uint32_t idPV = idesc_bf16(128, 64, false, true);
@@ -326,59 +355,49 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       fence_after_sync();
     }
 
-    // den, out, gN = G / den, gd = -(G . out) / den
-    float gd;
+    // den, out, gN = G / den (this half's columns), G . out (half), then gd
+    float gd, inv;
     {
       uint32_t oz[16];
       tmem_ld16(tl + kFOz, oz);
+      const float rowsum = CAUSAL ? rsum[row] + rsum[128 + row] : 0.f;
       const float den = rowsum + __uint_as_float(oz[0]) + __uint_as_float(oz[1]);
-      const float inv = 1.f / den;
-      float go = 0.f;
-      float gn[64];
+      inv = 1.f / den;
+      uint32_t r[32];
+      tmem_ld32(tl + kFO + 32 * h, r);
+      float go = 0.f, gn[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tl + kFO + 32 * half, r);
+      for (int c = 0; c < 2; ++c) {
+        float gv[16];
+        load_row16(gt, row, 4 * h + 2 * c, gv);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float gv[16];
-          load_row16(gt, i, half * 4 + 2 * c, gv);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float out = __uint_as_float(r[16 * c + q]) * inv;
-            go += gv[q] * out;
-            gn[32 * half + 16 * c + q] = gv[q] * inv;
-          }
+        for (int q = 0; q < 16; ++q) {
+          go += gv[q] * (__uint_as_float(r[16 * c + q]) * inv);
+          gn[16 * c + q] = gv[q] * inv;
         }
       }
-      gd = -go * inv;
-      store_split_row(sm.gn_hi, sm.gn_lo, i, gn);
-      gds[i] = gd;
-      if (i < nvalid) {
-        den_out[(size_t)bh * g.N + t0 + i] = den;
-        gd_out[(size_t)bh * g.N + t0 + i] = gd;
+      gout[h * 128 + row] = go;
+      store_split_half(sm.gn_hi, sm.gn_lo, row, h, gn);
+      fence_proxy_async_smem();
+      __syncthreads();
+      gd = -(gout[row] + gout[128 + row]) * inv;
+      if (h == 0 && row < nvalid) {
+        den_out[(size_t)bh * g.N + t0 + row] = den;
+        gd_out[(size_t)bh * g.N + t0 + row] = gd;
       }
-      // this chunk's share of r = sum_i gd_i phi(Q_i)
+      // this chunk's share of r = sum_i gd_i phi(Q_i) (float32 phi = hi + lo)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float qv[16], ql[16];
-        load_row16(qt, i, 2 * c, qv);
-        load_row16(sm.qlo, i, 2 * c, ql);
+        load_row16(qt, row, 4 * h + 2 * c, qv);
+        load_row16(sm.qlo, row, 4 * h + 2 * c, ql);
 #pragma unroll
         for (int q = 0; q < 16; ++q) z[16 * c + q] = gd * (qv[q] + ql[q]);
       }
-      const float2 cs = warp_column_sums(z);
-      dz[warp * 64 + 2 * lane] = cs.x;
-      dz[warp * 64 + 2 * lane + 1] = cs.y;
+      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
     }
-    fence_proxy_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (warp == 0) {
-      r0 += dz[2 * lane] + dz[64 + 2 * lane] + dz[128 + 2 * lane] + dz[192 + 2 * lane];
-      r1 += dz[2 * lane + 1] + dz[65 + 2 * lane] + dz[129 + 2 * lane] + dz[193 + 2 * lane];
-    }
+    sync_tc();
+    if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), va = smem_u32(vt), ql = smem_u32(sm.qlo);
       const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
@@ -403,7 +422,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, 1);
-      // segment sum of phi(Q)^T gN (hi + lo)
+      // segment sum of phi(Q)^T gN: hi*hi + hi*lo + lo*hi
       const uint32_t idR = idesc_bf16(64, 64, true, true);
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
@@ -424,28 +443,16 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     fence_after_sync();
 
     if (CAUSAL) {  // T_L = (T + gd_i) masked to j <= i, bf16 hi + lo, TMEM A operands
+      uint32_t thv[2][16], tlv[2][16];
+      float unused = 0.f;
+      masked_split_slices<true>(tl + kFP, h, q4, row, gd, thv, tlv, unused);
+      sync_tc();
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        uint32_t th[16], tlo[16];
-        if (sl <= warp) {
-          uint32_t r[32];
-          tmem_ld32(tl + kFP + 32 * sl, r);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int j0 = 32 * sl + 2 * c;
-            split_bf16(j0 <= i ? __uint_as_float(r[2 * c]) + gd : 0.f,
-                       j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) + gd : 0.f, th[c], tlo[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
-        }
-        tmem_st16(tl + kFP + 16 * sl, th);
-        tmem_st16(tl + kFL + 16 * sl, tlo);
+      for (int t = 0; t < 2; ++t) {
+        tmem_st16(tl + kFP + 16 * (2 * h + t), thv[t]);
+        tmem_st16(tl + kFL + 16 * (2 * h + t), tlv[t]);
       }
-      fence_before_sync();
-      __syncthreads();
-      fence_after_sync();
+      sync_tc();
       if (tid == 0) {
         const uint32_t ka = smem_u32(kt), kl = smem_u32(sm.klo);
         const uint32_t idTK = idesc_bf16(128, 64, false, true);
@@ -465,23 +472,22 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       fence_after_sync();
     }
 
-    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns
+    {
       uint32_t r[32];
-      tmem_ld32(tl + kFQ + 32 * half, r);
-      if (i < nvalid) {
-        float4* dst = reinterpret_cast<float4*>(dq + ((size_t)bh * g.N + t0 + i) * kDim + 32 * half);
+      tmem_ld32(tl + kFQ + 32 * h, r);
+      if (row < nvalid) {
+        float4* dst = reinterpret_cast<float4*>(dq + ((size_t)bh * g.N + t0 + row) * kDim + 32 * h);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float qv[16];
-          load_row16(qt, i, half * 4 + 2 * c, qv);
+          load_row16(qt, row, 4 * h + 2 * c, qv);
 #pragma unroll
           for (int q = 0; q < 16; q += 4) {
             float o[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int d = 32 * half + 16 * c + q + u;
+              const int d = 32 * h + 16 * c + q + u;
               o[u] = (__uint_as_float(r[16 * c + q + u]) + gd * zsnap[d]) * fminf(qv[q + u], 1.f);
             }
             dst[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
@@ -492,26 +498,18 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
       float* dst = rpartial + (size_t)item * kStateFloats;
+      uint32_t r[32];
+      tmem_ld32(tl + kFR + 32 * h, r);
+      if (sthread) {
+        float4* d4 = reinterpret_cast<float4*>(dst + srow * kDim + 32 * h);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tl + kFR + 32 * half, r);
-        if (sthread) {
-          float4* d4 = reinterpret_cast<float4*>(dst + srow * kDim + 32 * half);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
+        for (int j = 0; j < 8; ++j)
+          d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
-      if (warp == 0) {
-        dst[kDim * kDim + 2 * lane] = r0;
-        dst[kDim * kDim + 2 * lane + 1] = r1;
-      }
+      if (tid < kDim) dst[kDim * kDim + tid] = rr;
     }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+    sync_tc();
     ++consumed;
     cc.advance(g);
   }
@@ -522,9 +520,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ++consumed;
     }
   }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -538,7 +534,7 @@ constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
 constexpr uint32_t kRL = 448;   // 64: bf16 lo part of T_L^T
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kBT, 1)
 tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                  Geometry g, const float* __restrict__ rsuffix, const float* __restrict__ den_in,
@@ -552,6 +548,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   float* dens = sm.arr + 192;    // 128
   float* dz = sm.arr + 320;      // [4][64]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int q4 = warp & 3, h = warp >> 2;
+  const int row = q4 * 32 + lane;  // key row for the gradients, query row for gN
+  const int srow = q4 * 16 + lane;
+  const bool sthread = lane < 16;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -562,9 +562,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tmem_alloc(sm.tslot, 512);
     tmem_relinquish();
   }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  sync_tc();
   const uint32_t tbase = *sm.tslot;
   const uint32_t tl = lane_base(tbase);
 
@@ -589,26 +587,23 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float rrun[64];
+  float rrun[32];  // R row srow, columns [32h, 32h + 32)
   float rr = 0.f;  // r[d] for d = tid < 64
-  const int srow = warp * 16 + lane;
-  const bool sthread = lane < 16;
   long long consumed = 0;
   uint32_t ph = 0;
-  float z[64];
+  float z[32];
 
   while (cc.valid(g)) {
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
     const int nvalid = min(kC, g.N - t0);
-    const int j = tid;  // key row of this thread (also the query row it prepares)
     if (tid == 0 && cp.valid(g)) issue(cp);
     if (first) {
       const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 8; ++q) {
           const float4 x = s4[q];
           rrun[4 * q] = x.x;
           rrun[4 * q + 1] = x.y;
@@ -618,9 +613,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (tid < kDim) rr = src[kDim * kDim + tid];
     }
-    if ((CAUSAL || first) && sthread) store_split_row(sm.s_hi, sm.s_lo, srow, rrun);
+    if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, rrun);
     if (tid < kDim) rsnap[tid] = rr;
-    if (CAUSAL) {
+    if (CAUSAL && tid < kC) {
       const bool valid = tid < nvalid;
       dens[tid] = valid ? den_in[(size_t)bh * g.N + t0 + tid] : 1.f;
       gds[tid] = valid ? gd_in[(size_t)bh * g.N + t0 + tid] : 0.f;
@@ -631,34 +626,30 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 31)) break;
-    phi_row<false>(kt, tid, nvalid, z);
+    phi_half(kt, row, h, nvalid);
     if (CAUSAL) {
-      phi_row_split(qt, sm.qlo, tid, kC, z);
-      // gN row (query row = tid) and this chunk's share of r
-      const float inv = 1.f / dens[tid];
-      float gn[64];
+      phi_half_split(qt, sm.qlo, row, h, kC, z);
+      // gN (query row = row) for this half, and this chunk's share of r
+      const float inv = 1.f / dens[row];
+      const float gdr = gds[row];
+      float gn[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float gv[16];
-        load_row16(gt, tid, 2 * c, gv);
+        load_row16(gt, row, 4 * h + 2 * c, gv);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          gn[16 * c + q] = gv[q] * inv;
-          z[16 * c + q] *= gds[tid];
-        }
+        for (int q = 0; q < 16; ++q) gn[16 * c + q] = gv[q] * inv;
       }
-      store_split_row(sm.gn_hi, sm.gn_lo, tid, gn);
-      const float2 cs = warp_column_sums(z);
-      dz[warp * 64 + 2 * lane] = cs.x;
-      dz[warp * 64 + 2 * lane + 1] = cs.y;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) z[q] *= gdr;
+      store_split_half(sm.gn_hi, sm.gn_lo, row, h, gn);
+      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
     }
     fence_proxy_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+    sync_tc();
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
-      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo), ql = smem_u32(sm.qlo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
       if (CAUSAL) {
         const uint32_t idP = idesc_bf16(128, 128, false, false);
@@ -680,7 +671,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
                  idR, 1);
-        const uint32_t ql = smem_u32(sm.qlo);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase + kRR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
@@ -709,52 +699,49 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
 
     if (CAUSAL) {
-      // key row j keeps query columns i >= j
+      // key row keeps query columns i >= row
+      uint32_t pph[2][16], ppl[2][16], pth[2][16], ptl[2][16];
+      float unused = 0.f;
+      masked_split_slices<false>(tl + kRP, h, q4, row, 0.f, pph, ppl, unused);
+      // T^T + gd_i: gd depends on the column, so it is added here per column
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        uint32_t pp[16], pt[16], ptl[16];
-        if (sl >= warp) {
+      for (int t = 0; t < 2; ++t) {
+        const int sl = 2 * h + t;
+        if (sl >= q4) {
           uint32_t r[32];
-          tmem_ld32(tl + kRP + 32 * sl, r);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int i0 = 32 * sl + 2 * c;
-            pp[c] = pack_bf16(i0 >= j ? __uint_as_float(r[2 * c]) : 0.f,
-                              i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) : 0.f);
-          }
           tmem_ld32(tl + kRT + 32 * sl, r);
+          const bool diag = sl == q4;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int i0 = 32 * sl + 2 * c;
-            split_bf16(i0 >= j ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
-                       i0 + 1 >= j ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f, pt[c],
-                       ptl[c]);
+            const bool k0 = !diag || i0 >= row, k1 = !diag || i0 + 1 >= row;
+            split_bf16(k0 ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
+                       k1 ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f, pth[t][c], ptl[t][c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pp[c] = pt[c] = ptl[c] = 0u;
+          for (int c = 0; c < 16; ++c) pth[t][c] = ptl[t][c] = 0u;
         }
-        tmem_st16(tl + kRP + 16 * sl, pp);
-        tmem_st16(tl + kRT + 16 * sl, pt);
-        tmem_st16(tl + kRL + 16 * sl, ptl);
       }
       {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
         uint32_t r[32];
+        tmem_ld32(tl + kRR + 32 * h, r);
+        if (sthread) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tl + kRR + 32 * half, r);
-          if (sthread) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) rrun[32 * half + q] += __uint_as_float(r[q]);
-          }
+          for (int q = 0; q < 32; ++q) rrun[q] += __uint_as_float(r[q]);
         }
       }
       if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-      fence_before_sync();
-      __syncthreads();
-      fence_after_sync();
+      sync_tc();  // all reads of P^T, T^T done before the bf16 parts overwrite them
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        tmem_st16(tl + kRP + 16 * (2 * h + t), pph[t]);
+        tmem_st16(tl + kRT + 16 * (2 * h + t), pth[t]);
+        tmem_st16(tl + kRL + 16 * (2 * h + t), ptl[t]);
+      }
+      sync_tc();
       if (tid == 0) {
-        const uint32_t qa = smem_u32(qt);
+        const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
         const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
         const uint32_t idV = idesc_bf16(128, 64, false, true);
 #pragma unroll
@@ -763,7 +750,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gla + k * 2048, 1024, 1024), idV, 1);
-        const uint32_t ql = smem_u32(sm.qlo);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)  // dphiK += T_L^T phi(Q): hi*hi + hi*lo + lo*hi
           mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
@@ -780,27 +766,25 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
     }
 
-    // dk = (dphiK + r_next) * phi'(k), dv
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t r[32];
-      tmem_ld32(tl + kRK + 32 * half, r);
-      uint32_t w[32];
-      tmem_ld32(tl + kRV + 32 * half, w);
-      if (j < nvalid) {
-        const size_t row = (size_t)bh * g.N + t0 + j;
-        float4* dkp = reinterpret_cast<float4*>(dk + row * kDim + 32 * half);
-        float4* dvp = reinterpret_cast<float4*>(dv + row * kDim + 32 * half);
+    // dk = (dphiK + r_next) * phi'(k), dv; this half's columns
+    {
+      uint32_t r[32], w[32];
+      tmem_ld32(tl + kRK + 32 * h, r);
+      tmem_ld32(tl + kRV + 32 * h, w);
+      if (row < nvalid) {
+        const size_t grow = (size_t)bh * g.N + t0 + row;
+        float4* dkp = reinterpret_cast<float4*>(dk + grow * kDim + 32 * h);
+        float4* dvp = reinterpret_cast<float4*>(dv + grow * kDim + 32 * h);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float kv[16];
-          load_row16(kt, j, half * 4 + 2 * c, kv);
+          load_row16(kt, row, 4 * h + 2 * c, kv);
 #pragma unroll
           for (int q = 0; q < 16; q += 4) {
             float o[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int d = 32 * half + 16 * c + q + u;
+              const int d = 32 * h + 16 * c + q + u;
               o[u] = (__uint_as_float(r[16 * c + q + u]) + rsnap[d]) * fminf(kv[q + u], 1.f);
             }
             dkp[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
@@ -811,9 +795,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
       }
     }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+    sync_tc();
     ++consumed;
     cc.advance(g);
   }
@@ -824,9 +806,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ++consumed;
     }
   }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -875,8 +855,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   auto run_q = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem) * sms);
-    kern<<<ctas, kThreadsTC, kBwdSmem, st>>>(tq, tk, tv, tg, g, sprefix, rpartial, dq, den, gd, hdr);
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
+    kern<<<ctas, kBT, kBwdSmem, st>>>(tq, tk, tv, tg, g, sprefix, rpartial, dq, den, gd, hdr);
     count_launches(1);
     return cudaGetLastError();
   };
@@ -887,8 +867,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   auto run_kv = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem) * sms);
-    kern<<<ctas, kThreadsTC, kBwdSmem, st>>>(tq, tk, tv, tg, g, rsuffix, den, gd, dk, dv, hdr);
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
+    kern<<<ctas, kBT, kBwdSmem, st>>>(tq, tk, tv, tg, g, rsuffix, den, gd, dk, dv, hdr);
     count_launches(1);
     return cudaGetLastError();
   };

@@ -134,6 +134,62 @@ __device__ __forceinline__ void phi_row_split(uint8_t* tile, uint8_t* lo, int ro
   }
 }
 
+// Half-row variants for kernels where two warpgroups share each row: half h
+// owns the logical 16-byte chunks [4h, 4h + 4), i.e. columns [32h, 32h + 32).
+__device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nvalid) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, (4 * h + c) * 16));
+    const uint4 w = *p;
+    uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      u[q] = pack_bf16(valid ? phi_fast(bf16_lo_f(u[q])) : 0.f,
+                       valid ? phi_fast(bf16_hi_f(u[q])) : 0.f);
+    *p = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
+__device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int row, int h,
+                                               int nvalid, float (&z)[32]) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t off = sw128(row, (4 * h + c) * 16);
+    uint4* p = reinterpret_cast<uint4*>(tile + off);
+    const uint4 w = *p;
+    uint32_t u[4] = {w.x, w.y, w.z, w.w}, l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a = valid ? phi_fast(bf16_lo_f(u[q])) : 0.f;
+      const float b = valid ? phi_fast(bf16_hi_f(u[q])) : 0.f;
+      u[q] = pack_bf16(a, b);
+      l[q] = pack_bf16(a - bf16_lo_f(u[q]), b - bf16_hi_f(u[q]));
+      z[8 * c + 2 * q] = a;
+      z[8 * c + 2 * q + 1] = b;
+    }
+    *p = make_uint4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// Sum z[32] over the 32 lanes of a warp; lane l ends with column l.
+__device__ __forceinline__ float warp_column_sums32(float (&z)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = lane & w;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float mine = up ? z[w + j] : z[j];
+      const float other = up ? z[j] : z[w + j];
+      z[j] = mine + __shfl_xor_sync(0xffffffffu, other, w);
+    }
+  }
+  return z[0];
+}
+
 // Sum z[64] over the 32 lanes of a warp; lane l ends with columns 2l, 2l+1.
 __device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
   const int lane = threadIdx.x & 31;
@@ -203,9 +259,9 @@ inline cudaError_t configure(K kernel, int smem) {
 // occupancy answer and a count from the kernel's registers and shared memory
 // against the SM's register file and shared memory (1 KB reserved per CTA).
 template <typename K>
-inline int resident_ctas(K kernel, int smem) {
+inline int resident_ctas(K kernel, int smem, int threads = kThreadsTC) {
   int api = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api, kernel, kThreadsTC, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api, kernel, threads, smem) != cudaSuccess)
     api = 0;
   int dev = 0, smem_sm = 0, regs_sm = 0;
   cudaFuncAttributes fa;
@@ -217,7 +273,7 @@ inline int resident_ctas(K kernel, int smem) {
           cudaSuccess &&
       cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
     const int regs_warp = ((fa.numRegs + 7) / 8 * 8) * 32;
-    const int regs_cta = regs_warp * (kThreadsTC / 32);
+    const int regs_cta = regs_warp * (threads / 32);
     const int by_smem = smem_sm / (smem + (int)fa.sharedSizeBytes + 1024);
     const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
     manual = by_smem < by_regs ? by_smem : by_regs;
