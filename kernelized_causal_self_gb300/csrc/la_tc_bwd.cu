@@ -39,12 +39,11 @@ namespace {
 
 constexpr int kBwdStages = 2;
 constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows each
-constexpr int kZRows = 16 * 128;        // [Z_hi; Z_lo; 0 ...]
 constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
 constexpr int kArr = 4096;              // small float arrays
 constexpr int kLoB = 2 * kTile;         // phi(Q), phi(K) lo parts
 constexpr int kBwdSmem =
-    1024 + kBwdStages * 4 * kTile + kSnapB + kZRows + kGnB + kLoB + kArr + 2048;
+    1024 + kBwdStages * 4 * kTile + kSnapB + kGnB + kLoB + kArr + 2048;
 
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
@@ -69,7 +68,6 @@ struct BwdSmem {
   uint8_t* stages;
   uint8_t* s_hi;
   uint8_t* s_lo;
-  uint8_t* zrows;
   uint8_t* gn_hi;
   uint8_t* gn_lo;
   uint8_t* qlo;
@@ -84,8 +82,7 @@ struct BwdSmem {
     stages = sm;
     s_hi = sm + kBwdStages * 4 * kTile;
     s_lo = s_hi + kDim * 128;
-    zrows = s_lo + kDim * 128;
-    gn_hi = zrows + kZRows;
+    gn_hi = s_lo + kDim * 128;
     gn_lo = gn_hi + kTile;
     qlo = gn_lo + kTile;
     klo = qlo + kTile;
@@ -127,51 +124,23 @@ __device__ __forceinline__ void sync_tc() {
 }
 
 // --------------------------------------------------- forward direction: dq
+//
+// With W = G V^T (bf16 x bf16 products, exact in the float32 accumulator):
+//   den_i   = rowsum(P_L)_i + phi(Q_i) . Z_prev
+//   G.num_i = sum_j P_L,ij W_ij + G_i . (phi(Q_i) S_prev)
+//   gd_i    = -(G.num_i) / den_i^2,   gN_i = G_i / den_i
+//   T_ij    = W_ij / den_i + gd_i      (= (v_j - out_i) . gN_i, in float32)
+// so one epilogue after the first MMA group yields T_L, gN and gd, and the
+// second group accumulates dphiQ = T_L phi(K) + gN S_prev^T and the segment
+// sum of phi(Q)^T gN.
 
 // TMEM columns
-constexpr uint32_t kFP = 0;     // 128: P, then bf16 P_L in [0,64); then T, bf16 T_L in [0,64)
-constexpr uint32_t kFO = 128;   // 64: numerator
-constexpr uint32_t kFOz = 192;  // 16: phi(Q) . [Z_hi, Z_lo]
-constexpr uint32_t kFQ = 256;   // 64: dphiQ
+constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T
+constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
+constexpr uint32_t kFO = 256;   // 64: phi(Q) S_prev
 constexpr uint32_t kFS = 320;   // 64: dS^T (M = 64 layout)
-constexpr uint32_t kFR = 384;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
-constexpr uint32_t kFL = 448;   // 64: bf16 lo parts of P_L, then of T_L
-
-// Masked row slices sl of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs.
-// keep(j) decides which columns survive; `add` is added to kept values.
-template <bool LOWER>
-__device__ __forceinline__ void masked_split_slices(uint32_t taddr, int h, int q4, int row,
-                                                    float add, uint32_t (&hi)[2][16],
-                                                    uint32_t (&lo)[2][16], float& sum) {
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int sl = 2 * h + t;
-    // LOWER (query rows, keep j <= row): slices past the diagonal are all zero.
-    // upper (key rows, keep i >= row): slices before the diagonal are all zero.
-    const bool any = LOWER ? sl <= q4 : sl >= q4;
-    if (any) {
-      uint32_t r[32];
-      tmem_ld32(taddr + 32 * sl, r);
-      const bool diag = sl == q4;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int j0 = 32 * sl + 2 * c;
-        bool k0 = true, k1 = true;
-        if (diag) {
-          k0 = LOWER ? j0 <= row : j0 >= row;
-          k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
-        }
-        const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
-        const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
-        split_bf16(a, b, hi[t][c], lo[t][c]);
-        sum += a + b;
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) hi[t][c] = lo[t][c] = 0u;
-    }
-  }
-}
+constexpr uint32_t kFQ = 384;   // 64: dphiQ
+constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kBT, 1)
@@ -184,8 +153,8 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   BwdSmem sm(smraw);
   float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
   float* dz = sm.arr + 64;       // [4][64]: warp column sums
-  float* rsum = sm.arr + 320;    // [2][128]: half-row sums of P_L
-  float* gout = sm.arr + 576;    // [2][128]: half-row G . out
+  float* rsum = sm.arr + 320;    // [2][128]: half-row parts of den
+  float* gnum = sm.arr + 576;    // [2][128]: half-row parts of G . num
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
   const int row = q4 * 32 + lane;  // query row of this thread
@@ -197,8 +166,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(sm.mma_bar, 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < kZRows / 16; e += blockDim.x)
-    reinterpret_cast<uint4*>(sm.zrows)[e] = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     tmem_alloc(sm.tslot, 512);
     tmem_relinquish();
@@ -259,13 +226,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     }
     if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, srun);
-    if (tid < kDim) {
-      const __nv_bfloat16 hb = __float2bfloat16_rn(zrun);
-      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(0, 2 * tid)) = hb;
-      *reinterpret_cast<__nv_bfloat16*>(sm.zrows + sw128(1, 2 * tid)) =
-          __float2bfloat16_rn(zrun - __bfloat162float(hb));
-      zsnap[tid] = zrun;
-    }
+    if (tid < kDim) zsnap[tid] = zrun;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
     uint8_t* kt = sm.tile(s, kK);
@@ -280,17 +241,20 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     fence_proxy_async_smem();
     sync_tc();
     if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt), ga = smem_u32(gt);
       const uint32_t kl = smem_u32(sm.klo);
-      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo), za = smem_u32(sm.zrows);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
       if (CAUSAL) {
-        const uint32_t idP = idesc_bf16(128, 128, false, false);
+        const uint32_t id128 = idesc_bf16(128, 128, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // P = phi(Q) (phi(K)_hi + phi(K)_lo)^T
+          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), id128, k);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
+          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(kl + k * 32, 16, 1024), id128, 1);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(kl + k * 32, 16, 1024), idP, 1);
+        for (int k = 0; k < 4; ++k)  // W = G V^T
+          mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
         const uint32_t idS = idesc_bf16(64, 64, true, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
@@ -308,79 +272,81 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
-      const uint32_t idZ = idesc_bf16(128, 16, false, false);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
       mma_commit(sm.mma_bar);
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
     ph ^= 1;
     fence_after_sync();
 
-    if (CAUSAL) {
-      uint32_t phv[2][16], plv[2][16];
-      float part = 0.f;
-      masked_split_slices<true>(tl + kFP, h, q4, row, 0.f, phv, plv, part);
-      rsum[h * 128 + row] = part;
-      {
-        uint32_t r[32];
-        tmem_ld32(tl + kFS + 32 * h, r);
-        if (sthread) {
+    // ---- epilogue: den, G.num, then gd, gN and T_L
+    float wv[2][32];  // masked W of this thread's two slices (causal)
+    {
+      float dpart = 0.f, npart = 0.f;
+      if (CAUSAL) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
+        for (int t = 0; t < 2; ++t) {
+          const int sl = 2 * h + t;
+          if (sl <= q4) {
+            uint32_t rp[32], rw[32];
+            tmem_ld32(tl + kFP + 32 * sl, rp);
+            tmem_ld32(tl + kFW + 32 * sl, rw);
+            const bool diag = sl == q4;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const bool keep = !diag || 32 * sl + c <= row;
+              const float p = keep ? __uint_as_float(rp[c]) : 0.f;
+              wv[t][c] = keep ? __uint_as_float(rw[c]) : 0.f;
+              dpart += p;
+              npart += p * wv[t][c];
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) wv[t][c] = 0.f;
+          }
         }
       }
-      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-      sync_tc();  // every read of fp32 P is done before P_L overwrites it
+      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this half
+        uint32_t ro[32];
+        tmem_ld32(tl + kFO + 32 * h, ro);
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        tmem_st16(tl + kFP + 16 * (2 * h + t), phv[t]);
-        tmem_st16(tl + kFL + 16 * (2 * h + t), plv[t]);
+        for (int c = 0; c < 2; ++c) {
+          float gv[16], qv[16], ql[16];
+          load_row16(gt, row, 4 * h + 2 * c, gv);
+          load_row16(qt, row, 4 * h + 2 * c, qv);
+          load_row16(sm.qlo, row, 4 * h + 2 * c, ql);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            npart += gv[q] * __uint_as_float(ro[16 * c + q]);
+            dpart += (qv[q] + ql[q]) * zsnap[32 * h + 16 * c + q];
+          }
+        }
       }
-      sync_tc();
-      if (tid == 0) {
-        const uint32_t va = smem_u32(vt);
-        const uint32_t idPV = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFO, tbase + kFP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFO, tbase + kFL + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
-        mma_commit(sm.mma_bar);
-      }
-      if (!wait_uniform(sm.mma_bar, ph, hdr, 23)) break;
-      ph ^= 1;
-      fence_after_sync();
+      rsum[h * 128 + row] = dpart;
+      gnum[h * 128 + row] = npart;
     }
-
-    // den, out, gN = G / den (this half's columns), G . out (half), then gd
-    float gd, inv;
-    {
-      uint32_t oz[16];
-      tmem_ld16(tl + kFOz, oz);
-      const float rowsum = CAUSAL ? rsum[row] + rsum[128 + row] : 0.f;
-      const float den = rowsum + __uint_as_float(oz[0]) + __uint_as_float(oz[1]);
-      inv = 1.f / den;
+    if (CAUSAL) {
       uint32_t r[32];
-      tmem_ld32(tl + kFO + 32 * h, r);
-      float go = 0.f, gn[32];
+      tmem_ld32(tl + kFS + 32 * h, r);
+      if (sthread) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
+      }
+      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+    }
+    sync_tc();  // partials visible; every read of W is done
+    const float den = rsum[row] + rsum[128 + row];
+    const float inv = 1.f / den;
+    const float gd = -(gnum[row] + gnum[128 + row]) * inv * inv;
+    {
+      float gn[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float gv[16];
         load_row16(gt, row, 4 * h + 2 * c, gv);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          go += gv[q] * (__uint_as_float(r[16 * c + q]) * inv);
-          gn[16 * c + q] = gv[q] * inv;
-        }
+        for (int q = 0; q < 16; ++q) gn[16 * c + q] = gv[q] * inv;
       }
-      gout[h * 128 + row] = go;
       store_split_half(sm.gn_hi, sm.gn_lo, row, h, gn);
-      fence_proxy_async_smem();
-      __syncthreads();
-      gd = -(gout[row] + gout[128 + row]) * inv;
       if (h == 0 && row < nvalid) {
         den_out[(size_t)bh * g.N + t0 + row] = den;
         gd_out[(size_t)bh * g.N + t0 + row] = gd;
@@ -396,26 +362,49 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
     }
+    if (CAUSAL) {  // T_L = W / den + gd (j <= i), bf16 hi + lo over the spent W columns
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int sl = 2 * h + t;
+        uint32_t th[16], tlo[16];
+        const bool diag = sl == q4;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int j0 = 32 * sl + 2 * c;
+          const bool k0 = sl < q4 || (diag && j0 <= row);
+          const bool k1 = sl < q4 || (diag && j0 + 1 <= row);
+          split_bf16(k0 ? wv[t][2 * c] * inv + gd : 0.f, k1 ? wv[t][2 * c + 1] * inv + gd : 0.f,
+                     th[c], tlo[c]);
+        }
+        tmem_st16(tl + kFW + 16 * sl, th);
+        tmem_st16(tl + kFW + 64 + 16 * sl, tlo);
+      }
+    }
+    fence_proxy_async_smem();
     sync_tc();
     if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), va = smem_u32(vt), ql = smem_u32(sm.qlo);
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), ql = smem_u32(sm.qlo);
+      const uint32_t kl = smem_u32(sm.klo);
       const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
-      if (CAUSAL) {  // T = gN V^T (hi + lo)
-        const uint32_t idT = idesc_bf16(128, 128, false, false);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kFP, sdesc(gha + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), idT, k);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kFP, sdesc(gla + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), idT, 1);
-      }
-      // dphiQ = gN S_prev^T: B is the S^T snapshot read MN-major (rows m, d contiguous)
       const uint32_t idQ = idesc_bf16(128, 64, false, true);
+      if (CAUSAL) {  // dphiQ = T_L phi(K): hi*hi + hi*lo + lo*hi
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(kl + k * 2048, 1024, 1024), idQ, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ts(tbase + kFQ, tbase + kFW + 64 + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, 1);
+      }
+      // += gN S_prev^T: B is the S^T snapshot read MN-major (rows m, d contiguous)
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, k);
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ,
+               (CAUSAL || k > 0) ? 1u : 0u);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idQ, 1);
@@ -441,36 +430,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
     ph ^= 1;
     fence_after_sync();
-
-    if (CAUSAL) {  // T_L = (T + gd_i) masked to j <= i, bf16 hi + lo, TMEM A operands
-      uint32_t thv[2][16], tlv[2][16];
-      float unused = 0.f;
-      masked_split_slices<true>(tl + kFP, h, q4, row, gd, thv, tlv, unused);
-      sync_tc();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        tmem_st16(tl + kFP + 16 * (2 * h + t), thv[t]);
-        tmem_st16(tl + kFL + 16 * (2 * h + t), tlv[t]);
-      }
-      sync_tc();
-      if (tid == 0) {
-        const uint32_t ka = smem_u32(kt), kl = smem_u32(sm.klo);
-        const uint32_t idTK = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFQ, tbase + kFP + k * 8, sdesc(ka + k * 2048, 1024, 1024), idTK, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFQ, tbase + kFP + k * 8, sdesc(kl + k * 2048, 1024, 1024), idTK, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFQ, tbase + kFL + k * 8, sdesc(ka + k * 2048, 1024, 1024), idTK, 1);
-        mma_commit(sm.mma_bar);
-      }
-      if (!wait_uniform(sm.mma_bar, ph, hdr, 25)) break;
-      ph ^= 1;
-      fence_after_sync();
-    }
 
     // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns
     {
@@ -525,9 +484,48 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // --------------------------------------------------- reverse direction: dk, dv
+//
+// Key rows j on the TMEM lanes: P^T = phi(K) phi(Q)^T, W^T = V G^T, and
+// T^T_ji = W^T_ji / den_i + gd_i with den_i, gd_i saved by the forward-direction
+// kernel.
+
+// Masked row slices of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs for
+// this thread's half (slices 2h, 2h + 1). LOWER keeps j <= row (query rows),
+// otherwise i >= row (key rows).
+template <bool LOWER>
+__device__ __forceinline__ void masked_split_slices(uint32_t taddr, int h, int q4, int row,
+                                                    float add, uint32_t (&hi)[2][16],
+                                                    uint32_t (&lo)[2][16], float& sum) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int sl = 2 * h + t;
+    const bool any = LOWER ? sl <= q4 : sl >= q4;
+    if (any) {
+      uint32_t r[32];
+      tmem_ld32(taddr + 32 * sl, r);
+      const bool diag = sl == q4;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int j0 = 32 * sl + 2 * c;
+        bool k0 = true, k1 = true;
+        if (diag) {
+          k0 = LOWER ? j0 <= row : j0 >= row;
+          k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
+        }
+        const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
+        const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
+        split_bf16(a, b, hi[t][c], lo[t][c]);
+        sum += a + b;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) hi[t][c] = lo[t][c] = 0u;
+    }
+  }
+}
 
 constexpr uint32_t kRP = 0;     // 128: P^T (rows keys), then bf16 P_L^T in [0, 64)
-constexpr uint32_t kRT = 128;   // 128: T^T, then bf16 T_L^T in [128, 192)
+constexpr uint32_t kRT = 128;   // 128: W^T = V G^T, then bf16 T_L^T in [128, 192)
 constexpr uint32_t kRV = 256;   // 64: dV
 constexpr uint32_t kRK = 320;   // 64: dphiK
 constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
@@ -544,8 +542,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   BwdSmem sm(smraw);
   // the state snapshot buffers hold R rows d (m contiguous)
   float* rsnap = sm.arr;         // 64: r before the chunk
-  float* gds = sm.arr + 64;      // 128
-  float* dens = sm.arr + 192;    // 128
+  float* gds = sm.arr + 64;      // 128: gd_i
+  float* invs = sm.arr + 192;    // 128: 1 / den_i
   float* dz = sm.arr + 320;      // [4][64]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
@@ -592,12 +590,33 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   long long consumed = 0;
   uint32_t ph = 0;
   float z[32];
+  // den_i, gd_i of the chunk being processed, loaded one chunk ahead
+  float nden = 1.f, ngd = 0.f;
+  auto fetch_dg = [&](const RevCursor& c) {
+    if (CAUSAL && tid < kC && c.valid(g)) {
+      const int t = c.chunk * kC + tid;
+      const bool valid = t < g.N;
+      const size_t at = (size_t)g.bh_of(c.item) * g.N + t;
+      nden = valid ? den_in[at] : 1.f;
+      ngd = valid ? gd_in[at] : 0.f;
+    }
+  };
+  fetch_dg(cc);
 
   while (cc.valid(g)) {
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
     const int nvalid = min(kC, g.N - t0);
     if (tid == 0 && cp.valid(g)) issue(cp);
+    if (CAUSAL && tid < kC) {
+      invs[tid] = 1.f / nden;
+      gds[tid] = ngd;
+    }
+    {
+      RevCursor nx = cc;
+      nx.advance(g);
+      fetch_dg(nx);
+    }
     if (first) {
       const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (sthread) {
@@ -615,11 +634,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, rrun);
     if (tid < kDim) rsnap[tid] = rr;
-    if (CAUSAL && tid < kC) {
-      const bool valid = tid < nvalid;
-      dens[tid] = valid ? den_in[(size_t)bh * g.N + t0 + tid] : 1.f;
-      gds[tid] = valid ? gd_in[(size_t)bh * g.N + t0 + tid] : 0.f;
-    }
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
     uint8_t* kt = sm.tile(s, kK);
@@ -630,7 +644,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (CAUSAL) {
       phi_half_split(qt, sm.qlo, row, h, kC, z);
       // gN (query row = row) for this half, and this chunk's share of r
-      const float inv = 1.f / dens[row];
+      const float inv = invs[row];
       const float gdr = gds[row];
       float gn[32];
 #pragma unroll
@@ -656,12 +670,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // P^T = phi(K) phi(Q)^T
           mma_ss(tbase + kRP, sdesc(ka + k * 32, 16, 1024), sdesc(qa + k * 32, 16, 1024), idP, k);
+        const uint32_t ga = smem_u32(gt);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // T^T = V gN^T (hi + lo)
-          mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(gha + k * 32, 16, 1024), idP, k);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(gla + k * 32, 16, 1024), idP, 1);
+        for (int k = 0; k < 4; ++k)  // W^T = V G^T
+          mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(ga + k * 32, 16, 1024), idP, k);
         const uint32_t idR = idesc_bf16(64, 64, true, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
@@ -703,7 +715,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       uint32_t pph[2][16], ppl[2][16], pth[2][16], ptl[2][16];
       float unused = 0.f;
       masked_split_slices<false>(tl + kRP, h, q4, row, 0.f, pph, ppl, unused);
-      // T^T + gd_i: gd depends on the column, so it is added here per column
+      // T^T_ji = W^T_ji / den_i + gd_i (column-dependent scale and shift)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int sl = 2 * h + t;
@@ -715,8 +727,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 16; ++c) {
             const int i0 = 32 * sl + 2 * c;
             const bool k0 = !diag || i0 >= row, k1 = !diag || i0 + 1 >= row;
-            split_bf16(k0 ? __uint_as_float(r[2 * c]) + gds[i0] : 0.f,
-                       k1 ? __uint_as_float(r[2 * c + 1]) + gds[i0 + 1] : 0.f, pth[t][c], ptl[t][c]);
+            split_bf16(k0 ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
+                       k1 ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
+                       pth[t][c], ptl[t][c]);
           }
         } else {
 #pragma unroll
