@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/la.h"
+#include "la.h"
 
 namespace la {
 

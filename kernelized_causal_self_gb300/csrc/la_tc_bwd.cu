@@ -305,19 +305,20 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
-      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this half
+      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this half. The Z dot
+         // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
+         // the rounding of phi(Q) cancels in num / den.
         uint32_t ro[32];
         tmem_ld32(tl + kFO + 32 * h, ro);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float gv[16], qv[16], ql[16];
+          float gv[16], qv[16];
           load_row16(gt, row, 4 * h + 2 * c, gv);
           load_row16(qt, row, 4 * h + 2 * c, qv);
-          load_row16(sm.qlo, row, 4 * h + 2 * c, ql);
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             npart += gv[q] * __uint_as_float(ro[16 * c + q]);
-            dpart += (qv[q] + ql[q]) * zsnap[32 * h + 16 * c + q];
+            dpart += qv[q] * zsnap[32 * h + 16 * c + q];
           }
         }
       }
