@@ -75,6 +75,7 @@ struct BwdSmem {
   float* arr;
   uint64_t* full;
   uint64_t* mma_bar;
+  uint64_t* sbar;  // [2] completion of the state MMAs (dS, dR), each awaited later
   uint32_t* tslot;
   __device__ explicit BwdSmem(uint8_t* raw) {
     uint8_t* sm =
@@ -90,7 +91,8 @@ struct BwdSmem {
     uint8_t* misc = reinterpret_cast<uint8_t*>(arr) + kArr;
     full = reinterpret_cast<uint64_t*>(misc);
     mma_bar = full + kBwdStages;
-    tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+    sbar = mma_bar + 1;
+    tslot = reinterpret_cast<uint32_t*>(sbar + 2);
   }
   __device__ uint8_t* tile(int stage, int which) { return stages + (stage * 4 + which) * kTile; }
 };
@@ -115,6 +117,31 @@ __device__ __forceinline__ void store_split_half(uint8_t* hi_buf, uint8_t* lo_bu
     *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
     *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
   }
+}
+
+// Stores this thread's 32 floats (chunk row `row`, columns [32h, 32h + 32)) of
+// a [rows][64] float32 output. The warp passes its 32 half-rows through a
+// private 4 KB staging area (XOR-swizzled, conflict-free), so that each store
+// instruction writes four whole 128-byte row segments instead of 32 scattered
+// 16-byte pieces. `out_row0` points at column 32h of the chunk's row 0; rows
+// >= nvalid are not written.
+__device__ __forceinline__ void store_half_rows(float* out_row0, int row, int nvalid,
+                                                const float (&x)[32], float4* stage) {
+  const int lane = threadIdx.x & 31;
+  const int base = row - lane;  // first row of this warp
+#pragma unroll
+  for (int f = 0; f < 8; ++f)
+    stage[lane * 8 + (f ^ (lane & 7))] =
+        make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
+  __syncwarp();
+  const int f = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = 4 * k + (lane >> 3);
+    const float4 v = stage[r * 8 + (f ^ (r & 7))];
+    if (base + r < nvalid) reinterpret_cast<float4*>(out_row0 + (size_t)(base + r) * kDim)[f] = v;
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -164,6 +191,8 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
+    mbar_init(&sm.sbar[0], 1);
+    mbar_init(&sm.sbar[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -198,7 +227,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   float srun[32];             // S^T row srow, columns [32h, 32h + 32)
   float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
-  uint32_t ph = 0;
+  uint32_t ph = 0, sph0 = 0, sph1 = 0;
   float z[32];
 
   while (cc.valid(g)) {
@@ -255,15 +284,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // W = G V^T
           mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
-        const uint32_t idS = idesc_bf16(64, 64, true, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
-                 idS, k);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024),
-                 idS, 1);
       }
       const uint32_t idO = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -273,6 +293,18 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
       mma_commit(sm.mma_bar);
+      if (CAUSAL) {  // state increment, awaited only when the state is updated
+        const uint32_t idS = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
+                 idS, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024),
+                 idS, 1);
+        mma_commit(&sm.sbar[0]);
+      }
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
     ph ^= 1;
@@ -325,15 +357,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       rsum[h * 128 + row] = dpart;
       gnum[h * 128 + row] = npart;
     }
-    if (CAUSAL) {
-      uint32_t r[32];
-      tmem_ld32(tl + kFS + 32 * h, r);
-      if (sthread) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
-      }
-      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-    }
+    if (CAUSAL && tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     sync_tc();  // partials visible; every read of W is done
     const float den = rsum[row] + rsum[128 + row];
     const float inv = 1.f / den;
@@ -412,7 +436,8 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, 1);
-      // segment sum of phi(Q)^T gN: hi*hi + hi*lo + lo*hi
+      mma_commit(sm.mma_bar);
+      // segment sum of phi(Q)^T gN (hi*hi + hi*lo + lo*hi), awaited at the chunk's end
       const uint32_t idR = idesc_bf16(64, 64, true, true);
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
@@ -426,33 +451,44 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < kC / 16; ++k)
         mma_ss(tbase + kFR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
                1);
-      mma_commit(sm.mma_bar);
+      mma_commit(&sm.sbar[1]);
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
     ph ^= 1;
     fence_after_sync();
 
-    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns
+    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns,
+    // staged through the spent phi(K) tiles (warps 0-3: K tile, 4-7: its lo part)
     {
       uint32_t r[32];
       tmem_ld32(tl + kFQ + 32 * h, r);
-      if (row < nvalid) {
-        float4* dst = reinterpret_cast<float4*>(dq + ((size_t)bh * g.N + t0 + row) * kDim + 32 * h);
+      float o[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float qv[16];
-          load_row16(qt, row, 4 * h + 2 * c, qv);
+      for (int c = 0; c < 2; ++c) {
+        float qv[16];
+        load_row16(qt, row, 4 * h + 2 * c, qv);
 #pragma unroll
-          for (int q = 0; q < 16; q += 4) {
-            float o[4];
+        for (int q = 0; q < 16; ++q)
+          o[16 * c + q] =
+              (__uint_as_float(r[16 * c + q]) + gd * zsnap[32 * h + 16 * c + q]) * fminf(qv[q], 1.f);
+      }
+      float4* stage = reinterpret_cast<float4*>((h == 0 ? kt : sm.klo) + q4 * 4096);
+      store_half_rows(dq + ((size_t)bh * g.N + t0) * kDim + 32 * h, row, nvalid, o, stage);
+    }
+    // state MMAs of this chunk (dS from the first group, dR from the second)
+    if (CAUSAL) {
+      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27)) break;
+      sph0 ^= 1;
+    }
+    if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
+    sph1 ^= 1;
+    fence_after_sync();
+    if (CAUSAL) {
+      uint32_t r[32];
+      tmem_ld32(tl + kFS + 32 * h, r);
+      if (sthread) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int d = 32 * h + 16 * c + q + u;
-              o[u] = (__uint_as_float(r[16 * c + q + u]) + gd * zsnap[d]) * fminf(qv[q + u], 1.f);
-            }
-            dst[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
-          }
-        }
+        for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
       }
     }
 
@@ -555,6 +591,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
+    mbar_init(&sm.sbar[0], 1);
+    mbar_init(&sm.sbar[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -589,7 +627,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   float rrun[32];  // R row srow, columns [32h, 32h + 32)
   float rr = 0.f;  // r[d] for d = tid < 64
   long long consumed = 0;
-  uint32_t ph = 0;
+  uint32_t ph = 0, sph = 0;
   float z[32];
   // den_i, gd_i of the chunk being processed, loaded one chunk ahead
   float nden = 1.f, ngd = 0.f;
@@ -675,19 +713,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // W^T = V G^T
           mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(ga + k * 32, 16, 1024), idP, k);
-        const uint32_t idR = idesc_bf16(64, 64, true, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
-                 idR, k);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
-                 idR, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
-                 idR, 1);
       }
       // dV = phi(K) R_next: B = R rows d read MN-major (n = m contiguous)
       const uint32_t idVn = idesc_bf16(128, 64, false, true);
@@ -706,6 +731,22 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idKn, 1);
       mma_commit(sm.mma_bar);
+      if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated
+        const uint32_t idR = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+                 idR, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
+                 idR, 1);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+                 idR, 1);
+        mma_commit(&sm.sbar[1]);
+      }
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 32)) break;
     ph ^= 1;
@@ -737,15 +778,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 16; ++c) pth[t][c] = ptl[t][c] = 0u;
         }
       }
-      {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
-        uint32_t r[32];
-        tmem_ld32(tl + kRR + 32 * h, r);
-        if (sthread) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) rrun[q] += __uint_as_float(r[q]);
-        }
-      }
-      if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
       sync_tc();  // all reads of P^T, T^T done before the bf16 parts overwrite them
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -780,34 +812,40 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
     }
 
-    // dk = (dphiK + r_next) * phi'(k), dv; this half's columns
+    // dk = (dphiK + r_next) * phi'(k), dv; this half's columns, staged through the
+    // spent V / G tiles (warps 0-3 / 4-7)
     {
       uint32_t r[32], w[32];
       tmem_ld32(tl + kRK + 32 * h, r);
       tmem_ld32(tl + kRV + 32 * h, w);
-      if (row < nvalid) {
-        const size_t grow = (size_t)bh * g.N + t0 + row;
-        float4* dkp = reinterpret_cast<float4*>(dk + grow * kDim + 32 * h);
-        float4* dvp = reinterpret_cast<float4*>(dv + grow * kDim + 32 * h);
+      float o[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float kv[16];
-          load_row16(kt, row, 4 * h + 2 * c, kv);
+      for (int c = 0; c < 2; ++c) {
+        float kv[16];
+        load_row16(kt, row, 4 * h + 2 * c, kv);
 #pragma unroll
-          for (int q = 0; q < 16; q += 4) {
-            float o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int d = 32 * h + 16 * c + q + u;
-              o[u] = (__uint_as_float(r[16 * c + q + u]) + rsnap[d]) * fminf(kv[q + u], 1.f);
-            }
-            dkp[(16 * c + q) / 4] = make_float4(o[0], o[1], o[2], o[3]);
-            dvp[(16 * c + q) / 4] =
-                make_float4(__uint_as_float(w[16 * c + q]), __uint_as_float(w[16 * c + q + 1]),
-                            __uint_as_float(w[16 * c + q + 2]), __uint_as_float(w[16 * c + q + 3]));
-          }
-        }
+        for (int q = 0; q < 16; ++q)
+          o[16 * c + q] =
+              (__uint_as_float(r[16 * c + q]) + rsnap[32 * h + 16 * c + q]) * fminf(kv[q], 1.f);
       }
+      float4* stage = reinterpret_cast<float4*>((h == 0 ? vt : gt) + q4 * 4096);
+      const size_t off = ((size_t)bh * g.N + t0) * kDim + 32 * h;
+      store_half_rows(dk + off, row, nvalid, o, stage);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(w[q]);
+      store_half_rows(dv + off, row, nvalid, o, stage);
+    }
+    if (CAUSAL) {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
+      if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
+      sph ^= 1;
+      fence_after_sync();
+      uint32_t r[32];
+      tmem_ld32(tl + kRR + 32 * h, r);
+      if (sthread) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) rrun[q] += __uint_as_float(r[q]);
+      }
+      if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     }
     sync_tc();
     ++consumed;
