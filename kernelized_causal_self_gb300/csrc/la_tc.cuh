@@ -115,6 +115,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Blocks until the grid this launch depends on (the previous kernel in the
+// stream, launched with programmatic stream serialization) has completed and
+// its memory is visible. Returns at once when there is no such dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the dependent grid start launching (its own pdl_wait still waits for
+// this grid to complete).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulation.

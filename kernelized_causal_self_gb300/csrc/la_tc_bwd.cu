@@ -202,6 +202,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   sync_tc();
   const uint32_t tbase = *sm.tslot;
   const uint32_t tl = lane_base(tbase);
+  pdl_wait();
 
   const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
   Cursor cc, cp;
@@ -509,6 +510,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     ++consumed;
     cc.advance(g);
   }
+  pdl_trigger();
   if (tid == 0) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
@@ -602,6 +604,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   sync_tc();
   const uint32_t tbase = *sm.tslot;
   const uint32_t tl = lane_base(tbase);
+  pdl_wait();
 
   const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
   RevCursor cc, cp;
@@ -851,6 +854,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ++consumed;
     cc.advance(g);
   }
+  pdl_trigger();
   if (tid == 0) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
@@ -908,9 +912,10 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    kern<<<ctas, kBT, kBwdSmem, st>>>(tq, tk, tv, tg, g, sprefix, rpartial, dq, den, gd, hdr);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, g,
+                     (const float*)sprefix, rpartial, dq, den, gd, hdr);
     count_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
   };
   e = causal ? run_q(tc_bwd_q_kernel<true>) : run_q(tc_bwd_q_kernel<false>);
   if (e != cudaSuccess) return e;
@@ -920,9 +925,10 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    kern<<<ctas, kBT, kBwdSmem, st>>>(tq, tk, tv, tg, g, rsuffix, den, gd, dk, dv, hdr);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, g,
+                     (const float*)rsuffix, (const float*)den, (const float*)gd, dk, dv, hdr);
     count_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
   };
   return causal ? run_kv(tc_bwd_kv_kernel<true>) : run_kv(tc_bwd_kv_kernel<false>);
 }

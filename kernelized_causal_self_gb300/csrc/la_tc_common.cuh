@@ -285,6 +285,25 @@ inline int resident_ctas(K kernel, int smem, int threads = kThreadsTC) {
 int sm_count();
 Geometry make_geometry(int BH, int N);
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; every kernel launched this way
+// calls pdl_wait() before its first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 enum ScanMode { kScanPrefix = 0, kScanTotal = 1, kScanSuffix = 2 };
 
 // Segment increments dS^T = V^T phi(K), dZ = sum phi(K) into partial[item].

@@ -68,6 +68,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   __syncthreads();
   fence_after_sync();
   const uint32_t tbase = *tslot;
+  pdl_wait();
 
   Cursor cc, cp;
   cc.start(g);
@@ -170,6 +171,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     ++consumed;
     cc.advance(g);
   }
+  pdl_trigger();
   // drain: every issued load must land before the CTA exits
   if (tid == 0) {
     while (consumed < issued) {
@@ -199,6 +201,7 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
                   int mode, float* __restrict__ S_out, float* __restrict__ Z_out) {
   const int bh = blockIdx.y;
   const int e = blockIdx.x * kScanThreads + threadIdx.x;
+  pdl_wait();
   if (e >= kStateFloats) return;
   float run = 0.f;
   const bool rev = mode == kScanSuffix;
@@ -283,6 +286,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   fence_after_sync();
   const uint32_t tbase = *tslot;
   const uint32_t tl = lane_base(tbase);
+  pdl_wait();
 
   const uint32_t tx_bytes = CAUSAL ? 3 * kTile : kTile;
   Cursor cc, cp;
@@ -501,6 +505,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ++consumed;
     cc.advance(g);
   }
+  pdl_trigger();
   if (tid == 0) {
     while (consumed < issued) {  // loads still in flight after an early exit
       const int s = consumed % kAttStages;
@@ -546,9 +551,10 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
     cudaError_t e = configure(kern, smem);
     if (e != cudaSuccess) return e;
     const int ctas = min(g.n_items(), resident_ctas(kern, smem) * sm_count());
-    kern<<<ctas, kThreadsTC, smem, st>>>(*tk, *tv, g, partial, hdr);
+    cudaError_t err = launch_pdl(kern, dim3(ctas), dim3(kThreadsTC), smem, st, *tk, *tv, g, partial,
+                                 hdr);
     count_launches(1);
-    return cudaGetLastError();
+    return err != cudaSuccess ? err : cudaGetLastError();
   };
   return precise ? run(tc_state_kernel<true>, state_smem<true>())
                  : run(tc_state_kernel<false>, state_smem<false>());
@@ -557,9 +563,10 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
                         float* Z_out, cudaStream_t st) {
   const dim3 grid((kStateFloats + kScanThreads - 1) / kScanThreads, g.BH);
-  state_scan_kernel<<<grid, kScanThreads, 0, st>>>(partial, out, g.BH, g.n_seg, mode, S_out, Z_out);
+  cudaError_t e = launch_pdl(state_scan_kernel, grid, dim3(kScanThreads), 0, st, partial, out,
+                             g.BH, g.n_seg, mode, S_out, Z_out);
   count_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace tcx
@@ -598,12 +605,16 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
     e = configure(tc_attend_kernel<true>, kAttSmem);
     if (e != cudaSuccess) return e;
     const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem) * sms);
-    tc_attend_kernel<true><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
+    e = launch_pdl(tc_attend_kernel<true>, dim3(ctas), dim3(kThreadsTC), kAttSmem, st, tq, tk, tv,
+                   to, g, (const float*)prefix, hdr);
+    if (e != cudaSuccess) return e;
   } else {
     e = configure(tc_attend_kernel<false>, kAttSmem);
     if (e != cudaSuccess) return e;
     const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem) * sms);
-    tc_attend_kernel<false><<<ctas, kThreadsTC, kAttSmem, st>>>(tq, tk, tv, to, g, prefix, hdr);
+    e = launch_pdl(tc_attend_kernel<false>, dim3(ctas), dim3(kThreadsTC), kAttSmem, st, tq, tk, tv,
+                   to, g, (const float*)prefix, hdr);
+    if (e != cudaSuccess) return e;
   }
   count_launches(1);
   return cudaGetLastError();
