@@ -40,6 +40,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS)
 
 
+# DRAM bytes per call measured with ncu (profiles/dram_traffic_la_calls_b4h8n16384.md) and the
+# kernel-source revision they were taken on; reported only while the sources still match.
+TRAFFIC_REVISION = "762a58ef88e13b46"
+TRAFFIC_BYTES = {"la_backward": 1044.2e6, "la_forward": 396.0e6}
+
+
+def kernel_revision():
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "kernelized_causal_self_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "la.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 # Algorithmic bytes per token-head (bf16 inputs, float32 gradients).
 def fwd_bytes(w):
     return 2 * (2 * w.D + 2 * w.M)                     # q, k, v read + out written
@@ -364,8 +383,11 @@ def run_ours(args, world, rank, local):
     dom = max(cand, key=lambda n: cand[n][0])
     d_ms, d_bytes, per_unit = cand[dom]
     achieved = d_bytes / (d_ms * 1e-3) / 1e9
+    rev = kernel_revision()
+    traffic = TRAFFIC_BYTES.get(dom) if rev == TRAFFIC_REVISION else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "peak_source": peaks.get("source"),
+                "frac": achieved / hbm, "traffic": traffic, "kernel_revision": rev,
+                "peak_source": peaks.get("source"),
                 "algorithmic_bytes_per_token_head": per_unit, "token_heads_per_launch": th,
                 "launch_ms": d_ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms}
 
