@@ -82,6 +82,19 @@ __device__ __forceinline__ float phi_fast(float x) {
   return __expf(fminf(x, 0.f)) + fmaxf(x, 0.f);
 }
 
+// phi on two packed bf16 values: exp(min(x, 0)) + max(x, 0), with min, max and
+// the final add as bf16x2 operations and only the exponential in float32. The
+// add rounds once: for x > 0 it is the exact 1 + x rounded, for x <= 0 the
+// rounded exponential plus 0.
+__device__ __forceinline__ uint32_t phi2_bf16(uint32_t u) {
+  __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&u);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const float2 f = __bfloat1622float2(__hmin2(x, zero));
+  const __nv_bfloat162 e = __floats2bfloat162_rn(__expf(f.x), __expf(f.y));
+  __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // phi on one 128 x 64 bf16 tile row (row = tid), in place in the swizzled
 // layout; rows >= nvalid become 0. With KEEP the rounded values are also
 // returned in z[64] for the column sums.
@@ -95,9 +108,7 @@ __device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, floa
     uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      float a = valid ? phi_fast(bf16_lo_f(u[h])) : 0.f;
-      float b = valid ? phi_fast(bf16_hi_f(u[h])) : 0.f;
-      u[h] = pack_bf16(a, b);
+      u[h] = valid ? phi2_bf16(u[h]) : 0u;
       if (KEEP) {
         z[lc * 8 + 2 * h] = bf16_lo_f(u[h]);
         z[lc * 8 + 2 * h + 1] = bf16_hi_f(u[h]);
@@ -144,9 +155,7 @@ __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nval
     const uint4 w = *p;
     uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      u[q] = pack_bf16(valid ? phi_fast(bf16_lo_f(u[q])) : 0.f,
-                       valid ? phi_fast(bf16_hi_f(u[q])) : 0.f);
+    for (int q = 0; q < 4; ++q) u[q] = valid ? phi2_bf16(u[q]) : 0u;
     *p = make_uint4(u[0], u[1], u[2], u[3]);
   }
 }

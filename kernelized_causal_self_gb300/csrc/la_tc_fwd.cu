@@ -235,7 +235,9 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
 // --------------------------------------------------------- 3. chunk attention
 
 constexpr int kAttStages = 2;  // 2 CTAs per SM
-constexpr int kSnapBytes = kDim * 128 + 16 * 128;  // S^T rows (64), then [Z; 0 x 15] rows (16)
+// S^T rows (64), then [Z; 0 x 15] rows (16), then 16 rows of ones (the B operand
+// that turns P_L into its row sums on the tensor core)
+constexpr int kSnapBytes = kDim * 128 + 16 * 128 + 16 * 128;
 constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
 
 // TMEM columns (256 per CTA, two CTAs per SM)
@@ -256,6 +258,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t* snap = sm + kAttStages * 3 * kTile;
   uint8_t* s_hi = snap;
   uint8_t* zrow = snap + kDim * 128;
+  uint8_t* ones = zrow + 16 * 128;
   uint8_t* misc = snap + kSnapBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
   uint64_t* mma_bar = full + kAttStages;
@@ -274,9 +277,11 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       prefetch_tensormap(&tm_v);
     }
   }
-  // rows 1..15 of the [Z; 0...] operand stay zero
-  for (int e = tid; e < 16 * 128 / 16; e += blockDim.x)
+  // rows 1..15 of the [Z; 0...] operand stay zero; the ones operand is constant
+  for (int e = tid; e < 16 * 128 / 16; e += blockDim.x) {
     reinterpret_cast<uint4*>(zrow)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  }
   if (warp == 0) {
     tmem_alloc(tslot, kTmemCols);
     tmem_relinquish();
@@ -412,9 +417,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     mma_phase ^= 1;
     fence_after_sync();
 
-    float rowsum = 0.f;
     if (CAUSAL) {
-      // masked P row -> bf16, written back over the first 64 TMEM columns
+      // masked P row -> bf16, written back over the first 64 TMEM columns; its
+      // row sums (the intra-chunk part of den) come from an MMA with ones
       const int i = tid;  // query row within the chunk
 #pragma unroll
       for (int sl = 0; sl < 4; ++sl) {
@@ -422,13 +427,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (sl <= warp) {  // warp-uniform: slices past the diagonal are all zero
           uint32_t r[32];
           tmem_ld32(tl + kColP + 32 * sl, r);
+          if (sl < warp) {  // below the diagonal block: nothing is masked
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int j0 = 32 * sl + 2 * c;
-            const float a = j0 <= i ? __uint_as_float(r[2 * c]) : 0.f;
-            const float b = j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f;
-            pk[c] = pack_bf16(a, b);
-            rowsum += bf16_lo_f(pk[c]) + bf16_hi_f(pk[c]);
+            for (int c = 0; c < 16; ++c)
+              pk[c] = pack_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int j0 = 32 * sl + 2 * c;
+              pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) : 0.f,
+                                j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f);
+            }
           }
         } else {
 #pragma unroll
@@ -458,10 +467,15 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kColO, tbase + kColP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
+        // den = phi(Q) . Z_prev + rowsum(P_L): both land in the same column
         const uint32_t idZ = idesc_bf16(128, 16, false, false);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+        const uint32_t oa = smem_u32(ones);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)  // every ones row reads the same 2 KB buffer
+          mma_ts(tbase + kColOz, tbase + kColP + k * 8, sdesc(oa + (k % 4) * 32, 16, 1024), idZ, 1);
         mma_commit(mma_bar);
       }
       if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
@@ -476,7 +490,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     {
       uint32_t oz[16];
       tmem_ld16(tl + kColOz, oz);
-      const float den = rowsum + __uint_as_float(oz[0]);
+      const float den = __uint_as_float(oz[0]);
       const float inv = 1.f / den;
       uint32_t r[32];
 #pragma unroll
