@@ -33,7 +33,7 @@ namespace tcx {
 constexpr int kStateStages = 2;  // 3 CTAs per SM (2 with the precise variant)
 template <bool PRECISE>
 constexpr int state_smem() {
-  return 1024 + kStateStages * 2 * kTile + (PRECISE ? kTile : 0) + 2048;
+  return 1024 + kStateStages * 2 * kTile + (PRECISE ? kTile : 0) + 2048 + 2048;
 }
 
 // PRECISE: phi(K) enters the MMA as a bf16 hi + lo pair and dZ sums the
@@ -46,11 +46,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = sm;  // [stage][K tile | V tile]
   uint8_t* klo = sm + kStateStages * 2 * kTile;  // phi(K) lo part (PRECISE)
-  uint8_t* misc = klo + (PRECISE ? kTile : 0);
+  uint8_t* ones = klo + (PRECISE ? kTile : 0);   // 2 KB of bf16 ones (B operand of dZ)
+  uint8_t* misc = ones + 2048;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // kStateStages
   uint64_t* mma_bar = full + kStateStages;                      // 1
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
-  float* dz = reinterpret_cast<float*>(misc + 128);             // [4][64]
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (tid == 0) {
@@ -60,8 +60,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
+  for (int e = tid; e < 2048 / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();
   if (warp == 0) {
-    tmem_alloc(tslot, 64);
+    tmem_alloc(tslot, 128);  // [0, 64): dS^T, [64, 80): dZ (both M = 64 layout)
     tmem_relinquish();
   }
   fence_before_sync();
@@ -89,7 +92,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   bool ok = true;
   long long consumed = 0;
   uint32_t mma_phase = 0;
-  float zrun0 = 0.f, zrun1 = 0.f;  // this thread's share of dZ: columns 2*lane, 2*lane+1 (warp 0 only)
   float zacc[64];
   while (cc.valid(g) && ok) {
     const int item = cc.item;
@@ -108,10 +110,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (PRECISE)
       phi_row_split(kt, klo, tid, nvalid, zacc);
     else
-      phi_row<true>(kt, tid, nvalid, zacc);
-    float2 cs = warp_column_sums(zacc);
-    dz[warp * 64 + 2 * lane] = cs.x;
-    dz[warp * 64 + 2 * lane + 1] = cs.y;
+      phi_row<false>(kt, tid, nvalid, zacc);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -128,14 +127,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024), id, 1);
       }
+      // dZ[d] += sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
+      const uint32_t oa = smem_u32(ones);
+      const uint32_t idz = idesc_bf16(64, 16, true, false);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + 64, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024), idz,
+               (first && k == 0) ? 0u : 1u);
+      if (PRECISE) {
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + 64, sdesc(kl + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
+                 idz, 1);
+      }
       mma_commit(mma_bar);
-    }
-    if (warp == 0) {
-      const float a = dz[2 * lane] + dz[64 + 2 * lane] + dz[128 + 2 * lane] + dz[192 + 2 * lane];
-      const float b = dz[2 * lane + 1] + dz[64 + 2 * lane + 1] + dz[128 + 2 * lane + 1] +
-                      dz[192 + 2 * lane + 1];
-      zrun0 = first ? a : zrun0 + a;
-      zrun1 = first ? b : zrun1 + b;
     }
     // the tile stage and dz are reused only after the MMA has consumed them
     if (!wait_uniform(mma_bar, mma_phase, hdr, 2)) {
@@ -160,9 +165,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         }
       }
-      if (warp == 0) {
-        dst[kDim * kDim + 2 * lane] = zrun0;
-        dst[kDim * kDim + 2 * lane + 1] = zrun1;
+      {
+        uint32_t r16[16];
+        tmem_ld16(lane_base(tbase) + 64, r16);
+        if (lane < 16) dst[kDim * kDim + row] = __uint_as_float(r16[0]);
       }
       (void)bh;
     }
@@ -183,7 +189,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tbase, 64);
+  if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // ----------------------------------------------------------- 2. segment scan
@@ -242,7 +248,8 @@ constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
 
 // TMEM columns (256 per CTA, two CTAs per SM)
 constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T; then bf16 P in [0, 64)
-constexpr uint32_t kColOz = 64;   // 16: phi(Q) . Z_prev (in the dead half of P)
+constexpr uint32_t kColOz = 64;   // 16: den = phi(Q) . Z_prev + rowsum(P_L) (dead half of P)
+constexpr uint32_t kColZ = 80;    // 16: dZ = phi(K)^T 1 (M = 64 layout, dead half of P)
 constexpr uint32_t kColO = 128;   // 64: numerator
 constexpr uint32_t kColS = 192;   // 64: dS^T (M = 64 layout)
 constexpr uint32_t kTmemCols = 256;
@@ -314,8 +321,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  // running state: S^T row m (threads with lane < 16: m = 16 * warp + lane) and
-  // Z[d] (threads 0..63: d = tid)
+  // running state: S^T row m and Z[m] (threads with lane < 16: m = 16 * warp + lane)
   float srun[64];
   float zrun = 0.f;
   const int srow = warp * 16 + lane;
@@ -348,7 +354,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           srun[4 * j + 3] = x.w;
         }
       }
-      if (tid < kDim) zrun = src[kDim * kDim + tid];
+      if (sthread) zrun = src[kDim * kDim + srow];
     }
     const int s = consumed % kAttStages;
     uint8_t* qt = stages + s * 3 * kTile;
@@ -367,19 +373,14 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *reinterpret_cast<uint4*>(s_hi + sw128(srow, c * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
     }
-    if ((CAUSAL || first) && tid < kDim)
-      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * tid)) = __float2bfloat16_rn(zrun);
+    if ((CAUSAL || first) && sthread)
+      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * srow)) = __float2bfloat16_rn(zrun);
     if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
       ok = false;
       break;
     }
     phi_row<false>(qt, tid, kC, zacc);  // padded query rows are never stored
-    if (CAUSAL) {
-      phi_row<true>(kt, tid, nvalid, zacc);
-      const float2 cs = warp_column_sums(zacc);
-      dz[warp * 64 + 2 * lane] = cs.x;
-      dz[warp * 64 + 2 * lane + 1] = cs.y;
-    }
+    if (CAUSAL) phi_row<false>(kt, tid, nvalid, zacc);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -457,12 +458,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
         }
       }
-      if (tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
       fence_before_sync();
       __syncthreads();
       fence_after_sync();
       if (tid == 0) {
         const uint32_t va = smem_u32(vt), qa = smem_u32(qt), za = smem_u32(zrow);
+        const uint32_t ka = smem_u32(kt);
         const uint32_t idPV = idesc_bf16(128, 64, false, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
@@ -476,6 +477,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)  // every ones row reads the same 2 KB buffer
           mma_ts(tbase + kColOz, tbase + kColP + k * 8, sdesc(oa + (k % 4) * 32, 16, 1024), idZ, 1);
+        // dZ[d] = sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
+        const uint32_t idDZ = idesc_bf16(64, 16, true, false);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kColZ, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
+                 idDZ, k);
         mma_commit(mma_bar);
       }
       if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
@@ -486,6 +493,11 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
     }
 
+    if (CAUSAL) {  // Z += dZ (row srow of the M = 64 accumulator)
+      uint32_t r16[16];
+      tmem_ld16(tl + kColZ, r16);
+      if (sthread) zrun += __uint_as_float(r16[0]);
+    }
     // out = num / den -> bf16, staged in the Q slot (all MMAs reading it are done)
     {
       uint32_t oz[16];
