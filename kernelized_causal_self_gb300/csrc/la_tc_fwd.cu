@@ -30,7 +30,8 @@ namespace tcx {
 
 // ------------------------------------------------------- 1. segment states
 
-constexpr int kStateStages = 2;  // 3 CTAs per SM (2 with the precise variant)
+constexpr int kStateStages = 2;
+constexpr int kStateThreads = 256;  // two threads per tile row (column halves), 2 CTAs per SM
 template <bool PRECISE>
 constexpr int state_smem() {
   return 1024 + kStateStages * 2 * kTile + (PRECISE ? kTile : 0) + 2048 + 2048;
@@ -39,7 +40,7 @@ constexpr int state_smem() {
 // PRECISE: phi(K) enters the MMA as a bf16 hi + lo pair and dZ sums the
 // float32 phi values (used by the backward, whose dq needs phi(K) beyond bf16).
 template <bool PRECISE>
-__global__ void __launch_bounds__(kThreadsTC, PRECISE ? 2 : 3)
+__global__ void __launch_bounds__(kStateThreads, 2)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
@@ -53,6 +54,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int q4 = warp & 3, h = warp >> 2;
+  const int trow = q4 * 32 + lane;  // tile row of this thread (column half h)
   if (tid == 0) {
     for (int s = 0; s < kStateStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
@@ -92,7 +95,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   bool ok = true;
   long long consumed = 0;
   uint32_t mma_phase = 0;
-  float zacc[64];
+  float zacc[32];
   while (cc.valid(g) && ok) {
     const int item = cc.item;
     const int bh = g.bh_of(item);
@@ -108,9 +111,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       break;
     }
     if (PRECISE)
-      phi_row_split(kt, klo, tid, nvalid, zacc);
+      phi_half_split(kt, klo, trow, h, nvalid, zacc);
     else
-      phi_row<false>(kt, tid, nvalid, zacc);
+      phi_half(kt, trow, h, nvalid);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -151,24 +154,22 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     fence_after_sync();
     if (last) {
       float* dst = partial + (size_t)item * kStateFloats;
-      // M = 64 accumulator: row r sits in TMEM lane 32 * (r / 16) + r % 16
+      // M = 64 accumulator: row r sits in TMEM lane 32 * (r / 16) + r % 16;
+      // this thread writes columns [32h, 32h + 32) of row 16 * q4 + lane
       uint32_t r[32];
-      const int row = warp * 16 + lane;
+      const int row = q4 * 16 + lane;
+      tmem_ld32(lane_base(tbase) + h * 32, r);
+      if (lane < 16) {
+        float4* d4 = reinterpret_cast<float4*>(dst + row * kDim + h * 32);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(lane_base(tbase) + half * 32, r);
-        if (lane < 16) {
-          float4* d4 = reinterpret_cast<float4*>(dst + row * kDim + half * 32);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
+        for (int j = 0; j < 8; ++j)
+          d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       {
         uint32_t r16[16];
         tmem_ld16(lane_base(tbase) + 64, r16);
-        if (lane < 16) dst[kDim * kDim + row] = __uint_as_float(r16[0]);
+        if (lane < 16 && h == 0) dst[kDim * kDim + row] = __uint_as_float(r16[0]);
       }
       (void)bh;
     }
@@ -254,8 +255,14 @@ constexpr uint32_t kColO = 128;   // 64: numerator
 constexpr uint32_t kColS = 192;   // 64: dS^T (M = 64 layout)
 constexpr uint32_t kTmemCols = 256;
 
+// 256 threads: warp w covers TMEM lane quarter w % 4 (rows 32 (w % 4) .. + 31)
+// and half h = w / 4 of each row's columns, so every row is shared by two
+// threads; two CTAs per SM. P is compacted in place (fp32 to bf16): all reads
+// finish before a barrier, the writes follow it.
+constexpr int kAttThreads = 256;
+
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsTC, 2)
+__global__ void __launch_bounds__(kAttThreads, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  Geometry g, const float* __restrict__ prefix, WorkspaceHeader* hdr) {
@@ -270,9 +277,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
   uint64_t* mma_bar = full + kAttStages;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
-  float* dz = reinterpret_cast<float*>(misc + 128);  // [4][64]
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int q4 = warp & 3, h = warp >> 2;
+  const int row = q4 * 32 + lane;   // chunk row (query) of this thread
+  const int srow = q4 * 16 + lane;  // state row (M = 64 layout), valid for lane < 16
+  const bool sthread = lane < 16;
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
@@ -321,16 +331,13 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  // running state: S^T row m and Z[m] (threads with lane < 16: m = 16 * warp + lane)
-  float srun[64];
+  // running state: S^T row srow, columns [32h, 32h + 32), and Z[srow] (lane < 16)
+  float srun[32];
   float zrun = 0.f;
-  const int srow = warp * 16 + lane;
-  const bool sthread = lane < 16;
 
   bool ok = true;
   long long consumed = 0;
   uint32_t mma_phase = 0;
-  float zacc[64];
   while (cc.valid(g) && ok) {
     const int item = cc.item;
     const int bh = g.bh_of(item);
@@ -344,17 +351,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (first) {  // state before this segment
       const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim);
+        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
           const float4 x = s4[j];
           srun[4 * j] = x.x;
           srun[4 * j + 1] = x.y;
           srun[4 * j + 2] = x.z;
           srun[4 * j + 3] = x.w;
         }
+        zrun = src[kDim * kDim + srow];
       }
-      if (sthread) zrun = src[kDim * kDim + srow];
     }
     const int s = consumed % kAttStages;
     uint8_t* qt = stages + s * 3 * kTile;
@@ -366,21 +373,22 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // product phi(Q_i) . S[:, m] the rounding averages to ~2^-9 / sqrt(D).
     if ((CAUSAL || first) && sthread) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t hi[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) hi[h] = pack_bf16(srun[8 * c + 2 * h], srun[8 * c + 2 * h + 1]);
-        *reinterpret_cast<uint4*>(s_hi + sw128(srow, c * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        for (int q = 0; q < 4; ++q) hi[q] = pack_bf16(srun[8 * c + 2 * q], srun[8 * c + 2 * q + 1]);
+        *reinterpret_cast<uint4*>(s_hi + sw128(srow, (4 * h + c) * 16)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
+      if (h == 0)
+        *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * srow)) = __float2bfloat16_rn(zrun);
     }
-    if ((CAUSAL || first) && sthread)
-      *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * srow)) = __float2bfloat16_rn(zrun);
     if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
       ok = false;
       break;
     }
-    phi_row<false>(qt, tid, kC, zacc);  // padded query rows are never stored
-    if (CAUSAL) phi_row<false>(kt, tid, nvalid, zacc);
+    phi_half(qt, row, h, kC);  // padded query rows are never stored
+    if (CAUSAL) phi_half(kt, row, h, nvalid);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -421,43 +429,44 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (CAUSAL) {
       // masked P row -> bf16, written back over the first 64 TMEM columns; its
       // row sums (the intra-chunk part of den) come from an MMA with ones
-      const int i = tid;  // query row within the chunk
+      uint32_t pk[2][16];
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        uint32_t pk[16];
-        if (sl <= warp) {  // warp-uniform: slices past the diagonal are all zero
+      for (int t = 0; t < 2; ++t) {
+        const int sl = 2 * h + t;
+        if (sl <= q4) {  // warp-uniform: slices past the diagonal are all zero
           uint32_t r[32];
           tmem_ld32(tl + kColP + 32 * sl, r);
-          if (sl < warp) {  // below the diagonal block: nothing is masked
+          if (sl < q4) {  // below the diagonal block: nothing is masked
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              pk[c] = pack_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+              pk[t][c] = pack_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
           } else {
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int j0 = 32 * sl + 2 * c;
-              pk[c] = pack_bf16(j0 <= i ? __uint_as_float(r[2 * c]) : 0.f,
-                                j0 + 1 <= i ? __uint_as_float(r[2 * c + 1]) : 0.f);
+              pk[t][c] = pack_bf16(j0 <= row ? __uint_as_float(r[2 * c]) : 0.f,
+                                   j0 + 1 <= row ? __uint_as_float(r[2 * c + 1]) : 0.f);
             }
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+          for (int c = 0; c < 16; ++c) pk[t][c] = 0u;
         }
-        tmem_st16(tl + kColP + 16 * sl, pk);
       }
-      // state update: S^T += dS^T (rows of the M = 64 accumulator), Z += dZ
+      // state update: S^T += dS^T (this half's columns of row srow)
       {
         uint32_t r[32];
+        tmem_ld32(tl + kColS + 32 * h, r);
+        if (sthread) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tl + kColS + 32 * half, r);
-          if (sthread) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) srun[32 * half + j] += __uint_as_float(r[j]);
-          }
+          for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
         }
       }
+      fence_before_sync();
+      __syncthreads();  // every read of fp32 P is done before bf16 P overwrites it
+      fence_after_sync();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) tmem_st16(tl + kColP + 16 * (2 * h + t), pk[t]);
       fence_before_sync();
       __syncthreads();
       fence_after_sync();
@@ -491,33 +500,29 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       mma_phase ^= 1;
       fence_after_sync();
+      {  // Z += dZ (row srow of the M = 64 accumulator)
+        uint32_t r16[16];
+        tmem_ld16(tl + kColZ, r16);
+        if (sthread) zrun += __uint_as_float(r16[0]);
+      }
     }
 
-    if (CAUSAL) {  // Z += dZ (row srow of the M = 64 accumulator)
-      uint32_t r16[16];
-      tmem_ld16(tl + kColZ, r16);
-      if (sthread) zrun += __uint_as_float(r16[0]);
-    }
-    // out = num / den -> bf16, staged in the Q slot (all MMAs reading it are done)
+    // out = num / den -> bf16, this half's columns, staged in the Q slot (all
+    // MMAs reading it are done)
     {
       uint32_t oz[16];
       tmem_ld16(tl + kColOz, oz);
-      const float den = __uint_as_float(oz[0]);
-      const float inv = 1.f / den;
+      const float inv = 1.f / __uint_as_float(oz[0]);
       uint32_t r[32];
+      tmem_ld32(tl + kColO + 32 * h, r);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tl + kColO + 32 * half, r);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h)
-            o[h] = pack_bf16(__uint_as_float(r[8 * c + 2 * h]) * inv,
-                             __uint_as_float(r[8 * c + 2 * h + 1]) * inv);
-          *reinterpret_cast<uint4*>(qt + sw128(tid, (half * 4 + c) * 16)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        for (int q = 0; q < 4; ++q)
+          o[q] = pack_bf16(__uint_as_float(r[8 * c + 2 * q]) * inv,
+                           __uint_as_float(r[8 * c + 2 * q + 1]) * inv);
+        *reinterpret_cast<uint4*>(qt + sw128(row, (4 * h + c) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
     fence_proxy_async_smem();
@@ -576,9 +581,9 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
   auto run = [&](auto kern, int smem) {
     cudaError_t e = configure(kern, smem);
     if (e != cudaSuccess) return e;
-    const int ctas = min(g.n_items(), resident_ctas(kern, smem) * sm_count());
-    cudaError_t err = launch_pdl(kern, dim3(ctas), dim3(kThreadsTC), smem, st, *tk, *tv, g, partial,
-                                 hdr);
+    const int ctas = min(g.n_items(), resident_ctas(kern, smem, kStateThreads) * sm_count());
+    cudaError_t err = launch_pdl(kern, dim3(ctas), dim3(kStateThreads), smem, st, *tk, *tv, g,
+                                 partial, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
@@ -630,15 +635,17 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
   if (causal) {
     e = configure(tc_attend_kernel<true>, kAttSmem);
     if (e != cudaSuccess) return e;
-    const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem) * sms);
-    e = launch_pdl(tc_attend_kernel<true>, dim3(ctas), dim3(kThreadsTC), kAttSmem, st, tq, tk, tv,
+    const int ctas =
+        min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem, kAttThreads) * sms);
+    e = launch_pdl(tc_attend_kernel<true>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
                    to, g, (const float*)prefix, hdr);
     if (e != cudaSuccess) return e;
   } else {
     e = configure(tc_attend_kernel<false>, kAttSmem);
     if (e != cudaSuccess) return e;
-    const int ctas = min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem) * sms);
-    e = launch_pdl(tc_attend_kernel<false>, dim3(ctas), dim3(kThreadsTC), kAttSmem, st, tq, tk, tv,
+    const int ctas =
+        min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem, kAttThreads) * sms);
+    e = launch_pdl(tc_attend_kernel<false>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
                    to, g, (const float*)prefix, hdr);
     if (e != cudaSuccess) return e;
   }
