@@ -68,6 +68,43 @@ def test_forward_small(la, shape, dtype, causal):
     assert_close(got, want, dtype, "out")
 
 
+# Long causal sequences with few (batch, head) pairs: many chunks per segment
+# and many segments per sequence, ragged last chunks.
+LONG = [(1, 2, 41 * 128 + 17), (1, 1, 70 * 128 + 3), (2, 3, 33 * 128)]
+
+
+@pytest.mark.parametrize("shape", LONG, ids=lambda s: "b%dh%dn%d" % s)
+def test_forward_long_causal(la, shape):
+    B, H, N = shape
+    got, (q, k, v) = _fwd_case(la, 500 + N, B, H, N, 64, 64, inputs.BF16, True, 0.125)
+    assert_close(got, oracle.forward(q, k, v, True), "bf16", "out")
+
+
+def test_prefill_long_state(la):
+    B, H, N = 2, 2, 40 * 128 + 77
+    q, k, v = inputs.qkv(611, B, H, N, 64, 64, 0.125, inputs.BF16)
+    out, S, Z = la.la_prefill(_t(q, inputs.BF16), _t(k, inputs.BF16), _t(v, inputs.BF16))
+    torch.cuda.synchronize()
+    want, S_ref, Z_ref = oracle.prefill(q, k, v)
+    assert_close(out.float().cpu().numpy(), want, "bf16", "prefill out")
+    assert_close(S.cpu().numpy(), S_ref, "bf16", "S_N")
+    assert_close(Z.cpu().numpy(), Z_ref, "bf16", "Z_N")
+
+
+def test_forward_reuses_workspace(la):
+    """Two causal calls on one workspace: the second must not see the first's
+    segment states, and the status word stays LA_OK."""
+    B, H, N = 2, 4, 36 * 128 + 5
+    nbytes = la.la_forward_workspace_bytes(B, H, N, 64, 64, True, la.LA_BF16)
+    ws = torch.empty((nbytes,), dtype=torch.uint8, device=DEV)
+    for seed in (701, 702):
+        q, k, v = inputs.qkv(seed, B, H, N, 64, 64, 0.125, inputs.BF16)
+        out = la.la_forward(_t(q, inputs.BF16), _t(k, inputs.BF16), _t(v, inputs.BF16),
+                            causal=True, workspace=ws)
+        assert la.la_workspace_status(ws) == la.LA_OK
+        assert_close(out.float().cpu().numpy(), oracle.forward(q, k, v, True), "bf16", f"seed {seed}")
+
+
 def test_forward_constant_v(la):
     # out_i = c exactly for constant V (normalisation); bf16 output rounding only
     B, H, N, D, M = 2, 2, 517, 64, 64
