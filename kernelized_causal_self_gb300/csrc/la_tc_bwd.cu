@@ -682,7 +682,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 31)) break;
-    phi_half(kt, row, h, nvalid);
+    phi_half<true>(kt, row, h, nvalid);
     if (CAUSAL) {
       phi_half_split(qt, sm.qlo, row, h, kC, z);
       // gN (query row = row) for this half, and this chunk's share of r

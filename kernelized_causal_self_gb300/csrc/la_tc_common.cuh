@@ -82,11 +82,31 @@ __device__ __forceinline__ float phi_fast(float x) {
   return __expf(fminf(x, 0.f)) + fmaxf(x, 0.f);
 }
 
-// phi on two packed bf16 values: exp(min(x, 0)) + max(x, 0), with min, max and
-// the final add as bf16x2 operations and only the exponential in float32. The
-// add rounds once: for x > 0 it is the exact 1 + x rounded, for x <= 0 the
-// rounded exponential plus 0.
+// phi on two packed bf16 values, exp(min(x, 0)) + max(x, 0), in bf16x2
+// arithmetic throughout: t = min(x, 0) log2(e) as one fused multiply-add with
+// log2(e) split into two bf16 parts (t = m L_hi + bf16(m L_lo), rounded once),
+// the packed base-2 exponential of t, and the final add. Besides the rounding
+// of the result, the exponential carries the rounding of t: a relative error
+// of at most 2^-9 |t| ln 2 (below one bf16 ulp for |x| < 2).
 __device__ __forceinline__ uint32_t phi2_bf16(uint32_t u) {
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&u);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 l_hi = __float2bfloat162_rn(1.4453125f);           // bf16(log2 e)
+  const __nv_bfloat162 l_lo = __float2bfloat162_rn(-0.0026174591110366f);  // log2 e - l_hi
+  const __nv_bfloat162 m = __hmin2(x, zero);
+  const __nv_bfloat162 t = __hfma2(m, l_hi, __hmul2(m, l_lo));
+  const uint32_t tu = *reinterpret_cast<const uint32_t*>(&t);
+  uint32_t eu;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(eu) : "r"(tu));
+  const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162*>(&eu);
+  const __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// phi on two packed bf16 values with a float32 exponential (each result is
+// phi of the exact input, rounded once): the backward's variant, where dq and
+// dk cancel the constant part of phi and keep only what k and q add to it.
+__device__ __forceinline__ uint32_t phi2_bf16_exact(uint32_t u) {
   __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&u);
   const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
   const float2 f = __bfloat1622float2(__hmin2(x, zero));
@@ -95,58 +115,9 @@ __device__ __forceinline__ uint32_t phi2_bf16(uint32_t u) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// phi on one 128 x 64 bf16 tile row (row = tid), in place in the swizzled
-// layout; rows >= nvalid become 0. With KEEP the rounded values are also
-// returned in z[64] for the column sums.
-template <bool KEEP>
-__device__ __forceinline__ void phi_row(uint8_t* tile, int row, int nvalid, float (&z)[64]) {
-  const bool valid = row < nvalid;
-#pragma unroll
-  for (int lc = 0; lc < 8; ++lc) {
-    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, lc * 16));
-    uint4 w = *p;
-    uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      u[h] = valid ? phi2_bf16(u[h]) : 0u;
-      if (KEEP) {
-        z[lc * 8 + 2 * h] = bf16_lo_f(u[h]);
-        z[lc * 8 + 2 * h + 1] = bf16_hi_f(u[h]);
-      }
-    }
-    *p = make_uint4(u[0], u[1], u[2], u[3]);
-  }
-}
-
-// phi on one tile row, split into a bf16 hi part (written in place) and the
-// bf16 of the remainder phi - hi (written at the same swizzled position of
-// `lo`), so hi + lo carries ~16 bits; rows >= nvalid become 0. z receives the
-// float32 values of phi (for column sums).
-__device__ __forceinline__ void phi_row_split(uint8_t* tile, uint8_t* lo, int row, int nvalid,
-                                              float (&z)[64]) {
-  const bool valid = row < nvalid;
-#pragma unroll
-  for (int lc = 0; lc < 8; ++lc) {
-    const uint32_t off = sw128(row, lc * 16);
-    uint4* p = reinterpret_cast<uint4*>(tile + off);
-    const uint4 w = *p;
-    uint32_t u[4] = {w.x, w.y, w.z, w.w}, l[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float a = valid ? phi_fast(bf16_lo_f(u[h])) : 0.f;
-      const float b = valid ? phi_fast(bf16_hi_f(u[h])) : 0.f;
-      u[h] = pack_bf16(a, b);
-      l[h] = pack_bf16(a - bf16_lo_f(u[h]), b - bf16_hi_f(u[h]));
-      z[lc * 8 + 2 * h] = a;
-      z[lc * 8 + 2 * h + 1] = b;
-    }
-    *p = make_uint4(u[0], u[1], u[2], u[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
 // Half-row variants for kernels where two warpgroups share each row: half h
 // owns the logical 16-byte chunks [4h, 4h + 4), i.e. columns [32h, 32h + 32).
+template <bool EXACT = false>
 __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nvalid) {
   const bool valid = row < nvalid;
 #pragma unroll
@@ -155,7 +126,7 @@ __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nval
     const uint4 w = *p;
     uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) u[q] = valid ? phi2_bf16(u[q]) : 0u;
+    for (int q = 0; q < 4; ++q) u[q] = valid ? (EXACT ? phi2_bf16_exact(u[q]) : phi2_bf16(u[q])) : 0u;
     *p = make_uint4(u[0], u[1], u[2], u[3]);
   }
 }

@@ -113,7 +113,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (PRECISE)
       phi_half_split(kt, klo, trow, h, nvalid, zacc);
     else
-      phi_half(kt, trow, h, nvalid);
+      phi_half<true>(kt, trow, h, nvalid);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -387,8 +387,11 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ok = false;
       break;
     }
-    phi_half(qt, row, h, kC);  // padded query rows are never stored
-    if (CAUSAL) phi_half(kt, row, h, nvalid);
+    // phi(Q) with the packed-bf16 exponential: its rounding enters numerator and
+    // denominator alike and largely cancels in out = num / den; phi(K) exact, since
+    // the state sums phi(K) v^T over random-sign v (padded query rows are never stored)
+    phi_half(qt, row, h, kC);
+    if (CAUSAL) phi_half<true>(kt, row, h, nvalid);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
