@@ -321,8 +321,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int sl = 2 * h + t;
           if (sl <= q4) {
             uint32_t rp[32], rw[32];
-            tmem_ld32(tl + kFP + 32 * sl, rp);
-            tmem_ld32(tl + kFW + 32 * sl, rw);
+            tmem_ld32x2(tl + kFP + 32 * sl, rp, tl + kFW + 32 * sl, rw);
             const bool diag = sl == q4;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -819,8 +818,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // spent V / G tiles (warps 0-3 / 4-7)
     {
       uint32_t r[32], w[32];
-      tmem_ld32(tl + kRK + 32 * h, r);
-      tmem_ld32(tl + kRV + 32 * h, w);
+      tmem_ld32x2(tl + kRK + 32 * h, r, tl + kRV + 32 * h, w);
       float o[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {

@@ -120,28 +120,35 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     fence_after_sync();
     if (tid == 0) {
       const uint32_t va = smem_u32(vt), ka = smem_u32(kt), kl = smem_u32(klo);
-      const uint32_t id = idesc_bf16(64, 64, true, true);
-#pragma unroll
-      for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024), id,
-               (first && k == 0) ? 0u : 1u);
-      if (PRECISE) {
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024), id, 1);
-      }
-      // dZ[d] += sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
       const uint32_t oa = smem_u32(ones);
-      const uint32_t idz = idesc_bf16(64, 16, true, false);
-#pragma unroll
-      for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + 64, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024), idz,
-               (first && k == 0) ? 0u : 1u);
       if (PRECISE) {
+        // phi(K)^T hi and lo stacked as one M = 128 MN-major operand (its two
+        // 64-row halves are the hi and the lo tile, kl - ka bytes apart):
+        // dS = phi(K)^T V with rows d, hi parts in TMEM lanes 0-63 and lo parts
+        // in lanes 64-127, summed at the segment's end; dZ = phi(K)^T 1 alike.
+        const uint32_t lbo = kl - ka;
+        const uint32_t idS = idesc_bf16(128, 64, true, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + 64, sdesc(kl + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
-                 idz, 1);
+          mma_ss(tbase, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS,
+                 (first && k == 0) ? 0u : 1u);
+        const uint32_t idz = idesc_bf16(128, 16, true, false);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + 64, sdesc(ka + k * 2048, lbo, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
+                 idz, (first && k == 0) ? 0u : 1u);
+      } else {
+        const uint32_t id = idesc_bf16(64, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024), id,
+                 (first && k == 0) ? 0u : 1u);
+        // dZ[d] += sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
+        const uint32_t idz = idesc_bf16(64, 16, true, false);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + 64, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024), idz,
+                 (first && k == 0) ? 0u : 1u);
       }
       mma_commit(mma_bar);
     }
@@ -152,7 +159,42 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     mma_phase ^= 1;
     fence_after_sync();
-    if (last) {
+    if (PRECISE && last) {
+      // M = 128 accumulators: lane r holds row d = r % 64 of the hi (r < 64) or
+      // the lo (r >= 64) part. The lo halves go through the spent K / V tiles
+      // (16 KB + 256 B); the hi-half threads add them and write S^T [m][d], Z.
+      float* dst = partial + (size_t)item * kStateFloats;
+      uint32_t r[32], r16[16];
+      tmem_ld32(lane_base(tbase) + h * 32, r);
+      tmem_ld16(lane_base(tbase) + 64, r16);
+      float* xs = reinterpret_cast<float*>(kt);
+      float* zs = reinterpret_cast<float*>(vt);
+      const int d = 32 * (q4 & 1) + lane;
+      if (q4 >= 2) {
+        float4* x4 = reinterpret_cast<float4*>(xs + d * kDim + 32 * h);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          x4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        if (h == 0) zs[d] = __uint_as_float(r16[0]);
+      }
+      __syncthreads();
+      if (q4 < 2) {
+        const float4* x4 = reinterpret_cast<const float4*>(xs + d * kDim + 32 * h);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 lo = x4[j];
+          const int m = 32 * h + 4 * j;
+          dst[(m + 0) * kDim + d] = __uint_as_float(r[4 * j]) + lo.x;
+          dst[(m + 1) * kDim + d] = __uint_as_float(r[4 * j + 1]) + lo.y;
+          dst[(m + 2) * kDim + d] = __uint_as_float(r[4 * j + 2]) + lo.z;
+          dst[(m + 3) * kDim + d] = __uint_as_float(r[4 * j + 3]) + lo.w;
+        }
+        if (h == 0) dst[kDim * kDim + d] = __uint_as_float(r16[0]) + zs[d];
+      }
+      fence_proxy_async_smem();  // before TMA refills the tiles used here
+      (void)bh;
+    } else if (last) {
       float* dst = partial + (size_t)item * kStateFloats;
       // M = 64 accumulator: row r sits in TMEM lane 32 * (r / 16) + r % 16;
       // this thread writes columns [32h, 32h + 32) of row 16 * q4 + lane
@@ -513,11 +555,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // out = num / den -> bf16, this half's columns, staged in the Q slot (all
     // MMAs reading it are done)
     {
-      uint32_t oz[16];
-      tmem_ld16(tl + kColOz, oz);
+      uint32_t oz[16], r[32];
+      tmem_ld16_32(tl + kColOz, oz, tl + kColO + 32 * h, r);
       const float inv = 1.f / __uint_as_float(oz[0]);
-      uint32_t r[32];
-      tmem_ld32(tl + kColO + 32 * h, r);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[4];
