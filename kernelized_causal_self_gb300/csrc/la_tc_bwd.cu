@@ -437,19 +437,20 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, 1);
       mma_commit(sm.mma_bar);
-      // segment sum of phi(Q)^T gN (hi*hi + hi*lo + lo*hi), awaited at the chunk's end
-      const uint32_t idR = idesc_bf16(64, 64, true, true);
+      // segment sum of phi(Q)^T gN, awaited at the chunk's end: phi(Q)^T hi and
+      // lo stacked as one M = 128 MN-major operand (the two 64-row halves are
+      // the hi and lo tiles, ql - qa bytes apart), times gN hi, then gN lo; the
+      // hi-row and lo-row halves (TMEM lanes 0-63 / 64-127) are summed at the
+      // segment's end
+      const uint32_t idR = idesc_bf16(128, 64, true, true);
+      const uint32_t lbo = ql - qa;
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
                (first && k == 0) ? 0u : 1u);
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
-               1);
-#pragma unroll
-      for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
                1);
       mma_commit(&sm.sbar[1]);
     }
@@ -493,17 +494,33 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
+      // lane 32 q4 + lane holds row d = 32 (q4 % 2) + lane: hi part for q4 < 2, lo
+      // part for q4 >= 2; the lo parts pass through the spent gN hi buffer
       float* dst = rpartial + (size_t)item * kStateFloats;
       uint32_t r[32];
       tmem_ld32(tl + kFR + 32 * h, r);
-      if (sthread) {
-        float4* d4 = reinterpret_cast<float4*>(dst + srow * kDim + 32 * h);
+      float* xs = reinterpret_cast<float*>(sm.gn_hi);
+      const int d = 32 * (q4 & 1) + lane;
+      if (q4 >= 2) {
+        float4* x4 = reinterpret_cast<float4*>(xs + d * kDim + 32 * h);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+          x4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
+      __syncthreads();
+      if (q4 < 2) {
+        const float4* x4 = reinterpret_cast<const float4*>(xs + d * kDim + 32 * h);
+        float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 32 * h);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 lo = x4[j];
+          d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
+                              __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
+        }
+      }
       if (tid < kDim) dst[kDim * kDim + tid] = rr;
+      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
     }
     sync_tc();
     ++consumed;
