@@ -499,22 +499,21 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float* dst = rpartial + (size_t)item * kStateFloats;
       uint32_t r[32];
       tmem_ld32(tl + kFR + 32 * h, r);
-      float* xs = reinterpret_cast<float*>(sm.gn_hi);
+      float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
       const int d = 32 * (q4 & 1) + lane;
       if (q4 >= 2) {
-        float4* x4 = reinterpret_cast<float4*>(xs + d * kDim + 32 * h);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          x4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       __syncthreads();
       if (q4 < 2) {
-        const float4* x4 = reinterpret_cast<const float4*>(xs + d * kDim + 32 * h);
         float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 32 * h);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float4 lo = x4[j];
+          const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
           d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
                               __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
         }
@@ -603,8 +602,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
   const int row = q4 * 32 + lane;  // key row for the gradients, query row for gN
-  const int srow = q4 * 16 + lane;
-  const bool sthread = lane < 16;
+  // R carry: row d = 32 (q4 % 2) + lane, held by the threads of TMEM lanes 0-63
+  const int drow = 32 * (q4 & 1) + lane;
+  const bool dthread = q4 < 2;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -643,7 +643,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float rrun[32];  // R row srow, columns [32h, 32h + 32)
+  float rrun[32];  // R row drow, columns [32h, 32h + 32) (dthread)
   float rr = 0.f;  // r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0, sph = 0;
@@ -677,8 +677,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     if (first) {
       const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
+      if (dthread) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + drow * kDim + 32 * h);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float4 x = s4[q];
@@ -690,7 +690,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (tid < kDim) rr = src[kDim * kDim + tid];
     }
-    if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, rrun);
+    if ((CAUSAL || first) && dthread) store_split_half(sm.s_hi, sm.s_lo, drow, h, rrun);
     if (tid < kDim) rsnap[tid] = rr;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
@@ -750,19 +750,19 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idKn, 1);
       mma_commit(sm.mma_bar);
-      if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated
-        const uint32_t idR = idesc_bf16(64, 64, true, true);
+      if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated:
+        // phi(Q)^T hi and lo stacked as one M = 128 MN-major operand (ql - qa
+        // bytes apart) times gN hi, then gN lo; rows d of the hi part in TMEM
+        // lanes 0-63, of the lo part in lanes 64-127
+        const uint32_t idR = idesc_bf16(128, 64, true, true);
+        const uint32_t lbo = ql - qa;
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024),
                  idR, k);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, 1024, 1024), sdesc(gla + k * 2048, 1024, 1024),
-                 idR, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(ql + k * 2048, 1024, 1024), sdesc(gha + k * 2048, 1024, 1024),
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024),
                  idR, 1);
         mma_commit(&sm.sbar[1]);
       }
@@ -859,10 +859,27 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
       uint32_t r[32];
       tmem_ld32(tl + kRR + 32 * h, r);
-      if (sthread) {
+      // the lo-part rows (lanes 64-127) pass through the spent gN hi buffer
+      float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
+      if (!dthread) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) rrun[q] += __uint_as_float(r[q]);
+        for (int j = 0; j < 8; ++j)
+          xs[drow * 16 + ((8 * h + j) ^ (drow & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
+      __syncthreads();
+      if (dthread) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 lo = xs[drow * 16 + ((8 * h + j) ^ (drow & 15))];
+          rrun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
+          rrun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
+          rrun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
+          rrun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+        }
+      }
+      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
       if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     }
     sync_tc();

@@ -167,23 +167,22 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       uint32_t r[32], r16[16];
       tmem_ld32(lane_base(tbase) + h * 32, r);
       tmem_ld16(lane_base(tbase) + 64, r16);
-      float* xs = reinterpret_cast<float*>(kt);
+      float4* xs = reinterpret_cast<float4*>(kt);  // [64][16] float4, XOR-swizzled rows
       float* zs = reinterpret_cast<float*>(vt);
       const int d = 32 * (q4 & 1) + lane;
       if (q4 >= 2) {
-        float4* x4 = reinterpret_cast<float4*>(xs + d * kDim + 32 * h);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          x4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         if (h == 0) zs[d] = __uint_as_float(r16[0]);
       }
       __syncthreads();
       if (q4 < 2) {
-        const float4* x4 = reinterpret_cast<const float4*>(xs + d * kDim + 32 * h);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float4 lo = x4[j];
+          const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
           const int m = 32 * h + 4 * j;
           dst[(m + 0) * kDim + d] = __uint_as_float(r[4 * j]) + lo.x;
           dst[(m + 1) * kDim + d] = __uint_as_float(r[4 * j + 1]) + lo.y;
