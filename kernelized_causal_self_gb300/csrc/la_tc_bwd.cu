@@ -75,7 +75,7 @@ struct BwdSmem {
   float* arr;
   uint64_t* full;
   uint64_t* mma_bar;
-  uint64_t* sbar;  // [2] completion of the state MMAs (dS, dR), each awaited later
+  uint64_t* sbar;  // sbar[1]: the deferred state MMAs (and all the issuer issued before them)
   uint32_t* tslot;
   __device__ explicit BwdSmem(uint8_t* raw) {
     uint8_t* sm =
@@ -165,7 +165,7 @@ __device__ __forceinline__ void sync_tc() {
 constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T
 constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
 constexpr uint32_t kFO = 256;   // 64: phi(Q) S_prev
-constexpr uint32_t kFS = 320;   // 64: dS^T (M = 64 layout)
+constexpr uint32_t kFS = 320;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
 constexpr uint32_t kFQ = 384;   // 64: dphiQ
 constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
@@ -185,13 +185,13 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
   const int row = q4 * 32 + lane;  // query row of this thread
-  const int srow = q4 * 16 + lane;  // state row (M = 64 layout), valid for lane < 16
-  const bool sthread = lane < 16;
+  // S carry: row d = 32 (q4 % 2) + lane, held by the threads of TMEM lanes 0-63
+  const int drow = 32 * (q4 & 1) + lane;
+  const bool dthread = q4 < 2;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
-    mbar_init(&sm.sbar[0], 1);
     mbar_init(&sm.sbar[1], 1);
     fence_mbar_init();
   }
@@ -225,10 +225,10 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float srun[32];             // S^T row srow, columns [32h, 32h + 32)
+  float srun[32];             // S row drow, columns m in [32h, 32h + 32) (dthread)
   float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
-  uint32_t ph = 0, sph0 = 0, sph1 = 0;
+  uint32_t ph = 0, sph1 = 0;
   float z[32];
 
   while (cc.valid(g)) {
@@ -239,23 +239,16 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0 && cp.valid(g)) issue(cp);
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
+      if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this half
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 x = s4[j];
-          srun[4 * j] = x.x;
-          srun[4 * j + 1] = x.y;
-          srun[4 * j + 2] = x.z;
-          srun[4 * j + 3] = x.w;
-        }
+        for (int j = 0; j < 32; ++j) srun[j] = src[(32 * h + j) * kDim + drow];
       }
       if (tid < kDim) {
         zrun = src[kDim * kDim + tid];
         rr = 0.f;
       }
     }
-    if ((CAUSAL || first) && sthread) store_split_half(sm.s_hi, sm.s_lo, srow, h, srun);
+    if ((CAUSAL || first) && dthread) store_split_half(sm.s_hi, sm.s_lo, drow, h, srun);
     if (tid < kDim) zsnap[tid] = zrun;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
@@ -286,25 +279,23 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int k = 0; k < 4; ++k)  // W = G V^T
           mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
       }
-      const uint32_t idO = idesc_bf16(128, 64, false, false);
+      // phi(Q) S_prev: B = the snapshot, rows d (= K), m contiguous (MN-major)
+      const uint32_t idO = idesc_bf16(128, 64, false, true);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idO, k);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idO, 1);
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idO, 1);
       mma_commit(sm.mma_bar);
-      if (CAUSAL) {  // state increment, awaited only when the state is updated
-        const uint32_t idS = idesc_bf16(64, 64, true, true);
+      if (CAUSAL) {  // state increment, complete when the second group's barrier is:
+        // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
+        // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
+        const uint32_t idS = idesc_bf16(128, 64, true, true);
+        const uint32_t lbo = kl - ka;
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
-                 idS, k);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(va + k * 2048, 1024, 1024), sdesc(kl + k * 2048, 1024, 1024),
-                 idS, 1);
-        mma_commit(&sm.sbar[0]);
+          mma_ss(tbase + kFS, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS, k);
       }
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
@@ -425,17 +416,18 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int k = 0; k < kC / 16; ++k)
           mma_ts(tbase + kFQ, tbase + kFW + 64 + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, 1);
       }
-      // += gN S_prev^T: B is the S^T snapshot read MN-major (rows m, d contiguous)
+      // += gN S_prev^T: B = the snapshot, rows d (= N), m contiguous (K-major)
+      const uint32_t idQs = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ,
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs,
                (CAUSAL || k > 0) ? 1u : 0u);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idQ, 1);
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idQs, 1);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idQ, 1);
+        mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs, 1);
       mma_commit(sm.mma_bar);
       // segment sum of phi(Q)^T gN, awaited at the chunk's end: phi(Q)^T hi and
       // lo stacked as one M = 128 MN-major operand (the two 64-row halves are
@@ -476,21 +468,34 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float4* stage = reinterpret_cast<float4*>((h == 0 ? kt : sm.klo) + q4 * 4096);
       store_half_rows(dq + ((size_t)bh * g.N + t0) * kDim + 32 * h, row, nvalid, o, stage);
     }
-    // state MMAs of this chunk (dS from the first group, dR from the second)
-    if (CAUSAL) {
-      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27)) break;
-      sph0 ^= 1;
-    }
+    // state MMAs of this chunk: the second group's barrier also covers dS,
+    // issued earlier by the same thread
     if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
     sph1 ^= 1;
     fence_after_sync();
-    if (CAUSAL) {
+    if (CAUSAL) {  // S += dS: the lo-part rows pass through the spent gN lo buffer
       uint32_t r[32];
       tmem_ld32(tl + kFS + 32 * h, r);
-      if (sthread) {
+      float4* xs = reinterpret_cast<float4*>(sm.gn_lo);  // [64][16] float4, XOR-swizzled rows
+      if (!dthread) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
+        for (int j = 0; j < 8; ++j)
+          xs[drow * 16 + ((8 * h + j) ^ (drow & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
+      __syncthreads();
+      if (dthread) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 lo = xs[drow * 16 + ((8 * h + j) ^ (drow & 15))];
+          srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
+          srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
+          srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
+          srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+        }
+      }
+      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
     }
 
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
@@ -609,7 +614,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
-    mbar_init(&sm.sbar[0], 1);
     mbar_init(&sm.sbar[1], 1);
     fence_mbar_init();
   }
