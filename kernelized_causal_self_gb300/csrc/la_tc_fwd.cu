@@ -385,7 +385,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_begin(item);
     const int nvalid = min(kC, g.N - t0);
-    if (tid == 0 && cp.valid(g)) {
+    if (!CAUSAL && tid == 0 && cp.valid(g)) {  // causal: issued after the first MMA group
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
       issue(cp);
     }
@@ -462,6 +462,13 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
       }
       mma_commit(mma_bar);
+      // causal: the next chunk's tiles are issued here rather than at the top
+      // of the iteration, so that the output store last read from that stage
+      // (issued at the end of the previous iteration) has drained by now
+      if (CAUSAL && cp.valid(g)) {
+        bulk_wait_read<0>();
+        issue(cp);
+      }
     }
     if (!wait_uniform(mma_bar, mma_phase, hdr, 12)) {
       ok = false;
