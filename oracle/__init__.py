@@ -8,7 +8,7 @@ Pinned functions (each checked in ``tests/test_oracle.py`` against something
 other than itself: a hand-derived worked example, closed forms, invariants,
 brute force, the degree-2 polynomial special case, or central finite
 differences): elu_plus_one, elu_plus_one_grad, masked_attention,
-linearized_attention, recurrent_attention, forward, prefill, decode_step,
+masked_attention_rows, linearized_attention, recurrent_attention, forward, prefill, decode_step,
 backward, denominators. No function here is parity unpinned.
 """
 
@@ -21,6 +21,7 @@ from .linear_attention import (  # noqa: F401
     forward,
     linearized_attention,
     masked_attention,
+    masked_attention_rows,
     poly2_feature,
     prefill,
     recurrent_attention,

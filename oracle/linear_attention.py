@@ -87,6 +87,24 @@ def masked_attention(q, k, v, causal=True, feature=elu_plus_one):
     return (sim @ v) / sim.sum(axis=-1, keepdims=True)
 
 
+def masked_attention_rows(q, k, v, rows, feature=elu_plus_one):
+    """The causal masked form of masked_attention at selected query rows only.
+
+    Same definition ([summary §3.1], [summary §3.3]: out_i = sum_{j<=i}
+    sim(Q_i, K_j) V_j / sum_{j<=i} sim(Q_i, K_j)), evaluated one row at a time,
+    so that long sequences can be checked where the N x N similarity matrix
+    would not fit. q, k: [N, D] and v: [N, M] of one sequence; rows: query
+    positions. Returns [len(rows), M].
+    """
+    fk = feature(k)
+    v = np.asarray(v, dtype=F64)
+    out = []
+    for i in rows:
+        w = fk[: i + 1] @ feature(q[i])         # sim(Q_i, K_j) for j <= i
+        out.append((w @ v[: i + 1]) / w.sum())
+    return np.stack(out)
+
+
 def linearized_attention(q, k, v, feature=elu_plus_one):
     """Non-causal linear attention by associativity.
 

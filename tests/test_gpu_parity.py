@@ -257,6 +257,49 @@ def test_full_size_backward_sampled(la):
             assert_close(_np(got[b, h]), want, w.dtype, f"{name}[{b},{h}]")
 
 
+# ------------------------------------------------------------- maximum sizes
+
+def test_forward_million_tokens_sampled(la):
+    """2^20 + 37 tokens per sequence (8,193 chunks, ragged last chunk): sampled
+    rows of the causal forward against the masked form, and the prefill's final
+    state against the full sums."""
+    B, H, N = 1, 2, (1 << 20) + 37
+    g = torch.Generator(device=DEV)
+    g.manual_seed(20)
+    q = inputs.torch_normal(g, (B, H, N, 64), 0.125, inputs.BF16, DEV)
+    k = inputs.torch_normal(g, (B, H, N, 64), 0.125, inputs.BF16, DEV)
+    v = inputs.torch_normal(g, (B, H, N, 64), 0.125, inputs.BF16, DEV)
+    out = la.la_forward(q, k, v, causal=True)
+    _, S, Z = la.la_prefill(q, k, v)
+    torch.cuda.synchronize()
+    rows = [0, 1, 127, 128, 4095, 523777, N - 38, N - 1]
+    for h in range(H):
+        qh, kh, vh = _np(q[0, h]), _np(k[0, h]), _np(v[0, h])
+        want = oracle.masked_attention_rows(qh, kh, vh, rows)
+        assert_close(_np(out[0, h])[rows], want, "bf16", f"out rows, head {h}")
+        _, S_ref, Z_ref = oracle.linearized_attention(qh, kh, vh)
+        assert_close(S[0, h].cpu().numpy(), S_ref, "bf16", f"S_N, head {h}")
+        assert_close(Z[0, h].cpu().numpy(), Z_ref, "bf16", f"Z_N, head {h}")
+
+
+def test_many_short_sequences_sampled(la):
+    """B * H = 2048 sequences of 77 tokens (one ragged chunk each): forward and
+    backward on sampled sequences."""
+    B, H, N = 64, 32, 77
+    g = torch.Generator(device=DEV)
+    g.manual_seed(21)
+    q, k, v, d = (inputs.torch_normal(g, (B, H, N, 64), 0.125, inputs.BF16, DEV) for _ in range(4))
+    out = la.la_forward(q, k, v, causal=True)
+    dq, dk, dv = la.la_backward(q, k, v, d, causal=True)
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (17, 5), (B - 1, H - 1)):
+        qh, kh, vh, dh = _np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(d[b, h])
+        assert_close(_np(out[b, h]), oracle.forward(qh, kh, vh, True), "bf16", f"out[{b},{h}]")
+        wq, wk, wv = oracle.backward(qh, kh, vh, dh, True)
+        for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+            assert_close(_np(got[b, h]), want, "bf16", f"{name}[{b},{h}]")
+
+
 def test_full_size_decode_sampled(la):
     w = inputs.WORKLOADS["decode_s256h8d64_prefill1024_steps3072"]
     q, k, v, g = _device_inputs(w)

@@ -118,6 +118,18 @@ def test_masked_equals_recurrence(N, D, M):
     np.testing.assert_allclose(oracle.forward(q, k, v, causal=True), a, rtol=1e-12, atol=1e-12)
 
 
+def test_masked_rows_equal_full_masked_form():
+    # every row of a sequence that spans the row-by-row loop's edge cases
+    # (first row, last row): an off-by-one in the mask fails here
+    N, D, M = 37, 6, 5
+    q, k, v = _rand(7, N, D), _rand(8, N, D), _rand(9, N, M)
+    full = la.masked_attention(q, k, v, causal=True)
+    rows = list(range(N))
+    np.testing.assert_allclose(la.masked_attention_rows(q, k, v, rows), full, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(la.masked_attention_rows(q, k, v, [N - 1, 0, 5]), full[[N - 1, 0, 5]],
+                               rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("N,D,M", [(1, 3, 2), (33, 8, 5)])
 def test_masked_equals_linearized_noncausal(N, D, M):
     q, k, v = _rand(4, 2, N, D), _rand(5, 2, N, D), _rand(6, 2, N, M)
