@@ -106,6 +106,33 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
                int B, int H, int N, int D, int M, int dtype,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * la_extend -- causal forward over N new tokens of B streams that continue
+ * from a stored recurrent state (chunked prefill, multi-token decode).
+ *
+ * [deck slide 4], [summary §3.3.2, §3.4]: the causally masked layer is an RNN,
+ * so a stream's next tokens depend on its past only through (S, Z). For each
+ * stream b and head h, with (S, Z) the state in pool entry slots[b] (head h)
+ * on entry, out[b][h][i] = phi(q_i)^T S_i / phi(q_i)^T Z_i for i = 0..N-1 with
+ * S_i = S + sum_{j<=i} phi(k_j) v_j^T, Z_i = Z + sum_{j<=i} phi(k_j), and the
+ * entry holds (S_{N-1}, Z_{N-1}) on return. N = 1 is one la_decode_step; a
+ * zero state gives la_prefill.
+ *
+ * q, k: [B][H][N][D]; v, out: [B][H][N][M] in `dtype`.
+ * S_pool [pool_size][H][D][M], Z_pool [pool_size][H][D] float32, caller-owned,
+ * read and updated in place.
+ * slots: device int[B] (4-byte aligned) naming each stream's pool entry, all
+ * distinct; nullptr means entry b (then pool_size >= B). A slot outside
+ * [0, pool_size) is not read or written: that stream starts from a zero state,
+ * and la_workspace_status reports LA_ERR_INVALID_ARG afterwards.
+ * Workspace: la_forward_workspace_bytes(B, H, N, D, M, 1, dtype).
+ * N == 0 returns LA_OK without touching the pool.
+ */
+int la_extend(const void* q, const void* k, const void* v, void* out,
+              float* S_pool, float* Z_pool, const int* slots, int pool_size,
+              int B, int H, int N, int D, int M, int dtype,
+              void* workspace, size_t workspace_bytes, void* stream);
+
 /* Scratch needed by la_backward for this shape, in bytes. */
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype);
 
@@ -170,9 +197,10 @@ int la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
 
 /*
  * la_workspace_status -- synchronises `stream` and reads the status word a
- * previous la_forward / la_prefill / la_backward left in `workspace`:
- * LA_OK, or LA_ERR_TIMEOUT if a bounded cross-CTA wait gave up (the outputs
- * of that call are then invalid). Clears the word. Debug / test use.
+ * previous la_forward / la_prefill / la_extend / la_backward left in
+ * `workspace`: LA_OK; LA_ERR_TIMEOUT if a bounded cross-CTA wait gave up (the
+ * outputs of that call are then invalid); LA_ERR_INVALID_ARG if la_extend met
+ * a slot outside its pool. Clears the word. Debug / test use.
  */
 int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream);
 

@@ -11,7 +11,7 @@ import ctypes
 import os
 
 __all__ = [
-    "la_forward", "la_prefill", "la_backward", "la_decode_step",
+    "la_forward", "la_prefill", "la_extend", "la_backward", "la_decode_step",
     "la_forward_workspace_bytes", "la_backward_workspace_bytes",
     "la_workspace_status", "la_status_string", "la_kernel_launches", "library_path",
     "load_library",
@@ -37,6 +37,7 @@ _SIGNATURES = {
     "la_backward_workspace_bytes": (_c_size, [_c_int] * 7),
     "la_forward": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_prefill": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_extend": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_backward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
@@ -187,6 +188,36 @@ def la_prefill(q, k, v, out=None, S=None, Z=None, workspace=None):
                         ws.numel() * ws.element_size(), _stream_ptr(dev))
     _check("la_prefill", st)
     return out, S, Z
+
+
+def la_extend(q, k, v, S_pool, Z_pool, slots=None, out=None, workspace=None):
+    """Causal forward over N new tokens of B streams continuing from stored state.
+
+    S_pool [P,H,D,M], Z_pool [P,H,D] float32 hold per-stream states; stream b uses
+    entry slots[b] (int32 device tensor of B distinct entries; None: entry b) and
+    its entry is advanced past the N tokens in place. Returns out [B,H,N,M].
+    """
+    import torch
+    lib = load_library()
+    _need_cuda(q, k, v, S_pool, Z_pool)
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dev = q.device
+    out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
+    _need_cuda(out)
+    if slots is not None:
+        _need_cuda(slots)
+        if slots.dtype != torch.int32 or slots.numel() != B or not slots.is_contiguous():
+            raise ValueError("slots must be a contiguous int32 tensor of B entries")
+    nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.la_extend(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S_pool.data_ptr(),
+                       Z_pool.data_ptr(), 0 if slots is None else slots.data_ptr(), S_pool.shape[0],
+                       B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                       _stream_ptr(dev))
+    _check("la_extend", st)
+    return out
 
 
 def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace=None):

@@ -94,10 +94,10 @@ int la_forward(const void* q, const void* k, const void* v, void* out, int B, in
   cudaError_t e = clear_header(workspace, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
   if (la::tc_forward_supported(D, M, dtype))
-    return from_cuda(la::tc_forward(q, k, v, out, nullptr, nullptr, B * H, N, causal != 0,
+    return from_cuda(la::tc_forward(q, k, v, out, la::StateIO{}, B * H, N, causal != 0,
                                     workspace, st));
-  return from_cuda(la::simt_forward(q, k, v, out, nullptr, nullptr, B * H, N, D, M, causal != 0,
-                                    dtype, st));
+  return from_cuda(la::simt_forward(q, k, v, out, la::StateIO{}, B * H, N, D, M, causal != 0,
+                                    dtype, static_cast<la::WorkspaceHeader*>(workspace), st));
 }
 
 int la_prefill(const void* q, const void* k, const void* v, void* out, float* S, float* Z, int B,
@@ -118,9 +118,43 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
   cudaStream_t st = as_stream(stream);
   cudaError_t e = clear_header(workspace, st);
   if (e != cudaSuccess) return LA_ERR_CUDA;
+  la::StateIO io;
+  io.S = S;
+  io.Z = Z;
+  io.H = H;
+  io.pool = B;
   if (la::tc_forward_supported(D, M, dtype))
-    return from_cuda(la::tc_forward(q, k, v, out, S, Z, B * H, N, true, workspace, st));
-  return from_cuda(la::simt_forward(q, k, v, out, S, Z, B * H, N, D, M, true, dtype, st));
+    return from_cuda(la::tc_forward(q, k, v, out, io, B * H, N, true, workspace, st));
+  return from_cuda(la::simt_forward(q, k, v, out, io, B * H, N, D, M, true, dtype,
+                                    static_cast<la::WorkspaceHeader*>(workspace), st));
+}
+
+int la_extend(const void* q, const void* k, const void* v, void* out, float* S_pool,
+              float* Z_pool, const int* slots, int pool_size, int B, int H, int N, int D, int M,
+              int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S_pool, Z_pool})) return LA_ERR_INVALID_ARG;
+  if (slots == nullptr ? pool_size < B : pool_size < 1) return LA_ERR_INVALID_ARG;
+  if (slots != nullptr && (reinterpret_cast<uintptr_t>(slots) & 3u) != 0) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = clear_header(workspace, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  la::StateIO io;
+  io.S = S_pool;
+  io.Z = Z_pool;
+  io.slots = slots;
+  io.H = H;
+  io.pool = pool_size;
+  io.read_init = true;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_forward(q, k, v, out, io, B * H, N, true, workspace, st));
+  return from_cuda(la::simt_forward(q, k, v, out, io, B * H, N, D, M, true, dtype,
+                                    static_cast<la::WorkspaceHeader*>(workspace), st));
 }
 
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
@@ -169,7 +203,7 @@ int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream) {
     e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return LA_ERR_CUDA;
-    return h.status == LA_ERR_TIMEOUT ? LA_ERR_TIMEOUT : LA_ERR_CUDA;
+    return (h.status == LA_ERR_TIMEOUT || h.status == LA_ERR_INVALID_ARG) ? h.status : LA_ERR_CUDA;
   }
   return LA_OK;
 }

@@ -4,15 +4,32 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include "la_common.cuh"
+
 namespace la {
+
+// Where a causal forward takes its initial state and leaves its final state:
+// S [entries][D][M] and Z [entries][D] float32, sequence bh = b * H + h at entry
+// slots[b] * H + h (slots == nullptr: entry bh). read_init: start from the
+// entry's contents (and overwrite them in place), else start from zero.
+// Entries of slots outside [0, pool) skip that sequence's state and set the
+// workspace status word to LA_ERR_INVALID_ARG.
+struct StateIO {
+  float* S = nullptr;
+  float* Z = nullptr;
+  const int* slots = nullptr;
+  int H = 1;
+  int pool = 0;
+  bool read_init = false;
+};
 
 // Adds n to the process-wide kernel launch count reported by la_kernel_launches().
 void count_launches(unsigned n);
 
 // ---- general-shape CUDA-core path (any dtype, D and M multiples of 8 up to 128)
-cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
-                         float* Z_out, int BH, int N, int D, int M, bool causal, int dtype,
-                         cudaStream_t st);
+cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out,
+                         const StateIO& io, int BH, int N, int D, int M, bool causal, int dtype,
+                         WorkspaceHeader* hdr, cudaStream_t st);
 size_t simt_backward_workspace(int BH, int N);
 cudaError_t simt_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                           float* dk, float* dv, int BH, int N, int D, int M, bool causal,
@@ -21,8 +38,8 @@ cudaError_t simt_backward(const void* q, const void* k, const void* v, const voi
 // ---- tensor-core path (bf16, D = M = 64): tcgen05 + TMEM + TMA
 bool tc_forward_supported(int D, int M, int dtype);
 size_t tc_forward_workspace(int BH, int N);
-cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
-                       float* Z_out, int BH, int N, bool causal, void* ws, cudaStream_t st);
+cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
+                       int BH, int N, bool causal, void* ws, cudaStream_t st);
 size_t tc_backward_workspace(int BH, int N);
 cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                         float* dk, float* dv, int BH, int N, bool causal, void* ws,

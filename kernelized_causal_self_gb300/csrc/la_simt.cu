@@ -74,8 +74,7 @@ __device__ __forceinline__ void pair_dots(const float* a, const float* b, int L,
 template <typename T, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                    T* __restrict__ out, float* __restrict__ S_out, float* __restrict__ Z_out,
-                    int N, int D, int M) {
+                    T* __restrict__ out, StateIO io, WorkspaceHeader* hdr, int N, int D, int M) {
   extern __shared__ float sm[];
   float* S = sm;                   // D*M
   float* Z = S + D * M;            // D
@@ -91,8 +90,18 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
   v += bh * (size_t)N * M;
   out += bh * (size_t)N * M;
 
-  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = 0.f;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = 0.f;
+  // the sequence's state entry: initial state (extend) and final state (prefill, extend)
+  size_t entry = bh;
+  bool entry_ok = io.S != nullptr;
+  if (entry_ok && io.slots != nullptr) {
+    const int slot = io.slots[bh / io.H];
+    entry_ok = slot >= 0 && slot < io.pool;
+    entry = (size_t)slot * io.H + bh % io.H;
+    if (!entry_ok && threadIdx.x == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+  }
+  const bool init = entry_ok && io.read_init;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = init ? io.S[entry * D * M + e] : 0.f;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = init ? io.Z[entry * D + e] : 0.f;
   __syncthreads();
 
   if (!CAUSAL) {  // full sums first
@@ -139,9 +148,9 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     }
   }
 
-  if (S_out != nullptr) {
-    for (int e = threadIdx.x; e < D * M; e += blockDim.x) S_out[bh * D * M + e] = S[e];
-    for (int e = threadIdx.x; e < D; e += blockDim.x) Z_out[bh * D + e] = Z[e];
+  if (entry_ok) {
+    for (int e = threadIdx.x; e < D * M; e += blockDim.x) io.S[entry * D * M + e] = S[e];
+    for (int e = threadIdx.x; e < D; e += blockDim.x) io.Z[entry * D + e] = Z[e];
   }
 }
 
@@ -440,12 +449,13 @@ cudaError_t launch(K kernel, int grid, size_t smem, cudaStream_t st, Args... arg
 }
 
 template <typename T>
-cudaError_t forward_t(const void* q, const void* k, const void* v, void* out, float* S_out,
-                      float* Z_out, int BH, int N, int D, int M, bool causal, cudaStream_t st) {
+cudaError_t forward_t(const void* q, const void* k, const void* v, void* out, const StateIO& io,
+                      int BH, int N, int D, int M, bool causal, WorkspaceHeader* hdr,
+                      cudaStream_t st) {
   const size_t smem = fwd_smem(D, M);
   auto args = [&](auto kern) {
-    return launch(kern, BH, smem, st, (const T*)q, (const T*)k, (const T*)v, (T*)out, S_out,
-                  Z_out, N, D, M);
+    return launch(kern, BH, smem, st, (const T*)q, (const T*)k, (const T*)v, (T*)out, io, hdr, N,
+                  D, M);
   };
   return causal ? args(simt_forward_kernel<T, true>) : args(simt_forward_kernel<T, false>);
 }
@@ -475,11 +485,11 @@ cudaError_t backward_t(const void* q, const void* k, const void* v, const void* 
 
 }  // namespace
 
-cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
-                         float* Z_out, int BH, int N, int D, int M, bool causal, int dtype,
-                         cudaStream_t st) {
-  if (dtype == LA_F32) return forward_t<float>(q, k, v, out, S_out, Z_out, BH, N, D, M, causal, st);
-  return forward_t<__nv_bfloat16>(q, k, v, out, S_out, Z_out, BH, N, D, M, causal, st);
+cudaError_t simt_forward(const void* q, const void* k, const void* v, void* out,
+                         const StateIO& io, int BH, int N, int D, int M, bool causal, int dtype,
+                         WorkspaceHeader* hdr, cudaStream_t st) {
+  if (dtype == LA_F32) return forward_t<float>(q, k, v, out, io, BH, N, D, M, causal, hdr, st);
+  return forward_t<__nv_bfloat16>(q, k, v, out, io, BH, N, D, M, causal, hdr, st);
 }
 
 size_t simt_backward_workspace(int BH, int N) {

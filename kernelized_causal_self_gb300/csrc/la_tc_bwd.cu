@@ -940,7 +940,7 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
 
   cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, true, st);
   if (e != cudaSuccess) return e;
-  e = launch_scan(spartial, sprefix, g, causal ? kScanPrefix : kScanTotal, nullptr, nullptr, st);
+  e = launch_scan(spartial, sprefix, g, causal ? kScanPrefix : kScanTotal, StateIO{}, hdr, st);
   if (e != cudaSuccess) return e;
 
   const int sms = sm_count();
@@ -955,7 +955,7 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   };
   e = causal ? run_q(tc_bwd_q_kernel<true>) : run_q(tc_bwd_q_kernel<false>);
   if (e != cudaSuccess) return e;
-  e = launch_scan(rpartial, rsuffix, g, causal ? kScanSuffix : kScanTotal, nullptr, nullptr, st);
+  e = launch_scan(rpartial, rsuffix, g, causal ? kScanSuffix : kScanTotal, StateIO{}, hdr, st);
   if (e != cudaSuccess) return e;
   auto run_kv = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);

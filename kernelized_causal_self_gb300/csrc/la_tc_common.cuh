@@ -291,8 +291,10 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
                                   float* partial, WorkspaceHeader* hdr, bool precise,
                                   cudaStream_t st);
 // Prefix / total / suffix of the per-segment states (see ScanMode).
-cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
-                        float* Z_out, cudaStream_t st);
+// With io.S set, the prefix / total also starts from io's initial state (when
+// io.read_init) and the full sum is written to io's entries (prefill, extend).
+cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode,
+                        const StateIO& io, WorkspaceHeader* hdr, cudaStream_t st);
 
 }  // namespace tcx
 }  // namespace la

@@ -236,22 +236,36 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // ----------------------------------------------------------- 2. segment scan
 
-// mode kScanPrefix:  out[seg][bh] = sum_{s < seg} partial[s][bh]  (causal, forward)
-// mode kScanTotal:   out[bh]      = sum_s partial[s][bh]          (non-causal)
-// mode kScanSuffix:  out[seg][bh] = sum_{s > seg} partial[s][bh]  (causal, reverse)
-// S_out[bh][d][m], Z_out[bh][d] = full sum when requested (prefill).
+// mode kScanPrefix:  out[seg][bh] = S0 + sum_{s < seg} partial[s][bh]  (causal, forward)
+// mode kScanTotal:   out[bh]      = sum_s partial[s][bh]               (non-causal)
+// mode kScanSuffix:  out[seg][bh] = sum_{s > seg} partial[s][bh]       (causal, reverse)
+// S0 is the entry's initial state when io.read_init, else 0; with io.S set the
+// full sum (S0 + all segments) is written to the entry: S [d][m], Z [d].
 // One thread per state element; the segment loads are issued in batches of 8
 // so the walk over segments is not a chain of dependent global loads.
 constexpr int kScanThreads = 128;
 
 __global__ void __launch_bounds__(kScanThreads)
 state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, int BH, int n_seg,
-                  int mode, float* __restrict__ S_out, float* __restrict__ Z_out) {
+                  int mode, StateIO io, WorkspaceHeader* hdr) {
   const int bh = blockIdx.y;
   const int e = blockIdx.x * kScanThreads + threadIdx.x;
   pdl_wait();
   if (e >= kStateFloats) return;
-  float run = 0.f;
+  // the sequence's state entry (prefill, extend)
+  size_t entry = (size_t)bh;
+  bool entry_ok = io.S != nullptr;
+  if (entry_ok && io.slots != nullptr) {
+    const int slot = io.slots[bh / io.H];
+    entry_ok = slot >= 0 && slot < io.pool;
+    entry = (size_t)slot * io.H + bh % io.H;
+    if (!entry_ok && e == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+  }
+  const int m = e / kDim, d = e % kDim;  // e < 4096: S^T [m][d]; else Z [e - 4096]
+  float* cell = !entry_ok ? nullptr
+                          : (e < kDim * kDim ? io.S + entry * kDim * kDim + d * kDim + m
+                                             : io.Z + entry * kDim + (e - kDim * kDim));
+  float run = (cell != nullptr && io.read_init && mode == kScanPrefix) ? *cell : 0.f;
   const bool rev = mode == kScanSuffix;
   for (int s0 = 0; s0 < n_seg; s0 += 8) {
     float x[8];
@@ -270,14 +284,7 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
     }
   }
   if (mode == kScanTotal) out[(size_t)bh * kStateFloats + e] = run;
-  if (S_out != nullptr) {
-    if (e < kDim * kDim) {
-      const int m = e / kDim, d = e % kDim;
-      S_out[(size_t)bh * kDim * kDim + d * kDim + m] = run;
-    } else {
-      Z_out[(size_t)bh * kDim + (e - kDim * kDim)] = run;
-    }
-  }
+  if (cell != nullptr) *cell = run;
 }
 
 // --------------------------------------------------------- 3. chunk attention
@@ -640,11 +647,11 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
                  : run(tc_state_kernel<false>, state_smem<false>());
 }
 
-cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode, float* S_out,
-                        float* Z_out, cudaStream_t st) {
+cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode,
+                        const StateIO& io, WorkspaceHeader* hdr, cudaStream_t st) {
   const dim3 grid((kStateFloats + kScanThreads - 1) / kScanThreads, g.BH);
   cudaError_t e = launch_pdl(state_scan_kernel, grid, dim3(kScanThreads), 0, st, partial, out,
-                             g.BH, g.n_seg, mode, S_out, Z_out);
+                             g.BH, g.n_seg, mode, io, hdr);
   count_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -660,8 +667,8 @@ size_t tc_forward_workspace(int BH, int N) {
   return kHeaderBytes + 2 * align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256);
 }
 
-cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, float* S_out,
-                       float* Z_out, int BH, int N, bool causal, void* ws, cudaStream_t st) {
+cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
+                       int BH, int N, bool causal, void* ws, cudaStream_t st) {
   const Geometry g = make_geometry(BH, N);
   WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
@@ -676,7 +683,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, f
 
   cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
   if (e != cudaSuccess) return e;
-  e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, S_out, Z_out, st);
+  e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
 

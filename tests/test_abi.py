@@ -37,7 +37,7 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill",
+    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill", "la_extend",
               "la_forward_workspace_bytes", "la_backward_workspace_bytes",
               "la_status_string", "la_workspace_status"):
         assert n in names
@@ -53,7 +53,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_binding_mirrors_the_abi_names():
-    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill",
+    for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill", "la_extend",
               "la_forward_workspace_bytes", "la_backward_workspace_bytes",
               "la_status_string", "la_workspace_status"):
         assert callable(getattr(la, n))
@@ -83,6 +83,24 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, ws=0) == la.LA_ERR_WORKSPACE
     assert _fwd(lib, ws=ODD) == la.LA_ERR_WORKSPACE
     assert _fwd(lib, wsb=16) == la.LA_ERR_WORKSPACE
+
+
+def _ext(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, S=FAKE, Z=FAKE, slots=FAKE, pool=4, B=2, H=1, N=16,
+         D=64, M=64, dtype=1, ws=FAKE, wsb=1 << 20):
+    return lib.la_extend(q, k, v, out, S, Z, slots, pool, B, H, N, D, M, dtype, ws, wsb, None)
+
+
+def test_extend_rejects_bad_arguments(lib):
+    assert _ext(lib, S=0) == la.LA_ERR_INVALID_ARG
+    assert _ext(lib, Z=ODD) == la.LA_ERR_INVALID_ARG
+    assert _ext(lib, slots=FAKE + 2) == la.LA_ERR_INVALID_ARG        # slots must be 4-byte aligned
+    assert _ext(lib, pool=0) == la.LA_ERR_INVALID_ARG
+    assert _ext(lib, slots=0, pool=1, B=2) == la.LA_ERR_INVALID_ARG  # identity slots need B entries
+    assert _ext(lib, D=12) == la.LA_ERR_INVALID_ARG
+    assert _ext(lib, q=0) == la.LA_ERR_INVALID_ARG
+    assert _ext(lib, ws=0) == la.LA_ERR_WORKSPACE
+    assert _ext(lib, wsb=16) == la.LA_ERR_WORKSPACE
+    assert _ext(lib, q=0, k=0, v=0, out=0, N=0) == la.LA_OK           # nothing to extend
 
 
 def test_empty_sequence_is_a_noop(lib):

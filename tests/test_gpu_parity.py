@@ -186,6 +186,105 @@ def test_prefill_then_decode_matches_forward(la, dtype):
         assert_close(o.float().cpu().numpy(), want[:, :, t], dtype, f"decode step {t}")
 
 
+# ------------------------------------------------------- extend from a stored state
+
+EXTEND = [(3, 2, 300, 64, 64, inputs.BF16), (2, 3, 45, 32, 48, inputs.F32), (2, 2, 1, 64, 64, inputs.BF16)]
+
+
+@pytest.mark.parametrize("case", EXTEND, ids=lambda s: "b%dh%dn%dd%dm%d-%s" % s)
+def test_extend_from_pool_state(la, case):
+    """Streams continue from states held in a larger pool (permuted slots): the
+    outputs and the advanced states match the recurrence from those states, and
+    pool entries no stream names are left as they were."""
+    B, H, N, D, M, dt = case
+    scale = 0.125 if dt == inputs.BF16 else 1.0
+    P = B + 3
+    q, k, v = inputs.qkv(800 + N, B, H, N, D, M, scale, dt)
+    S0 = np.abs(inputs.normal(801, (P, H, D, M), 1.0, inputs.F32, 0)) * 4.0
+    Z0 = np.abs(inputs.normal(801, (P, H, D), 1.0, inputs.F32, 1)) * 4.0 + 1.0
+    slots = np.array([(2 * b + 1) % P for b in range(B)], dtype=np.int32)  # distinct, permuted
+    tS, tZ = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+    out = la.la_extend(_t(q, dt), _t(k, dt), _t(v, dt), tS, tZ,
+                       slots=torch.from_numpy(slots).to(DEV))
+    torch.cuda.synchronize()
+    got_S, got_Z = tS.cpu().numpy(), tZ.cpu().numpy()
+    for b in range(B):
+        want, S_ref, Z_ref = oracle.recurrent_attention(q[b], k[b], v[b], S0[slots[b]], Z0[slots[b]])
+        assert_close(out[b].float().cpu().numpy(), want, dt, f"out[{b}]")
+        assert_close(got_S[slots[b]], S_ref, dt, f"S[{slots[b]}]")
+        assert_close(got_Z[slots[b]], Z_ref, dt, f"Z[{slots[b]}]")
+    untouched = sorted(set(range(P)) - set(slots.tolist()))
+    assert np.array_equal(got_S[untouched], S0[untouched].astype(np.float32))
+    assert np.array_equal(got_Z[untouched], Z0[untouched].astype(np.float32))
+
+
+def test_prefill_then_extend_matches_forward(la):
+    """Prefill of the first 1000 tokens, then two extensions of 257 and 129:
+    outputs and final state as one causal forward / prefill over all 1386."""
+    B, H, D, M, dt = 2, 2, 64, 64, inputs.BF16
+    cuts = [0, 1000, 1257, 1386]
+    q, k, v = inputs.qkv(810, B, H, cuts[-1], D, M, 0.125, dt)
+    want, S_ref, Z_ref = oracle.prefill(q, k, v)
+    tq, tk, tv = _t(q, dt), _t(k, dt), _t(v, dt)
+    outs = []
+    o, S, Z = la.la_prefill(tq[:, :, :cuts[1]].contiguous(), tk[:, :, :cuts[1]].contiguous(),
+                            tv[:, :, :cuts[1]].contiguous())
+    outs.append(o)
+    for a, b in zip(cuts[1:-1], cuts[2:]):
+        outs.append(la.la_extend(tq[:, :, a:b].contiguous(), tk[:, :, a:b].contiguous(),
+                                 tv[:, :, a:b].contiguous(), S, Z))
+    torch.cuda.synchronize()
+    got = torch.cat(outs, dim=2).float().cpu().numpy()
+    assert_close(got, want, "bf16", "out")
+    assert_close(S.cpu().numpy(), S_ref, "bf16", "S_N")
+    assert_close(Z.cpu().numpy(), Z_ref, "bf16", "Z_N")
+
+
+def test_extend_one_token_equals_decode_step(la):
+    n, H, D, M = 5, 3, 64, 64
+    q = inputs.normal(820, (n, H, 1, D), 0.125, inputs.BF16, 0)
+    k = inputs.normal(820, (n, H, 1, D), 0.125, inputs.BF16, 1)
+    v = inputs.normal(820, (n, H, 1, M), 0.125, inputs.BF16, 2)
+    S0 = np.abs(inputs.normal(820, (n, H, D, M), 1.0, inputs.F32, 3))
+    Z0 = np.abs(inputs.normal(820, (n, H, D), 1.0, inputs.F32, 4)) + 1.0
+    Sa, Za = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+    Sb, Zb = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+    tq, tk, tv = _t(q, inputs.BF16), _t(k, inputs.BF16), _t(v, inputs.BF16)
+    o_ext = la.la_extend(tq, tk, tv, Sa, Za)
+    o_dec = la.la_decode_step(tq[:, :, 0].contiguous(), tk[:, :, 0].contiguous(),
+                              tv[:, :, 0].contiguous(), Sb, Zb)
+    torch.cuda.synchronize()
+    wo, wS, wZ = oracle.decode_step(q[:, :, 0], k[:, :, 0], v[:, :, 0], S0, Z0)
+    assert_close(o_ext[:, :, 0].float().cpu().numpy(), wo, "bf16", "extend out")
+    assert_close(o_dec.float().cpu().numpy(), wo, "bf16", "decode out")
+    assert_close(Sa.cpu().numpy(), wS, "bf16", "extend S")
+    assert_close(Za.cpu().numpy(), wZ, "bf16", "extend Z")
+
+
+def test_extend_reports_a_bad_slot(la):
+    """A slot outside the pool is neither read nor written: that stream starts
+    from zero, the others are unaffected, and the status word says so."""
+    B, H, N, P = 3, 2, 200, 4
+    q, k, v = inputs.qkv(830, B, H, N, 64, 64, 0.125, inputs.BF16)
+    S0 = np.abs(inputs.normal(831, (P, H, 64, 64), 1.0, inputs.F32, 0))
+    Z0 = np.abs(inputs.normal(831, (P, H, 64), 1.0, inputs.F32, 1)) + 1.0
+    slots = np.array([1, 7, 3], dtype=np.int32)
+    tS, tZ = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+    nbytes = la.la_forward_workspace_bytes(B, H, N, 64, 64, True, la.LA_BF16)
+    ws = torch.zeros((nbytes,), dtype=torch.uint8, device=DEV)
+    out = la.la_extend(_t(q, inputs.BF16), _t(k, inputs.BF16), _t(v, inputs.BF16), tS, tZ,
+                       slots=torch.from_numpy(slots).to(DEV), workspace=ws)
+    assert la.la_workspace_status(ws) == la.LA_ERR_INVALID_ARG
+    got_S = tS.cpu().numpy()
+    for b, sl in ((0, 1), (2, 3)):
+        want, S_ref, _ = oracle.recurrent_attention(q[b], k[b], v[b], S0[sl], Z0[sl])
+        assert_close(out[b].float().cpu().numpy(), want, "bf16", f"out[{b}]")
+        assert_close(got_S[sl], S_ref, "bf16", f"S[{sl}]")
+    assert_close(out[1].float().cpu().numpy(), oracle.forward(q[1], k[1], v[1], True), "bf16", "out[1]")
+    for sl in (0, 2):
+        assert np.array_equal(got_S[sl], S0[sl].astype(np.float32))
+
+
 def test_decode_step_odd_shapes(la):
     for D, M in ((8, 8), (32, 16), (128, 128), (16, 120)):
         n, H = 3, 2
