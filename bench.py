@@ -72,6 +72,35 @@ def decode_bytes(w):
     return 8 * w.D * w.M + 8 * w.D + 2 * (2 * w.D + 2 * w.M)  # S, Z read+write; q,k,v,out
 
 
+EXTEND_TOKENS, EXTEND_POOL = 64, 512  # new tokens per stream per la_extend call; pool entries
+
+
+def extend_bytes(w, T):
+    """Per stream-head and call: q, k, v, out for T tokens + the state read and written."""
+    return T * fwd_bytes(w) + 8 * w.D * w.M + 8 * w.D
+
+
+def extend_setup(la, w, g, device, S, Z):
+    """The decode workload's streams, their states scattered over a larger pool (stream b
+    in entry 2b + 1), and EXTEND_TOKENS new tokens per stream."""
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    T, P = EXTEND_TOKENS, EXTEND_POOL
+    shp_qk, shp_v = (w.B, w.H, T, w.D), (w.B, w.H, T, w.M)
+    eq = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, device)
+    ek = inputs.torch_normal(g, shp_qk, w.scale, w.dtype, device)
+    ev = inputs.torch_normal(g, shp_v, w.scale, w.dtype, device)
+    slots = ((2 * torch.arange(w.B, device=device) + 1) % P).to(torch.int32)
+    pS = torch.zeros((P, w.H, w.D, w.M), dtype=torch.float32, device=device)
+    pZ = torch.zeros((P, w.H, w.D), dtype=torch.float32, device=device)
+    pS[slots.long()] = S
+    pZ[slots.long()] = Z
+    eo = torch.empty(shp_v, dtype=eq.dtype, device=device)
+    ws = torch.empty(la.la_forward_workspace_bytes(w.B, w.H, T, w.D, w.M, True), dtype=torch.uint8,
+                     device=device)
+    return lambda: la.la_extend(eq, ek, ev, pS, pZ, slots=slots, out=eo, workspace=ws)
+
+
 class Clocks:
     """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
 
@@ -147,7 +176,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's calls directly instead of replaying CUDA graphs")
     ap.add_argument("--part", default=None,
-                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode"],
+                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode", "extend"],
                     help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
@@ -281,6 +310,14 @@ def run_parts(la, device, peaks, reps=10):
         "tokens_per_s": w.B * T / (ms * 1e-3), "ms_per_step": per_step, "hbm_gbs": gbs,
         "roofline_frac": gbs / hbm, "steps": T, "launch": "CUDA graph of 3072 la_decode_step calls",
         "l2": "S/Z state (33.5 MB) fits in L2; fraction can exceed 1"}
+    # extend: EXTEND_TOKENS new tokens per stream from states in a pool, one call
+    fn = extend_setup(la, w, g, device, S0, Z0)
+    ms = statistics.median(time_calls(fn, reps, 3, flush))
+    gbs = w.B * w.H * extend_bytes(w, EXTEND_TOKENS) / (ms * 1e-3) / 1e9
+    parts[f"extend_s256h8d64_t{EXTEND_TOKENS}_pool{EXTEND_POOL}"] = {
+        "tokens_per_s": w.B * EXTEND_TOKENS / (ms * 1e-3), "ms": ms, "hbm_gbs": gbs,
+        "roofline_frac": gbs / hbm, "same_tokens_as_decode_steps_ms": per_step * EXTEND_TOKENS,
+        "launch": "one la_extend call", "l2": "flushed between calls"}
     return parts
 
 
@@ -564,7 +601,8 @@ def run_part(args):
     device = torch.device("cuda", 0)
     name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "fwd3072": "causal_fwd_b8h8n3072d64",
             "noncausal": "noncausal_fwd_b4h8n4096d64",
-            "decode": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
+            "decode": "decode_s256h8d64_prefill1024_steps3072",
+            "extend": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
     w = inputs.WORKLOADS[name]
     q, k, v, dout, g = device_inputs(w, device, dout=True)
     if args.part == "decode":
@@ -573,6 +611,9 @@ def run_part(args):
         sk = inputs.torch_normal(g, (w.B, w.H, w.D), w.scale, w.dtype, device)
         sv = inputs.torch_normal(g, (w.B, w.H, w.M), w.scale, w.dtype, device)
         fn = lambda: la.la_decode_step(sq, sk, sv, S, Z)
+    elif args.part == "extend":
+        _, S, Z = la.la_prefill(q, k, v)
+        fn = extend_setup(la, w, g, device, S, Z)
     elif args.part == "bwd":
         fn = lambda: la.la_backward(q, k, v, dout, True)
     elif args.part == "fwdbwd":
