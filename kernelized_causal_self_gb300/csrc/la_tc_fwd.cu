@@ -313,7 +313,8 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kAttThreads, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 Geometry g, const float* __restrict__ prefix, WorkspaceHeader* hdr) {
+                 Geometry g, const float* __restrict__ prefix, StateIO io, bool direct,
+                 WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = sm;  // [stage][Q | K | V]
@@ -396,7 +397,25 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
       issue(cp);
     }
-    if (first) {  // state before this segment
+    // direct (causal, one chunk per sequence): the state before the chunk is the
+    // sequence's entry in io (or zero), and the state after it goes back there
+    size_t entry = (size_t)bh;
+    bool entry_ok = direct && io.S != nullptr;
+    if (entry_ok && io.slots != nullptr) {
+      const int slot = io.slots[bh / io.H];
+      entry_ok = slot >= 0 && slot < io.pool;
+      entry = (size_t)slot * io.H + bh % io.H;
+      if (!entry_ok && tid == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+    }
+    if (direct) {  // S [entry][d][m]: this thread's row m = srow, columns d of its half
+      const bool init = entry_ok && io.read_init;
+      if (sthread) {
+        const float* src = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + srow;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) srun[j] = init ? src[(size_t)j * kDim] : 0.f;
+        zrun = init ? io.Z[entry * kDim + srow] : 0.f;
+      }
+    } else if (first) {  // state before this segment
       const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (sthread) {
         const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
@@ -563,6 +582,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tmem_ld16(tl + kColZ, r16);
         if (sthread) zrun += __uint_as_float(r16[0]);
       }
+      if (entry_ok && sthread) {  // direct: the state after the sequence's only chunk
+        float* dst = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + srow;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(size_t)j * kDim] = srun[j];
+        if (h == 0) io.Z[entry * kDim + srow] = zrun;
+      }
     }
 
     // out = num / den -> bf16, this half's columns, staged in the Q slot (all
@@ -681,10 +706,16 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
       !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
-  if (e != cudaSuccess) return e;
-  e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
-  if (e != cudaSuccess) return e;
+  // causal with one chunk per sequence: no segment states or scan; the attend
+  // kernel takes the state from io (or zero) and writes the final state there
+  const bool direct = causal && g.n_chunks == 1;
+  cudaError_t e = cudaSuccess;
+  if (!direct) {
+    e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
+    if (e != cudaSuccess) return e;
+    e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
+    if (e != cudaSuccess) return e;
+  }
   const int sms = sm_count();
 
   // non-causal: one item per chunk range of the readout, all reading prefix[bh]
@@ -694,7 +725,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
     const int ctas =
         min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem, kAttThreads) * sms);
     e = launch_pdl(tc_attend_kernel<true>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
-                   to, g, (const float*)prefix, hdr);
+                   to, g, (const float*)prefix, io, direct, hdr);
     if (e != cudaSuccess) return e;
   } else {
     e = configure(tc_attend_kernel<false>, kAttSmem);
@@ -702,7 +733,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
     const int ctas =
         min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem, kAttThreads) * sms);
     e = launch_pdl(tc_attend_kernel<false>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
-                   to, g, (const float*)prefix, hdr);
+                   to, g, (const float*)prefix, StateIO{}, false, hdr);
     if (e != cudaSuccess) return e;
   }
   count_launches(1);

@@ -188,7 +188,10 @@ def test_prefill_then_decode_matches_forward(la, dtype):
 
 # ------------------------------------------------------- extend from a stored state
 
-EXTEND = [(3, 2, 300, 64, 64, inputs.BF16), (2, 3, 45, 32, 48, inputs.F32), (2, 2, 1, 64, 64, inputs.BF16)]
+# tensor-core path through the segment scan (N > 128) and directly (N <= 128, one
+# chunk per sequence), and the CUDA-core path
+EXTEND = [(3, 2, 300, 64, 64, inputs.BF16), (4, 2, 100, 64, 64, inputs.BF16),
+          (2, 3, 45, 32, 48, inputs.F32), (2, 2, 1, 64, 64, inputs.BF16)]
 
 
 @pytest.mark.parametrize("case", EXTEND, ids=lambda s: "b%dh%dn%dd%dm%d-%s" % s)
@@ -261,10 +264,11 @@ def test_extend_one_token_equals_decode_step(la):
     assert_close(Za.cpu().numpy(), wZ, "bf16", "extend Z")
 
 
-def test_extend_reports_a_bad_slot(la):
+@pytest.mark.parametrize("N", [200, 90])
+def test_extend_reports_a_bad_slot(la, N):
     """A slot outside the pool is neither read nor written: that stream starts
     from zero, the others are unaffected, and the status word says so."""
-    B, H, N, P = 3, 2, 200, 4
+    B, H, P = 3, 2, 4
     q, k, v = inputs.qkv(830, B, H, N, 64, 64, 0.125, inputs.BF16)
     S0 = np.abs(inputs.normal(831, (P, H, 64, 64), 1.0, inputs.F32, 0))
     Z0 = np.abs(inputs.normal(831, (P, H, 64), 1.0, inputs.F32, 1)) + 1.0
