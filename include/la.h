@@ -125,12 +125,16 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
  * distinct; nullptr means entry b (then pool_size >= B). A slot outside
  * [0, pool_size) is not read or written: that stream starts from a zero state,
  * and la_workspace_status reports LA_ERR_INVALID_ARG afterwards.
+ * lens: device int[B] (4-byte aligned), stream b's token count n_b (clamped to
+ * [0, N]): only its first n_b tokens are read and its state advances by n_b;
+ * out rows at or past n_b are unspecified, and the padding rows of q, k, v may
+ * hold anything. nullptr: every stream has N tokens.
  * Workspace: la_forward_workspace_bytes(B, H, N, D, M, 1, dtype).
  * N == 0 returns LA_OK without touching the pool.
  */
 int la_extend(const void* q, const void* k, const void* v, void* out,
-              float* S_pool, float* Z_pool, const int* slots, int pool_size,
-              int B, int H, int N, int D, int M, int dtype,
+              float* S_pool, float* Z_pool, const int* slots, const int* lens,
+              int pool_size, int B, int H, int N, int D, int M, int dtype,
               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Scratch needed by la_backward for this shape, in bytes. */

@@ -37,7 +37,7 @@ _SIGNATURES = {
     "la_backward_workspace_bytes": (_c_size, [_c_int] * 7),
     "la_forward": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_prefill": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
-    "la_extend": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
+    "la_extend": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_backward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
@@ -190,12 +190,14 @@ def la_prefill(q, k, v, out=None, S=None, Z=None, workspace=None):
     return out, S, Z
 
 
-def la_extend(q, k, v, S_pool, Z_pool, slots=None, out=None, workspace=None):
-    """Causal forward over N new tokens of B streams continuing from stored state.
+def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspace=None):
+    """Causal forward over new tokens of B streams continuing from stored state.
 
     S_pool [P,H,D,M], Z_pool [P,H,D] float32 hold per-stream states; stream b uses
     entry slots[b] (int32 device tensor of B distinct entries; None: entry b) and
-    its entry is advanced past the N tokens in place. Returns out [B,H,N,M].
+    its entry is advanced past its tokens in place: the first lens[b] of the N
+    (int32 device tensor; None: all N). Returns out [B,H,N,M]; rows at or past
+    lens[b] are unspecified.
     """
     import torch
     lib = load_library()
@@ -206,14 +208,16 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, out=None, workspace=None):
     dev = q.device
     out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
     _need_cuda(out)
-    if slots is not None:
-        _need_cuda(slots)
-        if slots.dtype != torch.int32 or slots.numel() != B or not slots.is_contiguous():
-            raise ValueError("slots must be a contiguous int32 tensor of B entries")
+    for name, t in (("slots", slots), ("lens", lens)):
+        if t is not None:
+            _need_cuda(t)
+            if t.dtype != torch.int32 or t.numel() != B:
+                raise ValueError(f"{name} must be a contiguous int32 tensor of B entries")
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
     ws = _workspace(nbytes, dev, workspace)
     st = lib.la_extend(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S_pool.data_ptr(),
-                       Z_pool.data_ptr(), 0 if slots is None else slots.data_ptr(), S_pool.shape[0],
+                       Z_pool.data_ptr(), 0 if slots is None else slots.data_ptr(),
+                       0 if lens is None else lens.data_ptr(), S_pool.shape[0],
                        B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
                        _stream_ptr(dev))
     _check("la_extend", st)

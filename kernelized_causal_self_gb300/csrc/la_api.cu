@@ -130,12 +130,14 @@ int la_prefill(const void* q, const void* k, const void* v, void* out, float* S,
 }
 
 int la_extend(const void* q, const void* k, const void* v, void* out, float* S_pool,
-              float* Z_pool, const int* slots, int pool_size, int B, int H, int N, int D, int M,
-              int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+              float* Z_pool, const int* slots, const int* lens, int pool_size, int B, int H,
+              int N, int D, int M, int dtype, void* workspace, size_t workspace_bytes,
+              void* stream) {
   if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
   if (!ptrs_ok({S_pool, Z_pool})) return LA_ERR_INVALID_ARG;
   if (slots == nullptr ? pool_size < B : pool_size < 1) return LA_ERR_INVALID_ARG;
   if (slots != nullptr && (reinterpret_cast<uintptr_t>(slots) & 3u) != 0) return LA_ERR_INVALID_ARG;
+  if (lens != nullptr && (reinterpret_cast<uintptr_t>(lens) & 3u) != 0) return LA_ERR_INVALID_ARG;
   if (N == 0) return LA_OK;
   if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
   const size_t need = la_forward_workspace_bytes(B, H, N, D, M, 1, dtype);
@@ -151,6 +153,7 @@ int la_extend(const void* q, const void* k, const void* v, void* out, float* S_p
   io.H = H;
   io.pool = pool_size;
   io.read_init = true;
+  io.lens = lens;
   if (la::tc_forward_supported(D, M, dtype))
     return from_cuda(la::tc_forward(q, k, v, out, io, B * H, N, true, workspace, st));
   return from_cuda(la::simt_forward(q, k, v, out, io, B * H, N, D, M, true, dtype,

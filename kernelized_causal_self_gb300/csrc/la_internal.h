@@ -21,6 +21,8 @@ struct StateIO {
   int H = 1;
   int pool = 0;
   bool read_init = false;
+  // per-stream token counts (device int[B], each clamped to [0, N]); nullptr: all N
+  const int* lens = nullptr;
 };
 
 // Adds n to the process-wide kernel launch count reported by la_kernel_launches().

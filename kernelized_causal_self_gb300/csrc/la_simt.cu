@@ -100,6 +100,8 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     if (!entry_ok && threadIdx.x == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
   }
   const bool init = entry_ok && io.read_init;
+  // this stream's token count (the rest of the sequence is padding, never read)
+  if (io.lens != nullptr) N = max(0, min(io.lens[bh / io.H], N));
   for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = init ? io.S[entry * D * M + e] : 0.f;
   for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = init ? io.Z[entry * D + e] : 0.f;
   __syncthreads();

@@ -24,6 +24,10 @@ constexpr int kStateFloats = kDim * kDim + kDim;  // S^T [m][d] then Z [d]
 
 struct Geometry {
   int BH, N, n_chunks, seg_chunks, n_seg;
+  // forward only: stream b = bh / H uses its first lens[b] tokens (nullptr: all N)
+  const int* lens = nullptr;
+  int H = 1;
+  __device__ int len(int bh) const { return lens ? max(0, min(lens[bh / H], N)) : N; }
   __host__ __device__ int n_items() const { return BH * n_seg; }
   // item -> (bh, seg): segment-major so that a segment's predecessors were
   // scheduled earlier
@@ -129,6 +133,16 @@ __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nval
     for (int q = 0; q < 4; ++q) u[q] = valid ? (EXACT ? phi2_bf16_exact(u[q]) : phi2_bf16(u[q])) : 0u;
     *p = make_uint4(u[0], u[1], u[2], u[3]);
   }
+}
+
+// Zeroes this thread's half of tile row `row` (columns [32h, 32h + 32)) when the
+// row is past the valid rows: rows beyond a sequence's length may hold any bits
+// (even NaN), and a zero weight times NaN is still NaN.
+__device__ __forceinline__ void zero_half_if_past(uint8_t* tile, int row, int h, int nvalid) {
+  if (row < nvalid) return;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + sw128(row, (4 * h + c) * 16)) = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int row, int h,

@@ -100,7 +100,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int item = cc.item;
     const int bh = g.bh_of(item);
     const bool first = cc.chunk == g.chunk_begin(item);
-    const int nvalid = min(kC, g.N - cc.chunk * kC);
+    const int nvalid = min(kC, g.len(bh) - cc.chunk * kC);
     const bool last = cc.chunk + 1 == g.chunk_end(item);
     if (tid == 0 && cp.valid(g)) issue(cp);
     const int s = consumed % kStateStages;
@@ -114,6 +114,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       phi_half_split(kt, klo, trow, h, nvalid, zacc);
     else
       phi_half<true>(kt, trow, h, nvalid);
+    if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -392,7 +393,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int bh = g.bh_of(item);
     const int t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_begin(item);
-    const int nvalid = min(kC, g.N - t0);
+    const int nvalid = min(kC, g.len(bh) - t0);
     if (!CAUSAL && tid == 0 && cp.valid(g)) {  // causal: issued after the first MMA group
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
       issue(cp);
@@ -458,7 +459,10 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // denominator alike and largely cancels in out = num / den; phi(K) exact, since
     // the state sums phi(K) v^T over random-sign v (padded query rows are never stored)
     phi_half(qt, row, h, kC);
-    if (CAUSAL) phi_half<true>(kt, row, h, nvalid);
+    if (CAUSAL) {
+      phi_half<true>(kt, row, h, nvalid);
+      if (nvalid < kC) zero_half_if_past(vt, row, h, nvalid);
+    }
     fence_proxy_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -694,7 +698,9 @@ size_t tc_forward_workspace(int BH, int N) {
 
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
                        int BH, int N, bool causal, void* ws, cudaStream_t st) {
-  const Geometry g = make_geometry(BH, N);
+  Geometry g = make_geometry(BH, N);
+  g.lens = io.lens;
+  g.H = io.H;
   WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
   float* prefix = partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;

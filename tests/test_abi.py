@@ -85,15 +85,16 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, wsb=16) == la.LA_ERR_WORKSPACE
 
 
-def _ext(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, S=FAKE, Z=FAKE, slots=FAKE, pool=4, B=2, H=1, N=16,
-         D=64, M=64, dtype=1, ws=FAKE, wsb=1 << 20):
-    return lib.la_extend(q, k, v, out, S, Z, slots, pool, B, H, N, D, M, dtype, ws, wsb, None)
+def _ext(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, S=FAKE, Z=FAKE, slots=FAKE, lens=FAKE, pool=4, B=2,
+         H=1, N=16, D=64, M=64, dtype=1, ws=FAKE, wsb=1 << 20):
+    return lib.la_extend(q, k, v, out, S, Z, slots, lens, pool, B, H, N, D, M, dtype, ws, wsb, None)
 
 
 def test_extend_rejects_bad_arguments(lib):
     assert _ext(lib, S=0) == la.LA_ERR_INVALID_ARG
     assert _ext(lib, Z=ODD) == la.LA_ERR_INVALID_ARG
     assert _ext(lib, slots=FAKE + 2) == la.LA_ERR_INVALID_ARG        # slots must be 4-byte aligned
+    assert _ext(lib, lens=FAKE + 2) == la.LA_ERR_INVALID_ARG         # lens too
     assert _ext(lib, pool=0) == la.LA_ERR_INVALID_ARG
     assert _ext(lib, slots=0, pool=1, B=2) == la.LA_ERR_INVALID_ARG  # identity slots need B entries
     assert _ext(lib, D=12) == la.LA_ERR_INVALID_ARG

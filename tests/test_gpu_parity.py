@@ -221,6 +221,39 @@ def test_extend_from_pool_state(la, case):
     assert np.array_equal(got_Z[untouched], Z0[untouched].astype(np.float32))
 
 
+LENS = [(4, 2, 300, 64, 64, inputs.BF16, (300, 129, 0, 257)),
+        (4, 2, 100, 64, 64, inputs.BF16, (100, 1, 37, 0)),
+        (2, 3, 45, 32, 48, inputs.F32, (45, 12))]
+
+
+@pytest.mark.parametrize("case", LENS, ids=lambda s: "b%dh%dn%dd%dm%d-%s" % s[:6])
+def test_extend_per_stream_lengths(la, case):
+    """Streams advance by different token counts in one call; the padding rows
+    past each count hold NaN and must not reach anything that is kept."""
+    B, H, N, D, M, dt, lens = case
+    scale = 0.125 if dt == inputs.BF16 else 1.0
+    q, k, v = inputs.qkv(840 + N, B, H, N, D, M, scale, dt)
+    S0 = np.abs(inputs.normal(841, (B, H, D, M), 1.0, inputs.F32, 0))
+    Z0 = np.abs(inputs.normal(841, (B, H, D), 1.0, inputs.F32, 1)) + 1.0
+    pq, pk, pv = q.copy(), k.copy(), v.copy()
+    for b, n in enumerate(lens):
+        pq[b, :, n:] = np.nan
+        pk[b, :, n:] = np.nan
+        pv[b, :, n:] = np.nan
+    tS, tZ = _t(S0, inputs.F32), _t(Z0, inputs.F32)
+    out = la.la_extend(_t(pq, dt), _t(pk, dt), _t(pv, dt), tS, tZ,
+                       lens=torch.tensor(lens, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    got_S, got_Z = tS.cpu().numpy(), tZ.cpu().numpy()
+    for b, n in enumerate(lens):
+        want, S_ref, Z_ref = oracle.recurrent_attention(q[b, :, :n], k[b, :, :n], v[b, :, :n],
+                                                        S0[b], Z0[b])
+        if n:
+            assert_close(out[b, :, :n].float().cpu().numpy(), want, dt, f"out[{b}]")
+        assert_close(got_S[b], S_ref, dt, f"S[{b}]")
+        assert_close(got_Z[b], Z_ref, dt, f"Z[{b}]")
+
+
 def test_prefill_then_extend_matches_forward(la):
     """Prefill of the first 1000 tokens, then two extensions of 257 and 129:
     outputs and final state as one causal forward / prefill over all 1386."""
