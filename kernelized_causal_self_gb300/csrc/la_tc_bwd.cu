@@ -313,14 +313,23 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (sl <= q4) {
             uint32_t rp[32], rw[32];
             tmem_ld32x2(tl + kFP + 32 * sl, rp, tl + kFW + 32 * sl, rw);
-            const bool diag = sl == q4;
+            if (sl < q4) {  // below the diagonal block: nothing is masked (warp-uniform)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const bool keep = !diag || 32 * sl + c <= row;
-              const float p = keep ? __uint_as_float(rp[c]) : 0.f;
-              wv[t][c] = keep ? __uint_as_float(rw[c]) : 0.f;
-              dpart += p;
-              npart += p * wv[t][c];
+              for (int c = 0; c < 32; ++c) {
+                const float p = __uint_as_float(rp[c]);
+                wv[t][c] = __uint_as_float(rw[c]);
+                dpart += p;
+                npart += p * wv[t][c];
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const bool keep = 32 * sl + c <= row;
+                const float p = keep ? __uint_as_float(rp[c]) : 0.f;
+                wv[t][c] = keep ? __uint_as_float(rw[c]) : 0.f;
+                dpart += p;
+                npart += p * wv[t][c];
+              }
             }
           } else {
 #pragma unroll
@@ -383,14 +392,20 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int t = 0; t < 2; ++t) {
         const int sl = 2 * h + t;
         uint32_t th[16], tlo[16];
-        const bool diag = sl == q4;
+        if (sl < q4) {  // warp-uniform: full slice, diagonal slice, or all zero
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int j0 = 32 * sl + 2 * c;
-          const bool k0 = sl < q4 || (diag && j0 <= row);
-          const bool k1 = sl < q4 || (diag && j0 + 1 <= row);
-          split_bf16(k0 ? wv[t][2 * c] * inv + gd : 0.f, k1 ? wv[t][2 * c + 1] * inv + gd : 0.f,
-                     th[c], tlo[c]);
+          for (int c = 0; c < 16; ++c)
+            split_bf16(wv[t][2 * c] * inv + gd, wv[t][2 * c + 1] * inv + gd, th[c], tlo[c]);
+        } else if (sl == q4) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int j0 = 32 * sl + 2 * c;
+            split_bf16(j0 <= row ? wv[t][2 * c] * inv + gd : 0.f,
+                       j0 + 1 <= row ? wv[t][2 * c + 1] * inv + gd : 0.f, th[c], tlo[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
         }
         tmem_st16(tl + kFW + 16 * sl, th);
         tmem_st16(tl + kFW + 64 + 16 * sl, tlo);
@@ -562,19 +577,25 @@ __device__ __forceinline__ void masked_split_slices(uint32_t taddr, int h, int q
     if (any) {
       uint32_t r[32];
       tmem_ld32(taddr + 32 * sl, r);
-      const bool diag = sl == q4;
+      if (sl != q4) {  // off the diagonal block: nothing is masked (warp-uniform)
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int j0 = 32 * sl + 2 * c;
-        bool k0 = true, k1 = true;
-        if (diag) {
-          k0 = LOWER ? j0 <= row : j0 >= row;
-          k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
+        for (int c = 0; c < 16; ++c) {
+          const float a = __uint_as_float(r[2 * c]) + add;
+          const float b = __uint_as_float(r[2 * c + 1]) + add;
+          split_bf16(a, b, hi[t][c], lo[t][c]);
+          sum += a + b;
         }
-        const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
-        const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
-        split_bf16(a, b, hi[t][c], lo[t][c]);
-        sum += a + b;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int j0 = 32 * sl + 2 * c;
+          const bool k0 = LOWER ? j0 <= row : j0 >= row;
+          const bool k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
+          const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
+          const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
+          split_bf16(a, b, hi[t][c], lo[t][c]);
+          sum += a + b;
+        }
       }
     } else {
 #pragma unroll
@@ -787,14 +808,22 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (sl >= q4) {
           uint32_t r[32];
           tmem_ld32(tl + kRT + 32 * sl, r);
-          const bool diag = sl == q4;
+          if (sl != q4) {  // below the diagonal block: nothing is masked (warp-uniform)
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int i0 = 32 * sl + 2 * c;
-            const bool k0 = !diag || i0 >= row, k1 = !diag || i0 + 1 >= row;
-            split_bf16(k0 ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
-                       k1 ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
-                       pth[t][c], ptl[t][c]);
+            for (int c = 0; c < 16; ++c) {
+              const int i0 = 32 * sl + 2 * c;
+              split_bf16(__uint_as_float(r[2 * c]) * invs[i0] + gds[i0],
+                         __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1], pth[t][c],
+                         ptl[t][c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int i0 = 32 * sl + 2 * c;
+              split_bf16(i0 >= row ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
+                         i0 + 1 >= row ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
+                         pth[t][c], ptl[t][c]);
+            }
           }
         } else {
 #pragma unroll
