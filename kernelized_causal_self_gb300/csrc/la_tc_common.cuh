@@ -121,9 +121,9 @@ __device__ __forceinline__ uint32_t phi2_bf16_exact(uint32_t u) {
 
 // Half-row variants for kernels where two warpgroups share each row: half h
 // owns the logical 16-byte chunks [4h, 4h + 4), i.e. columns [32h, 32h + 32).
-template <bool EXACT = false>
-__device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nvalid) {
-  const bool valid = row < nvalid;
+template <bool EXACT, bool MASK>
+__device__ __forceinline__ void phi_half_impl(uint8_t* tile, int row, int h, int nvalid) {
+  const bool valid = !MASK || row < nvalid;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, (4 * h + c) * 16));
@@ -133,6 +133,16 @@ __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nval
     for (int q = 0; q < 4; ++q) u[q] = valid ? (EXACT ? phi2_bf16_exact(u[q]) : phi2_bf16(u[q])) : 0u;
     *p = make_uint4(u[0], u[1], u[2], u[3]);
   }
+}
+
+// (the row mask is applied only in a tile with padding rows; nvalid is the
+// same for the whole CTA, so the branch is uniform)
+template <bool EXACT = false>
+__device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nvalid) {
+  if (nvalid >= kC)
+    phi_half_impl<EXACT, false>(tile, row, h, nvalid);
+  else
+    phi_half_impl<EXACT, true>(tile, row, h, nvalid);
 }
 
 // Zeroes this thread's half of tile row `row` (columns [32h, 32h + 32)) when the
@@ -145,9 +155,10 @@ __device__ __forceinline__ void zero_half_if_past(uint8_t* tile, int row, int h,
     *reinterpret_cast<uint4*>(tile + sw128(row, (4 * h + c) * 16)) = make_uint4(0, 0, 0, 0);
 }
 
-__device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int row, int h,
-                                               int nvalid, float (&z)[32]) {
-  const bool valid = row < nvalid;
+template <bool MASK>
+__device__ __forceinline__ void phi_half_split_impl(uint8_t* tile, uint8_t* lo, int row, int h,
+                                                    int nvalid, float (&z)[32]) {
+  const bool valid = !MASK || row < nvalid;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t off = sw128(row, (4 * h + c) * 16);
@@ -166,6 +177,14 @@ __device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int r
     *p = make_uint4(u[0], u[1], u[2], u[3]);
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
   }
+}
+
+__device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int row, int h,
+                                               int nvalid, float (&z)[32]) {
+  if (nvalid >= kC)
+    phi_half_split_impl<false>(tile, lo, row, h, nvalid, z);
+  else
+    phi_half_split_impl<true>(tile, lo, row, h, nvalid, z);
 }
 
 // Sum z[32] over the 32 lanes of a warp; lane l ends with column l.
