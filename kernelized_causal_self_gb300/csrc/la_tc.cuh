@@ -305,5 +305,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // box of [b2][b1][b0] and 128-byte swizzle; zero fill out of bounds.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t b0, uint32_t b1, uint32_t b2);
+// The same over a float32 tensor (the box's inner extent b0 * 4 bytes must be <= 128).
+bool make_tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint32_t b0, uint32_t b1, uint32_t b2);
 
 }  // namespace la

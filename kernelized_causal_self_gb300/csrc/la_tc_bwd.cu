@@ -615,9 +615,9 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kBT, 1)
 tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                 const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                  Geometry g, const float* __restrict__ rsuffix, const float* __restrict__ den_in,
-                 const float* __restrict__ gd_in, float* __restrict__ dk, float* __restrict__ dv,
-                 WorkspaceHeader* hdr) {
+                 const float* __restrict__ gd_in, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   BwdSmem sm(smraw);
   // the state snapshot buffers hold R rows d (m contiguous)
@@ -690,7 +690,12 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
     const int nvalid = min(kC, g.N - t0);
-    if (tid == 0 && cp.valid(g)) issue(cp);
+    if (tid == 0) {
+      // the stage being refilled and the phi(Q) lo tile held the previous chunk's
+      // dk / dv staging: its TMA stores must have read them
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
+    }
     if (CAUSAL && tid < kC) {
       invs[tid] = 1.f / nden;
       gds[tid] = ngd;
@@ -864,8 +869,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
     }
 
-    // dk = (dphiK + r_next) * phi'(k), dv; this half's columns, staged through the
-    // spent V / G tiles (warps 0-3 / 4-7)
+    // dk = (dphiK + r_next) * phi'(k) and dv, this half's columns, staged as 128 x 32
+    // float32 boxes (128-byte swizzle) for TMA stores: dk in the spent V / G tiles, dv in
+    // the spent phi(Q) hi / lo tiles (the R MMAs that read those ran before the second
+    // group, whose completion was awaited)
     {
       uint32_t r[32], w[32];
       tmem_ld32x2(tl + kRK + 32 * h, r, tl + kRV + 32 * h, w);
@@ -879,12 +886,25 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           o[16 * c + q] =
               (__uint_as_float(r[16 * c + q]) + rsnap[32 * h + 16 * c + q]) * fminf(kv[q], 1.f);
       }
-      float4* stage = reinterpret_cast<float4*>((h == 0 ? vt : gt) + q4 * 4096);
-      const size_t off = ((size_t)bh * g.N + t0) * kDim + 32 * h;
-      store_half_rows(dk + off, row, nvalid, o, stage);
+      uint8_t* sk = h == 0 ? vt : gt;
+      uint8_t* sv = h == 0 ? qt : sm.qlo;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(w[q]);
-      store_half_rows(dv + off, row, nvalid, o, stage);
+      for (int c = 0; c < 8; ++c) {
+        *reinterpret_cast<float4*>(sk + sw128(row, c * 16)) =
+            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        *reinterpret_cast<float4*>(sv + sw128(row, c * 16)) =
+            make_float4(__uint_as_float(w[4 * c]), __uint_as_float(w[4 * c + 1]),
+                        __uint_as_float(w[4 * c + 2]), __uint_as_float(w[4 * c + 3]));
+      }
+    }
+    fence_proxy_async_smem();
+    sync_tc();
+    if (tid == 0) {  // rows past the sequence end are clipped by the tensor maps
+      tma_store_3d(&tm_dk, vt, 0, t0, bh);
+      tma_store_3d(&tm_dk, gt, 32, t0, bh);
+      tma_store_3d(&tm_dv, qt, 0, t0, bh);
+      tma_store_3d(&tm_dv, sm.qlo, 32, t0, bh);
+      bulk_commit();
     }
     if (CAUSAL) {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
       if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
@@ -926,6 +946,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 36);
       ++consumed;
     }
+    bulk_wait_all<0>();
   }
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
@@ -959,12 +980,14 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   float* den = reinterpret_cast<float*>(base + 4 * sb);
   float* gd = den + align_up(sizeof(float) * (size_t)BH * N, 256) / sizeof(float);
 
-  CUtensorMap tq, tk, tv, tg;
+  CUtensorMap tq, tk, tv, tg, tdk, tdv;
   const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
   if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
-      !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1))
+      !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_f32_3d(&tdk, dk, kDim, n, bh, 32, kC, 1) ||
+      !make_tmap_f32_3d(&tdv, dv, kDim, n, bh, 32, kC, 1))
     return cudaErrorInvalidValue;
 
   cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, true, st);
@@ -990,8 +1013,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, g,
-                     (const float*)rsuffix, (const float*)den, (const float*)gd, dk, dv, hdr);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, tdk, tdv, g,
+                     (const float*)rsuffix, (const float*)den, (const float*)gd, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
