@@ -119,31 +119,6 @@ __device__ __forceinline__ void store_split_half(uint8_t* hi_buf, uint8_t* lo_bu
   }
 }
 
-// Stores this thread's 32 floats (chunk row `row`, columns [32h, 32h + 32)) of
-// a [rows][64] float32 output. The warp passes its 32 half-rows through a
-// private 4 KB staging area (XOR-swizzled, conflict-free), so that each store
-// instruction writes four whole 128-byte row segments instead of 32 scattered
-// 16-byte pieces. `out_row0` points at column 32h of the chunk's row 0; rows
-// >= nvalid are not written.
-__device__ __forceinline__ void store_half_rows(float* out_row0, int row, int nvalid,
-                                                const float (&x)[32], float4* stage) {
-  const int lane = threadIdx.x & 31;
-  const int base = row - lane;  // first row of this warp
-#pragma unroll
-  for (int f = 0; f < 8; ++f)
-    stage[lane * 8 + (f ^ (lane & 7))] =
-        make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
-  __syncwarp();
-  const int f = lane & 7;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int r = 4 * k + (lane >> 3);
-    const float4 v = stage[r * 8 + (f ^ (r & 7))];
-    if (base + r < nvalid) reinterpret_cast<float4*>(out_row0 + (size_t)(base + r) * kDim)[f] = v;
-  }
-  __syncwarp();
-}
-
 __device__ __forceinline__ void sync_tc() {
   fence_before_sync();
   __syncthreads();
@@ -173,9 +148,9 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kBT, 1)
 tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                Geometry g, const float* __restrict__ sprefix, float* __restrict__ rpartial,
-                float* __restrict__ dq, float* __restrict__ den_out, float* __restrict__ gd_out,
-                WorkspaceHeader* hdr) {
+                const __grid_constant__ CUtensorMap tm_dq, Geometry g,
+                const float* __restrict__ sprefix, float* __restrict__ rpartial,
+                float* __restrict__ den_out, float* __restrict__ gd_out, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   BwdSmem sm(smraw);
   float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
@@ -236,7 +211,12 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool first = cc.chunk == g.chunk_begin(item);
     const bool last = cc.chunk + 1 == g.chunk_end(item);
     const int nvalid = min(kC, g.N - t0);
-    if (tid == 0 && cp.valid(g)) issue(cp);
+    if (tid == 0) {
+      // the stage being refilled and the phi(K) lo tile held the previous chunk's dq
+      // staging: its TMA stores must have read them
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
+    }
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this half
@@ -466,7 +446,8 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     fence_after_sync();
 
     // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns,
-    // staged through the spent phi(K) tiles (warps 0-3: K tile, 4-7: its lo part)
+    // staged as a 128 x 32 float32 box (128-byte swizzle) for a TMA store in the spent
+    // phi(K) tiles (warps 0-3: K tile, 4-7: its lo part)
     {
       uint32_t r[32];
       tmem_ld32(tl + kFQ + 32 * h, r);
@@ -480,8 +461,18 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           o[16 * c + q] =
               (__uint_as_float(r[16 * c + q]) + gd * zsnap[32 * h + 16 * c + q]) * fminf(qv[q], 1.f);
       }
-      float4* stage = reinterpret_cast<float4*>((h == 0 ? kt : sm.klo) + q4 * 4096);
-      store_half_rows(dq + ((size_t)bh * g.N + t0) * kDim + 32 * h, row, nvalid, o, stage);
+      uint8_t* sq = h == 0 ? kt : sm.klo;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(sq + sw128(row, c * 16)) =
+            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    sync_tc();
+    if (tid == 0) {  // rows past the sequence end are clipped by the tensor map
+      tma_store_3d(&tm_dq, kt, 0, t0, bh);
+      tma_store_3d(&tm_dq, sm.klo, 32, t0, bh);
+      bulk_commit();
     }
     // state MMAs of this chunk: the second group's barrier also covers dS,
     // issued earlier by the same thread
@@ -552,6 +543,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 26);
       ++consumed;
     }
+    bulk_wait_all<0>();
   }
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
@@ -980,12 +972,13 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   float* den = reinterpret_cast<float*>(base + 4 * sb);
   float* gd = den + align_up(sizeof(float) * (size_t)BH * N, 256) / sizeof(float);
 
-  CUtensorMap tq, tk, tv, tg, tdk, tdv;
+  CUtensorMap tq, tk, tv, tg, tdq, tdk, tdv;
   const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
   if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_f32_3d(&tdq, dq, kDim, n, bh, 32, kC, 1) ||
       !make_tmap_f32_3d(&tdk, dk, kDim, n, bh, 32, kC, 1) ||
       !make_tmap_f32_3d(&tdv, dv, kDim, n, bh, 32, kC, 1))
     return cudaErrorInvalidValue;
@@ -1000,8 +993,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, g,
-                     (const float*)sprefix, rpartial, dq, den, gd, hdr);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, tdq, g,
+                     (const float*)sprefix, rpartial, den, gd, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
