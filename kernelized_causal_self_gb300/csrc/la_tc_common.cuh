@@ -244,6 +244,31 @@ __device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
   return make_float2(z[0], z[1]);
 }
 
+// Bounded wait that also gives up once another thread of the CTA has given up
+// (a shared abort flag), so that one timeout winds the whole CTA down; for
+// kernels whose warps wait on different barriers at different times.
+__device__ __forceinline__ bool mbar_wait_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                WorkspaceHeader* hdr, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_timeout(hdr, site);
+      return false;
+    }
+  }
+}
+
+// The same, agreed by the whole warp (warp-collective TMEM accesses follow).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               WorkspaceHeader* hdr, int site) {
+  return __all_sync(0xffffffffu, mbar_wait_abort(bar, parity, abort, hdr, site));
+}
+
 // Block-uniform bounded wait: every thread waits, then all agree on the outcome
 // (a timeout seen by any thread ends the loop for the whole CTA together).
 __device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, WorkspaceHeader* hdr,

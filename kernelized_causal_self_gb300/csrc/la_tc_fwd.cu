@@ -30,11 +30,19 @@ namespace tcx {
 
 // ------------------------------------------------------- 1. segment states
 
-constexpr int kStateStages = 2;
-constexpr int kStateThreads = 256;  // two threads per tile row (column halves), 2 CTAs per SM
+constexpr int kStateWorkers = 256;  // two threads per tile row (column halves)
+constexpr int kStateThreads = kStateWorkers + 32;  // + one control warp; 2 CTAs per SM
+// Eight worker warps apply phi to the K tiles as they land; one control thread
+// issues the loads and the MMAs, each as soon as what it needs is done (a
+// stage is refilled once the MMAs that read it are done). A segment's sums land
+// in one of two TMEM accumulators and are read out while the next one fills.
+template <bool PRECISE>
+constexpr int state_stages() { return PRECISE ? 2 : 3; }
+template <bool PRECISE>
+constexpr int state_stage_bytes() { return (PRECISE ? 3 : 2) * kTile; }  // K, V (, phi(K) lo)
 template <bool PRECISE>
 constexpr int state_smem() {
-  return 1024 + kStateStages * 2 * kTile + (PRECISE ? kTile : 0) + 2048 + 2048;
+  return 1024 + state_stages<PRECISE>() * state_stage_bytes<PRECISE>() + 2048 + 256 + 256;
 }
 
 // PRECISE: phi(K) enters the MMA as a bf16 hi + lo pair and dZ sums the
@@ -43,22 +51,35 @@ template <bool PRECISE>
 __global__ void __launch_bounds__(kStateThreads, 2)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
+  constexpr int S = state_stages<PRECISE>(), SB = state_stage_bytes<PRECISE>();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = sm;  // [stage][K tile | V tile]
-  uint8_t* klo = sm + kStateStages * 2 * kTile;  // phi(K) lo part (PRECISE)
-  uint8_t* ones = klo + (PRECISE ? kTile : 0);   // 2 KB of bf16 ones (B operand of dZ)
-  uint8_t* misc = ones + 2048;
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc);          // kStateStages
-  uint64_t* mma_bar = full + kStateStages;                      // 1
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  uint8_t* stages = sm;                        // [stage][K tile | V tile (| phi(K) lo)]
+  uint8_t* ones = stages + S * SB;             // 16 x 64 bf16 ones (the stacked block of dZ)
+  float* zx = reinterpret_cast<float*>(ones + 2048);  // 64 floats: dZ lo parts (PRECISE)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 2048 + 256);  // S: tiles landed
+  uint64_t* empty = full + S;                  // S: the chunk's MMAs are done with the stage
+  uint64_t* phid = empty + S;                  // S: every worker's phi of the stage is in
+  uint64_t* segbar = phid + S;                 // 2: a segment's last MMAs are done
+  uint64_t* xbar = segbar + 2;                 // readout exchange (PRECISE), 256 arrivals
+  uint64_t* drain = xbar + 1;                  // every MMA of the CTA is done
+  volatile int* abort = reinterpret_cast<volatile int*>(drain + 1);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int q4 = warp & 3, h = warp >> 2;
-  const int trow = q4 * 32 + lane;  // tile row of this thread (column half h)
+  const int q4 = warp & 3, h = (warp >> 2) & 1;
+  const int trow = q4 * 32 + lane;  // tile row of this worker (column half h)
   if (tid == 0) {
-    for (int s = 0; s < kStateStages; ++s) mbar_init(&full[s], 1);
-    mbar_init(mma_bar, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&phid[s], kStateWorkers);
+    }
+    mbar_init(&segbar[0], 1);
+    mbar_init(&segbar[1], 1);
+    mbar_init(xbar, kStateWorkers);
+    mbar_init(drain, 1);
+    *abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -66,8 +87,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   for (int e = tid; e < 2048 / 16; e += blockDim.x)
     reinterpret_cast<uint4*>(ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_proxy_async_smem();
-  if (warp == 0) {
-    tmem_alloc(tslot, 128);  // [0, 64): dS^T, [64, 80): dZ (both M = 64 layout)
+  if (warp == kStateWorkers / 32) {
+    tmem_alloc(tslot, 256);  // accumulator p (segment parity) in columns [128 p, 128 p + 80)
     tmem_relinquish();
   }
   fence_before_sync();
@@ -76,163 +97,205 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const uint32_t tbase = *tslot;
   pdl_wait();
 
-  Cursor cc, cp;
-  cc.start(g);
-  cp.start(g);
-  long long issued = 0;
-  auto issue = [&](Cursor& c) {
-    const int s = issued % kStateStages;
-    uint8_t* st = stages + s * 2 * kTile;
-    mbar_arrive_expect_tx(&full[s], 2 * kTile);
-    tma_load_3d(st, &tm_k, &full[s], 0, c.chunk * kC, g.bh_of(c.item));
-    tma_load_3d(st + kTile, &tm_v, &full[s], 0, c.chunk * kC, g.bh_of(c.item));
-    ++issued;
-    c.advance(g);
-  };
-  if (tid == 0)
-    for (int i = 0; i < kStateStages - 1 && cp.valid(g); ++i) issue(cp);
-
-  bool ok = true;
-  long long consumed = 0;
-  uint32_t mma_phase = 0;
-  float zacc[32];
-  while (cc.valid(g) && ok) {
-    const int item = cc.item;
-    const int bh = g.bh_of(item);
-    const bool first = cc.chunk == g.chunk_begin(item);
-    const int nvalid = min(kC, g.len(bh) - cc.chunk * kC);
-    const bool last = cc.chunk + 1 == g.chunk_end(item);
-    if (tid == 0 && cp.valid(g)) issue(cp);
-    const int s = consumed % kStateStages;
-    uint8_t* kt = stages + s * 2 * kTile;
-    uint8_t* vt = kt + kTile;
-    if (!wait_uniform(&full[s], (consumed / kStateStages) & 1, hdr, 1)) {
-      ok = false;
-      break;
-    }
-    if (PRECISE)
-      phi_half_split(kt, klo, trow, h, nvalid, zacc);
-    else
-      phi_half<true>(kt, trow, h, nvalid);
-    if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
-    fence_proxy_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    if (tid == 0) {
-      const uint32_t va = smem_u32(vt), ka = smem_u32(kt), kl = smem_u32(klo);
+  if (warp == kStateWorkers / 32) {
+    // ------------------------------------------------------------- control
+    if (lane == 0) {
+      Cursor cl, cm;  // next chunk to load, next chunk to multiply
+      cl.start(g);
+      cm.start(g);
+      long long total = 0;
+      for (Cursor c = cl; c.valid(g); c.advance(g)) ++total;
+      long long nl = 0, nm = 0;
+      int nseg = 0;
       const uint32_t oa = smem_u32(ones);
-      if (PRECISE) {
-        // phi(K)^T hi and lo stacked as one M = 128 MN-major operand (its two
-        // 64-row halves are the hi and the lo tile, kl - ka bytes apart):
-        // dS = phi(K)^T V with rows d, hi parts in TMEM lanes 0-63 and lo parts
-        // in lanes 64-127, summed at the segment's end; dZ = phi(K)^T 1 alike.
-        const uint32_t lbo = kl - ka;
-        const uint32_t idS = idesc_bf16(128, 64, true, true);
+      uint64_t idle_since = globaltimer_ns();
+      while (nm < total) {
+        bool moved = false;
+        if (nm < nl && mbar_test_wait(&phid[nm % S], (uint32_t)((nm / S) & 1))) {
+          fence_after_sync();
+          const int s = (int)(nm % S);
+          const bool first = cm.chunk == g.chunk_begin(cm.item);
+          const bool last = cm.chunk + 1 == g.chunk_end(cm.item);
+          const uint32_t acc = tbase + 128 * (nseg & 1);
+          const uint32_t ka = smem_u32(stages + s * SB), va = ka + kTile, kl = ka + 2 * kTile;
+          // The ones block of an operand is 16 token rows: every K step of 16
+          // tokens reads the same block, its descriptor's leading byte offset
+          // measured from that step's start (oa - (va + 2048 k)).
+          if (PRECISE) {
+            // [phi(K)^T hi; phi(K)^T lo] (M = 128 MN-major, the two 64-row halves
+            // kl - ka bytes apart) times [V | 1] (N = 80 MN-major, columns 64.. from
+            // the ones block): dS with rows d in columns [0, 64) and dZ in column 64,
+            // hi parts in TMEM lanes 0-63 and lo parts in lanes 64-127
+            const uint32_t idS = idesc_bf16(128, 80, true, true);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS,
-                 (first && k == 0) ? 0u : 1u);
-        const uint32_t idz = idesc_bf16(128, 16, true, false);
+            for (int k = 0; k < kC / 16; ++k)
+              mma_ss(acc, sdesc(ka + k * 2048, kl - ka, 1024),
+                     sdesc(va + k * 2048, oa - (va + k * 2048), 1024), idS, (first && k == 0) ? 0u : 1u);
+          } else {
+            // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
+            // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+            const uint32_t idS = idesc_bf16(128, 64, true, true);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + 64, sdesc(ka + k * 2048, lbo, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
-                 idz, (first && k == 0) ? 0u : 1u);
-      } else {
-        const uint32_t id = idesc_bf16(64, 64, true, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024), id,
-                 (first && k == 0) ? 0u : 1u);
-        // dZ[d] += sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
-        const uint32_t idz = idesc_bf16(64, 16, true, false);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + 64, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024), idz,
-                 (first && k == 0) ? 0u : 1u);
-      }
-      mma_commit(mma_bar);
-    }
-    // the tile stage and dz are reused only after the MMA has consumed them
-    if (!wait_uniform(mma_bar, mma_phase, hdr, 2)) {
-      ok = false;
-      break;
-    }
-    mma_phase ^= 1;
-    fence_after_sync();
-    if (PRECISE && last) {
-      // M = 128 accumulators: lane r holds row d = r % 64 of the hi (r < 64) or
-      // the lo (r >= 64) part. The lo halves go through the spent K / V tiles
-      // (16 KB + 256 B); the hi-half threads add them and write S^T [m][d], Z.
-      float* dst = partial + (size_t)item * kStateFloats;
-      uint32_t r[32], r16[16];
-      tmem_ld32(lane_base(tbase) + h * 32, r);
-      tmem_ld16(lane_base(tbase) + 64, r16);
-      float4* xs = reinterpret_cast<float4*>(kt);  // [64][16] float4, XOR-swizzled rows
-      float* zs = reinterpret_cast<float*>(vt);
-      const int d = 32 * (q4 & 1) + lane;
-      if (q4 >= 2) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        if (h == 0) zs[d] = __uint_as_float(r16[0]);
-      }
-      __syncthreads();
-      if (q4 < 2) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
-          const int m = 32 * h + 4 * j;
-          dst[(m + 0) * kDim + d] = __uint_as_float(r[4 * j]) + lo.x;
-          dst[(m + 1) * kDim + d] = __uint_as_float(r[4 * j + 1]) + lo.y;
-          dst[(m + 2) * kDim + d] = __uint_as_float(r[4 * j + 2]) + lo.z;
-          dst[(m + 3) * kDim + d] = __uint_as_float(r[4 * j + 3]) + lo.w;
+            for (int k = 0; k < kC / 16; ++k)
+              mma_ss(acc, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                     sdesc(ka + k * 2048, 1024, 1024), idS, (first && k == 0) ? 0u : 1u);
+          }
+          mma_commit(&empty[s]);
+          if (last) mma_commit(&segbar[nseg++ & 1]);
+          cm.advance(g);
+          ++nm;
+          moved = true;
         }
-        if (h == 0) dst[kDim * kDim + d] = __uint_as_float(r16[0]) + zs[d];
+        if (nl < total && (nl < S || mbar_test_wait(&empty[nl % S], (uint32_t)(((nl - S) / S) & 1)))) {
+          const int s = (int)(nl % S);
+          uint8_t* st = stages + s * SB;
+          mbar_arrive_expect_tx(&full[s], 2 * kTile);
+          tma_load_3d(st, &tm_k, &full[s], 0, cl.chunk * kC, g.bh_of(cl.item));
+          tma_load_3d(st + kTile, &tm_v, &full[s], 0, cl.chunk * kC, g.bh_of(cl.item));
+          cl.advance(g);
+          ++nl;
+          moved = true;
+        }
+        if (moved) {
+          idle_since = globaltimer_ns();
+        } else if (*abort) {
+          break;
+        } else if (globaltimer_ns() - idle_since > kWaitLimitNs) {
+          *abort = 1;
+          record_timeout(hdr, 4);
+          break;
+        } else {
+          __nanosleep(32);
+        }
       }
-      fence_proxy_async_smem();  // before TMA refills the tiles used here
-      (void)bh;
-    } else if (last) {
-      float* dst = partial + (size_t)item * kStateFloats;
-      // M = 64 accumulator: row r sits in TMEM lane 32 * (r / 16) + r % 16;
-      // this thread writes columns [32h, 32h + 32) of row 16 * q4 + lane
-      uint32_t r[32];
-      const int row = q4 * 16 + lane;
-      tmem_ld32(lane_base(tbase) + h * 32, r);
-      if (lane < 16) {
-        float4* d4 = reinterpret_cast<float4*>(dst + row * kDim + h * 32);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      }
-      {
-        uint32_t r16[16];
-        tmem_ld16(lane_base(tbase) + 64, r16);
-        if (lane < 16 && h == 0) dst[kDim * kDim + row] = __uint_as_float(r16[0]);
-      }
-      (void)bh;
+      // every issued load lands and every MMA completes before the CTA lets go of
+      // its shared memory and TMEM (time-bounded only: not cut short by the abort flag)
+      for (long long k = nl > S ? nl - S : 0; k < nl; ++k)
+        if (!mbar_wait(&full[k % S], (uint32_t)((k / S) & 1))) record_timeout(hdr, 3);
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0)) record_timeout(hdr, 5);
     }
-    fence_before_sync();
-    __syncthreads();
-    ++consumed;
-    cc.advance(g);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- workers
+    uint32_t xphase = 0;
+    // a segment's sums -> partial[item]; xbuf: a free 16 KB tile (PRECISE)
+    auto readout = [&](int item, int p, uint8_t* xbuf) -> bool {
+      float* dst = partial + (size_t)item * kStateFloats;
+      const uint32_t acc = lane_base(tbase) + 128 * p;
+      uint32_t r[32];
+      tmem_ld32(acc + h * 32, r);
+      if (PRECISE) {
+        // lane r holds row d = r % 64 of the hi (r < 64) or the lo (r >= 64)
+        // part: dS in columns [0, 64), dZ in column 64. The lo halves go through
+        // xbuf and zx; the hi-half threads add them and write S^T [m][d], Z.
+        uint32_t r16[16];
+        tmem_ld16(acc + 64, r16);
+        float4* xs = reinterpret_cast<float4*>(xbuf);  // [64][16] float4, XOR-swizzled rows
+        const int d = 32 * (q4 & 1) + lane;
+        if (q4 >= 2) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          if (h == 0) zx[d] = __uint_as_float(r16[0]);
+        }
+        mbar_arrive(xbar);  // the lo halves are in
+        if (!mbar_wait_warp(xbar, xphase, abort, hdr, 6)) return false;
+        xphase ^= 1;
+        if (q4 < 2) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
+            const int m = 32 * h + 4 * j;
+            dst[(m + 0) * kDim + d] = __uint_as_float(r[4 * j]) + lo.x;
+            dst[(m + 1) * kDim + d] = __uint_as_float(r[4 * j + 1]) + lo.y;
+            dst[(m + 2) * kDim + d] = __uint_as_float(r[4 * j + 2]) + lo.z;
+            dst[(m + 3) * kDim + d] = __uint_as_float(r[4 * j + 3]) + lo.w;
+          }
+          if (h == 0) dst[kDim * kDim + d] = __uint_as_float(r16[0]) + zx[d];
+        }
+        mbar_arrive(xbar);  // the exchange buffer is read: phi may overwrite it
+        if (!mbar_wait_warp(xbar, xphase, abort, hdr, 7)) return false;
+        xphase ^= 1;
+      } else {
+        // lanes 0..63: dS^T row m = lane, columns d; lanes 64..127: dZ[d] (every
+        // lane alike). This thread writes columns [32h, 32h + 32) of its row.
+        if (q4 < 2 || (q4 == 2 && lane == 0)) {
+          float4* d4 = reinterpret_cast<float4*>(dst + (q4 < 2 ? (32 * q4 + lane) * kDim : kDim * kDim) + h * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      return true;
+    };
+
+    Cursor cc;
+    cc.start(g);
+    long long consumed = 0;
+    int nseg = 0;                    // segments whose last chunk has passed
+    int pend_item = -1, pend_p = 0;  // segment awaiting its readout
+    uint32_t pend_phase = 0;
+    float zacc[32];
+    bool ok = true;
+    while (cc.valid(g)) {
+      const int item = cc.item;
+      const int bh = g.bh_of(item);
+      const int nvalid = min(kC, g.len(bh) - cc.chunk * kC);
+      const bool last = cc.chunk + 1 == g.chunk_end(item);
+      const int s = consumed % S;
+      uint8_t* kt = stages + s * SB;
+      uint8_t* vt = kt + kTile;
+      if (!mbar_wait_warp(&full[s], (uint32_t)((consumed / S) & 1), abort, hdr, 1)) {
+        ok = false;
+        break;
+      }
+      if (PRECISE)
+        phi_half_split(kt, kt + 2 * kTile, trow, h, nvalid, zacc);
+      else
+        phi_half<true>(kt, trow, h, nvalid);
+      if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
+      fence_proxy_async_smem();
+      mbar_arrive(&phid[s]);
+      // the segment that ended with the previous chunk: its accumulator is not
+      // the one this chunk's MMAs use, and (PRECISE) the previous stage's phi(K)
+      // lo tile, which its MMAs were the last to read, carries the exchange
+      if (pend_item >= 0) {
+        if (!mbar_wait_warp(&segbar[pend_p], pend_phase, abort, hdr, 2)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        if (!readout(pend_item, pend_p, stages + ((consumed + S - 1) % S) * SB + 2 * kTile)) {
+          ok = false;
+          break;
+        }
+        fence_before_sync();
+        pend_item = -1;
+      }
+      if (last) {
+        pend_item = item;
+        pend_p = nseg & 1;
+        pend_phase = (uint32_t)((nseg >> 1) & 1);
+        ++nseg;
+      }
+      ++consumed;
+      cc.advance(g);
+    }
+    if (ok && pend_item >= 0 && mbar_wait_warp(&segbar[pend_p], pend_phase, abort, hdr, 2)) {
+      fence_after_sync();
+      readout(pend_item, pend_p, stages + ((consumed + S - 1) % S) * SB + 2 * kTile);
+      fence_before_sync();
+    }
   }
   pdl_trigger();
-  // drain: every issued load must land before the CTA exits
-  if (tid == 0) {
-    while (consumed < issued) {
-      const int s = consumed % kStateStages;
-      if (!mbar_wait(&full[s], (consumed / kStateStages) & 1)) record_timeout(hdr, 3);
-      ++consumed;
-    }
-  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tbase, 128);
+  if (warp == kStateWorkers / 32) tmem_dealloc(tbase, 256);
 }
 
 // ----------------------------------------------------------- 2. segment scan
