@@ -354,17 +354,18 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
 // --------------------------------------------------------- 3. chunk attention
 
 constexpr int kAttStages = 2;  // 2 CTAs per SM
-// S^T rows (64), then [Z; 0 x 15] rows (16), then 16 rows of ones (the B operand
-// that turns P_L into its row sums on the tensor core)
+// S^T rows (64), then [Z; 0 x 15] rows (16): together the N = 80 B operand of
+// phi(Q) [S^T; Z; 0]^T; then 16 rows of ones (the stacked block that adds the
+// row sums of P_L and the column sums of phi(K) to the MMAs that need them)
 constexpr int kSnapBytes = kDim * 128 + 16 * 128 + 16 * 128;
 constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
 
-// TMEM columns (256 per CTA, two CTAs per SM)
-constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T; then bf16 P in [0, 64)
-constexpr uint32_t kColOz = 64;   // 16: den = phi(Q) . Z_prev + rowsum(P_L) (dead half of P)
-constexpr uint32_t kColZ = 80;    // 16: dZ = phi(K)^T 1 (M = 64 layout, dead half of P)
-constexpr uint32_t kColO = 128;   // 64: numerator
-constexpr uint32_t kColS = 192;   // 64: dS^T (M = 64 layout)
+// TMEM columns (256 per CTA, two CTAs per SM). The first MMA group writes P
+// and the state increment; the second, issued once both are read, writes the
+// output over P's dead upper half and the spent increment.
+constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T; then bf16 P_L in [0, 64)
+constexpr uint32_t kColS = 128;   // 64: dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+constexpr uint32_t kColO = 64;    // 80: numerator in [64, 128), denominator in column 128
 constexpr uint32_t kTmemCols = 256;
 
 // 256 threads: warp w covers TMEM lane quarter w % 4 (rows 32 (w % 4) .. + 31)
@@ -394,8 +395,10 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
   const int row = q4 * 32 + lane;   // chunk row (query) of this thread
-  const int srow = q4 * 16 + lane;  // state row (M = 64 layout), valid for lane < 16
-  const bool sthread = lane < 16;
+  // the state carry: lane quarters 0, 1 hold S^T row m = row, the first lane
+  // of quarter 2 holds Z (the TMEM lanes the stacked increment lands in)
+  const bool sthread = q4 < 2;
+  const bool zthread = q4 == 2 && lane == 0;
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
@@ -444,9 +447,10 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  // running state: S^T row srow, columns [32h, 32h + 32), and Z[srow] (lane < 16)
+  // running state: S^T row `row` (sthread) or Z (zthread), columns [32h, 32h + 32)
   float srun[32];
-  float zrun = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) srun[j] = 0.f;
 
   bool ok = true;
   long long consumed = 0;
@@ -471,27 +475,26 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       entry = (size_t)slot * io.H + bh % io.H;
       if (!entry_ok && tid == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
     }
-    if (direct) {  // S [entry][d][m]: this thread's row m = srow, columns d of its half
+    if (direct) {  // S [entry][d][m]: this thread's row m = row, columns d of its half
       const bool init = entry_ok && io.read_init;
       if (sthread) {
-        const float* src = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + srow;
+        const float* src = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + row;
 #pragma unroll
         for (int j = 0; j < 32; ++j) srun[j] = init ? src[(size_t)j * kDim] : 0.f;
-        zrun = init ? io.Z[entry * kDim + srow] : 0.f;
-      }
-    } else if (first) {  // state before this segment
-      const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (sthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + srow * kDim + 32 * h);
+      } else if (zthread) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 x = s4[j];
-          srun[4 * j] = x.x;
-          srun[4 * j + 1] = x.y;
-          srun[4 * j + 2] = x.z;
-          srun[4 * j + 3] = x.w;
-        }
-        zrun = src[kDim * kDim + srow];
+        for (int j = 0; j < 32; ++j) srun[j] = init ? io.Z[entry * kDim + 32 * h + j] : 0.f;
+      }
+    } else if (first && (sthread || zthread)) {  // state before this segment
+      const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+      const float4* s4 = reinterpret_cast<const float4*>(src + (sthread ? row * kDim : kDim * kDim) + 32 * h);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = s4[j];
+        srun[4 * j] = x.x;
+        srun[4 * j + 1] = x.y;
+        srun[4 * j + 2] = x.z;
+        srun[4 * j + 3] = x.w;
       }
     }
     const int s = consumed % kAttStages;
@@ -499,20 +502,19 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* kt = qt + kTile;
     uint8_t* vt = qt + 2 * kTile;
     // snapshot of the float32 state before this chunk, rounded to bf16, as
-    // K-major B operands: S^T rows m, and Z as row 0 of a 16-row operand.
+    // one K-major B operand of 80 rows: S^T rows m, then Z, then zero rows.
     // Each S element is rounded independently, so over the D-term dot
     // product phi(Q_i) . S[:, m] the rounding averages to ~2^-9 / sqrt(D).
-    if ((CAUSAL || first) && sthread) {
+    if ((CAUSAL || first) && (sthread || zthread)) {
+      uint8_t* dst = sthread ? s_hi : zrow;
+      const int r0 = sthread ? row : 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t hi[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) hi[q] = pack_bf16(srun[8 * c + 2 * q], srun[8 * c + 2 * q + 1]);
-        *reinterpret_cast<uint4*>(s_hi + sw128(srow, (4 * h + c) * 16)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(dst + sw128(r0, (4 * h + c) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
-      if (h == 0)
-        *reinterpret_cast<__nv_bfloat16*>(zrow + sw128(0, 2 * srow)) = __float2bfloat16_rn(zrun);
     }
     if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
       ok = false;
@@ -530,29 +532,29 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    // The ones block of an operand is 16 token rows: every K step of 16 tokens
+    // reads the same block, its descriptor's leading byte offset measured from
+    // that step's start (oa - (va + 2048 k)).
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
-      const uint32_t ha = smem_u32(s_hi), za = smem_u32(zrow);
+      const uint32_t ha = smem_u32(s_hi), oa = smem_u32(ones);
       if (CAUSAL) {
         const uint32_t idP = idesc_bf16(128, 128, false, false);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k)  // P = phi(Q) phi(K)^T
           mma_ss(tbase + kColP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
-        const uint32_t idS = idesc_bf16(64, 64, true, true);
+        // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
+        // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+        const uint32_t idS = idesc_bf16(128, 64, true, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kColS, sdesc(va + k * 2048, 1024, 1024), sdesc(ka + k * 2048, 1024, 1024),
-                 idS, k);
-      }
-      const uint32_t idO = idesc_bf16(128, 64, false, false);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
-      if (!CAUSAL) {  // causal: issued after the P epilogue, into the freed half of P
-        const uint32_t idZ = idesc_bf16(128, 16, false, false);
+          mma_ss(tbase + kColS, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                 sdesc(ka + k * 2048, 1024, 1024), idS, k);
+      } else {  // num and den = phi(Q) [S^T; Z; 0]^T, the state being the total
+        const uint32_t idO = idesc_bf16(128, 80, false, false);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
+          mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
       }
       mma_commit(mma_bar);
       // causal: the next chunk's tiles are issued here rather than at the top
@@ -597,17 +599,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 16; ++c) pk[t][c] = 0u;
         }
       }
-      // state update: S^T += dS^T (this half's columns of row srow)
-      {
+      // state update: S^T += dS^T (row `row`), Z += dZ (TMEM lane 64), this half's columns
+      if (q4 <= 2) {
         uint32_t r[32];
         tmem_ld32(tl + kColS + 32 * h, r);
-        if (sthread) {
+        if (sthread || zthread) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
         }
       }
       fence_before_sync();
-      __syncthreads();  // every read of fp32 P is done before bf16 P overwrites it
+      __syncthreads();  // every read of fp32 P and of the increment is done before they are overwritten
       fence_after_sync();
 #pragma unroll
       for (int t = 0; t < 2; ++t) tmem_st16(tl + kColP + 16 * (2 * h + t), pk[t]);
@@ -615,27 +617,20 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       __syncthreads();
       fence_after_sync();
       if (tid == 0) {
-        const uint32_t va = smem_u32(vt), qa = smem_u32(qt), za = smem_u32(zrow);
-        const uint32_t ka = smem_u32(kt);
-        const uint32_t idPV = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kColO, tbase + kColP + k * 8, sdesc(va + k * 2048, 1024, 1024), idPV, 1);
-        // den = phi(Q) . Z_prev + rowsum(P_L): both land in the same column
-        const uint32_t idZ = idesc_bf16(128, 16, false, false);
+        const uint32_t va = smem_u32(vt), qa = smem_u32(qt), ha = smem_u32(s_hi);
+        const uint32_t oa = smem_u32(ones);
+        // phi(Q) [S^T; Z; 0]^T + P_L [V | 1] (N = 80; V's columns 64.. from the ones
+        // block): the numerator in columns [0, 64) of kColO and the denominator
+        // phi(Q) . Z_prev + rowsum(P_L) in column 64, from the same bf16 weights
+        const uint32_t idO = idesc_bf16(128, 80, false, false);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kColOz, sdesc(qa + k * 32, 16, 1024), sdesc(za + k * 32, 16, 1024), idZ, k);
-        const uint32_t oa = smem_u32(ones);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // every ones row reads the same 2 KB buffer
-          mma_ts(tbase + kColOz, tbase + kColP + k * 8, sdesc(oa + (k % 4) * 32, 16, 1024), idZ, 1);
-        // dZ[d] = sum_t phi(K)[t][d]: phi(K)^T (MN-major A, M = 64) times ones
-        const uint32_t idDZ = idesc_bf16(64, 16, true, false);
+          mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
+        const uint32_t idPV = idesc_bf16(128, 80, false, true);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kColZ, sdesc(ka + k * 2048, 1024, 1024), sdesc(oa + (k % 4) * 32, 16, 1024),
-                 idDZ, k);
+          mma_ts(tbase + kColO, tbase + kColP + k * 8, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                 idPV, 1);
         mma_commit(mma_bar);
       }
       if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
@@ -644,16 +639,15 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       mma_phase ^= 1;
       fence_after_sync();
-      {  // Z += dZ (row srow of the M = 64 accumulator)
-        uint32_t r16[16];
-        tmem_ld16(tl + kColZ, r16);
-        if (sthread) zrun += __uint_as_float(r16[0]);
-      }
-      if (entry_ok && sthread) {  // direct: the state after the sequence's only chunk
-        float* dst = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + srow;
+      if (entry_ok) {  // direct: the state after the sequence's only chunk
+        if (sthread) {
+          float* dst = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + row;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[(size_t)j * kDim] = srun[j];
-        if (h == 0) io.Z[entry * kDim + srow] = zrun;
+          for (int j = 0; j < 32; ++j) dst[(size_t)j * kDim] = srun[j];
+        } else if (zthread) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) io.Z[entry * kDim + 32 * h + j] = srun[j];
+        }
       }
     }
 
@@ -661,7 +655,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // MMAs reading it are done)
     {
       uint32_t oz[16], r[32];
-      tmem_ld16_32(tl + kColOz, oz, tl + kColO + 32 * h, r);
+      tmem_ld16_32(tl + kColO + 64, oz, tl + kColO + 32 * h, r);
       const float inv = 1.f / __uint_as_float(oz[0]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
