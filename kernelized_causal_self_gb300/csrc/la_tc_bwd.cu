@@ -40,7 +40,7 @@ namespace {
 constexpr int kBwdStages = 2;
 constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows each
 constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
-constexpr int kArr = 4096;              // small float arrays
+constexpr int kArr = 8192;              // small float arrays
 constexpr int kLoB = 2 * kTile;         // phi(Q), phi(K) lo parts
 constexpr int kBwdSmem =
     1024 + kBwdStages * 4 * kTile + kSnapB + kGnB + kLoB + kArr + 2048;
@@ -104,6 +104,74 @@ enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 // handled by two threads. Where a TMEM region is compacted in place (fp32 P
 // into bf16 P_L), all reads finish before a barrier and the writes follow it.
 constexpr int kBT = 256;
+// The forward-direction kernel runs 512 threads: warp w covers TMEM lane quarter
+// w % 4 and column quarter qc = w / 4 (16 of the 64 state columns, the 32-column
+// slice qc of the chunk's 128), so every row is handled by four threads.
+constexpr int kBTQ = 512;
+
+// Quarter-row store of x[16] (columns [16 qc, 16 qc + 16)) as bf16 hi and lo rows.
+__device__ __forceinline__ void store_split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, int row, int qc,
+                                                    const float* x) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t hh[4], ll[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) split_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1], hh[q], ll[q]);
+    const uint32_t off = sw128(row, (2 * qc + c) * 16);
+    *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+    *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+  }
+}
+
+// phi on columns [16 qc, 16 qc + 16) of a tile row, rounded to bf16 in place with
+// the rounding error kept as a bf16 lo part in `lo`; z gets the float32 values.
+// Rows >= nvalid become zero.
+template <bool MASK>
+__device__ __forceinline__ void phi_quarter_split_impl(uint8_t* tile, uint8_t* lo, int row, int qc,
+                                                       int nvalid, float (&z)[16]) {
+  const bool valid = !MASK || row < nvalid;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t off = sw128(row, (2 * qc + c) * 16);
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + off);
+    uint32_t u[4] = {w.x, w.y, w.z, w.w}, l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a = valid ? phi_fast(bf16_lo_f(u[q])) : 0.f;
+      const float b = valid ? phi_fast(bf16_hi_f(u[q])) : 0.f;
+      u[q] = pack_bf16(a, b);
+      l[q] = pack_bf16(a - bf16_lo_f(u[q]), b - bf16_hi_f(u[q]));
+      z[8 * c + 2 * q] = a;
+      z[8 * c + 2 * q + 1] = b;
+    }
+    *reinterpret_cast<uint4*>(tile + off) = make_uint4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+__device__ __forceinline__ void phi_quarter_split(uint8_t* tile, uint8_t* lo, int row, int qc, int nvalid,
+                                                  float (&z)[16]) {
+  if (nvalid >= kC)
+    phi_quarter_split_impl<false>(tile, lo, row, qc, nvalid, z);
+  else
+    phi_quarter_split_impl<true>(tile, lo, row, qc, nvalid, z);
+}
+
+// Sum z[16] over the 32 lanes of a warp; lanes l and l + 16 end with column l % 16.
+__device__ __forceinline__ float warp_column_sums16(float (&z)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool up = lane & w;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float mine = up ? z[w + j] : z[j];
+      const float other = up ? z[j] : z[w + j];
+      z[j] = mine + __shfl_xor_sync(0xffffffffu, other, w);
+    }
+  }
+  return z[0] + __shfl_xor_sync(0xffffffffu, z[0], 16);
+}
 
 // Half-row store of x[32] (columns [32h, 32h + 32)) as bf16 hi and lo rows.
 __device__ __forceinline__ void store_split_half(uint8_t* hi_buf, uint8_t* lo_buf, int row, int h,
@@ -145,7 +213,7 @@ constexpr uint32_t kFQ = 384;   // 64: dphiQ
 constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kBTQ, 1)
 tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                 const __grid_constant__ CUtensorMap tm_dq, Geometry g,
@@ -155,14 +223,14 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   BwdSmem sm(smraw);
   float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
   float* dz = sm.arr + 64;       // [4][64]: warp column sums
-  float* rsum = sm.arr + 320;    // [2][128]: half-row parts of den
-  float* gnum = sm.arr + 576;    // [2][128]: half-row parts of G . num
+  float* rsum = sm.arr + 320;    // [4][128]: quarter-row parts of den
+  float* gnum = sm.arr + 832;    // [4][128]: quarter-row parts of G . num
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int q4 = warp & 3, h = warp >> 2;
-  const int row = q4 * 32 + lane;  // query row of this thread
-  // S carry: row d = 32 (q4 % 2) + lane, held by the threads of TMEM lanes 0-63
-  const int drow = 32 * (q4 & 1) + lane;
-  const bool dthread = q4 < 2;
+  const int lq = warp & 3, qc = warp >> 2;
+  const int row = lq * 32 + lane;  // query row of this thread
+  // S carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
+  const int drow = 32 * (lq & 1) + lane;
+  const bool dthread = lq < 2;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -200,11 +268,11 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float srun[32];             // S row drow, columns m in [32h, 32h + 32) (dthread)
+  float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
   float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0, sph1 = 0;
-  float z[32];
+  float z[16];
 
   while (cc.valid(g)) {
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
@@ -219,16 +287,16 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this half
+      if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
 #pragma unroll
-        for (int j = 0; j < 32; ++j) srun[j] = src[(32 * h + j) * kDim + drow];
+        for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + drow];
       }
       if (tid < kDim) {
         zrun = src[kDim * kDim + tid];
         rr = 0.f;
       }
     }
-    if ((CAUSAL || first) && dthread) store_split_half(sm.s_hi, sm.s_lo, drow, h, srun);
+    if ((CAUSAL || first) && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
     if (tid < kDim) zsnap[tid] = zrun;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
@@ -236,10 +304,11 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 21)) break;
-    phi_half_split(qt, sm.qlo, row, h, kC, z);
+    phi_quarter_split(qt, sm.qlo, row, qc, kC, z);
     if (CAUSAL) {
-      phi_half_split(kt, sm.klo, row, h, nvalid, z);
-      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
+      phi_quarter_split(kt, sm.klo, row, qc, nvalid, z);
+      const float cs = warp_column_sums16(z);
+      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
     }
     fence_proxy_async_smem();
     sync_tc();
@@ -283,113 +352,95 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     fence_after_sync();
 
     // ---- epilogue: den, G.num, then gd, gN and T_L
-    float wv[2][32];  // masked W of this thread's two slices (causal)
+    float wv[32];  // masked W of this thread's slice qc (causal)
     {
       float dpart = 0.f, npart = 0.f;
       if (CAUSAL) {
+        if (qc <= lq) {  // warp-uniform
+          uint32_t rp[32], rw[32];
+          tmem_ld32x2(tl + kFP + 32 * qc, rp, tl + kFW + 32 * qc, rw);
+          if (qc < lq) {  // below the diagonal block: nothing is masked
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int sl = 2 * h + t;
-          if (sl <= q4) {
-            uint32_t rp[32], rw[32];
-            tmem_ld32x2(tl + kFP + 32 * sl, rp, tl + kFW + 32 * sl, rw);
-            if (sl < q4) {  // below the diagonal block: nothing is masked (warp-uniform)
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const float p = __uint_as_float(rp[c]);
-                wv[t][c] = __uint_as_float(rw[c]);
-                dpart += p;
-                npart += p * wv[t][c];
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const bool keep = 32 * sl + c <= row;
-                const float p = keep ? __uint_as_float(rp[c]) : 0.f;
-                wv[t][c] = keep ? __uint_as_float(rw[c]) : 0.f;
-                dpart += p;
-                npart += p * wv[t][c];
-              }
+            for (int c = 0; c < 32; ++c) {
+              const float p = __uint_as_float(rp[c]);
+              wv[c] = __uint_as_float(rw[c]);
+              dpart += p;
+              npart += p * wv[c];
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) wv[t][c] = 0.f;
+            for (int c = 0; c < 32; ++c) {
+              const bool keep = 32 * qc + c <= row;
+              const float p = keep ? __uint_as_float(rp[c]) : 0.f;
+              wv[c] = keep ? __uint_as_float(rw[c]) : 0.f;
+              dpart += p;
+              npart += p * wv[c];
+            }
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) wv[c] = 0.f;
         }
       }
-      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this half. The Z dot
+      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this quarter. The Z dot
          // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
          // the rounding of phi(Q) cancels in num / den.
-        uint32_t ro[32];
-        tmem_ld32(tl + kFO + 32 * h, ro);
+        uint32_t ro[16];
+        tmem_ld16(tl + kFO + 16 * qc, ro);
+        float gv[16], qv[16];
+        load_row16(gt, row, 2 * qc, gv);
+        load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float gv[16], qv[16];
-          load_row16(gt, row, 4 * h + 2 * c, gv);
-          load_row16(qt, row, 4 * h + 2 * c, qv);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            npart += gv[q] * __uint_as_float(ro[16 * c + q]);
-            dpart += qv[q] * zsnap[32 * h + 16 * c + q];
-          }
+        for (int q = 0; q < 16; ++q) {
+          npart += gv[q] * __uint_as_float(ro[q]);
+          dpart += qv[q] * zsnap[16 * qc + q];
         }
       }
-      rsum[h * 128 + row] = dpart;
-      gnum[h * 128 + row] = npart;
+      rsum[qc * 128 + row] = dpart;
+      gnum[qc * 128 + row] = npart;
     }
     if (CAUSAL && tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     sync_tc();  // partials visible; every read of W is done
-    const float den = rsum[row] + rsum[128 + row];
+    const float den = (rsum[row] + rsum[128 + row]) + (rsum[256 + row] + rsum[384 + row]);
     const float inv = 1.f / den;
-    const float gd = -(gnum[row] + gnum[128 + row]) * inv * inv;
+    const float gd = -((gnum[row] + gnum[128 + row]) + (gnum[256 + row] + gnum[384 + row])) * inv * inv;
     {
-      float gn[32];
+      float gn[16];
+      load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float gv[16];
-        load_row16(gt, row, 4 * h + 2 * c, gv);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) gn[16 * c + q] = gv[q] * inv;
-      }
-      store_split_half(sm.gn_hi, sm.gn_lo, row, h, gn);
-      if (h == 0 && row < nvalid) {
+      for (int q = 0; q < 16; ++q) gn[q] *= inv;
+      store_split_quarter(sm.gn_hi, sm.gn_lo, row, qc, gn);
+      if (qc == 0 && row < nvalid) {
         den_out[(size_t)bh * g.N + t0 + row] = den;
         gd_out[(size_t)bh * g.N + t0 + row] = gd;
       }
       // this chunk's share of r = sum_i gd_i phi(Q_i) (float32 phi = hi + lo)
+      float qv[16], ql[16];
+      load_row16(qt, row, 2 * qc, qv);
+      load_row16(sm.qlo, row, 2 * qc, ql);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float qv[16], ql[16];
-        load_row16(qt, row, 4 * h + 2 * c, qv);
-        load_row16(sm.qlo, row, 4 * h + 2 * c, ql);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) z[16 * c + q] = gd * (qv[q] + ql[q]);
-      }
-      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
+      for (int q = 0; q < 16; ++q) z[q] = gd * (qv[q] + ql[q]);
+      const float cs = warp_column_sums16(z);
+      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
     }
     if (CAUSAL) {  // T_L = W / den + gd (j <= i), bf16 hi + lo over the spent W columns
+      uint32_t th[16], tlo[16];
+      if (qc < lq) {  // warp-uniform: full slice, diagonal slice, or all zero
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int sl = 2 * h + t;
-        uint32_t th[16], tlo[16];
-        if (sl < q4) {  // warp-uniform: full slice, diagonal slice, or all zero
+        for (int c = 0; c < 16; ++c) split_bf16(wv[2 * c] * inv + gd, wv[2 * c + 1] * inv + gd, th[c], tlo[c]);
+      } else if (qc == lq) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            split_bf16(wv[t][2 * c] * inv + gd, wv[t][2 * c + 1] * inv + gd, th[c], tlo[c]);
-        } else if (sl == q4) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int j0 = 32 * sl + 2 * c;
-            split_bf16(j0 <= row ? wv[t][2 * c] * inv + gd : 0.f,
-                       j0 + 1 <= row ? wv[t][2 * c + 1] * inv + gd : 0.f, th[c], tlo[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
+        for (int c = 0; c < 16; ++c) {
+          const int j0 = 32 * qc + 2 * c;
+          split_bf16(j0 <= row ? wv[2 * c] * inv + gd : 0.f, j0 + 1 <= row ? wv[2 * c + 1] * inv + gd : 0.f,
+                     th[c], tlo[c]);
         }
-        tmem_st16(tl + kFW + 16 * sl, th);
-        tmem_st16(tl + kFW + 64 + 16 * sl, tlo);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
       }
+      tmem_st16(tl + kFW + 16 * qc, th);
+      tmem_st16(tl + kFW + 64 + 16 * qc, tlo);
     }
     fence_proxy_async_smem();
     sync_tc();
@@ -445,26 +496,21 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     ph ^= 1;
     fence_after_sync();
 
-    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this half's columns,
-    // staged as a 128 x 32 float32 box (128-byte swizzle) for a TMA store in the spent
-    // phi(K) tiles (warps 0-3: K tile, 4-7: its lo part)
+    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this quarter's
+    // columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for TMA stores in
+    // the spent phi(K) tiles (quarters 0, 1: K tile; 2, 3: its lo part)
     {
-      uint32_t r[32];
-      tmem_ld32(tl + kFQ + 32 * h, r);
-      float o[32];
+      uint32_t r[16];
+      tmem_ld16(tl + kFQ + 16 * qc, r);
+      float qv[16], o[16];
+      load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float qv[16];
-        load_row16(qt, row, 4 * h + 2 * c, qv);
+      for (int q = 0; q < 16; ++q)
+        o[q] = (__uint_as_float(r[q]) + gd * zsnap[16 * qc + q]) * fminf(qv[q], 1.f);
+      uint8_t* sq = qc < 2 ? kt : sm.klo;
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          o[16 * c + q] =
-              (__uint_as_float(r[16 * c + q]) + gd * zsnap[32 * h + 16 * c + q]) * fminf(qv[q], 1.f);
-      }
-      uint8_t* sq = h == 0 ? kt : sm.klo;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4*>(sq + sw128(row, c * 16)) =
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<float4*>(sq + sw128(row, (qc & 1) * 64 + c * 16)) =
             make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
     }
     fence_proxy_async_smem();
@@ -480,21 +526,21 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     sph1 ^= 1;
     fence_after_sync();
     if (CAUSAL) {  // S += dS: the lo-part rows pass through the spent gN lo buffer
-      uint32_t r[32];
-      tmem_ld32(tl + kFS + 32 * h, r);
+      uint32_t r[16];
+      tmem_ld16(tl + kFS + 16 * qc, r);
       float4* xs = reinterpret_cast<float4*>(sm.gn_lo);  // [64][16] float4, XOR-swizzled rows
       if (!dthread) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          xs[drow * 16 + ((8 * h + j) ^ (drow & 15))] =
+        for (int j = 0; j < 4; ++j)
+          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
               make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       __syncthreads();
       if (dthread) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 lo = xs[drow * 16 + ((8 * h + j) ^ (drow & 15))];
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
           srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
           srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
           srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
@@ -505,26 +551,26 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
-      // lane 32 q4 + lane holds row d = 32 (q4 % 2) + lane: hi part for q4 < 2, lo
-      // part for q4 >= 2; the lo parts pass through the spent gN hi buffer
+      // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
+      // part for lq >= 2; the lo parts pass through the spent gN hi buffer
       float* dst = rpartial + (size_t)item * kStateFloats;
-      uint32_t r[32];
-      tmem_ld32(tl + kFR + 32 * h, r);
+      uint32_t r[16];
+      tmem_ld16(tl + kFR + 16 * qc, r);
       float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
-      const int d = 32 * (q4 & 1) + lane;
-      if (q4 >= 2) {
+      const int d = drow;
+      if (lq >= 2) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
+        for (int j = 0; j < 4; ++j)
+          xs[d * 16 + ((4 * qc + j) ^ (d & 15))] =
               make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       __syncthreads();
-      if (q4 < 2) {
-        float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 32 * h);
+      if (lq < 2) {
+        float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 16 * qc);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[d * 16 + ((4 * qc + j) ^ (d & 15))];
           d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
                               __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
         }
@@ -992,8 +1038,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   auto run_q = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, tdq, g,
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sms);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, g,
                      (const float*)sprefix, rpartial, den, gd, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
