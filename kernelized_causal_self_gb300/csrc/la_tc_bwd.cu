@@ -99,14 +99,11 @@ struct BwdSmem {
 
 enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 
-// Both kernels run 256 threads: warp w covers TMEM lane quarter w % 4 (rows
-// 32 (w % 4) .. + 31) and half h = w / 4 of each row's columns, so every row is
-// handled by two threads. Where a TMEM region is compacted in place (fp32 P
-// into bf16 P_L), all reads finish before a barrier and the writes follow it.
-constexpr int kBT = 256;
-// The forward-direction kernel runs 512 threads: warp w covers TMEM lane quarter
-// w % 4 and column quarter qc = w / 4 (16 of the 64 state columns, the 32-column
-// slice qc of the chunk's 128), so every row is handled by four threads.
+// Both kernels run 512 threads: warp w covers TMEM lane quarter w % 4 (rows
+// 32 (w % 4) .. + 31) and column quarter qc = w / 4 (16 of the 64 state
+// columns, the 32-column slice qc of the chunk's 128), so every row is handled
+// by four threads. Where a TMEM region is compacted in place (fp32 P into bf16
+// P_L), all reads finish before a barrier and the writes follow it.
 constexpr int kBTQ = 512;
 
 // Quarter-row store of x[16] (columns [16 qc, 16 qc + 16)) as bf16 hi and lo rows.
@@ -171,20 +168,6 @@ __device__ __forceinline__ float warp_column_sums16(float (&z)[16]) {
     }
   }
   return z[0] + __shfl_xor_sync(0xffffffffu, z[0], 16);
-}
-
-// Half-row store of x[32] (columns [32h, 32h + 32)) as bf16 hi and lo rows.
-__device__ __forceinline__ void store_split_half(uint8_t* hi_buf, uint8_t* lo_buf, int row, int h,
-                                                 const float* x) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t hh[4], ll[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) split_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1], hh[q], ll[q]);
-    const uint32_t off = sw128(row, (4 * h + c) * 16);
-    *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-    *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
-  }
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -601,44 +584,44 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // T^T_ji = W^T_ji / den_i + gd_i with den_i, gd_i saved by the forward-direction
 // kernel.
 
-// Masked row slices of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs for
-// this thread's half (slices 2h, 2h + 1). LOWER keeps j <= row (query rows),
-// otherwise i >= row (key rows).
+// Masked slice sl of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs. LOWER
+// keeps j <= row (query rows), otherwise i >= row (key rows).
 template <bool LOWER>
-__device__ __forceinline__ void masked_split_slices(uint32_t taddr, int h, int q4, int row,
-                                                    float add, uint32_t (&hi)[2][16],
-                                                    uint32_t (&lo)[2][16], float& sum) {
+__device__ __forceinline__ void masked_split_slice(uint32_t taddr, int sl, int lq, int row, uint32_t (&hi)[16],
+                                                   uint32_t (&lo)[16]) {
+  const bool any = LOWER ? sl <= lq : sl >= lq;
+  if (any) {  // warp-uniform
+    uint32_t r[32];
+    tmem_ld32(taddr + 32 * sl, r);
+    if (sl != lq) {  // off the diagonal block: nothing is masked
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int sl = 2 * h + t;
-    const bool any = LOWER ? sl <= q4 : sl >= q4;
-    if (any) {
-      uint32_t r[32];
-      tmem_ld32(taddr + 32 * sl, r);
-      if (sl != q4) {  // off the diagonal block: nothing is masked (warp-uniform)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a = __uint_as_float(r[2 * c]) + add;
-          const float b = __uint_as_float(r[2 * c + 1]) + add;
-          split_bf16(a, b, hi[t][c], lo[t][c]);
-          sum += a + b;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int j0 = 32 * sl + 2 * c;
-          const bool k0 = LOWER ? j0 <= row : j0 >= row;
-          const bool k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
-          const float a = k0 ? __uint_as_float(r[2 * c]) + add : 0.f;
-          const float b = k1 ? __uint_as_float(r[2 * c + 1]) + add : 0.f;
-          split_bf16(a, b, hi[t][c], lo[t][c]);
-          sum += a + b;
-        }
-      }
+      for (int c = 0; c < 16; ++c) split_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
     } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) hi[t][c] = lo[t][c] = 0u;
+      for (int c = 0; c < 16; ++c) {
+        const int j0 = 32 * sl + 2 * c;
+        const bool k0 = LOWER ? j0 <= row : j0 >= row;
+        const bool k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
+        split_bf16(k0 ? __uint_as_float(r[2 * c]) : 0.f, k1 ? __uint_as_float(r[2 * c + 1]) : 0.f, hi[c], lo[c]);
+      }
     }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) hi[c] = lo[c] = 0u;
+  }
+}
+
+// phi with the float32 exponential on columns [16 qc, 16 qc + 16) of a tile row,
+// in place; rows >= nvalid become zero.
+__device__ __forceinline__ void phi_quarter_exact(uint8_t* tile, int row, int qc, int nvalid) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, (2 * qc + c) * 16));
+    const uint4 w = *p;
+    *p = valid ? make_uint4(phi2_bf16_exact(w.x), phi2_bf16_exact(w.y), phi2_bf16_exact(w.z),
+                            phi2_bf16_exact(w.w))
+               : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -650,7 +633,7 @@ constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
 constexpr uint32_t kRL = 448;   // 64: bf16 lo part of T_L^T
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kBTQ, 1)
 tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -664,11 +647,11 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   float* invs = sm.arr + 192;    // 128: 1 / den_i
   float* dz = sm.arr + 320;      // [4][64]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int q4 = warp & 3, h = warp >> 2;
-  const int row = q4 * 32 + lane;  // key row for the gradients, query row for gN
-  // R carry: row d = 32 (q4 % 2) + lane, held by the threads of TMEM lanes 0-63
-  const int drow = 32 * (q4 & 1) + lane;
-  const bool dthread = q4 < 2;
+  const int lq = warp & 3, qc = warp >> 2;
+  const int row = lq * 32 + lane;  // key row for the gradients, query row for gN
+  // R carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
+  const int drow = 32 * (lq & 1) + lane;
+  const bool dthread = lq < 2;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -706,11 +689,11 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float rrun[32];  // R row drow, columns [32h, 32h + 32) (dthread)
+  float rrun[16];  // R row drow, columns [16 qc, 16 qc + 16) (dthread)
   float rr = 0.f;  // r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0, sph = 0;
-  float z[32];
+  float z[16];
   // den_i, gd_i of the chunk being processed, loaded one chunk ahead
   float nden = 1.f, ngd = 0.f;
   auto fetch_dg = [&](const RevCursor& c) {
@@ -746,9 +729,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (first) {
       const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (dthread) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + drow * kDim + 32 * h);
+        const float4* s4 = reinterpret_cast<const float4*>(src + drow * kDim + 16 * qc);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           const float4 x = s4[q];
           rrun[4 * q] = x.x;
           rrun[4 * q + 1] = x.y;
@@ -758,7 +741,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (tid < kDim) rr = src[kDim * kDim + tid];
     }
-    if ((CAUSAL || first) && dthread) store_split_half(sm.s_hi, sm.s_lo, drow, h, rrun);
+    if ((CAUSAL || first) && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, rrun);
     if (tid < kDim) rsnap[tid] = rr;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
@@ -766,24 +749,22 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
     if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 31)) break;
-    phi_half<true>(kt, row, h, nvalid);
+    phi_quarter_exact(kt, row, qc, nvalid);
     if (CAUSAL) {
-      phi_half_split(qt, sm.qlo, row, h, kC, z);
-      // gN (query row = row) for this half, and this chunk's share of r
+      phi_quarter_split(qt, sm.qlo, row, qc, kC, z);
+      // gN (query row = row) for this quarter, and this chunk's share of r
       const float inv = invs[row];
       const float gdr = gds[row];
-      float gn[32];
+      float gn[16];
+      load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float gv[16];
-        load_row16(gt, row, 4 * h + 2 * c, gv);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) gn[16 * c + q] = gv[q] * inv;
+      for (int q = 0; q < 16; ++q) {
+        gn[q] *= inv;
+        z[q] *= gdr;
       }
-#pragma unroll
-      for (int q = 0; q < 32; ++q) z[q] *= gdr;
-      store_split_half(sm.gn_hi, sm.gn_lo, row, h, gn);
-      dz[q4 * 64 + 32 * h + lane] = warp_column_sums32(z);
+      store_split_quarter(sm.gn_hi, sm.gn_lo, row, qc, gn);
+      const float cs = warp_column_sums16(z);
+      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
     }
     fence_proxy_async_smem();
     sync_tc();
@@ -840,46 +821,37 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
 
     if (CAUSAL) {
-      // key row keeps query columns i >= row
-      uint32_t pph[2][16], ppl[2][16], pth[2][16], ptl[2][16];
-      float unused = 0.f;
-      masked_split_slices<false>(tl + kRP, h, q4, row, 0.f, pph, ppl, unused);
+      // key row keeps query columns i >= row; slice qc of P^T and of T^T
+      uint32_t pph[16], ppl[16], pth[16], ptl[16];
+      masked_split_slice<false>(tl + kRP, qc, lq, row, pph, ppl);
       // T^T_ji = W^T_ji / den_i + gd_i (column-dependent scale and shift)
+      if (qc >= lq) {  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(tl + kRT + 32 * qc, r);
+        if (qc != lq) {  // below the diagonal block: nothing is masked
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int sl = 2 * h + t;
-        if (sl >= q4) {
-          uint32_t r[32];
-          tmem_ld32(tl + kRT + 32 * sl, r);
-          if (sl != q4) {  // below the diagonal block: nothing is masked (warp-uniform)
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int i0 = 32 * sl + 2 * c;
-              split_bf16(__uint_as_float(r[2 * c]) * invs[i0] + gds[i0],
-                         __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1], pth[t][c],
-                         ptl[t][c]);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int i0 = 32 * sl + 2 * c;
-              split_bf16(i0 >= row ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
-                         i0 + 1 >= row ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
-                         pth[t][c], ptl[t][c]);
-            }
+          for (int c = 0; c < 16; ++c) {
+            const int i0 = 32 * qc + 2 * c;
+            split_bf16(__uint_as_float(r[2 * c]) * invs[i0] + gds[i0],
+                       __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1], pth[c], ptl[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pth[t][c] = ptl[t][c] = 0u;
+          for (int c = 0; c < 16; ++c) {
+            const int i0 = 32 * qc + 2 * c;
+            split_bf16(i0 >= row ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
+                       i0 + 1 >= row ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
+                       pth[c], ptl[c]);
+          }
         }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pth[c] = ptl[c] = 0u;
       }
       sync_tc();  // all reads of P^T, T^T done before the bf16 parts overwrite them
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        tmem_st16(tl + kRP + 16 * (2 * h + t), pph[t]);
-        tmem_st16(tl + kRT + 16 * (2 * h + t), pth[t]);
-        tmem_st16(tl + kRL + 16 * (2 * h + t), ptl[t]);
-      }
+      tmem_st16(tl + kRP + 16 * qc, pph);
+      tmem_st16(tl + kRT + 16 * qc, pth);
+      tmem_st16(tl + kRL + 16 * qc, ptl);
       sync_tc();
       if (tid == 0) {
         const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
@@ -907,30 +879,25 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       fence_after_sync();
     }
 
-    // dk = (dphiK + r_next) * phi'(k) and dv, this half's columns, staged as 128 x 32
+    // dk = (dphiK + r_next) * phi'(k) and dv, this quarter's columns, staged in 128 x 32
     // float32 boxes (128-byte swizzle) for TMA stores: dk in the spent V / G tiles, dv in
     // the spent phi(Q) hi / lo tiles (the R MMAs that read those ran before the second
     // group, whose completion was awaited)
     {
-      uint32_t r[32], w[32];
-      tmem_ld32x2(tl + kRK + 32 * h, r, tl + kRV + 32 * h, w);
-      float o[32];
+      uint32_t r[16], w[16];
+      tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRV + 16 * qc, w);
+      float kv[16], o[16];
+      load_row16(kt, row, 2 * qc, kv);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float kv[16];
-        load_row16(kt, row, 4 * h + 2 * c, kv);
+      for (int q = 0; q < 16; ++q)
+        o[q] = (__uint_as_float(r[q]) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
+      uint8_t* sk = qc < 2 ? vt : gt;
+      uint8_t* sv = qc < 2 ? qt : sm.qlo;
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          o[16 * c + q] =
-              (__uint_as_float(r[16 * c + q]) + rsnap[32 * h + 16 * c + q]) * fminf(kv[q], 1.f);
-      }
-      uint8_t* sk = h == 0 ? vt : gt;
-      uint8_t* sv = h == 0 ? qt : sm.qlo;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<float4*>(sk + sw128(row, c * 16)) =
-            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-        *reinterpret_cast<float4*>(sv + sw128(row, c * 16)) =
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t off = sw128(row, (qc & 1) * 64 + c * 16);
+        *reinterpret_cast<float4*>(sk + off) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        *reinterpret_cast<float4*>(sv + off) =
             make_float4(__uint_as_float(w[4 * c]), __uint_as_float(w[4 * c + 1]),
                         __uint_as_float(w[4 * c + 2]), __uint_as_float(w[4 * c + 3]));
       }
@@ -948,22 +915,22 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
       sph ^= 1;
       fence_after_sync();
-      uint32_t r[32];
-      tmem_ld32(tl + kRR + 32 * h, r);
+      uint32_t r[16];
+      tmem_ld16(tl + kRR + 16 * qc, r);
       // the lo-part rows (lanes 64-127) pass through the spent gN hi buffer
       float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
       if (!dthread) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          xs[drow * 16 + ((8 * h + j) ^ (drow & 15))] =
+        for (int j = 0; j < 4; ++j)
+          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
               make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       __syncthreads();
       if (dthread) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 lo = xs[drow * 16 + ((8 * h + j) ^ (drow & 15))];
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
           rrun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
           rrun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
           rrun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
@@ -1051,8 +1018,8 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
   auto run_kv = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBT) * sms);
-    err = launch_pdl(kern, dim3(ctas), dim3(kBT), kBwdSmem, st, tq, tk, tv, tg, tdk, tdv, g,
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sms);
+    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdk, tdv, g,
                      (const float*)rsuffix, (const float*)den, (const float*)gd, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
