@@ -188,11 +188,11 @@ __device__ __forceinline__ void sync_tc() {
 // sum of phi(Q)^T gN.
 
 // TMEM columns
-constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T
+constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T; after the first epilogue, dphiQ (kFQ)
 constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
 constexpr uint32_t kFO = 256;   // 64: phi(Q) S_prev
 constexpr uint32_t kFS = 320;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
-constexpr uint32_t kFQ = 384;   // 64: dphiQ
+constexpr uint32_t kFQ = 0;     // 128: dphiQ as two 64-column parts (P's columns, spent by then)
 constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
 template <bool CAUSAL>
@@ -433,27 +433,26 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t kl = smem_u32(sm.klo);
       const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
-      const uint32_t idQ = idesc_bf16(128, 64, false, true);
-      if (CAUSAL) {  // dphiQ = T_L phi(K): hi*hi + hi*lo + lo*hi
+      // dphiQ = T_L phi(K) + gN S_prev^T with the hi*hi + hi*lo + lo*hi terms of
+      // each product; the hi*lo partners share their A operand, so they sit side by
+      // side in one N = 128 instruction, and dphiQ is the sum of the accumulator's
+      // two 64-column halves (columns [64, 128) carry only the hi*lo terms)
+      const uint32_t idQ2 = idesc_bf16(128, 128, false, true), idQ = idesc_bf16(128, 64, false, true);
+      if (CAUSAL) {
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, k);
+        for (int k = 0; k < kC / 16; ++k)  // T_hi [phi(K)_hi | phi(K)_lo] (N blocks kl - ka apart)
+          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(ka + k * 2048, kl - ka, 1024), idQ2, k);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(kl + k * 2048, 1024, 1024), idQ, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
+        for (int k = 0; k < kC / 16; ++k)  // T_lo phi(K)_hi
           mma_ts(tbase + kFQ, tbase + kFW + 64 + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, 1);
       }
-      // += gN S_prev^T: B = the snapshot, rows d (= N), m contiguous (K-major)
-      const uint32_t idQs = idesc_bf16(128, 64, false, false);
+      // B = the snapshot, rows d (= N), m contiguous (K-major): the S_lo rows follow
+      // the S_hi rows, so gN_hi [S_hi; S_lo]^T is one N = 128 product
+      const uint32_t idQs2 = idesc_bf16(128, 128, false, false), idQs = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs,
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs2,
                (CAUSAL || k > 0) ? 1u : 0u);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idQs, 1);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs, 1);
@@ -483,13 +482,14 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for TMA stores in
     // the spent phi(K) tiles (quarters 0, 1: K tile; 2, 3: its lo part)
     {
-      uint32_t r[16];
-      tmem_ld16(tl + kFQ + 16 * qc, r);
+      uint32_t r[16], r2[16];
+      tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
       float qv[16], o[16];
       load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        o[q] = (__uint_as_float(r[q]) + gd * zsnap[16 * qc + q]) * fminf(qv[q], 1.f);
+        o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zsnap[16 * qc + q]) *
+               fminf(qv[q], 1.f);
       uint8_t* sq = qc < 2 ? kt : sm.klo;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
