@@ -190,8 +190,8 @@ __device__ __forceinline__ void sync_tc() {
 // TMEM columns
 constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T; after the first epilogue, dphiQ (kFQ)
 constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
-constexpr uint32_t kFO = 256;   // 64: phi(Q) S_prev
-constexpr uint32_t kFS = 320;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
+constexpr uint32_t kFO = 256;   // 128: phi(Q) S_prev as phi(Q) S_hi (0..63) and phi(Q) S_lo (64..127)
+constexpr uint32_t kFS = 384;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
 constexpr uint32_t kFQ = 0;     // 128: dphiQ as two 64-column parts (P's columns, spent by then)
 constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
@@ -311,14 +311,12 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int k = 0; k < 4; ++k)  // W = G V^T
           mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
       }
-      // phi(Q) S_prev: B = the snapshot, rows d (= K), m contiguous (MN-major)
-      const uint32_t idO = idesc_bf16(128, 64, false, true);
+      // phi(Q) [S_hi | S_lo]: B = the snapshot, rows d (= K), m contiguous
+      // (MN-major), its hi and lo tiles the two 64-column N blocks (la - ha apart)
+      const uint32_t idO = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idO, k);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idO, 1);
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idO, k);
       mma_commit(sm.mma_bar);
       if (CAUSAL) {  // state increment, complete when the second group's barrier is:
         // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
@@ -368,14 +366,14 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this quarter. The Z dot
          // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
          // the rounding of phi(Q) cancels in num / den.
-        uint32_t ro[16];
-        tmem_ld16(tl + kFO + 16 * qc, ro);
+        uint32_t ro[16], ro2[16];
+        tmem_ld16x2(tl + kFO + 16 * qc, ro, tl + kFO + 64 + 16 * qc, ro2);
         float gv[16], qv[16];
         load_row16(gt, row, 2 * qc, gv);
         load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          npart += gv[q] * __uint_as_float(ro[q]);
+          npart += gv[q] * (__uint_as_float(ro[q]) + __uint_as_float(ro2[q]));
           dpart += qv[q] * zsnap[16 * qc + q];
         }
       }
@@ -625,10 +623,14 @@ __device__ __forceinline__ void phi_quarter_exact(uint8_t* tile, int row, int qc
   }
 }
 
-constexpr uint32_t kRP = 0;     // 128: P^T (rows keys), then bf16 P_L^T in [0, 64)
-constexpr uint32_t kRT = 128;   // 128: W^T = V G^T, then bf16 T_L^T in [128, 192)
-constexpr uint32_t kRV = 256;   // 64: dV
-constexpr uint32_t kRK = 320;   // 64: dphiK
+// The gradients accumulate as two 64-column parts each (the hi*lo partner
+// products of a hi/lo pair sit side by side in N = 128 MMAs) and are summed in
+// the epilogue.
+constexpr uint32_t kRP = 0;     // 128: P^T (rows keys), then bf16 P_L^T in [0, 64) and T_L^T hi in [64, 128)
+constexpr uint32_t kRH = 64;    // bf16 hi part of T_L^T
+constexpr uint32_t kRT = 128;   // 128: W^T = V G^T, spent by the first epilogue
+constexpr uint32_t kRV = 128;   // 128: dV parts (over W^T)
+constexpr uint32_t kRK = 256;   // 128: dphiK parts
 constexpr uint32_t kRR = 384;   // 64: this chunk's phi(Q)^T gN (M = 64 layout)
 constexpr uint32_t kRL = 448;   // 64: bf16 lo part of T_L^T
 
@@ -688,6 +690,18 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   };
   if (tid == 0)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
+  // the state terms, first into the gradient accumulators: dV = phi(K) [R_hi | R_lo]
+  // (B = R rows d read MN-major, n = m contiguous; hi and lo tiles la - ha apart)
+  // and dphiK = V [R_hi; R_lo]^T (B = R rows d read K-major, the lo rows after the hi)
+  auto issue_state_terms = [&](uint32_t ka, uint32_t va, uint32_t ha, uint32_t la) {
+    const uint32_t idVn = idesc_bf16(128, 128, false, true), idKn = idesc_bf16(128, 128, false, false);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idVn, k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idKn, k);
+  };
 
   float rrun[16];  // R row drow, columns [16 qc, 16 qc + 16) (dthread)
   float rr = 0.f;  // r[d] for d = tid < 64
@@ -782,22 +796,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int k = 0; k < 4; ++k)  // W^T = V G^T
           mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(ga + k * 32, 16, 1024), idP, k);
       }
-      // dV = phi(K) R_next: B = R rows d read MN-major (n = m contiguous)
-      const uint32_t idVn = idesc_bf16(128, 64, false, true);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(ha + k * 2048, 1024, 1024), idVn, k);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(la + k * 2048, 1024, 1024), idVn, 1);
-      // dphiK = V R_next^T: B = R rows d read K-major (k = m contiguous)
-      const uint32_t idKn = idesc_bf16(128, 64, false, false);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idKn, k);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(la + k * 32, 16, 1024), idKn, 1);
+      if (!CAUSAL) issue_state_terms(ka, va, ha, la);  // causal: in the second group
       mma_commit(sm.mma_bar);
       if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated:
         // phi(Q)^T hi and lo stacked as one M = 128 MN-major operand (ql - qa
@@ -850,27 +849,22 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       sync_tc();  // all reads of P^T, T^T done before the bf16 parts overwrite them
       tmem_st16(tl + kRP + 16 * qc, pph);
-      tmem_st16(tl + kRT + 16 * qc, pth);
+      tmem_st16(tl + kRH + 16 * qc, pth);
       tmem_st16(tl + kRL + 16 * qc, ptl);
       sync_tc();
       if (tid == 0) {
         const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
         const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
-        const uint32_t idV = idesc_bf16(128, 64, false, true);
+        issue_state_terms(smem_u32(kt), smem_u32(vt), smem_u32(sm.s_hi), smem_u32(sm.s_lo));
+        const uint32_t idV2 = idesc_bf16(128, 128, false, true), idV = idesc_bf16(128, 64, false, true);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T gN
-          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gha + k * 2048, 1024, 1024), idV, 1);
+        for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T [gN_hi | gN_lo] (N blocks gla - gha apart)
+          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gha + k * 2048, gla - gha, 1024), idV2, 1);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gla + k * 2048, 1024, 1024), idV, 1);
+        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_hi^T [phi(Q)_hi | phi(Q)_lo]
+          mma_ts(tbase + kRK, tbase + kRH + k * 8, sdesc(qa + k * 2048, ql - qa, 1024), idV2, 1);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_L^T phi(Q): hi*hi + hi*lo + lo*hi
-          mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ts(tbase + kRK, tbase + kRT + k * 8, sdesc(ql + k * 2048, 1024, 1024), idV, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
+        for (int k = 0; k < kC / 16; ++k)  // + T_lo^T phi(Q)_hi
           mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
         mma_commit(sm.mma_bar);
       }
@@ -884,13 +878,16 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // the spent phi(Q) hi / lo tiles (the R MMAs that read those ran before the second
     // group, whose completion was awaited)
     {
-      uint32_t r[16], w[16];
-      tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRV + 16 * qc, w);
+      uint32_t r[16], r2[16], w[16], w2[16];
+      tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRK + 64 + 16 * qc, r2);
+      tmem_ld16x2(tl + kRV + 16 * qc, w, tl + kRV + 64 + 16 * qc, w2);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(__uint_as_float(w[q]) + __uint_as_float(w2[q]));
       float kv[16], o[16];
       load_row16(kt, row, 2 * qc, kv);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        o[q] = (__uint_as_float(r[q]) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
+        o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
       uint8_t* sk = qc < 2 ? vt : gt;
       uint8_t* sv = qc < 2 ? qt : sm.qlo;
 #pragma unroll
