@@ -582,30 +582,29 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // T^T_ji = W^T_ji / den_i + gd_i with den_i, gd_i saved by the forward-direction
 // kernel.
 
-// Masked slice sl of a 128-column fp32 TMEM matrix -> bf16 hi/lo packs. LOWER
-// keeps j <= row (query rows), otherwise i >= row (key rows).
+// Masked slice sl of a 128-column fp32 TMEM matrix -> packed bf16. LOWER keeps
+// j <= row (query rows), otherwise i >= row (key rows).
 template <bool LOWER>
-__device__ __forceinline__ void masked_split_slice(uint32_t taddr, int sl, int lq, int row, uint32_t (&hi)[16],
-                                                   uint32_t (&lo)[16]) {
+__device__ __forceinline__ void masked_pack_slice(uint32_t taddr, int sl, int lq, int row, uint32_t (&hi)[16]) {
   const bool any = LOWER ? sl <= lq : sl >= lq;
   if (any) {  // warp-uniform
     uint32_t r[32];
     tmem_ld32(taddr + 32 * sl, r);
     if (sl != lq) {  // off the diagonal block: nothing is masked
 #pragma unroll
-      for (int c = 0; c < 16; ++c) split_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]), hi[c], lo[c]);
+      for (int c = 0; c < 16; ++c) hi[c] = pack_bf16(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
     } else {
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const int j0 = 32 * sl + 2 * c;
         const bool k0 = LOWER ? j0 <= row : j0 >= row;
         const bool k1 = LOWER ? j0 + 1 <= row : j0 + 1 >= row;
-        split_bf16(k0 ? __uint_as_float(r[2 * c]) : 0.f, k1 ? __uint_as_float(r[2 * c + 1]) : 0.f, hi[c], lo[c]);
+        hi[c] = pack_bf16(k0 ? __uint_as_float(r[2 * c]) : 0.f, k1 ? __uint_as_float(r[2 * c + 1]) : 0.f);
       }
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) hi[c] = lo[c] = 0u;
+    for (int c = 0; c < 16; ++c) hi[c] = 0u;
   }
 }
 
@@ -821,8 +820,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (CAUSAL) {
       // key row keeps query columns i >= row; slice qc of P^T and of T^T
-      uint32_t pph[16], ppl[16], pth[16], ptl[16];
-      masked_split_slice<false>(tl + kRP, qc, lq, row, pph, ppl);
+      uint32_t pph[16], pth[16], ptl[16];
+      masked_pack_slice<false>(tl + kRP, qc, lq, row, pph);  // P_L^T enters the MMA as bf16
       // T^T_ji = W^T_ji / den_i + gd_i (column-dependent scale and shift)
       if (qc >= lq) {  // warp-uniform
         uint32_t r[32];
@@ -878,26 +877,30 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // the spent phi(Q) hi / lo tiles (the R MMAs that read those ran before the second
     // group, whose completion was awaited)
     {
-      uint32_t r[16], r2[16], w[16], w2[16];
-      tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRK + 64 + 16 * qc, r2);
-      tmem_ld16x2(tl + kRV + 16 * qc, w, tl + kRV + 64 + 16 * qc, w2);
+      uint8_t* sk = qc < 2 ? vt : gt;
+      uint8_t* sv = qc < 2 ? qt : sm.qlo;
+      {
+        uint32_t w[16], w2[16];
+        tmem_ld16x2(tl + kRV + 16 * qc, w, tl + kRV + 64 + 16 * qc, w2);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(__uint_as_float(w[q]) + __uint_as_float(w2[q]));
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<float4*>(sv + sw128(row, (qc & 1) * 64 + c * 16)) = make_float4(
+              __uint_as_float(w[4 * c]) + __uint_as_float(w2[4 * c]),
+              __uint_as_float(w[4 * c + 1]) + __uint_as_float(w2[4 * c + 1]),
+              __uint_as_float(w[4 * c + 2]) + __uint_as_float(w2[4 * c + 2]),
+              __uint_as_float(w[4 * c + 3]) + __uint_as_float(w2[4 * c + 3]));
+      }
+      uint32_t r[16], r2[16];
+      tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRK + 64 + 16 * qc, r2);
       float kv[16], o[16];
       load_row16(kt, row, 2 * qc, kv);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
-      uint8_t* sk = qc < 2 ? vt : gt;
-      uint8_t* sv = qc < 2 ? qt : sm.qlo;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t off = sw128(row, (qc & 1) * 64 + c * 16);
-        *reinterpret_cast<float4*>(sk + off) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-        *reinterpret_cast<float4*>(sv + off) =
-            make_float4(__uint_as_float(w[4 * c]), __uint_as_float(w[4 * c + 1]),
-                        __uint_as_float(w[4 * c + 2]), __uint_as_float(w[4 * c + 3]));
-      }
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<float4*>(sk + sw128(row, (qc & 1) * 64 + c * 16)) =
+            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
     }
     fence_proxy_async_smem();
     sync_tc();
