@@ -734,11 +734,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       invs[tid] = 1.f / nden;
       gds[tid] = ngd;
     }
-    {
-      RevCursor nx = cc;
-      nx.advance(g);
-      fetch_dg(nx);
-    }
     if (first) {
       const float* src = rsuffix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (dthread) {
@@ -813,6 +808,11 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  idR, 1);
         mma_commit(&sm.sbar[1]);
       }
+    }
+    {  // the next chunk's den, gd: their latency hides behind the first MMA group
+      RevCursor nx = cc;
+      nx.advance(g);
+      fetch_dg(nx);
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 32)) break;
     ph ^= 1;
