@@ -262,12 +262,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool first = cc.chunk == g.chunk_begin(item);
     const bool last = cc.chunk + 1 == g.chunk_end(item);
     const int nvalid = min(kC, g.N - t0);
-    if (tid == 0) {
-      // the stage being refilled and the phi(K) lo tile held the previous chunk's dq
-      // staging: its TMA stores must have read them
-      bulk_wait_read<0>();
-      if (cp.valid(g)) issue(cp);
-    }
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
@@ -318,6 +312,10 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idO, k);
       mma_commit(sm.mma_bar);
+      // the next chunk's tiles go into the previous chunk's stage, whose dq staging
+      // TMA stores have had this chunk's phi to finish reading it
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
       if (CAUSAL) {  // state increment, complete when the second group's barrier is:
         // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
         // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
@@ -478,7 +476,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this quarter's
     // columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for TMA stores in
-    // the spent phi(K) tiles (quarters 0, 1: K tile; 2, 3: its lo part)
+    // the chunk's spent K and G tiles (quarters 0, 1: K tile; 2, 3: G tile)
     {
       uint32_t r[16], r2[16];
       tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
@@ -488,7 +486,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int q = 0; q < 16; ++q)
         o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zsnap[16 * qc + q]) *
                fminf(qv[q], 1.f);
-      uint8_t* sq = qc < 2 ? kt : sm.klo;
+      uint8_t* sq = qc < 2 ? kt : gt;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         *reinterpret_cast<float4*>(sq + sw128(row, (qc & 1) * 64 + c * 16)) =
@@ -498,7 +496,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     sync_tc();
     if (tid == 0) {  // rows past the sequence end are clipped by the tensor map
       tma_store_3d(&tm_dq, kt, 0, t0, bh);
-      tma_store_3d(&tm_dq, sm.klo, 32, t0, bh);
+      tma_store_3d(&tm_dq, gt, 32, t0, bh);
       bulk_commit();
     }
     // state MMAs of this chunk: the second group's barrier also covers dS,
@@ -724,12 +722,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
     const int nvalid = min(kC, g.N - t0);
-    if (tid == 0) {
-      // the stage being refilled and the phi(Q) lo tile held the previous chunk's
-      // dk / dv staging: its TMA stores must have read them
-      bulk_wait_read<0>();
-      if (cp.valid(g)) issue(cp);
-    }
     if (CAUSAL && tid < kC) {
       invs[tid] = 1.f / nden;
       gds[tid] = ngd;
@@ -792,6 +784,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (!CAUSAL) issue_state_terms(ka, va, ha, la);  // causal: in the second group
       mma_commit(sm.mma_bar);
+      // the next chunk's tiles go into the previous chunk's stage, whose dk / dv
+      // staging TMA stores have had this chunk's phi to finish reading it
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
       if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated:
         // phi(Q)^T hi and lo stacked as one M = 128 MN-major operand (ql - qa
         // bytes apart) times gN hi, then gN lo; rows d of the hi part in TMEM
@@ -814,6 +810,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       nx.advance(g);
       fetch_dg(nx);
     }
+    // phi'(k) of this quarter row, read before the barrier that precedes the dk / dv
+    // staging writes into the K tile
+    float kv[16];
+    if (!CAUSAL) load_row16(kt, row, 2 * qc, kv);
     if (!wait_uniform(sm.mma_bar, ph, hdr, 32)) break;
     ph ^= 1;
     fence_after_sync();
@@ -867,18 +867,19 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
         mma_commit(sm.mma_bar);
       }
+      load_row16(kt, row, 2 * qc, kv);
       if (!wait_uniform(sm.mma_bar, ph, hdr, 33)) break;
       ph ^= 1;
       fence_after_sync();
     }
 
     // dk = (dphiK + r_next) * phi'(k) and dv, this quarter's columns, staged in 128 x 32
-    // float32 boxes (128-byte swizzle) for TMA stores: dk in the spent V / G tiles, dv in
-    // the spent phi(Q) hi / lo tiles (the R MMAs that read those ran before the second
-    // group, whose completion was awaited)
+    // float32 boxes (128-byte swizzle) for TMA stores in the chunk's spent tiles: dk in
+    // V / G, dv in Q / K (the R MMAs that read Q ran before the second group, whose
+    // completion was awaited)
     {
       uint8_t* sk = qc < 2 ? vt : gt;
-      uint8_t* sv = qc < 2 ? qt : sm.qlo;
+      uint8_t* sv = qc < 2 ? qt : kt;
       {
         uint32_t w[16], w2[16];
         tmem_ld16x2(tl + kRV + 16 * qc, w, tl + kRV + 64 + 16 * qc, w2);
@@ -892,8 +893,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       uint32_t r[16], r2[16];
       tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRK + 64 + 16 * qc, r2);
-      float kv[16], o[16];
-      load_row16(kt, row, 2 * qc, kv);
+      float o[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
@@ -908,7 +908,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tma_store_3d(&tm_dk, vt, 0, t0, bh);
       tma_store_3d(&tm_dk, gt, 32, t0, bh);
       tma_store_3d(&tm_dv, qt, 0, t0, bh);
-      tma_store_3d(&tm_dv, sm.qlo, 32, t0, bh);
+      tma_store_3d(&tm_dv, kt, 32, t0, bh);
       bulk_commit();
     }
     if (CAUSAL) {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
