@@ -218,6 +218,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
+    mbar_init(&sm.sbar[0], 1);
     mbar_init(&sm.sbar[1], 1);
     fence_mbar_init();
   }
@@ -254,7 +255,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
   float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
-  uint32_t ph = 0, sph1 = 0;
+  uint32_t ph = 0, sph0 = 0, sph1 = 0;
   float z[16];
 
   while (cc.valid(g)) {
@@ -324,6 +325,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
           mma_ss(tbase + kFS, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS, k);
+        mma_commit(&sm.sbar[0]);
       }
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
@@ -470,6 +472,34 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                1);
       mma_commit(&sm.sbar[1]);
     }
+    if (CAUSAL) {  // S += dS while the second group runs: the lo-part rows pass
+                   // through the chunk's V tile (no MMA reads it any more)
+      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27)) break;
+      sph0 ^= 1;
+      fence_after_sync();
+      uint32_t r[16];
+      tmem_ld16(tl + kFS + 16 * qc, r);
+      float4* xs = reinterpret_cast<float4*>(vt);  // [64][16] float4, XOR-swizzled rows
+      if (!dthread) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+      __syncthreads();
+      if (dthread) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
+          srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
+          srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
+          srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
+          srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+        }
+      }
+      fence_proxy_async_smem();  // the V tile is a TMA destination again
+    }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
     ph ^= 1;
     fence_after_sync();
@@ -499,35 +529,10 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_store_3d(&tm_dq, gt, 32, t0, bh);
       bulk_commit();
     }
-    // state MMAs of this chunk: the second group's barrier also covers dS,
-    // issued earlier by the same thread
+    // the segment sums of phi(Q)^T gN (issued after the second group) are done
     if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
     sph1 ^= 1;
     fence_after_sync();
-    if (CAUSAL) {  // S += dS: the lo-part rows pass through the spent gN lo buffer
-      uint32_t r[16];
-      tmem_ld16(tl + kFS + 16 * qc, r);
-      float4* xs = reinterpret_cast<float4*>(sm.gn_lo);  // [64][16] float4, XOR-swizzled rows
-      if (!dthread) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      }
-      __syncthreads();
-      if (dthread) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
-          srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
-          srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
-          srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
-          srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
-        }
-      }
-      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
-    }
 
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
       // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
@@ -867,6 +872,35 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
         mma_commit(sm.mma_bar);
       }
+      {  // R_run += this chunk's phi(Q)^T gN and r += sum gd phi(Q), while the second
+         // group runs; the lo-part rows (lanes 64-127) pass through the chunk's G
+         // tile (no MMA reads it any more)
+        if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
+        sph ^= 1;
+        fence_after_sync();
+        uint32_t r[16];
+        tmem_ld16(tl + kRR + 16 * qc, r);
+        float4* xs = reinterpret_cast<float4*>(gt);  // [64][16] float4, XOR-swizzled rows
+        if (!dthread) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        __syncthreads();
+        if (dthread) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
+            rrun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
+            rrun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
+            rrun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
+            rrun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+          }
+        }
+        if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+      }
       load_row16(kt, row, 2 * qc, kv);
       if (!wait_uniform(sm.mma_bar, ph, hdr, 33)) break;
       ph ^= 1;
@@ -910,35 +944,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tma_store_3d(&tm_dv, qt, 0, t0, bh);
       tma_store_3d(&tm_dv, kt, 32, t0, bh);
       bulk_commit();
-    }
-    if (CAUSAL) {  // R_run += this chunk's phi(Q)^T gN; r += sum gd phi(Q)
-      if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
-      sph ^= 1;
-      fence_after_sync();
-      uint32_t r[16];
-      tmem_ld16(tl + kRR + 16 * qc, r);
-      // the lo-part rows (lanes 64-127) pass through the spent gN hi buffer
-      float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
-      if (!dthread) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      }
-      __syncthreads();
-      if (dthread) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
-          rrun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
-          rrun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
-          rrun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
-          rrun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
-        }
-      }
-      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
-      if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     }
     sync_tc();
     ++consumed;
