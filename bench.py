@@ -42,8 +42,8 @@ def load_peaks():
 
 # DRAM bytes per call measured with ncu (profiles/dram_traffic_la_calls_b4h8n16384.md) and the
 # kernel-source revision they were taken on; reported only while the sources still match.
-TRAFFIC_REVISION = "4433e8051a1d7b76"
-TRAFFIC_BYTES = {"la_backward": 1043.8e6, "la_forward": 397.8e6}
+TRAFFIC_REVISION = "5f0fba101878cad6"
+TRAFFIC_BYTES = {"la_backward": 1045.7e6, "la_forward": 397.9e6}
 
 
 def kernel_revision():
