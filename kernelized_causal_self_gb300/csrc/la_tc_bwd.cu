@@ -170,6 +170,18 @@ __device__ __forceinline__ float warp_column_sums16(float (&z)[16]) {
   return z[0] + __shfl_xor_sync(0xffffffffu, z[0], 16);
 }
 
+// Block-uniform wait for a tile stage, folded together with an optional wait
+// for the previous chunk's deferred MMAs (one barrier for both).
+__device__ __forceinline__ bool wait_uniform2(uint64_t* bar, uint32_t parity, uint64_t* bar2,
+                                              uint32_t parity2, bool use2, WorkspaceHeader* hdr,
+                                              int site) {
+  bool ok = mbar_wait(bar, parity);
+  if (use2) ok = mbar_wait(bar2, parity2) && ok;
+  const bool all = __syncthreads_and(ok ? 1 : 0) != 0;
+  if (!all && threadIdx.x == 0) record_timeout(hdr, site);
+  return all;
+}
+
 __device__ __forceinline__ void sync_tc() {
   fence_before_sync();
   __syncthreads();
@@ -256,6 +268,9 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0, sph0 = 0, sph1 = 0;
+  // the previous chunk's segment-sum MMAs (sbar[1]) are still to be waited for:
+  // they read phi(Q) lo and gN, which the next chunk rewrites
+  bool r_pending = false;
   float z[16];
 
   while (cc.valid(g)) {
@@ -281,7 +296,13 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* kt = sm.tile(s, kK);
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
-    if (!wait_uniform(&sm.full[s], (consumed / kBwdStages) & 1, hdr, 21)) break;
+    if (!wait_uniform2(&sm.full[s], (consumed / kBwdStages) & 1, &sm.sbar[1], sph1, r_pending, hdr, 21))
+      break;
+    if (r_pending) {
+      sph1 ^= 1;
+      r_pending = false;
+      fence_after_sync();
+    }
     phi_quarter_split(qt, sm.qlo, row, qc, kC, z);
     if (CAUSAL) {
       phi_quarter_split(kt, sm.klo, row, qc, nvalid, z);
@@ -529,12 +550,12 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_store_3d(&tm_dq, gt, 32, t0, bh);
       bulk_commit();
     }
-    // the segment sums of phi(Q)^T gN (issued after the second group) are done
-    if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
-    sph1 ^= 1;
-    fence_after_sync();
-
+    r_pending = true;  // the segment sums of phi(Q)^T gN, issued after the second group
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
+      if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
+      sph1 ^= 1;
+      r_pending = false;
+      fence_after_sync();
       // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
       // part for lq >= 2; the lo parts pass through the spent gN hi buffer
       float* dst = rpartial + (size_t)item * kStateFloats;
@@ -561,12 +582,13 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (tid < kDim) dst[kDim * kDim + tid] = rr;
       fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
+      sync_tc();  // every read of the exchange is done before gN hi is rewritten
     }
-    sync_tc();
     ++consumed;
     cc.advance(g);
   }
   pdl_trigger();
+  if (r_pending && tid == 0 && !mbar_wait(&sm.sbar[1], sph1)) record_timeout(hdr, 29);
   if (tid == 0) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
@@ -945,7 +967,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tma_store_3d(&tm_dv, kt, 32, t0, bh);
       bulk_commit();
     }
-    sync_tc();
     ++consumed;
     cc.advance(g);
   }
