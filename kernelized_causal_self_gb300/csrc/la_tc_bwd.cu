@@ -226,6 +226,9 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // S carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
   const int drow = 32 * (lq & 1) + lane;
   const bool dthread = lq < 2;
+  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
+  // stores) belong to warp 1's first thread, so that the two issue in parallel
+  const bool tma_thread = tid == 32;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -261,7 +264,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     ++issued;
     c.advance(g);
   };
-  if (tid == 0)
+  if (tma_thread)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
   float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
@@ -311,6 +314,12 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     fence_proxy_async_smem();
     sync_tc();
+    if (tma_thread) {
+      // the next chunk's tiles go into the previous chunk's stage, whose dq staging
+      // TMA stores have had this chunk's phi to finish reading it
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
+    }
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt), ga = smem_u32(gt);
       const uint32_t kl = smem_u32(sm.klo);
@@ -334,10 +343,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; k < 4; ++k)
         mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idO, k);
       mma_commit(sm.mma_bar);
-      // the next chunk's tiles go into the previous chunk's stage, whose dq staging
-      // TMA stores have had this chunk's phi to finish reading it
-      bulk_wait_read<0>();
-      if (cp.valid(g)) issue(cp);
       if (CAUSAL) {  // state increment, complete when the second group's barrier is:
         // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
         // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
@@ -545,7 +550,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     fence_proxy_async_smem();
     sync_tc();
-    if (tid == 0) {  // rows past the sequence end are clipped by the tensor map
+    if (tma_thread) {  // rows past the sequence end are clipped by the tensor map
       tma_store_3d(&tm_dq, kt, 0, t0, bh);
       tma_store_3d(&tm_dq, gt, 32, t0, bh);
       bulk_commit();
@@ -589,7 +594,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
   pdl_trigger();
   if (r_pending && tid == 0 && !mbar_wait(&sm.sbar[1], sph1)) record_timeout(hdr, 29);
-  if (tid == 0) {
+  if (tma_thread) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
       if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 26);
@@ -678,6 +683,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // R carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
   const int drow = 32 * (lq & 1) + lane;
   const bool dthread = lq < 2;
+  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
+  // stores) belong to warp 1's first thread, so that the two issue in parallel
+  const bool tma_thread = tid == 32;
 
   if (tid == 0) {
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
@@ -712,7 +720,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ++issued;
     c.advance(g);
   };
-  if (tid == 0)
+  if (tma_thread)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
   // the state terms, first into the gradient accumulators: dV = phi(K) [R_hi | R_lo]
   // (B = R rows d read MN-major, n = m contiguous; hi and lo tiles la - ha apart)
@@ -795,6 +803,12 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     fence_proxy_async_smem();
     sync_tc();
+    if (tma_thread) {
+      // the next chunk's tiles go into the previous chunk's stage, whose dk / dv
+      // staging TMA stores have had this chunk's phi to finish reading it
+      bulk_wait_read<0>();
+      if (cp.valid(g)) issue(cp);
+    }
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
       const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo), ql = smem_u32(sm.qlo);
@@ -811,10 +825,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (!CAUSAL) issue_state_terms(ka, va, ha, la);  // causal: in the second group
       mma_commit(sm.mma_bar);
-      // the next chunk's tiles go into the previous chunk's stage, whose dk / dv
-      // staging TMA stores have had this chunk's phi to finish reading it
-      bulk_wait_read<0>();
-      if (cp.valid(g)) issue(cp);
       if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated:
         // phi(Q)^T hi and lo stacked as one M = 128 MN-major operand (ql - qa
         // bytes apart) times gN hi, then gN lo; rows d of the hi part in TMEM
@@ -960,7 +970,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     fence_proxy_async_smem();
     sync_tc();
-    if (tid == 0) {  // rows past the sequence end are clipped by the tensor maps
+    if (tma_thread) {  // rows past the sequence end are clipped by the tensor maps
       tma_store_3d(&tm_dk, vt, 0, t0, bh);
       tma_store_3d(&tm_dk, gt, 32, t0, bh);
       tma_store_3d(&tm_dv, qt, 0, t0, bh);
@@ -971,7 +981,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     cc.advance(g);
   }
   pdl_trigger();
-  if (tid == 0) {
+  if (tma_thread) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
       if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 36);

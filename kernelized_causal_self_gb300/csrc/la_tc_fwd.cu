@@ -399,6 +399,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // of quarter 2 holds Z (the TMEM lanes the stacked increment lands in)
   const bool sthread = q4 < 2;
   const bool zthread = q4 == 2 && lane == 0;
+  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
+  // stores) belong to warp 1's first thread, so that the two issue in parallel
+  const bool tma_thread = tid == 32;
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
@@ -444,7 +447,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ++issued;
     c.advance(g);
   };
-  if (tid == 0)
+  if (tma_thread)
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
 
   // running state: S^T row `row` (sthread) or Z (zthread), columns [32h, 32h + 32)
@@ -461,7 +464,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int t0 = cc.chunk * kC;
     const bool first = cc.chunk == g.chunk_begin(item);
     const int nvalid = min(kC, g.len(bh) - t0);
-    if (!CAUSAL && tid == 0 && cp.valid(g)) {  // causal: issued after the first MMA group
+    if (!CAUSAL && tma_thread && cp.valid(g)) {  // causal: issued with the first MMA group
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
       issue(cp);
     }
@@ -557,13 +560,14 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mma_ss(tbase + kColO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idO, k);
       }
       mma_commit(mma_bar);
-      // causal: the next chunk's tiles are issued here rather than at the top
-      // of the iteration, so that the output store last read from that stage
-      // (issued at the end of the previous iteration) has drained by now
-      if (CAUSAL && cp.valid(g)) {
-        bulk_wait_read<0>();
-        issue(cp);
-      }
+    }
+    // causal: the next chunk's tiles are issued here, while thread 0 issues the
+    // first MMA group, rather than at the top of the iteration, so that the output
+    // store last read from that stage (issued at the end of the previous iteration)
+    // has drained by now
+    if (CAUSAL && tma_thread && cp.valid(g)) {
+      bulk_wait_read<0>();
+      issue(cp);
     }
     if (!wait_uniform(mma_bar, mma_phase, hdr, 12)) {
       ok = false;
@@ -671,7 +675,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (tid == 0) {
+    if (tma_thread) {
       tma_store_3d(&tm_o, qt, 0, t0, bh);
       bulk_commit();
     }
@@ -679,7 +683,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     cc.advance(g);
   }
   pdl_trigger();
-  if (tid == 0) {
+  if (tma_thread) {
     while (consumed < issued) {  // loads still in flight after an early exit
       const int s = consumed % kAttStages;
       if (!mbar_wait(&full[s], (consumed / kAttStages) & 1)) record_timeout(hdr, 14);
