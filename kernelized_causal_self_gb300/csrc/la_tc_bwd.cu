@@ -253,7 +253,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   long long issued = 0;
   auto issue = [&](Cursor& c) {
     const int s = issued % kBwdStages;
-    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    const int bh = c.bh, t0 = c.chunk * kC;
     mbar_arrive_expect_tx(&sm.full[s], tx);
     tma_load_3d(sm.tile(s, kQ), &tm_q, &sm.full[s], 0, t0, bh);
     tma_load_3d(sm.tile(s, kG), &tm_g, &sm.full[s], 0, t0, bh);
@@ -277,9 +277,9 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   float z[16];
 
   while (cc.valid(g)) {
-    const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
-    const bool first = cc.chunk == g.chunk_begin(item);
-    const bool last = cc.chunk + 1 == g.chunk_end(item);
+    const int item = cc.item, bh = cc.bh, t0 = cc.chunk * kC;
+    const bool first = cc.first();
+    const bool last = cc.last();
     const int nvalid = min(kC, g.N - t0);
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
@@ -709,7 +709,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   long long issued = 0;
   auto issue = [&](RevCursor& c) {
     const int s = issued % kBwdStages;
-    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    const int bh = c.bh, t0 = c.chunk * kC;
     mbar_arrive_expect_tx(&sm.full[s], tx);
     tma_load_3d(sm.tile(s, kK), &tm_k, &sm.full[s], 0, t0, bh);
     tma_load_3d(sm.tile(s, kV), &tm_v, &sm.full[s], 0, t0, bh);
@@ -746,7 +746,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (CAUSAL && tid < kC && c.valid(g)) {
       const int t = c.chunk * kC + tid;
       const bool valid = t < g.N;
-      const size_t at = (size_t)g.bh_of(c.item) * g.N + t;
+      const size_t at = (size_t)c.bh * g.N + t;
       nden = valid ? den_in[at] : 1.f;
       ngd = valid ? gd_in[at] : 0.f;
     }
@@ -754,8 +754,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   fetch_dg(cc);
 
   while (cc.valid(g)) {
-    const int item = cc.item, bh = g.bh_of(item), t0 = cc.chunk * kC;
-    const bool first = cc.chunk == g.chunk_end(item) - 1;  // first processed
+    const int item = cc.item, bh = cc.bh, t0 = cc.chunk * kC;
+    const bool first = cc.chunk == cc.cend - 1;  // first processed
     const int nvalid = min(kC, g.N - t0);
     if (CAUSAL && tid < kC) {
       invs[tid] = 1.f / nden;

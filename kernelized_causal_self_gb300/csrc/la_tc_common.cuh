@@ -38,18 +38,35 @@ struct Geometry {
   }
 };
 
-// Walks (item, chunk) pairs of this CTA in processing order.
+// Walks (item, chunk) pairs of this CTA in processing order. The item's
+// (batch, head) index and chunk range are worked out once per item (they take
+// integer divisions by runtime sizes), not per chunk.
 struct Cursor {
   int item, chunk;
+  int bh, cbeg, cend;  // of `item`
+  __device__ void set_item(const Geometry& g) {
+    bh = g.bh_of(item);
+    cbeg = g.chunk_begin(item);
+    cend = g.chunk_end(item);
+  }
   __device__ void start(const Geometry& g) {
     item = blockIdx.x;
-    chunk = item < g.n_items() ? g.chunk_begin(item) : 0;
+    chunk = 0;
+    if (item < g.n_items()) {
+      set_item(g);
+      chunk = cbeg;
+    }
   }
   __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
+  __device__ bool first() const { return chunk == cbeg; }
+  __device__ bool last() const { return chunk + 1 == cend; }
   __device__ void advance(const Geometry& g) {
-    if (++chunk >= g.chunk_end(item)) {
+    if (++chunk >= cend) {
       item += gridDim.x;
-      if (item < g.n_items()) chunk = g.chunk_begin(item);
+      if (item < g.n_items()) {
+        set_item(g);
+        chunk = cbeg;
+      }
     }
   }
 };
@@ -57,15 +74,28 @@ struct Cursor {
 // Same items as Cursor, but each item's chunks from last to first.
 struct RevCursor {
   int item, chunk;
+  int bh, cbeg, cend;  // of `item`
+  __device__ void set_item(const Geometry& g) {
+    bh = g.bh_of(item);
+    cbeg = g.chunk_begin(item);
+    cend = g.chunk_end(item);
+  }
   __device__ void start(const Geometry& g) {
     item = blockIdx.x;
-    chunk = item < g.n_items() ? g.chunk_end(item) - 1 : 0;
+    chunk = 0;
+    if (item < g.n_items()) {
+      set_item(g);
+      chunk = cend - 1;
+    }
   }
   __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
   __device__ void advance(const Geometry& g) {
-    if (--chunk < g.chunk_begin(item)) {
+    if (--chunk < cbeg) {
       item += gridDim.x;
-      if (item < g.n_items()) chunk = g.chunk_end(item) - 1;
+      if (item < g.n_items()) {
+        set_item(g);
+        chunk = cend - 1;
+      }
     }
   }
 };

@@ -114,8 +114,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (nm < nl && mbar_test_wait(&phid[nm % S], (uint32_t)((nm / S) & 1))) {
           fence_after_sync();
           const int s = (int)(nm % S);
-          const bool first = cm.chunk == g.chunk_begin(cm.item);
-          const bool last = cm.chunk + 1 == g.chunk_end(cm.item);
+          const bool first = cm.first();
+          const bool last = cm.last();
           const uint32_t acc = tbase + 128 * (nseg & 1);
           const uint32_t ka = smem_u32(stages + s * SB), va = ka + kTile, kl = ka + 2 * kTile;
           // The ones block of an operand is 16 token rows: every K step of 16
@@ -150,8 +150,8 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           const int s = (int)(nl % S);
           uint8_t* st = stages + s * SB;
           mbar_arrive_expect_tx(&full[s], 2 * kTile);
-          tma_load_3d(st, &tm_k, &full[s], 0, cl.chunk * kC, g.bh_of(cl.item));
-          tma_load_3d(st + kTile, &tm_v, &full[s], 0, cl.chunk * kC, g.bh_of(cl.item));
+          tma_load_3d(st, &tm_k, &full[s], 0, cl.chunk * kC, cl.bh);
+          tma_load_3d(st + kTile, &tm_v, &full[s], 0, cl.chunk * kC, cl.bh);
           cl.advance(g);
           ++nl;
           moved = true;
@@ -243,9 +243,9 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     bool ok = true;
     while (cc.valid(g)) {
       const int item = cc.item;
-      const int bh = g.bh_of(item);
+      const int bh = cc.bh;
       const int nvalid = min(kC, g.len(bh) - cc.chunk * kC);
-      const bool last = cc.chunk + 1 == g.chunk_end(item);
+      const bool last = cc.last();
       const int s = consumed % S;
       uint8_t* kt = stages + s * SB;
       uint8_t* vt = kt + kTile;
@@ -437,7 +437,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   auto issue = [&](Cursor& c) {
     const int s = issued % kAttStages;
     uint8_t* st = stages + s * 3 * kTile;
-    const int bh = g.bh_of(c.item), t0 = c.chunk * kC;
+    const int bh = c.bh, t0 = c.chunk * kC;
     mbar_arrive_expect_tx(&full[s], tx_bytes);
     tma_load_3d(st, &tm_q, &full[s], 0, t0, bh);
     if (CAUSAL) {
@@ -460,9 +460,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint32_t mma_phase = 0;
   while (cc.valid(g) && ok) {
     const int item = cc.item;
-    const int bh = g.bh_of(item);
+    const int bh = cc.bh;
     const int t0 = cc.chunk * kC;
-    const bool first = cc.chunk == g.chunk_begin(item);
+    const bool first = cc.first();
     const int nvalid = min(kC, g.len(bh) - t0);
     if (!CAUSAL && tma_thread && cp.valid(g)) {  // causal: issued with the first MMA group
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
