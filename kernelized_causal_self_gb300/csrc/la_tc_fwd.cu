@@ -4,7 +4,8 @@
 // the chunks into segments. Three kernels:
 //
 //  1. tc_state_kernel: per segment, the state increment
-//       dS^T = V^T phi(K)  (tcgen05, M=64 x N=64, K = tokens), dZ = sum_t phi(K_t)
+//       dS^T = V^T phi(K), dZ = sum_t phi(K_t)  (one tcgen05 group per chunk:
+//       [V^T; 1^T] phi(K), M = 128 with a stacked block of ones, K = tokens)
 //     ("Transformers are RNNs": S = sum_j phi(K_j) V_j^T, Z = sum_j phi(K_j);
 //     nubint.ai review, "Proposed method"; zhengyuhong.cn deck, slide 3).
 //  2. state_scan_kernel: exclusive prefix over segments (causal; deck slide 4:
@@ -19,8 +20,9 @@
 //     summary §3.3.2: training stays parallel); it equals it up to rounding.
 //
 // phi is applied in shared memory right after each TMA tile lands (bf16 in,
-// float32 math, bf16 out). The carried state is float32; it enters the
-// tensor cores as a bf16 hi + lo pair, so the inter-chunk term keeps ~16 bits.
+// float32 math, bf16 out). The carried state is float32; the read-out takes it
+// rounded to bf16 (each element independently), and the backward's precise
+// segment states enter the tensor cores as bf16 hi + lo pairs.
 #include <cuda_bf16.h>
 
 #include "la_tc_common.cuh"
