@@ -247,9 +247,11 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   pdl_wait();
 
   const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
+  // items last to first: the segment-state kernel just streamed k and v first to
+  // last, and the reverse-direction kernel then starts where this one ends
   Cursor cc, cp;
-  cc.start(g);
-  cp.start(g);
+  cc.start(g, true);
+  cp.start(g, true);
   long long issued = 0;
   auto issue = [&](Cursor& c) {
     const int s = issued % kBwdStages;

@@ -38,32 +38,39 @@ struct Geometry {
   }
 };
 
-// Walks (item, chunk) pairs of this CTA in processing order. The item's
-// (batch, head) index and chunk range are worked out once per item (they take
-// integer divisions by runtime sizes), not per chunk.
+// Walks (item, chunk) pairs of this CTA in processing order: the CTA's items
+// blockIdx.x, blockIdx.x + gridDim.x, ... first to last, or (back) last to
+// first, each item's chunks in order. A kernel that re-reads what a kernel
+// before it streamed walks its items back, so that it starts on the tiles the
+// other read last (the ones still in L2). The item's (batch, head) index and
+// chunk range are worked out once per item (they take integer divisions by
+// runtime sizes), not per chunk.
 struct Cursor {
   int item, chunk;
   int bh, cbeg, cend;  // of `item`
+  int step;            // +-gridDim.x
   __device__ void set_item(const Geometry& g) {
     bh = g.bh_of(item);
     cbeg = g.chunk_begin(item);
     cend = g.chunk_end(item);
   }
-  __device__ void start(const Geometry& g) {
+  __device__ void start(const Geometry& g, bool back = false) {
     item = blockIdx.x;
+    step = back ? -(int)gridDim.x : (int)gridDim.x;
+    if (back && item < g.n_items()) item += (g.n_items() - 1 - item) / (int)gridDim.x * (int)gridDim.x;
     chunk = 0;
-    if (item < g.n_items()) {
+    if (valid(g)) {
       set_item(g);
       chunk = cbeg;
     }
   }
-  __device__ bool valid(const Geometry& g) const { return item < g.n_items(); }
+  __device__ bool valid(const Geometry& g) const { return (unsigned)item < (unsigned)g.n_items(); }
   __device__ bool first() const { return chunk == cbeg; }
   __device__ bool last() const { return chunk + 1 == cend; }
   __device__ void advance(const Geometry& g) {
     if (++chunk >= cend) {
-      item += gridDim.x;
-      if (item < g.n_items()) {
+      item += step;
+      if (valid(g)) {
         set_item(g);
         chunk = cbeg;
       }

@@ -432,9 +432,10 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   pdl_wait();
 
   const uint32_t tx_bytes = CAUSAL ? 3 * kTile : kTile;
+  // items last to first: the segment-state kernel just streamed k and v first to last
   Cursor cc, cp;
-  cc.start(g);
-  cp.start(g);
+  cc.start(g, true);
+  cp.start(g, true);
   long long issued = 0;
   auto issue = [&](Cursor& c) {
     const int s = issued % kAttStages;
