@@ -52,7 +52,7 @@ enum la_status {
   LA_ERR_INVALID_ARG = 1, /* null pointer, bad dimension, unsupported D/M, misaligned pointer */
   LA_ERR_WORKSPACE = 2,   /* workspace missing or smaller than the *_workspace_bytes() size */
   LA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-  LA_ERR_TIMEOUT = 4,     /* a bounded cross-CTA wait expired (see la_workspace_status) */
+  LA_ERR_TIMEOUT = 4,     /* a bounded wait inside a kernel expired (see la_workspace_status) */
   LA_ERR_TOO_LARGE = 5    /* the problem needs more scratch than la_forward_noalloc holds */
 };
 
@@ -202,9 +202,10 @@ int la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
 /*
  * la_workspace_status -- synchronises `stream` and reads the status word a
  * previous la_forward / la_prefill / la_extend / la_backward left in
- * `workspace`: LA_OK; LA_ERR_TIMEOUT if a bounded cross-CTA wait gave up (the
- * outputs of that call are then invalid); LA_ERR_INVALID_ARG if la_extend met
- * a slot outside its pool. Clears the word. Debug / test use.
+ * `workspace`: LA_OK; LA_ERR_TIMEOUT if a bounded wait inside a kernel (for a
+ * TMA copy or a group of tensor-core MMAs) gave up, the outputs of that call
+ * then being invalid; LA_ERR_INVALID_ARG if la_extend met a slot outside its
+ * pool. Clears the word. Debug / test use.
  */
 int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream);
 

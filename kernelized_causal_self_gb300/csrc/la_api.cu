@@ -61,7 +61,7 @@ const char* la_status_string(int status) {
       return "invalid argument (null or misaligned pointer, bad dimension, or unsupported D/M/dtype)";
     case LA_ERR_WORKSPACE: return "workspace missing or too small";
     case LA_ERR_CUDA: return "CUDA runtime error";
-    case LA_ERR_TIMEOUT: return "a bounded cross-CTA wait expired; outputs are invalid";
+    case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel expired; outputs are invalid";
     case LA_ERR_TOO_LARGE:
       return "problem needs more scratch than la_forward_noalloc's fixed array holds";
     default: return "unknown status";

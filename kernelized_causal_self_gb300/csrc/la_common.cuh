@@ -30,10 +30,10 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 // Workspace header: the first 256 bytes of every workspace.
 struct WorkspaceHeader {
-  int status;          // LA_OK or LA_ERR_TIMEOUT, written by kernels
-  int wait_site;       // where a bounded wait gave up (debug)
-  unsigned int ticket; // dynamic work counter (reset before each launch)
-  unsigned int pad[61];
+  int status;     // LA_OK, LA_ERR_TIMEOUT (a bounded wait gave up) or LA_ERR_INVALID_ARG
+                  // (la_extend met a slot outside its pool), written by kernels
+  int wait_site;  // where a bounded wait gave up (debug)
+  unsigned int pad[62];
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header must stay 256 bytes");
 
