@@ -1,7 +1,9 @@
 """Thin Python binding over the C ABI in ``include/la.h``.
 
-Argument marshalling only: tensors are checked for device, dtype, shape and
-contiguity, their ``data_ptr()`` and the current CUDA stream are handed to the
+Argument marshalling only: every tensor is checked for shape and dtype against
+the layouts of ``include/la.h`` (sizes taken from ``q`` and ``v``), then for
+being a contiguous CUDA tensor on ``q``'s device, since the library sees only
+raw pointers; their ``data_ptr()`` and the current CUDA stream are handed to the
 shared library, and outputs/workspaces are allocated with PyTorch (the caller's
 allocator). Every step of the computation runs in the library's CUDA kernels;
 there is no fallback. If the library is missing the calls raise.
@@ -94,12 +96,31 @@ def _stream_ptr(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _need_cuda(*ts):
+def _need_cuda(*ts, device=None):
+    """Contiguous CUDA tensors, all on `device` (default: the first one's)."""
     for t in ts:
         if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError(f"tensors must all be on {device}, got one on {t.device}")
+
+
+def _expect(fn, name, t, shape, dtype):
+    """`t` has exactly `shape` and `dtype` (the library reads and writes that many elements)."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{fn}: {name} must be {dtype} of shape {tuple(shape)}, "
+                         f"got {t.dtype} of shape {tuple(t.shape)}")
+
+
+def _dims(fn, q, v, rank):
+    """(leading sizes of q, D, M) for q [..., D], v [..., M] of the given rank."""
+    if q.dim() != rank or v.dim() != rank:
+        raise ValueError(f"{fn}: q and v must have {rank} dimensions")
+    return tuple(q.shape[:-1]), q.shape[-1], v.shape[-1]
 
 
 def _workspace(nbytes, device, workspace):
@@ -107,6 +128,7 @@ def _workspace(nbytes, device, workspace):
     if workspace is not None:
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError("workspace too small")
+        _need_cuda(workspace, device=device)
         return workspace
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
@@ -127,16 +149,16 @@ def la_backward_workspace_bytes(B, H, N, D, M, causal=True, dtype=LA_BF16):
 def la_forward(q, k, v, causal=True, out=None, workspace=None):
     """out[B,H,N,M] = kernelized attention of q, k [B,H,N,D] and v [B,H,N,M]."""
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v)
-    B, H, N, D = q.shape
-    M = v.shape[-1]
-    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or not (q.dtype == k.dtype == v.dtype):
-        raise ValueError("q, k, v shapes/dtypes do not match")
+    (B, H, N), D, M = _dims("la_forward", q, v, 4)
+    _expect("la_forward", "k", k, q.shape, q.dtype)
+    _expect("la_forward", "v", v, (B, H, N, M), q.dtype)
+    if out is not None:
+        _expect("la_forward", "out", out, (B, H, N, M), q.dtype)
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, *([] if out is None else [out]))
+    lib = load_library()
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
-    _need_cuda(out)
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
     ws = _workspace(nbytes, q.device, workspace)
     st = lib.la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D, M,
@@ -154,14 +176,16 @@ def la_forward_noalloc(q, k, v, causal=True, out=None):
     made during stream capture.
     """
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v)
-    B, H, N, D = q.shape
-    M = v.shape[-1]
+    (B, H, N), D, M = _dims("la_forward_noalloc", q, v, 4)
+    _expect("la_forward_noalloc", "k", k, q.shape, q.dtype)
+    _expect("la_forward_noalloc", "v", v, (B, H, N, M), q.dtype)
+    if out is not None:
+        _expect("la_forward_noalloc", "out", out, (B, H, N, M), q.dtype)
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, *([] if out is None else [out]))
+    lib = load_library()
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
-    _need_cuda(out)
     st = lib.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
                                 D, M, int(bool(causal)), dt, _stream_ptr(q.device))
     _check("la_forward_noalloc", st)
@@ -171,16 +195,21 @@ def la_forward_noalloc(q, k, v, causal=True, out=None):
 def la_prefill(q, k, v, out=None, S=None, Z=None, workspace=None):
     """Causal forward plus the final float32 state S [B,H,D,M], Z [B,H,D]."""
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v)
-    B, H, N, D = q.shape
-    M = v.shape[-1]
+    fn, f32 = "la_prefill", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    given = [(n, t) for n, t in (("out", out), ("S", S), ("Z", Z)) if t is not None]
+    for name, t in given:
+        _expect(fn, name, t, {"out": (B, H, N, M), "S": (B, H, D, M), "Z": (B, H, D)}[name],
+                q.dtype if name == "out" else f32)
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, *[t for _, t in given])
+    lib = load_library()
     dev = q.device
     out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
-    S = torch.empty((B, H, D, M), dtype=torch.float32, device=dev) if S is None else S
-    Z = torch.empty((B, H, D), dtype=torch.float32, device=dev) if Z is None else Z
-    _need_cuda(out, S, Z)
+    S = torch.empty((B, H, D, M), dtype=f32, device=dev) if S is None else S
+    Z = torch.empty((B, H, D), dtype=f32, device=dev) if Z is None else Z
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
     ws = _workspace(nbytes, dev, workspace)
     st = lib.la_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S.data_ptr(),
@@ -200,24 +229,31 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspac
     lens[b] are unspecified.
     """
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v, S_pool, Z_pool)
-    B, H, N, D = q.shape
-    M = v.shape[-1]
+    fn, f32 = "la_extend", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    if S_pool.dim() != 4:
+        raise ValueError(f"{fn}: S_pool must be [pool, H, D, M]")
+    P = S_pool.shape[0]
+    _expect(fn, "S_pool", S_pool, (P, H, D, M), f32)
+    _expect(fn, "Z_pool", Z_pool, (P, H, D), f32)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, M), q.dtype)
+    for name, t in (("slots", slots), ("lens", lens)):
+        if t is not None and (t.dtype != torch.int32 or t.numel() != B):
+            raise ValueError(f"{name} must be a contiguous int32 tensor of B entries")
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, S_pool, Z_pool,
+               *[t for t in (out, slots, lens) if t is not None])
+    lib = load_library()
     dev = q.device
     out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
-    _need_cuda(out)
-    for name, t in (("slots", slots), ("lens", lens)):
-        if t is not None:
-            _need_cuda(t)
-            if t.dtype != torch.int32 or t.numel() != B:
-                raise ValueError(f"{name} must be a contiguous int32 tensor of B entries")
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
     ws = _workspace(nbytes, dev, workspace)
     st = lib.la_extend(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S_pool.data_ptr(),
                        Z_pool.data_ptr(), 0 if slots is None else slots.data_ptr(),
-                       0 if lens is None else lens.data_ptr(), S_pool.shape[0],
+                       0 if lens is None else lens.data_ptr(), P,
                        B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
                        _stream_ptr(dev))
     _check("la_extend", st)
@@ -227,17 +263,21 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspac
 def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace=None):
     """float32 gradients (dq, dk, dv) of sum(dout * la_forward(q, k, v))."""
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v, dout)
-    B, H, N, D = q.shape
-    M = v.shape[-1]
+    fn, f32 = "la_backward", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    _expect(fn, "dout", dout, (B, H, N, M), q.dtype)
+    given = [(n, t) for n, t in (("dq", dq), ("dk", dk), ("dv", dv)) if t is not None]
+    for name, t in given:
+        _expect(fn, name, t, (B, H, N, M) if name == "dv" else (B, H, N, D), f32)
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, dout, *[t for _, t in given])
+    lib = load_library()
     dev = q.device
-    f32 = torch.float32
     dq = torch.empty((B, H, N, D), dtype=f32, device=dev) if dq is None else dq
     dk = torch.empty((B, H, N, D), dtype=f32, device=dev) if dk is None else dk
     dv = torch.empty((B, H, N, M), dtype=f32, device=dev) if dv is None else dv
-    _need_cuda(dq, dk, dv)
     nbytes = lib.la_backward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
     ws = _workspace(nbytes, dev, workspace)
     st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
@@ -250,11 +290,17 @@ def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace
 def la_decode_step(q, k, v, S, Z, out=None):
     """One recurrent step: q, k [S,H,D], v [S,H,M]; S, Z updated in place; returns out."""
     import torch
-    lib = load_library()
-    _need_cuda(q, k, v, S, Z)
-    n, H, D = q.shape
-    M = v.shape[-1]
+    fn, f32 = "la_decode_step", torch.float32
+    (n, H), D, M = _dims(fn, q, v, 3)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (n, H, M), q.dtype)
+    _expect(fn, "S", S, (n, H, D, M), f32)
+    _expect(fn, "Z", Z, (n, H, D), f32)
+    if out is not None:
+        _expect(fn, "out", out, (n, H, M), q.dtype)
     dt = _dtype_code(q)
+    _need_cuda(q, k, v, S, Z, *([] if out is None else [out]))
+    lib = load_library()
     out = torch.empty((n, H, M), dtype=q.dtype, device=q.device) if out is None else out
     st = lib.la_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), S.data_ptr(), Z.data_ptr(),
                             out.data_ptr(), n, H, D, M, dt, _stream_ptr(q.device))
