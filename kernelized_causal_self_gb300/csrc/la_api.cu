@@ -34,6 +34,12 @@ bool valid_dims(int B, int H, int N, int D, int M) {
 
 bool valid_dtype(int dtype) { return dtype == LA_F32 || dtype == LA_BF16; }
 
+// Workspace queries: shapes that the entry points reject (including B * H
+// beyond an int) need only the header.
+bool query_dims_ok(int B, int H, int N) {
+  return B >= 1 && H >= 1 && N >= 0 && (long long)B * H <= 0x7fffffffLL;
+}
+
 bool ptrs_ok(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
     if (p == nullptr || !aligned16(p)) return false;
@@ -45,7 +51,7 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // The caller's workspace arrives with arbitrary contents: clear its header
-// (status word, work counters) on the stream before any kernel reads it.
+// (status word, wait site) on the stream before any kernel reads it.
 cudaError_t clear_header(void* ws, cudaStream_t st) {
   return cudaMemsetAsync(ws, 0, la::kHeaderBytes, st);
 }
@@ -76,7 +82,7 @@ unsigned long long la_kernel_launches(void) {
 
 size_t la_forward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
   (void)causal;
-  if (B < 1 || H < 1 || N < 0) return la::kHeaderBytes;
+  if (!query_dims_ok(B, H, N)) return la::kHeaderBytes;
   if (la::tc_forward_supported(D, M, dtype)) return la::tc_forward_workspace(B * H, N);
   return la::kHeaderBytes;
 }
@@ -162,7 +168,7 @@ int la_extend(const void* q, const void* k, const void* v, void* out, float* S_p
 
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
   (void)causal;
-  if (B < 1 || H < 1 || N < 0) return la::kHeaderBytes;
+  if (!query_dims_ok(B, H, N)) return la::kHeaderBytes;
   if (la::tc_forward_supported(D, M, dtype)) return la::tc_backward_workspace(B * H, N);
   return la::simt_backward_workspace(B * H, N);
 }

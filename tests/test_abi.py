@@ -131,3 +131,13 @@ def test_workspace_sizes(lib):
         d = lib.la_backward_workspace_bytes(4, 8, 16384, 64, 64, causal, 1)
         assert 256 <= c <= d
         assert a % 16 == 0 and c % 16 == 0
+
+
+def test_workspace_queries_of_rejected_shapes_need_only_the_header(lib):
+    # B * H beyond an int, and non-positive sizes: the entry points reject these,
+    # so the queries answer with the 256-byte header alone (no overflowed product)
+    # (65537 * 65537 wraps to +131073 in 32 bits, 46341 * 46341 to a negative int)
+    for B, H, N in ((65537, 65537, 128), (46341, 46341, 128), (0, 8, 16), (4, 8, -1)):
+        for causal in (0, 1):
+            assert lib.la_forward_workspace_bytes(B, H, N, 64, 64, causal, 1) == 256
+            assert lib.la_backward_workspace_bytes(B, H, N, 64, 64, causal, 1) == 256
