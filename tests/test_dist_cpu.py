@@ -51,3 +51,57 @@ def test_two_gloo_ranks_agree_on_max_time():
 def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.25, 1, None) == 3.25
+
+
+def _shard_worker(rank, world, port, q):
+    """Rank r holds tokens [r N / world, (r + 1) N / world) of every (b, h) sequence."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import numpy as np
+
+    import oracle
+    from kernelized_causal_self_gb300 import inputs
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        B, H, N, D, M = 2, 2, 90, 8, 6
+        xq, xk, xv = inputs.qkv(21, B, H, N, D, M, 0.5, inputs.F32)
+        lo, hi = rank * N // world, (rank + 1) * N // world
+        sq, sk, sv = xq[:, :, lo:hi], xk[:, :, lo:hi], xv[:, :, lo:hi]
+        # the one exchange: every shard's own sums (S_r, Z_r), all-gathered
+        _, S_r, Z_r = oracle.linearized_attention(sq, sk, sv)
+        packed = torch.from_numpy(np.concatenate([S_r.reshape(-1), Z_r.reshape(-1)]))
+        parts = [torch.empty_like(packed) for _ in range(world)]
+        dist.all_gather(parts, packed)
+        # the exclusive prefix over the shards before this one is the state it starts from
+        pre = sum((parts[r].numpy() for r in range(rank)), np.zeros_like(packed.numpy()))
+        S0 = pre[: B * H * D * M].reshape(B, H, D, M)
+        Z0 = pre[B * H * D * M:].reshape(B, H, D)
+        out, _, _ = oracle.recurrent_attention(sq, sk, sv, S0=S0, Z0=Z0)
+        q.put((rank, out, oracle.forward(xq, xk, xv, True)[:, :, lo:hi]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sequence_shards_with_an_exclusive_state_prefix_equal_the_causal_forward():
+    """Sequence sharding needs one exchange: the exclusive prefix over the shards'
+    (S, Z) sums. Two gloo ranks, each holding half of every sequence, reproduce the
+    unsharded causal forward (fp64 oracle on both sides)."""
+    import numpy as np
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_shard_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted((q.get(timeout=120) for _ in range(world)), key=lambda t: t[0])
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, out, want in got:
+        np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-13)
+    # the prefix matters: the second half run from a zero state is far from the truth
+    import oracle
+    from kernelized_causal_self_gb300 import inputs
+    xq, xk, xv = inputs.qkv(21, 2, 2, 90, 8, 6, 0.5, inputs.F32)
+    alone = oracle.recurrent_attention(xq[:, :, 45:], xk[:, :, 45:], xv[:, :, 45:])[0]
+    assert np.max(np.abs(alone - got[1][2])) > 1e-2
