@@ -40,7 +40,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS)
 
 
-# DRAM bytes per call measured with ncu (profiles/dram_traffic_la_calls_b4h8n16384.md) and the
+# DRAM bytes per call measured with ncu (read + write, summed over the call's kernels) and the
 # kernel-source revision they were taken on; reported only while the sources still match.
 TRAFFIC_REVISION = "f6d72013e5eef699"
 TRAFFIC_BYTES = {"la_backward": 1047.5e6, "la_forward": 398.2e6}
@@ -223,8 +223,16 @@ def device_inputs(w, device, dout=False):
 
 
 def l2_flush_buffer(device):
+    """256 MB (twice the L2) read between timed calls to evict what the last call left."""
     import torch
-    return torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    return torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
+
+
+def flush_l2(buf):
+    """Evict L2 by reading `buf` (a reduction, outside the timed region). A read leaves clean
+    lines behind, so the next timed call pays no write-back of the flush's own lines, and the
+    dirty lines of the previous call are written back here rather than inside the next one."""
+    buf.sum()
 
 
 def time_calls(fn, reps, warm, flush=None):
@@ -236,7 +244,7 @@ def time_calls(fn, reps, warm, flush=None):
     times = []
     for _ in range(reps):
         if flush is not None:
-            flush.zero_()
+            flush_l2(flush)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(st)
@@ -267,7 +275,8 @@ def run_parts(la, device, peaks, reps=10):
         gbs = th * fwd_bytes(w) / (ms * 1e-3) / 1e9
         key = ("causal_fwd_b4h8n16384d64" if name == MAIN else name)
         parts[key] = {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms": ms,
-                      "hbm_gbs": gbs, "roofline_frac": gbs / hbm, "l2": "flushed between calls"}
+                      "hbm_gbs": gbs, "roofline_frac": gbs / hbm,
+                      "l2": "flushed between calls (256 MB read)"}
         del q, k, v, out
     # decode: prefill, then the per-token steps replayed from a CUDA graph
     w = inputs.WORKLOADS["decode_s256h8d64_prefill1024_steps3072"]
@@ -310,6 +319,9 @@ def run_parts(la, device, peaks, reps=10):
         "tokens_per_s": w.B * T / (ms * 1e-3), "ms_per_step": per_step, "hbm_gbs": gbs,
         "roofline_frac": gbs / hbm, "steps": T, "launch": "CUDA graph of 3072 la_decode_step calls",
         "l2": "S/Z state (33.5 MB) fits in L2; fraction can exceed 1"}
+    # decode with a state too large for L2: DECODE_HBM_STREAMS streams x 8 heads (134 MB of S),
+    # so every step reads and writes S in HBM
+    parts[f"decode_s{DECODE_HBM_STREAMS}h{w.H}d{w.D}_hbm"] = decode_hbm_part(la, w, device, hbm)
     # extend: EXTEND_TOKENS new tokens per stream from states in a pool, one call
     fn = extend_setup(la, w, g, device, S0, Z0)
     ms = statistics.median(time_calls(fn, reps, 3, flush))
@@ -317,8 +329,65 @@ def run_parts(la, device, peaks, reps=10):
     parts[f"extend_s256h8d64_t{EXTEND_TOKENS}_pool{EXTEND_POOL}"] = {
         "tokens_per_s": w.B * EXTEND_TOKENS / (ms * 1e-3), "ms": ms, "hbm_gbs": gbs,
         "roofline_frac": gbs / hbm, "same_tokens_as_decode_steps_ms": per_step * EXTEND_TOKENS,
-        "launch": "one la_extend call", "l2": "flushed between calls"}
+        "launch": "one la_extend call", "l2": "flushed between calls (256 MB read)"}
     return parts
+
+
+DECODE_HBM_STREAMS, DECODE_HBM_STEPS, DECODE_HBM_PREFILL = 1024, 128, 128
+
+
+def decode_hbm_part(la, w, device, hbm):
+    """Decode steps over DECODE_HBM_STREAMS streams (the decode workload's heads, head size and
+    inputs' distribution), whose float32 S/Z state (134 MB) exceeds the 129 MB L2: a prefill of
+    DECODE_HBM_PREFILL tokens builds it, then a CUDA graph of DECODE_HBM_STEPS steps is timed."""
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    n, T = DECODE_HBM_STREAMS, DECODE_HBM_STEPS
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 1)
+    shp = (n, w.H, DECODE_HBM_PREFILL)
+    q = inputs.torch_normal(g, shp + (w.D,), w.scale, w.dtype, device)
+    k = inputs.torch_normal(g, shp + (w.D,), w.scale, w.dtype, device)
+    v = inputs.torch_normal(g, shp + (w.M,), w.scale, w.dtype, device)
+    _, S, Z = la.la_prefill(q, k, v)
+    del q, k, v
+    sq = inputs.torch_normal(g, (T, n, w.H, w.D), w.scale, w.dtype, device)
+    sk = inputs.torch_normal(g, (T, n, w.H, w.D), w.scale, w.dtype, device)
+    sv = inputs.torch_normal(g, (T, n, w.H, w.M), w.scale, w.dtype, device)
+    outs = torch.empty((T, n, w.H, w.M), dtype=sq.dtype, device=device)
+    S0, Z0 = S.clone(), Z.clone()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for t in range(3):
+            la.la_decode_step(sq[t], sk[t], sv[t], S, Z, out=outs[t])
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(T):
+            la.la_decode_step(sq[t], sk[t], sv[t], S, Z, out=outs[t])
+
+    def replay():
+        S.copy_(S0)
+        Z.copy_(Z0)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    replay()
+    ms = statistics.median([replay() for _ in range(3)])
+    per_step = ms / T
+    gbs = n * w.H * decode_bytes(w) / (per_step * 1e-3) / 1e9
+    return {"tokens_per_s": n * T / (ms * 1e-3), "ms_per_step": per_step, "hbm_gbs": gbs,
+            "roofline_frac": gbs / hbm, "steps": T, "streams": n,
+            "launch": f"CUDA graph of {T} la_decode_step calls",
+            "l2": f"S/Z state ({n * w.H * (w.D * w.M + w.D) * 4 / 1e6:.0f} MB) exceeds L2: "
+                  "an HBM-bound step"}
 
 
 def run_ours(args, world, rank, local):
@@ -526,65 +595,93 @@ def run_e2e(la, w, q, k, v, dout, device, K):
                     f"{nb} batch slices pipelined over copy-in, compute and copy-out streams"}
 
 
-def cpu_baseline(w, budget_s=20.0):
-    """fp64 oracle (as it stands) on host cores: causal forward + backward of one (b, h)
-    sequence per sample, as many samples as fit in ~budget_s."""
-    import numpy as np
+def _oracle_worker_init():
+    """Pool worker set-up: one BLAS/OpenMP thread per process (the pool supplies the cores)."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    import oracle  # noqa: F401  (import cost kept out of the timed map)
+
+
+def _oracle_fwdbwd(task):
+    """Causal forward + backward of one (b, h) sequence of `n` positions with the fp64 oracle,
+    as it stands; the inputs are drawn like the workload's (seed, sample index)."""
+    seed, idx, n, D, M, scale, dtype = task
     import oracle
     from kernelized_causal_self_gb300 import inputs
-    n = w.N
-    q, k, v = inputs.qkv(w.seed, 1, 1, n, w.D, w.M, w.scale, w.dtype)
-    g = inputs.upstream_grad(w.seed, 1, 1, n, w.M, w.scale, w.dtype)
+    q, k, v = inputs.qkv(seed * 100003 + idx, 1, 1, n, D, M, scale, dtype)
+    g = inputs.upstream_grad(seed * 100003 + idx, 1, 1, n, M, scale, dtype)
     q, k, v, g = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
     t0 = time.perf_counter()
-    done = 0
-    while True:
-        oracle.forward(q, k, v, True)
-        oracle.backward(q, k, v, g, True)
-        done += 1
-        if time.perf_counter() - t0 > budget_s or done >= 4:
-            break
-    sec = time.perf_counter() - t0
-    tokens = done * n / w.H           # one head of N positions = N/H token-equivalents
-    return {"value": tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} x (one (b,h) sequence, N={n}, causal fwd + bwd, float64 NumPy, "
-                      f"single thread), {sec:.1f} s"}
+    oracle.forward(q, k, v, True)
+    oracle.backward(q, k, v, g, True)
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """The fp64 oracle on the host's cores: one worker process per core, started with `spawn`
+    (safe after CUDA has been initialised), each running whole (b, h) sequences."""
+
+    def __init__(self, cores=None):
+        import multiprocessing as mp
+        self.cores = int(cores or os.cpu_count() or 1)
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init)
+
+    def run(self, w, n, n_seq, offset=0):
+        """Wall time (s) of n_seq sequences of n positions spread over the workers."""
+        tasks = [(w.seed, offset + i, n, w.D, w.M, w.scale, w.dtype) for i in range(n_seq)]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_fwdbwd, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(w):
+    """fp64 oracle (as it stands) on the host's cores: causal forward + backward of whole (b, h)
+    sequences of the workload, one sequence per core, timed after a warm-up round."""
+    pool = OraclePool()
+    try:
+        pool.run(w, 256, pool.cores)                  # workers up, imports done
+        sec = pool.run(w, w.N, pool.cores, offset=1000)
+    finally:
+        pool.close()
+    tokens = pool.cores * w.N / w.H   # one head of N positions = N/H token-equivalents
+    return {"value": tokens / sec, "unit": "tokens/s", "cores": pool.cores,
+            "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": f"{pool.cores} (b,h) sequences of N={w.N} (one per core, {pool.cores} worker "
+                      f"processes), causal fwd + bwd, float64 NumPy recurrence, {sec:.1f} s wall"}
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the fp64 oracle on the host, a bounded sample per step."""
+    """Reference arm: the fp64 oracle on the host's cores, a bounded sample per step."""
     if rank != 0:
         return
     from kernelized_causal_self_gb300 import inputs
-    import oracle
     w = inputs.WORKLOADS[MAIN]
-    n = 2048   # first 2048 positions of one (b, h) sequence per step
-    q, k, v = inputs.qkv(w.seed, 1, 1, n, w.D, w.M, w.scale, w.dtype)
-    g = inputs.upstream_grad(w.seed, 1, 1, n, w.M, w.scale, w.dtype)
-    q, k, v, g = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
-
-    def step():
-        oracle.forward(q, k, v, True)
-        oracle.backward(q, k, v, g, True)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    sec = (time.perf_counter() - t0) / args.steps
-    value = (n / w.H) / sec
-    sample = (f"per step: causal fwd + bwd of the first {n} positions of one (b,h) sequence "
-              f"of {MAIN}, float64 NumPy oracle, single thread")
+    n = 2048   # first 2048 positions of one (b, h) sequence per core per step
+    pool = OraclePool()
+    try:
+        for i in range(args.warmup):
+            pool.run(w, n, pool.cores, offset=i * pool.cores)
+        secs = [pool.run(w, n, pool.cores, offset=(args.warmup + i) * pool.cores)
+                for i in range(args.steps)]
+    finally:
+        pool.close()
+    sec = sum(secs) / len(secs)
+    value = pool.cores * (n / w.H) / sec
+    sample = (f"per step: causal fwd + bwd of {n} positions of {pool.cores} (b,h) sequences of "
+              f"{MAIN} (one per core, {pool.cores} worker processes), float64 NumPy oracle")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
-                   "sample_positions": n},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                   "sample_positions": n, "sequences_per_step": pool.cores},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": pool.cores, "kind": "oracle",
+                         "host_cpus": os.cpu_count(), "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -625,11 +722,42 @@ def run_part(args):
                       "median_ms": statistics.median(t)}), flush=True)
 
 
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n, argv, script=None):
+    """Run `script` (this file by default) as n local processes, one per GPU: rank r gets
+    RANK = LOCAL_RANK = r, WORLD_SIZE = n and a 127.0.0.1 rendezvous, as torchrun would set
+    them. The replicas share nothing on the data path; they meet only at the barriers around
+    the timed region and in the max over ranks. Returns the worst exit code."""
+    port = str(_free_port())
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=port)
+        procs.append(subprocess.Popen([sys.executable, script or os.path.abspath(__file__), *argv],
+                                      env=env))
+    codes = [p.wait() for p in procs]
+    return max(codes, key=abs)
+
+
 def main():
     args = parse()
     if args.part is not None:
         run_part(args)
         return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by torchrun: start the replicas here, one process per GPU
+        if args.impl == "ours":
+            import torch
+            if torch.cuda.device_count() < args.gpus:
+                sys.exit(f"bench.py --gpus {args.gpus}: only {torch.cuda.device_count()} CUDA "
+                         "device(s) visible")
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

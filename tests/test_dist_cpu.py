@@ -105,3 +105,57 @@ def test_sequence_shards_with_an_exclusive_state_prefix_equal_the_causal_forward
     xq, xk, xv = inputs.qkv(21, 2, 2, 90, 8, 6, 0.5, inputs.F32)
     alone = oracle.recurrent_attention(xq[:, :, 45:], xk[:, :, 45:], xv[:, :, 45:])[0]
     assert np.max(np.abs(alone - got[1][2])) > 1e-2
+
+
+# The stand-in for bench.py's step used below: the same rank set-up, barrier and
+# max over ranks that run_ours uses, with no GPU work in between.
+_STUB_STEP = '''
+import json, sys
+sys.path.insert(0, {root!r})
+import torch
+import bench
+world, rank, local = bench.dist_setup(None)
+bench.barrier(world)
+t = bench.max_over_ranks(1.0 + rank, world, torch.device("cpu"))
+if rank == 0:
+    print(json.dumps({{"n_gpus": world, "ms": t, "local_rank": local}}), flush=True)
+bench.barrier(world)
+if world > 1:
+    import torch.distributed as dist
+    dist.destroy_process_group()
+'''
+
+
+def test_gpus_flag_starts_one_replica_per_gpu(tmp_path, capfd):
+    """bench.py --gpus 2 outside torchrun starts two ranks itself (RANK, LOCAL_RANK,
+    WORLD_SIZE, 127.0.0.1 rendezvous); they meet in the barrier and the max over
+    ranks, and rank 0 alone prints, with n_gpus = 2."""
+    import json
+
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    stub = tmp_path / "stub_step.py"
+    stub.write_text(_STUB_STEP.format(root=root))
+    assert bench.launch_replicas(2, ["--gpus", "2"], script=str(stub)) == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    got = json.loads(lines[0])
+    assert got == {"n_gpus": 2, "ms": 2.0, "local_rank": 0}
+
+
+def test_gpus_flag_refuses_more_gpus_than_visible(monkeypatch):
+    import sys
+
+    import bench
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "2"])
+    monkeypatch.setattr(torch.cuda, "device_count", lambda: 1)
+    started = []
+    monkeypatch.setattr(bench, "launch_replicas", lambda *a, **k: started.append(a) or 0)
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert "only 1 CUDA device" in str(e.value.code) and not started
+    monkeypatch.setattr(torch.cuda, "device_count", lambda: 2)
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert e.value.code == 0 and started == [(2, ["--gpus", "2"])]
