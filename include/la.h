@@ -200,6 +200,24 @@ int la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
                        int B, int H, int N, int D, int M, int causal, int dtype, void* stream);
 
 /*
+ * la_forward_noalloc_status -- the status word of the fixed scratch array on
+ * the current device, as la_workspace_status reads a caller's workspace:
+ * synchronises `stream`, returns LA_OK or the LA_ERR_TIMEOUT a bounded wait of
+ * the last la_forward_noalloc call recorded (its outputs are then invalid),
+ * and clears the word. Each la_forward_noalloc call clears it on entry, so it
+ * describes the last call only. Allocates nothing.
+ */
+int la_forward_noalloc_status(void* stream);
+
+/*
+ * la_debug_noalloc_set_status -- test hook (no counterpart on the pages):
+ * writes `status` and `wait_site` into the status header of the fixed scratch
+ * array on the current device, as a kernel whose bounded wait ran out would,
+ * so that tests can check la_forward_noalloc_status reads and clears it.
+ */
+int la_debug_noalloc_set_status(int status, int wait_site, void* stream);
+
+/*
  * la_workspace_status -- synchronises `stream` and reads the status word a
  * previous la_forward / la_prefill / la_extend / la_backward left in
  * `workspace`: LA_OK; LA_ERR_TIMEOUT if a bounded wait inside a kernel (for a
@@ -208,6 +226,47 @@ int la_forward_noalloc(const void* q, const void* k, const void* v, void* out,
  * pool. Clears the word. Debug / test use.
  */
 int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * la_workspace_wait_site -- synchronises `stream` and returns the code of the
+ * bounded wait that last gave up in the call that used `workspace` (0 if none
+ * did; -1 if the header cannot be read). The codes are internal to the
+ * kernels; the two the failure test hooks below make run out are
+ * LA_SITE_FORWARD_LOAD and LA_SITE_BACKWARD_LOAD. Does not clear anything.
+ */
+enum la_wait_site {
+  LA_SITE_FORWARD_LOAD = 11,  /* forward chunk-attention kernel, waiting for a chunk's tiles */
+  LA_SITE_BACKWARD_LOAD = 21  /* backward forward-direction kernel, waiting for a chunk's tiles */
+};
+int la_workspace_wait_site(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Failure-detection test hooks (the pages have no counterpart; test use only).
+ *
+ * la_debug_forward_fault / la_debug_backward_fault run la_forward /
+ * la_backward on the tensor-core path (bf16, D = M = 64) with one TMA load
+ * withheld: CTA 0 of the main kernel (the forward's chunk attention, the
+ * backward's forward-direction kernel) skips issuing its load number
+ * `withhold_load` (counted from 0 in its own issue order), so the wait for it
+ * can only run out, and bounds its main-loop waits by `wait_limit_ns`
+ * (1 us .. 2 s; every other wait keeps the normal 2 s limit). Nothing faults:
+ * the CTA records LA_ERR_TIMEOUT and the wait site in the workspace header,
+ * waits (with the full limit) for its issued copies and MMAs, frees its tensor
+ * memory and returns; the other CTAs finish normally. The outputs are then
+ * invalid. If CTA 0 issues fewer loads than withhold_load + 1 nothing is
+ * withheld. Returns LA_ERR_INVALID_ARG off the tensor-core path, for
+ * withhold_load < 0 or a limit out of range; otherwise as la_forward /
+ * la_backward.
+ */
+int la_debug_forward_fault(const void* q, const void* k, const void* v, void* out,
+                           int B, int H, int N, int D, int M, int causal, int dtype,
+                           void* workspace, size_t workspace_bytes, int withhold_load,
+                           unsigned long long wait_limit_ns, void* stream);
+int la_debug_backward_fault(const void* q, const void* k, const void* v, const void* dout,
+                            float* dq, float* dk, float* dv,
+                            int B, int H, int N, int D, int M, int causal, int dtype,
+                            void* workspace, size_t workspace_bytes, int withhold_load,
+                            unsigned long long wait_limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -19,11 +19,14 @@ __all__ = [
     "load_library",
     "LAError", "LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_WORKSPACE", "LA_ERR_CUDA",
     "LA_ERR_TIMEOUT", "LA_ERR_TOO_LARGE", "LA_F32", "LA_BF16", "la_forward_noalloc",
+    "la_forward_noalloc_status", "la_workspace_wait_site",
+    "LA_SITE_FORWARD_LOAD", "LA_SITE_BACKWARD_LOAD",
 ]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 LA_ERR_TOO_LARGE = 5
 LA_F32, LA_BF16 = 0, 1
+LA_SITE_FORWARD_LOAD, LA_SITE_BACKWARD_LOAD = 11, 21
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "liblagb300.so")
@@ -44,6 +47,13 @@ _SIGNATURES = {
     "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
     "la_forward_noalloc": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp]),
+    "la_forward_noalloc_status": (_c_int, [_vp]),
+    "la_debug_noalloc_set_status": (_c_int, [_c_int, _c_int, _vp]),
+    "la_workspace_wait_site": (_c_int, [_vp, _c_size, _vp]),
+    "la_debug_forward_fault": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _c_int,
+                                                                    ctypes.c_ulonglong, _vp]),
+    "la_debug_backward_fault": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _c_int,
+                                                                     ctypes.c_ulonglong, _vp]),
 }
 
 
@@ -89,6 +99,14 @@ def _dtype_code(t):
     if t.dtype == torch.bfloat16:
         return LA_BF16
     raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _on_device(device):
+    """Context that makes `device` current around a library call: the library looks up
+    per-device state (la_forward_noalloc's fixed scratch) on the current device, and the
+    stream it is handed belongs to `device`."""
+    import torch
+    return torch.cuda.device(device)
 
 
 def _stream_ptr(device):
@@ -161,9 +179,10 @@ def la_forward(q, k, v, causal=True, out=None, workspace=None):
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
     ws = _workspace(nbytes, q.device, workspace)
-    st = lib.la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D, M,
-                        int(bool(causal)), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
-                        _stream_ptr(q.device))
+    with _on_device(q.device):
+        st = lib.la_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, D,
+                            M, int(bool(causal)), dt, ws.data_ptr(),
+                            ws.numel() * ws.element_size(), _stream_ptr(q.device))
     _check("la_forward", st)
     return out
 
@@ -186,8 +205,9 @@ def la_forward_noalloc(q, k, v, causal=True, out=None):
     lib = load_library()
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
-    st = lib.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
-                                D, M, int(bool(causal)), dt, _stream_ptr(q.device))
+    with _on_device(q.device):
+        st = lib.la_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                    N, D, M, int(bool(causal)), dt, _stream_ptr(q.device))
     _check("la_forward_noalloc", st)
     return out
 
@@ -212,9 +232,10 @@ def la_prefill(q, k, v, out=None, S=None, Z=None, workspace=None):
     Z = torch.empty((B, H, D), dtype=f32, device=dev) if Z is None else Z
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.la_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S.data_ptr(),
-                        Z.data_ptr(), B, H, N, D, M, dt, ws.data_ptr(),
-                        ws.numel() * ws.element_size(), _stream_ptr(dev))
+    with _on_device(dev):
+        st = lib.la_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S.data_ptr(),
+                            Z.data_ptr(), B, H, N, D, M, dt, ws.data_ptr(),
+                            ws.numel() * ws.element_size(), _stream_ptr(dev))
     _check("la_prefill", st)
     return out, S, Z
 
@@ -251,11 +272,13 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspac
     out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
     nbytes = lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.la_extend(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S_pool.data_ptr(),
-                       Z_pool.data_ptr(), 0 if slots is None else slots.data_ptr(),
-                       0 if lens is None else lens.data_ptr(), P,
-                       B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
-                       _stream_ptr(dev))
+    with _on_device(dev):
+        st = lib.la_extend(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           S_pool.data_ptr(), Z_pool.data_ptr(),
+                           0 if slots is None else slots.data_ptr(),
+                           0 if lens is None else lens.data_ptr(), P,
+                           B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                           _stream_ptr(dev))
     _check("la_extend", st)
     return out
 
@@ -280,9 +303,11 @@ def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace
     dv = torch.empty((B, H, N, M), dtype=f32, device=dev) if dv is None else dv
     nbytes = lib.la_backward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
-                         dk.data_ptr(), dv.data_ptr(), B, H, N, D, M, int(bool(causal)), dt,
-                         ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(dev))
+    with _on_device(dev):
+        st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, M,
+                             int(bool(causal)), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                             _stream_ptr(dev))
     _check("la_backward", st)
     return dq, dk, dv
 
@@ -302,8 +327,10 @@ def la_decode_step(q, k, v, S, Z, out=None):
     _need_cuda(q, k, v, S, Z, *([] if out is None else [out]))
     lib = load_library()
     out = torch.empty((n, H, M), dtype=q.dtype, device=q.device) if out is None else out
-    st = lib.la_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), S.data_ptr(), Z.data_ptr(),
-                            out.data_ptr(), n, H, D, M, dt, _stream_ptr(q.device))
+    with _on_device(q.device):
+        st = lib.la_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), S.data_ptr(),
+                                Z.data_ptr(), out.data_ptr(), n, H, D, M, dt,
+                                _stream_ptr(q.device))
     _check("la_decode_step", st)
     return out
 
@@ -311,5 +338,27 @@ def la_decode_step(q, k, v, S, Z, out=None):
 def la_workspace_status(workspace):
     """Synchronise and read (then clear) the status word a call left in `workspace`."""
     lib = load_library()
-    return lib.la_workspace_status(workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                   _stream_ptr(workspace.device))
+    with _on_device(workspace.device):
+        return lib.la_workspace_status(workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream_ptr(workspace.device))
+
+
+def la_workspace_wait_site(workspace):
+    """Synchronise and read the code of the bounded wait that last gave up in the call that
+    used `workspace` (0: none). Nothing is cleared."""
+    lib = load_library()
+    with _on_device(workspace.device):
+        return lib.la_workspace_wait_site(workspace.data_ptr(),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream_ptr(workspace.device))
+
+
+def la_forward_noalloc_status(device=None):
+    """Synchronise and read (then clear) the status word of la_forward_noalloc's fixed
+    scratch on `device` (default: the current CUDA device)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    lib = load_library()
+    with _on_device(dev):
+        return lib.la_forward_noalloc_status(_stream_ptr(dev))

@@ -200,6 +200,65 @@ int la_decode_step(const void* q, const void* k, const void* v, float* S, float*
                                    as_stream(stream)));
 }
 
+namespace {
+
+// Shared by the two failure test hooks: the tensor-core path only, a withheld
+// load number >= 0 and a wait limit between 1 us and the normal 2 s.
+bool fault_args_ok(int D, int M, int dtype, int withhold_load, unsigned long long wait_ns) {
+  return la::tc_forward_supported(D, M, dtype) && withhold_load >= 0 && wait_ns >= 1000ull &&
+         wait_ns <= 2000000000ull;
+}
+
+}  // namespace
+
+int la_debug_forward_fault(const void* q, const void* k, const void* v, void* out, int B, int H,
+                           int N, int D, int M, int causal, int dtype, void* workspace,
+                           size_t workspace_bytes, int withhold_load,
+                           unsigned long long wait_limit_ns, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype) || N == 0) return LA_ERR_INVALID_ARG;
+  if (!fault_args_ok(D, M, dtype, withhold_load, wait_limit_ns)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  la::FaultHook fh;
+  fh.load = withhold_load;
+  fh.wait_ns = wait_limit_ns;
+  return from_cuda(la::tc_forward(q, k, v, out, la::StateIO{}, B * H, N, causal != 0, workspace,
+                                  st, &fh));
+}
+
+int la_debug_backward_fault(const void* q, const void* k, const void* v, const void* dout,
+                            float* dq, float* dk, float* dv, int B, int H, int N, int D, int M,
+                            int causal, int dtype, void* workspace, size_t workspace_bytes,
+                            int withhold_load, unsigned long long wait_limit_ns, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype) || N == 0) return LA_ERR_INVALID_ARG;
+  if (!fault_args_ok(D, M, dtype, withhold_load, wait_limit_ns)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({q, k, v, dout, dq, dk, dv})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_backward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  la::FaultHook fh;
+  fh.load = withhold_load;
+  fh.wait_ns = wait_limit_ns;
+  return from_cuda(la::tc_backward(q, k, v, dout, dq, dk, dv, B * H, N, causal != 0, workspace,
+                                   st, &fh));
+}
+
+int la_workspace_wait_site(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || workspace_bytes < la::kHeaderBytes) return -1;
+  cudaStream_t st = as_stream(stream);
+  la::WorkspaceHeader h;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return -1;
+  return h.wait_site;
+}
+
 int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream) {
   if (workspace == nullptr || workspace_bytes < la::kHeaderBytes) return LA_ERR_WORKSPACE;
   cudaStream_t st = as_stream(stream);

@@ -25,6 +25,15 @@ struct StateIO {
   const int* lens = nullptr;
 };
 
+// Test hook of the failure-detection tests (la_debug_forward_fault,
+// la_debug_backward_fault): CTA 0 of the call's main kernel (the forward's chunk
+// attention, the backward's forward-direction kernel) withholds its TMA load
+// number `load` and bounds its main-loop waits by `wait_ns`. load < 0: off.
+struct FaultHook {
+  int load = -1;
+  unsigned long long wait_ns = 0;
+};
+
 // Adds n to the process-wide kernel launch count reported by la_kernel_launches().
 void count_launches(unsigned n);
 
@@ -41,11 +50,12 @@ cudaError_t simt_backward(const void* q, const void* k, const void* v, const voi
 bool tc_forward_supported(int D, int M, int dtype);
 size_t tc_forward_workspace(int BH, int N);
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
-                       int BH, int N, bool causal, void* ws, cudaStream_t st);
+                       int BH, int N, bool causal, void* ws, cudaStream_t st,
+                       const FaultHook* fault = nullptr);
 size_t tc_backward_workspace(int BH, int N);
 cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                         float* dk, float* dv, int BH, int N, bool causal, void* ws,
-                        cudaStream_t st);
+                        cudaStream_t st, const FaultHook* fault = nullptr);
 
 // ---- decode step (memory-bound CUDA-core kernel)
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,

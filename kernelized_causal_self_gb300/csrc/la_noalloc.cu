@@ -4,6 +4,8 @@
 // device pointers for inputs and outputs by an application or framework that
 // owns the allocator, or they run where cudaMalloc is not permitted). The
 // array below is the whole scratch; nothing is allocated or freed here.
+#include <stddef.h>
+
 #include <mutex>
 
 #include "la_common.cuh"
@@ -53,4 +55,22 @@ extern "C" int la_forward_noalloc(const void* q, const void* k, const void* v, v
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return LA_ERR_CUDA;
   return la_forward(q, k, v, out, B, H, N, D, M, causal, dtype, scratch, kScratchBytes, stream);
+}
+
+extern "C" int la_forward_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return LA_ERR_CUDA;
+  return la_workspace_status(scratch, kScratchBytes, stream);
+}
+
+extern "C" int la_debug_noalloc_set_status(int status, int wait_site, void* stream) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return LA_ERR_CUDA;
+  static_assert(offsetof(la::WorkspaceHeader, status) == 0, "status word first");
+  static_assert(offsetof(la::WorkspaceHeader, wait_site) == sizeof(int), "wait site second");
+  const int word[2] = {status, wait_site};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(scratch, word, sizeof(word), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }

@@ -76,6 +76,7 @@ struct BwdSmem {
   uint64_t* full;
   uint64_t* mma_bar;
   uint64_t* sbar;  // sbar[1]: the deferred state MMAs (and all the issuer issued before them)
+  uint64_t* drain;  // every MMA of the CTA is done (end of the kernel)
   uint32_t* tslot;
   __device__ explicit BwdSmem(uint8_t* raw) {
     uint8_t* sm =
@@ -92,7 +93,8 @@ struct BwdSmem {
     full = reinterpret_cast<uint64_t*>(misc);
     mma_bar = full + kBwdStages;
     sbar = mma_bar + 1;
-    tslot = reinterpret_cast<uint32_t*>(sbar + 2);
+    drain = sbar + 2;
+    tslot = reinterpret_cast<uint32_t*>(drain + 1);
   }
   __device__ uint8_t* tile(int stage, int which) { return stages + (stage * 4 + which) * kTile; }
 };
@@ -174,9 +176,9 @@ __device__ __forceinline__ float warp_column_sums16(float (&z)[16]) {
 // for the previous chunk's deferred MMAs (one barrier for both).
 __device__ __forceinline__ bool wait_uniform2(uint64_t* bar, uint32_t parity, uint64_t* bar2,
                                               uint32_t parity2, bool use2, WorkspaceHeader* hdr,
-                                              int site) {
-  bool ok = mbar_wait(bar, parity);
-  if (use2) ok = mbar_wait(bar2, parity2) && ok;
+                                              int site, uint64_t limit_ns) {
+  bool ok = mbar_wait(bar, parity, limit_ns);
+  if (use2) ok = mbar_wait(bar2, parity2, limit_ns) && ok;
   const bool all = __syncthreads_and(ok ? 1 : 0) != 0;
   if (!all && threadIdx.x == 0) record_timeout(hdr, site);
   return all;
@@ -235,6 +237,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(sm.mma_bar, 1);
     mbar_init(&sm.sbar[0], 1);
     mbar_init(&sm.sbar[1], 1);
+    mbar_init(sm.drain, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -247,6 +250,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   pdl_wait();
 
   const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
+  const uint64_t wlim = g.wait_ns();  // main-loop wait limit (shortened only by the test hook)
   // items last to first: the segment-state kernel just streamed k and v first to
   // last, and the reverse-direction kernel then starts where this one ends
   Cursor cc, cp;
@@ -254,6 +258,11 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   cp.start(g, true);
   long long issued = 0;
   auto issue = [&](Cursor& c) {
+    if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
+      ++issued;
+      c.advance(g);
+      return;
+    }
     const int s = issued % kBwdStages;
     const int bh = c.bh, t0 = c.chunk * kC;
     mbar_arrive_expect_tx(&sm.full[s], tx);
@@ -301,7 +310,8 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint8_t* kt = sm.tile(s, kK);
     uint8_t* vt = sm.tile(s, kV);
     uint8_t* gt = sm.tile(s, kG);
-    if (!wait_uniform2(&sm.full[s], (consumed / kBwdStages) & 1, &sm.sbar[1], sph1, r_pending, hdr, 21))
+    if (!wait_uniform2(&sm.full[s], (consumed / kBwdStages) & 1, &sm.sbar[1], sph1, r_pending, hdr, 21,
+                       wlim))
       break;
     if (r_pending) {
       sph1 ^= 1;
@@ -356,7 +366,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mma_commit(&sm.sbar[0]);
       }
     }
-    if (!wait_uniform(sm.mma_bar, ph, hdr, 22)) break;
+    if (!wait_uniform(sm.mma_bar, ph, hdr, 22, wlim)) break;
     ph ^= 1;
     fence_after_sync();
 
@@ -502,7 +512,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (CAUSAL) {  // S += dS while the second group runs: the lo-part rows pass
                    // through the chunk's V tile (no MMA reads it any more)
-      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27)) break;
+      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27, wlim)) break;
       sph0 ^= 1;
       fence_after_sync();
       uint32_t r[16];
@@ -528,7 +538,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       fence_proxy_async_smem();  // the V tile is a TMA destination again
     }
-    if (!wait_uniform(sm.mma_bar, ph, hdr, 24)) break;
+    if (!wait_uniform(sm.mma_bar, ph, hdr, 24, wlim)) break;
     ph ^= 1;
     fence_after_sync();
 
@@ -559,7 +569,7 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     r_pending = true;  // the segment sums of phi(Q)^T gN, issued after the second group
     if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
-      if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28)) break;
+      if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28, wlim)) break;
       sph1 ^= 1;
       r_pending = false;
       fence_after_sync();
@@ -599,11 +609,14 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tma_thread) {
     while (consumed < issued) {
       const int s = consumed % kBwdStages;
-      if (!mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1)) record_timeout(hdr, 26);
+      if (!(g.faulty() && consumed == g.fault_load) &&
+          !mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1))
+        record_timeout(hdr, 26);
       ++consumed;
     }
     bulk_wait_all<0>();
   }
+  drain_mmas(sm.drain, hdr, 25);
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
@@ -693,6 +706,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
     mbar_init(&sm.sbar[1], 1);
+    mbar_init(sm.drain, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -991,6 +1005,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     bulk_wait_all<0>();
   }
+  drain_mmas(sm.drain, hdr, 35);
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
@@ -1011,8 +1026,13 @@ size_t tc_backward_workspace(int BH, int N) {
 
 cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                         float* dk, float* dv, int BH, int N, bool causal, void* ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, const FaultHook* fault) {
   const Geometry g = make_geometry(BH, N);
+  Geometry gq = g;  // the forward-direction kernel's copy, with the test hook if any
+  if (fault != nullptr) {
+    gq.fault_load = fault->load;
+    gq.fault_wait_ns = fault->wait_ns;
+  }
   WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
   char* base = static_cast<char*>(ws) + kHeaderBytes;
   const size_t sb = states_bytes(g);
@@ -1044,7 +1064,7 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sms);
-    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, g,
+    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, gq,
                      (const float*)sprefix, rpartial, den, gd, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();

@@ -26,6 +26,14 @@ struct Geometry {
   // forward only: stream b = bh / H uses its first lens[b] tokens (nullptr: all N)
   const int* lens = nullptr;
   int H = 1;
+  // Failure test hook (la_debug_*_fault): CTA 0 withholds its TMA load number
+  // fault_load (no copy is issued, so the wait for it can only run out) and
+  // bounds its main-loop waits by fault_wait_ns. -1: off (every launch but the
+  // test hook's).
+  int fault_load = -1;
+  unsigned long long fault_wait_ns = 0;
+  __device__ bool faulty() const { return fault_load >= 0 && blockIdx.x == 0; }
+  __device__ uint64_t wait_ns() const { return faulty() ? fault_wait_ns : kWaitLimitNs; }
   __device__ int len(int bh) const { return lens ? max(0, min(lens[bh / H], N)) : N; }
   __host__ __device__ int n_items() const { return BH * n_seg; }
   // item -> (bh, seg): segment-major so that a segment's predecessors were
@@ -251,10 +259,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 // Block-uniform bounded wait: every thread waits, then all agree on the outcome
 // (a timeout seen by any thread ends the loop for the whole CTA together).
 __device__ __forceinline__ bool wait_uniform(uint64_t* bar, uint32_t parity, WorkspaceHeader* hdr,
-                                             int site) {
-  const bool all = __syncthreads_and(mbar_wait(bar, parity) ? 1 : 0) != 0;
+                                             int site, uint64_t limit_ns = kWaitLimitNs) {
+  const bool all = __syncthreads_and(mbar_wait(bar, parity, limit_ns) ? 1 : 0) != 0;
   if (!all && threadIdx.x == 0) record_timeout(hdr, site);
   return all;
+}
+
+// End of a kernel whose thread 0 issued tcgen05 MMAs: one commit after all of
+// them, waited for with the full limit, so that TMEM is never freed (nor shared
+// memory released) under an MMA still in flight, whatever made the loop end.
+__device__ __forceinline__ void drain_mmas(uint64_t* drain, WorkspaceHeader* hdr, int site) {
+  if (threadIdx.x == 0) {
+    mma_commit(drain);
+    if (!mbar_wait(drain, 0)) record_timeout(hdr, site);
+  }
 }
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tbase) {

@@ -392,7 +392,8 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t* misc = snap + kSnapBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
   uint64_t* mma_bar = full + kAttStages;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  uint64_t* drain = mma_bar + 1;  // every MMA of the CTA is done (end of the kernel)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
@@ -407,6 +408,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
+    mbar_init(drain, 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_o);
@@ -432,12 +434,18 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   pdl_wait();
 
   const uint32_t tx_bytes = CAUSAL ? 3 * kTile : kTile;
+  const uint64_t wlim = g.wait_ns();  // main-loop wait limit (shortened only by the test hook)
   // items last to first: the segment-state kernel just streamed k and v first to last
   Cursor cc, cp;
   cc.start(g, true);
   cp.start(g, true);
   long long issued = 0;
   auto issue = [&](Cursor& c) {
+    if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
+      ++issued;
+      c.advance(g);
+      return;
+    }
     const int s = issued % kAttStages;
     uint8_t* st = stages + s * 3 * kTile;
     const int bh = c.bh, t0 = c.chunk * kC;
@@ -522,7 +530,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *reinterpret_cast<uint4*>(dst + sw128(r0, (4 * h + c) * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
     }
-    if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11)) {
+    if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 11, wlim)) {
       ok = false;
       break;
     }
@@ -572,7 +580,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bulk_wait_read<0>();
       issue(cp);
     }
-    if (!wait_uniform(mma_bar, mma_phase, hdr, 12)) {
+    if (!wait_uniform(mma_bar, mma_phase, hdr, 12, wlim)) {
       ok = false;
       break;
     }
@@ -640,7 +648,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  idPV, 1);
         mma_commit(mma_bar);
       }
-      if (!wait_uniform(mma_bar, mma_phase, hdr, 13)) {
+      if (!wait_uniform(mma_bar, mma_phase, hdr, 13, wlim)) {
         ok = false;
         break;
       }
@@ -689,11 +697,14 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (tma_thread) {
     while (consumed < issued) {  // loads still in flight after an early exit
       const int s = consumed % kAttStages;
-      if (!mbar_wait(&full[s], (consumed / kAttStages) & 1)) record_timeout(hdr, 14);
+      if (!(g.faulty() && consumed == g.fault_load) &&
+          !mbar_wait(&full[s], (consumed / kAttStages) & 1))
+        record_timeout(hdr, 14);
       ++consumed;
     }
     bulk_wait_all<0>();
   }
+  drain_mmas(drain, hdr, 15);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -761,10 +772,15 @@ size_t tc_forward_workspace(int BH, int N) {
 }
 
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
-                       int BH, int N, bool causal, void* ws, cudaStream_t st) {
+                       int BH, int N, bool causal, void* ws, cudaStream_t st,
+                       const FaultHook* fault) {
   Geometry g = make_geometry(BH, N);
   g.lens = io.lens;
   g.H = io.H;
+  if (fault != nullptr) {  // read by the attend kernel only
+    g.fault_load = fault->load;
+    g.fault_wait_ns = fault->wait_ns;
+  }
   WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
   float* prefix = partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;

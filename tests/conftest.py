@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Largest parity errors of the session (GPU tests), next to their tolerances."""
+    try:
+        from tests.helpers import RECORD, TOL
+    except Exception:  # pragma: no cover
+        return
+    lines = []
+    for dtype, book in RECORD.items():
+        for key, (val, what) in sorted(book.items()):
+            lines.append(f"{dtype:5s} {key:32s} {val:.3e}  (tolerance {TOL[dtype]:.0e})  at {what}")
+    if lines:
+        terminalreporter.write_sep("-", "largest parity errors against the fp64 oracle")
+        for ln in lines:
+            terminalreporter.write_line(ln)

@@ -54,10 +54,27 @@ def errors(got, want, dtype):
     return {"normwise": normwise_err(got, want), "significant_rel": significant_rel_err(got, want)}
 
 
+# Every comparison's errors, by dtype: the session summary (conftest.py) prints the
+# largest of each, with the plain elementwise relative error of the bf16 cases
+# (not a pass criterion, so that its gap to the criteria above stays visible).
+RECORD = {"f32": {}, "bf16": {}}
+
+
+def _record(dtype, errs, what):
+    book = RECORD[dtype]
+    for key, val in errs.items():
+        if key not in book or val > book[key][0]:
+            book[key] = (val, what)
+
+
 def assert_close(got, want, dtype, what=""):
     if np.any(~np.isfinite(_f64(got))):
         raise AssertionError(f"{what}: non-finite values")
     errs = errors(got, want, dtype)
+    report = dict(errs)
+    if dtype == "bf16":
+        report["plain_max_rel (reported only)"] = max_rel_err(got, want)
+    _record(dtype, report, what)
     bad = {k: v for k, v in errs.items() if not v < TOL[dtype]}
-    assert not bad, f"{what}: {errs} (tolerance {TOL[dtype]})"
+    assert not bad, f"{what}: {report} (tolerance {TOL[dtype]})"
     return errs

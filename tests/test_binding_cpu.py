@@ -78,3 +78,52 @@ def test_decode_checks_state_and_output():
     _raises("Z must be", la.la_decode_step, q, q, v, S, _t(4, 3, 8, dtype=F32))
     _raises("out must be", la.la_decode_step, q, q, v, S, Z, out=_t(4, 3, 16))
     _raises("CUDA device", la.la_decode_step, q, q, v, S, Z)
+
+
+def test_every_library_call_runs_with_the_tensors_device_current(monkeypatch):
+    """The library looks up per-device state on the current device and launches on the
+    stream it is given (the tensors' device's), so each wrapper makes the tensors' device
+    current around its call into the library. Checked with a recording stand-in for the
+    device guard and for the library."""
+    events = []
+
+    class Guard:
+        def __init__(self, dev):
+            self.dev = str(dev)
+
+        def __enter__(self):
+            events.append(("enter", self.dev))
+
+        def __exit__(self, *exc):
+            events.append(("exit", self.dev))
+
+    class FakeLib:
+        def __getattr__(self, name):
+            def fn(*args):
+                events.append(("call", name))
+                return 256 if name.endswith("_bytes") else 0
+            return fn
+
+    monkeypatch.setattr(la, "_on_device", Guard)
+    monkeypatch.setattr(la, "load_library", lambda: FakeLib())
+    monkeypatch.setattr(la, "_need_cuda", lambda *a, **k: None)
+    monkeypatch.setattr(la, "_stream_ptr", lambda dev: 0)
+    q, v = _t(2, 3, 10, 16), _t(2, 3, 10, 8)
+    S, Z = _t(2, 3, 16, 8, dtype=F32), _t(2, 3, 16, dtype=F32)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    la.la_forward(q, q, v)
+    la.la_forward_noalloc(q, q, v)
+    la.la_prefill(q, q, v)
+    la.la_extend(q, q, v, S, Z)
+    la.la_backward(q, q, v, v)
+    la.la_decode_step(q[:, :, 0], q[:, :, 0], v[:, :, 0], S, Z)
+    la.la_workspace_status(ws)
+    la.la_workspace_wait_site(ws)
+    la.la_forward_noalloc_status(device="cpu")
+    calls = [i for i, e in enumerate(events) if e[0] == "call" and not e[1].endswith("_bytes")]
+    assert [events[i][1] for i in calls] == [
+        "la_forward", "la_forward_noalloc", "la_prefill", "la_extend", "la_backward",
+        "la_decode_step", "la_workspace_status", "la_workspace_wait_site",
+        "la_forward_noalloc_status"]
+    for i in calls:
+        assert events[i - 1] == ("enter", "cpu") and events[i + 1] == ("exit", "cpu"), events[i]

@@ -73,11 +73,18 @@ def test_forward_small(la, shape, dtype, causal):
 LONG = [(1, 2, 41 * 128 + 17), (1, 1, 70 * 128 + 3), (2, 3, 33 * 128)]
 
 
+# Headroom kept on the long causal forwards: their worst significant-element error
+# was 1.45e-2 against the 2e-2 bound; a kernel change that spends the margin fails here.
+LONG_MARGIN = 1.75e-2
+
+
 @pytest.mark.parametrize("shape", LONG, ids=lambda s: "b%dh%dn%d" % s)
 def test_forward_long_causal(la, shape):
     B, H, N = shape
     got, (q, k, v) = _fwd_case(la, 500 + N, B, H, N, 64, 64, inputs.BF16, True, 0.125)
-    assert_close(got, oracle.forward(q, k, v, True), "bf16", "out")
+    errs = assert_close(got, oracle.forward(q, k, v, True), "bf16", f"long causal out {shape}")
+    assert errs["significant_rel"] < LONG_MARGIN, errs
+    assert errs["normwise"] < LONG_MARGIN, errs
 
 
 def test_prefill_long_state(la):
