@@ -161,6 +161,65 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Sequence shards. [summary §3.3, §3.3.1], [deck slide 4]: causal attention is
+ * a prefix recurrence over (S, Z), and its gradient a pair of cumulative sums
+ * running in opposite directions. A causal sequence cut into consecutive shards
+ * (one per rank, each holding tokens [n_r, n_{r+1}) of every (b, h) sequence)
+ * therefore needs exactly two exchanges, each of D*M + D float32 per head:
+ *   forward:  (S0, Z0) of shard r = sum over shards before r of their own
+ *             (S, Z) sums (la_state_sums), an exclusive prefix;
+ *   backward: (R0, r0) of shard r = sum over shards after r of their own
+ *             reverse sums (R_own, r_own from la_backward_shard_q), an
+ *             exclusive suffix.
+ * With those, shard r computes exactly its part of the unsharded results:
+ *   la_forward_shard(S0, Z0)         -> out of its tokens,
+ *   la_backward_shard_q(S0, Z0)      -> dq of its tokens, and R_own, r_own,
+ *   la_backward_shard_kv(R0, r0)     -> dk, dv of its tokens.
+ * The exchange itself (e.g. an all-gather of the per-shard sums) is the
+ * caller's; nothing here communicates. Causal only. State layouts as S and Z
+ * above ([B][H][D][M], [B][H][D] float32); R is [B][H][D][M] (R[d][m]) and r
+ * [B][H][D]. Workspaces: la_forward_workspace_bytes(..., causal = 1, dtype)
+ * for la_state_sums and la_forward_shard, la_backward_workspace_bytes(...) for
+ * the two backward passes, which must be given the same workspace, in order,
+ * with nothing in between on it.
+ */
+
+/* la_state_sums -- S = sum_j phi(k_j) v_j^T, Z = sum_j phi(k_j) of each
+ * (b, h) sequence (the review's "Proposed method", deck slide 3), written to
+ * S, Z. k: [B][H][N][D], v: [B][H][N][M] in `dtype`. N == 0 writes zeros. */
+int la_state_sums(const void* k, const void* v, float* S, float* Z,
+                  int B, int H, int N, int D, int M, int dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* la_forward_shard -- causal forward of N tokens that follow the state
+ * (S0, Z0) (read only): out_i = phi(q_i)^T S_i / phi(q_i)^T Z_i with
+ * S_i = S0 + sum_{j<=i} phi(k_j) v_j^T, Z_i = Z0 + sum_{j<=i} phi(k_j). */
+int la_forward_shard(const void* q, const void* k, const void* v, void* out,
+                     const float* S0, const float* Z0,
+                     int B, int H, int N, int D, int M, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* la_backward_shard_q -- first backward pass of a shard ([summary App. A]:
+ * the forward-direction sums): dq of its tokens given the state (S0, Z0)
+ * before them (read only), and the shard's own reverse sums
+ * R_own = sum_i phi(q_i) gN_i^T, r_own = sum_i gd_i phi(q_i) (float32,
+ * written). den_i and gd_i stay in `workspace` for the second pass. N == 0
+ * writes R_own = 0, r_own = 0. */
+int la_backward_shard_q(const void* q, const void* k, const void* v, const void* dout,
+                        float* dq, const float* S0, const float* Z0, float* R_own, float* r_own,
+                        int B, int H, int N, int D, int M, int dtype,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* la_backward_shard_kv -- second backward pass of a shard (the reverse-
+ * direction sums): dk, dv of its tokens given the reverse sums (R0, r0) of
+ * the tokens after the shard (read only), with the workspace of its
+ * la_backward_shard_q call. */
+int la_backward_shard_kv(const void* q, const void* k, const void* v, const void* dout,
+                         float* dk, float* dv, const float* R0, const float* r0,
+                         int B, int H, int N, int D, int M, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * la_decode_step -- one recurrent generation step per (stream, head).
  *
  * [deck slide 4], [summary §3.3.2, §3.4]: update, then read out:

@@ -20,6 +20,7 @@ __all__ = [
     "LAError", "LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_WORKSPACE", "LA_ERR_CUDA",
     "LA_ERR_TIMEOUT", "LA_ERR_TOO_LARGE", "LA_F32", "LA_BF16", "la_forward_noalloc",
     "la_forward_noalloc_status", "la_workspace_wait_site",
+    "la_state_sums", "la_forward_shard", "la_backward_shard_q", "la_backward_shard_kv",
     "LA_SITE_FORWARD_LOAD", "LA_SITE_BACKWARD_LOAD",
 ]
 
@@ -48,6 +49,10 @@ _SIGNATURES = {
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
     "la_forward_noalloc": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp]),
     "la_forward_noalloc_status": (_c_int, [_vp]),
+    "la_state_sums": (_c_int, [_vp] * 4 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_forward_shard": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_backward_shard_q": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_backward_shard_kv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_debug_noalloc_set_status": (_c_int, [_c_int, _c_int, _vp]),
     "la_workspace_wait_site": (_c_int, [_vp, _c_size, _vp]),
     "la_debug_forward_fault": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _c_int,
@@ -362,3 +367,128 @@ def la_forward_noalloc_status(device=None):
     lib = load_library()
     with _on_device(dev):
         return lib.la_forward_noalloc_status(_stream_ptr(dev))
+
+
+# ------------------------------------------------------------ sequence shards
+
+def _state_shapes(B, H, D, M):
+    return (B, H, D, M), (B, H, D)
+
+
+def la_state_sums(k, v, S=None, Z=None, workspace=None):
+    """A shard's own sums S = sum_j phi(k_j) v_j^T [B,H,D,M], Z = sum_j phi(k_j) [B,H,D]."""
+    import torch
+    fn, f32 = "la_state_sums", torch.float32
+    (B, H, N), D, M = _dims(fn, k, v, 4)
+    _expect(fn, "v", v, (B, H, N, M), k.dtype)
+    sS, sZ = _state_shapes(B, H, D, M)
+    for name, t, shp in (("S", S, sS), ("Z", Z, sZ)):
+        if t is not None:
+            _expect(fn, name, t, shp, f32)
+    dt = _dtype_code(k)
+    _need_cuda(k, v, *[t for t in (S, Z) if t is not None])
+    lib = load_library()
+    dev = k.device
+    S = torch.empty(sS, dtype=f32, device=dev) if S is None else S
+    Z = torch.empty(sZ, dtype=f32, device=dev) if Z is None else Z
+    ws = _workspace(lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt), dev, workspace)
+    with _on_device(dev):
+        st = lib.la_state_sums(k.data_ptr(), v.data_ptr(), S.data_ptr(), Z.data_ptr(), B, H, N, D,
+                               M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
+                               _stream_ptr(dev))
+    _check(fn, st)
+    return S, Z
+
+
+def la_forward_shard(q, k, v, S0, Z0, out=None, workspace=None):
+    """Causal forward of a shard's tokens after the state (S0, Z0) of the tokens before them."""
+    import torch
+    fn, f32 = "la_forward_shard", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    sS, sZ = _state_shapes(B, H, D, M)
+    _expect(fn, "S0", S0, sS, f32)
+    _expect(fn, "Z0", Z0, sZ, f32)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, M), q.dtype)
+    dt = _dtype_code(q)
+    _need_cuda(q, k, v, S0, Z0, *([] if out is None else [out]))
+    lib = load_library()
+    dev = q.device
+    out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
+    ws = _workspace(lib.la_forward_workspace_bytes(B, H, N, D, M, 1, dt), dev, workspace)
+    with _on_device(dev):
+        st = lib.la_forward_shard(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  S0.data_ptr(), Z0.data_ptr(), B, H, N, D, M, dt, ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check(fn, st)
+    return out
+
+
+def la_backward_shard_q(q, k, v, dout, S0, Z0, dq=None, R_own=None, r_own=None, workspace=None):
+    """First backward pass of a shard: (dq, R_own, r_own, workspace); pass the workspace on
+    to la_backward_shard_kv."""
+    import torch
+    fn, f32 = "la_backward_shard_q", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    _expect(fn, "dout", dout, (B, H, N, M), q.dtype)
+    sS, sZ = _state_shapes(B, H, D, M)
+    _expect(fn, "S0", S0, sS, f32)
+    _expect(fn, "Z0", Z0, sZ, f32)
+    given = [(n, t, shp) for n, t, shp in (("dq", dq, (B, H, N, D)), ("R_own", R_own, sS),
+                                           ("r_own", r_own, sZ)) if t is not None]
+    for name, t, shp in given:
+        _expect(fn, name, t, shp, f32)
+    dt = _dtype_code(q)
+    _need_cuda(q, k, v, dout, S0, Z0, *[t for _, t, _ in given])
+    lib = load_library()
+    dev = q.device
+    dq = torch.empty((B, H, N, D), dtype=f32, device=dev) if dq is None else dq
+    R_own = torch.empty(sS, dtype=f32, device=dev) if R_own is None else R_own
+    r_own = torch.empty(sZ, dtype=f32, device=dev) if r_own is None else r_own
+    ws = _workspace(lib.la_backward_workspace_bytes(B, H, N, D, M, 1, dt), dev, workspace)
+    with _on_device(dev):
+        st = lib.la_backward_shard_q(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                     dq.data_ptr(), S0.data_ptr(), Z0.data_ptr(), R_own.data_ptr(),
+                                     r_own.data_ptr(), B, H, N, D, M, dt, ws.data_ptr(),
+                                     ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check(fn, st)
+    return dq, R_own, r_own, ws
+
+
+def la_backward_shard_kv(q, k, v, dout, R0, r0, workspace, dk=None, dv=None):
+    """Second backward pass of a shard: (dk, dv) given the reverse sums (R0, r0) of the tokens
+    after it and the workspace of its la_backward_shard_q call."""
+    import torch
+    fn, f32 = "la_backward_shard_kv", torch.float32
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    _expect(fn, "dout", dout, (B, H, N, M), q.dtype)
+    sS, sZ = _state_shapes(B, H, D, M)
+    _expect(fn, "R0", R0, sS, f32)
+    _expect(fn, "r0", r0, sZ, f32)
+    given = [(n, t, shp) for n, t, shp in (("dk", dk, (B, H, N, D)), ("dv", dv, (B, H, N, M)))
+             if t is not None]
+    for name, t, shp in given:
+        _expect(fn, name, t, shp, f32)
+    dt = _dtype_code(q)
+    lib = load_library()
+    nbytes = lib.la_backward_workspace_bytes(B, H, N, D, M, 1, dt)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"{fn}: workspace too small")
+    _need_cuda(q, k, v, dout, R0, r0, workspace, *[t for _, t, _ in given])
+    dev = q.device
+    dk = torch.empty((B, H, N, D), dtype=f32, device=dev) if dk is None else dk
+    dv = torch.empty((B, H, N, M), dtype=f32, device=dev) if dv is None else dv
+    with _on_device(dev):
+        st = lib.la_backward_shard_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                      dk.data_ptr(), dv.data_ptr(), R0.data_ptr(), r0.data_ptr(),
+                                      B, H, N, D, M, dt, workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream_ptr(dev))
+    _check(fn, st)
+    return dk, dv

@@ -192,6 +192,114 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout, f
                                      dtype, workspace, st));
 }
 
+// ------------------------------------------------------- sequence shards
+
+namespace {
+
+// (S, Z)-shaped state entries [B][H][D][M], [B][H][D] of a shard call, entry bh.
+la::StateIO shard_io(float* S, float* Z, int B, int H, bool read_init, bool write_final) {
+  la::StateIO io;
+  io.S = S;
+  io.Z = Z;
+  io.H = H;
+  io.pool = B;
+  io.read_init = read_init;
+  io.write_final = write_final;
+  return io;
+}
+
+}  // namespace
+
+int la_state_sums(const void* k, const void* v, float* S, float* Z, int B, int H, int N, int D,
+                  int M, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S, Z})) return LA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (N == 0) {
+    cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)B * H * D * M, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(Z, 0, sizeof(float) * (size_t)B * H * D, st);
+    return from_cuda(e);
+  }
+  if (!ptrs_ok({k, v})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  const la::StateIO io = shard_io(S, Z, B, H, false, true);
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_state_sums(k, v, io, B * H, N, workspace, st));
+  return from_cuda(la::simt_state_sums(k, v, io, B * H, N, D, M, dtype, st));
+}
+
+int la_forward_shard(const void* q, const void* k, const void* v, void* out, const float* S0,
+                     const float* Z0, int B, int H, int N, int D, int M, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S0, Z0})) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  // the entries are read, never written (the kernels take them through const-free
+  // pointers but write only when write_final is set)
+  const la::StateIO io = shard_io(const_cast<float*>(S0), const_cast<float*>(Z0), B, H, true, false);
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_forward(q, k, v, out, io, B * H, N, true, workspace, st));
+  return from_cuda(la::simt_forward(q, k, v, out, io, B * H, N, D, M, true, dtype,
+                                    static_cast<la::WorkspaceHeader*>(workspace), st));
+}
+
+int la_backward_shard_q(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                        const float* S0, const float* Z0, float* R_own, float* r_own, int B, int H,
+                        int N, int D, int M, int dtype, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S0, Z0, R_own, r_own})) return LA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (N == 0) {  // no tokens: the shard adds nothing to the reverse sums
+    cudaError_t e = cudaMemsetAsync(R_own, 0, sizeof(float) * (size_t)B * H * D * M, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(r_own, 0, sizeof(float) * (size_t)B * H * D, st);
+    return from_cuda(e);
+  }
+  if (!ptrs_ok({q, k, v, dout, dq})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_backward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  const la::StateIO pre = shard_io(const_cast<float*>(S0), const_cast<float*>(Z0), B, H, true, false);
+  la::StateIO own = shard_io(R_own, r_own, B, H, false, true);
+  own.rows_are_d = true;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_backward_q(q, k, v, dout, dq, &pre, &own, B * H, N, true, workspace,
+                                       st));
+  return from_cuda(la::simt_backward_q(q, k, v, dout, dq, &pre, &own, B * H, N, D, M, true,
+                                       dtype, workspace, st));
+}
+
+int la_backward_shard_kv(const void* q, const void* k, const void* v, const void* dout, float* dk,
+                         float* dv, const float* R0, const float* r0, int B, int H, int N, int D,
+                         int M, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({R0, r0})) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, dout, dk, dv})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_backward_workspace_bytes(B, H, N, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  // the header is not cleared: the status of the dq pass stays visible
+  la::StateIO suf = shard_io(const_cast<float*>(R0), const_cast<float*>(r0), B, H, true, false);
+  suf.rows_are_d = true;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_backward_kv(q, k, v, dout, dk, dv, &suf, B * H, N, true, workspace,
+                                        st));
+  return from_cuda(la::simt_backward_kv(q, k, v, dout, dk, dv, &suf, B * H, N, D, M, true, dtype,
+                                        workspace, st));
+}
+
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
                    int n_streams, int H, int D, int M, int dtype, void* stream) {
   if (!valid_dims(n_streams, H, 1, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;

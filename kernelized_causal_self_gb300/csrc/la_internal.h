@@ -23,6 +23,12 @@ struct StateIO {
   bool read_init = false;
   // per-stream token counts (device int[B], each clamped to [0, N]); nullptr: all N
   const int* lens = nullptr;
+  // write the final state back to the entries (prefill, extend); false: the
+  // entries are read-only initial states (sequence shards)
+  bool write_final = true;
+  // (scans of the backward's reverse sums) the per-segment sums are R [d][m]
+  // rather than S^T [m][d]; the entries are [D][M] either way
+  bool rows_are_d = false;
 };
 
 // Test hook of the failure-detection tests (la_debug_forward_fault,
@@ -46,13 +52,38 @@ cudaError_t simt_backward(const void* q, const void* k, const void* v, const voi
                           float* dk, float* dv, int BH, int N, int D, int M, bool causal,
                           int dtype, void* ws, cudaStream_t st);
 
+// state sums of each sequence: S = sum_j phi(k_j) v_j^T, Z = sum_j phi(k_j) into io's
+// entries (general shapes)
+cudaError_t simt_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, int D,
+                            int M, int dtype, cudaStream_t st);
+// backward of sequence shards on the CUDA-core path: the dq pass from the prefix state in
+// `pre` (S, Z entries, read-only; nullptr: zero) writing the shard's own reverse sums into
+// `own` (R, r entries; nullptr: not written), and the dk/dv pass from the suffix sums in
+// `suf` (nullptr: zero). The workspace carries den_i, gd_i from the first to the second.
+cudaError_t simt_backward_q(const void* q, const void* k, const void* v, const void* dout,
+                            float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
+                            int D, int M, bool causal, int dtype, void* ws, cudaStream_t st);
+cudaError_t simt_backward_kv(const void* q, const void* k, const void* v, const void* dout,
+                             float* dk, float* dv, const StateIO* suf, int BH, int N, int D,
+                             int M, bool causal, int dtype, void* ws, cudaStream_t st);
+
 // ---- tensor-core path (bf16, D = M = 64): tcgen05 + TMEM + TMA
 bool tc_forward_supported(int D, int M, int dtype);
 size_t tc_forward_workspace(int BH, int N);
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
                        int BH, int N, bool causal, void* ws, cudaStream_t st,
                        const FaultHook* fault = nullptr);
+cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, void* ws,
+                          cudaStream_t st);
 size_t tc_backward_workspace(int BH, int N);
+// The backward in its two passes (see simt_backward_q / simt_backward_kv); tc_backward
+// runs both from zero states.
+cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const void* dout,
+                          float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
+                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault = nullptr);
+cudaError_t tc_backward_kv(const void* q, const void* k, const void* v, const void* dout,
+                           float* dk, float* dv, const StateIO* suf, int BH, int N, bool causal,
+                           void* ws, cudaStream_t st);
 cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                         float* dk, float* dv, int BH, int N, bool causal, void* ws,
                         cudaStream_t st, const FaultHook* fault = nullptr);

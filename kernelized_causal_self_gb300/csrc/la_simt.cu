@@ -150,7 +150,7 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     }
   }
 
-  if (entry_ok) {
+  if (entry_ok && io.write_final) {
     for (int e = threadIdx.x; e < D * M; e += blockDim.x) io.S[entry * D * M + e] = S[e];
     for (int e = threadIdx.x; e < D; e += blockDim.x) io.Z[entry * D + e] = Z[e];
   }
@@ -188,11 +188,13 @@ __device__ __forceinline__ Acc warp_sum(Acc x) {
 }
 
 // Writes dq and, per token, den_i and gd_i = -(dout_i . out_i) / den_i.
+// S0, Z0: the state before the sequence ([bh][D][M], [bh][D]; nullptr: zero).
 template <typename T, typename Acc, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const T* __restrict__ dout, float* __restrict__ dq,
-                   Acc* __restrict__ ws_den, Acc* __restrict__ ws_gd, int N, int D, int M) {
+                   Acc* __restrict__ ws_den, Acc* __restrict__ ws_gd, int N, int D, int M,
+                   const float* __restrict__ S0, const float* __restrict__ Z0) {
   extern __shared__ __align__(16) unsigned char smraw[];
   Acc* S = reinterpret_cast<Acc*>(smraw);  // D*M
   Acc* Z = S + D * M;                       // D
@@ -215,8 +217,9 @@ simt_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   ws_gd += bh * (size_t)N;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = 0;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = 0;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x)
+    S[e] = S0 != nullptr ? (Acc)S0[bh * D * M + e] : (Acc)0;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = Z0 != nullptr ? (Acc)Z0[bh * D + e] : (Acc)0;
   __syncthreads();
   if (!CAUSAL) {
     for (int t0 = 0; t0 < N; t0 += kChunk) {
@@ -338,12 +341,13 @@ __device__ __forceinline__ void load_gN(const T* __restrict__ dout, const Acc* _
   for (int r = threadIdx.x; r < kChunk; r += blockDim.x) gd[r] = r < nv ? gd_g[r] : (Acc)0;
 }
 
+// R0, r0: the reverse sums after the sequence ([bh][D][M], [bh][D]; nullptr: zero).
 template <typename T, typename Acc, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      const T* __restrict__ dout, float* __restrict__ dk, float* __restrict__ dv,
                      const Acc* __restrict__ ws_den, const Acc* __restrict__ ws_gd, int N, int D,
-                     int M) {
+                     int M, const float* __restrict__ R0, const float* __restrict__ r0) {
   extern __shared__ __align__(16) unsigned char smraw[];
   Acc* R = reinterpret_cast<Acc*>(smraw);  // D*M
   Acc* r = R + D * M;                       // D
@@ -365,8 +369,9 @@ simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   ws_den += bh * (size_t)N;
   ws_gd += bh * (size_t)N;
 
-  for (int e = threadIdx.x; e < D * M; e += blockDim.x) R[e] = 0;
-  for (int e = threadIdx.x; e < D; e += blockDim.x) r[e] = 0;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x)
+    R[e] = R0 != nullptr ? (Acc)R0[bh * D * M + e] : (Acc)0;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) r[e] = r0 != nullptr ? (Acc)r0[bh * D + e] : (Acc)0;
   __syncthreads();
   const int n_chunks = (N + kChunk - 1) / kChunk;
   if (!CAUSAL) {
@@ -427,6 +432,77 @@ simt_bwd_dkdv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   }
 }
 
+// ------------------------------------------------ state sums, reverse sums
+
+// S = sum_j phi(k_j) v_j^T, Z = sum_j phi(k_j) of each sequence into io's entries.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+simt_state_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, StateIO io, int N, int D,
+                       int M) {
+  extern __shared__ float sm[];
+  float* S = sm;                // D*M
+  float* Z = S + D * M;         // D
+  float* fk = Z + D;            // kChunk*D
+  float* vv = fk + kChunk * D;  // kChunk*M
+  const size_t bh = blockIdx.x;
+  k += bh * (size_t)N * D;
+  v += bh * (size_t)N * M;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = 0.f;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = 0.f;
+  __syncthreads();
+  for (int t0 = 0; t0 < N; t0 += kChunk) {
+    const int nv = min(kChunk, N - t0);
+    load_rows<T>(k + (size_t)t0 * D, nv, D, fk, true);
+    load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
+    __syncthreads();
+    accumulate_state(S, Z, fk, vv, D, M);
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) io.S[bh * D * M + e] = S[e];
+  for (int e = threadIdx.x; e < D; e += blockDim.x) io.Z[bh * D + e] = Z[e];
+}
+
+// R = sum_i phi(q_i) gN_i^T, r = sum_i gd_i phi(q_i) of each sequence (its own
+// reverse sums, from den_i and gd_i of the dq pass) into R_out [bh][D][M], r_out [bh][D].
+template <typename T, typename Acc>
+__global__ void __launch_bounds__(kThreads)
+simt_reverse_sums_kernel(const T* __restrict__ q, const T* __restrict__ dout,
+                         const Acc* __restrict__ ws_den, const Acc* __restrict__ ws_gd,
+                         float* __restrict__ R_out, float* __restrict__ r_out, int N, int D, int M) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  Acc* R = reinterpret_cast<Acc*>(smraw);  // D*M
+  Acc* r = R + D * M;                       // D
+  Acc* gd = r + D;                          // kChunk
+  Acc* g = gd + kChunk;                     // kChunk*M  (gN)
+  float* fq = reinterpret_cast<float*>(g + kChunk * M);  // kChunk*D
+  const size_t bh = blockIdx.x;
+  q += bh * (size_t)N * D;
+  dout += bh * (size_t)N * M;
+  ws_den += bh * (size_t)N;
+  ws_gd += bh * (size_t)N;
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) R[e] = 0;
+  for (int e = threadIdx.x; e < D; e += blockDim.x) r[e] = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < N; t0 += kChunk) {
+    const int nv = min(kChunk, N - t0);
+    load_rows<T>(q + (size_t)t0 * D, nv, D, fq, true);
+    load_gN<T, Acc>(dout + (size_t)t0 * M, ws_den + t0, ws_gd + t0, nv, M, g, gd);
+    __syncthreads();
+    accumulate_reverse_state<Acc>(R, r, fq, g, gd, D, M);
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < D * M; e += blockDim.x) R_out[bh * D * M + e] = (float)R[e];
+  for (int e = threadIdx.x; e < D; e += blockDim.x) r_out[bh * D + e] = (float)r[e];
+}
+
+size_t sums_smem(int D, int M) {
+  return sizeof(float) * ((size_t)D * M + D + kChunk * D + kChunk * M);
+}
+template <typename Acc>
+size_t rsums_smem(int D, int M) {
+  return sizeof(Acc) * ((size_t)D * M + D + kChunk + kChunk * M) + sizeof(float) * kChunk * D;
+}
+
 size_t fwd_smem(int D, int M) {
   return sizeof(float) * ((size_t)D * M + D + 2 * kChunk * D + kChunk * M + kChunk * kChunk + kChunk);
 }
@@ -463,26 +539,40 @@ cudaError_t forward_t(const void* q, const void* k, const void* v, void* out, co
 }
 
 template <typename T, typename Acc>
-cudaError_t backward_t(const void* q, const void* k, const void* v, const void* dout, float* dq,
-                       float* dk, float* dv, int BH, int N, int D, int M, bool causal, void* ws,
-                       cudaStream_t st) {
+cudaError_t backward_q_t(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                         const StateIO* pre, const StateIO* own, int BH, int N, int D, int M,
+                         bool causal, void* ws, cudaStream_t st) {
   Acc* den = reinterpret_cast<Acc*>(static_cast<char*>(ws) + kHeaderBytes);
   Acc* gd = den + (size_t)BH * N;
+  const float* S0 = (causal && pre != nullptr) ? pre->S : nullptr;
+  const float* Z0 = (causal && pre != nullptr) ? pre->Z : nullptr;
   cudaError_t err;
   if (causal)
     err = launch(simt_bwd_dq_kernel<T, Acc, true>, BH, dq_smem<Acc>(D, M), st, (const T*)q,
-                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
+                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M, S0, Z0);
   else
     err = launch(simt_bwd_dq_kernel<T, Acc, false>, BH, dq_smem<Acc>(D, M), st, (const T*)q,
-                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M);
-  if (err != cudaSuccess) return err;
+                 (const T*)k, (const T*)v, (const T*)dout, dq, den, gd, N, D, M, S0, Z0);
+  if (err != cudaSuccess || own == nullptr) return err;
+  return launch(simt_reverse_sums_kernel<T, Acc>, BH, rsums_smem<Acc>(D, M), st, (const T*)q,
+                (const T*)dout, (const Acc*)den, (const Acc*)gd, own->S, own->Z, N, D, M);
+}
+
+template <typename T, typename Acc>
+cudaError_t backward_kv_t(const void* q, const void* k, const void* v, const void* dout, float* dk,
+                          float* dv, const StateIO* suf, int BH, int N, int D, int M, bool causal,
+                          void* ws, cudaStream_t st) {
+  Acc* den = reinterpret_cast<Acc*>(static_cast<char*>(ws) + kHeaderBytes);
+  Acc* gd = den + (size_t)BH * N;
+  const float* R0 = (causal && suf != nullptr) ? suf->S : nullptr;
+  const float* r0 = (causal && suf != nullptr) ? suf->Z : nullptr;
   if (causal)
     return launch(simt_bwd_dkdv_kernel<T, Acc, true>, BH, dkdv_smem<Acc>(D, M), st, (const T*)q,
                   (const T*)k, (const T*)v, (const T*)dout, dk, dv, (const Acc*)den,
-                  (const Acc*)gd, N, D, M);
+                  (const Acc*)gd, N, D, M, R0, r0);
   return launch(simt_bwd_dkdv_kernel<T, Acc, false>, BH, dkdv_smem<Acc>(D, M), st, (const T*)q,
                 (const T*)k, (const T*)v, (const T*)dout, dk, dv, (const Acc*)den,
-                (const Acc*)gd, N, D, M);
+                (const Acc*)gd, N, D, M, R0, r0);
 }
 
 }  // namespace
@@ -498,13 +588,40 @@ size_t simt_backward_workspace(int BH, int N) {
   return kHeaderBytes + align_up(2 * sizeof(double) * (size_t)BH * N, 256);
 }
 
+cudaError_t simt_backward_q(const void* q, const void* k, const void* v, const void* dout,
+                            float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
+                            int D, int M, bool causal, int dtype, void* ws, cudaStream_t st) {
+  if (dtype == LA_F32)
+    return backward_q_t<float, double>(q, k, v, dout, dq, pre, own, BH, N, D, M, causal, ws, st);
+  return backward_q_t<__nv_bfloat16, float>(q, k, v, dout, dq, pre, own, BH, N, D, M, causal, ws,
+                                            st);
+}
+
+cudaError_t simt_backward_kv(const void* q, const void* k, const void* v, const void* dout,
+                             float* dk, float* dv, const StateIO* suf, int BH, int N, int D,
+                             int M, bool causal, int dtype, void* ws, cudaStream_t st) {
+  if (dtype == LA_F32)
+    return backward_kv_t<float, double>(q, k, v, dout, dk, dv, suf, BH, N, D, M, causal, ws, st);
+  return backward_kv_t<__nv_bfloat16, float>(q, k, v, dout, dk, dv, suf, BH, N, D, M, causal,
+                                             ws, st);
+}
+
 cudaError_t simt_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
                           float* dk, float* dv, int BH, int N, int D, int M, bool causal,
                           int dtype, void* ws, cudaStream_t st) {
+  cudaError_t e = simt_backward_q(q, k, v, dout, dq, nullptr, nullptr, BH, N, D, M, causal, dtype,
+                                  ws, st);
+  if (e != cudaSuccess) return e;
+  return simt_backward_kv(q, k, v, dout, dk, dv, nullptr, BH, N, D, M, causal, dtype, ws, st);
+}
+
+cudaError_t simt_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, int D,
+                            int M, int dtype, cudaStream_t st) {
   if (dtype == LA_F32)
-    return backward_t<float, double>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws, st);
-  return backward_t<__nv_bfloat16, float>(q, k, v, dout, dq, dk, dv, BH, N, D, M, causal, ws,
-                                          st);
+    return launch(simt_state_sums_kernel<float>, BH, sums_smem(D, M), st, (const float*)k,
+                  (const float*)v, io, N, D, M);
+  return launch(simt_state_sums_kernel<__nv_bfloat16>, BH, sums_smem(D, M), st,
+                (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, io, N, D, M);
 }
 
 }  // namespace la

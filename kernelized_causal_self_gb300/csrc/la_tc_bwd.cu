@@ -1024,65 +1024,102 @@ size_t tc_backward_workspace(int BH, int N) {
   return kHeaderBytes + 4 * states_bytes(g) + 2 * align_up(sizeof(float) * (size_t)BH * N, 256);
 }
 
-cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
-                        float* dk, float* dv, int BH, int N, bool causal, void* ws,
-                        cudaStream_t st, const FaultHook* fault) {
+namespace {
+
+// The backward's workspace: header, then per-segment states (S partials and
+// prefix, R partials and suffix), then den_i and gd_i per token.
+struct BwdWork {
+  WorkspaceHeader* hdr;
+  float *spartial, *sprefix, *rpartial, *rsuffix, *den, *gd;
+  BwdWork(void* ws, const Geometry& g, int BH, int N) {
+    hdr = static_cast<WorkspaceHeader*>(ws);
+    char* base = static_cast<char*>(ws) + kHeaderBytes;
+    const size_t sb = states_bytes(g);
+    spartial = reinterpret_cast<float*>(base);
+    sprefix = reinterpret_cast<float*>(base + sb);
+    rpartial = reinterpret_cast<float*>(base + 2 * sb);
+    rsuffix = reinterpret_cast<float*>(base + 3 * sb);
+    den = reinterpret_cast<float*>(base + 4 * sb);
+    gd = den + align_up(sizeof(float) * (size_t)BH * N, 256) / sizeof(float);
+  }
+};
+
+}  // namespace
+
+cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const void* dout,
+                          float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
+                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault) {
   const Geometry g = make_geometry(BH, N);
   Geometry gq = g;  // the forward-direction kernel's copy, with the test hook if any
   if (fault != nullptr) {
     gq.fault_load = fault->load;
     gq.fault_wait_ns = fault->wait_ns;
   }
-  WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
-  char* base = static_cast<char*>(ws) + kHeaderBytes;
-  const size_t sb = states_bytes(g);
-  float* spartial = reinterpret_cast<float*>(base);
-  float* sprefix = reinterpret_cast<float*>(base + sb);
-  float* rpartial = reinterpret_cast<float*>(base + 2 * sb);
-  float* rsuffix = reinterpret_cast<float*>(base + 3 * sb);
-  float* den = reinterpret_cast<float*>(base + 4 * sb);
-  float* gd = den + align_up(sizeof(float) * (size_t)BH * N, 256) / sizeof(float);
-
-  CUtensorMap tq, tk, tv, tg, tdq, tdk, tdv;
+  BwdWork w(ws, g, BH, N);
+  CUtensorMap tq, tk, tv, tg, tdq;
   const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
   if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1) ||
-      !make_tmap_f32_3d(&tdq, dq, kDim, n, bh, 32, kC, 1) ||
-      !make_tmap_f32_3d(&tdk, dk, kDim, n, bh, 32, kC, 1) ||
-      !make_tmap_f32_3d(&tdv, dv, kDim, n, bh, 32, kC, 1))
+      !make_tmap_f32_3d(&tdq, dq, kDim, n, bh, 32, kC, 1))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_segment_states(&tk, &tv, g, spartial, hdr, true, st);
+  cudaError_t e = launch_segment_states(&tk, &tv, g, w.spartial, w.hdr, true, st);
   if (e != cudaSuccess) return e;
-  e = launch_scan(spartial, sprefix, g, causal ? kScanPrefix : kScanTotal, StateIO{}, hdr, st);
+  e = launch_scan(w.spartial, w.sprefix, g, causal ? kScanPrefix : kScanTotal,
+                  pre != nullptr ? *pre : StateIO{}, w.hdr, st);
   if (e != cudaSuccess) return e;
-
-  const int sms = sm_count();
   auto run_q = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sms);
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sm_count());
     err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, gq,
-                     (const float*)sprefix, rpartial, den, gd, hdr);
+                     (const float*)w.sprefix, w.rpartial, w.den, w.gd, w.hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
   e = causal ? run_q(tc_bwd_q_kernel<true>) : run_q(tc_bwd_q_kernel<false>);
-  if (e != cudaSuccess) return e;
-  e = launch_scan(rpartial, rsuffix, g, causal ? kScanSuffix : kScanTotal, StateIO{}, hdr, st);
+  if (e != cudaSuccess || own == nullptr) return e;
+  // the shard's own reverse sums: the total over its segments (rsuffix is scratch here)
+  return launch_scan(w.rpartial, w.rsuffix, g, kScanTotal, *own, w.hdr, st);
+}
+
+cudaError_t tc_backward_kv(const void* q, const void* k, const void* v, const void* dout,
+                           float* dk, float* dv, const StateIO* suf, int BH, int N, bool causal,
+                           void* ws, cudaStream_t st) {
+  const Geometry g = make_geometry(BH, N);
+  BwdWork w(ws, g, BH, N);
+  CUtensorMap tq, tk, tv, tg, tdk, tdv;
+  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
+  if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tg, dout, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_f32_3d(&tdk, dk, kDim, n, bh, 32, kC, 1) ||
+      !make_tmap_f32_3d(&tdv, dv, kDim, n, bh, 32, kC, 1))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_scan(w.rpartial, w.rsuffix, g, causal ? kScanSuffix : kScanTotal,
+                              suf != nullptr ? *suf : StateIO{}, w.hdr, st);
   if (e != cudaSuccess) return e;
   auto run_kv = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sms);
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sm_count());
     err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdk, tdv, g,
-                     (const float*)rsuffix, (const float*)den, (const float*)gd, hdr);
+                     (const float*)w.rsuffix, (const float*)w.den, (const float*)w.gd, w.hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
   return causal ? run_kv(tc_bwd_kv_kernel<true>) : run_kv(tc_bwd_kv_kernel<false>);
+}
+
+cudaError_t tc_backward(const void* q, const void* k, const void* v, const void* dout, float* dq,
+                        float* dk, float* dv, int BH, int N, bool causal, void* ws,
+                        cudaStream_t st, const FaultHook* fault) {
+  cudaError_t e = tc_backward_q(q, k, v, dout, dq, nullptr, nullptr, BH, N, causal, ws, st, fault);
+  if (e != cudaSuccess) return e;
+  return tc_backward_kv(q, k, v, dout, dk, dv, nullptr, BH, N, causal, ws, st);
 }
 
 }  // namespace la

@@ -189,6 +189,32 @@ __device__ __forceinline__ void phi_half(uint8_t* tile, int row, int h, int nval
     phi_half_impl<EXACT, true>(tile, row, h, nvalid);
 }
 
+// psi(x) = phi(x) - 1 (x for x > 0, exp(x) - 1 otherwise) on two packed bf16
+// values, each rounded once. phi(k) = 1 + psi(k) with |psi| << 1 for the small
+// inputs of attention, so a sum over phi(k) splits into an exact count (or an
+// exact column sum) and a sum over psi(k) whose bf16 rounding is ~10x smaller
+// than that of phi(k) itself.
+__device__ __forceinline__ uint32_t psi2_bf16(uint32_t u) {
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&u);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const float2 m = __bfloat1622float2(__hmin2(x, zero));
+  const float2 p = __bfloat1622float2(__hmax2(x, zero));
+  const __nv_bfloat162 r = __floats2bfloat162_rn(__expf(m.x) - 1.f + p.x, __expf(m.y) - 1.f + p.y);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// psi on this thread's half of tile row `row`, in place; rows >= nvalid become 0.
+__device__ __forceinline__ void psi_half(uint8_t* tile, int row, int h, int nvalid) {
+  const bool valid = row < nvalid;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, (4 * h + c) * 16));
+    const uint4 w = *p;
+    *p = valid ? make_uint4(psi2_bf16(w.x), psi2_bf16(w.y), psi2_bf16(w.z), psi2_bf16(w.w))
+               : make_uint4(0, 0, 0, 0);
+  }
+}
+
 // Zeroes this thread's half of tile row `row` (columns [32h, 32h + 32)) when the
 // row is past the valid rows: rows beyond a sequence's length may hold any bits
 // (even NaN), and a zero weight times NaN is still NaN.

@@ -4,10 +4,13 @@
 // the chunks into segments. Three kernels:
 //
 //  1. tc_state_kernel: per segment, the state increment
-//       dS^T = V^T phi(K), dZ = sum_t phi(K_t)  (one tcgen05 group per chunk:
-//       [V^T; 1^T] phi(K), M = 128 with a stacked block of ones, K = tokens)
+//       dS^T = V^T phi(K), dZ = sum_t phi(K_t)
 //     ("Transformers are RNNs": S = sum_j phi(K_j) V_j^T, Z = sum_j phi(K_j);
-//     nubint.ai review, "Proposed method"; zhengyuhong.cn deck, slide 3).
+//     nubint.ai review, "Proposed method"; zhengyuhong.cn deck, slide 3),
+//     taken as phi(K) = 1 + psi(K): one tcgen05 group per chunk,
+//     [V^T; 1^T] [psi(K) | 1] (M = 128 and N = 80 with stacked blocks of ones),
+//     gives V^T psi(K), the column sums of V, and sum_t psi(K_t); then
+//     dS^T[m][d] = (V^T psi(K))[m][d] + sum_t V[t][m], dZ[d] = sum_t psi + count.
 //  2. state_scan_kernel: exclusive prefix over segments (causal; deck slide 4:
 //     S_i = S_{i-1} + phi(K_i) V_i^T) or the full sum (non-causal), in float32;
 //     optionally the final state for prefill.
@@ -135,12 +138,15 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                      sdesc(va + k * 2048, oa - (va + k * 2048), 1024), idS, (first && k == 0) ? 0u : 1u);
           } else {
             // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
-            // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
-            const uint32_t idS = idesc_bf16(128, 64, true, true);
+            // [psi(K) | 1] (N = 80 MN-major, columns 64.. from the ones block):
+            // lanes 0-63 get (V^T psi(K))[m][d] in columns [0, 64) and the column
+            // sum of V[:, m] in column 64; lanes 64-127 get sum_t psi(K)[t][d]
+            const uint32_t idS = idesc_bf16(128, 80, true, true);
 #pragma unroll
             for (int k = 0; k < kC / 16; ++k)
               mma_ss(acc, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
-                     sdesc(ka + k * 2048, 1024, 1024), idS, (first && k == 0) ? 0u : 1u);
+                     sdesc(ka + k * 2048, oa - (ka + k * 2048), 1024), idS,
+                     (first && k == 0) ? 0u : 1u);
           }
           mma_commit(&empty[s]);
           if (last) mma_commit(&segbar[nseg++ & 1]);
@@ -222,14 +228,25 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (!mbar_wait_warp(xbar, xphase, abort, hdr, 7)) return false;
         xphase ^= 1;
       } else {
-        // lanes 0..63: dS^T row m = lane, columns d; lanes 64..127: dZ[d] (every
-        // lane alike). This thread writes columns [32h, 32h + 32) of its row.
+        // lanes 0..63: row m = lane of V^T psi(K) (columns d) plus the column sum
+        // of V[:, m] (column 64); lanes 64..127: sum_t psi(K)[t][d] (every lane
+        // alike), plus the segment's count of valid tokens. This thread writes
+        // columns [32h, 32h + 32) of its row.
         if (q4 < 2 || (q4 == 2 && lane == 0)) {
+          float add;
+          if (q4 < 2) {
+            uint32_t r16[16];
+            tmem_ld16(acc + 64, r16);
+            add = __uint_as_float(r16[0]);
+          } else {
+            const int c0 = g.chunk_begin(item), c1 = g.chunk_end(item);
+            add = (float)max(0, min(g.len(g.bh_of(item)) - c0 * kC, (c1 - c0) * kC));
+          }
           float4* d4 = reinterpret_cast<float4*>(dst + (q4 < 2 ? (32 * q4 + lane) * kDim : kDim * kDim) + h * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            d4[j] = make_float4(__uint_as_float(r[4 * j]) + add, __uint_as_float(r[4 * j + 1]) + add,
+                                __uint_as_float(r[4 * j + 2]) + add, __uint_as_float(r[4 * j + 3]) + add);
         }
       }
       return true;
@@ -258,7 +275,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       if (PRECISE)
         phi_half_split(kt, kt + 2 * kTile, trow, h, nvalid, zacc);
       else
-        phi_half<true>(kt, trow, h, nvalid);
+        psi_half(kt, trow, h, nvalid);
       if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
       fence_proxy_async_smem();
       mbar_arrive(&phid[s]);
@@ -304,9 +321,11 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // mode kScanPrefix:  out[seg][bh] = S0 + sum_{s < seg} partial[s][bh]  (causal, forward)
 // mode kScanTotal:   out[bh]      = sum_s partial[s][bh]               (non-causal)
-// mode kScanSuffix:  out[seg][bh] = sum_{s > seg} partial[s][bh]       (causal, reverse)
-// S0 is the entry's initial state when io.read_init, else 0; with io.S set the
-// full sum (S0 + all segments) is written to the entry: S [d][m], Z [d].
+// mode kScanSuffix:  out[seg][bh] = S0 + sum_{s > seg} partial[s][bh]  (causal, reverse)
+// S0 is the entry's initial state when io.read_init (prefix and suffix modes),
+// else 0; with io.S set and io.write_final the full sum (S0 + all segments) is
+// written to the entry: S [d][m], Z [d]. The partials are S^T [m][d] (the
+// segment-state kernel's) or, with io.rows_are_d, R [d][m] (the backward's).
 // One thread per state element; the segment loads are issued in batches of 8
 // so the walk over segments is not a chain of dependent global loads.
 constexpr int kScanThreads = 128;
@@ -327,11 +346,12 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
     entry = (size_t)slot * io.H + bh % io.H;
     if (!entry_ok && e == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
   }
-  const int m = e / kDim, d = e % kDim;  // e < 4096: S^T [m][d]; else Z [e - 4096]
+  // e < 4096: S^T [m][d] (or R [d][m]); else Z [e - 4096]
+  const int m = io.rows_are_d ? e % kDim : e / kDim, d = io.rows_are_d ? e / kDim : e % kDim;
   float* cell = !entry_ok ? nullptr
                           : (e < kDim * kDim ? io.S + entry * kDim * kDim + d * kDim + m
                                              : io.Z + entry * kDim + (e - kDim * kDim));
-  float run = (cell != nullptr && io.read_init && mode == kScanPrefix) ? *cell : 0.f;
+  float run = (cell != nullptr && io.read_init && mode != kScanTotal) ? *cell : 0.f;
   const bool rev = mode == kScanSuffix;
   for (int s0 = 0; s0 < n_seg; s0 += 8) {
     float x[8];
@@ -350,7 +370,7 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
     }
   }
   if (mode == kScanTotal) out[(size_t)bh * kStateFloats + e] = run;
-  if (cell != nullptr) *cell = run;
+  if (cell != nullptr && io.write_final) *cell = run;
 }
 
 // --------------------------------------------------------- 3. chunk attention
@@ -654,7 +674,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       mma_phase ^= 1;
       fence_after_sync();
-      if (entry_ok) {  // direct: the state after the sequence's only chunk
+      if (entry_ok && io.write_final) {  // direct: the state after the sequence's only chunk
         if (sthread) {
           float* dst = io.S + entry * kDim * kDim + (size_t)(32 * h) * kDim + row;
 #pragma unroll
@@ -771,6 +791,22 @@ size_t tc_forward_workspace(int BH, int N) {
   return kHeaderBytes + 2 * align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256);
 }
 
+cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, void* ws,
+                          cudaStream_t st) {
+  const Geometry g = make_geometry(BH, N);
+  WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
+  float* total = partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;
+  CUtensorMap tk, tv;
+  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
+  if (!make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
+  if (e != cudaSuccess) return e;
+  return launch_scan(partial, total, g, kScanTotal, io, hdr, st);
+}
+
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
                        int BH, int N, bool causal, void* ws, cudaStream_t st,
                        const FaultHook* fault) {
@@ -792,9 +828,13 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
       !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
 
-  // causal with one chunk per sequence: no segment states or scan; the attend
-  // kernel takes the state from io (or zero) and writes the final state there
-  const bool direct = causal && g.n_chunks == 1;
+  // causal with one chunk per sequence, continuing a stored state: no segment
+  // states or scan; the attend kernel takes the state from io (or zero) and
+  // writes the final state there. A fresh prefill takes the segment path, whose
+  // state increment is the psi form (see tc_state_kernel): the attend kernel's
+  // own increment rounds phi(K) to bf16, which a sum from a zero state over
+  // random-sign v leaves at ~2% on the state's significant elements.
+  const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
   cudaError_t e = cudaSuccess;
   if (!direct) {
     e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);

@@ -168,3 +168,41 @@ def test_fault_hooks_reject_bad_arguments(lib):
     args[16] = -2
     assert lib.la_debug_backward_fault(*args) == la.LA_ERR_INVALID_ARG   # negative load number
     assert lib.la_workspace_wait_site(None, 0, None) == -1
+
+
+def test_shard_entry_points_reject_bad_arguments(lib):
+    wsf = lib.la_forward_workspace_bytes(1, 2, 300, 64, 64, 1, 1)
+    wsb = lib.la_backward_workspace_bytes(1, 2, 300, 64, 64, 1, 1)
+    # la_state_sums(k, v, S, Z, B, H, N, D, M, dtype, ws, wsb, stream)
+    assert lib.la_state_sums(FAKE, FAKE, 0, FAKE, 1, 2, 300, 64, 64, 1, FAKE, wsf, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert lib.la_state_sums(FAKE, FAKE, FAKE, FAKE, 1, 2, 300, 64, 60, 1, FAKE, wsf, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert lib.la_state_sums(0, FAKE, FAKE, FAKE, 1, 2, 300, 64, 64, 1, FAKE, wsf, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert lib.la_state_sums(FAKE, FAKE, FAKE, FAKE, 1, 2, 300, 64, 64, 1, FAKE, 16, None) == \
+        la.LA_ERR_WORKSPACE
+    # la_forward_shard(q, k, v, out, S0, Z0, B, H, N, D, M, dtype, ws, wsb, stream)
+    assert lib.la_forward_shard(FAKE, FAKE, FAKE, FAKE, ODD, FAKE, 1, 2, 300, 64, 64, 1, FAKE, wsf,
+                                None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_shard(FAKE, FAKE, FAKE, 0, FAKE, FAKE, 1, 2, 300, 64, 64, 1, FAKE, wsf,
+                                None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_shard(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 300, 64, 64, 1, 0, wsf,
+                                None) == la.LA_ERR_WORKSPACE
+    assert lib.la_forward_shard(0, 0, 0, 0, FAKE, FAKE, 1, 2, 0, 64, 64, 1, 0, 0, None) == la.LA_OK
+    # la_backward_shard_q(q, k, v, dout, dq, S0, Z0, R_own, r_own, B, H, N, D, M, dtype, ws, wsb, st)
+    args = [FAKE] * 9 + [1, 2, 300, 64, 64, 1, FAKE, wsb, None]
+    bad = list(args)
+    bad[7] = 0                                                   # R_own missing
+    assert lib.la_backward_shard_q(*bad) == la.LA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[16] = wsb - 1
+    assert lib.la_backward_shard_q(*bad) == la.LA_ERR_WORKSPACE
+    # la_backward_shard_kv(q, k, v, dout, dk, dv, R0, r0, B, H, N, D, M, dtype, ws, wsb, st)
+    args = [FAKE] * 8 + [1, 2, 300, 64, 64, 1, FAKE, wsb, None]
+    bad = list(args)
+    bad[6] = ODD
+    assert lib.la_backward_shard_kv(*bad) == la.LA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[15] = 0
+    assert lib.la_backward_shard_kv(*bad) == la.LA_ERR_WORKSPACE
