@@ -176,7 +176,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's calls directly instead of replaying CUDA graphs")
     ap.add_argument("--part", default=None,
-                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode", "extend"],
+                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode", "extend",
+                             "poly2"],
                     help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
@@ -319,6 +320,9 @@ def run_parts(la, device, peaks, reps=10):
         "tokens_per_s": w.B * T / (ms * 1e-3), "ms_per_step": per_step, "hbm_gbs": gbs,
         "roofline_frac": gbs / hbm, "steps": T, "launch": "CUDA graph of 3072 la_decode_step calls",
         "l2": "S/Z state (33.5 MB) fits in L2; fraction can exceed 1"}
+    # degree-2 polynomial feature map on the main workload's shape (forward, causal)
+    parts["poly2_causal_fwd_b4h8n16384d64"] = poly2_part(la, inputs.WORKLOADS[MAIN], device, peaks,
+                                                         flush, reps)
     # decode with a state too large for L2: DECODE_HBM_STREAMS streams x 8 heads (134 MB of S),
     # so every step reads and writes S in HBM
     parts[f"decode_s{DECODE_HBM_STREAMS}h{w.H}d{w.D}_hbm"] = decode_hbm_part(la, w, device, hbm)
@@ -331,6 +335,30 @@ def run_parts(la, device, peaks, reps=10):
         "roofline_frac": gbs / hbm, "same_tokens_as_decode_steps_ms": per_step * EXTEND_TOKENS,
         "launch": "one la_extend call", "l2": "flushed between calls (256 MB read)"}
     return parts
+
+
+def poly2_flops(w):
+    """Algorithmic flops per token-head of the degree-2 feature map (D^2 features): the
+    read-out phi(q)^T S and the update S += phi(k) v^T, 2 D^2 M each (the intra-chunk
+    products of the chunked form are implementation work, not counted)."""
+    return 4 * w.D * w.D * w.M
+
+
+def poly2_part(la, w, device, peaks, flush, reps):
+    import torch
+    q, k, v, _ = device_inputs(w, device)
+    out = torch.empty_like(v)
+    ws = torch.empty(la.la_poly2_workspace_bytes(w.B, w.H, w.N, w.D, w.M, True),
+                     dtype=torch.uint8, device=device)
+    ms = statistics.median(time_calls(lambda: la.la_forward_poly2(q, k, v, True, out, ws),
+                                      reps, 3, flush))
+    th = w.B * w.H * w.N
+    tflops = th * poly2_flops(w) / (ms * 1e-3) / 1e12
+    gbs = th * fwd_bytes(w) / (ms * 1e-3) / 1e9
+    return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms": ms, "tflops": tflops,
+            "roofline_frac": tflops / peaks["bf16_tflops"], "bound": "tensor",
+            "flops_per_token_head": poly2_flops(w), "hbm_gbs": gbs,
+            "hbm_frac": gbs / peaks["hbm_gbs"], "l2": "flushed between calls (256 MB read)"}
 
 
 DECODE_HBM_STREAMS, DECODE_HBM_STEPS, DECODE_HBM_PREFILL = 1024, 128, 128
@@ -696,7 +724,8 @@ def run_part(args):
     labuild.build()
     la.load_library()
     device = torch.device("cuda", 0)
-    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "fwd3072": "causal_fwd_b8h8n3072d64",
+    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "poly2": MAIN,
+            "fwd3072": "causal_fwd_b8h8n3072d64",
             "noncausal": "noncausal_fwd_b4h8n4096d64",
             "decode": "decode_s256h8d64_prefill1024_steps3072",
             "extend": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
@@ -713,6 +742,8 @@ def run_part(args):
         fn = extend_setup(la, w, g, device, S, Z)
     elif args.part == "bwd":
         fn = lambda: la.la_backward(q, k, v, dout, True)
+    elif args.part == "poly2":
+        fn = lambda: la.la_forward_poly2(q, k, v, True)
     elif args.part == "fwdbwd":
         fn = lambda: (la.la_forward(q, k, v, True), la.la_backward(q, k, v, dout, True))
     else:

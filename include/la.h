@@ -161,6 +161,23 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * la_forward_poly2 -- kernelized attention with the degree-2 polynomial
+ * feature map: [summary §3.2.1], the kernel sim(x, y) = (x . y)^2 has the
+ * exact finite feature map phi(x) = vec(x x^T) (D^2 features), so
+ *   out_i = sum_{j<=i} (q_i . k_j)^2 v_j / sum_{j<=i} (q_i . k_j)^2
+ *         = phi(q_i)^T S_i / phi(q_i)^T Z_i
+ * with the S/Z recurrence of la_forward over the D^2-dimensional features
+ * ([deck slide 4]). Layouts and ownership as la_forward. Supported: bf16,
+ * D = M = 64 (4096 features), causal != 0; anything else returns
+ * LA_ERR_INVALID_ARG. Workspace: la_poly2_workspace_bytes() (the state part
+ * of every numerator and denominator in float32, 260 bytes per token and head).
+ */
+size_t la_poly2_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype);
+int la_forward_poly2(const void* q, const void* k, const void* v, void* out,
+                     int B, int H, int N, int D, int M, int causal, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Sequence shards. [summary §3.3, §3.3.1], [deck slide 4]: causal attention is
  * a prefix recurrence over (S, Z), and its gradient a pair of cumulative sums
  * running in opposite directions. A causal sequence cut into consecutive shards

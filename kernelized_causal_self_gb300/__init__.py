@@ -21,6 +21,7 @@ __all__ = [
     "LA_ERR_TIMEOUT", "LA_ERR_TOO_LARGE", "LA_F32", "LA_BF16", "la_forward_noalloc",
     "la_forward_noalloc_status", "la_workspace_wait_site",
     "la_state_sums", "la_forward_shard", "la_backward_shard_q", "la_backward_shard_kv",
+    "la_forward_poly2", "la_poly2_workspace_bytes",
     "LA_SITE_FORWARD_LOAD", "LA_SITE_BACKWARD_LOAD",
 ]
 
@@ -50,6 +51,8 @@ _SIGNATURES = {
     "la_forward_noalloc": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp]),
     "la_forward_noalloc_status": (_c_int, [_vp]),
     "la_state_sums": (_c_int, [_vp] * 4 + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "la_poly2_workspace_bytes": (_c_size, [_c_int] * 7),
+    "la_forward_poly2": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_forward_shard": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_backward_shard_q": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_backward_shard_kv": (_c_int, [_vp] * 8 + [_c_int] * 6 + [_vp, _c_size, _vp]),
@@ -492,3 +495,33 @@ def la_backward_shard_kv(q, k, v, dout, R0, r0, workspace, dk=None, dv=None):
                                       _stream_ptr(dev))
     _check(fn, st)
     return dk, dv
+
+
+# ---------------------------------------------- degree-2 polynomial feature map
+
+def la_poly2_workspace_bytes(B, H, N, D, M, causal=True, dtype=LA_BF16):
+    return load_library().la_poly2_workspace_bytes(B, H, N, D, M, int(bool(causal)), dtype)
+
+
+def la_forward_poly2(q, k, v, causal=True, out=None, workspace=None):
+    """out[B,H,N,M] = causal attention with sim(q, k) = (q . k)^2 (feature map vec(x x^T))."""
+    import torch
+    fn = "la_forward_poly2"
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, M), q.dtype)
+    dt = _dtype_code(q)
+    _need_cuda(q, k, v, *([] if out is None else [out]))
+    lib = load_library()
+    dev = q.device
+    out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
+    ws = _workspace(lib.la_poly2_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt), dev,
+                    workspace)
+    with _on_device(dev):
+        st = lib.la_forward_poly2(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                  N, D, M, int(bool(causal)), dt, ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check(fn, st)
+    return out

@@ -192,6 +192,28 @@ int la_backward(const void* q, const void* k, const void* v, const void* dout, f
                                      dtype, workspace, st));
 }
 
+// ---------------------------------------------- degree-2 polynomial feature map
+
+size_t la_poly2_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
+  if (!query_dims_ok(B, H, N) || !la::poly2_supported(D, M, dtype, causal)) return la::kHeaderBytes;
+  return la::poly2_workspace(B * H, N);
+}
+
+int la_forward_poly2(const void* q, const void* k, const void* v, void* out, int B, int H, int N,
+                     int D, int M, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!la::poly2_supported(D, M, dtype, causal)) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_poly2_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::poly2_forward(q, k, v, out, B * H, N, workspace, st));
+}
+
 // ------------------------------------------------------- sequence shards
 
 namespace {

@@ -88,6 +88,12 @@ cudaError_t tc_backward(const void* q, const void* k, const void* v, const void*
                         float* dk, float* dv, int BH, int N, bool causal, void* ws,
                         cudaStream_t st, const FaultHook* fault = nullptr);
 
+// ---- degree-2 polynomial feature map (bf16, D = M = 64, causal): tcgen05 + TMEM + TMA
+bool poly2_supported(int D, int M, int dtype, int causal);
+size_t poly2_workspace(int BH, int N);
+cudaError_t poly2_forward(const void* q, const void* k, const void* v, void* out, int BH, int N,
+                          void* ws, cudaStream_t st);
+
 // ---- decode step (memory-bound CUDA-core kernel)
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
                         int n_sh, int D, int M, int dtype, cudaStream_t st);

@@ -1,0 +1,480 @@
+// Degree-2 polynomial feature map, causal, bf16 inputs with D = M = 64.
+//
+// paperlayer.ai summary §3.2.1: the degree-2 polynomial kernel
+// sim(x, y) = (x . y)^2 has the exact finite feature map phi(x) = vec(x x^T)
+// (D^2 = 4096 features), so its attention is a linear attention with that map:
+//   out_i = sum_{j<=i} (q_i . k_j)^2 v_j / sum_{j<=i} (q_i . k_j)^2
+//         = phi(q_i)^T S_i / phi(q_i)^T Z_i,
+//   S_i = sum_{j<=i} phi(k_j) v_j^T (4096 x 64),  Z_i = sum_{j<=i} phi(k_j)
+// (the S/Z recurrence of the zhengyuhong.cn deck, slide 4, with this phi).
+//
+// Chunked like the elu + 1 forward (chunks of C = 128 tokens, L the inclusive
+// lower-triangular mask):
+//   num = [(Q K^T)^2 (.) L] V + Phi(Q) S_prev,  den = rowsum[(Q K^T)^2 (.) L] + Phi(Q) Z_prev.
+// With S_a the 64 x 64 block of S whose feature rows are (a, b), b = 0..63:
+//   Phi(Q) S = sum_a diag(q_a) Q S_a = sum_a Phi(Q)_a S_a,  Phi(Q)_a = q_a (.) Q,
+//   S_a += Phi(K)_a^T V,  Phi(K)_a = k_a (.) K,
+// and, since Z = vec(G) with G = sum_j k_j k_j^T, phi(q)^T Z = q^T G q.
+//
+// Kernels:
+//  1. tc_poly2_state_kernel: one CTA per (sequence, group of 8 feature blocks),
+//     walking the sequence's chunks in order. Its 8 blocks of S stay in TMEM
+//     in float32 (two blocks stacked per M = 128 accumulator). Per chunk and
+//     block pair it forms Phi(Q)_a and Phi(K)_a (bf16) in shared memory from the
+//     chunk's q and k, snapshots S_a (bf16) and issues the read-out Phi(Q)_a S_a
+//     (before the update) and the update [Phi(K)_a; Phi(K)_{a+1}]^T V on the
+//     tensor cores. The CTA's partial numerators (the state part of num) are
+//     added into a float32 buffer with vector atomics; the CTA of group 0 also
+//     carries G and adds q^T G_prev q to the denominators.
+//  2. tc_poly2_out_kernel: one CTA per chunk: P = Q K^T on the tensor cores,
+//     squared and masked in float32, rounded to bf16 into TMEM, then
+//     P_L [V | 1] (numerator and row sums in one N = 80 group), plus the
+//     buffered state part, divided, rounded to bf16 and stored.
+#include <cuda_bf16.h>
+
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace tcx {
+namespace {
+
+constexpr int kP2Groups = 8;                  // feature groups per sequence
+constexpr int kP2Blocks = kDim / kP2Groups;   // feature blocks a per group (8)
+constexpr int kP2Threads = 512;               // warp w: TMEM lane quarter w % 4, column quarter w / 4
+constexpr int kP2Stages = 2;
+constexpr int kSnapBlock = kDim * 128;        // a 64 x 64 bf16 block, 128-byte rows
+constexpr int kP2Smem = 1024 + kP2Stages * 3 * kTile   // Q, K, V stages
+                        + 2 * 2 * kSnapBlock          // S snapshots: 2 buffers x block pair
+                        + kSnapBlock                  // G snapshot
+                        + 2048                        // 16 rows of ones
+                        + 4 * kTile                   // Phi(Q)_a, Phi(Q)_a+1, Phi(K)_a, Phi(K)_a+1
+                        + 256;                        // barriers, TMEM slot
+
+// TMEM columns
+constexpr uint32_t kP2S = 0;     // 4 x 64: S block pairs (lanes 0-63 block a, 64-127 block a + 1)
+constexpr uint32_t kP2N = 256;   // 64: this chunk's state numerator (rows = tokens)
+constexpr uint32_t kP2G = 320;   // 64: G in lanes 0-63 ([K^T; 1^T] K; lanes 64-127 unused)
+constexpr uint32_t kP2Q = 384;   // 64: Q G_prev (rows = tokens)
+
+// 16 consecutive raw bf16 of row `row`, logical 16-byte chunks c0, c0 + 1 -> float.
+__device__ __forceinline__ void row16(const uint8_t* tile, int row, int c0, float* out) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128(row, (c0 + c) * 16));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      out[8 * c + 2 * q] = bf16_lo_f(u[q]);
+      out[8 * c + 2 * q + 1] = bf16_hi_f(u[q]);
+    }
+  }
+}
+
+// 8 raw bf16 of row `row` at logical 16-byte chunk c0 -> float.
+__device__ __forceinline__ void row8(const uint8_t* tile, int row, int c0, float* out) {
+  const uint4 w = *reinterpret_cast<const uint4*>(tile + sw128(row, c0 * 16));
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q] = bf16_lo_f(u[q]);
+    out[2 * q + 1] = bf16_hi_f(u[q]);
+  }
+}
+
+// x[16] * s -> bf16 at row `row`, columns [16 cq, 16 cq + 16) of a swizzled tile.
+__device__ __forceinline__ void put16_scaled(uint8_t* tile, int row, int cq, const float* x, float s) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = pack_bf16(x[8 * c + 2 * q] * s, x[8 * c + 2 * q + 1] * s);
+    *reinterpret_cast<uint4*>(tile + sw128(row, (2 * cq + c) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// 16 float32 TMEM values -> bf16 at row `row`, columns [16 cq, 16 cq + 16) (zero if !keep).
+__device__ __forceinline__ void put16_tmem(uint8_t* tile, int row, int cq, const uint32_t (&r)[16],
+                                           bool keep) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = keep ? pack_bf16(__uint_as_float(r[8 * c + 2 * q]), __uint_as_float(r[8 * c + 2 * q + 1])) : 0u;
+    *reinterpret_cast<uint4*>(tile + sw128(row, (2 * cq + c) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kP2Threads, 1)
+tc_poly2_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, int N, float* __restrict__ num_state,
+                      float* __restrict__ den_state, WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = sm;                                  // [stage][Q | K | V]
+  uint8_t* snap = stages + kP2Stages * 3 * kTile;        // [2][2][64 x 128 B]
+  uint8_t* gsnap = snap + 4 * kSnapBlock;
+  uint8_t* ones = gsnap + kSnapBlock;
+  uint8_t* phq = ones + 2048;                            // Phi(Q)_a, Phi(Q)_a+1
+  uint8_t* phk = phq + 2 * kTile;                        // Phi(K)_a, Phi(K)_a+1
+  uint64_t* full = reinterpret_cast<uint64_t*>(phk + 2 * kTile);  // kP2Stages
+  uint64_t* mma_bar = full + kP2Stages;
+  uint64_t* drain = mma_bar + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int q4 = warp & 3, cq = warp >> 2;
+  const int row = q4 * 32 + lane;                 // token row (read-out) / feature row b of a pair
+  const int bh = blockIdx.x / kP2Groups, grp = blockIdx.x % kP2Groups;
+  const int a0 = grp * kP2Blocks;
+  const int n_chunks = (N + kC - 1) / kC;
+  const bool tma_thread = tid == 32;
+
+  if (tid == 0) {
+    for (int s = 0; s < kP2Stages; ++s) mbar_init(&full[s], 1);
+    mbar_init(mma_bar, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  for (int e = tid; e < 2048 / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tl = lane_base(tbase);
+  pdl_wait();
+
+  auto issue = [&](int c) {
+    const int s = c % kP2Stages;
+    uint8_t* st = stages + s * 3 * kTile;
+    mbar_arrive_expect_tx(&full[s], 3 * kTile);
+    tma_load_3d(st, &tm_q, &full[s], 0, c * kC, bh);
+    tma_load_3d(st + kTile, &tm_k, &full[s], 0, c * kC, bh);
+    tma_load_3d(st + 2 * kTile, &tm_v, &full[s], 0, c * kC, bh);
+  };
+  int issued = 0;
+  if (tma_thread && n_chunks > 0) issue(issued++);
+
+  const uint32_t idRO = idesc_bf16(128, 64, false, true);  // Phi(Q)_a (K-major) x S_a (MN-major)
+  const uint32_t idUP = idesc_bf16(128, 64, true, true);   // [Phi(K)_a; Phi(K)_a+1]^T x V, both MN-major
+  uint32_t ph = 0;
+  bool ok = true;
+  int c = 0;
+  for (; c < n_chunks && ok; ++c) {
+    const int s = c % kP2Stages;
+    uint8_t* qt = stages + s * 3 * kTile;
+    uint8_t* kt = qt + kTile;
+    uint8_t* vt = qt + 2 * kTile;
+    const int t0 = c * kC;
+    const bool first = c == 0;
+    // the next chunk's tiles go to the other stage, which the previous chunk (all
+    // of its MMAs and reads done at its end) has released
+    if (tma_thread && c + 1 < n_chunks) issue(issued++);
+    if (!wait_uniform(&full[s], (c / kP2Stages) & 1, hdr, 41)) {
+      ok = false;
+      break;
+    }
+    // this thread's raw q and k (columns [16 cq, 16 cq + 16)) and the group's 8
+    // columns a of its row (rows past N were filled with zeros by the copy)
+    float qv[16], kv[16], qa[kP2Blocks], ka[kP2Blocks];
+    row16(qt, row, 2 * cq, qv);
+    row16(kt, row, 2 * cq, kv);
+    row8(qt, row, a0 / 8, qa);   // a0 is a multiple of 8: one logical 16-byte chunk
+    row8(kt, row, a0 / 8, ka);
+    if (grp == 0) {  // G_prev -> bf16 snapshot (rows b in lanes 0-63; zero before the first chunk)
+      if (q4 < 2) {
+        uint32_t r[16];
+        tmem_ld16(tl + kP2G + 16 * cq, r);
+        put16_tmem(gsnap, row, cq, r, !first);
+      }
+    }
+    for (int p = 0; p < kP2Blocks / 2 && ok; ++p) {
+      if (p > 0) {  // the previous pair's MMAs are done with the Phi buffers
+        if (!wait_uniform(mma_bar, ph, hdr, 42)) {
+          ok = false;
+          break;
+        }
+        ph ^= 1;
+        fence_after_sync();
+      }
+      put16_scaled(phq, row, cq, qv, qa[2 * p]);
+      put16_scaled(phq + kTile, row, cq, qv, qa[2 * p + 1]);
+      put16_scaled(phk, row, cq, kv, ka[2 * p]);
+      put16_scaled(phk + kTile, row, cq, kv, ka[2 * p + 1]);
+      {  // S pair p before this chunk's update -> bf16 snapshot (zero before the first chunk)
+        uint32_t r[16];
+        tmem_ld16(tl + kP2S + 64 * p + 16 * cq, r);
+        uint8_t* dst = snap + ((p & 1) * 2 + (q4 >> 1)) * kSnapBlock;
+        put16_tmem(dst, 32 * (q4 & 1) + lane, cq, r, !first);
+      }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+      if (tid == 0) {
+        const uint32_t qa_ = smem_u32(qt), ka_ = smem_u32(kt), va = smem_u32(vt);
+        const uint32_t pq = smem_u32(phq), pk = smem_u32(phk), oa = smem_u32(ones);
+        const uint32_t sa = smem_u32(snap + (p & 1) * 2 * kSnapBlock);
+        if (p == 0 && grp == 0) {
+          // Q G_prev (A = raw Q K-major, B = G snapshot MN-major), then G += [K^T; 1^T] K
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tbase + kP2Q, sdesc(qa_ + k * 32, 16, 1024), sdesc(smem_u32(gsnap) + k * 2048, 1024, 1024),
+                   idRO, k);
+#pragma unroll
+          for (int k = 0; k < kC / 16; ++k)
+            mma_ss(tbase + kP2G, sdesc(ka_ + k * 2048, oa - (ka_ + k * 2048), 1024),
+                   sdesc(ka_ + k * 2048, 1024, 1024), idUP, (first && k == 0) ? 0u : 1u);
+        }
+        // read-out: num += Phi(Q)_a S_a + Phi(Q)_a+1 S_a+1 (S before this chunk)
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tbase + kP2N, sdesc(pq + blk * kTile + k * 32, 16, 1024),
+                   sdesc(sa + blk * kSnapBlock + k * 2048, 1024, 1024), idRO,
+                   (p == 0 && blk == 0 && k == 0) ? 0u : 1u);
+        // update: S pair += [Phi(K)_a; Phi(K)_a+1]^T V (M = 128, the two 64-row halves
+        // kTile apart; K = the chunk's tokens)
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kP2S + 64 * p, sdesc(pk + k * 2048, kTile, 1024), sdesc(va + k * 2048, 1024, 1024),
+                 idUP, (first && k == 0) ? 0u : 1u);
+        mma_commit(mma_bar);
+      }
+    }
+    if (!ok) break;
+    if (!wait_uniform(mma_bar, ph, hdr, 43)) {
+      ok = false;
+      break;
+    }
+    ph ^= 1;
+    fence_after_sync();
+    // the state part of this chunk's numerators (and, group 0, of its denominators)
+    const bool valid = t0 + row < N;
+    {
+      uint32_t r[16];
+      tmem_ld16(tl + kP2N + 16 * cq, r);
+      if (valid) {
+        float4* dst = reinterpret_cast<float4*>(num_state + ((size_t)bh * N + t0 + row) * kDim + 16 * cq);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          atomicAdd(dst + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+      }
+    }
+    if (grp == 0) {  // q^T G_prev q over this thread's 16 columns
+      uint32_t r[16];
+      tmem_ld16(tl + kP2Q + 16 * cq, r);
+      float d = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) d += qv[j] * __uint_as_float(r[j]);
+      if (valid) atomicAdd(den_state + (size_t)bh * N + t0 + row, d);
+    }
+  }
+  pdl_trigger();
+  if (tma_thread)  // copies issued for chunks the loop did not consume (after an early exit)
+    for (int k = c; k < issued; ++k)
+      if (!mbar_wait(&full[k % kP2Stages], (k / kP2Stages) & 1)) record_timeout(hdr, 44);
+  drain_mmas(drain, hdr, 45);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ output
+
+constexpr int kP2OutThreads = 128;  // thread = chunk row
+// Q, K, V tiles + ones; padded so that at most two CTAs share an SM (their TMEM)
+constexpr int kP2OutSmem = 1024 + 3 * kTile + 2048 + 256 + 48 * 1024;
+constexpr uint32_t kP2OP = 0;    // 128: P = Q K^T, then bf16 P_L in [0, 64)
+constexpr uint32_t kP2OO = 128;  // 80: P_L [V | 1]: numerator in [0, 64), row sum in column 64
+
+__global__ void __launch_bounds__(kP2OutThreads)
+tc_poly2_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    int N, const float* __restrict__ num_state, const float* __restrict__ den_state,
+                    WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qt = sm;
+  uint8_t* kt = qt + kTile;
+  uint8_t* vt = kt + kTile;
+  uint8_t* ones = vt + kTile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 2048);
+  uint64_t* mma_bar = full + 1;
+  uint64_t* drain = mma_bar + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int tid = threadIdx.x, warp = tid / 32;
+  const int n_chunks = (N + kC - 1) / kC;
+  const int bh = blockIdx.x / n_chunks, chunk = blockIdx.x % n_chunks;
+  const int t0 = chunk * kC, row = tid;
+  if (tid == 0) {
+    mbar_init(full, 1);
+    mbar_init(mma_bar, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < 2048 / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
+  pdl_wait();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(full, 3 * kTile);
+    tma_load_3d(qt, &tm_q, full, 0, t0, bh);
+    tma_load_3d(kt, &tm_k, full, 0, t0, bh);
+    tma_load_3d(vt, &tm_v, full, 0, t0, bh);
+  }
+  bool ok = wait_uniform(full, 0, hdr, 46);
+  if (ok) {
+    if (tid == 0) {  // P = Q K^T
+      const uint32_t idP = idesc_bf16(128, 128, false, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kP2OP, sdesc(smem_u32(qt) + k * 32, 16, 1024), sdesc(smem_u32(kt) + k * 32, 16, 1024),
+               idP, k);
+      mma_commit(mma_bar);
+    }
+    ok = wait_uniform(mma_bar, 0, hdr, 47);
+  }
+  if (ok) {
+    fence_after_sync();
+    // (q_i . k_j)^2 for j <= i, in float32, rounded once to bf16 and packed over
+    // the first 64 columns (this thread's own TMEM lane: read all, then write)
+    uint32_t pk[4][16];
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) {
+      uint32_t r[32];
+      tmem_ld32(tl + kP2OP + 32 * sl, r);
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const int j0 = 32 * sl + 2 * cc;
+        const float a = __uint_as_float(r[2 * cc]), b = __uint_as_float(r[2 * cc + 1]);
+        pk[sl][cc] = pack_bf16(j0 <= row ? a * a : 0.f, j0 + 1 <= row ? b * b : 0.f);
+      }
+    }
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) tmem_st16(tl + kP2OP + 16 * sl, pk[sl]);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {  // P_L [V | 1] (N = 80; V's columns 64.. from the ones block)
+      const uint32_t va = smem_u32(vt), oa = smem_u32(ones);
+      const uint32_t idPV = idesc_bf16(128, 80, false, true);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ts(tbase + kP2OO, tbase + kP2OP + k * 8, sdesc(va + k * 2048, oa - (va + k * 2048), 1024), idPV, k);
+      mma_commit(mma_bar);
+    }
+    ok = wait_uniform(mma_bar, 1, hdr, 48);
+  }
+  if (ok) {
+    fence_after_sync();
+    uint32_t rd[16], ra[32], rb[32];
+    tmem_ld16(tl + kP2OO + 64, rd);
+    tmem_ld32x2(tl + kP2OO, ra, tl + kP2OO + 32, rb);
+    const bool valid = t0 + row < N;
+    const size_t at = (size_t)bh * N + t0 + row;
+    const float den = __uint_as_float(rd[0]) + (valid ? den_state[at] : 1.f);
+    const float inv = 1.f / den;
+    const float4* ns = reinterpret_cast<const float4*>(num_state + at * kDim);
+    // out = num / den -> bf16, staged in the Q tile (no MMA reads it any more)
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16) {
+      const uint32_t* src = c16 < 4 ? ra : rb;
+      const int b = (c16 & 3) * 8;
+      const float4 s0 = valid ? ns[2 * c16] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 s1 = valid ? ns[2 * c16 + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float n[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = pack_bf16((__uint_as_float(src[b + 2 * q]) + n[2 * q]) * inv,
+                         (__uint_as_float(src[b + 2 * q + 1]) + n[2 * q + 1]) * inv);
+      *reinterpret_cast<uint4*>(qt + sw128(row, c16 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {  // rows past the sequence end are clipped by the tensor map
+      tma_store_3d(&tm_o, qt, 0, t0, bh);
+      bulk_commit();
+      bulk_wait_all<0>();
+    }
+  }
+  pdl_trigger();
+  if (tid == 0 && !ok) {  // after an early exit: the tile copy and the MMAs issued are done
+    if (!mbar_wait(full, 0)) record_timeout(hdr, 49);
+  }
+  drain_mmas(drain, hdr, 50);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+}  // namespace
+}  // namespace tcx
+
+using namespace tcx;
+
+bool poly2_supported(int D, int M, int dtype, int causal) {
+  return dtype == LA_BF16 && D == 64 && M == 64 && causal != 0;
+}
+
+size_t poly2_workspace(int BH, int N) {
+  return kHeaderBytes + align_up(sizeof(float) * (size_t)BH * N * (kDim + 1), 256);
+}
+
+cudaError_t poly2_forward(const void* q, const void* k, const void* v, void* out, int BH, int N,
+                          void* ws, cudaStream_t st) {
+  WorkspaceHeader* hdr = static_cast<WorkspaceHeader*>(ws);
+  float* num_state = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
+  float* den_state = num_state + (size_t)BH * N * kDim;
+  CUtensorMap tq, tk, tv, to;
+  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
+  if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
+      !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(num_state, 0, sizeof(float) * (size_t)BH * N * (kDim + 1), st);
+  if (e != cudaSuccess) return e;
+  e = configure(tc_poly2_state_kernel, kP2Smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(tc_poly2_state_kernel, dim3(BH * kP2Groups), dim3(kP2Threads), kP2Smem, st, tq, tk,
+                 tv, N, num_state, den_state, hdr);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  e = configure(tc_poly2_out_kernel, kP2OutSmem);
+  if (e != cudaSuccess) return e;
+  const int n_chunks = (N + kC - 1) / kC;
+  e = launch_pdl(tc_poly2_out_kernel, dim3(BH * n_chunks), dim3(kP2OutThreads), kP2OutSmem, st, tq,
+                 tk, tv, to, N, (const float*)num_state, (const float*)den_state, hdr);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace la
