@@ -20,12 +20,14 @@
 //  1. tc_poly2_state_kernel: one CTA per (sequence, group of 8 feature blocks),
 //     walking the sequence's chunks in order. Its 8 blocks of S stay in TMEM
 //     in float32 (two blocks stacked per M = 128 accumulator). Per chunk and
-//     block pair it forms Phi(Q)_a and Phi(K)_a (bf16) in shared memory from the
-//     chunk's q and k, snapshots S_a (bf16) and issues the read-out Phi(Q)_a S_a
-//     (before the update) and the update [Phi(K)_a; Phi(K)_{a+1}]^T V on the
-//     tensor cores. The CTA's partial numerators (the state part of num) are
-//     added into a float32 buffer with vector atomics; the CTA of group 0 also
-//     carries G and adds q^T G_prev q to the denominators.
+//     block pair (a, a + 1) it snapshots S_a, S_a+1 (bf16) and forms
+//     Phi(K)_a = k_a (.) K (bf16) in shared memory, then issues on the tensor
+//     cores X = Q [S_a | S_a+1] (the read-out, before the update) and the update
+//     [Phi(K)_a; Phi(K)_a+1]^T V; the next pair's snapshot and Phi(K) are formed
+//     while these run. The read-out finishes in float32 on the CUDA cores,
+//     num_i += q_ia X_a[i] + q_i(a+1) X_a+1[i], and the chunk's state
+//     numerators are added into a float32 buffer with vector reductions; the CTA
+//     of group 0 also carries G and adds q^T G_prev q to the denominators.
 //  2. tc_poly2_out_kernel: one CTA per chunk: P = Q K^T on the tensor cores,
 //     squared and masked in float32, rounded to bf16 into TMEM, then
 //     P_L [V | 1] (numerator and row sums in one N = 80 group), plus the
@@ -47,14 +49,14 @@ constexpr int kP2Smem = 1024 + kP2Stages * 3 * kTile   // Q, K, V stages
                         + 2 * 2 * kSnapBlock          // S snapshots: 2 buffers x block pair
                         + kSnapBlock                  // G snapshot
                         + 2048                        // 16 rows of ones
-                        + 4 * kTile                   // Phi(Q)_a, Phi(Q)_a+1, Phi(K)_a, Phi(K)_a+1
+                        + 2 * 2 * kTile               // Phi(K)_a, Phi(K)_a+1: 2 buffers
                         + 256;                        // barriers, TMEM slot
 
 // TMEM columns
 constexpr uint32_t kP2S = 0;     // 4 x 64: S block pairs (lanes 0-63 block a, 64-127 block a + 1)
-constexpr uint32_t kP2N = 256;   // 64: this chunk's state numerator (rows = tokens)
-constexpr uint32_t kP2G = 320;   // 64: G in lanes 0-63 ([K^T; 1^T] K; lanes 64-127 unused)
-constexpr uint32_t kP2Q = 384;   // 64: Q G_prev (rows = tokens)
+constexpr uint32_t kP2X = 256;   // 128: Q [S_a | S_a+1] of the pair in flight (rows = tokens)
+constexpr uint32_t kP2G = 384;   // 64: G in lanes 0-63 ([K^T; 1^T] K; lanes 64-127 unused)
+constexpr uint32_t kP2Q = 448;   // 64: Q G_prev (rows = tokens)
 
 // 16 consecutive raw bf16 of row `row`, logical 16-byte chunks c0, c0 + 1 -> float.
 __device__ __forceinline__ void row16(const uint8_t* tile, int row, int c0, float* out) {
@@ -92,6 +94,17 @@ __device__ __forceinline__ void put16_scaled(uint8_t* tile, int row, int cq, con
   }
 }
 
+// Fire-and-forget float32 additions to global memory (no value comes back, so
+// nothing waits for the L2 round trip).
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red_add(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
+
 // 16 float32 TMEM values -> bf16 at row `row`, columns [16 cq, 16 cq + 16) (zero if !keep).
 __device__ __forceinline__ void put16_tmem(uint8_t* tile, int row, int cq, const uint32_t (&r)[16],
                                            bool keep) {
@@ -115,9 +128,8 @@ tc_poly2_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   uint8_t* snap = stages + kP2Stages * 3 * kTile;        // [2][2][64 x 128 B]
   uint8_t* gsnap = snap + 4 * kSnapBlock;
   uint8_t* ones = gsnap + kSnapBlock;
-  uint8_t* phq = ones + 2048;                            // Phi(Q)_a, Phi(Q)_a+1
-  uint8_t* phk = phq + 2 * kTile;                        // Phi(K)_a, Phi(K)_a+1
-  uint64_t* full = reinterpret_cast<uint64_t*>(phk + 2 * kTile);  // kP2Stages
+  uint8_t* phk = ones + 2048;                            // [2][Phi(K)_a | Phi(K)_a+1]
+  uint64_t* full = reinterpret_cast<uint64_t*>(phk + 4 * kTile);  // kP2Stages
   uint64_t* mma_bar = full + kP2Stages;
   uint64_t* drain = mma_bar + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -164,7 +176,8 @@ tc_poly2_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   int issued = 0;
   if (tma_thread && n_chunks > 0) issue(issued++);
 
-  const uint32_t idRO = idesc_bf16(128, 64, false, true);  // Phi(Q)_a (K-major) x S_a (MN-major)
+  const uint32_t idX = idesc_bf16(128, 128, false, true);  // Q (K-major) x [S_a | S_a+1] (MN-major)
+  const uint32_t idQG = idesc_bf16(128, 64, false, true);  // Q x G_prev
   const uint32_t idUP = idesc_bf16(128, 64, true, true);   // [Phi(K)_a; Phi(K)_a+1]^T x V, both MN-major
   uint32_t ph = 0;
   bool ok = true;
@@ -185,92 +198,95 @@ tc_poly2_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     // this thread's raw q and k (columns [16 cq, 16 cq + 16)) and the group's 8
     // columns a of its row (rows past N were filled with zeros by the copy)
-    float qv[16], kv[16], qa[kP2Blocks], ka[kP2Blocks];
+    float qv[16], kv[16], qa[kP2Blocks], ka[kP2Blocks], num[16];
     row16(qt, row, 2 * cq, qv);
     row16(kt, row, 2 * cq, kv);
     row8(qt, row, a0 / 8, qa);   // a0 is a multiple of 8: one logical 16-byte chunk
     row8(kt, row, a0 / 8, ka);
-    if (grp == 0) {  // G_prev -> bf16 snapshot (rows b in lanes 0-63; zero before the first chunk)
-      if (q4 < 2) {
-        uint32_t r[16];
-        tmem_ld16(tl + kP2G + 16 * cq, r);
-        put16_tmem(gsnap, row, cq, r, !first);
-      }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) num[j] = 0.f;
+    if (grp == 0 && q4 < 2) {  // G_prev -> bf16 snapshot (rows b in lanes 0-63; zero before the first chunk)
+      uint32_t r[16];
+      tmem_ld16(tl + kP2G + 16 * cq, r);
+      put16_tmem(gsnap, row, cq, r, !first);
     }
-    for (int p = 0; p < kP2Blocks / 2 && ok; ++p) {
-      if (p > 0) {  // the previous pair's MMAs are done with the Phi buffers
-        if (!wait_uniform(mma_bar, ph, hdr, 42)) {
-          ok = false;
-          break;
-        }
-        ph ^= 1;
-        fence_after_sync();
-      }
-      put16_scaled(phq, row, cq, qv, qa[2 * p]);
-      put16_scaled(phq + kTile, row, cq, qv, qa[2 * p + 1]);
-      put16_scaled(phk, row, cq, kv, ka[2 * p]);
-      put16_scaled(phk + kTile, row, cq, kv, ka[2 * p + 1]);
-      {  // S pair p before this chunk's update -> bf16 snapshot (zero before the first chunk)
-        uint32_t r[16];
-        tmem_ld16(tl + kP2S + 64 * p + 16 * cq, r);
-        uint8_t* dst = snap + ((p & 1) * 2 + (q4 >> 1)) * kSnapBlock;
-        put16_tmem(dst, 32 * (q4 & 1) + lane, cq, r, !first);
-      }
-      fence_proxy_async_smem();
-      fence_before_sync();
-      __syncthreads();
-      fence_after_sync();
-      if (tid == 0) {
-        const uint32_t qa_ = smem_u32(qt), ka_ = smem_u32(kt), va = smem_u32(vt);
-        const uint32_t pq = smem_u32(phq), pk = smem_u32(phk), oa = smem_u32(ones);
-        const uint32_t sa = smem_u32(snap + (p & 1) * 2 * kSnapBlock);
-        if (p == 0 && grp == 0) {
-          // Q G_prev (A = raw Q K-major, B = G snapshot MN-major), then G += [K^T; 1^T] K
+    // pair p's operands: S_a, S_a+1 before this chunk's update (bf16; zero before
+    // the first chunk) and Phi(K)_a, Phi(K)_a+1, into buffer p & 1
+    auto build = [&](int p) {
+      uint32_t r[16];
+      tmem_ld16(tl + kP2S + 64 * p + 16 * cq, r);
+      put16_tmem(snap + ((p & 1) * 2 + (q4 >> 1)) * kSnapBlock, 32 * (q4 & 1) + lane, cq, r, !first);
+      uint8_t* pk = phk + (p & 1) * 2 * kTile;
+      put16_scaled(pk, row, cq, kv, ka[2 * p]);
+      put16_scaled(pk + kTile, row, cq, kv, ka[2 * p + 1]);
+    };
+    auto issue_pair = [&](int p) {
+      const uint32_t qa_ = smem_u32(qt), ka_ = smem_u32(kt), va = smem_u32(vt);
+      const uint32_t pk = smem_u32(phk + (p & 1) * 2 * kTile), oa = smem_u32(ones);
+      const uint32_t sa = smem_u32(snap + (p & 1) * 2 * kSnapBlock);
+      if (p == 0 && grp == 0) {
+        // Q G_prev (A = raw Q K-major, B = G snapshot MN-major), then G += [K^T; 1^T] K
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tbase + kP2Q, sdesc(qa_ + k * 32, 16, 1024), sdesc(smem_u32(gsnap) + k * 2048, 1024, 1024),
-                   idRO, k);
-#pragma unroll
-          for (int k = 0; k < kC / 16; ++k)
-            mma_ss(tbase + kP2G, sdesc(ka_ + k * 2048, oa - (ka_ + k * 2048), 1024),
-                   sdesc(ka_ + k * 2048, 1024, 1024), idUP, (first && k == 0) ? 0u : 1u);
-        }
-        // read-out: num += Phi(Q)_a S_a + Phi(Q)_a+1 S_a+1 (S before this chunk)
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tbase + kP2N, sdesc(pq + blk * kTile + k * 32, 16, 1024),
-                   sdesc(sa + blk * kSnapBlock + k * 2048, 1024, 1024), idRO,
-                   (p == 0 && blk == 0 && k == 0) ? 0u : 1u);
-        // update: S pair += [Phi(K)_a; Phi(K)_a+1]^T V (M = 128, the two 64-row halves
-        // kTile apart; K = the chunk's tokens)
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kP2Q, sdesc(qa_ + k * 32, 16, 1024), sdesc(smem_u32(gsnap) + k * 2048, 1024, 1024),
+                 idQG, k);
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kP2S + 64 * p, sdesc(pk + k * 2048, kTile, 1024), sdesc(va + k * 2048, 1024, 1024),
-                 idUP, (first && k == 0) ? 0u : 1u);
-        mma_commit(mma_bar);
+          mma_ss(tbase + kP2G, sdesc(ka_ + k * 2048, oa - (ka_ + k * 2048), 1024),
+                 sdesc(ka_ + k * 2048, 1024, 1024), idUP, (first && k == 0) ? 0u : 1u);
+      }
+      // read-out: X = Q [S_a | S_a+1] (the two snapshot blocks as N blocks kSnapBlock apart)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kP2X, sdesc(qa_ + k * 32, 16, 1024), sdesc(sa + k * 2048, kSnapBlock, 1024), idX, k);
+      // update: S pair += [Phi(K)_a; Phi(K)_a+1]^T V (M = 128, the two 64-row halves kTile
+      // apart; K = the chunk's tokens)
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + kP2S + 64 * p, sdesc(pk + k * 2048, kTile, 1024), sdesc(va + k * 2048, 1024, 1024),
+               idUP, (first && k == 0) ? 0u : 1u);
+      mma_commit(mma_bar);
+    };
+    build(0);
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) issue_pair(0);
+#pragma unroll
+    for (int p = 0; p < kP2Blocks / 2; ++p) {
+      // the next pair's operands go to the other buffers (their last readers, pair
+      // p - 1's MMAs, are done) while pair p's MMAs run
+      if (p + 1 < kP2Blocks / 2) build(p + 1);
+      if (!wait_uniform(mma_bar, ph, hdr, 42)) {
+        ok = false;
+        break;
+      }
+      ph ^= 1;
+      fence_after_sync();
+      {  // num += q_a X_a + q_a+1 X_a+1 over this thread's 16 columns
+        uint32_t xa[16], xb[16];
+        tmem_ld16x2(tl + kP2X + 16 * cq, xa, tl + kP2X + 64 + 16 * cq, xb);
+        const float sa = qa[2 * p], sb = qa[2 * p + 1];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          num[j] = fmaf(sb, __uint_as_float(xb[j]), fmaf(sa, __uint_as_float(xa[j]), num[j]));
+      }
+      if (p + 1 < kP2Blocks / 2) {
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncthreads();  // X is read and the next pair's operands are in place
+        fence_after_sync();
+        if (tid == 0) issue_pair(p + 1);
       }
     }
     if (!ok) break;
-    if (!wait_uniform(mma_bar, ph, hdr, 43)) {
-      ok = false;
-      break;
-    }
-    ph ^= 1;
-    fence_after_sync();
     // the state part of this chunk's numerators (and, group 0, of its denominators)
     const bool valid = t0 + row < N;
-    {
-      uint32_t r[16];
-      tmem_ld16(tl + kP2N + 16 * cq, r);
-      if (valid) {
-        float4* dst = reinterpret_cast<float4*>(num_state + ((size_t)bh * N + t0 + row) * kDim + 16 * cq);
+    if (valid) {
+      float* dst = num_state + ((size_t)bh * N + t0 + row) * kDim + 16 * cq;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          atomicAdd(dst + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
-      }
+      for (int j = 0; j < 4; ++j) red_add4(dst + 4 * j, num[4 * j], num[4 * j + 1], num[4 * j + 2], num[4 * j + 3]);
     }
     if (grp == 0) {  // q^T G_prev q over this thread's 16 columns
       uint32_t r[16];
@@ -278,8 +294,11 @@ tc_poly2_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       float d = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) d += qv[j] * __uint_as_float(r[j]);
-      if (valid) atomicAdd(den_state + (size_t)bh * N + t0 + row, d);
+      if (valid) red_add(den_state + (size_t)bh * N + t0 + row, d);
     }
+    fence_before_sync();
+    __syncthreads();  // every TMEM read of this chunk is done before the next one's MMAs
+    fence_after_sync();
   }
   pdl_trigger();
   if (tma_thread)  // copies issued for chunks the loop did not consume (after an early exit)
