@@ -176,8 +176,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's calls directly instead of replaying CUDA graphs")
     ap.add_argument("--part", default=None,
-                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "decode", "extend",
-                             "poly2"],
+                    choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "bwdfwd", "decode",
+                             "extend", "poly2"],
                     help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
@@ -447,8 +447,8 @@ def run_ours(args, world, rank, local):
     def fwd():
         la.la_forward(q, k, v, True, out, wsf)
 
-    def bwd():
-        la.la_backward(q, k, v, dout, True, dq, dk, dv, wsb)
+    def bwd():  # the training order: the backward reads the forward's segment states
+        la.la_backward(q, k, v, dout, True, dq, dk, dv, wsb, fwd_workspace=wsf)
 
     # Each call is captured once into a CUDA graph (kernels + workspace memsets,
     # with programmatic-dependent-launch edges) and replayed per step.
@@ -530,7 +530,8 @@ def run_ours(args, world, rank, local):
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
-                   "step": "la_forward + la_backward (causal)", "grads": "float32",
+                   "step": "la_forward + la_backward (causal; the backward reads the "
+                           "forward's segment states from its workspace)", "grads": "float32",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "CUDA graph replay per call" if per_step_launches is not None
                    else "direct launches",
@@ -592,7 +593,7 @@ def run_e2e(la, w, q, k, v, dout, device, K):
                 sl = slice(b, b + 1)
                 la.la_forward(q[sl], k[sl], v[sl], True, out=o[sl], workspace=wf)
                 la.la_backward(q[sl], k[sl], v[sl], dout[sl], True, dq=gq[sl], dk=gk[sl], dv=gv[sl],
-                               workspace=wb)
+                               workspace=wb, fwd_workspace=wf)
                 e_done[b].record(s_cmp)
         for b in range(nb):
             s_out.wait_event(e_done[b])
@@ -724,7 +725,7 @@ def run_part(args):
     labuild.build()
     la.load_library()
     device = torch.device("cuda", 0)
-    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "poly2": MAIN,
+    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "bwdfwd": MAIN, "poly2": MAIN,
             "fwd3072": "causal_fwd_b8h8n3072d64",
             "noncausal": "noncausal_fwd_b4h8n4096d64",
             "decode": "decode_s256h8d64_prefill1024_steps3072",
@@ -742,6 +743,11 @@ def run_part(args):
         fn = extend_setup(la, w, g, device, S, Z)
     elif args.part == "bwd":
         fn = lambda: la.la_backward(q, k, v, dout, True)
+    elif args.part == "bwdfwd":  # the backward reading a forward's segment states
+        wsf = torch.empty(la.la_forward_workspace_bytes(w.B, w.H, w.N, w.D, w.M, True),
+                          dtype=torch.uint8, device=device)
+        la.la_forward(q, k, v, True, workspace=wsf)
+        fn = lambda: la.la_backward(q, k, v, dout, True, fwd_workspace=wsf)
     elif args.part == "poly2":
         fn = lambda: la.la_forward_poly2(q, k, v, True)
     elif args.part == "fwdbwd":

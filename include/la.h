@@ -237,6 +237,24 @@ int la_backward_shard_kv(const void* q, const void* k, const void* v, const void
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * la_backward_from_forward -- la_backward that reuses the segment states a
+ * la_forward call left in its workspace (the forward-direction sums S, Z before
+ * each segment of the sequence, [summary §3.3.1]), instead of recomputing them:
+ * the training order, where the backward follows the forward on the same
+ * inputs. Same arguments, results and status codes as la_backward, plus
+ * fwd_workspace / fwd_workspace_bytes: the workspace of a la_forward call with
+ * the same q, k, B, H, N, D, M, causal and dtype, completed (or earlier on the
+ * same stream) and not reused since. Where that forward keeps no states (one
+ * chunk per sequence, or the CUDA-core path) they are computed as la_backward
+ * does. The forward workspace is only read.
+ */
+int la_backward_from_forward(const void* q, const void* k, const void* v, const void* dout,
+                             float* dq, float* dk, float* dv,
+                             int B, int H, int N, int D, int M, int causal, int dtype,
+                             const void* fwd_workspace, size_t fwd_workspace_bytes,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * la_decode_step -- one recurrent generation step per (stream, head).
  *
  * [deck slide 4], [summary §3.3.2, §3.4]: update, then read out:

@@ -52,6 +52,8 @@ _SIGNATURES = {
     "la_forward_noalloc_status": (_c_int, [_vp]),
     "la_state_sums": (_c_int, [_vp] * 4 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_poly2_workspace_bytes": (_c_size, [_c_int] * 7),
+    "la_backward_from_forward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp, _c_size,
+                                                                     _vp]),
     "la_forward_poly2": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_forward_shard": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_backward_shard_q": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_vp, _c_size, _vp]),
@@ -291,8 +293,13 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspac
     return out
 
 
-def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace=None):
-    """float32 gradients (dq, dk, dv) of sum(dout * la_forward(q, k, v))."""
+def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace=None,
+                fwd_workspace=None):
+    """float32 gradients (dq, dk, dv) of sum(dout * la_forward(q, k, v)).
+
+    fwd_workspace: the workspace of a la_forward call on the same q, k, v (and causal), not
+    reused since; its segment states are then read instead of recomputed
+    (la_backward_from_forward)."""
     import torch
     fn, f32 = "la_backward", torch.float32
     (B, H, N), D, M = _dims(fn, q, v, 4)
@@ -311,11 +318,20 @@ def la_backward(q, k, v, dout, causal=True, dq=None, dk=None, dv=None, workspace
     dv = torch.empty((B, H, N, M), dtype=f32, device=dev) if dv is None else dv
     nbytes = lib.la_backward_workspace_bytes(B, H, N, D, M, int(bool(causal)), dt)
     ws = _workspace(nbytes, dev, workspace)
+    if fwd_workspace is not None:
+        _need_cuda(fwd_workspace, device=dev)
     with _on_device(dev):
-        st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
-                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, M,
-                             int(bool(causal)), dt, ws.data_ptr(), ws.numel() * ws.element_size(),
-                             _stream_ptr(dev))
+        if fwd_workspace is None:
+            st = lib.la_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, M,
+                                 int(bool(causal)), dt, ws.data_ptr(),
+                                 ws.numel() * ws.element_size(), _stream_ptr(dev))
+        else:
+            st = lib.la_backward_from_forward(
+                q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                dk.data_ptr(), dv.data_ptr(), B, H, N, D, M, int(bool(causal)), dt,
+                fwd_workspace.data_ptr(), fwd_workspace.numel() * fwd_workspace.element_size(),
+                ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(dev))
     _check("la_backward", st)
     return dq, dk, dv
 

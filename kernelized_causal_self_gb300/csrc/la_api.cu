@@ -322,6 +322,33 @@ int la_backward_shard_kv(const void* q, const void* k, const void* v, const void
                                         workspace, st));
 }
 
+int la_backward_from_forward(const void* q, const void* k, const void* v, const void* dout,
+                             float* dq, float* dk, float* dv, int B, int H, int N, int D, int M,
+                             int causal, int dtype, const void* fwd_workspace,
+                             size_t fwd_workspace_bytes, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, dout, dq, dk, dv})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_backward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  const size_t need_fwd = la_forward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (fwd_workspace == nullptr || !aligned16(fwd_workspace) || fwd_workspace_bytes < need_fwd)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  if (!la::tc_forward_supported(D, M, dtype))  // the CUDA-core path keeps no forward states
+    return from_cuda(la::simt_backward(q, k, v, dout, dq, dk, dv, B * H, N, D, M, causal != 0,
+                                       dtype, workspace, st));
+  const float* pre = la::tc_forward_prefix(fwd_workspace, B * H, N, causal != 0);
+  cudaError_t e = la::tc_backward_q(q, k, v, dout, dq, nullptr, nullptr, B * H, N, causal != 0,
+                                    workspace, st, nullptr, pre);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::tc_backward_kv(q, k, v, dout, dk, dv, nullptr, B * H, N, causal != 0,
+                                      workspace, st));
+}
+
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,
                    int n_streams, int H, int D, int M, int dtype, void* stream) {
   if (!valid_dims(n_streams, H, 1, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;

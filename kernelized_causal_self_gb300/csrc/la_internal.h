@@ -80,7 +80,12 @@ size_t tc_backward_workspace(int BH, int N);
 // runs both from zero states.
 cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const void* dout,
                           float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
-                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault = nullptr);
+                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault = nullptr,
+                          const float* fwd_prefix = nullptr);
+// The per-segment states a tensor-core la_forward call left in its workspace (causal:
+// exclusive prefixes; non-causal: totals), laid out as the backward reads them (both use
+// make_geometry(BH, N)); nullptr if that forward computed none (one chunk per sequence).
+const float* tc_forward_prefix(const void* fwd_ws, int BH, int N, bool causal);
 cudaError_t tc_backward_kv(const void* q, const void* k, const void* v, const void* dout,
                            float* dk, float* dv, const StateIO* suf, int BH, int N, bool causal,
                            void* ws, cudaStream_t st);

@@ -1048,7 +1048,8 @@ struct BwdWork {
 
 cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const void* dout,
                           float* dq, const StateIO* pre, const StateIO* own, int BH, int N,
-                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault) {
+                          bool causal, void* ws, cudaStream_t st, const FaultHook* fault,
+                          const float* fwd_prefix) {
   const Geometry g = make_geometry(BH, N);
   Geometry gq = g;  // the forward-direction kernel's copy, with the test hook if any
   if (fault != nullptr) {
@@ -1065,17 +1066,24 @@ cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const voi
       !make_tmap_f32_3d(&tdq, dq, kDim, n, bh, 32, kC, 1))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_segment_states(&tk, &tv, g, w.spartial, w.hdr, true, st);
-  if (e != cudaSuccess) return e;
-  e = launch_scan(w.spartial, w.sprefix, g, causal ? kScanPrefix : kScanTotal,
-                  pre != nullptr ? *pre : StateIO{}, w.hdr, st);
-  if (e != cudaSuccess) return e;
+  // the segment states before each segment: the forward's (same geometry, same inputs), or
+  // computed here (segment increments in the psi form, then the prefix / total scan)
+  const float* sprefix = fwd_prefix;
+  cudaError_t e = cudaSuccess;
+  if (sprefix == nullptr) {
+    e = launch_segment_states(&tk, &tv, g, w.spartial, w.hdr, false, st);
+    if (e != cudaSuccess) return e;
+    e = launch_scan(w.spartial, w.sprefix, g, causal ? kScanPrefix : kScanTotal,
+                    pre != nullptr ? *pre : StateIO{}, w.hdr, st);
+    if (e != cudaSuccess) return e;
+    sprefix = w.sprefix;
+  }
   auto run_q = [&](auto kern) {
     cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sm_count());
     err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, gq,
-                     (const float*)w.sprefix, w.rpartial, w.den, w.gd, w.hdr);
+                     sprefix, w.rpartial, w.den, w.gd, w.hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };

@@ -741,16 +741,53 @@ int sm_count() {
   return n;
 }
 
+namespace {
+
+// Items (segment-major: item = seg * BH + bh) are dealt round robin to G persistent
+// CTAs. Returns the largest number of chunks and of items any CTA gets when each
+// sequence of n_chunks chunks is cut into segments of s chunks (the last one shorter).
+void deal(long long BH, long long n_chunks, long long s, long long G, long long& max_chunks,
+          long long& max_items) {
+  const long long n_seg = (n_chunks + s - 1) / s, last = n_chunks - (n_seg - 1) * s;
+  const long long items = BH * n_seg, lo = items - BH;  // [lo, items): the short last segments
+  max_chunks = max_items = 0;
+  for (long long c = 0; c < G && c < items; ++c) {
+    const long long n = (items - 1 - c) / G + 1;
+    // items c + kG in [lo, items)
+    const long long k0 = lo > c ? (lo - c + G - 1) / G : 0;
+    const long long n_short = n > k0 ? n - k0 : 0;
+    const long long chunks = n * s - n_short * (s - last);
+    max_chunks = chunks > max_chunks ? chunks : max_chunks;
+    max_items = n > max_items ? n : max_items;
+  }
+}
+
+}  // namespace
+
+// Segment length: the one that minimises a model of a forward + backward's time. The
+// forward's kernels run two CTAs per SM, the backward's one; a CTA's time is its chunk
+// count (the backward's chunks cost ~4x the forward's) plus a little per item (state
+// loads, read-outs), and every item adds its states to the scans' traffic.
 Geometry make_geometry(int BH, int N) {
   Geometry g;
   g.BH = BH;
   g.N = N;
   g.n_chunks = (N + kC - 1) / kC;
-  // segments: aim for >= 4 items per SM while keeping segments >= 2 chunks
-  const int target_items = 4 * sm_count();
-  int seg_chunks = (int)(((long long)BH * g.n_chunks + target_items - 1) / target_items);
-  seg_chunks = max(2, seg_chunks);
-  g.seg_chunks = min(seg_chunks, g.n_chunks);
+  const long long sms = sm_count();
+  double best = 1e300;
+  int best_s = 1;
+  for (int s = 1; s <= g.n_chunks && s <= 64; ++s) {
+    long long fc, fi, bc, bi;
+    deal(BH, g.n_chunks, s, 2 * sms, fc, fi);
+    deal(BH, g.n_chunks, s, sms, bc, bi);
+    const long long items = (long long)BH * ((g.n_chunks + s - 1) / s);
+    const double cost = 3.9 * fc + 15.0 * bc + 0.2 * fi + 0.5 * bi + 0.02 * items;
+    if (cost <= best) {  // ties go to the longer segment
+      best = cost;
+      best_s = s;
+    }
+  }
+  g.seg_chunks = best_s;
   g.n_seg = (g.n_chunks + g.seg_chunks - 1) / g.seg_chunks;
   return g;
 }
@@ -789,6 +826,13 @@ bool tc_forward_supported(int D, int M, int dtype) { return dtype == LA_BF16 && 
 size_t tc_forward_workspace(int BH, int N) {
   const Geometry g = make_geometry(BH, N);
   return kHeaderBytes + 2 * align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256);
+}
+
+const float* tc_forward_prefix(const void* fwd_ws, int BH, int N, bool causal) {
+  const Geometry g = make_geometry(BH, N);
+  if (causal && g.n_chunks == 1) return nullptr;  // the direct path: no segment states
+  const float* partial = reinterpret_cast<const float*>(static_cast<const char*>(fwd_ws) + kHeaderBytes);
+  return partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;
 }
 
 cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, void* ws,

@@ -206,3 +206,21 @@ def test_shard_entry_points_reject_bad_arguments(lib):
     bad = list(args)
     bad[15] = 0
     assert lib.la_backward_shard_kv(*bad) == la.LA_ERR_WORKSPACE
+
+
+def test_backward_from_forward_rejects_bad_arguments(lib):
+    wsb = lib.la_backward_workspace_bytes(1, 2, 300, 64, 64, 1, 1)
+    wsf = lib.la_forward_workspace_bytes(1, 2, 300, 64, 64, 1, 1)
+    args = [FAKE] * 7 + [1, 2, 300, 64, 64, 1, 1, FAKE, wsf, FAKE, wsb, None]
+    bad = list(args)
+    bad[4] = 0                                  # dq missing
+    assert lib.la_backward_from_forward(*bad) == la.LA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[14] = 0                                 # no forward workspace
+    assert lib.la_backward_from_forward(*bad) == la.LA_ERR_WORKSPACE
+    bad = list(args)
+    bad[15] = wsf - 16                          # forward workspace too small for this shape
+    assert lib.la_backward_from_forward(*bad) == la.LA_ERR_WORKSPACE
+    bad = list(args)
+    bad[17] = 16                                # backward workspace too small
+    assert lib.la_backward_from_forward(*bad) == la.LA_ERR_WORKSPACE

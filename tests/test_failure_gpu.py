@@ -42,7 +42,8 @@ def _p(t):
 
 
 def _case():
-    # 8 chunks in 2 sequences: CTA 0 of each kernel has one 2-chunk segment (loads 0, 1)
+    # 8 chunks in 2 sequences; the hooks withhold CTA 0's first load (load 0), which
+    # every segment layout gives it
     B, H, N = 1, 2, 1000
     q, k, v = inputs.qkv(901, B, H, N, 64, 64, 0.125, inputs.BF16)
     g = inputs.upstream_grad(901, B, H, N, 64, 0.125, inputs.BF16)
@@ -59,7 +60,7 @@ def test_forward_load_wait_runs_out_and_the_next_call_is_exact(la):
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     t0 = time.perf_counter()
     rc = lib.la_debug_forward_fault(_p(tq), _p(tk), _p(tv), _p(out), B, H, N, 64, 64, 1,
-                                    la.LA_BF16, _p(ws), nbytes, 1, LIMIT_NS, st)
+                                    la.LA_BF16, _p(ws), nbytes, 0, LIMIT_NS, st)
     assert rc == la.LA_OK
     torch.cuda.synchronize()
     assert time.perf_counter() - t0 < 1.0          # returned on its own, well inside 2 s
@@ -82,7 +83,7 @@ def test_backward_load_wait_runs_out_and_the_next_call_is_exact(la):
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     t0 = time.perf_counter()
     rc = lib.la_debug_backward_fault(_p(tq), _p(tk), _p(tv), _p(tg), _p(dq), _p(dk), _p(dv),
-                                     B, H, N, 64, 64, 1, la.LA_BF16, _p(ws), nbytes, 1, LIMIT_NS,
+                                     B, H, N, 64, 64, 1, la.LA_BF16, _p(ws), nbytes, 0, LIMIT_NS,
                                      st)
     assert rc == la.LA_OK
     torch.cuda.synchronize()

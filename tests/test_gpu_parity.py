@@ -478,3 +478,33 @@ def test_full_size_decode_sampled(la):
         fv = np.concatenate([_np(v[s, h]), _np(sv[:, s, h])])
         want = oracle.forward(fq, fk, fv, True)[w.N:]
         assert_close(_np(outs[:, s, h]), want, w.dtype, f"decode[{s},{h}]")
+
+
+# ------------------------------------------- backward reusing the forward's states
+
+@pytest.mark.parametrize("case", [(2, 3, 1000, 64, 64, inputs.BF16, True),
+                                  (2, 3, 1000, 64, 64, inputs.BF16, False),
+                                  (1, 2, 100, 64, 64, inputs.BF16, True),    # one chunk: no states kept
+                                  (1, 2, 300, 32, 48, inputs.F32, True)],    # CUDA-core path
+                         ids=["bf16-causal", "bf16-noncausal", "bf16-one-chunk", "f32"])
+def test_backward_from_forward_states(la, case):
+    """la_backward after la_forward on the same inputs, reading the forward's segment
+    states from its workspace: the gradients match the oracle, and the forward
+    workspace is left as it was."""
+    B, H, N, D, M, dt, causal = case
+    scale = 0.125 if dt == inputs.BF16 else 1.0
+    q, k, v = inputs.qkv(1500 + N, B, H, N, D, M, scale, dt)
+    g = inputs.upstream_grad(1500 + N, B, H, N, M, scale, dt)
+    tq, tk, tv, tg = (_t(x, dt) for x in (q, k, v, g))
+    dcode = la.LA_BF16 if dt == inputs.BF16 else la.LA_F32
+    fws = torch.empty((la.la_forward_workspace_bytes(B, H, N, D, M, causal, dcode),),
+                      dtype=torch.uint8, device=DEV)
+    out = la.la_forward(tq, tk, tv, causal=causal, workspace=fws)
+    keep = fws.clone()
+    dq, dk, dv = la.la_backward(tq, tk, tv, tg, causal=causal, fwd_workspace=fws)
+    torch.cuda.synchronize()
+    assert torch.equal(fws, keep)
+    assert_close(out.float().cpu().numpy(), oracle.forward(q, k, v, causal), dt, "out")
+    wq, wk, wv = oracle.backward(q, k, v, g, causal)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        assert_close(got.cpu().numpy(), want, dt, f"{name} from the forward's states")
