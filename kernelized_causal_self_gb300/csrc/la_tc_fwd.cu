@@ -28,6 +28,10 @@
 // segment states enter the tensor cores as bf16 hi + lo pairs.
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "la_tc_common.cuh"
 
 namespace la {
@@ -768,26 +772,46 @@ void deal(long long BH, long long n_chunks, long long s, long long G, long long&
 // forward's kernels run two CTAs per SM, the backward's one; a CTA's time is its chunk
 // count (the backward's chunks cost ~4x the forward's) plus a little per item (state
 // loads, read-outs), and every item adds its states to the scans' traffic.
-Geometry make_geometry(int BH, int N) {
-  Geometry g;
-  g.BH = BH;
-  g.N = N;
-  g.n_chunks = (N + kC - 1) / kC;
+int choose_segment(int BH, int n_chunks) {
   const long long sms = sm_count();
   double best = 1e300;
   int best_s = 1;
-  for (int s = 1; s <= g.n_chunks && s <= 64; ++s) {
+  for (int s = 1; s <= n_chunks && s <= 64; ++s) {
     long long fc, fi, bc, bi;
-    deal(BH, g.n_chunks, s, 2 * sms, fc, fi);
-    deal(BH, g.n_chunks, s, sms, bc, bi);
-    const long long items = (long long)BH * ((g.n_chunks + s - 1) / s);
+    deal(BH, n_chunks, s, 2 * sms, fc, fi);
+    deal(BH, n_chunks, s, sms, bc, bi);
+    const long long items = (long long)BH * ((n_chunks + s - 1) / s);
     const double cost = 3.9 * fc + 15.0 * bc + 0.2 * fi + 0.5 * bi + 0.02 * items;
     if (cost <= best) {  // ties go to the longer segment
       best = cost;
       best_s = s;
     }
   }
-  g.seg_chunks = best_s;
+  return best_s;
+}
+
+Geometry make_geometry(int BH, int N) {
+  Geometry g;
+  g.BH = BH;
+  g.N = N;
+  g.n_chunks = (N + kC - 1) / kC;
+  // the choice is a pure function of (BH, n_chunks) and the SM count; it is
+  // remembered so that a call (and its workspace query) pays for the search once
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> memo;
+  int s = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find({BH, g.n_chunks});
+    if (it != memo.end()) s = it->second;
+  }
+  if (s == 0) {
+    s = choose_segment(BH, g.n_chunks);
+    std::lock_guard<std::mutex> lock(mu);
+    if (memo.size() > 4096) memo.clear();
+    memo[{BH, g.n_chunks}] = s;
+  }
+  g.seg_chunks = s;
   g.n_seg = (g.n_chunks + g.seg_chunks - 1) / g.seg_chunks;
   return g;
 }
