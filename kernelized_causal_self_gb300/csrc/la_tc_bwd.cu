@@ -1071,7 +1071,7 @@ cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const voi
   const float* sprefix = fwd_prefix;
   cudaError_t e = cudaSuccess;
   if (sprefix == nullptr) {
-    e = launch_segment_states(&tk, &tv, g, w.spartial, w.hdr, false, st);
+    e = launch_segment_states(&tk, &tv, g, w.spartial, w.hdr, st);
     if (e != cudaSuccess) return e;
     e = launch_scan(w.spartial, w.sprefix, g, causal ? kScanPrefix : kScanTotal,
                     pre != nullptr ? *pre : StateIO{}, w.hdr, st);

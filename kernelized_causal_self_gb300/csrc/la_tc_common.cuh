@@ -369,8 +369,7 @@ enum ScanMode { kScanPrefix = 0, kScanTotal = 1, kScanSuffix = 2 };
 
 // Segment increments dS^T = V^T phi(K), dZ = sum phi(K) into partial[item].
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, bool precise,
-                                  cudaStream_t st);
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st);
 // Prefix / total / suffix of the per-segment states (see ScanMode).
 // With io.S set, the prefix / total also starts from io's initial state (when
 // io.read_init) and the full sum is written to io's entries (prefill, extend).

@@ -24,8 +24,7 @@
 //
 // phi is applied in shared memory right after each TMA tile lands (bf16 in,
 // float32 math, bf16 out). The carried state is float32; the read-out takes it
-// rounded to bf16 (each element independently), and the backward's precise
-// segment states enter the tensor cores as bf16 hi + lo pairs.
+// rounded to bf16 (each element independently).
 #include <cuda_bf16.h>
 
 #include <map>
@@ -41,37 +40,27 @@ namespace tcx {
 
 constexpr int kStateWorkers = 256;  // two threads per tile row (column halves)
 constexpr int kStateThreads = kStateWorkers + 32;  // + one control warp; 2 CTAs per SM
-// Eight worker warps apply phi to the K tiles as they land; one control thread
+// Eight worker warps apply psi to the K tiles as they land; one control thread
 // issues the loads and the MMAs, each as soon as what it needs is done (a
 // stage is refilled once the MMAs that read it are done). A segment's sums land
 // in one of two TMEM accumulators and are read out while the next one fills.
-template <bool PRECISE>
-constexpr int state_stages() { return PRECISE ? 2 : 3; }
-template <bool PRECISE>
-constexpr int state_stage_bytes() { return (PRECISE ? 3 : 2) * kTile; }  // K, V (, phi(K) lo)
-template <bool PRECISE>
-constexpr int state_smem() {
-  return 1024 + state_stages<PRECISE>() * state_stage_bytes<PRECISE>() + 2048 + 256 + 256;
-}
+constexpr int kStateStages = 3;
+constexpr int kStateStageBytes = 2 * kTile;  // K, V
+constexpr int kStateSmem = 1024 + kStateStages * kStateStageBytes + 2048 + 256;
 
-// PRECISE: phi(K) enters the MMA as a bf16 hi + lo pair and dZ sums the
-// float32 phi values (used by the backward, whose dq needs phi(K) beyond bf16).
-template <bool PRECISE>
 __global__ void __launch_bounds__(kStateThreads, 2)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
-  constexpr int S = state_stages<PRECISE>(), SB = state_stage_bytes<PRECISE>();
+  constexpr int S = kStateStages, SB = kStateStageBytes;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = sm;                        // [stage][K tile | V tile (| phi(K) lo)]
-  uint8_t* ones = stages + S * SB;             // 16 x 64 bf16 ones (the stacked block of dZ)
-  float* zx = reinterpret_cast<float*>(ones + 2048);  // 64 floats: dZ lo parts (PRECISE)
-  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 2048 + 256);  // S: tiles landed
+  uint8_t* stages = sm;                        // [stage][K tile | V tile]
+  uint8_t* ones = stages + S * SB;             // 16 x 64 bf16 ones (the stacked blocks)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 2048);  // S: tiles landed
   uint64_t* empty = full + S;                  // S: the chunk's MMAs are done with the stage
-  uint64_t* phid = empty + S;                  // S: every worker's phi of the stage is in
+  uint64_t* phid = empty + S;                  // S: every worker's psi of the stage is in
   uint64_t* segbar = phid + S;                 // 2: a segment's last MMAs are done
-  uint64_t* xbar = segbar + 2;                 // readout exchange (PRECISE), 256 arrivals
-  uint64_t* drain = xbar + 1;                  // every MMA of the CTA is done
+  uint64_t* drain = segbar + 2;                // every MMA of the CTA is done
   volatile int* abort = reinterpret_cast<volatile int*>(drain + 1);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
 
@@ -86,7 +75,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     mbar_init(&segbar[0], 1);
     mbar_init(&segbar[1], 1);
-    mbar_init(xbar, kStateWorkers);
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -126,32 +114,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           const bool first = cm.first();
           const bool last = cm.last();
           const uint32_t acc = tbase + 128 * (nseg & 1);
-          const uint32_t ka = smem_u32(stages + s * SB), va = ka + kTile, kl = ka + 2 * kTile;
-          // The ones block of an operand is 16 token rows: every K step of 16
-          // tokens reads the same block, its descriptor's leading byte offset
-          // measured from that step's start (oa - (va + 2048 k)).
-          if (PRECISE) {
-            // [phi(K)^T hi; phi(K)^T lo] (M = 128 MN-major, the two 64-row halves
-            // kl - ka bytes apart) times [V | 1] (N = 80 MN-major, columns 64.. from
-            // the ones block): dS with rows d in columns [0, 64) and dZ in column 64,
-            // hi parts in TMEM lanes 0-63 and lo parts in lanes 64-127
-            const uint32_t idS = idesc_bf16(128, 80, true, true);
+          const uint32_t ka = smem_u32(stages + s * SB), va = ka + kTile;
+          // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
+          // [psi(K) | 1] (N = 80 MN-major, columns 64.. from the ones block):
+          // lanes 0-63 get (V^T psi(K))[m][d] in columns [0, 64) and the column
+          // sum of V[:, m] in column 64; lanes 64-127 get sum_t psi(K)[t][d]. The
+          // ones block of an operand is 16 token rows: every K step of 16 tokens
+          // reads the same block, its descriptor's leading byte offset measured
+          // from that step's start (oa - (va + 2048 k)).
+          const uint32_t idS = idesc_bf16(128, 80, true, true);
 #pragma unroll
-            for (int k = 0; k < kC / 16; ++k)
-              mma_ss(acc, sdesc(ka + k * 2048, kl - ka, 1024),
-                     sdesc(va + k * 2048, oa - (va + k * 2048), 1024), idS, (first && k == 0) ? 0u : 1u);
-          } else {
-            // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
-            // [psi(K) | 1] (N = 80 MN-major, columns 64.. from the ones block):
-            // lanes 0-63 get (V^T psi(K))[m][d] in columns [0, 64) and the column
-            // sum of V[:, m] in column 64; lanes 64-127 get sum_t psi(K)[t][d]
-            const uint32_t idS = idesc_bf16(128, 80, true, true);
-#pragma unroll
-            for (int k = 0; k < kC / 16; ++k)
-              mma_ss(acc, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
-                     sdesc(ka + k * 2048, oa - (ka + k * 2048), 1024), idS,
-                     (first && k == 0) ? 0u : 1u);
-          }
+          for (int k = 0; k < kC / 16; ++k)
+            mma_ss(acc, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                   sdesc(ka + k * 2048, oa - (ka + k * 2048), 1024), idS,
+                   (first && k == 0) ? 0u : 1u);
           mma_commit(&empty[s]);
           if (last) mma_commit(&segbar[nseg++ & 1]);
           cm.advance(g);
@@ -190,70 +166,32 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------- workers
-    uint32_t xphase = 0;
-    // a segment's sums -> partial[item]; xbuf: a free 16 KB tile (PRECISE)
-    auto readout = [&](int item, int p, uint8_t* xbuf) -> bool {
+    // a segment's sums -> partial[item]: S^T [m][d], then Z [d]
+    auto readout = [&](int item, int p) {
       float* dst = partial + (size_t)item * kStateFloats;
       const uint32_t acc = lane_base(tbase) + 128 * p;
       uint32_t r[32];
       tmem_ld32(acc + h * 32, r);
-      if (PRECISE) {
-        // lane r holds row d = r % 64 of the hi (r < 64) or the lo (r >= 64)
-        // part: dS in columns [0, 64), dZ in column 64. The lo halves go through
-        // xbuf and zx; the hi-half threads add them and write S^T [m][d], Z.
-        uint32_t r16[16];
-        tmem_ld16(acc + 64, r16);
-        float4* xs = reinterpret_cast<float4*>(xbuf);  // [64][16] float4, XOR-swizzled rows
-        const int d = 32 * (q4 & 1) + lane;
-        if (q4 >= 2) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            xs[d * 16 + ((8 * h + j) ^ (d & 15))] =
-                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          if (h == 0) zx[d] = __uint_as_float(r16[0]);
-        }
-        mbar_arrive(xbar);  // the lo halves are in
-        if (!mbar_wait_warp(xbar, xphase, abort, hdr, 6)) return false;
-        xphase ^= 1;
+      // lanes 0..63: row m = lane of V^T psi(K) (columns d) plus the column sum of
+      // V[:, m] (column 64); lanes 64..127: sum_t psi(K)[t][d] (every lane alike),
+      // plus the segment's count of valid tokens. This thread writes columns
+      // [32h, 32h + 32) of its row.
+      if (q4 < 2 || (q4 == 2 && lane == 0)) {
+        float add;
         if (q4 < 2) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 lo = xs[d * 16 + ((8 * h + j) ^ (d & 15))];
-            const int m = 32 * h + 4 * j;
-            dst[(m + 0) * kDim + d] = __uint_as_float(r[4 * j]) + lo.x;
-            dst[(m + 1) * kDim + d] = __uint_as_float(r[4 * j + 1]) + lo.y;
-            dst[(m + 2) * kDim + d] = __uint_as_float(r[4 * j + 2]) + lo.z;
-            dst[(m + 3) * kDim + d] = __uint_as_float(r[4 * j + 3]) + lo.w;
-          }
-          if (h == 0) dst[kDim * kDim + d] = __uint_as_float(r16[0]) + zx[d];
+          uint32_t r16[16];
+          tmem_ld16(acc + 64, r16);
+          add = __uint_as_float(r16[0]);
+        } else {
+          const int c0 = g.chunk_begin(item), c1 = g.chunk_end(item);
+          add = (float)max(0, min(g.len(g.bh_of(item)) - c0 * kC, (c1 - c0) * kC));
         }
-        mbar_arrive(xbar);  // the exchange buffer is read: phi may overwrite it
-        if (!mbar_wait_warp(xbar, xphase, abort, hdr, 7)) return false;
-        xphase ^= 1;
-      } else {
-        // lanes 0..63: row m = lane of V^T psi(K) (columns d) plus the column sum
-        // of V[:, m] (column 64); lanes 64..127: sum_t psi(K)[t][d] (every lane
-        // alike), plus the segment's count of valid tokens. This thread writes
-        // columns [32h, 32h + 32) of its row.
-        if (q4 < 2 || (q4 == 2 && lane == 0)) {
-          float add;
-          if (q4 < 2) {
-            uint32_t r16[16];
-            tmem_ld16(acc + 64, r16);
-            add = __uint_as_float(r16[0]);
-          } else {
-            const int c0 = g.chunk_begin(item), c1 = g.chunk_end(item);
-            add = (float)max(0, min(g.len(g.bh_of(item)) - c0 * kC, (c1 - c0) * kC));
-          }
-          float4* d4 = reinterpret_cast<float4*>(dst + (q4 < 2 ? (32 * q4 + lane) * kDim : kDim * kDim) + h * 32);
+        float4* d4 = reinterpret_cast<float4*>(dst + (q4 < 2 ? (32 * q4 + lane) * kDim : kDim * kDim) + h * 32);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]) + add, __uint_as_float(r[4 * j + 1]) + add,
-                                __uint_as_float(r[4 * j + 2]) + add, __uint_as_float(r[4 * j + 3]) + add);
-        }
+        for (int j = 0; j < 8; ++j)
+          d4[j] = make_float4(__uint_as_float(r[4 * j]) + add, __uint_as_float(r[4 * j + 1]) + add,
+                              __uint_as_float(r[4 * j + 2]) + add, __uint_as_float(r[4 * j + 3]) + add);
       }
-      return true;
     };
 
     Cursor cc;
@@ -262,7 +200,6 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     int nseg = 0;                    // segments whose last chunk has passed
     int pend_item = -1, pend_p = 0;  // segment awaiting its readout
     uint32_t pend_phase = 0;
-    float zacc[32];
     bool ok = true;
     while (cc.valid(g)) {
       const int item = cc.item;
@@ -276,26 +213,19 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ok = false;
         break;
       }
-      if (PRECISE)
-        phi_half_split(kt, kt + 2 * kTile, trow, h, nvalid, zacc);
-      else
-        psi_half(kt, trow, h, nvalid);
+      psi_half(kt, trow, h, nvalid);
       if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
       fence_proxy_async_smem();
       mbar_arrive(&phid[s]);
-      // the segment that ended with the previous chunk: its accumulator is not
-      // the one this chunk's MMAs use, and (PRECISE) the previous stage's phi(K)
-      // lo tile, which its MMAs were the last to read, carries the exchange
+      // the segment that ended with the previous chunk: its accumulator is not the
+      // one this chunk's MMAs use
       if (pend_item >= 0) {
         if (!mbar_wait_warp(&segbar[pend_p], pend_phase, abort, hdr, 2)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        if (!readout(pend_item, pend_p, stages + ((consumed + S - 1) % S) * SB + 2 * kTile)) {
-          ok = false;
-          break;
-        }
+        readout(pend_item, pend_p);
         fence_before_sync();
         pend_item = -1;
       }
@@ -310,7 +240,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     if (ok && pend_item >= 0 && mbar_wait_warp(&segbar[pend_p], pend_phase, abort, hdr, 2)) {
       fence_after_sync();
-      readout(pend_item, pend_p, stages + ((consumed + S - 1) % S) * SB + 2 * kTile);
+      readout(pend_item, pend_p);
       fence_before_sync();
     }
   }
@@ -817,19 +747,14 @@ Geometry make_geometry(int BH, int N) {
 }
 
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, bool precise,
-                                  cudaStream_t st) {
-  auto run = [&](auto kern, int smem) {
-    cudaError_t e = configure(kern, smem);
-    if (e != cudaSuccess) return e;
-    const int ctas = min(g.n_items(), resident_ctas(kern, smem, kStateThreads) * sm_count());
-    cudaError_t err = launch_pdl(kern, dim3(ctas), dim3(kStateThreads), smem, st, *tk, *tv, g,
-                                 partial, hdr);
-    count_launches(1);
-    return err != cudaSuccess ? err : cudaGetLastError();
-  };
-  return precise ? run(tc_state_kernel<true>, state_smem<true>())
-                 : run(tc_state_kernel<false>, state_smem<false>());
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st) {
+  cudaError_t e = configure(tc_state_kernel, kStateSmem);
+  if (e != cudaSuccess) return e;
+  const int ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem, kStateThreads) * sm_count());
+  e = launch_pdl(tc_state_kernel, dim3(ctas), dim3(kStateThreads), kStateSmem, st, *tk, *tv, g,
+                 partial, hdr);
+  count_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode,
@@ -870,7 +795,7 @@ cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int B
   if (!make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
       !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
+  cudaError_t e = launch_segment_states(&tk, &tv, g, partial, hdr, st);
   if (e != cudaSuccess) return e;
   return launch_scan(partial, total, g, kScanTotal, io, hdr, st);
 }
@@ -905,7 +830,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
   cudaError_t e = cudaSuccess;
   if (!direct) {
-    e = launch_segment_states(&tk, &tv, g, partial, hdr, false, st);
+    e = launch_segment_states(&tk, &tv, g, partial, hdr, st);
     if (e != cudaSuccess) return e;
     e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
     if (e != cudaSuccess) return e;
