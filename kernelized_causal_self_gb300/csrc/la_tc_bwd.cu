@@ -192,91 +192,22 @@ __device__ __forceinline__ void sync_tc() {
 
 // --------------------------------------------------- forward direction: dq
 //
-// phi = 1 + psi with psi = phi - 1 (|psi| ~ 0.1 for these inputs). Each sum is
-// split into a part that is the same for every feature d, kept in float32 on the
-// CUDA cores, and a small part that goes through the tensor cores in bf16 (one
-// bf16 part per operand suffices there: the operands are small). With
-// b_i = sum_d psi(q_i)_d, c_j = sum_d psi(k_j)_d, W = G V^T (exact in float32),
-// S_prev = 1 s^T + Psi with s the mean of S_prev over d, Z_prev = z + Zpsi likewise
-// (so sum_d Psi[d][m] = 0 and sum_d Zpsi[d] = 0):
-//   P_ij    = phi(q_i) . phi(k_j) = D + b_i + c_j + psi(q_i) . psi(k_j)
-//   den_i   = rowsum(P_L)_i + (D + b_i) z + (psi(Q) Zpsi)_i
-//   G.num_i = sum_j P_L,ij W_ij + (D + b_i) (G_i . s) + G_i . (psi(Q) Psi)_i
-//   gd_i = -(G.num_i) / den_i^2,  gN_i = G_i / den_i,  T_ij = W_ij / den_i + gd_i (j <= i)
-//   dphiQ_i = [rowsum(T_L)_i + s . gN_i + gd_i z] + (T_L psi(K))_i + (gN_i Psi^T) + gd_i Zpsi
-// and the segment's reverse sums R = sum_i phi(q_i) gN_i^T = 1 Gsum^T + psi(Q)^T gN,
-// r = gdsum + sum_i gd_i psi(q_i) (Gsum, gdsum and the last sum in float32).
-
-constexpr int kQArr = 20480;  // float arrays of the dq kernel
-constexpr int kBwdQSmem = 1024 + kBwdStages * 4 * kTile + 2 * kDim * 128 + kTile + 2048 + kQArr + 256;
-
-struct QSmem {
-  uint8_t* stages;
-  uint8_t* snap;   // Psi bf16 [d][m] (64 rows), then the Zpsi block (row d, column 0)
-  uint8_t* gn;     // gN bf16 [i][m]
-  uint8_t* ones;   // 16 rows of bf16 ones
-  float* arr;
-  uint64_t* full;
-  uint64_t* mma_bar;
-  uint64_t* sbar;  // [0]: the state increment; [1]: the reverse sums
-  uint64_t* drain;
-  uint32_t* tslot;
-  __device__ explicit QSmem(uint8_t* raw) {
-    uint8_t* sm =
-        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-    stages = sm;
-    snap = sm + kBwdStages * 4 * kTile;
-    gn = snap + 2 * kDim * 128;
-    ones = gn + kTile;
-    arr = reinterpret_cast<float*>(ones + 2048);
-    full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(arr) + kQArr);
-    mma_bar = full + kBwdStages;
-    sbar = mma_bar + 1;
-    drain = sbar + 2;
-    tslot = reinterpret_cast<uint32_t*>(drain + 1);
-  }
-  __device__ uint8_t* tile(int stage, int which) { return stages + (stage * 4 + which) * kTile; }
-};
-
-// psi on columns [16 qc, 16 qc + 16) of a tile row, rounded to bf16 in place (rows >=
-// nvalid become 0); returns the sum of the rounded values and leaves them in z.
-__device__ __forceinline__ float psi_quarter(uint8_t* tile, int row, int qc, int nvalid, float (&z)[16]) {
-  const bool valid = row < nvalid;
-  float sum = 0.f;
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint4* p = reinterpret_cast<uint4*>(tile + sw128(row, (2 * qc + c) * 16));
-    const uint4 w = *p;
-    uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      u[q] = valid ? psi2_bf16(u[q]) : 0u;
-      z[8 * c + 2 * q] = bf16_lo_f(u[q]);
-      z[8 * c + 2 * q + 1] = bf16_hi_f(u[q]);
-      sum += z[8 * c + 2 * q] + z[8 * c + 2 * q + 1];
-    }
-    *p = make_uint4(u[0], u[1], u[2], u[3]);
-  }
-  return sum;
-}
-
-// x[16] -> bf16 at row `row`, columns [16 qc, 16 qc + 16) of a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_quarter(uint8_t* buf, int row, int qc, const float* x) {
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = pack_bf16(x[8 * c + 2 * q], x[8 * c + 2 * q + 1]);
-    *reinterpret_cast<uint4*>(buf + sw128(row, (2 * qc + c) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
+// With W = G V^T (bf16 x bf16 products, exact in the float32 accumulator):
+//   den_i   = rowsum(P_L)_i + phi(Q_i) . Z_prev
+//   G.num_i = sum_j P_L,ij W_ij + G_i . (phi(Q_i) S_prev)
+//   gd_i    = -(G.num_i) / den_i^2,   gN_i = G_i / den_i
+//   T_ij    = W_ij / den_i + gd_i      (= (v_j - out_i) . gN_i, in float32)
+// so one epilogue after the first MMA group yields T_L, gN and gd, and the
+// second group accumulates dphiQ = T_L phi(K) + gN S_prev^T and the segment
+// sum of phi(Q)^T gN.
 
 // TMEM columns
-constexpr uint32_t kFP = 0;     // 128: psi(Q) psi(K)^T; after the first epilogue, dphiQ's MMA part (64)
-constexpr uint32_t kFW = 128;   // 128: W = G V^T; then T_L as bf16 in [128, 192)
-constexpr uint32_t kFO = 256;   // 80: psi(Q) [Psi | Zpsi]
-constexpr uint32_t kFS = 336;   // 80: [psi(K)^T; 1^T] [V | 1]: lanes 0-63 dPsi, dZpsi; 64-127 column sums of V
-constexpr uint32_t kFR = 416;   // 64: segment sum of psi(Q)^T gN (lanes 0-63)
+constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T; after the first epilogue, dphiQ (kFQ)
+constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
+constexpr uint32_t kFO = 256;   // 128: phi(Q) S_prev as phi(Q) S_hi (0..63) and phi(Q) S_lo (64..127)
+constexpr uint32_t kFS = 384;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
+constexpr uint32_t kFQ = 0;     // 128: dphiQ as two 64-column parts (P's columns, spent by then)
+constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kBTQ, 1)
@@ -286,27 +217,16 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float* __restrict__ sprefix, float* __restrict__ rpartial,
                 float* __restrict__ den_out, float* __restrict__ gd_out, WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
-  QSmem sm(smraw);
-  float* bpart = sm.arr;              // [4][128]: quarter sums of psi(q_i)
-  float* cpart = bpart + 512;         // [4][128]: quarter sums of psi(k_j)
-  float* btot = cpart + 512;          // 128: b_i
-  float* ctot = btot + 128;           // 128: c_j
-  float* rsum = ctot + 128;           // [4][128]: quarter parts of den
-  float* gnum = rsum + 512;           // [4][128]: quarter parts of G . num
-  float* gvs = gnum + 512;            // [4][128]: quarter parts of G . s
-  float* tsum = gvs + 512;            // [4][128]: quarter parts of rowsum(T_L)
-  float* smean = tsum + 512;          // 64: s, the mean of S_prev over d
-  float* colp = smean + 64;           // [2][64]: the two warps' column sums of S over d
-  float* zpsi = colp + 128;           // 64: Zpsi (float32)
-  float* dz = zpsi + 64;              // [4][64]: warp column sums of gN
-  float* rz = dz + 256;               // [4][64]: warp column sums of gd psi(q)
-  float* dvs = rz + 256;              // 64: this chunk's column sums of V
-  float* gsm = dvs + 64;              // 64: the segment's Gsum (read-out)
-  float* scal = gsm + 64;             // [0..1]: warp sums of Z; [2]: z; [4..7]: warp sums of gd; [8]: gdsum
+  BwdSmem sm(smraw);
+  float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
+  float* dz = sm.arr + 64;       // [4][64]: warp column sums
+  float* rsum = sm.arr + 320;    // [4][128]: quarter-row parts of den
+  float* gnum = sm.arr + 832;    // [4][128]: quarter-row parts of G . num
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int lq = warp & 3, qc = warp >> 2;
   const int row = lq * 32 + lane;  // query row of this thread
-  // S carry: row d = row (threads of TMEM lanes 0-63), columns m in [16 qc, 16 qc + 16)
+  // S carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
+  const int drow = 32 * (lq & 1) + lane;
   const bool dthread = lq < 2;
   // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
   // stores) belong to warp 1's first thread, so that the two issue in parallel
@@ -320,11 +240,6 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(sm.drain, 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < 2048 / 16; e += blockDim.x)
-    reinterpret_cast<uint4*>(sm.ones)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  for (int e = tid; e < kDim * 128 / 16; e += blockDim.x)  // the Zpsi block: only column 0 is ever set
-    reinterpret_cast<uint4*>(sm.snap + kDim * 128)[e] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(sm.tslot, 512);
     tmem_relinquish();
@@ -363,14 +278,12 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tma_thread)
     for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
 
-  float srun[16];              // S row d = row, columns [16 qc, 16 qc + 16) (dthread)
-  float zrun = 0.f;            // Z[d], d = tid < 64
-  float gsum = 0.f, rr = 0.f;  // the segment's Gsum[m], sum gd psi(q)_d for m, d = tid < 64
-  float gdsum = 0.f;           // the segment's sum of gd (tid 0)
+  float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
+  float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
   long long consumed = 0;
   uint32_t ph = 0, sph0 = 0, sph1 = 0;
-  // the previous chunk's reverse-sum MMAs (sbar[1]) are still to be waited for: they
-  // read psi(Q) and gN, which the next chunk rewrites
+  // the previous chunk's segment-sum MMAs (sbar[1]) are still to be waited for:
+  // they read phi(Q) lo and gN, which the next chunk rewrites
   bool r_pending = false;
   float z[16];
 
@@ -381,32 +294,17 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int nvalid = min(kC, g.N - t0);
     if (first) {
       const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (dthread) {  // the prefix is S^T [m][d]: column d = row, rows m of this quarter
+      if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
 #pragma unroll
-        for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + row];
+        for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + drow];
       }
       if (tid < kDim) {
         zrun = src[kDim * kDim + tid];
-        gsum = 0.f;
         rr = 0.f;
       }
-      gdsum = 0.f;
     }
-    const bool snapshot = CAUSAL || first;
-    if (snapshot) {  // the two warps' column sums of S over d, and of Z
-      if (dthread) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = srun[j];
-        const float cs = warp_column_sums16(z);
-        if (lane < 16) colp[lq * 64 + 16 * qc + lane] = cs;
-      }
-      if (tid < kDim) {
-        float zs = zrun;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
-        if (lane == 0) scal[warp] = zs;
-      }
-    }
+    if ((CAUSAL || first) && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
+    if (tid < kDim) zsnap[tid] = zrun;
     const int s = consumed % kBwdStages;
     uint8_t* qt = sm.tile(s, kQ);
     uint8_t* kt = sm.tile(s, kK);
@@ -420,95 +318,79 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       r_pending = false;
       fence_after_sync();
     }
-    float zbar = scal[2];  // z of the previous chunk until refreshed below (non-causal: kept)
-    if (snapshot) {  // Psi = S - 1 s^T and Zpsi = Z - z (float32 means, bf16 Psi for the MMAs)
-      zbar = (scal[0] + scal[1]) * (1.f / kDim);
-      if (dthread) {
-        float x[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float m = (colp[16 * qc + j] + colp[64 + 16 * qc + j]) * (1.f / kDim);
-          x[j] = srun[j] - m;
-          if (lq == 0 && lane == j) smean[16 * qc + j] = m;
-        }
-        store_quarter(sm.snap, row, qc, x);
-      }
-      if (tid < kDim) {
-        const float zp = zrun - zbar;
-        zpsi[tid] = zp;
-        *reinterpret_cast<__nv_bfloat16*>(sm.snap + kDim * 128 + sw128(tid, 0)) = __float2bfloat16_rn(zp);
-      }
+    phi_quarter_split(qt, sm.qlo, row, qc, kC, z);
+    if (CAUSAL) {
+      phi_quarter_split(kt, sm.klo, row, qc, nvalid, z);
+      const float cs = warp_column_sums16(z);
+      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
     }
-    // psi(Q), psi(K) in place (bf16), with their per-row sums
-    bpart[qc * 128 + row] = psi_quarter(qt, row, qc, kC, z);
-    if (CAUSAL) cpart[qc * 128 + row] = psi_quarter(kt, row, qc, nvalid, z);
     fence_proxy_async_smem();
     sync_tc();
-    if (tid == 0) scal[2] = zbar;
     if (tma_thread) {
       // the next chunk's tiles go into the previous chunk's stage, whose dq staging
-      // TMA stores have had this chunk's psi to finish reading it
+      // TMA stores have had this chunk's phi to finish reading it
       bulk_wait_read<0>();
       if (cp.valid(g)) issue(cp);
     }
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt), ga = smem_u32(gt);
-      const uint32_t ha = smem_u32(sm.snap), oa = smem_u32(sm.ones);
+      const uint32_t kl = smem_u32(sm.klo);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
       if (CAUSAL) {
         const uint32_t id128 = idesc_bf16(128, 128, false, false);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // psi(Q) psi(K)^T
+        for (int k = 0; k < 4; ++k)  // P = phi(Q) (phi(K)_hi + phi(K)_lo)^T
           mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), id128, k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(kl + k * 32, 16, 1024), id128, 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // W = G V^T
           mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
       }
-      // psi(Q) [Psi | Zpsi]: B = the snapshot, rows d (= K), m contiguous (MN-major);
-      // the Zpsi block (column 0 of its rows) is the second N block, kDim * 128 bytes on
-      const uint32_t idO = idesc_bf16(128, 80, false, true);
+      // phi(Q) [S_hi | S_lo]: B = the snapshot, rows d (= K), m contiguous
+      // (MN-major), its hi and lo tiles the two 64-column N blocks (la - ha apart)
+      const uint32_t idO = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, kDim * 128, 1024), idO, k);
+        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idO, k);
       mma_commit(sm.mma_bar);
       if (CAUSAL) {  // state increment, complete when the second group's barrier is:
-        // [psi(K)^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
-        // [V | 1] (N = 80 MN-major, columns 64.. from the ones block)
-        const uint32_t idS = idesc_bf16(128, 80, true, true);
+        // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
+        // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
+        const uint32_t idS = idesc_bf16(128, 64, true, true);
+        const uint32_t lbo = kl - ka;
 #pragma unroll
         for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(ka + k * 2048, oa - (ka + k * 2048), 1024),
-                 sdesc(va + k * 2048, oa - (va + k * 2048), 1024), idS, k);
+          mma_ss(tbase + kFS, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS, k);
         mma_commit(&sm.sbar[0]);
       }
-    }
-    if (qc == 0) {  // the rows' sums of psi, read after the next barrier
-      btot[row] = (bpart[row] + bpart[128 + row]) + (bpart[256 + row] + bpart[384 + row]);
-      if (CAUSAL) ctot[row] = (cpart[row] + cpart[128 + row]) + (cpart[256 + row] + cpart[384 + row]);
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 22, wlim)) break;
     ph ^= 1;
     fence_after_sync();
 
-    // ---- epilogue: den, G.num (and G.s), in float32
-    const float dbi = (float)kDim + btot[row];
+    // ---- epilogue: den, G.num, then gd, gN and T_L
     float wv[32];  // masked W of this thread's slice qc (causal)
-    float gv[16];  // G_i over this thread's columns, then gN_i
     {
-      float dpart = 0.f, npart = 0.f, gpart = 0.f;
+      float dpart = 0.f, npart = 0.f;
       if (CAUSAL) {
         if (qc <= lq) {  // warp-uniform
           uint32_t rp[32], rw[32];
           tmem_ld32x2(tl + kFP + 32 * qc, rp, tl + kFW + 32 * qc, rw);
-          const float4* c4 = reinterpret_cast<const float4*>(ctot + 32 * qc);
+          if (qc < lq) {  // below the diagonal block: nothing is masked
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const float4 cj = c4[c8];
-            const float cjs[4] = {cj.x, cj.y, cj.z, cj.w};
+            for (int c = 0; c < 32; ++c) {
+              const float p = __uint_as_float(rp[c]);
+              wv[c] = __uint_as_float(rw[c]);
+              dpart += p;
+              npart += p * wv[c];
+            }
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c8 + e;
-              const bool keep = qc < lq || 32 * qc + c <= row;
-              const float p = keep ? __uint_as_float(rp[c]) + dbi + cjs[e] : 0.f;
+            for (int c = 0; c < 32; ++c) {
+              const bool keep = 32 * qc + c <= row;
+              const float p = keep ? __uint_as_float(rp[c]) : 0.f;
               wv[c] = keep ? __uint_as_float(rw[c]) : 0.f;
               dpart += p;
               npart += p * wv[c];
@@ -519,143 +401,159 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int c = 0; c < 32; ++c) wv[c] = 0.f;
         }
       }
-      {  // the state part over this quarter: G_i . ((D + b_i) s + (psi(Q) Psi)_i), G_i . s
-        uint32_t ro[16];
-        tmem_ld16(tl + kFO + 16 * qc, ro);
+      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this quarter. The Z dot
+         // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
+         // the rounding of phi(Q) cancels in num / den.
+        uint32_t ro[16], ro2[16];
+        tmem_ld16x2(tl + kFO + 16 * qc, ro, tl + kFO + 64 + 16 * qc, ro2);
+        float gv[16], qv[16];
         load_row16(gt, row, 2 * qc, gv);
+        load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const float sm_q = smean[16 * qc + q];
-          npart += gv[q] * fmaf(dbi, sm_q, __uint_as_float(ro[q]));
-          gpart += gv[q] * sm_q;
+          npart += gv[q] * (__uint_as_float(ro[q]) + __uint_as_float(ro2[q]));
+          dpart += qv[q] * zsnap[16 * qc + q];
         }
-      }
-      if (qc == 0) {  // phi(q_i) . Z_prev = (D + b_i) z + (psi(Q) Zpsi)_i
-        uint32_t r16[16];
-        tmem_ld16(tl + kFO + 64, r16);
-        dpart += fmaf(dbi, zbar, __uint_as_float(r16[0]));
       }
       rsum[qc * 128 + row] = dpart;
       gnum[qc * 128 + row] = npart;
-      gvs[qc * 128 + row] = gpart;
     }
-    sync_tc();  // partials visible; every read of P and W is done
+    if (CAUSAL && tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
+    sync_tc();  // partials visible; every read of W is done
     const float den = (rsum[row] + rsum[128 + row]) + (rsum[256 + row] + rsum[384 + row]);
     const float inv = 1.f / den;
     const float gd = -((gnum[row] + gnum[128 + row]) + (gnum[256 + row] + gnum[384 + row])) * inv * inv;
     {
+      float gn[16];
+      load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) gv[q] *= inv;  // gN
-      store_quarter(sm.gn, row, qc, gv);
+      for (int q = 0; q < 16; ++q) gn[q] *= inv;
+      store_split_quarter(sm.gn_hi, sm.gn_lo, row, qc, gn);
       if (qc == 0 && row < nvalid) {
         den_out[(size_t)bh * g.N + t0 + row] = den;
         gd_out[(size_t)bh * g.N + t0 + row] = gd;
       }
-      // this chunk's shares of Gsum = sum_i gN_i and of sum_i gd_i psi(q_i), and of sum_i gd_i
+      // this chunk's share of r = sum_i gd_i phi(Q_i) (float32 phi = hi + lo)
+      float qv[16], ql[16];
+      load_row16(qt, row, 2 * qc, qv);
+      load_row16(sm.qlo, row, 2 * qc, ql);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) z[q] = gv[q];
-      float cs = warp_column_sums16(z);
+      for (int q = 0; q < 16; ++q) z[q] = gd * (qv[q] + ql[q]);
+      const float cs = warp_column_sums16(z);
       if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
-      load_row16(qt, row, 2 * qc, z);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) z[q] *= gd;
-      cs = warp_column_sums16(z);
-      if (lane < 16) rz[lq * 64 + 16 * qc + lane] = cs;
-      if (qc == 0) {
-        float gs = gd;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-        if (lane == 0) scal[4 + lq] = gs;
-      }
     }
-    if (CAUSAL) {  // T_L = W / den + gd (j <= i) as bf16 over the spent W columns, and its row sum
-      uint32_t th[16];
-      float ts = 0.f;
-      if (qc <= lq) {  // warp-uniform: full or diagonal slice
+    if (CAUSAL) {  // T_L = W / den + gd (j <= i), bf16 hi + lo over the spent W columns
+      uint32_t th[16], tlo[16];
+      if (qc < lq) {  // warp-uniform: full slice, diagonal slice, or all zero
+#pragma unroll
+        for (int c = 0; c < 16; ++c) split_bf16(wv[2 * c] * inv + gd, wv[2 * c + 1] * inv + gd, th[c], tlo[c]);
+      } else if (qc == lq) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int j0 = 32 * qc + 2 * c;
-          const float a = (qc < lq || j0 <= row) ? fmaf(wv[2 * c], inv, gd) : 0.f;
-          const float b = (qc < lq || j0 + 1 <= row) ? fmaf(wv[2 * c + 1], inv, gd) : 0.f;
-          th[c] = pack_bf16(a, b);
-          ts += a + b;
+          split_bf16(j0 <= row ? wv[2 * c] * inv + gd : 0.f, j0 + 1 <= row ? wv[2 * c + 1] * inv + gd : 0.f,
+                     th[c], tlo[c]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) th[c] = 0u;
+        for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
       }
       tmem_st16(tl + kFW + 16 * qc, th);
-      tsum[qc * 128 + row] = ts;
+      tmem_st16(tl + kFW + 64 + 16 * qc, tlo);
     }
     fence_proxy_async_smem();
     sync_tc();
-    if (tid < kDim) {
-      gsum += (dz[tid] + dz[64 + tid]) + (dz[128 + tid] + dz[192 + tid]);
-      rr += (rz[tid] + rz[64 + tid]) + (rz[128 + tid] + rz[192 + tid]);
-    }
-    gdsum += (scal[4] + scal[5]) + (scal[6] + scal[7]);
+    if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
     if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt);
-      const uint32_t gna = smem_u32(sm.gn), ha = smem_u32(sm.snap), oa = smem_u32(sm.ones);
-      const uint32_t idQ = idesc_bf16(128, 64, false, true);
+      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), ql = smem_u32(sm.qlo);
+      const uint32_t kl = smem_u32(sm.klo);
+      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
+      // dphiQ = T_L phi(K) + gN S_prev^T with the hi*hi + hi*lo + lo*hi terms of
+      // each product; the hi*lo partners share their A operand, so they sit side by
+      // side in one N = 128 instruction, and dphiQ is the sum of the accumulator's
+      // two 64-column halves (columns [64, 128) carry only the hi*lo terms)
+      const uint32_t idQ2 = idesc_bf16(128, 128, false, true), idQ = idesc_bf16(128, 64, false, true);
       if (CAUSAL) {
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // T_L psi(K) (A = T_L from TMEM; B = psi(K) MN-major)
-          mma_ts(tbase + kFP, tbase + kFW + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, k);
+        for (int k = 0; k < kC / 16; ++k)  // T_hi [phi(K)_hi | phi(K)_lo] (N blocks kl - ka apart)
+          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(ka + k * 2048, kl - ka, 1024), idQ2, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)  // T_lo phi(K)_hi
+          mma_ts(tbase + kFQ, tbase + kFW + 64 + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, 1);
       }
-      // gN Psi^T: B = the snapshot, rows d (= N), m contiguous (K-major)
-      const uint32_t idQs = idesc_bf16(128, 64, false, false);
+      // B = the snapshot, rows d (= N), m contiguous (K-major): the S_lo rows follow
+      // the S_hi rows, so gN_hi [S_hi; S_lo]^T is one N = 128 product
+      const uint32_t idQs2 = idesc_bf16(128, 128, false, false), idQs = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFP, sdesc(gna + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs,
+        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs2,
                (CAUSAL || k > 0) ? 1u : 0u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs, 1);
       mma_commit(sm.mma_bar);
-      // segment sum of psi(Q)^T gN, awaited at the chunk's end: [psi(Q)^T; 1^T] (M = 128
-      // MN-major, rows 64.. from the ones block) times gN (N = 64 MN-major)
+      // segment sum of phi(Q)^T gN, awaited at the chunk's end: phi(Q)^T hi and
+      // lo stacked as one M = 128 MN-major operand (the two 64-row halves are
+      // the hi and lo tiles, ql - qa bytes apart), times gN hi, then gN lo; the
+      // hi-row and lo-row halves (TMEM lanes 0-63 / 64-127) are summed at the
+      // segment's end
       const uint32_t idR = idesc_bf16(128, 64, true, true);
+      const uint32_t lbo = ql - qa;
 #pragma unroll
       for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(qa + k * 2048, oa - (qa + k * 2048), 1024),
-               sdesc(gna + k * 2048, 1024, 1024), idR, (first && k == 0) ? 0u : 1u);
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
+               (first && k == 0) ? 0u : 1u);
+#pragma unroll
+      for (int k = 0; k < kC / 16; ++k)
+        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
+               1);
       mma_commit(&sm.sbar[1]);
     }
-    if (CAUSAL) {  // S += dS, Z += dZ while the second group runs
+    if (CAUSAL) {  // S += dS while the second group runs: the lo-part rows pass
+                   // through the chunk's V tile (no MMA reads it any more)
       if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27, wlim)) break;
       sph0 ^= 1;
       fence_after_sync();
       uint32_t r[16];
-      tmem_ld16(tl + kFS + 16 * qc, r);  // lanes 0-63: dPsi rows d; lanes 64-127: column sums of V
-      uint32_t r16[16];
-      if (qc == 0) tmem_ld16(tl + kFS + 64, r16);  // lanes 0-63: dZpsi[d]
-      if (lq == 2 && lane == 0) {
+      tmem_ld16(tl + kFS + 16 * qc, r);
+      float4* xs = reinterpret_cast<float4*>(vt);  // [64][16] float4, XOR-swizzled rows
+      if (!dthread) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dvs[16 * qc + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 4; ++j)
+          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
       __syncthreads();
       if (dthread) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) srun[j] += __uint_as_float(r[j]) + dvs[16 * qc + j];
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
+          srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
+          srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
+          srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
+          srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+        }
       }
-      if (tid < kDim) zrun += __uint_as_float(r16[0]) + (float)nvalid;
+      fence_proxy_async_smem();  // the V tile is a TMA destination again
     }
     if (!wait_uniform(sm.mma_bar, ph, hdr, 24, wlim)) break;
     ph ^= 1;
     fence_after_sync();
 
-    // dq = (dphiQ + gd Zpsi) * phi'(q), phi'(q) = min(1 + psi(q), 1); this quarter's
+    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this quarter's
     // columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for TMA stores in
     // the chunk's spent K and G tiles (quarters 0, 1: K tile; 2, 3: G tile)
     {
-      const float tsr = CAUSAL ? (tsum[row] + tsum[128 + row]) + (tsum[256 + row] + tsum[384 + row]) : 0.f;
-      const float gsr = (gvs[row] + gvs[128 + row]) + (gvs[256 + row] + gvs[384 + row]);
-      const float ci = tsr + gsr * inv + gd * zbar;
-      uint32_t r[16];
-      tmem_ld16(tl + kFP + 16 * qc, r);
+      uint32_t r[16], r2[16];
+      tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
       float qv[16], o[16];
       load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        o[q] = (ci + __uint_as_float(r[q]) + gd * zpsi[16 * qc + q]) * fminf(1.f + qv[q], 1.f);
+        o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zsnap[16 * qc + q]) *
+               fminf(qv[q], 1.f);
       uint8_t* sq = qc < 2 ? kt : gt;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -669,28 +567,39 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_store_3d(&tm_dq, gt, 32, t0, bh);
       bulk_commit();
     }
-    r_pending = true;  // the segment sums of psi(Q)^T gN, issued after the second group
-    if (last) {  // segment partial: R [d][m] = Gsum[m] + (psi(Q)^T gN)[d][m], r[d]
+    r_pending = true;  // the segment sums of phi(Q)^T gN, issued after the second group
+    if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
       if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28, wlim)) break;
       sph1 ^= 1;
       r_pending = false;
       fence_after_sync();
-      if (tid < kDim) gsm[tid] = gsum;
-      __syncthreads();
+      // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
+      // part for lq >= 2; the lo parts pass through the spent gN hi buffer
       float* dst = rpartial + (size_t)item * kStateFloats;
       uint32_t r[16];
       tmem_ld16(tl + kFR + 16 * qc, r);
-      if (dthread) {
-        float4* d4 = reinterpret_cast<float4*>(dst + row * kDim + 16 * qc);
+      float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
+      const int d = drow;
+      if (lq >= 2) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          d4[j] = make_float4(__uint_as_float(r[4 * j]) + gsm[16 * qc + 4 * j],
-                              __uint_as_float(r[4 * j + 1]) + gsm[16 * qc + 4 * j + 1],
-                              __uint_as_float(r[4 * j + 2]) + gsm[16 * qc + 4 * j + 2],
-                              __uint_as_float(r[4 * j + 3]) + gsm[16 * qc + 4 * j + 3]);
+          xs[d * 16 + ((4 * qc + j) ^ (d & 15))] =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
-      if (tid < kDim) dst[kDim * kDim + tid] = rr + gdsum;
-      sync_tc();  // every read of gsm is done before a later segment rewrites it
+      __syncthreads();
+      if (lq < 2) {
+        float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 16 * qc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 lo = xs[d * 16 + ((4 * qc + j) ^ (d & 15))];
+          d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
+                              __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
+        }
+      }
+      if (tid < kDim) dst[kDim * kDim + tid] = rr;
+      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
+      sync_tc();  // every read of the exchange is done before gN hi is rewritten
     }
     ++consumed;
     cc.advance(g);
@@ -1170,10 +1079,10 @@ cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const voi
     sprefix = w.sprefix;
   }
   auto run_q = [&](auto kern) {
-    cudaError_t err = configure(kern, kBwdQSmem);
+    cudaError_t err = configure(kern, kBwdSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdQSmem, kBTQ) * sm_count());
-    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdQSmem, st, tq, tk, tv, tg, tdq, gq,
+    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sm_count());
+    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, gq,
                      sprefix, w.rpartial, w.den, w.gd, w.hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
