@@ -9,7 +9,8 @@ other than itself: a hand-derived worked example, closed forms, invariants,
 brute force, the degree-2 polynomial special case, or central finite
 differences): elu_plus_one, elu_plus_one_grad, masked_attention,
 masked_attention_rows, linearized_attention, recurrent_attention, forward, prefill, decode_step,
-backward, denominators. No function here is parity unpinned.
+backward, denominators, poly2_feature, random_fourier_feature. No function here is parity
+unpinned.
 """
 
 from .linear_attention import (  # noqa: F401
@@ -24,5 +25,6 @@ from .linear_attention import (  # noqa: F401
     masked_attention_rows,
     poly2_feature,
     prefill,
+    random_fourier_feature,
     recurrent_attention,
 )

@@ -64,6 +64,24 @@ def poly2_feature(x):
     return outer.reshape(x.shape[:-1] + (x.shape[-1] * x.shape[-1],))
 
 
+def random_fourier_feature(x, W, b):
+    """Random Fourier features of the RBF kernel.
+
+    [summary §5] names random Fourier features, approximating the RBF kernel, as the
+    feature map to try next, without a definition. The plainest one, the random
+    Fourier features of Rahimi and Recht (2007): with the F rows w_f of W drawn
+    i.i.d. N(0, sigma^-2 I) and b_f uniform on [0, 2 pi),
+        phi(x) = sqrt(2 / F) [cos(w_1 . x + b_1), ..., cos(w_F . x + b_F)],
+    so that E[phi(x) . phi(y)] = exp(-|x - y|^2 / (2 sigma^2)). The draws are inputs:
+    W is [F, D], b is [F]; x is [..., D]; returns [..., F].
+    """
+    x = np.asarray(x, dtype=F64)
+    W = np.asarray(W, dtype=F64)
+    b = np.asarray(b, dtype=F64)
+    F = W.shape[0]
+    return np.sqrt(2.0 / F) * np.cos(x @ W.T + b)
+
+
 # ---------------------------------------------------------------------------
 # Forward: three independent forms of the same result
 # ---------------------------------------------------------------------------

@@ -6,6 +6,8 @@
   normalizers, non-causal = causal at i = N, key-order invariance, causality),
 * the degree-2 polynomial kernel, whose exact feature map turns the associative
   path into an explicit kernel sum,
+* random Fourier features, whose inner products estimate the RBF kernel
+  (a Monte Carlo check at many features),
 * central finite differences for the cumulative-sum backward,
 * prefill + decode steps = causal forward over the concatenated sequence,
 * mutation checks: a plausible mistake planted in a copy of the oracle must
@@ -381,3 +383,33 @@ def test_mutant_backward_fails_finite_differences(flaw):
     _check_backward_fd(lambda q, k, v, G, causal=True: _explicit_backward(q, k, v, G, causal), True)
     with pytest.raises(AssertionError):
         _check_backward_fd(bad, True)
+
+
+# ------------------------------------------------------- random Fourier features
+
+def test_random_fourier_features_estimate_the_rbf_kernel():
+    """E[phi(x) . phi(y)] = exp(-|x - y|^2 / (2 sigma^2)) for W ~ N(0, sigma^-2 I), b ~ U[0, 2 pi):
+    with F = 2^17 features the estimate is within a few 1/sqrt(F) of the kernel (checked
+    for D != F, so a transposed W cannot pass, and at several distances)."""
+    rng = np.random.default_rng(7)
+    D, F, sigma = 8, 1 << 17, 1.5
+    W = rng.standard_normal((F, D)) / sigma
+    b = rng.uniform(0.0, 2.0 * np.pi, F)
+    x = rng.standard_normal((6, D)) * 0.6
+    y = x + rng.standard_normal((6, D)) * np.array([0.0, 0.2, 0.5, 1.0, 1.5, 2.5])[:, None]
+    got = np.sum(la.random_fourier_feature(x, W, b) * la.random_fourier_feature(y, W, b), axis=-1)
+    want = np.exp(-np.sum((x - y) ** 2, axis=-1) / (2 * sigma ** 2))
+    assert np.max(np.abs(got - want)) < 6.0 / np.sqrt(F)
+    assert abs(got[0] - 1.0) < 6.0 / np.sqrt(F)            # x = y: the kernel is 1
+    # without the random phases the estimate is a different kernel
+    bad = np.sum(np.sqrt(2.0 / F) * np.cos(x @ W.T) * np.sqrt(2.0 / F) * np.cos(y @ W.T), axis=-1)
+    assert np.max(np.abs(bad - want)) > 0.05
+
+
+def test_random_fourier_features_shape_and_scale():
+    rng = np.random.default_rng(8)
+    W = rng.standard_normal((12, 5))
+    b = rng.uniform(0.0, 2.0 * np.pi, 12)
+    f = la.random_fourier_feature(rng.standard_normal((3, 4, 5)), W, b)
+    assert f.shape == (3, 4, 12)
+    assert np.max(np.abs(f)) <= np.sqrt(2.0 / 12) + 1e-15     # each feature is sqrt(2/F) cos(.)
