@@ -178,6 +178,27 @@ int la_forward_poly2(const void* q, const void* k, const void* v, void* out,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * la_forward_rff -- kernelized attention with random Fourier features of the
+ * RBF kernel. [summary §5] names them, approximating the RBF kernel, as the
+ * next feature map; the pages give no definition, and the one taken is Rahimi
+ * and Recht's (2007): with the F rows w_f of W and the phases b_f drawn by the
+ * caller (w_f ~ N(0, sigma^-2 I), b_f ~ U[0, 2 pi) for an RBF kernel of width
+ * sigma),
+ *   phi(x) = sqrt(2 / F) [cos(w_1 . x + b_1), ..., cos(w_F . x + b_F)],
+ * and the attention is la_forward's (causal or not) with this phi in place of
+ * elu + 1. phi(q) . phi(k) is an estimate of exp(-|q - k|^2 / (2 sigma^2)) and
+ * can be negative, so a denominator phi(q_i)^T Z_i near zero makes out_i
+ * ill-conditioned (the plain definition behaves the same).
+ * W: [F][D] in `dtype` (row-major), bias: [F] float32, device memory.
+ * Supported: bf16, D = M = F = 64; else LA_ERR_INVALID_ARG. Workspace:
+ * la_rff_workspace_bytes() (la_forward's, then the bf16 features of q and k).
+ */
+size_t la_rff_workspace_bytes(int B, int H, int N, int D, int M, int F, int causal, int dtype);
+int la_forward_rff(const void* q, const void* k, const void* v, const void* W, const float* bias,
+                   void* out, int B, int H, int N, int D, int M, int F, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Sequence shards. [summary §3.3, §3.3.1], [deck slide 4]: causal attention is
  * a prefix recurrence over (S, Z), and its gradient a pair of cumulative sums
  * running in opposite directions. A causal sequence cut into consecutive shards

@@ -21,7 +21,7 @@ __all__ = [
     "LA_ERR_TIMEOUT", "LA_ERR_TOO_LARGE", "LA_F32", "LA_BF16", "la_forward_noalloc",
     "la_forward_noalloc_status", "la_workspace_wait_site",
     "la_state_sums", "la_forward_shard", "la_backward_shard_q", "la_backward_shard_kv",
-    "la_forward_poly2", "la_poly2_workspace_bytes",
+    "la_forward_poly2", "la_poly2_workspace_bytes", "la_forward_rff", "la_rff_workspace_bytes",
     "LA_SITE_FORWARD_LOAD", "LA_SITE_BACKWARD_LOAD",
 ]
 
@@ -52,6 +52,8 @@ _SIGNATURES = {
     "la_forward_noalloc_status": (_c_int, [_vp]),
     "la_state_sums": (_c_int, [_vp] * 4 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_poly2_workspace_bytes": (_c_size, [_c_int] * 7),
+    "la_rff_workspace_bytes": (_c_size, [_c_int] * 8),
+    "la_forward_rff": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_vp, _c_size, _vp]),
     "la_backward_from_forward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp, _c_size,
                                                                      _vp]),
     "la_forward_poly2": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
@@ -539,5 +541,42 @@ def la_forward_poly2(q, k, v, causal=True, out=None, workspace=None):
         st = lib.la_forward_poly2(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
                                   N, D, M, int(bool(causal)), dt, ws.data_ptr(),
                                   ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check(fn, st)
+    return out
+
+
+# ------------------------------------------------------ random Fourier features
+
+def la_rff_workspace_bytes(B, H, N, D, M, F, causal=True, dtype=LA_BF16):
+    return load_library().la_rff_workspace_bytes(B, H, N, D, M, F, int(bool(causal)), dtype)
+
+
+def la_forward_rff(q, k, v, W, bias, causal=True, out=None, workspace=None):
+    """out[B,H,N,M] = attention with phi(x) = sqrt(2/F) cos(W x + bias) (random Fourier
+    features of the RBF kernel); W [F, D] in q's dtype, bias [F] float32."""
+    import torch
+    fn = "la_forward_rff"
+    (B, H, N), D, M = _dims(fn, q, v, 4)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (B, H, N, M), q.dtype)
+    if W.dim() != 2:
+        raise ValueError(f"{fn}: W must be [F, D]")
+    F = W.shape[0]
+    _expect(fn, "W", W, (F, D), q.dtype)
+    _expect(fn, "bias", bias, (F,), torch.float32)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, M), q.dtype)
+    dt = _dtype_code(q)
+    _need_cuda(q, k, v, W, bias, *([] if out is None else [out]))
+    lib = load_library()
+    dev = q.device
+    out = torch.empty((B, H, N, M), dtype=q.dtype, device=dev) if out is None else out
+    ws = _workspace(lib.la_rff_workspace_bytes(B, H, N, D, M, F, int(bool(causal)), dt), dev,
+                    workspace)
+    with _on_device(dev):
+        st = lib.la_forward_rff(q.data_ptr(), k.data_ptr(), v.data_ptr(), W.data_ptr(),
+                                bias.data_ptr(), out.data_ptr(), B, H, N, D, M, F,
+                                int(bool(causal)), dt, ws.data_ptr(),
+                                ws.numel() * ws.element_size(), _stream_ptr(dev))
     _check(fn, st)
     return out

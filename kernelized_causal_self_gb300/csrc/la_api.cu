@@ -214,6 +214,29 @@ int la_forward_poly2(const void* q, const void* k, const void* v, void* out, int
   return from_cuda(la::poly2_forward(q, k, v, out, B * H, N, workspace, st));
 }
 
+// ------------------------------------------------------ random Fourier features
+
+size_t la_rff_workspace_bytes(int B, int H, int N, int D, int M, int F, int causal, int dtype) {
+  (void)causal;
+  if (!query_dims_ok(B, H, N) || !la::rff_supported(D, M, F, dtype)) return la::kHeaderBytes;
+  return la::rff_workspace(B * H, N);
+}
+
+int la_forward_rff(const void* q, const void* k, const void* v, const void* W, const float* bias,
+                   void* out, int B, int H, int N, int D, int M, int F, int causal, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!la::rff_supported(D, M, F, dtype)) return LA_ERR_INVALID_ARG;
+  if (N == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, W, bias, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_rff_workspace_bytes(B, H, N, D, M, F, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  return from_cuda(la::rff_forward(q, k, v, W, bias, out, B * H, N, causal != 0, workspace, st));
+}
+
 // ------------------------------------------------------- sequence shards
 
 namespace {

@@ -70,9 +70,10 @@ cudaError_t simt_backward_kv(const void* q, const void* k, const void* v, const 
 // ---- tensor-core path (bf16, D = M = 64): tcgen05 + TMEM + TMA
 bool tc_forward_supported(int D, int M, int dtype);
 size_t tc_forward_workspace(int BH, int N);
+// identity: q and k hold features already (the identity feature map), else elu + 1 applies.
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
                        int BH, int N, bool causal, void* ws, cudaStream_t st,
-                       const FaultHook* fault = nullptr);
+                       const FaultHook* fault = nullptr, bool identity = false);
 cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int BH, int N, void* ws,
                           cudaStream_t st);
 size_t tc_backward_workspace(int BH, int N);
@@ -98,6 +99,14 @@ bool poly2_supported(int D, int M, int dtype, int causal);
 size_t poly2_workspace(int BH, int N);
 cudaError_t poly2_forward(const void* q, const void* k, const void* v, void* out, int BH, int N,
                           void* ws, cudaStream_t st);
+
+// ---- random Fourier features (bf16, D = M = F = 64): features on tcgen05, then the
+// identity-feature forward
+bool rff_supported(int D, int M, int F, int dtype);
+size_t rff_workspace(int BH, int N);
+cudaError_t rff_forward(const void* q, const void* k, const void* v, const void* W,
+                        const float* bias, void* out, int BH, int N, bool causal, void* ws,
+                        cudaStream_t st);
 
 // ---- decode step (memory-bound CUDA-core kernel)
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* out,

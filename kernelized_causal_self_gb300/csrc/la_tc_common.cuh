@@ -368,8 +368,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 enum ScanMode { kScanPrefix = 0, kScanTotal = 1, kScanSuffix = 2 };
 
 // Segment increments dS^T = V^T phi(K), dZ = sum phi(K) into partial[item].
+// identity: the K tiles hold the features f already (summed as they are), else the
+// elu + 1 map (summed in the psi form).
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st);
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st,
+                                  bool identity = false);
 // Prefix / total / suffix of the per-segment states (see ScanMode).
 // With io.S set, the prefix / total also starts from io's initial state (when
 // io.read_init) and the full sum is written to io's entries (prefill, extend).

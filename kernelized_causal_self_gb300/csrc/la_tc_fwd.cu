@@ -48,6 +48,10 @@ constexpr int kStateStages = 3;
 constexpr int kStateStageBytes = 2 * kTile;  // K, V
 constexpr int kStateSmem = 1024 + kStateStages * kStateStageBytes + 2048 + 256;
 
+// IDENT: the K tiles hold the features f already (the identity feature map): the
+// group then gives V^T f and sum_t f directly (features centred on zero, nothing
+// to split off). Else inputs to which the elu + 1 map applies, in the psi form.
+template <bool IDENT>
 __global__ void __launch_bounds__(kStateThreads, 2)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
@@ -177,12 +181,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // plus the segment's count of valid tokens. This thread writes columns
       // [32h, 32h + 32) of its row.
       if (q4 < 2 || (q4 == 2 && lane == 0)) {
-        float add;
+        float add = 0.f;  // identity features: the sums are the state itself
         if (q4 < 2) {
           uint32_t r16[16];
           tmem_ld16(acc + 64, r16);
-          add = __uint_as_float(r16[0]);
-        } else {
+          if (!IDENT) add = __uint_as_float(r16[0]);
+        } else if (!IDENT) {
           const int c0 = g.chunk_begin(item), c1 = g.chunk_end(item);
           add = (float)max(0, min(g.len(g.bh_of(item)) - c0 * kC, (c1 - c0) * kC));
         }
@@ -213,7 +217,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ok = false;
         break;
       }
-      psi_half(kt, trow, h, nvalid);
+      if (IDENT)
+        zero_half_if_past(kt, trow, h, nvalid);
+      else
+        psi_half(kt, trow, h, nvalid);
       if (nvalid < kC) zero_half_if_past(vt, trow, h, nvalid);
       fence_proxy_async_smem();
       mbar_arrive(&phid[s]);
@@ -330,7 +337,7 @@ constexpr uint32_t kTmemCols = 256;
 // finish before a barrier, the writes follow it.
 constexpr int kAttThreads = 256;
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool IDENT>
 __global__ void __launch_bounds__(kAttThreads, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -491,10 +498,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // phi(Q) with the packed-bf16 exponential: its rounding enters numerator and
     // denominator alike and largely cancels in out = num / den; phi(K) exact, since
     // the state sums phi(K) v^T over random-sign v (padded query rows are never stored)
-    phi_half(qt, row, h, kC);
-    if (CAUSAL) {
-      phi_half<true>(kt, row, h, nvalid);
-      if (nvalid < kC) zero_half_if_past(vt, row, h, nvalid);
+    if (IDENT) {  // the tiles hold the features: only the rows past the end are cleared
+      if (CAUSAL && nvalid < kC) {
+        zero_half_if_past(kt, row, h, nvalid);
+        zero_half_if_past(vt, row, h, nvalid);
+      }
+    } else {
+      phi_half(qt, row, h, kC);
+      if (CAUSAL) {
+        phi_half<true>(kt, row, h, nvalid);
+        if (nvalid < kC) zero_half_if_past(vt, row, h, nvalid);
+      }
     }
     fence_proxy_async_smem();
     fence_before_sync();
@@ -747,14 +761,17 @@ Geometry make_geometry(int BH, int N) {
 }
 
 cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, const Geometry& g,
-                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st) {
-  cudaError_t e = configure(tc_state_kernel, kStateSmem);
-  if (e != cudaSuccess) return e;
-  const int ctas = min(g.n_items(), resident_ctas(tc_state_kernel, kStateSmem, kStateThreads) * sm_count());
-  e = launch_pdl(tc_state_kernel, dim3(ctas), dim3(kStateThreads), kStateSmem, st, *tk, *tv, g,
-                 partial, hdr);
-  count_launches(1);
-  return e != cudaSuccess ? e : cudaGetLastError();
+                                  float* partial, WorkspaceHeader* hdr, cudaStream_t st,
+                                  bool identity) {
+  auto run = [&](auto kern) {
+    cudaError_t e = configure(kern, kStateSmem);
+    if (e != cudaSuccess) return e;
+    const int ctas = min(g.n_items(), resident_ctas(kern, kStateSmem, kStateThreads) * sm_count());
+    e = launch_pdl(kern, dim3(ctas), dim3(kStateThreads), kStateSmem, st, *tk, *tv, g, partial, hdr);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  };
+  return identity ? run(tc_state_kernel<true>) : run(tc_state_kernel<false>);
 }
 
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode,
@@ -802,7 +819,7 @@ cudaError_t tc_state_sums(const void* k, const void* v, const StateIO& io, int B
 
 cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, const StateIO& io,
                        int BH, int N, bool causal, void* ws, cudaStream_t st,
-                       const FaultHook* fault) {
+                       const FaultHook* fault, bool identity) {
   Geometry g = make_geometry(BH, N);
   g.lens = io.lens;
   g.H = io.H;
@@ -830,7 +847,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
   cudaError_t e = cudaSuccess;
   if (!direct) {
-    e = launch_segment_states(&tk, &tv, g, partial, hdr, st);
+    e = launch_segment_states(&tk, &tv, g, partial, hdr, st, identity);
     if (e != cudaSuccess) return e;
     e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
     if (e != cudaSuccess) return e;
@@ -838,25 +855,20 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   const int sms = sm_count();
 
   // non-causal: one item per chunk range of the readout, all reading prefix[bh]
-  if (causal) {
-    e = configure(tc_attend_kernel<true>, kAttSmem);
-    if (e != cudaSuccess) return e;
-    const int ctas =
-        min(g.n_items(), resident_ctas(tc_attend_kernel<true>, kAttSmem, kAttThreads) * sms);
-    e = launch_pdl(tc_attend_kernel<true>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
-                   to, g, (const float*)prefix, io, direct, hdr);
-    if (e != cudaSuccess) return e;
-  } else {
-    e = configure(tc_attend_kernel<false>, kAttSmem);
-    if (e != cudaSuccess) return e;
-    const int ctas =
-        min(g.n_items(), resident_ctas(tc_attend_kernel<false>, kAttSmem, kAttThreads) * sms);
-    e = launch_pdl(tc_attend_kernel<false>, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv,
-                   to, g, (const float*)prefix, StateIO{}, false, hdr);
-    if (e != cudaSuccess) return e;
-  }
-  count_launches(1);
-  return cudaGetLastError();
+  auto attend = [&](auto kern, const StateIO& kio, bool kdirect) {
+    cudaError_t err = configure(kern, kAttSmem);
+    if (err != cudaSuccess) return err;
+    const int ctas = min(g.n_items(), resident_ctas(kern, kAttSmem, kAttThreads) * sms);
+    err = launch_pdl(kern, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv, to, g,
+                     (const float*)prefix, kio, kdirect, hdr);
+    count_launches(1);
+    return err != cudaSuccess ? err : cudaGetLastError();
+  };
+  if (causal)
+    return identity ? attend(tc_attend_kernel<true, true>, io, direct)
+                    : attend(tc_attend_kernel<true, false>, io, direct);
+  return identity ? attend(tc_attend_kernel<false, true>, StateIO{}, false)
+                  : attend(tc_attend_kernel<false, false>, StateIO{}, false);
 }
 
 }  // namespace la

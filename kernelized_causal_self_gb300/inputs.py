@@ -74,6 +74,12 @@ def normal(seed, shape, scale=1.0, dtype=F32, stream=0):
     return bf16_round(x) if dtype == BF16 else x
 
 
+def uniform(seed, shape, lo, hi, stream=0):
+    """i.i.d. uniform on [lo, hi) from PCG64(seed, stream), float32."""
+    rng = np.random.Generator(np.random.PCG64([seed, stream]))
+    return (lo + (hi - lo) * rng.random(size=shape)).astype(np.float32)
+
+
 def qkv(seed, B, H, N, D, M, scale=1.0, dtype=F32):
     """q, k: [B, H, N, D]; v: [B, H, N, M]; drawn in that order (streams 0, 1, 2)."""
     q = normal(seed, (B, H, N, D), scale, dtype, stream=0)
