@@ -177,7 +177,7 @@ def parse():
                     help="launch the step's calls directly instead of replaying CUDA graphs")
     ap.add_argument("--part", default=None,
                     choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "bwdfwd", "decode",
-                             "extend", "poly2"],
+                             "extend", "poly2", "rff"],
                     help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
@@ -323,6 +323,9 @@ def run_parts(la, device, peaks, reps=10):
     # degree-2 polynomial feature map on the main workload's shape (forward, causal)
     parts["poly2_causal_fwd_b4h8n16384d64"] = poly2_part(la, inputs.WORKLOADS[MAIN], device, peaks,
                                                          flush, reps)
+    # random Fourier features (F = 64) on the main workload's shape (forward, causal)
+    parts["rff_causal_fwd_b4h8n16384d64"] = rff_part(la, inputs.WORKLOADS[MAIN], device, peaks,
+                                                     flush, reps)
     # decode with a state too large for L2: DECODE_HBM_STREAMS streams x 8 heads (134 MB of S),
     # so every step reads and writes S in HBM
     parts[f"decode_s{DECODE_HBM_STREAMS}h{w.H}d{w.D}_hbm"] = decode_hbm_part(la, w, device, hbm)
@@ -359,6 +362,37 @@ def poly2_part(la, w, device, peaks, flush, reps):
             "roofline_frac": tflops / peaks["bf16_tflops"], "bound": "tensor",
             "flops_per_token_head": poly2_flops(w), "hbm_gbs": gbs,
             "hbm_frac": gbs / peaks["hbm_gbs"], "l2": "flushed between calls (256 MB read)"}
+
+
+RFF_FEATURES = 64
+
+
+def rff_inputs(w, device):
+    """W [F, D] with rows ~ N(0, I) (bf16) and phases b ~ U[0, 2 pi) (float32), seeded."""
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    W = inputs.to_torch(inputs.normal(w.seed, (RFF_FEATURES, w.D), 1.0, w.dtype, 7), w.dtype, device)
+    b = torch.from_numpy(inputs.uniform(w.seed, (RFF_FEATURES,), 0.0, 6.283185307179586, 8)).to(device)
+    return W, b
+
+
+def rff_part(la, w, device, peaks, flush, reps):
+    """Causal forward with random Fourier features; HBM-bound like the elu + 1 forward (the
+    feature GEMM is 2 * 2 * D * F flop per token-head), measured against the same 512 B per
+    token-head (the features written and read back are implementation traffic)."""
+    import torch
+    q, k, v, _ = device_inputs(w, device)
+    W, b = rff_inputs(w, device)
+    out = torch.empty_like(v)
+    ws = torch.empty(la.la_rff_workspace_bytes(w.B, w.H, w.N, w.D, w.M, RFF_FEATURES, True),
+                     dtype=torch.uint8, device=device)
+    ms = statistics.median(time_calls(lambda: la.la_forward_rff(q, k, v, W, b, True, out, ws),
+                                      reps, 3, flush))
+    th = w.B * w.H * w.N
+    gbs = th * fwd_bytes(w) / (ms * 1e-3) / 1e9
+    return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms": ms, "hbm_gbs": gbs,
+            "roofline_frac": gbs / peaks["hbm_gbs"], "bound": "hbm", "features": RFF_FEATURES,
+            "l2": "flushed between calls (256 MB read)"}
 
 
 DECODE_HBM_STREAMS, DECODE_HBM_STEPS, DECODE_HBM_PREFILL = 1024, 128, 128
@@ -725,7 +759,7 @@ def run_part(args):
     labuild.build()
     la.load_library()
     device = torch.device("cuda", 0)
-    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "bwdfwd": MAIN, "poly2": MAIN,
+    name = {"fwdbwd": MAIN, "fwd16k": MAIN, "bwd": MAIN, "bwdfwd": MAIN, "poly2": MAIN, "rff": MAIN,
             "fwd3072": "causal_fwd_b8h8n3072d64",
             "noncausal": "noncausal_fwd_b4h8n4096d64",
             "decode": "decode_s256h8d64_prefill1024_steps3072",
@@ -750,6 +784,9 @@ def run_part(args):
         fn = lambda: la.la_backward(q, k, v, dout, True, fwd_workspace=wsf)
     elif args.part == "poly2":
         fn = lambda: la.la_forward_poly2(q, k, v, True)
+    elif args.part == "rff":
+        W, b = rff_inputs(w, device)
+        fn = lambda: la.la_forward_rff(q, k, v, W, b, True)
     elif args.part == "fwdbwd":
         fn = lambda: (la.la_forward(q, k, v, True), la.la_backward(q, k, v, dout, True))
     else:
