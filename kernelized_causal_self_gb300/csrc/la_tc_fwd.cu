@@ -496,11 +496,8 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       break;
     }
     // phi(Q) with the packed-bf16 exponential: its rounding enters numerator and
-    // denominator alike and largely cancels in out = num / den. phi(K) likewise on the
-    // segment path, where the carried increments only span the segment's chunks (the
-    // long-range state comes from the psi-form segment sums); exact on the direct path,
-    // whose state after the chunk is written back and summed over random-sign v by
-    // later calls (padded query rows are never stored)
+    // denominator alike and largely cancels in out = num / den; phi(K) exact, since
+    // the state sums phi(K) v^T over random-sign v (padded query rows are never stored)
     if (IDENT) {  // the tiles hold the features: only the rows past the end are cleared
       if (CAUSAL && nvalid < kC) {
         zero_half_if_past(kt, row, h, nvalid);
@@ -509,10 +506,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else {
       phi_half(qt, row, h, kC);
       if (CAUSAL) {
-        if (direct)
-          phi_half<true>(kt, row, h, nvalid);
-        else
-          phi_half(kt, row, h, nvalid);
+        phi_half<true>(kt, row, h, nvalid);
         if (nvalid < kC) zero_half_if_past(vt, row, h, nvalid);
       }
     }
