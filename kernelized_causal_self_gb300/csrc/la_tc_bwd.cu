@@ -172,22 +172,113 @@ __device__ __forceinline__ float warp_column_sums16(float (&z)[16]) {
   return z[0] + __shfl_xor_sync(0xffffffffu, z[0], 16);
 }
 
-// Block-uniform wait for a tile stage, folded together with an optional wait
-// for the previous chunk's deferred MMAs (one barrier for both).
-__device__ __forceinline__ bool wait_uniform2(uint64_t* bar, uint32_t parity, uint64_t* bar2,
-                                              uint32_t parity2, bool use2, WorkspaceHeader* hdr,
-                                              int site, uint64_t limit_ns) {
-  bool ok = mbar_wait(bar, parity, limit_ns);
-  if (use2) ok = mbar_wait(bar2, parity2, limit_ns) && ok;
-  const bool all = __syncthreads_and(ok ? 1 : 0) != 0;
-  if (!all && threadIdx.x == 0) record_timeout(hdr, site);
-  return all;
-}
-
 __device__ __forceinline__ void sync_tc() {
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+}
+
+// --------------------------------------------------- warp-specialised kernels
+//
+// 640 threads: warps 0-15 are the workers (warp w covers TMEM lane quarter
+// w % 4 and column quarter w / 4, every tile row handled by four threads);
+// warp 16 issues the MMAs and warp 17 the TMA loads and stores, one thread
+// each; warps 18 and 19 complete that control warpgroup, whose registers go to
+// the workers. The workers hand the MMA warp its operands through mbarriers
+// (one arrival per warp), and the TMA warp the staged outputs; among themselves
+// they synchronise on a named barrier. Nothing else waits for the thread that
+// issues a group of MMAs, and while a chunk's second group runs the workers
+// already prepare the next chunk's tiles, which the TMA warp loaded into the
+// other stage.
+constexpr int kWorkers = 512;
+constexpr int kWsThreads = kWorkers + 128;
+constexpr int kMmaWarp = 16, kTmaWarp = 17;
+constexpr int kWorkerRegs = 104, kControlRegs = 64;  // 512 x 104 + 128 x 64 = 640 x 96
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Named barrier 1 over the 512 workers, reducing a flag: true for all if any
+// worker passes true (a failed wait ends the loop for every worker together).
+__device__ __forceinline__ bool workers_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 512, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait of one thread that also gives up once another role has given up.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          WorkspaceHeader* hdr, int site, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      record_timeout(hdr, site);
+      return false;
+    }
+  }
+}
+
+// The same for a whole warp (warp-collective TMEM accesses follow).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          WorkspaceHeader* hdr, int site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, role_wait(bar, parity, abort, hdr, site, limit_ns));
+}
+
+// One arrival per warp on a barrier that counts the 16 worker warps, once every
+// lane's writes are in.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with each descriptor given as its two 32-bit
+// halves: stepping through K then changes only the low half (the start
+// address >> 4, far below its 14-bit limit here), one add per operand.
+__device__ __forceinline__ void mma_ss_h(uint32_t d, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ra, rb;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %5, p;\n\t}" ::"r"(d),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// N MMAs over consecutive K = 16 slices, the descriptors advanced by AS / BS
+// bytes per slice (32 inside a K-major swizzle atom, 2048 = 16 rows of an
+// MN-major tile); acc0: whether the first one accumulates.
+template <int N, uint32_t AS, uint32_t BS>
+__device__ __forceinline__ void mma_run(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc0) {
+  const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32);
+  const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    mma_ss_h(d, alo + k * (AS >> 4), ahi, blo + k * (BS >> 4), bhi, idesc, k == 0 ? acc0 : 1u);
+}
+
+// The same with A in TMEM (8 columns of packed bf16 per slice), accumulating.
+template <int N, uint32_t BS>
+__device__ __forceinline__ void mma_run_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) mma_ts(d, a_tmem + 8 * k, b + k * (BS >> 4), idesc, 1u);
 }
 
 // --------------------------------------------------- forward direction: dq
@@ -202,331 +293,422 @@ __device__ __forceinline__ void sync_tc() {
 // sum of phi(Q)^T gN.
 
 // TMEM columns
-constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T; after the first epilogue, dphiQ (kFQ)
-constexpr uint32_t kFW = 128;   // 128: W = G V^T; then bf16 T_L hi in [128,192), lo in [192,256)
-constexpr uint32_t kFO = 256;   // 128: phi(Q) S_prev as phi(Q) S_hi (0..63) and phi(Q) S_lo (64..127)
+constexpr uint32_t kFP = 0;     // 128: P = phi(Q) phi(K)^T; after the first epilogue, bf16 T_L
+                                // hi in [0,64), lo in [64,128) (kFT)
+constexpr uint32_t kFW = 128;   // 128: W = G V^T
+constexpr uint32_t kFO = 256;   // 128: phi(Q) S_prev as phi(Q) S_hi (0..63) and phi(Q) S_lo (64..127);
+                                // after the first epilogue, dphiQ as two 64-column parts (kFQ)
+constexpr uint32_t kFT = 0;
+constexpr uint32_t kFQ = 256;
 constexpr uint32_t kFS = 384;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
-constexpr uint32_t kFQ = 0;     // 128: dphiQ as two 64-column parts (P's columns, spent by then)
-constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 64 layout)
+constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 128 layout, like dS)
+
+// A stage holds one chunk: the loaded Q, K, V, G tiles (phi applied to Q and K
+// in place) and the lo parts of phi(K) and phi(Q). gN takes the place of G (hi)
+// and of the spent V (lo); dq is staged in the K and phi(K) lo tiles.
+enum { kSQ = 0, kSK = 1, kSV = 2, kSG = 3, kSKL = 4, kSQL = 5, kQStageTiles = 6 };
+constexpr int kQArr = 1664;  // floats: Z snapshots, column sums, den / G.num partials
+constexpr int kQSmem = 1024 + 2 * kQStageTiles * kTile + 2 * kDim * 128 + kQArr * 4 + 128;
+
+struct QSmem {
+  uint8_t* stages;
+  uint8_t* s_hi;  // state snapshot S_prev as bf16 hi and lo, rows d, m contiguous
+  uint8_t* s_lo;
+  float* arr;
+  uint64_t* full;      // [2] a stage's tiles landed
+  uint64_t* g1_ready;  // the workers' operands of the first group are in (16 warps)
+  uint64_t* g2_ready;  // ... of the second group
+  uint64_t* st_ready;  // the chunk's dq is staged, and the workers are done with its stage
+  uint64_t* g1_done;   // P, W, phi(Q) S_prev
+  uint64_t* ds_done;   // dS (the last reader of V)
+  uint64_t* gn_free;   // gN S_prev^T and the segment sums (the last readers of the gN tiles,
+                       // the snapshot and the phi(Q) tiles)
+  uint64_t* g2_done;   // dphiQ
+  uint64_t* dq_read;   // the workers have read dphiQ (16 warps)
+  uint64_t* drain;     // every MMA of the CTA is done (end of the kernel)
+  int* abort;
+  uint32_t* tslot;
+  __device__ explicit QSmem(uint8_t* raw) {
+    uint8_t* sm =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    stages = sm;
+    s_hi = sm + 2 * kQStageTiles * kTile;
+    s_lo = s_hi + kDim * 128;
+    arr = reinterpret_cast<float*>(s_lo + kDim * 128);
+    uint64_t* b = reinterpret_cast<uint64_t*>(arr + kQArr);
+    full = b;
+    g1_ready = b + 2;
+    g2_ready = b + 3;
+    st_ready = b + 4;
+    g1_done = b + 5;
+    ds_done = b + 6;
+    gn_free = b + 7;
+    g2_done = b + 8;
+    dq_read = b + 9;
+    drain = b + 10;
+    abort = reinterpret_cast<int*>(b + 11);
+    tslot = reinterpret_cast<uint32_t*>(b + 11) + 1;
+  }
+  __device__ uint8_t* tile(int s, int which) { return stages + (s * kQStageTiles + which) * kTile; }
+};
+
+// MMA warp, one thread: per chunk the first group once the workers' phi and
+// snapshot are in, the second once gN and T_L are.
+template <bool CAUSAL>
+__device__ __forceinline__ void bwd_q_mma(QSmem& sm, const Geometry& g, uint32_t tbase,
+                                          volatile int* abort, WorkspaceHeader* hdr) {
+  Cursor c;
+  c.start(g, true);
+  const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
+  long long n = 0;
+  while (c.valid(g)) {
+    const int s = (int)(n & 1);
+    const uint32_t ph = (uint32_t)(n & 1);
+    const uint32_t qa = smem_u32(sm.tile(s, kSQ)), ka = smem_u32(sm.tile(s, kSK));
+    const uint32_t va = smem_u32(sm.tile(s, kSV)), ga = smem_u32(sm.tile(s, kSG));
+    const uint32_t kl = smem_u32(sm.tile(s, kSKL)), ql = smem_u32(sm.tile(s, kSQL));
+    if (!role_wait(sm.g1_ready, ph, abort, hdr, 41, kWaitLimitNs)) break;
+    // P overwrites the previous chunk's T_L: its second group must be done
+    if (n > 0 && !role_wait(sm.g2_done, ph ^ 1, abort, hdr, 44, kWaitLimitNs)) break;
+    fence_after_sync();
+    // K-major operands step 32 bytes per K = 16 slice (inside the swizzle atom),
+    // MN-major ones 2048 bytes (16 rows of 128 bytes)
+    if (CAUSAL) {
+      const uint32_t id128 = idesc_bf16(128, 128, false, false);
+      // P = phi(Q) (phi(K)_hi + phi(K)_lo)^T, W = G V^T
+      mma_run<4, 32, 32>(tbase + kFP, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id128, 0);
+      mma_run<4, 32, 32>(tbase + kFP, sdesc(qa, 16, 1024), sdesc(kl, 16, 1024), id128, 1);
+      mma_run<4, 32, 32>(tbase + kFW, sdesc(ga, 16, 1024), sdesc(va, 16, 1024), id128, 0);
+    }
+    // phi(Q) S_prev overwrites the previous chunk's dphiQ: the workers must have read it
+    if (n > 0 && !role_wait(sm.dq_read, ph ^ 1, abort, hdr, 45, kWaitLimitNs)) break;
+    fence_after_sync();
+    // phi(Q) [S_hi | S_lo]: B = the snapshot, rows d (= K), m contiguous
+    // (MN-major), its hi and lo tiles the two 64-column N blocks (la - ha apart)
+    mma_run<4, 32, 2048>(tbase + kFO, sdesc(qa, 16, 1024), sdesc(ha, la - ha, 1024),
+                         idesc_bf16(128, 128, false, true), 0);
+    mma_commit(sm.g1_done);
+    if (CAUSAL) {  // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
+                   // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
+      mma_run<kC / 16, 2048, 2048>(tbase + kFS, sdesc(ka, kl - ka, 1024), sdesc(va, 1024, 1024),
+                                   idesc_bf16(128, 64, true, true), 0);
+      mma_commit(sm.ds_done);
+    }
+    if (!role_wait(sm.g2_ready, ph, abort, hdr, 42, kWaitLimitNs)) break;
+    fence_after_sync();
+    // gN [S_hi; S_lo]^T + gN_lo S_hi^T first: B = the snapshot, rows d (= N), m
+    // contiguous (K-major), the S_lo rows after the S_hi rows (one N = 128
+    // product); gN hi sits in the G tile, gN lo in the V tile. dphiQ is the sum
+    // of the accumulator's two 64-column halves.
+    const uint32_t gha = ga, gla = va;
+    mma_run<4, 32, 32>(tbase + kFQ, sdesc(gha, 16, 1024), sdesc(ha, 16, 1024),
+                       idesc_bf16(128, 128, false, false), 0);
+    mma_run<4, 32, 32>(tbase + kFQ, sdesc(gla, 16, 1024), sdesc(ha, 16, 1024),
+                       idesc_bf16(128, 64, false, false), 1);
+    // segment sum of phi(Q)^T gN: phi(Q)^T hi and lo stacked as one M = 128
+    // MN-major operand (ql - qa bytes apart) times gN hi, then gN lo; the hi-row
+    // and lo-row halves (TMEM lanes 0-63 / 64-127) are summed at the segment's end
+    const uint32_t idR = idesc_bf16(128, 64, true, true);
+    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc(qa, ql - qa, 1024), sdesc(gha, 1024, 1024), idR,
+                                 c.first() ? 0u : 1u);
+    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc(qa, ql - qa, 1024), sdesc(gla, 1024, 1024), idR, 1);
+    mma_commit(sm.gn_free);
+    if (CAUSAL) {
+      // + T_L phi(K) with the hi*hi + hi*lo + lo*hi terms; the hi*lo partners share
+      // their A operand (T_L in TMEM, 8 columns per K = 16 slice), so they sit side
+      // by side in one N = 128 instruction: T_hi [phi(K)_hi | phi(K)_lo] (N blocks
+      // kl - ka apart), then T_lo phi(K)_hi
+      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT, sdesc(ka, kl - ka, 1024),
+                                idesc_bf16(128, 128, false, true));
+      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT + 64, sdesc(ka, 1024, 1024),
+                                idesc_bf16(128, 64, false, true));
+    }
+    mma_commit(sm.g2_done);
+    ++n;
+    c.advance(g);
+  }
+  // every MMA completes before the CTA frees TMEM (time-bounded only)
+  mma_commit(sm.drain);
+  if (!mbar_wait(sm.drain, 0)) record_timeout(hdr, 25);
+}
+
+// TMA warp, one thread: loads two chunks ahead of the workers, stores each
+// chunk's dq once it is staged and then refills that stage.
+template <bool CAUSAL>
+__device__ __forceinline__ void bwd_q_tma(QSmem& sm, const Geometry& g, const CUtensorMap* tm_q,
+                                          const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                          const CUtensorMap* tm_g, const CUtensorMap* tm_dq,
+                                          volatile int* abort, WorkspaceHeader* hdr) {
+  const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
+  Cursor cl, cs;
+  cl.start(g, true);
+  cs = cl;
+  long long nl = 0, ns = 0;
+  auto load = [&]() {
+    const int s = (int)(nl & 1);
+    if (!(g.faulty() && nl == g.fault_load)) {  // test hook: this load is withheld
+      const int t0 = cl.chunk * kC;
+      mbar_arrive_expect_tx(&sm.full[s], tx);
+      tma_load_3d(sm.tile(s, kSQ), tm_q, &sm.full[s], 0, t0, cl.bh);
+      tma_load_3d(sm.tile(s, kSG), tm_g, &sm.full[s], 0, t0, cl.bh);
+      if (CAUSAL) {
+        tma_load_3d(sm.tile(s, kSK), tm_k, &sm.full[s], 0, t0, cl.bh);
+        tma_load_3d(sm.tile(s, kSV), tm_v, &sm.full[s], 0, t0, cl.bh);
+      }
+    }
+    ++nl;
+    cl.advance(g);
+  };
+  while (nl < 2 && cl.valid(g)) load();
+  while (cs.valid(g)) {
+    const int s = (int)(ns & 1);
+    if (!role_wait(sm.st_ready, (uint32_t)(ns & 1), abort, hdr, 43, kWaitLimitNs)) break;
+    // rows past the sequence end are clipped by the tensor map
+    tma_store_3d(tm_dq, sm.tile(s, kSK), 0, cs.chunk * kC, cs.bh);
+    tma_store_3d(tm_dq, sm.tile(s, kSKL), 32, cs.chunk * kC, cs.bh);
+    bulk_commit();
+    if (cl.valid(g)) {
+      bulk_wait_read<0>();
+      load();
+    }
+    ++ns;
+    cs.advance(g);
+  }
+  // every issued load lands and every store completes before the CTA lets go of
+  // its shared memory (time-bounded only)
+  for (long long k = ns; k < nl; ++k)
+    if (!(g.faulty() && k == g.fault_load) && !mbar_wait(&sm.full[k & 1], (uint32_t)((k >> 1) & 1)))
+      record_timeout(hdr, 26);
+  bulk_wait_all<0>();
+}
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(kBTQ, 1)
-tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const __grid_constant__ CUtensorMap tm_dq, Geometry g,
-                const float* __restrict__ sprefix, float* __restrict__ rpartial,
-                float* __restrict__ den_out, float* __restrict__ gd_out, WorkspaceHeader* hdr) {
-  extern __shared__ uint8_t smraw[];
-  BwdSmem sm(smraw);
-  float* zsnap = sm.arr;         // 64: Z before the chunk (float32)
-  float* dz = sm.arr + 64;       // [4][64]: warp column sums
-  float* rsum = sm.arr + 320;    // [4][128]: quarter-row parts of den
-  float* gnum = sm.arr + 832;    // [4][128]: quarter-row parts of G . num
+__device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint32_t tbase,
+                                              volatile int* abort, const float* __restrict__ sprefix,
+                                              float* __restrict__ rpartial, float* __restrict__ den_out,
+                                              float* __restrict__ gd_out, WorkspaceHeader* hdr) {
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int lq = warp & 3, qc = warp >> 2;
   const int row = lq * 32 + lane;  // query row of this thread
   // S carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
   const int drow = 32 * (lq & 1) + lane;
   const bool dthread = lq < 2;
-  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
-  // stores) belong to warp 1's first thread, so that the two issue in parallel
-  const bool tma_thread = tid == 32;
-
-  if (tid == 0) {
-    for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
-    mbar_init(sm.mma_bar, 1);
-    mbar_init(&sm.sbar[0], 1);
-    mbar_init(&sm.sbar[1], 1);
-    mbar_init(sm.drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(sm.tslot, 512);
-    tmem_relinquish();
-  }
-  sync_tc();
-  const uint32_t tbase = *sm.tslot;
   const uint32_t tl = lane_base(tbase);
-  pdl_wait();
+  const uint64_t wlim = g.wait_ns();  // tile waits (shortened only by the test hook)
+  float* zsnap = sm.arr;        // [2][64]: Z before the chunk, by chunk parity
+  float* dzk = sm.arr + 128;    // [4][64]: column sums of the prepared chunk's phi(K)
+  float* dzr = sm.arr + 384;    // [4][64]: the chunk's column sums of gd phi(Q)
+  float* rsum = sm.arr + 640;   // [4][128]: quarter-row parts of den
+  float* gnum = sm.arr + 1152;  // [4][128]: quarter-row parts of G . num
 
-  const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
-  const uint64_t wlim = g.wait_ns();  // main-loop wait limit (shortened only by the test hook)
-  // items last to first: the segment-state kernel just streamed k and v first to
-  // last, and the reverse-direction kernel then starts where this one ends
-  Cursor cc, cp;
-  cc.start(g, true);
-  cp.start(g, true);
-  long long issued = 0;
-  auto issue = [&](Cursor& c) {
-    if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
-      ++issued;
-      c.advance(g);
-      return;
-    }
-    const int s = issued % kBwdStages;
-    const int bh = c.bh, t0 = c.chunk * kC;
-    mbar_arrive_expect_tx(&sm.full[s], tx);
-    tma_load_3d(sm.tile(s, kQ), &tm_q, &sm.full[s], 0, t0, bh);
-    tma_load_3d(sm.tile(s, kG), &tm_g, &sm.full[s], 0, t0, bh);
+  // phi of a stage's tiles in place, the rounding errors into the lo tiles
+  auto phi_stage = [&](int s, int nvalid) {
+    float z[16];
     if (CAUSAL) {
-      tma_load_3d(sm.tile(s, kK), &tm_k, &sm.full[s], 0, t0, bh);
-      tma_load_3d(sm.tile(s, kV), &tm_v, &sm.full[s], 0, t0, bh);
-    }
-    ++issued;
-    c.advance(g);
-  };
-  if (tma_thread)
-    for (int i = 0; i < kBwdStages - 1 && cp.valid(g); ++i) issue(cp);
-
-  float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
-  float zrun = 0.f, rr = 0.f;  // Z[d], r[d] for d = tid < 64
-  long long consumed = 0;
-  uint32_t ph = 0, sph0 = 0, sph1 = 0;
-  // the previous chunk's segment-sum MMAs (sbar[1]) are still to be waited for:
-  // they read phi(Q) lo and gN, which the next chunk rewrites
-  bool r_pending = false;
-  float z[16];
-
-  while (cc.valid(g)) {
-    const int item = cc.item, bh = cc.bh, t0 = cc.chunk * kC;
-    const bool first = cc.first();
-    const bool last = cc.last();
-    const int nvalid = min(kC, g.N - t0);
-    if (first) {
-      const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
-      if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
-#pragma unroll
-        for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + drow];
-      }
-      if (tid < kDim) {
-        zrun = src[kDim * kDim + tid];
-        rr = 0.f;
-      }
-    }
-    if ((CAUSAL || first) && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
-    if (tid < kDim) zsnap[tid] = zrun;
-    const int s = consumed % kBwdStages;
-    uint8_t* qt = sm.tile(s, kQ);
-    uint8_t* kt = sm.tile(s, kK);
-    uint8_t* vt = sm.tile(s, kV);
-    uint8_t* gt = sm.tile(s, kG);
-    if (!wait_uniform2(&sm.full[s], (consumed / kBwdStages) & 1, &sm.sbar[1], sph1, r_pending, hdr, 21,
-                       wlim))
-      break;
-    if (r_pending) {
-      sph1 ^= 1;
-      r_pending = false;
-      fence_after_sync();
-    }
-    phi_quarter_split(qt, sm.qlo, row, qc, kC, z);
-    if (CAUSAL) {
-      phi_quarter_split(kt, sm.klo, row, qc, nvalid, z);
+      phi_quarter_split(sm.tile(s, kSK), sm.tile(s, kSKL), row, qc, nvalid, z);
       const float cs = warp_column_sums16(z);
-      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
+      if (lane < 16) dzk[lq * 64 + 16 * qc + lane] = cs;
     }
+    phi_quarter_split(sm.tile(s, kSQ), sm.tile(s, kSQL), row, qc, kC, z);
     fence_proxy_async_smem();
-    sync_tc();
-    if (tma_thread) {
-      // the next chunk's tiles go into the previous chunk's stage, whose dq staging
-      // TMA stores have had this chunk's phi to finish reading it
-      bulk_wait_read<0>();
-      if (cp.valid(g)) issue(cp);
+  };
+  float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
+  float zrun = 0.f, zinc = 0.f, rr = 0.f;  // Z[d], the chunk's phi(K) column sums, r[d] (tid < 64)
+  // the state a segment starts from: carry and snapshot
+  auto start_item = [&](int item, int bh) {
+    const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+    if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
+#pragma unroll
+      for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + drow];
+      store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
     }
-    if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt), ga = smem_u32(gt);
-      const uint32_t kl = smem_u32(sm.klo);
-      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
-      if (CAUSAL) {
-        const uint32_t id128 = idesc_bf16(128, 128, false, false);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // P = phi(Q) (phi(K)_hi + phi(K)_lo)^T
-          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), id128, k);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tbase + kFP, sdesc(qa + k * 32, 16, 1024), sdesc(kl + k * 32, 16, 1024), id128, 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // W = G V^T
-          mma_ss(tbase + kFW, sdesc(ga + k * 32, 16, 1024), sdesc(va + k * 32, 16, 1024), id128, k);
-      }
-      // phi(Q) [S_hi | S_lo]: B = the snapshot, rows d (= K), m contiguous
-      // (MN-major), its hi and lo tiles the two 64-column N blocks (la - ha apart)
-      const uint32_t idO = idesc_bf16(128, 128, false, true);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFO, sdesc(qa + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idO, k);
-      mma_commit(sm.mma_bar);
-      if (CAUSAL) {  // state increment, complete when the second group's barrier is:
-        // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
-        // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
-        const uint32_t idS = idesc_bf16(128, 64, true, true);
-        const uint32_t lbo = kl - ka;
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kFS, sdesc(ka + k * 2048, lbo, 1024), sdesc(va + k * 2048, 1024, 1024), idS, k);
-        mma_commit(&sm.sbar[0]);
-      }
-    }
-    if (!wait_uniform(sm.mma_bar, ph, hdr, 22, wlim)) break;
-    ph ^= 1;
-    fence_after_sync();
+    if (tid < kDim) zrun = src[kDim * kDim + tid];
+    fence_proxy_async_smem();
+  };
 
-    // ---- epilogue: den, G.num, then gd, gN and T_L
-    float wv[32];  // masked W of this thread's slice qc (causal)
-    {
-      float dpart = 0.f, npart = 0.f;
-      if (CAUSAL) {
-        if (qc <= lq) {  // warp-uniform
-          uint32_t rp[32], rw[32];
-          tmem_ld32x2(tl + kFP + 32 * qc, rp, tl + kFW + 32 * qc, rw);
-          if (qc < lq) {  // below the diagonal block: nothing is masked
+  // Hand the MMA warp chunk cc's operands: Z and the state snapshot before the
+  // chunk (a segment's first chunk had its state set up by start_item), phi of its
+  // tiles being in already.
+  auto state_in = [&](const Cursor& c, long long nc) {
+    if (tid < kDim) {
+      if (CAUSAL && !c.first()) zrun += zinc;
+      if (CAUSAL) zinc = (dzk[tid] + dzk[64 + tid]) + (dzk[128 + tid] + dzk[192 + tid]);
+      zsnap[64 * (nc & 1) + tid] = zrun;
+    }
+    if (CAUSAL && !c.first() && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
+    fence_proxy_async_smem();
+    fence_before_sync();  // the previous chunk's TMEM reads, before this chunk's first group
+    warp_arrive(sm.g1_ready);
+  };
+
+  Cursor cc;
+  cc.start(g, true);
+  Cursor cn = cc;  // the chunk after cc
+  cn.advance(g);
+  long long n = 0;
+  bool bad = false;
+  if (cc.valid(g)) {
+    if (warp_wait(&sm.full[0], 0, abort, hdr, 21, wlim)) {
+      phi_stage(0, min(kC, g.N - cc.chunk * kC));
+      start_item(cc.item, cc.bh);
+    } else {
+      bad = true;
+    }
+  }
+  // The loop is left only where all workers agree (a named-barrier reduction of
+  // their failure flags): a warp whose wait ran out skips its work and its
+  // arrivals until the next such point, so that no worker waits at a named
+  // barrier for one that has left.
+  if (!workers_any(bad)) {
+    if (cc.valid(g)) state_in(cc, 0);
+    while (cc.valid(g)) {
+      const int item = cc.item, bh = cc.bh, t0 = cc.chunk * kC;
+      const bool last = cc.last();
+      const int nvalid = min(kC, g.N - t0);
+      const int s = (int)(n & 1);
+      const uint32_t ph = (uint32_t)(n & 1);
+      uint8_t* qt = sm.tile(s, kSQ);
+      uint8_t* kt = sm.tile(s, kSK);
+      uint8_t* vt = sm.tile(s, kSV);
+      uint8_t* gt = sm.tile(s, kSG);
+      uint8_t* klt = sm.tile(s, kSKL);
+      uint8_t* qlt = sm.tile(s, kSQL);
+      const float* zs = zsnap + 64 * s;
+
+      // ---- epilogue of the first group: den, G.num
+      if (!bad && warp_wait(sm.g1_done, ph, abort, hdr, 22)) {
+        fence_after_sync();
+        float dpart = 0.f, npart = 0.f;
+        if (CAUSAL && qc <= lq) {  // warp-uniform; slice qc of P and W in two 16-column halves
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float p = __uint_as_float(rp[c]);
-              wv[c] = __uint_as_float(rw[c]);
-              dpart += p;
-              npart += p * wv[c];
+          for (int h = 0; h < 2; ++h) {
+            uint32_t rp[16], rw[16];
+            tmem_ld16x2(tl + kFP + 32 * qc + 16 * h, rp, tl + kFW + 32 * qc + 16 * h, rw);
+            if (qc < lq) {  // below the diagonal block: nothing is masked
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const float p = __uint_as_float(rp[c]);
+                dpart += p;
+                npart += p * __uint_as_float(rw[c]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const float p = 32 * qc + 16 * h + c <= row ? __uint_as_float(rp[c]) : 0.f;
+                dpart += p;
+                npart += p * __uint_as_float(rw[c]);
+              }
+            }
+          }
+        }
+        {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this quarter. The Z dot
+           // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
+           // the rounding of phi(Q) cancels in num / den.
+          uint32_t ro[16], ro2[16];
+          tmem_ld16x2(tl + kFO + 16 * qc, ro, tl + kFO + 64 + 16 * qc, ro2);
+          float gv[16], qv[16];
+          load_row16(gt, row, 2 * qc, gv);
+          load_row16(qt, row, 2 * qc, qv);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            npart += gv[q] * (__uint_as_float(ro[q]) + __uint_as_float(ro2[q]));
+            dpart += qv[q] * zs[16 * qc + q];
+          }
+        }
+        rsum[qc * 128 + row] = dpart;
+        gnum[qc * 128 + row] = npart;
+        fence_before_sync();
+      } else {
+        bad = true;
+      }
+      if (workers_any(bad)) break;  // partials visible; every read of P and O is done
+      fence_after_sync();
+
+      // ---- gd, gN (into the G and the spent V tiles), T_L (over the spent P)
+      float gd;
+      {
+        const float den = (rsum[row] + rsum[128 + row]) + (rsum[256 + row] + rsum[384 + row]);
+        const float inv = 1.f / den;
+        gd = -((gnum[row] + gnum[128 + row]) + (gnum[256 + row] + gnum[384 + row])) * inv * inv;
+        if (CAUSAL) {  // T_L = W / den + gd (j <= i), bf16 hi + lo
+          uint32_t th[16], tlo[16];
+          if (qc <= lq) {  // warp-uniform: full slice or diagonal slice
+            uint32_t rw[16], rw2[16];
+            tmem_ld16x2(tl + kFW + 32 * qc, rw, tl + kFW + 32 * qc + 16, rw2);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int j0 = 32 * qc + 2 * c;
+              const float w0 = __uint_as_float(c < 8 ? rw[2 * c] : rw2[2 * c - 16]);
+              const float w1 = __uint_as_float(c < 8 ? rw[2 * c + 1] : rw2[2 * c - 15]);
+              split_bf16(qc < lq || j0 <= row ? w0 * inv + gd : 0.f,
+                         qc < lq || j0 + 1 <= row ? w1 * inv + gd : 0.f, th[c], tlo[c]);
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const bool keep = 32 * qc + c <= row;
-              const float p = keep ? __uint_as_float(rp[c]) : 0.f;
-              wv[c] = keep ? __uint_as_float(rw[c]) : 0.f;
-              dpart += p;
-              npart += p * wv[c];
-            }
+            for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
           }
+          tmem_st16(tl + kFT + 16 * qc, th);
+          tmem_st16(tl + kFT + 64 + 16 * qc, tlo);
+        }
+        if (!CAUSAL || warp_wait(sm.ds_done, ph, abort, hdr, 27)) {  // dS has read V
+          float gn[16];
+          load_row16(gt, row, 2 * qc, gn);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) gn[q] *= inv;
+          store_split_quarter(gt, vt, row, qc, gn);
+          fence_proxy_async_smem();
+          fence_before_sync();
+          warp_arrive(sm.g2_ready);
+          if (qc == 0 && row < nvalid) {
+            den_out[(size_t)bh * g.N + t0 + row] = den;
+            gd_out[(size_t)bh * g.N + t0 + row] = gd;
+          }
+          // this chunk's share of r = sum_i gd_i phi(Q_i) (float32 phi = hi + lo)
+          float qv[16], ql[16], z[16];
+          load_row16(qt, row, 2 * qc, qv);
+          load_row16(qlt, row, 2 * qc, ql);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) z[q] = gd * (qv[q] + ql[q]);
+          const float cs = warp_column_sums16(z);
+          if (lane < 16) dzr[lq * 64 + 16 * qc + lane] = cs;
         } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) wv[c] = 0.f;
+          bad = true;
         }
       }
-      {  // G_i . (phi(Q_i) S_prev) and phi(Q_i) . Z_prev over this quarter. The Z dot
-         // uses the same bf16 phi(Q) as the MMAs for P and phi(Q) S_prev, so that
-         // the rounding of phi(Q) cancels in num / den.
-        uint32_t ro[16], ro2[16];
-        tmem_ld16x2(tl + kFO + 16 * qc, ro, tl + kFO + 64 + 16 * qc, ro2);
-        float gv[16], qv[16];
-        load_row16(gt, row, 2 * qc, gv);
-        load_row16(qt, row, 2 * qc, qv);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          npart += gv[q] * (__uint_as_float(ro[q]) + __uint_as_float(ro2[q]));
-          dpart += qv[q] * zsnap[16 * qc + q];
-        }
+
+      // ---- while the second group runs: phi of the next chunk, the state carry
+      if (!bad && cn.valid(g)) {
+        if (warp_wait(&sm.full[s ^ 1], (uint32_t)(((n + 1) >> 1) & 1), abort, hdr, 21, wlim))
+          phi_stage(s ^ 1, min(kC, g.N - cn.chunk * kC));
+        else
+          bad = true;
       }
-      rsum[qc * 128 + row] = dpart;
-      gnum[qc * 128 + row] = npart;
-    }
-    if (CAUSAL && tid < kDim) zrun += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-    sync_tc();  // partials visible; every read of W is done
-    const float den = (rsum[row] + rsum[128 + row]) + (rsum[256 + row] + rsum[384 + row]);
-    const float inv = 1.f / den;
-    const float gd = -((gnum[row] + gnum[128 + row]) + (gnum[256 + row] + gnum[384 + row])) * inv * inv;
-    {
-      float gn[16];
-      load_row16(gt, row, 2 * qc, gn);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) gn[q] *= inv;
-      store_split_quarter(sm.gn_hi, sm.gn_lo, row, qc, gn);
-      if (qc == 0 && row < nvalid) {
-        den_out[(size_t)bh * g.N + t0 + row] = den;
-        gd_out[(size_t)bh * g.N + t0 + row] = gd;
-      }
-      // this chunk's share of r = sum_i gd_i phi(Q_i) (float32 phi = hi + lo)
-      float qv[16], ql[16];
-      load_row16(qt, row, 2 * qc, qv);
-      load_row16(sm.qlo, row, 2 * qc, ql);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) z[q] = gd * (qv[q] + ql[q]);
-      const float cs = warp_column_sums16(z);
-      if (lane < 16) dz[lq * 64 + 16 * qc + lane] = cs;
-    }
-    if (CAUSAL) {  // T_L = W / den + gd (j <= i), bf16 hi + lo over the spent W columns
-      uint32_t th[16], tlo[16];
-      if (qc < lq) {  // warp-uniform: full slice, diagonal slice, or all zero
-#pragma unroll
-        for (int c = 0; c < 16; ++c) split_bf16(wv[2 * c] * inv + gd, wv[2 * c + 1] * inv + gd, th[c], tlo[c]);
-      } else if (qc == lq) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int j0 = 32 * qc + 2 * c;
-          split_bf16(j0 <= row ? wv[2 * c] * inv + gd : 0.f, j0 + 1 <= row ? wv[2 * c + 1] * inv + gd : 0.f,
-                     th[c], tlo[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) th[c] = tlo[c] = 0u;
-      }
-      tmem_st16(tl + kFW + 16 * qc, th);
-      tmem_st16(tl + kFW + 64 + 16 * qc, tlo);
-    }
-    fence_proxy_async_smem();
-    sync_tc();
-    if (tid < kDim) rr += dz[tid] + dz[64 + tid] + dz[128 + tid] + dz[192 + tid];
-    if (tid == 0) {
-      const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), ql = smem_u32(sm.qlo);
-      const uint32_t kl = smem_u32(sm.klo);
-      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
-      const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
-      // dphiQ = T_L phi(K) + gN S_prev^T with the hi*hi + hi*lo + lo*hi terms of
-      // each product; the hi*lo partners share their A operand, so they sit side by
-      // side in one N = 128 instruction, and dphiQ is the sum of the accumulator's
-      // two 64-column halves (columns [64, 128) carry only the hi*lo terms)
-      const uint32_t idQ2 = idesc_bf16(128, 128, false, true), idQ = idesc_bf16(128, 64, false, true);
-      if (CAUSAL) {
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // T_hi [phi(K)_hi | phi(K)_lo] (N blocks kl - ka apart)
-          mma_ts(tbase + kFQ, tbase + kFW + k * 8, sdesc(ka + k * 2048, kl - ka, 1024), idQ2, k);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // T_lo phi(K)_hi
-          mma_ts(tbase + kFQ, tbase + kFW + 64 + k * 8, sdesc(ka + k * 2048, 1024, 1024), idQ, 1);
-      }
-      // B = the snapshot, rows d (= N), m contiguous (K-major): the S_lo rows follow
-      // the S_hi rows, so gN_hi [S_hi; S_lo]^T is one N = 128 product
-      const uint32_t idQs2 = idesc_bf16(128, 128, false, false), idQs = idesc_bf16(128, 64, false, false);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gha + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs2,
-               (CAUSAL || k > 0) ? 1u : 0u);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tbase + kFQ, sdesc(gla + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idQs, 1);
-      mma_commit(sm.mma_bar);
-      // segment sum of phi(Q)^T gN, awaited at the chunk's end: phi(Q)^T hi and
-      // lo stacked as one M = 128 MN-major operand (the two 64-row halves are
-      // the hi and lo tiles, ql - qa bytes apart), times gN hi, then gN lo; the
-      // hi-row and lo-row halves (TMEM lanes 0-63 / 64-127) are summed at the
-      // segment's end
-      const uint32_t idR = idesc_bf16(128, 64, true, true);
-      const uint32_t lbo = ql - qa;
-#pragma unroll
-      for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024), idR,
-               (first && k == 0) ? 0u : 1u);
-#pragma unroll
-      for (int k = 0; k < kC / 16; ++k)
-        mma_ss(tbase + kFR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024), idR,
-               1);
-      mma_commit(&sm.sbar[1]);
-    }
-    if (CAUSAL) {  // S += dS while the second group runs: the lo-part rows pass
-                   // through the chunk's V tile (no MMA reads it any more)
-      if (!wait_uniform(&sm.sbar[0], sph0, hdr, 27, wlim)) break;
-      sph0 ^= 1;
-      fence_after_sync();
-      uint32_t r[16];
-      tmem_ld16(tl + kFS + 16 * qc, r);
+      // the V tile (gN lo) is free once the segment sums have read it: the lo-part
+      // rows of dS pass through it to the carry's threads
       float4* xs = reinterpret_cast<float4*>(vt);  // [64][16] float4, XOR-swizzled rows
-      if (!dthread) {
+      if (!bad) {
+        if (warp_wait(sm.gn_free, ph, abort, hdr, 28)) {
+          fence_after_sync();
+          if (CAUSAL && !last && !dthread) {
+            uint32_t r[16];
+            tmem_ld16(tl + kFS + 16 * qc, r);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            for (int j = 0; j < 4; ++j)
+              xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
+                  make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+          // the next segment's starting state (the snapshot is no MMA's operand now)
+          if (last && cn.valid(g)) start_item(cn.item, cn.bh);
+        } else {
+          bad = true;
+        }
       }
-      __syncthreads();
-      if (dthread) {
+      if (workers_any(bad)) break;
+      if (tid < kDim) rr += (dzr[tid] + dzr[64 + tid]) + (dzr[128 + tid] + dzr[192 + tid]);
+      if (CAUSAL && !last && dthread) {  // S += dS (hi rows from TMEM, lo rows exchanged)
+        uint32_t r[16];
+        tmem_ld16(tl + kFS + 16 * qc, r);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
@@ -536,87 +718,120 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
         }
       }
-      fence_proxy_async_smem();  // the V tile is a TMA destination again
-    }
-    if (!wait_uniform(sm.mma_bar, ph, hdr, 24, wlim)) break;
-    ph ^= 1;
-    fence_after_sync();
+      // the next chunk's first group can start (it waits for dphiQ's reads below
+      // only before phi(Q) S_prev)
+      if (cn.valid(g)) state_in(cn, n + 1);
 
-    // dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this quarter's
-    // columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for TMA stores in
-    // the chunk's spent K and G tiles (quarters 0, 1: K tile; 2, 3: G tile)
-    {
-      uint32_t r[16], r2[16];
-      tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
-      float qv[16], o[16];
-      load_row16(qt, row, 2 * qc, qv);
+      // ---- dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this
+      // quarter's columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for
+      // TMA stores in the chunk's spent K and phi(K) lo tiles
+      if (warp_wait(sm.g2_done, ph, abort, hdr, 24)) {
+        fence_after_sync();
+        uint32_t r[16], r2[16];
+        tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
+        fence_before_sync();
+        warp_arrive(sm.dq_read);
+        float qv[16], o[16];
+        load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zsnap[16 * qc + q]) *
-               fminf(qv[q], 1.f);
-      uint8_t* sq = qc < 2 ? kt : gt;
+        for (int q = 0; q < 16; ++q)
+          o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zs[16 * qc + q]) * fminf(qv[q], 1.f);
+        uint8_t* sq = qc < 2 ? kt : klt;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<float4*>(sq + sw128(row, (qc & 1) * 64 + c * 16)) =
-            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    }
-    fence_proxy_async_smem();
-    sync_tc();
-    if (tma_thread) {  // rows past the sequence end are clipped by the tensor map
-      tma_store_3d(&tm_dq, kt, 0, t0, bh);
-      tma_store_3d(&tm_dq, gt, 32, t0, bh);
-      bulk_commit();
-    }
-    r_pending = true;  // the segment sums of phi(Q)^T gN, issued after the second group
-    if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
-      if (!wait_uniform(&sm.sbar[1], sph1, hdr, 28, wlim)) break;
-      sph1 ^= 1;
-      r_pending = false;
-      fence_after_sync();
-      // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
-      // part for lq >= 2; the lo parts pass through the spent gN hi buffer
-      float* dst = rpartial + (size_t)item * kStateFloats;
-      uint32_t r[16];
-      tmem_ld16(tl + kFR + 16 * qc, r);
-      float4* xs = reinterpret_cast<float4*>(sm.gn_hi);  // [64][16] float4, XOR-swizzled rows
-      const int d = drow;
-      if (lq >= 2) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          xs[d * 16 + ((4 * qc + j) ^ (d & 15))] =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<float4*>(sq + sw128(row, (qc & 1) * 64 + c * 16)) =
+              make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        fence_proxy_async_smem();
+        if (!last) warp_arrive(sm.st_ready);
+      } else {
+        bad = true;
       }
-      __syncthreads();
-      if (lq < 2) {
-        float4* d4 = reinterpret_cast<float4*>(dst + d * kDim + 16 * qc);
+      if (last) {  // segment partial: R = sum phi(Q)^T gN (rows d), r
+        // lane 32 lq + lane holds row d = 32 (lq % 2) + lane: hi part for lq < 2, lo
+        // part for lq >= 2; the lo parts pass through the spent G tile
+        float4* xr = reinterpret_cast<float4*>(gt);
+        uint32_t r[16];
+        if (!bad) {
+          tmem_ld16(tl + kFR + 16 * qc, r);
+          if (!dthread) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 lo = xs[d * 16 + ((4 * qc + j) ^ (d & 15))];
-          d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
-                              __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
+            for (int j = 0; j < 4; ++j)
+              xr[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
+                  make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
         }
+        if (workers_any(bad)) break;
+        float* dst = rpartial + (size_t)item * kStateFloats;
+        if (dthread) {
+          float4* d4 = reinterpret_cast<float4*>(dst + drow * kDim + 16 * qc);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 lo = xr[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
+            d4[j] = make_float4(__uint_as_float(r[4 * j]) + lo.x, __uint_as_float(r[4 * j + 1]) + lo.y,
+                                __uint_as_float(r[4 * j + 2]) + lo.z, __uint_as_float(r[4 * j + 3]) + lo.w);
+          }
+        }
+        if (tid < kDim) {
+          dst[kDim * kDim + tid] = rr;
+          rr = 0.f;
+        }
+        warp_arrive(sm.st_ready);  // the G tile too is done with now
       }
-      if (tid < kDim) dst[kDim * kDim + tid] = rr;
-      fence_proxy_async_smem();  // the gN buffer is an MMA operand again next chunk
-      sync_tc();  // every read of the exchange is done before gN hi is rewritten
+      ++n;
+      cc = cn;
+      cn.advance(g);
     }
-    ++consumed;
-    cc.advance(g);
+  }
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kWsThreads, 1)
+tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                const __grid_constant__ CUtensorMap tm_dq, Geometry g,
+                const float* __restrict__ sprefix, float* __restrict__ rpartial,
+                float* __restrict__ den_out, float* __restrict__ gd_out, WorkspaceHeader* hdr) {
+  extern __shared__ uint8_t smraw[];
+  QSmem sm(smraw);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (tid == 0) {
+    mbar_init(&sm.full[0], 1);
+    mbar_init(&sm.full[1], 1);
+    mbar_init(sm.g1_ready, kWorkers / 32);
+    mbar_init(sm.g2_ready, kWorkers / 32);
+    mbar_init(sm.st_ready, kWorkers / 32);
+    mbar_init(sm.g1_done, 1);
+    mbar_init(sm.ds_done, 1);
+    mbar_init(sm.gn_free, 1);
+    mbar_init(sm.g2_done, 1);
+    mbar_init(sm.dq_read, kWorkers / 32);
+    mbar_init(sm.drain, 1);
+    *sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sm.tslot, 512);
+    tmem_relinquish();
+  }
+  sync_tc();
+  const uint32_t tbase = *sm.tslot;
+  pdl_wait();
+  volatile int* abort = sm.abort;
+  if (warp >= kWorkers / 32) {
+    regs_dec<kControlRegs>();
+    if (lane == 0) {
+      if (warp == kMmaWarp)
+        bwd_q_mma<CAUSAL>(sm, g, tbase, abort, hdr);
+      else if (warp == kTmaWarp)
+        bwd_q_tma<CAUSAL>(sm, g, &tm_q, &tm_k, &tm_v, &tm_g, &tm_dq, abort, hdr);
+    }
+    __syncwarp();
+  } else {
+    regs_inc<kWorkerRegs>();
+    bwd_q_workers<CAUSAL>(sm, g, tbase, abort, sprefix, rpartial, den_out, gd_out, hdr);
   }
   pdl_trigger();
-  if (r_pending && tid == 0 && !mbar_wait(&sm.sbar[1], sph1)) record_timeout(hdr, 29);
-  if (tma_thread) {
-    while (consumed < issued) {
-      const int s = consumed % kBwdStages;
-      if (!(g.faulty() && consumed == g.fault_load) &&
-          !mbar_wait(&sm.full[s], (consumed / kBwdStages) & 1))
-        record_timeout(hdr, 26);
-      ++consumed;
-    }
-    bulk_wait_all<0>();
-  }
-  drain_mmas(sm.drain, hdr, 25);
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
@@ -1079,10 +1294,10 @@ cudaError_t tc_backward_q(const void* q, const void* k, const void* v, const voi
     sprefix = w.sprefix;
   }
   auto run_q = [&](auto kern) {
-    cudaError_t err = configure(kern, kBwdSmem);
+    cudaError_t err = configure(kern, kQSmem);
     if (err != cudaSuccess) return err;
-    const int ctas = min(g.n_items(), resident_ctas(kern, kBwdSmem, kBTQ) * sm_count());
-    err = launch_pdl(kern, dim3(ctas), dim3(kBTQ), kBwdSmem, st, tq, tk, tv, tg, tdq, gq,
+    const int ctas = min(g.n_items(), resident_ctas(kern, kQSmem, kWsThreads) * sm_count());
+    err = launch_pdl(kern, dim3(ctas), dim3(kWsThreads), kQSmem, st, tq, tk, tv, tg, tdq, gq,
                      sprefix, w.rpartial, w.den, w.gd, w.hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
