@@ -37,6 +37,7 @@ namespace la {
 namespace tcx {
 namespace {
 
+// Shared memory of the reverse-direction (dk, dv) kernel.
 constexpr int kBwdStages = 2;
 constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows each
 constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
@@ -101,11 +102,12 @@ struct BwdSmem {
 
 enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 
-// Both kernels run 512 threads: warp w covers TMEM lane quarter w % 4 (rows
-// 32 (w % 4) .. + 31) and column quarter qc = w / 4 (16 of the 64 state
-// columns, the 32-column slice qc of the chunk's 128), so every row is handled
-// by four threads. Where a TMEM region is compacted in place (fp32 P into bf16
-// P_L), all reads finish before a barrier and the writes follow it.
+// The reverse-direction kernel runs 512 threads: warp w covers TMEM lane quarter
+// w % 4 (rows 32 (w % 4) .. + 31) and column quarter qc = w / 4 (16 of the 64
+// state columns, the 32-column slice qc of the chunk's 128), so every row is
+// handled by four threads; thread 0 issues its MMAs. Where a TMEM region is
+// compacted in place (fp32 P into bf16 P_L), all reads finish before a barrier
+// and the writes follow it.
 constexpr int kBTQ = 512;
 
 // Quarter-row store of x[16] (columns [16 qc, 16 qc + 16)) as bf16 hi and lo rows.
@@ -193,7 +195,7 @@ __device__ __forceinline__ void sync_tc() {
 constexpr int kWorkers = 512;
 constexpr int kWsThreads = kWorkers + 128;
 constexpr int kMmaWarp = 16, kTmaWarp = 17;
-constexpr int kWorkerRegs = 104, kControlRegs = 64;  // 512 x 104 + 128 x 64 = 640 x 96
+constexpr int kWorkerRegs = 112, kControlRegs = 32;  // 512 x 112 + 128 x 32 = 640 x 96
 
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -248,37 +250,61 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// D[tmem] (+)= A[smem] * B[smem] with each descriptor given as its two 32-bit
-// halves: stepping through K then changes only the low half (the start
-// address >> 4, far below its 14-bit limit here), one add per operand.
-__device__ __forceinline__ void mma_ss_h(uint32_t d, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
-                                         uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+// Shared-memory descriptors as their low 32 bits (start address >> 4, leading
+// byte offset >> 4): every operand here has a 1024-byte stride offset and the
+// 128-byte swizzle, which make up the high half, the same for all of them.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);  // bits 32..63 of sdesc_lo(., .)
+
+// D[tmem] (+)= A[smem] * B[smem] from the descriptors' low halves plus constant
+// offsets (in 16-byte units), added inside the instruction sequence so that an
+// unrolled run of MMAs keeps only its base descriptors in registers.
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ss_l(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 ra, rb;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %5, p;\n\t}" ::"r"(d),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tadd.u32 al, %1, %6;\n\tadd.u32 bl, %2, %7;\n\t"
+      "mov.b64 ra, {al, %5};\n\tmov.b64 rb, {bl, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p;\n\t}" ::"r"(d),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+
+// The same with A in TMEM (its address offset also added in place).
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ts_l(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 rb;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tadd.u32 at, %1, %6;\n\tadd.u32 bl, %2, %7;\n\t"
+      "mov.b64 rb, {bl, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], rb, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi), "n"(AOFF), "n"(BOFF)
       : "memory");
 }
 
 // N MMAs over consecutive K = 16 slices, the descriptors advanced by AS / BS
 // bytes per slice (32 inside a K-major swizzle atom, 2048 = 16 rows of an
 // MN-major tile); acc0: whether the first one accumulates.
-template <int N, uint32_t AS, uint32_t BS>
-__device__ __forceinline__ void mma_run(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+template <int N, uint32_t AS, uint32_t BS, int K = 0>
+__device__ __forceinline__ void mma_run(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
                                         uint32_t acc0) {
-  const uint32_t alo = (uint32_t)a, ahi = (uint32_t)(a >> 32);
-  const uint32_t blo = (uint32_t)b, bhi = (uint32_t)(b >> 32);
-#pragma unroll
-  for (int k = 0; k < N; ++k)
-    mma_ss_h(d, alo + k * (AS >> 4), ahi, blo + k * (BS >> 4), bhi, idesc, k == 0 ? acc0 : 1u);
+  if constexpr (K < N) {
+    mma_ss_l<K * (AS >> 4), K * (BS >> 4)>(d, a_lo, b_lo, idesc, K == 0 ? acc0 : 1u);
+    mma_run<N, AS, BS, K + 1>(d, a_lo, b_lo, idesc, acc0);
+  }
 }
 
 // The same with A in TMEM (8 columns of packed bf16 per slice), accumulating.
-template <int N, uint32_t BS>
-__device__ __forceinline__ void mma_run_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
-#pragma unroll
-  for (int k = 0; k < N; ++k) mma_ts(d, a_tmem + 8 * k, b + k * (BS >> 4), idesc, 1u);
+template <int N, uint32_t BS, int K = 0>
+__device__ __forceinline__ void mma_run_ts(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc) {
+  if constexpr (K < N) {
+    mma_ts_l<8 * K, K * (BS >> 4)>(d, a_tmem, b_lo, idesc, 1u);
+    mma_run_ts<N, BS, K + 1>(d, a_tmem, b_lo, idesc);
+  }
 }
 
 // --------------------------------------------------- forward direction: dq
@@ -300,7 +326,8 @@ constexpr uint32_t kFO = 256;   // 128: phi(Q) S_prev as phi(Q) S_hi (0..63) and
                                 // after the first epilogue, dphiQ as two 64-column parts (kFQ)
 constexpr uint32_t kFT = 0;
 constexpr uint32_t kFQ = 256;
-constexpr uint32_t kFS = 384;   // 64: dS, M = 128 layout (rows d: hi part lanes 0-63, lo 64-127)
+constexpr uint32_t kFS = 384;   // 64: the S carry, M = 128 layout (rows d: prefix + hi parts in
+                                // lanes 0-63, lo parts in 64-127)
 constexpr uint32_t kFR = 448;   // 64: segment sum of phi(Q)^T gN (M = 128 layout, like dS)
 
 // A stage holds one chunk: the loaded Q, K, V, G tiles (phi applied to Q and K
@@ -310,47 +337,38 @@ enum { kSQ = 0, kSK = 1, kSV = 2, kSG = 3, kSKL = 4, kSQL = 5, kQStageTiles = 6 
 constexpr int kQArr = 1664;  // floats: Z snapshots, column sums, den / G.num partials
 constexpr int kQSmem = 1024 + 2 * kQStageTiles * kTile + 2 * kDim * 128 + kQArr * 4 + 128;
 
+// Addresses from one aligned base and constant offsets, so that a role keeps a
+// single pointer live instead of one per buffer.
 struct QSmem {
-  uint8_t* stages;
-  uint8_t* s_hi;  // state snapshot S_prev as bf16 hi and lo, rows d, m contiguous
-  uint8_t* s_lo;
-  float* arr;
-  uint64_t* full;      // [2] a stage's tiles landed
-  uint64_t* g1_ready;  // the workers' operands of the first group are in (16 warps)
-  uint64_t* g2_ready;  // ... of the second group
-  uint64_t* st_ready;  // the chunk's dq is staged, and the workers are done with its stage
-  uint64_t* g1_done;   // P, W, phi(Q) S_prev
-  uint64_t* ds_done;   // dS (the last reader of V)
-  uint64_t* gn_free;   // gN S_prev^T and the segment sums (the last readers of the gN tiles,
-                       // the snapshot and the phi(Q) tiles)
-  uint64_t* g2_done;   // dphiQ
-  uint64_t* dq_read;   // the workers have read dphiQ (16 warps)
-  uint64_t* drain;     // every MMA of the CTA is done (end of the kernel)
-  int* abort;
-  uint32_t* tslot;
-  __device__ explicit QSmem(uint8_t* raw) {
-    uint8_t* sm =
-        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-    stages = sm;
-    s_hi = sm + 2 * kQStageTiles * kTile;
-    s_lo = s_hi + kDim * 128;
-    arr = reinterpret_cast<float*>(s_lo + kDim * 128);
-    uint64_t* b = reinterpret_cast<uint64_t*>(arr + kQArr);
-    full = b;
-    g1_ready = b + 2;
-    g2_ready = b + 3;
-    st_ready = b + 4;
-    g1_done = b + 5;
-    ds_done = b + 6;
-    gn_free = b + 7;
-    g2_done = b + 8;
-    dq_read = b + 9;
-    drain = b + 10;
-    abort = reinterpret_cast<int*>(b + 11);
-    tslot = reinterpret_cast<uint32_t*>(b + 11) + 1;
-  }
-  __device__ uint8_t* tile(int s, int which) { return stages + (s * kQStageTiles + which) * kTile; }
+  static constexpr int kSnap = 2 * kQStageTiles * kTile;  // S_prev as bf16 hi, then lo (rows d)
+  static constexpr int kArrOff = kSnap + 2 * kDim * 128;
+  static constexpr int kBarOff = kArrOff + kQArr * 4;
+  enum {
+    kFull = 0,     // [2] a stage's tiles landed
+    kG1Ready = 2,  // the workers' operands of the first group are in (16 warps)
+    kG2Ready,      // ... of the second group
+    kStReady,      // the chunk's dq is staged, and the workers are done with its stage
+    kG1Done,       // P, W, phi(Q) S_prev
+    kDsDone,       // dS (the last reader of V)
+    kGnFree,       // gN S_prev^T and the segment sums (the last readers of the gN tiles,
+                   // the snapshot and the phi(Q) tiles)
+    kG2Done,       // dphiQ
+    kDqRead,       // the workers have read dphiQ (16 warps)
+    kDrain,        // every MMA of the CTA is done (end of the kernel)
+    kNBars
+  };
+  uint8_t* base;
+  __device__ explicit QSmem(uint8_t* raw)
+      : base(reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023))) {}
+  __device__ uint8_t* tile(int s, int which) const { return base + (s * kQStageTiles + which) * kTile; }
+  __device__ uint8_t* s_hi() const { return base + kSnap; }
+  __device__ uint8_t* s_lo() const { return base + kSnap + kDim * 128; }
+  __device__ float* arr() const { return reinterpret_cast<float*>(base + kArrOff); }
+  __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kBarOff) + i; }
+  __device__ int* abort() const { return reinterpret_cast<int*>(bar(kNBars)); }
+  __device__ uint32_t* tslot() const { return reinterpret_cast<uint32_t*>(bar(kNBars)) + 1; }
 };
+static_assert(QSmem::kBarOff + QSmem::kNBars * 8 + 8 <= kQSmem - 1024, "dq kernel shared memory");
 
 // MMA warp, one thread: per chunk the first group once the workers' phi and
 // snapshot are in, the second once gN and T_L are.
@@ -359,7 +377,7 @@ __device__ __forceinline__ void bwd_q_mma(QSmem& sm, const Geometry& g, uint32_t
                                           volatile int* abort, WorkspaceHeader* hdr) {
   Cursor c;
   c.start(g, true);
-  const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
+  const uint32_t ha = smem_u32(sm.s_hi()), la = smem_u32(sm.s_lo());
   long long n = 0;
   while (c.valid(g)) {
     const int s = (int)(n & 1);
@@ -367,69 +385,69 @@ __device__ __forceinline__ void bwd_q_mma(QSmem& sm, const Geometry& g, uint32_t
     const uint32_t qa = smem_u32(sm.tile(s, kSQ)), ka = smem_u32(sm.tile(s, kSK));
     const uint32_t va = smem_u32(sm.tile(s, kSV)), ga = smem_u32(sm.tile(s, kSG));
     const uint32_t kl = smem_u32(sm.tile(s, kSKL)), ql = smem_u32(sm.tile(s, kSQL));
-    if (!role_wait(sm.g1_ready, ph, abort, hdr, 41, kWaitLimitNs)) break;
+    if (!role_wait(sm.bar(QSmem::kG1Ready), ph, abort, hdr, 41, kWaitLimitNs)) break;
     // P overwrites the previous chunk's T_L: its second group must be done
-    if (n > 0 && !role_wait(sm.g2_done, ph ^ 1, abort, hdr, 44, kWaitLimitNs)) break;
+    if (n > 0 && !role_wait(sm.bar(QSmem::kG2Done), ph ^ 1, abort, hdr, 44, kWaitLimitNs)) break;
     fence_after_sync();
     // K-major operands step 32 bytes per K = 16 slice (inside the swizzle atom),
     // MN-major ones 2048 bytes (16 rows of 128 bytes)
     if (CAUSAL) {
       const uint32_t id128 = idesc_bf16(128, 128, false, false);
       // P = phi(Q) (phi(K)_hi + phi(K)_lo)^T, W = G V^T
-      mma_run<4, 32, 32>(tbase + kFP, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), id128, 0);
-      mma_run<4, 32, 32>(tbase + kFP, sdesc(qa, 16, 1024), sdesc(kl, 16, 1024), id128, 1);
-      mma_run<4, 32, 32>(tbase + kFW, sdesc(ga, 16, 1024), sdesc(va, 16, 1024), id128, 0);
+      mma_run<4, 32, 32>(tbase + kFP, sdesc_lo(qa, 16), sdesc_lo(ka, 16), id128, 0);
+      mma_run<4, 32, 32>(tbase + kFP, sdesc_lo(qa, 16), sdesc_lo(kl, 16), id128, 1);
+      mma_run<4, 32, 32>(tbase + kFW, sdesc_lo(ga, 16), sdesc_lo(va, 16), id128, 0);
     }
     // phi(Q) S_prev overwrites the previous chunk's dphiQ: the workers must have read it
-    if (n > 0 && !role_wait(sm.dq_read, ph ^ 1, abort, hdr, 45, kWaitLimitNs)) break;
+    if (n > 0 && !role_wait(sm.bar(QSmem::kDqRead), ph ^ 1, abort, hdr, 45, kWaitLimitNs)) break;
     fence_after_sync();
     // phi(Q) [S_hi | S_lo]: B = the snapshot, rows d (= K), m contiguous
     // (MN-major), its hi and lo tiles the two 64-column N blocks (la - ha apart)
-    mma_run<4, 32, 2048>(tbase + kFO, sdesc(qa, 16, 1024), sdesc(ha, la - ha, 1024),
+    mma_run<4, 32, 2048>(tbase + kFO, sdesc_lo(qa, 16), sdesc_lo(ha, la - ha),
                          idesc_bf16(128, 128, false, true), 0);
-    mma_commit(sm.g1_done);
-    if (CAUSAL) {  // dS = phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
+    mma_commit(sm.bar(QSmem::kG1Done));
+    if (CAUSAL) {  // S += phi(K)^T V with phi(K)^T hi and lo stacked as one M = 128
                    // MN-major operand (kl - ka bytes apart); hi rows in lanes 0-63, lo 64-127
-      mma_run<kC / 16, 2048, 2048>(tbase + kFS, sdesc(ka, kl - ka, 1024), sdesc(va, 1024, 1024),
-                                   idesc_bf16(128, 64, true, true), 0);
-      mma_commit(sm.ds_done);
+      mma_run<kC / 16, 2048, 2048>(tbase + kFS, sdesc_lo(ka, kl - ka), sdesc_lo(va, 1024),
+                                   idesc_bf16(128, 64, true, true), 1);
+      mma_commit(sm.bar(QSmem::kDsDone));
     }
-    if (!role_wait(sm.g2_ready, ph, abort, hdr, 42, kWaitLimitNs)) break;
+    if (!role_wait(sm.bar(QSmem::kG2Ready), ph, abort, hdr, 42, kWaitLimitNs)) break;
     fence_after_sync();
     // gN [S_hi; S_lo]^T + gN_lo S_hi^T first: B = the snapshot, rows d (= N), m
     // contiguous (K-major), the S_lo rows after the S_hi rows (one N = 128
     // product); gN hi sits in the G tile, gN lo in the V tile. dphiQ is the sum
     // of the accumulator's two 64-column halves.
     const uint32_t gha = ga, gla = va;
-    mma_run<4, 32, 32>(tbase + kFQ, sdesc(gha, 16, 1024), sdesc(ha, 16, 1024),
+    mma_run<4, 32, 32>(tbase + kFQ, sdesc_lo(gha, 16), sdesc_lo(ha, 16),
                        idesc_bf16(128, 128, false, false), 0);
-    mma_run<4, 32, 32>(tbase + kFQ, sdesc(gla, 16, 1024), sdesc(ha, 16, 1024),
+    mma_run<4, 32, 32>(tbase + kFQ, sdesc_lo(gla, 16), sdesc_lo(ha, 16),
                        idesc_bf16(128, 64, false, false), 1);
     // segment sum of phi(Q)^T gN: phi(Q)^T hi and lo stacked as one M = 128
     // MN-major operand (ql - qa bytes apart) times gN hi, then gN lo; the hi-row
     // and lo-row halves (TMEM lanes 0-63 / 64-127) are summed at the segment's end
     const uint32_t idR = idesc_bf16(128, 64, true, true);
-    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc(qa, ql - qa, 1024), sdesc(gha, 1024, 1024), idR,
+    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc_lo(qa, ql - qa), sdesc_lo(gha, 1024), idR,
                                  c.first() ? 0u : 1u);
-    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc(qa, ql - qa, 1024), sdesc(gla, 1024, 1024), idR, 1);
-    mma_commit(sm.gn_free);
+    mma_run<kC / 16, 2048, 2048>(tbase + kFR, sdesc_lo(qa, ql - qa), sdesc_lo(gla, 1024), idR, 1);
+    mma_commit(sm.bar(QSmem::kGnFree));
     if (CAUSAL) {
       // + T_L phi(K) with the hi*hi + hi*lo + lo*hi terms; the hi*lo partners share
       // their A operand (T_L in TMEM, 8 columns per K = 16 slice), so they sit side
       // by side in one N = 128 instruction: T_hi [phi(K)_hi | phi(K)_lo] (N blocks
       // kl - ka apart), then T_lo phi(K)_hi
-      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT, sdesc(ka, kl - ka, 1024),
+      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT, sdesc_lo(ka, kl - ka),
                                 idesc_bf16(128, 128, false, true));
-      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT + 64, sdesc(ka, 1024, 1024),
+      mma_run_ts<kC / 16, 2048>(tbase + kFQ, tbase + kFT + 64, sdesc_lo(ka, 1024),
                                 idesc_bf16(128, 64, false, true));
     }
-    mma_commit(sm.g2_done);
+    mma_commit(sm.bar(QSmem::kG2Done));
     ++n;
     c.advance(g);
   }
   // every MMA completes before the CTA frees TMEM (time-bounded only)
-  mma_commit(sm.drain);
-  if (!mbar_wait(sm.drain, 0)) record_timeout(hdr, 25);
+  mma_commit(sm.bar(QSmem::kDrain));
+  if (!mbar_wait(sm.bar(QSmem::kDrain), 0)) record_timeout(hdr, 25);
 }
 
 // TMA warp, one thread: loads two chunks ahead of the workers, stores each
@@ -448,12 +466,12 @@ __device__ __forceinline__ void bwd_q_tma(QSmem& sm, const Geometry& g, const CU
     const int s = (int)(nl & 1);
     if (!(g.faulty() && nl == g.fault_load)) {  // test hook: this load is withheld
       const int t0 = cl.chunk * kC;
-      mbar_arrive_expect_tx(&sm.full[s], tx);
-      tma_load_3d(sm.tile(s, kSQ), tm_q, &sm.full[s], 0, t0, cl.bh);
-      tma_load_3d(sm.tile(s, kSG), tm_g, &sm.full[s], 0, t0, cl.bh);
+      mbar_arrive_expect_tx(sm.bar(QSmem::kFull + (s)), tx);
+      tma_load_3d(sm.tile(s, kSQ), tm_q, sm.bar(QSmem::kFull + (s)), 0, t0, cl.bh);
+      tma_load_3d(sm.tile(s, kSG), tm_g, sm.bar(QSmem::kFull + (s)), 0, t0, cl.bh);
       if (CAUSAL) {
-        tma_load_3d(sm.tile(s, kSK), tm_k, &sm.full[s], 0, t0, cl.bh);
-        tma_load_3d(sm.tile(s, kSV), tm_v, &sm.full[s], 0, t0, cl.bh);
+        tma_load_3d(sm.tile(s, kSK), tm_k, sm.bar(QSmem::kFull + (s)), 0, t0, cl.bh);
+        tma_load_3d(sm.tile(s, kSV), tm_v, sm.bar(QSmem::kFull + (s)), 0, t0, cl.bh);
       }
     }
     ++nl;
@@ -462,7 +480,7 @@ __device__ __forceinline__ void bwd_q_tma(QSmem& sm, const Geometry& g, const CU
   while (nl < 2 && cl.valid(g)) load();
   while (cs.valid(g)) {
     const int s = (int)(ns & 1);
-    if (!role_wait(sm.st_ready, (uint32_t)(ns & 1), abort, hdr, 43, kWaitLimitNs)) break;
+    if (!role_wait(sm.bar(QSmem::kStReady), (uint32_t)(ns & 1), abort, hdr, 43, kWaitLimitNs)) break;
     // rows past the sequence end are clipped by the tensor map
     tma_store_3d(tm_dq, sm.tile(s, kSK), 0, cs.chunk * kC, cs.bh);
     tma_store_3d(tm_dq, sm.tile(s, kSKL), 32, cs.chunk * kC, cs.bh);
@@ -477,7 +495,7 @@ __device__ __forceinline__ void bwd_q_tma(QSmem& sm, const Geometry& g, const CU
   // every issued load lands and every store completes before the CTA lets go of
   // its shared memory (time-bounded only)
   for (long long k = ns; k < nl; ++k)
-    if (!(g.faulty() && k == g.fault_load) && !mbar_wait(&sm.full[k & 1], (uint32_t)((k >> 1) & 1)))
+    if (!(g.faulty() && k == g.fault_load) && !mbar_wait(sm.bar(QSmem::kFull + (k & 1)), (uint32_t)((k >> 1) & 1)))
       record_timeout(hdr, 26);
   bulk_wait_all<0>();
 }
@@ -495,11 +513,11 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
   const bool dthread = lq < 2;
   const uint32_t tl = lane_base(tbase);
   const uint64_t wlim = g.wait_ns();  // tile waits (shortened only by the test hook)
-  float* zsnap = sm.arr;        // [2][64]: Z before the chunk, by chunk parity
-  float* dzk = sm.arr + 128;    // [4][64]: column sums of the prepared chunk's phi(K)
-  float* dzr = sm.arr + 384;    // [4][64]: the chunk's column sums of gd phi(Q)
-  float* rsum = sm.arr + 640;   // [4][128]: quarter-row parts of den
-  float* gnum = sm.arr + 1152;  // [4][128]: quarter-row parts of G . num
+  float* zsnap = sm.arr();        // [2][64]: Z before the chunk, by chunk parity
+  float* dzk = sm.arr() + 128;    // [4][64]: column sums of the prepared chunk's phi(K)
+  float* dzr = sm.arr() + 384;    // [4][64]: the chunk's column sums of gd phi(Q)
+  float* rsum = sm.arr() + 640;   // [4][128]: quarter-row parts of den
+  float* gnum = sm.arr() + 1152;  // [4][128]: quarter-row parts of G . num
 
   // phi of a stage's tiles in place, the rounding errors into the lo tiles
   auto phi_stage = [&](int s, int nvalid) {
@@ -512,15 +530,27 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
     phi_quarter_split(sm.tile(s, kSQ), sm.tile(s, kSQL), row, qc, kC, z);
     fence_proxy_async_smem();
   };
-  float srun[16];             // S row drow, columns m in [16 qc, 16 qc + 16) (dthread)
   float zrun = 0.f, zinc = 0.f, rr = 0.f;  // Z[d], the chunk's phi(K) column sums, r[d] (tid < 64)
-  // the state a segment starts from: carry and snapshot
+  // The state a segment starts from: the snapshot, and the carry. The carry is the
+  // dS accumulator itself: the dS MMAs of a segment add into it, its hi-part rows
+  // (TMEM lanes 0-63, row d = drow) seeded with the prefix and its lo-part rows
+  // (lanes 64-127) with zeros, so that S before a chunk is the sum of the two.
   auto start_item = [&](int item, int bh) {
     const float* src = sprefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
+    float v[16];
     if (dthread) {  // the prefix is S^T [m][d]: column drow, rows m of this quarter
 #pragma unroll
-      for (int j = 0; j < 16; ++j) srun[j] = src[(16 * qc + j) * kDim + drow];
-      store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
+      for (int j = 0; j < 16; ++j) v[j] = src[(16 * qc + j) * kDim + drow];
+      store_split_quarter(sm.s_hi(), sm.s_lo(), drow, qc, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    }
+    if (CAUSAL) {
+      uint32_t u[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(v[j]);
+      tmem_st16(tl + kFS + 16 * qc, u);
     }
     if (tid < kDim) zrun = src[kDim * kDim + tid];
     fence_proxy_async_smem();
@@ -535,10 +565,8 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       if (CAUSAL) zinc = (dzk[tid] + dzk[64 + tid]) + (dzk[128 + tid] + dzk[192 + tid]);
       zsnap[64 * (nc & 1) + tid] = zrun;
     }
-    if (CAUSAL && !c.first() && dthread) store_split_quarter(sm.s_hi, sm.s_lo, drow, qc, srun);
-    fence_proxy_async_smem();
     fence_before_sync();  // the previous chunk's TMEM reads, before this chunk's first group
-    warp_arrive(sm.g1_ready);
+    warp_arrive(sm.bar(QSmem::kG1Ready));
   };
 
   Cursor cc;
@@ -548,7 +576,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
   long long n = 0;
   bool bad = false;
   if (cc.valid(g)) {
-    if (warp_wait(&sm.full[0], 0, abort, hdr, 21, wlim)) {
+    if (warp_wait(sm.bar(QSmem::kFull + (0)), 0, abort, hdr, 21, wlim)) {
       phi_stage(0, min(kC, g.N - cc.chunk * kC));
       start_item(cc.item, cc.bh);
     } else {
@@ -576,7 +604,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       const float* zs = zsnap + 64 * s;
 
       // ---- epilogue of the first group: den, G.num
-      if (!bad && warp_wait(sm.g1_done, ph, abort, hdr, 22)) {
+      if (!bad && warp_wait(sm.bar(QSmem::kG1Done), ph, abort, hdr, 22)) {
         fence_after_sync();
         float dpart = 0.f, npart = 0.f;
         if (CAUSAL && qc <= lq) {  // warp-uniform; slice qc of P and W in two 16-column halves
@@ -650,7 +678,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           tmem_st16(tl + kFT + 16 * qc, th);
           tmem_st16(tl + kFT + 64 + 16 * qc, tlo);
         }
-        if (!CAUSAL || warp_wait(sm.ds_done, ph, abort, hdr, 27)) {  // dS has read V
+        if (!CAUSAL || warp_wait(sm.bar(QSmem::kDsDone), ph, abort, hdr, 27)) {  // dS has read V
           float gn[16];
           load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
@@ -658,7 +686,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           store_split_quarter(gt, vt, row, qc, gn);
           fence_proxy_async_smem();
           fence_before_sync();
-          warp_arrive(sm.g2_ready);
+          warp_arrive(sm.bar(QSmem::kG2Ready));
           if (qc == 0 && row < nvalid) {
             den_out[(size_t)bh * g.N + t0 + row] = den;
             gd_out[(size_t)bh * g.N + t0 + row] = gd;
@@ -678,7 +706,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
 
       // ---- while the second group runs: phi of the next chunk, the state carry
       if (!bad && cn.valid(g)) {
-        if (warp_wait(&sm.full[s ^ 1], (uint32_t)(((n + 1) >> 1) & 1), abort, hdr, 21, wlim))
+        if (warp_wait(sm.bar(QSmem::kFull + (s ^ 1)), (uint32_t)(((n + 1) >> 1) & 1), abort, hdr, 21, wlim))
           phi_stage(s ^ 1, min(kC, g.N - cn.chunk * kC));
         else
           bad = true;
@@ -687,7 +715,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       // rows of dS pass through it to the carry's threads
       float4* xs = reinterpret_cast<float4*>(vt);  // [64][16] float4, XOR-swizzled rows
       if (!bad) {
-        if (warp_wait(sm.gn_free, ph, abort, hdr, 28)) {
+        if (warp_wait(sm.bar(QSmem::kGnFree), ph, abort, hdr, 28)) {
           fence_after_sync();
           if (CAUSAL && !last && !dthread) {
             uint32_t r[16];
@@ -706,17 +734,19 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       }
       if (workers_any(bad)) break;
       if (tid < kDim) rr += (dzr[tid] + dzr[64 + tid]) + (dzr[128 + tid] + dzr[192 + tid]);
-      if (CAUSAL && !last && dthread) {  // S += dS (hi rows from TMEM, lo rows exchanged)
+      if (CAUSAL && !last && dthread) {  // the next snapshot: hi rows from TMEM, lo rows exchanged
         uint32_t r[16];
         tmem_ld16(tl + kFS + 16 * qc, r);
+        float v[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float4 lo = xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))];
-          srun[4 * j] += __uint_as_float(r[4 * j]) + lo.x;
-          srun[4 * j + 1] += __uint_as_float(r[4 * j + 1]) + lo.y;
-          srun[4 * j + 2] += __uint_as_float(r[4 * j + 2]) + lo.z;
-          srun[4 * j + 3] += __uint_as_float(r[4 * j + 3]) + lo.w;
+          v[4 * j] = __uint_as_float(r[4 * j]) + lo.x;
+          v[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + lo.y;
+          v[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + lo.z;
+          v[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + lo.w;
         }
+        store_split_quarter(sm.s_hi(), sm.s_lo(), drow, qc, v);
       }
       // the next chunk's first group can start (it waits for dphiQ's reads below
       // only before phi(Q) S_prev)
@@ -725,12 +755,12 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       // ---- dq = (dphiQ + gd Z_prev) * phi'(q), phi'(q) = min(phi(q), 1); this
       // quarter's columns, staged in 128 x 32 float32 boxes (128-byte swizzle) for
       // TMA stores in the chunk's spent K and phi(K) lo tiles
-      if (warp_wait(sm.g2_done, ph, abort, hdr, 24)) {
+      if (warp_wait(sm.bar(QSmem::kG2Done), ph, abort, hdr, 24)) {
         fence_after_sync();
         uint32_t r[16], r2[16];
         tmem_ld16x2(tl + kFQ + 16 * qc, r, tl + kFQ + 64 + 16 * qc, r2);
         fence_before_sync();
-        warp_arrive(sm.dq_read);
+        warp_arrive(sm.bar(QSmem::kDqRead));
         float qv[16], o[16];
         load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
@@ -742,7 +772,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           *reinterpret_cast<float4*>(sq + sw128(row, (qc & 1) * 64 + c * 16)) =
               make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         fence_proxy_async_smem();
-        if (!last) warp_arrive(sm.st_ready);
+        if (!last) warp_arrive(sm.bar(QSmem::kStReady));
       } else {
         bad = true;
       }
@@ -776,7 +806,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           dst[kDim * kDim + tid] = rr;
           rr = 0.f;
         }
-        warp_arrive(sm.st_ready);  // the G tile too is done with now
+        warp_arrive(sm.bar(QSmem::kStReady));  // the G tile too is done with now
       }
       ++n;
       cc = cn;
@@ -796,28 +826,28 @@ tc_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   QSmem sm(smraw);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (tid == 0) {
-    mbar_init(&sm.full[0], 1);
-    mbar_init(&sm.full[1], 1);
-    mbar_init(sm.g1_ready, kWorkers / 32);
-    mbar_init(sm.g2_ready, kWorkers / 32);
-    mbar_init(sm.st_ready, kWorkers / 32);
-    mbar_init(sm.g1_done, 1);
-    mbar_init(sm.ds_done, 1);
-    mbar_init(sm.gn_free, 1);
-    mbar_init(sm.g2_done, 1);
-    mbar_init(sm.dq_read, kWorkers / 32);
-    mbar_init(sm.drain, 1);
-    *sm.abort = 0;
+    mbar_init(sm.bar(QSmem::kFull + (0)), 1);
+    mbar_init(sm.bar(QSmem::kFull + (1)), 1);
+    mbar_init(sm.bar(QSmem::kG1Ready), kWorkers / 32);
+    mbar_init(sm.bar(QSmem::kG2Ready), kWorkers / 32);
+    mbar_init(sm.bar(QSmem::kStReady), kWorkers / 32);
+    mbar_init(sm.bar(QSmem::kG1Done), 1);
+    mbar_init(sm.bar(QSmem::kDsDone), 1);
+    mbar_init(sm.bar(QSmem::kGnFree), 1);
+    mbar_init(sm.bar(QSmem::kG2Done), 1);
+    mbar_init(sm.bar(QSmem::kDqRead), kWorkers / 32);
+    mbar_init(sm.bar(QSmem::kDrain), 1);
+    *sm.abort() = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(sm.tslot, 512);
+    tmem_alloc(sm.tslot(), 512);
     tmem_relinquish();
   }
   sync_tc();
-  const uint32_t tbase = *sm.tslot;
+  const uint32_t tbase = *sm.tslot();
   pdl_wait();
-  volatile int* abort = sm.abort;
+  volatile int* abort = sm.abort();
   if (warp >= kWorkers / 32) {
     regs_dec<kControlRegs>();
     if (lane == 0) {
