@@ -317,15 +317,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-// registers -> TMEM (32 lanes x 8 columns), followed by the store wait.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-}
-
 // Byte offset of logical (row, byte) inside a 128-byte-swizzled tile whose
 // base is 1024-byte aligned: 16-byte chunk c of row r lands at chunk c ^ (r & 7).
 __host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte) {
