@@ -186,6 +186,23 @@ def test_backward_single_token(la, dtype, causal):
     assert float(dq.abs().max()) <= bound and float(dk.abs().max()) <= bound
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_backward_many_items_ragged(la, causal):
+    """256 (b, h) pairs of 828 tokens (six full chunks and a ragged one of 60): more
+    segment items than CTAs, so the backward kernels walk several items each and hand
+    the starting state of the next item over at every item's last chunk, which is the
+    short one; every gradient element is compared with the fp64 oracle."""
+    B, H, N = 4, 64, 828
+    dtype = inputs.BF16
+    q, k, v = inputs.qkv(910, B, H, N, 64, 64, 0.125, dtype)
+    g = inputs.upstream_grad(910, B, H, N, 64, 0.125, dtype)
+    dq, dk, dv = la.la_backward(_t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, dtype), causal)
+    torch.cuda.synchronize()
+    wq, wk, wv = oracle.backward(q, k, v, g, causal)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        assert_close(got.cpu().numpy(), want, dtype, f"{name} many items")
+
+
 # ------------------------------------------------------------ prefill/decode
 
 @pytest.mark.parametrize("dtype", [inputs.BF16, inputs.F32])
