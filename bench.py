@@ -101,6 +101,57 @@ def extend_setup(la, w, g, device, S, Z):
     return lambda: la.la_extend(eq, ek, ev, pS, pZ, slots=slots, out=eo, workspace=ws)
 
 
+PACKED_MAX = 1024  # a serving batch: stream lengths uniform in 1..PACKED_MAX (seeded)
+
+
+def packed_part(la, w, g, device, hbm, flush, reps, S, Z):
+    """The decode workload's 256 streams (8 heads) continuing from their pool states
+    with 1..PACKED_MAX new tokens each, in one la_extend_packed call on the packed
+    token-major batch; beside it the same batch padded to its longest stream through
+    la_extend with per-stream lengths."""
+    import torch
+    from kernelized_causal_self_gb300 import inputs
+    P = EXTEND_POOL
+    lens = inputs.stream_lengths(w.seed, w.B, 1, PACKED_MAX)
+    cu = torch.zeros(w.B + 1, dtype=torch.int64)
+    cu[1:] = torch.from_numpy(lens.astype("int64")).cumsum(0)
+    T, N = int(cu[-1]), int(lens.max())
+    cu = cu.to(torch.int32).to(device)
+    pq = inputs.torch_normal(g, (T, w.H, w.D), w.scale, w.dtype, device)
+    pk = inputs.torch_normal(g, (T, w.H, w.D), w.scale, w.dtype, device)
+    pv = inputs.torch_normal(g, (T, w.H, w.M), w.scale, w.dtype, device)
+    po = torch.empty((T, w.H, w.M), dtype=pq.dtype, device=device)
+    slots = ((2 * torch.arange(w.B, device=device) + 1) % P).to(torch.int32)
+    pS = torch.zeros((P, w.H, w.D, w.M), dtype=torch.float32, device=device)
+    pZ = torch.zeros((P, w.H, w.D), dtype=torch.float32, device=device)
+    pS[slots.long()] = S
+    pZ[slots.long()] = Z
+    ws = torch.empty(la.la_forward_workspace_bytes(w.B, w.H, N, w.D, w.M, True), dtype=torch.uint8,
+                     device=device)
+    ms = statistics.median(time_calls(
+        lambda: la.la_extend_packed(pq, pk, pv, pS, pZ, cu, N, slots=slots, out=po, workspace=ws),
+        reps, 3, flush))
+    nbytes = T * w.H * fwd_bytes(w) + w.B * w.H * (8 * w.D * w.M + 8 * w.D)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    # the same streams padded to N tokens each
+    dq = torch.zeros((w.B, w.H, N, w.D), dtype=pq.dtype, device=device)
+    dk, dv = torch.zeros_like(dq), torch.zeros((w.B, w.H, N, w.M), dtype=pq.dtype, device=device)
+    lt = torch.from_numpy(lens).to(device)
+    for b in range(w.B):
+        a, n = int(cu[b]), int(lens[b])
+        for dst, src in ((dq, pq), (dk, pk), (dv, pv)):
+            dst[b, :, :n] = src[a:a + n].transpose(0, 1)
+    do = torch.empty_like(dv)
+    del pq, pk, pv, po
+    ms_pad = statistics.median(time_calls(
+        lambda: la.la_extend(dq, dk, dv, pS, pZ, slots=slots, lens=lt, out=do, workspace=ws),
+        reps, 3, flush))
+    return {"tokens_per_s": T / (ms * 1e-3), "ms": ms, "tokens": T, "longest": N,
+            "hbm_gbs": gbs, "roofline_frac": gbs / hbm, "padded_la_extend_ms": ms_pad,
+            "lengths": f"uniform integers in 1..{PACKED_MAX}, seeded",
+            "launch": "one la_extend_packed call", "l2": "flushed between calls (256 MB read)"}
+
+
 class Clocks:
     """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
 
@@ -177,7 +228,7 @@ def parse():
                     help="launch the step's calls directly instead of replaying CUDA graphs")
     ap.add_argument("--part", default=None,
                     choices=["fwdbwd", "fwd16k", "fwd3072", "noncausal", "bwd", "bwdfwd", "decode",
-                             "extend", "poly2", "rff"],
+                             "extend", "packed", "poly2", "rff"],
                     help="time one entry point on one workload only (for profilers)")
     return ap.parse_args()
 
@@ -337,6 +388,9 @@ def run_parts(la, device, peaks, reps=10):
         "tokens_per_s": w.B * EXTEND_TOKENS / (ms * 1e-3), "ms": ms, "hbm_gbs": gbs,
         "roofline_frac": gbs / hbm, "same_tokens_as_decode_steps_ms": per_step * EXTEND_TOKENS,
         "launch": "one la_extend call", "l2": "flushed between calls (256 MB read)"}
+    # the same streams as a packed serving batch of 1..PACKED_MAX new tokens each
+    parts[f"extend_packed_s256h8d64_len1to{PACKED_MAX}_pool{EXTEND_POOL}"] = packed_part(
+        la, w, g, device, hbm, flush, reps, S0, Z0)
     return parts
 
 
@@ -763,7 +817,8 @@ def run_part(args):
             "fwd3072": "causal_fwd_b8h8n3072d64",
             "noncausal": "noncausal_fwd_b4h8n4096d64",
             "decode": "decode_s256h8d64_prefill1024_steps3072",
-            "extend": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
+            "extend": "decode_s256h8d64_prefill1024_steps3072",
+            "packed": "decode_s256h8d64_prefill1024_steps3072"}[args.part]
     w = inputs.WORKLOADS[name]
     q, k, v, dout, g = device_inputs(w, device, dout=True)
     if args.part == "decode":
@@ -775,6 +830,12 @@ def run_part(args):
     elif args.part == "extend":
         _, S, Z = la.la_prefill(q, k, v)
         fn = extend_setup(la, w, g, device, S, Z)
+    elif args.part == "packed":  # times both calls itself: prints its parts entry
+        _, S, Z = la.la_prefill(q, k, v)
+        entry = packed_part(la, w, g, device, load_peaks()["hbm_gbs"], l2_flush_buffer(device),
+                            max(args.steps, 1), S, Z)
+        print(json.dumps({"part": args.part, "workload": name, **entry}), flush=True)
+        return
     elif args.part == "bwd":
         fn = lambda: la.la_backward(q, k, v, dout, True)
     elif args.part == "bwdfwd":  # the backward reading a forward's segment states

@@ -137,6 +137,32 @@ int la_extend(const void* q, const void* k, const void* v, void* out,
               int pool_size, int B, int H, int N, int D, int M, int dtype,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * la_extend_packed -- la_extend on a packed, token-major batch: B streams of
+ * different lengths stored back to back with no padding (a serving batch).
+ *
+ * The method is la_extend's ([deck slide 4], [summary §3.3.2, §3.4]): each
+ * stream continues from its pool entry's (S, Z) and the entry advances past
+ * its tokens. Only the layout differs.
+ *
+ * q, k: [T][H][D]; v, out: [T][H][M] in `dtype` (T = total_tokens): row t
+ * holds token t of every head. cu_seqlens: device int[B + 1] (4-byte
+ * aligned): stream b's tokens are rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1,
+ * in order. max_len bounds every stream's length (it sizes the chunk grid and
+ * the workspace: la_forward_workspace_bytes(B, H, max_len, D, M, 1, dtype)).
+ * Out rows of a stream's tokens are written, no other row is. A stream whose
+ * bounds break 0 <= cu_seqlens[b] <= cu_seqlens[b + 1] <= T is treated as empty,
+ * and one longer than max_len as its first max_len tokens (rows after those are
+ * not written); either makes la_workspace_status report LA_ERR_INVALID_ARG
+ * afterwards. S_pool, Z_pool, slots, pool_size: as la_extend.
+ * total_tokens == 0 or max_len == 0 returns LA_OK without touching the pool;
+ * total_tokens above 2^30 returns LA_ERR_INVALID_ARG.
+ */
+int la_extend_packed(const void* q, const void* k, const void* v, void* out,
+                     float* S_pool, float* Z_pool, const int* slots, const int* cu_seqlens,
+                     int pool_size, int B, int H, int total_tokens, int max_len, int D, int M,
+                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Scratch needed by la_backward for this shape, in bytes. */
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype);
 

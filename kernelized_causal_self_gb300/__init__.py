@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "la_forward", "la_prefill", "la_extend", "la_backward", "la_decode_step",
+    "la_forward", "la_prefill", "la_extend", "la_extend_packed", "la_backward", "la_decode_step",
     "la_forward_workspace_bytes", "la_backward_workspace_bytes",
     "la_workspace_status", "la_status_string", "la_kernel_launches", "library_path",
     "load_library",
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "la_forward": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_prefill": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "la_extend": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_vp, _c_size, _vp]),
+    "la_extend_packed": (_c_int, [_vp] * 8 + [_c_int] * 8 + [_vp, _c_size, _vp]),
     "la_backward": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _vp]),
     "la_decode_step": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_vp]),
     "la_workspace_status": (_c_int, [_vp, _c_size, _vp]),
@@ -292,6 +293,48 @@ def la_extend(q, k, v, S_pool, Z_pool, slots=None, lens=None, out=None, workspac
                            B, H, N, D, M, dt, ws.data_ptr(), ws.numel() * ws.element_size(),
                            _stream_ptr(dev))
     _check("la_extend", st)
+    return out
+
+
+def la_extend_packed(q, k, v, S_pool, Z_pool, cu_seqlens, max_len, slots=None, out=None,
+                     workspace=None):
+    """la_extend on a packed batch: q, k [T,H,D] and v [T,H,M], stream b in rows
+    cu_seqlens[b] .. cu_seqlens[b+1]-1 (int32 device tensor of B + 1 offsets), each
+    stream at most max_len tokens. Returns out [T,H,M] (rows of no stream are left
+    as they were in `out`, uninitialised if it is None).
+    """
+    import torch
+    fn, f32 = "la_extend_packed", torch.float32
+    (T, H), D, M = _dims(fn, q, v, 3)
+    _expect(fn, "k", k, q.shape, q.dtype)
+    _expect(fn, "v", v, (T, H, M), q.dtype)
+    if S_pool.dim() != 4:
+        raise ValueError(f"{fn}: S_pool must be [pool, H, D, M]")
+    P = S_pool.shape[0]
+    _expect(fn, "S_pool", S_pool, (P, H, D, M), f32)
+    _expect(fn, "Z_pool", Z_pool, (P, H, D), f32)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a contiguous int32 tensor of B + 1 offsets")
+    B = cu_seqlens.numel() - 1
+    if slots is not None and (slots.dtype != torch.int32 or slots.numel() != B):
+        raise ValueError("slots must be a contiguous int32 tensor of B entries")
+    if out is not None:
+        _expect(fn, "out", out, (T, H, M), q.dtype)
+    dt = _dtype_code(q)
+    _need_cuda(q, k, v, S_pool, Z_pool, cu_seqlens,
+               *[t for t in (out, slots) if t is not None])
+    lib = load_library()
+    dev = q.device
+    out = torch.empty((T, H, M), dtype=q.dtype, device=dev) if out is None else out
+    nbytes = lib.la_forward_workspace_bytes(B, H, max_len, D, M, 1, dt)
+    ws = _workspace(nbytes, dev, workspace)
+    with _on_device(dev):
+        st = lib.la_extend_packed(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  S_pool.data_ptr(), Z_pool.data_ptr(),
+                                  0 if slots is None else slots.data_ptr(),
+                                  cu_seqlens.data_ptr(), P, B, H, T, int(max_len), D, M, dt,
+                                  ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(dev))
+    _check(fn, st)
     return out
 
 

@@ -166,6 +166,40 @@ int la_extend(const void* q, const void* k, const void* v, void* out, float* S_p
                                     static_cast<la::WorkspaceHeader*>(workspace), st));
 }
 
+int la_extend_packed(const void* q, const void* k, const void* v, void* out, float* S_pool,
+                     float* Z_pool, const int* slots, const int* cu_seqlens, int pool_size, int B,
+                     int H, int total_tokens, int max_len, int D, int M, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (B <= 0 || H <= 0 || max_len < 0 || total_tokens < 0 || total_tokens > (1 << 30))
+    return LA_ERR_INVALID_ARG;
+  if (!valid_dims(B, H, max_len, D, M) || !valid_dtype(dtype)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({S_pool, Z_pool}) || cu_seqlens == nullptr) return LA_ERR_INVALID_ARG;
+  if (slots == nullptr ? pool_size < B : pool_size < 1) return LA_ERR_INVALID_ARG;
+  if (slots != nullptr && (reinterpret_cast<uintptr_t>(slots) & 3u) != 0) return LA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return LA_ERR_INVALID_ARG;
+  if (max_len == 0 || total_tokens == 0) return LA_OK;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, max_len, D, M, 1, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = clear_header(workspace, st);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  la::StateIO io;
+  io.S = S_pool;
+  io.Z = Z_pool;
+  io.slots = slots;
+  io.H = H;
+  io.pool = pool_size;
+  io.read_init = true;
+  io.cu = cu_seqlens;
+  io.T = total_tokens;
+  if (la::tc_forward_supported(D, M, dtype))
+    return from_cuda(la::tc_forward(q, k, v, out, io, B * H, max_len, true, workspace, st));
+  return from_cuda(la::simt_forward(q, k, v, out, io, B * H, max_len, D, M, true, dtype,
+                                    static_cast<la::WorkspaceHeader*>(workspace), st));
+}
+
 size_t la_backward_workspace_bytes(int B, int H, int N, int D, int M, int causal, int dtype) {
   (void)causal;
   if (!query_dims_ok(B, H, N)) return la::kHeaderBytes;

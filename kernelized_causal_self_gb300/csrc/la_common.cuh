@@ -33,7 +33,8 @@ struct WorkspaceHeader {
   int status;     // LA_OK, LA_ERR_TIMEOUT (a bounded wait gave up) or LA_ERR_INVALID_ARG
                   // (la_extend met a slot outside its pool), written by kernels
   int wait_site;  // where a bounded wait gave up (debug)
-  unsigned int pad[62];
+  int tickets[2];  // items handed out so far (per-stream lengths: segment states, attention)
+  unsigned int pad[60];
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header must stay 256 bytes");
 

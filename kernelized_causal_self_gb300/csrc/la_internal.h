@@ -23,6 +23,10 @@ struct StateIO {
   bool read_init = false;
   // per-stream token counts (device int[B], each clamped to [0, N]); nullptr: all N
   const int* lens = nullptr;
+  // packed token-major layout [T][H][D] (tensor-core forward, CUDA-core forward):
+  // stream b holds rows cu[b] .. cu[b + 1] - 1 (device int[B + 1]); nullptr: [BH][N][D]
+  const int* cu = nullptr;
+  int T = 0;
   // write the final state back to the entries (prefill, extend); false: the
   // entries are read-only initial states (sequence shards)
   bool write_final = true;

@@ -37,6 +37,21 @@ __device__ __forceinline__ void load_rows(const T* __restrict__ src, int rows_va
   }
 }
 
+// load_rows for rows `rs` elements apart (the packed token-major layout)
+template <typename T>
+__device__ __forceinline__ void load_rows_strided(const T* __restrict__ src, int rows_valid,
+                                                  int cols, size_t rs, float* dst, bool apply_phi) {
+  for (int e = threadIdx.x; e < kChunk * cols; e += blockDim.x) {
+    const int r = e / cols, c = e % cols;
+    float x = 0.f;
+    if (r < rows_valid) {
+      x = to_f32<T>(src[(size_t)r * rs + c]);
+      if (apply_phi) x = phi(x);
+    }
+    dst[e] = x;
+  }
+}
+
 // S[d][m] += sum_j fk[j][d] * vv[j][m];  Z[d] += sum_j fk[j][d]
 __device__ __forceinline__ void accumulate_state(float* S, float* Z, const float* fk,
                                                  const float* vv, int D, int M) {
@@ -85,10 +100,30 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
   float* den = A + kChunk * kChunk;  // kChunk
 
   const size_t bh = blockIdx.x;
-  q += bh * (size_t)N * D;
-  k += bh * (size_t)N * D;
-  v += bh * (size_t)N * M;
-  out += bh * (size_t)N * M;
+  // this sequence's first row and the distance between its token rows: [BH][N][D],
+  // or the packed [T][H][D] with stream b = bh / H in rows cu[b] .. cu[b + 1] - 1
+  size_t rq = D, rv = M;
+  int len = N;
+  if (io.cu != nullptr) {
+    const int b = (int)(bh / io.H), s0 = io.cu[b], e0 = io.cu[b + 1];
+    const bool ok = 0 <= s0 && s0 <= e0 && e0 <= io.T;
+    if (!(ok && e0 - s0 <= N) && threadIdx.x == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+    len = ok ? min(e0 - s0, N) : 0;
+    const size_t r0 = ok ? (size_t)s0 : 0, hh = bh % io.H;
+    rq = (size_t)io.H * D;
+    rv = (size_t)io.H * M;
+    q += r0 * rq + hh * D;
+    k += r0 * rq + hh * D;
+    v += r0 * rv + hh * M;
+    out += r0 * rv + hh * M;
+  } else {
+    q += bh * (size_t)N * D;
+    k += bh * (size_t)N * D;
+    v += bh * (size_t)N * M;
+    out += bh * (size_t)N * M;
+    // this stream's token count (the rest of the sequence is padding, never read)
+    if (io.lens != nullptr) len = max(0, min(io.lens[bh / io.H], N));
+  }
 
   // the sequence's state entry: initial state (extend) and final state (prefill, extend)
   size_t entry = bh;
@@ -100,8 +135,7 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     if (!entry_ok && threadIdx.x == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
   }
   const bool init = entry_ok && io.read_init;
-  // this stream's token count (the rest of the sequence is padding, never read)
-  if (io.lens != nullptr) N = max(0, min(io.lens[bh / io.H], N));
+  N = len;
   for (int e = threadIdx.x; e < D * M; e += blockDim.x) S[e] = init ? io.S[entry * D * M + e] : 0.f;
   for (int e = threadIdx.x; e < D; e += blockDim.x) Z[e] = init ? io.Z[entry * D + e] : 0.f;
   __syncthreads();
@@ -109,8 +143,8 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
   if (!CAUSAL) {  // full sums first
     for (int t0 = 0; t0 < N; t0 += kChunk) {
       const int nv = min(kChunk, N - t0);
-      load_rows<T>(k + (size_t)t0 * D, nv, D, fk, true);
-      load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
+      load_rows_strided<T>(k + (size_t)t0 * rq, nv, D, rq, fk, true);
+      load_rows_strided<T>(v + (size_t)t0 * rv, nv, M, rv, vv, false);
       __syncthreads();
       accumulate_state(S, Z, fk, vv, D, M);
       __syncthreads();
@@ -119,10 +153,10 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 
   for (int t0 = 0; t0 < N; t0 += kChunk) {
     const int nv = min(kChunk, N - t0);
-    load_rows<T>(q + (size_t)t0 * D, nv, D, fq, true);
+    load_rows_strided<T>(q + (size_t)t0 * rq, nv, D, rq, fq, true);
     if (CAUSAL) {
-      load_rows<T>(k + (size_t)t0 * D, nv, D, fk, true);
-      load_rows<T>(v + (size_t)t0 * M, nv, M, vv, false);
+      load_rows_strided<T>(k + (size_t)t0 * rq, nv, D, rq, fk, true);
+      load_rows_strided<T>(v + (size_t)t0 * rv, nv, M, rv, vv, false);
     }
     __syncthreads();
     if (CAUSAL) pair_dots<true, false>(fq, fk, D, nv, A);
@@ -141,7 +175,7 @@ simt_forward_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       for (int d = 0; d < D; ++d) acc += fq[i * D + d] * S[d * M + m];
       if (CAUSAL)
         for (int j = 0; j <= i; ++j) acc += A[i * kChunk + j] * vv[j * M + m];
-      out[(size_t)t0 * M + e] = from_f32<T>(acc / den[i]);
+      out[(size_t)(t0 + i) * rv + m] = from_f32<T>(acc / den[i]);
     }
     __syncthreads();
     if (CAUSAL) {

@@ -375,7 +375,7 @@ static_assert(QSmem::kBarOff + QSmem::kNBars * 8 + 8 <= kQSmem - 1024, "dq kerne
 template <bool CAUSAL>
 __device__ __forceinline__ void bwd_q_mma(QSmem& sm, const Geometry& g, uint32_t tbase,
                                           volatile int* abort, WorkspaceHeader* hdr) {
-  Cursor c;
+  FullCursor c;
   c.start(g, true);
   const uint32_t ha = smem_u32(sm.s_hi()), la = smem_u32(sm.s_lo());
   long long n = 0;
@@ -458,7 +458,7 @@ __device__ __forceinline__ void bwd_q_tma(QSmem& sm, const Geometry& g, const CU
                                           const CUtensorMap* tm_g, const CUtensorMap* tm_dq,
                                           volatile int* abort, WorkspaceHeader* hdr) {
   const uint32_t tx = (CAUSAL ? 4 : 2) * kTile;
-  Cursor cl, cs;
+  FullCursor cl, cs;
   cl.start(g, true);
   cs = cl;
   long long nl = 0, ns = 0;
@@ -559,7 +559,7 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
   // Hand the MMA warp chunk cc's operands: Z and the state snapshot before the
   // chunk (a segment's first chunk had its state set up by start_item), phi of its
   // tiles being in already.
-  auto state_in = [&](const Cursor& c, long long nc) {
+  auto state_in = [&](const FullCursor& c, long long nc) {
     if (tid < kDim) {
       if (CAUSAL && !c.first()) zrun += zinc;
       if (CAUSAL) zinc = (dzk[tid] + dzk[64 + tid]) + (dzk[128 + tid] + dzk[192 + tid]);
@@ -569,9 +569,9 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
     warp_arrive(sm.bar(QSmem::kG1Ready));
   };
 
-  Cursor cc;
+  FullCursor cc;
   cc.start(g, true);
-  Cursor cn = cc;  // the chunk after cc
+  FullCursor cn = cc;  // the chunk after cc
   cn.advance(g);
   long long n = 0;
   bool bad = false;

@@ -34,7 +34,32 @@ struct Geometry {
   unsigned long long fault_wait_ns = 0;
   __device__ bool faulty() const { return fault_load >= 0 && blockIdx.x == 0; }
   __device__ uint64_t wait_ns() const { return faulty() ? fault_wait_ns : kWaitLimitNs; }
-  __device__ int len(int bh) const { return lens ? max(0, min(lens[bh / H], N)) : N; }
+  // forward only, packed token-major layout [T][H][D] (cu != nullptr): stream
+  // b = bh / H holds rows cu[b] .. cu[b + 1] - 1 of every head (its first N at
+  // most); bounds outside 0 <= cu[b] <= cu[b + 1] <= T give the stream no tokens
+  const int* cu = nullptr;
+  int T = 0;
+  __nv_bfloat16* out_rows = nullptr;  // the packed output (rows stored one by one)
+  __device__ void span(int bh, int& r0, int& n) const {
+    const int b = bh / H, s = cu[b], e = cu[b + 1];
+    const bool ok = 0 <= s && s <= e && e <= T;
+    r0 = ok ? s : T;
+    n = ok ? min(e - s, N) : 0;
+  }
+  // the stream's bounds are consistent and its length is at most N
+  __device__ bool span_ok(int bh) const {
+    const int b = bh / H, s = cu[b], e = cu[b + 1];
+    return 0 <= s && s <= e && e <= T && e - s <= N;
+  }
+  __device__ int len(int bh) const {
+    if (cu != nullptr) {
+      int r0, n;
+      span(bh, r0, n);
+      return n;
+    }
+    return lens ? max(0, min(lens[bh / H], N)) : N;
+  }
+
   __host__ __device__ int n_items() const { return BH * n_seg; }
   // item -> (bh, seg): segment-major so that a segment's predecessors were
   // scheduled earlier
@@ -53,23 +78,106 @@ struct Geometry {
 // other read last (the ones still in L2). The item's (batch, head) index and
 // chunk range are worked out once per item (they take integer divisions by
 // runtime sizes), not per chunk.
-struct Cursor {
+// With per-stream lengths (LENS: lens or the packed layout, forward only) an item's
+// range stops at the last chunk that holds tokens of its stream, and items with
+// none are skipped: a stream shorter than N costs only its own chunks. The items
+// are then dealt by tickets rather than round robin, since their sizes differ:
+// one thread per CTA (the producer) takes the next ticket from a counter in the
+// workspace header when it reaches the end of an item and passes the item on
+// through a ring in shared memory, which the CTA's other cursors (consumers) read
+// in the same order; -1 there ends the walk.
+constexpr int kRing = 8;
+
+template <bool LENS>
+struct CursorT {
   int item, chunk;
   int bh, cbeg, cend;  // of `item`
+  int n;               // LENS: its stream's token count
+  int r0, head;        // LENS, packed layout: the stream's first row, the item's head
   int step;            // +-gridDim.x
+  int* counter = nullptr;        // dealt by tickets: the producer's ticket counter
+  volatile int* ring = nullptr;  // dealt by tickets: the ring (producer and consumers)
+  int rpos = 0;
+  int ahead = -1;  // producer: the ticket requested while the previous item ran
+  bool back = false;
   __device__ void set_item(const Geometry& g) {
     bh = g.bh_of(item);
     cbeg = g.chunk_begin(item);
     cend = g.chunk_end(item);
+    if (LENS && g.cu != nullptr) {
+      g.span(bh, r0, n);
+      head = bh % g.H;
+      cend = min(cend, (n + kC - 1) / kC);
+    } else if (LENS && g.lens != nullptr) {
+      n = g.len(bh);
+      cend = min(cend, (n + kC - 1) / kC);
+    }
   }
-  __device__ void start(const Geometry& g, bool back = false) {
-    item = blockIdx.x;
-    step = back ? -(int)gridDim.x : (int)gridDim.x;
-    if (back && item < g.n_items()) item += (g.n_items() - 1 - item) / (int)gridDim.x * (int)gridDim.x;
+  // TMA coordinates (y, z) of the current chunk: (first token, sequence) in the
+  // [BH][N][D] layout, (head, row) in the packed one; a chunk wholly past the
+  // stream's end points past row T (the copy reads only fill values)
+  __device__ void tile_yz(const Geometry& g, int& y, int& z) const {
+    const int t0 = chunk * kC;
+    if (LENS && g.cu != nullptr) {
+      y = head;
+      z = t0 < n ? r0 + t0 : g.T;
+    } else {
+      y = t0;
+      z = bh;
+    }
+  }
+  // the first item from `item` on (in steps of `step`) with a chunk to process
+  __device__ void seek(const Geometry& g) {
     chunk = 0;
-    if (valid(g)) {
+    for (; valid(g); item += step) {
+      set_item(g);
+      if (cbeg < cend) {
+        chunk = cbeg;
+        return;
+      }
+    }
+  }
+  // dealt by tickets: the next item with a chunk to process (producer: from the
+  // counter, recorded in the ring; consumer: the ring's next entry)
+  __device__ void take(const Geometry& g) {
+    chunk = 0;
+    if (counter != nullptr) {
+      for (;;) {
+        // each ticket is requested one item ahead, so that the atomic's round trip
+        // overlaps the item's work instead of stalling the thread that takes it
+        const int t = ahead >= 0 ? ahead : atomicAdd(counter, 1);
+        ahead = atomicAdd(counter, 1);
+        item = t < g.n_items() ? (back ? g.n_items() - 1 - t : t) : -1;
+        if (item < 0) break;
+        set_item(g);
+        if (cbeg < cend) break;
+      }
+      ring[rpos++ % kRing] = item;
+    } else {
+      item = ring[rpos++ % kRing];
+    }
+    if (item >= 0) {
       set_item(g);
       chunk = cbeg;
+    }
+  }
+  __device__ void start(const Geometry& g, bool back_ = false) {
+    if (LENS && ring != nullptr) {
+      back = back_;
+      take(g);
+      return;
+    }
+    item = blockIdx.x;
+    step = back_ ? -(int)gridDim.x : (int)gridDim.x;
+    if (back_ && item < g.n_items()) item += (g.n_items() - 1 - item) / (int)gridDim.x * (int)gridDim.x;
+    if constexpr (LENS) {
+      seek(g);
+    } else {
+      chunk = 0;
+      if (valid(g)) {
+        set_item(g);
+        chunk = cbeg;
+      }
     }
   }
   __device__ bool valid(const Geometry& g) const { return (unsigned)item < (unsigned)g.n_items(); }
@@ -77,8 +185,14 @@ struct Cursor {
   __device__ bool last() const { return chunk + 1 == cend; }
   __device__ void advance(const Geometry& g) {
     if (++chunk >= cend) {
+      if (LENS && ring != nullptr) {
+        take(g);
+        return;
+      }
       item += step;
-      if (valid(g)) {
+      if constexpr (LENS) {
+        seek(g);
+      } else if (valid(g)) {
         set_item(g);
         chunk = cbeg;
       }
@@ -86,7 +200,10 @@ struct Cursor {
   }
 };
 
-// Same items as Cursor, but each item's chunks from last to first.
+using Cursor = CursorT<true>;       // the forward's kernels
+using FullCursor = CursorT<false>;  // every sequence N tokens long (the backward's)
+
+// Same items as FullCursor, but each item's chunks from last to first.
 struct RevCursor {
   int item, chunk;
   int bh, cbeg, cend;  // of `item`
@@ -280,6 +397,36 @@ __device__ __forceinline__ bool mbar_wait_abort(uint64_t* bar, uint32_t parity, 
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                WorkspaceHeader* hdr, int site) {
   return __all_sync(0xffffffffu, mbar_wait_abort(bar, parity, abort, hdr, site));
+}
+
+// A worker warp's wait for a stage's tiles when items are dealt by tickets: 1 when
+// the tiles of chunk n have landed, 2 when the CTA's work ended before chunk n (the
+// producer, having run out of items, stored the number of chunks it loaded in
+// `total`, -1 until then; no load for chunk n is then coming), 0 when the wait ran
+// out or the CTA is winding down. Agreed by the warp (the lowest outcome wins).
+__device__ __forceinline__ int mbar_wait_warp_or_end(uint64_t* bar, uint32_t parity,
+                                                     volatile int* abort, WorkspaceHeader* hdr,
+                                                     int site, volatile int* total, long long n) {
+  int r = 0;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) {
+      r = 1;
+      break;
+    }
+    const int tot = *total;
+    if (tot >= 0 && n >= tot) {
+      r = 2;
+      break;
+    }
+    if (*abort) break;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_timeout(hdr, site);
+      break;
+    }
+  }
+  return __reduce_min_sync(0xffffffffu, r);
 }
 
 // Block-uniform bounded wait: every thread waits, then all agree on the outcome

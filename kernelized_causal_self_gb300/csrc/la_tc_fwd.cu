@@ -51,7 +51,11 @@ constexpr int kStateSmem = 1024 + kStateStages * kStateStageBytes + 2048 + 256;
 // IDENT: the K tiles hold the features f already (the identity feature map): the
 // group then gives V^T f and sum_t f directly (features centred on zero, nothing
 // to split off). Else inputs to which the elu + 1 map applies, in the psi form.
-template <bool IDENT>
+// VARLEN: per-stream lengths (lens or the packed layout); the items are then dealt
+// by tickets: the control thread takes them as its loads reach them, the workers
+// read each from the ring once its first tiles have landed and learn of the end
+// from `loaded`.
+template <bool IDENT, bool VARLEN>
 __global__ void __launch_bounds__(kStateThreads, 2)
 tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 Geometry g, float* __restrict__ partial, WorkspaceHeader* hdr) {
@@ -67,7 +71,10 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint64_t* drain = segbar + 2;                // every MMA of the CTA is done
   volatile int* abort = reinterpret_cast<volatile int*>(drain + 1);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1) + 1;
+  volatile int* ring = reinterpret_cast<volatile int*>(tslot + 1);  // kRing items (tickets)
+  volatile int* loaded = ring + kRing;  // tickets: chunks loaded in all, once known (else -1)
 
+  constexpr bool TICKETS = VARLEN;  // items dealt by tickets (else round robin)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = (warp >> 2) & 1;
   const int trow = q4 * 32 + lane;  // tile row of this worker (column half h)
@@ -81,6 +88,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     mbar_init(&segbar[1], 1);
     mbar_init(drain, 1);
     *abort = 0;
+    *loaded = -1;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -101,16 +109,24 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   if (warp == kStateWorkers / 32) {
     // ------------------------------------------------------------- control
     if (lane == 0) {
-      Cursor cl, cm;  // next chunk to load, next chunk to multiply
+      CursorT<VARLEN> cl, cm;  // next chunk to load, next chunk to multiply
+      if constexpr (TICKETS) {
+        cl.ring = cm.ring = ring;
+        cl.counter = &hdr->tickets[0];
+      }
       cl.start(g);
       cm.start(g);
-      long long total = 0;
-      for (Cursor c = cl; c.valid(g); c.advance(g)) ++total;
+      long long total = 0;  // (VARLEN: not known in advance)
+      if constexpr (TICKETS) {
+        if (!cl.valid(g)) *loaded = 0;
+      } else {
+        for (CursorT<VARLEN> c = cl; c.valid(g); c.advance(g)) ++total;
+      }
       long long nl = 0, nm = 0;
       int nseg = 0;
       const uint32_t oa = smem_u32(ones);
       uint64_t idle_since = globaltimer_ns();
-      while (nm < total) {
+      while (TICKETS ? (nm < nl || cl.valid(g)) : nm < total) {
         bool moved = false;
         if (nm < nl && mbar_test_wait(&phid[nm % S], (uint32_t)((nm / S) & 1))) {
           fence_after_sync();
@@ -138,14 +154,20 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           ++nm;
           moved = true;
         }
-        if (nl < total && (nl < S || mbar_test_wait(&empty[nl % S], (uint32_t)(((nl - S) / S) & 1)))) {
+        if ((TICKETS ? cl.valid(g) : nl < total) &&
+            (nl < S || mbar_test_wait(&empty[nl % S], (uint32_t)(((nl - S) / S) & 1)))) {
           const int s = (int)(nl % S);
           uint8_t* st = stages + s * SB;
           mbar_arrive_expect_tx(&full[s], 2 * kTile);
-          tma_load_3d(st, &tm_k, &full[s], 0, cl.chunk * kC, cl.bh);
-          tma_load_3d(st + kTile, &tm_v, &full[s], 0, cl.chunk * kC, cl.bh);
+          int y, z;
+          cl.tile_yz(g, y, z);
+          tma_load_3d(st, &tm_k, &full[s], 0, y, z);
+          tma_load_3d(st + kTile, &tm_v, &full[s], 0, y, z);
           cl.advance(g);
           ++nl;
+          if constexpr (TICKETS) {
+            if (!cl.valid(g)) *loaded = (int)nl;
+          }
           moved = true;
         }
         if (moved) {
@@ -198,22 +220,41 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
     };
 
-    Cursor cc;
-    cc.start(g);
+    CursorT<VARLEN> cc;
+    if constexpr (TICKETS)
+      cc.ring = ring;
+    else
+      cc.start(g);
+    bool fresh = TICKETS;             // the next chunk starts an item still to be read
     long long consumed = 0;
     int nseg = 0;                    // segments whose last chunk has passed
     int pend_item = -1, pend_p = 0;  // segment awaiting its readout
     uint32_t pend_phase = 0;
     bool ok = true;
-    while (cc.valid(g)) {
-      const int item = cc.item;
-      const int bh = cc.bh;
-      const int nvalid = min(kC, g.len(bh) - cc.chunk * kC);
-      const bool last = cc.last();
+    while (TICKETS || cc.valid(g)) {
+      int item = cc.item, bh = cc.bh;
+      int nvalid = min(kC, (VARLEN ? cc.n : g.N) - cc.chunk * kC);
+      bool last = cc.last();
       const int s = consumed % S;
       uint8_t* kt = stages + s * SB;
       uint8_t* vt = kt + kTile;
-      if (!mbar_wait_warp(&full[s], (uint32_t)((consumed / S) & 1), abort, hdr, 1)) {
+      if constexpr (TICKETS) {
+        const int r = mbar_wait_warp_or_end(&full[s], (uint32_t)((consumed / S) & 1), abort, hdr, 1,
+                                            loaded, consumed);
+        if (r == 0) {
+          ok = false;
+          break;
+        }
+        if (r == 2) break;
+        if (fresh) {
+          cc.take(g);
+          fresh = false;
+        }
+        item = cc.item;
+        bh = cc.bh;
+        nvalid = min(kC, cc.n - cc.chunk * kC);
+        last = cc.last();
+      } else if (!mbar_wait_warp(&full[s], (uint32_t)((consumed / S) & 1), abort, hdr, 1)) {
         ok = false;
         break;
       }
@@ -243,7 +284,12 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ++nseg;
       }
       ++consumed;
-      cc.advance(g);
+      if constexpr (!TICKETS)
+        cc.advance(g);
+      else if (last)
+        fresh = true;
+      else
+        ++cc.chunk;
     }
     if (ok && pend_item >= 0 && mbar_wait_warp(&segbar[pend_p], pend_phase, abort, hdr, 2)) {
       fence_after_sync();
@@ -267,26 +313,48 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // else 0; with io.S set and io.write_final the full sum (S0 + all segments) is
 // written to the entry: S [d][m], Z [d]. The partials are S^T [m][d] (the
 // segment-state kernel's) or, with io.rows_are_d, R [d][m] (the backward's).
-// One thread per state element; the segment loads are issued in batches of 8
-// so the walk over segments is not a chain of dependent global loads.
+// Two forms. Few sequences: one thread per state element; the segment loads are
+// issued in batches of 8 so the walk over segments is not a chain of dependent
+// global loads. Many sequences (short ones, as in a serving batch): a block per
+// sequence, each thread holding 9 elements and the entry passed through shared
+// memory whole (read and written in its own [d][m] order), so that a block's few
+// dependent loads (slot, entry, partials) cover a whole state.
 constexpr int kScanThreads = 128;
+constexpr int kScanSeqThreads = 512;
+constexpr int kScanPer = (kStateFloats + kScanSeqThreads - 1) / kScanSeqThreads;  // 9
+
+// the sequence's state entry (prefill, extend); a slot outside the pool is reported
+__device__ __forceinline__ bool scan_entry(const StateIO& io, int bh, bool report,
+                                           WorkspaceHeader* hdr, size_t& entry) {
+  entry = (size_t)bh;
+  if (io.S == nullptr) return false;
+  if (io.slots == nullptr) return true;
+  const int slot = io.slots[bh / io.H];
+  entry = (size_t)slot * io.H + bh % io.H;
+  const bool ok = slot >= 0 && slot < io.pool;
+  if (!ok && report) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+  return ok;
+}
+
+// the segments that hold tokens: with per-stream lengths, the segments past the
+// stream's last chunk were skipped by the segment-state kernel (their sums are zero
+// and never written)
+__device__ __forceinline__ int scan_segments(const Geometry& g, int bh) {
+  if (g.lens == nullptr && g.cu == nullptr) return g.n_seg;
+  return min(g.n_seg, ((g.len(bh) + kC - 1) / kC + g.seg_chunks - 1) / g.seg_chunks);
+}
 
 __global__ void __launch_bounds__(kScanThreads)
-state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, int BH, int n_seg,
+state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, Geometry g,
                   int mode, StateIO io, WorkspaceHeader* hdr) {
   const int bh = blockIdx.y;
   const int e = blockIdx.x * kScanThreads + threadIdx.x;
+  const int BH = g.BH;
   pdl_wait();
   if (e >= kStateFloats) return;
-  // the sequence's state entry (prefill, extend)
-  size_t entry = (size_t)bh;
-  bool entry_ok = io.S != nullptr;
-  if (entry_ok && io.slots != nullptr) {
-    const int slot = io.slots[bh / io.H];
-    entry_ok = slot >= 0 && slot < io.pool;
-    entry = (size_t)slot * io.H + bh % io.H;
-    if (!entry_ok && e == 0) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
-  }
+  const int n_seg = scan_segments(g, bh);
+  size_t entry;
+  const bool entry_ok = scan_entry(io, bh, e == 0, hdr, entry);
   // e < 4096: S^T [m][d] (or R [d][m]); else Z [e - 4096]
   const int m = io.rows_are_d ? e % kDim : e / kDim, d = io.rows_are_d ? e / kDim : e % kDim;
   float* cell = !entry_ok ? nullptr
@@ -314,6 +382,87 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, in
   if (cell != nullptr && io.write_final) *cell = run;
 }
 
+// The per-sequence form: block bh, elements t + 512 i (i < 9) in the partials' order.
+__global__ void __launch_bounds__(kScanSeqThreads)
+state_scan_seq_kernel(const float* __restrict__ partial, float* __restrict__ out, Geometry g,
+                      int mode, StateIO io, WorkspaceHeader* hdr) {
+  __shared__ float st[kDim * (kDim + 1) + kDim];  // the entry: S [d][m] (rows padded), then Z
+  const int bh = blockIdx.x, t = threadIdx.x;
+  const int BH = g.BH;
+  pdl_wait();
+  const int n_seg = scan_segments(g, bh);
+  size_t entry;
+  const bool entry_ok = scan_entry(io, bh, t == 0, hdr, entry);
+  // element e -> its cell of the entry in shared memory
+  auto cell = [&](int e) {
+    if (e >= kDim * kDim) return kDim * (kDim + 1) + (e - kDim * kDim);
+    const int m = io.rows_are_d ? e % kDim : e / kDim, d = io.rows_are_d ? e / kDim : e % kDim;
+    return d * (kDim + 1) + m;
+  };
+  float run[kScanPer];
+  const bool init = entry_ok && io.read_init && mode != kScanTotal;
+  if (init) {
+    const float* S = io.S + entry * kDim * kDim;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int p = t + kScanSeqThreads * i;  // entry order: S [d][m], then Z
+      if (p < kDim * kDim)
+        st[(p / kDim) * (kDim + 1) + p % kDim] = S[p];
+      else if (p < kStateFloats)
+        st[kDim * (kDim + 1) + (p - kDim * kDim)] = io.Z[entry * kDim + (p - kDim * kDim)];
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < kScanPer; ++i) {
+    const int e = t + kScanSeqThreads * i;
+    run[i] = (init && e < kStateFloats) ? st[cell(e)] : 0.f;
+  }
+  const bool rev = mode == kScanSuffix;
+  for (int j = 0; j < n_seg; ++j) {
+    const int sg = rev ? n_seg - 1 - j : j;
+    const float* src = partial + ((size_t)sg * BH + bh) * kStateFloats;
+    float* dst = out + ((size_t)sg * BH + bh) * kStateFloats;
+    float x[kScanPer];
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int e = t + kScanSeqThreads * i;
+      x[i] = e < kStateFloats ? src[e] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int e = t + kScanSeqThreads * i;
+      if (e < kStateFloats) {
+        if (mode != kScanTotal) dst[e] = run[i];
+        run[i] += x[i];
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kScanPer; ++i) {
+    const int e = t + kScanSeqThreads * i;
+    if (mode == kScanTotal && e < kStateFloats) out[(size_t)bh * kStateFloats + e] = run[i];
+  }
+  if (entry_ok && io.write_final) {
+    if (init) __syncthreads();  // every read of the staged entry is done
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int e = t + kScanSeqThreads * i;
+      if (e < kStateFloats) st[cell(e)] = run[i];
+    }
+    __syncthreads();
+    float* S = io.S + entry * kDim * kDim;
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i) {
+      const int p = t + kScanSeqThreads * i;
+      if (p < kDim * kDim)
+        S[p] = st[(p / kDim) * (kDim + 1) + p % kDim];
+      else if (p < kStateFloats)
+        io.Z[entry * kDim + (p - kDim * kDim)] = st[kDim * (kDim + 1) + (p - kDim * kDim)];
+    }
+  }
+}
+
 // --------------------------------------------------------- 3. chunk attention
 
 constexpr int kAttStages = 2;  // 2 CTAs per SM
@@ -337,7 +486,11 @@ constexpr uint32_t kTmemCols = 256;
 // finish before a barrier, the writes follow it.
 constexpr int kAttThreads = 256;
 
-template <bool CAUSAL, bool IDENT>
+// VARLEN: per-stream lengths (lens or the packed layout): the items are dealt by
+// tickets (the TMA thread takes them, a chunk ahead, and every thread reads them
+// from the ring once a block barrier has passed since they were written), and in
+// the packed layout a stream's last rows are stored one by one.
+template <bool CAUSAL, bool IDENT, bool VARLEN>
 __global__ void __launch_bounds__(kAttThreads, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -355,7 +508,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* mma_bar = full + kAttStages;
   uint64_t* drain = mma_bar + 1;  // every MMA of the CTA is done (end of the kernel)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* ring = reinterpret_cast<volatile int*>(tslot + 1);  // kRing items (tickets)
 
+  constexpr bool TICKETS = VARLEN;  // items dealt by tickets (else round robin)
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int q4 = warp & 3, h = warp >> 2;
   const int row = q4 * 32 + lane;   // chunk row (query) of this thread
@@ -394,14 +549,31 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t tl = lane_base(tbase);
   pdl_wait();
 
+  // bad row offsets (or a stream longer than N) and, on the one-chunk path, slots
+  // outside the pool are reported for every stream, also for those without tokens
+  // (whose items the cursor skips)
+  if (VARLEN && (g.cu != nullptr || (direct && io.slots != nullptr))) {
+    for (int b = blockIdx.x * kAttThreads + tid; b < g.BH / g.H; b += gridDim.x * kAttThreads) {
+      bool bad = g.cu != nullptr && !g.span_ok(b * g.H);
+      if (direct && io.slots != nullptr) bad |= io.slots[b] < 0 || io.slots[b] >= io.pool;
+      if (bad) atomicExch(&hdr->status, (int)LA_ERR_INVALID_ARG);
+    }
+  }
   const uint32_t tx_bytes = CAUSAL ? 3 * kTile : kTile;
   const uint64_t wlim = g.wait_ns();  // main-loop wait limit (shortened only by the test hook)
   // items last to first: the segment-state kernel just streamed k and v first to last
-  Cursor cc, cp;
-  cc.start(g, true);
-  cp.start(g, true);
+  // (with tickets first to last: the items past short streams' ends, which hold no
+  // chunk, are then the last ones handed out)
+  CursorT<VARLEN> cc, cp;
+  if constexpr (TICKETS) {
+    cc.ring = cp.ring = ring;
+    cp.counter = &hdr->tickets[1];
+  } else {
+    cc.start(g, true);
+    cp.start(g, true);
+  }
   long long issued = 0;
-  auto issue = [&](Cursor& c) {
+  auto issue = [&](CursorT<VARLEN>& c) {
     if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
       ++issued;
       c.advance(g);
@@ -409,18 +581,25 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     const int s = issued % kAttStages;
     uint8_t* st = stages + s * 3 * kTile;
-    const int bh = c.bh, t0 = c.chunk * kC;
+    int y, z;
+    c.tile_yz(g, y, z);
     mbar_arrive_expect_tx(&full[s], tx_bytes);
-    tma_load_3d(st, &tm_q, &full[s], 0, t0, bh);
+    tma_load_3d(st, &tm_q, &full[s], 0, y, z);
     if (CAUSAL) {
-      tma_load_3d(st + kTile, &tm_k, &full[s], 0, t0, bh);
-      tma_load_3d(st + 2 * kTile, &tm_v, &full[s], 0, t0, bh);
+      tma_load_3d(st + kTile, &tm_k, &full[s], 0, y, z);
+      tma_load_3d(st + 2 * kTile, &tm_v, &full[s], 0, y, z);
     }
     ++issued;
     c.advance(g);
   };
-  if (tma_thread)
+  if (tma_thread) {
+    if constexpr (TICKETS) cp.start(g);
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
+  }
+  if constexpr (TICKETS) {
+    __syncthreads();
+    cc.start(g);
+  }
 
   // running state: S^T row `row` (sthread) or Z (zthread), columns [32h, 32h + 32)
   float srun[32];
@@ -435,7 +614,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int bh = cc.bh;
     const int t0 = cc.chunk * kC;
     const bool first = cc.first();
-    const int nvalid = min(kC, g.len(bh) - t0);
+    const int nvalid = min(kC, (VARLEN ? cc.n : g.N) - t0);
     if (!CAUSAL && tma_thread && cp.valid(g)) {  // causal: issued with the first MMA group
       bulk_wait_read<0>();  // the stage being refilled was last read by an output store
       issue(cp);
@@ -654,9 +833,23 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (tma_thread) {
-      tma_store_3d(&tm_o, qt, 0, t0, bh);
-      bulk_commit();
+    if (!VARLEN || g.cu == nullptr || nvalid == kC) {
+      if (tma_thread) {
+        int y, z;
+        cc.tile_yz(g, y, z);
+        tma_store_3d(&tm_o, qt, 0, y, z);
+        bulk_commit();
+      }
+    } else if (nvalid > 0) {
+      // packed layout, the stream's last chunk: its rows past the end belong to
+      // the next stream, so only the valid rows are stored, 16 bytes at a time
+      const size_t rs = (size_t)g.H * kDim;  // elements between token rows
+      __nv_bfloat16* dst = g.out_rows + (size_t)(cc.r0 + t0) * rs + (size_t)cc.head * kDim;
+      for (int u = tid; u < nvalid * 8; u += kAttThreads) {
+        const int r = u >> 3, c = u & 7;
+        *reinterpret_cast<uint4*>(dst + r * rs + 8 * c) =
+            *reinterpret_cast<const uint4*>(qt + sw128(r, 16 * c));
+      }
     }
     ++consumed;
     cc.advance(g);
@@ -771,14 +964,20 @@ cudaError_t launch_segment_states(const CUtensorMap* tk, const CUtensorMap* tv, 
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   };
-  return identity ? run(tc_state_kernel<true>) : run(tc_state_kernel<false>);
+  if (g.lens != nullptr || g.cu != nullptr)  // per-stream lengths (never identity features)
+    return identity ? cudaErrorInvalidValue : run(tc_state_kernel<false, true>);
+  return identity ? run(tc_state_kernel<true, false>) : run(tc_state_kernel<false, false>);
 }
 
 cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int mode,
                         const StateIO& io, WorkspaceHeader* hdr, cudaStream_t st) {
-  const dim3 grid((kStateFloats + kScanThreads - 1) / kScanThreads, g.BH);
-  cudaError_t e = launch_pdl(state_scan_kernel, grid, dim3(kScanThreads), 0, st, partial, out,
-                             g.BH, g.n_seg, mode, io, hdr);
+  // many short sequences: a block per sequence (a few dependent loads cover a whole state)
+  const cudaError_t e =
+      g.BH >= 2 * sm_count()
+          ? launch_pdl(state_scan_seq_kernel, dim3(g.BH), dim3(kScanSeqThreads), 0, st, partial,
+                       out, g, mode, io, hdr)
+          : launch_pdl(state_scan_kernel, dim3((kStateFloats + kScanThreads - 1) / kScanThreads, g.BH),
+                       dim3(kScanThreads), 0, st, partial, out, g, mode, io, hdr);
   count_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -823,6 +1022,9 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   Geometry g = make_geometry(BH, N);
   g.lens = io.lens;
   g.H = io.H;
+  g.cu = io.cu;
+  g.T = io.T;
+  g.out_rows = static_cast<__nv_bfloat16*>(out);
   if (fault != nullptr) {  // read by the attend kernel only
     g.fault_load = fault->load;
     g.fault_wait_ns = fault->wait_ns;
@@ -831,11 +1033,16 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeaderBytes);
   float* prefix = partial + align_up(sizeof(float) * kStateFloats * (size_t)g.n_items(), 256) / 4;
   CUtensorMap tq, tk, tv, to;
-  const uint64_t n = (uint64_t)N, bh = (uint64_t)BH;
-  if (!make_tmap_bf16_3d(&tq, q, kDim, n, bh, kDim, kC, 1) ||
-      !make_tmap_bf16_3d(&tk, k, kDim, n, bh, kDim, kC, 1) ||
-      !make_tmap_bf16_3d(&tv, v, kDim, n, bh, kDim, kC, 1) ||
-      !make_tmap_bf16_3d(&to, out, kDim, n, bh, kDim, kC, 1))
+  // [BH][N][D] as (d, token, sequence); the packed [T][H][D] as (d, head, row),
+  // a chunk being 128 rows of one head (the same 128-byte rows in shared memory)
+  const bool packed = io.cu != nullptr;
+  const uint64_t d1 = packed ? (uint64_t)io.H : (uint64_t)N;
+  const uint64_t d2 = packed ? (uint64_t)io.T : (uint64_t)BH;
+  const uint32_t b1 = packed ? 1 : kC, b2 = packed ? kC : 1;
+  if (!make_tmap_bf16_3d(&tq, q, kDim, d1, d2, kDim, b1, b2) ||
+      !make_tmap_bf16_3d(&tk, k, kDim, d1, d2, kDim, b1, b2) ||
+      !make_tmap_bf16_3d(&tv, v, kDim, d1, d2, kDim, b1, b2) ||
+      !make_tmap_bf16_3d(&to, out, kDim, d1, d2, kDim, b1, b2))
     return cudaErrorInvalidValue;
 
   // causal with one chunk per sequence, continuing a stored state: no segment
@@ -864,11 +1071,14 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
+  if (io.lens != nullptr || io.cu != nullptr)  // per-stream lengths: causal, elu + 1 only
+    return causal && !identity ? attend(tc_attend_kernel<true, false, true>, io, direct)
+                               : cudaErrorInvalidValue;
   if (causal)
-    return identity ? attend(tc_attend_kernel<true, true>, io, direct)
-                    : attend(tc_attend_kernel<true, false>, io, direct);
-  return identity ? attend(tc_attend_kernel<false, true>, StateIO{}, false)
-                  : attend(tc_attend_kernel<false, false>, StateIO{}, false);
+    return identity ? attend(tc_attend_kernel<true, true, false>, io, direct)
+                    : attend(tc_attend_kernel<true, false, false>, io, direct);
+  return identity ? attend(tc_attend_kernel<false, true, false>, StateIO{}, false)
+                  : attend(tc_attend_kernel<false, false, false>, StateIO{}, false);
 }
 
 }  // namespace la

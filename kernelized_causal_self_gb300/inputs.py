@@ -101,6 +101,12 @@ def decode_tokens(seed, steps, S, H, D, M, scale=1.0, dtype=F32):
     return q, k, v
 
 
+def stream_lengths(seed, B, lo, hi, stream=7):
+    """B stream lengths, i.i.d. uniform integers in [lo, hi] (a serving batch's mix)."""
+    rng = np.random.Generator(np.random.PCG64([seed, stream]))
+    return rng.integers(lo, hi + 1, size=B).astype(np.int32)
+
+
 def to_torch(x, dtype, device):
     """float32 numpy array (on `dtype`'s grid) -> torch tensor of that dtype."""
     import torch

@@ -38,7 +38,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill", "la_extend",
-              "la_forward_workspace_bytes", "la_backward_workspace_bytes",
+              "la_extend_packed", "la_forward_workspace_bytes", "la_backward_workspace_bytes",
               "la_status_string", "la_workspace_status"):
         assert n in names
 
@@ -54,7 +54,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_binding_mirrors_the_abi_names():
     for n in ("la_forward", "la_backward", "la_decode_step", "la_prefill", "la_extend",
-              "la_forward_workspace_bytes", "la_backward_workspace_bytes",
+              "la_extend_packed", "la_forward_workspace_bytes", "la_backward_workspace_bytes",
               "la_status_string", "la_workspace_status"):
         assert callable(getattr(la, n))
 
@@ -88,6 +88,31 @@ def test_forward_rejects_bad_arguments(lib):
 def _ext(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, S=FAKE, Z=FAKE, slots=FAKE, lens=FAKE, pool=4, B=2,
          H=1, N=16, D=64, M=64, dtype=1, ws=FAKE, wsb=1 << 20):
     return lib.la_extend(q, k, v, out, S, Z, slots, lens, pool, B, H, N, D, M, dtype, ws, wsb, None)
+
+
+def _extp(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, S=FAKE, Z=FAKE, slots=FAKE, cu=FAKE, pool=4, B=2,
+          H=1, T=64, max_len=16, D=64, M=64, dtype=1, ws=FAKE, wsb=1 << 20):
+    return lib.la_extend_packed(q, k, v, out, S, Z, slots, cu, pool, B, H, T, max_len, D, M, dtype,
+                                ws, wsb, None)
+
+
+def test_extend_packed_rejects_bad_arguments(lib):
+    assert _extp(lib, cu=0) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, cu=FAKE + 2) == la.LA_ERR_INVALID_ARG          # offsets 4-byte aligned
+    assert _extp(lib, slots=FAKE + 2) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, S=0) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, q=ODD) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, pool=1, slots=0) == la.LA_ERR_INVALID_ARG      # identity slots need B
+    assert _extp(lib, T=-1) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, T=(1 << 30) + 1) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, max_len=-1) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, B=0) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, D=12) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, dtype=7) == la.LA_ERR_INVALID_ARG
+    assert _extp(lib, ws=0) == la.LA_ERR_WORKSPACE
+    assert _extp(lib, wsb=16) == la.LA_ERR_WORKSPACE
+    assert _extp(lib, T=0) == la.LA_OK                               # nothing to do
+    assert _extp(lib, max_len=0) == la.LA_OK
 
 
 def test_extend_rejects_bad_arguments(lib):

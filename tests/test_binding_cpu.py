@@ -59,6 +59,24 @@ def test_extend_checks_pool_and_indices():
     _raises("CUDA device", la.la_extend, q, q, v, S, Z, slots=torch.tensor([1, 3], dtype=torch.int32))
 
 
+def test_extend_packed_checks_layout_and_offsets():
+    q, v = _t(9, 3, 16), _t(9, 3, 8)
+    S, Z = _t(5, 3, 16, 8, dtype=F32), _t(5, 3, 16, dtype=F32)
+    cu = torch.tensor([0, 4, 9], dtype=torch.int32)
+    _raises("3 dimensions", la.la_extend_packed, _t(1, 9, 3, 16), _t(1, 9, 3, 16), _t(1, 9, 3, 8),
+            S, Z, cu, 8)
+    _raises("k must be", la.la_extend_packed, q, _t(9, 3, 8), v, S, Z, cu, 8)
+    _raises("v must be", la.la_extend_packed, q, q, _t(8, 3, 8), S, Z, cu, 8)
+    _raises("S_pool must be", la.la_extend_packed, q, q, v, _t(5, 2, 16, 8, dtype=F32), Z, cu, 8)
+    _raises("Z_pool must be", la.la_extend_packed, q, q, v, S, _t(5, 3, 8, dtype=F32), cu, 8)
+    _raises("cu_seqlens must be", la.la_extend_packed, q, q, v, S, Z, cu.long(), 8)
+    _raises("cu_seqlens must be", la.la_extend_packed, q, q, v, S, Z, cu[:1], 8)
+    _raises("slots must be", la.la_extend_packed, q, q, v, S, Z, cu, 8,
+            slots=torch.zeros(3, dtype=torch.int32))
+    _raises("out must be", la.la_extend_packed, q, q, v, S, Z, cu, 8, out=_t(9, 3, 16))
+    _raises("CUDA device", la.la_extend_packed, q, q, v, S, Z, cu, 8)
+
+
 def test_backward_checks_gradients():
     q, v = _t(2, 3, 10, 16), _t(2, 3, 10, 8)
     _raises("dout must be", la.la_backward, q, q, v, _t(2, 3, 10, 16))
@@ -115,6 +133,8 @@ def test_every_library_call_runs_with_the_tensors_device_current(monkeypatch):
     la.la_forward_noalloc(q, q, v)
     la.la_prefill(q, q, v)
     la.la_extend(q, q, v, S, Z)
+    pq, pv = _t(10, 3, 16), _t(10, 3, 8)
+    la.la_extend_packed(pq, pq, pv, S, Z, torch.tensor([0, 4, 10], dtype=torch.int32), 6)
     la.la_backward(q, q, v, v)
     la.la_decode_step(q[:, :, 0], q[:, :, 0], v[:, :, 0], S, Z)
     la.la_workspace_status(ws)
@@ -122,7 +142,8 @@ def test_every_library_call_runs_with_the_tensors_device_current(monkeypatch):
     la.la_forward_noalloc_status(device="cpu")
     calls = [i for i, e in enumerate(events) if e[0] == "call" and not e[1].endswith("_bytes")]
     assert [events[i][1] for i in calls] == [
-        "la_forward", "la_forward_noalloc", "la_prefill", "la_extend", "la_backward",
+        "la_forward", "la_forward_noalloc", "la_prefill", "la_extend", "la_extend_packed",
+        "la_backward",
         "la_decode_step", "la_workspace_status", "la_workspace_wait_site",
         "la_forward_noalloc_status"]
     for i in calls:
