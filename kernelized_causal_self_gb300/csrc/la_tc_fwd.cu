@@ -362,12 +362,14 @@ state_scan_kernel(const float* __restrict__ partial, float* __restrict__ out, Ge
                                              : io.Z + entry * kDim + (e - kDim * kDim));
   float run = (cell != nullptr && io.read_init && mode != kScanTotal) ? *cell : 0.f;
   const bool rev = mode == kScanSuffix;
+  // a forward prefix with no entry to write needs no sums of the last segment
+  const int n_read = (mode == kScanPrefix && io.S == nullptr) ? n_seg - 1 : n_seg;
   for (int s0 = 0; s0 < n_seg; s0 += 8) {
     float x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int sg = rev ? n_seg - 1 - (s0 + j) : s0 + j;
-      x[j] = s0 + j < n_seg ? partial[((size_t)sg * BH + bh) * kStateFloats + e] : 0.f;
+      x[j] = s0 + j < n_read ? partial[((size_t)sg * BH + bh) * kStateFloats + e] : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -419,6 +421,8 @@ state_scan_seq_kernel(const float* __restrict__ partial, float* __restrict__ out
     run[i] = (init && e < kStateFloats) ? st[cell(e)] : 0.f;
   }
   const bool rev = mode == kScanSuffix;
+  // a forward prefix with no entry to write needs no sums of the last segment
+  const int n_read = (mode == kScanPrefix && io.S == nullptr) ? n_seg - 1 : n_seg;
   for (int j = 0; j < n_seg; ++j) {
     const int sg = rev ? n_seg - 1 - j : j;
     const float* src = partial + ((size_t)sg * BH + bh) * kStateFloats;
@@ -427,7 +431,7 @@ state_scan_seq_kernel(const float* __restrict__ partial, float* __restrict__ out
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
       const int e = t + kScanSeqThreads * i;
-      x[i] = e < kStateFloats ? src[e] : 0.f;
+      x[i] = (e < kStateFloats && j < n_read) ? src[e] : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
@@ -1054,8 +1058,14 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
   cudaError_t e = cudaSuccess;
   if (!direct) {
-    e = launch_segment_states(&tk, &tv, g, partial, hdr, st, identity);
-    if (e != cudaSuccess) return e;
+    // causal with no state to write back: the last segment's sums would only feed the
+    // sequence's final state, so the segment-state pass stops one segment short
+    Geometry gs = g;
+    if (causal && io.S == nullptr) gs.n_seg = g.n_seg - 1;
+    if (gs.n_items() > 0) {
+      e = launch_segment_states(&tk, &tv, gs, partial, hdr, st, identity);
+      if (e != cudaSuccess) return e;
+    }
     e = launch_scan(partial, prefix, g, causal ? kScanPrefix : kScanTotal, io, hdr, st);
     if (e != cudaSuccess) return e;
   }
