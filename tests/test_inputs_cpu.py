@@ -54,3 +54,13 @@ def test_draws_are_seeded_and_streams_differ():
     assert not np.array_equal(q, inputs.qkv(12, 2, 3, 50, 8, 8, 0.125, inputs.BF16)[0])
     assert np.array_equal(inputs.bf16_round(q), q)  # already on the bf16 grid
     assert abs(float(np.std(inputs.normal(3, (200_000,), 0.125))) - 0.125) < 2e-3
+
+
+def test_stream_lengths_are_seeded_and_in_range():
+    a = inputs.stream_lengths(930, 256, 1, 1024)
+    b = inputs.stream_lengths(930, 256, 1, 1024)
+    assert a.dtype == np.int32 and a.shape == (256,)
+    assert np.array_equal(a, b)
+    assert a.min() >= 1 and a.max() <= 1024
+    assert not np.array_equal(a, inputs.stream_lengths(931, 256, 1, 1024))
+    assert np.all(inputs.stream_lengths(5, 64, 7, 7) == 7)
