@@ -116,7 +116,7 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       cl.start(g);
       cm.start(g);
-      long long total = 0;  // (VARLEN: not known in advance)
+      long long total = 0;  // chunks to process (with tickets not known in advance)
       if constexpr (TICKETS) {
         if (!cl.valid(g)) *loaded = 0;
       } else {
@@ -232,9 +232,15 @@ tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     uint32_t pend_phase = 0;
     bool ok = true;
     while (TICKETS || cc.valid(g)) {
-      int item = cc.item, bh = cc.bh;
-      int nvalid = min(kC, (VARLEN ? cc.n : g.N) - cc.chunk * kC);
-      bool last = cc.last();
+      // the chunk's item (with tickets known only once its tiles have landed)
+      int item = 0, bh = 0, nvalid = 0;
+      bool last = false;
+      if constexpr (!TICKETS) {
+        item = cc.item;
+        bh = cc.bh;
+        nvalid = min(kC, (VARLEN ? cc.n : g.N) - cc.chunk * kC);
+        last = cc.last();
+      }
       const int s = consumed % S;
       uint8_t* kt = stages + s * SB;
       uint8_t* vt = kt + kTile;
