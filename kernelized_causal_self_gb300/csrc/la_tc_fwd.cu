@@ -495,16 +495,25 @@ constexpr uint32_t kTmemCols = 256;
 // threads; two CTAs per SM. P is compacted in place (fp32 to bf16): all reads
 // finish before a barrier, the writes follow it.
 constexpr int kAttThreads = 256;
+// the fused forward: clusters of one CTA per segment (the portable cluster size)
+constexpr int kMaxFusedSegments = 8;
 
 // VARLEN: per-stream lengths (lens or the packed layout): the items are dealt by
 // tickets (the TMA thread takes them, a chunk ahead, and every thread reads them
 // from the ring once a block barrier has passed since they were written), and in
 // the packed layout a stream's last rows are stored one by one.
-template <bool CAUSAL, bool IDENT, bool VARLEN>
+// FUSED: the whole forward in one launch for sequences of at most 8 segments: a
+// thread-block cluster per sequence, one CTA per segment (the cluster rank). Each
+// CTA first sums its segment's states in the psi form (what the segment-state
+// kernel does), the CTAs then read the sums they need from each other's shared
+// memory (causal: the segments before their own, in order; non-causal: all), and
+// each attends over its own segment from that state; the states also go to the
+// workspace, where the scan would have put them.
+template <bool CAUSAL, bool IDENT, bool VARLEN, bool FUSED>
 __global__ void __launch_bounds__(kAttThreads, 2)
 tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 Geometry g, const float* __restrict__ prefix, StateIO io, bool direct,
+                 Geometry g, float* __restrict__ prefix, StateIO io, bool direct,
                  WorkspaceHeader* hdr) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
@@ -578,7 +587,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if constexpr (TICKETS) {
     cc.ring = cp.ring = ring;
     cp.counter = &hdr->tickets[1];
-  } else {
+  } else if constexpr (!FUSED) {
     cc.start(g, true);
     cp.start(g, true);
   }
@@ -602,7 +611,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ++issued;
     c.advance(g);
   };
-  if (tma_thread) {
+  if (!FUSED && tma_thread) {
     if constexpr (TICKETS) cp.start(g);
     for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
   }
@@ -619,6 +628,154 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   bool ok = true;
   long long consumed = 0;
   uint32_t mma_phase = 0;
+  if constexpr (FUSED) {
+    // ---------------------------------------------------------------- fused
+    const int nseg = g.n_seg, seg = (int)cluster_ctarank(), bh = blockIdx.x / nseg;
+    const int item = seg * g.BH + bh;
+    const int c0 = g.chunk_begin(item), c1 = g.chunk_end(item);
+    // the segment's sums, fp32 in the partials' layout: S^T [m][d] in stage 0's Q
+    // slot, Z [d] in the snapshot area (both free until the attention starts)
+    float* pS = reinterpret_cast<float*>(stages);
+    float* pZ = reinterpret_cast<float*>(s_hi);
+    // causal: nobody reads the last segment's sums
+    if (!CAUSAL || seg + 1 < nseg) {
+      auto load_kv = [&](int c) {
+        const int st = issued % kAttStages;
+        uint8_t* base = stages + st * 3 * kTile;
+        mbar_arrive_expect_tx(&full[st], 2 * kTile);
+        tma_load_3d(base + kTile, &tm_k, &full[st], 0, c * kC, bh);
+        tma_load_3d(base + 2 * kTile, &tm_v, &full[st], 0, c * kC, bh);
+        ++issued;
+      };
+      int nl = c0;
+      if (tma_thread)
+        for (int i = 0; i < kAttStages && nl < c1; ++i) load_kv(nl++);
+      for (int c = c0; c < c1; ++c) {
+        const int s = consumed % kAttStages;
+        uint8_t* kt = stages + s * 3 * kTile + kTile;
+        uint8_t* vt = kt + kTile;
+        if (!wait_uniform(&full[s], (consumed / kAttStages) & 1, hdr, 16, wlim)) {
+          ok = false;
+          break;
+        }
+        const int nvalid = min(kC, g.N - c * kC);
+        psi_half(kt, row, h, nvalid);
+        if (nvalid < kC) zero_half_if_past(vt, row, h, nvalid);
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (tid == 0) {
+          // [V^T; 1^T] [psi(K) | 1] (M = 128, N = 80, both MN-major, the ones block
+          // standing in for rows 64.. and columns 64..): lanes 0-63 get
+          // (V^T psi(K))[m][d] and the column sum of V[:, m] (column 64), lanes
+          // 64-127 the column sums of psi(K)
+          const uint32_t ka = smem_u32(kt), va = smem_u32(vt), oa = smem_u32(ones);
+          const uint32_t idS = idesc_bf16(128, 80, true, true);
+#pragma unroll
+          for (int k = 0; k < kC / 16; ++k)
+            mma_ss(tbase + kColP, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                   sdesc(ka + k * 2048, oa - (ka + k * 2048), 1024), idS,
+                   (c == c0 && k == 0) ? 0u : 1u);
+          mma_commit(mma_bar);
+        }
+        // (waiting here for the chunk's MMAs, and refilling its stage right after,
+        // measured faster than deferring both by a chunk)
+        if (!wait_uniform(mma_bar, mma_phase, hdr, 17, wlim)) {
+          ok = false;
+          break;
+        }
+        mma_phase ^= 1;
+        fence_after_sync();
+        ++consumed;
+        if (tma_thread && nl < c1) load_kv(nl++);  // into the stage just released
+      }
+      if (ok) {  // the sums -> pS, pZ (this thread's row m or Z, columns [32h, 32h + 32))
+        uint32_t r[32];
+        tmem_ld32(tl + kColP + 32 * h, r);
+        if (sthread || zthread) {
+          float add;
+          if (sthread) {
+            uint32_t r16[16];
+            tmem_ld16(tl + kColP + 64, r16);
+            add = __uint_as_float(r16[0]);  // sum of V[:, m]: the constant part of phi
+          } else {
+            add = (float)max(0, min(g.N - c0 * kC, (c1 - c0) * kC));  // the segment's tokens
+          }
+          float4* d4 = reinterpret_cast<float4*>(sthread ? pS + row * kDim + 32 * h : pZ + 32 * h);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(__uint_as_float(r[4 * j]) + add, __uint_as_float(r[4 * j + 1]) + add,
+                                __uint_as_float(r[4 * j + 2]) + add, __uint_as_float(r[4 * j + 3]) + add);
+        }
+      }
+    }
+    fence_before_sync();
+    __syncwarp();
+    cluster_sync();  // every CTA's sums are in its shared memory
+    // the starting states, a slice of the state's elements per CTA: CTA q reads its
+    // slice from every CTA's sums, adds them in segment order (as the scan kernel
+    // does) and writes each CTA's starting state (causal: the sum over the segments
+    // before it; non-causal: the total) into that CTA's shared memory and into the
+    // workspace; every CTA then reads its own state locally
+    float* rS = reinterpret_cast<float*>(stages + 3 * kTile);  // stage 1's Q slot
+    float* rZ = pZ + kDim;
+    {
+      const int per = (kStateFloats + nseg - 1) / nseg;
+      const int e1 = min(kStateFloats, (seg + 1) * per);
+      for (int e = seg * per + tid; e < e1; e += kAttThreads) {
+        const uint32_t src = smem_u32(e < kDim * kDim ? pS + e : pZ + (e - kDim * kDim));
+        const uint32_t dst = smem_u32(e < kDim * kDim ? rS + e : rZ + (e - kDim * kDim));
+        float x[kMaxFusedSegments];
+#pragma unroll
+        for (int r = 0; r < kMaxFusedSegments; ++r)
+          x[r] = r < nseg ? ld_cluster_f32(cluster_map(src, (uint32_t)r)) : 0.f;
+        float run = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxFusedSegments; ++r) {
+          if (r < nseg) {
+            if (CAUSAL) {
+              st_cluster_f32(cluster_map(dst, (uint32_t)r), run);
+              prefix[((size_t)r * g.BH + bh) * kStateFloats + e] = run;
+            }
+            run += x[r];
+          }
+        }
+        if (!CAUSAL) {
+          for (int r = 0; r < nseg; ++r) st_cluster_f32(cluster_map(dst, (uint32_t)r), run);
+          prefix[(size_t)bh * kStateFloats + e] = run;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // every CTA's starting state is in its shared memory
+    if (sthread || zthread) {
+      const float4* s4 = reinterpret_cast<const float4*>(sthread ? rS + row * kDim + 32 * h : rZ + 32 * h);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = s4[j];
+        srun[4 * j] = x.x;
+        srun[4 * j + 1] = x.y;
+        srun[4 * j + 2] = x.z;
+        srun[4 * j + 3] = x.w;
+      }
+    }
+    // the starting states were written into this CTA's stage memory through the
+    // generic proxy (by other CTAs as well); the TMA loads that refill it below are
+    // ordered after those writes
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncthreads();  // the stages are refilled only after these reads
+    fence_after_sync();
+    // the attention over this segment: one item per CTA
+    cc.item = cp.item = item;
+    cc.step = cp.step = (int)gridDim.x;
+    cc.set_item(g);
+    cp.set_item(g);
+    cc.chunk = cp.chunk = c0;
+    if (tma_thread && ok)
+      for (int i = 0; i < kAttStages - 1 && cp.valid(g); ++i) issue(cp);
+  }
   while (cc.valid(g) && ok) {
     const int item = cc.item;
     const int bh = cc.bh;
@@ -649,7 +806,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int j = 0; j < 32; ++j) srun[j] = init ? io.Z[entry * kDim + 32 * h + j] : 0.f;
       }
-    } else if (first && (sthread || zthread)) {  // state before this segment
+    } else if (!FUSED && first && (sthread || zthread)) {  // state before this segment
       const float* src = prefix + (size_t)(CAUSAL ? item : bh) * kStateFloats;
       const float4* s4 = reinterpret_cast<const float4*>(src + (sthread ? row * kDim : kDim * kDim) + 32 * h);
 #pragma unroll
@@ -992,6 +1149,43 @@ cudaError_t launch_scan(const float* partial, float* out, const Geometry& g, int
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Whether clusters of `n` CTAs of the fused kernel `kern` can be resident (the query
+// remembered per kernel and n); configures the kernel's shared memory on every call.
+template <typename K>
+bool fused_fits(K kern, int n) {
+  if (configure(kern, kAttSmem) != cudaSuccess) return false;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, bool> memo;
+  const std::pair<const void*, int> key{reinterpret_cast<const void*>(kern), n};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  bool fits = false;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(kAttThreads);
+    cfg.dynamicSmemBytes = kAttSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = n;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess)
+      fits = clusters > 0;
+    else
+      cudaGetLastError();  // a refused query leaves no error behind
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  memo[key] = fits;
+  return fits;
+}
+
 }  // namespace tcx
 
 using namespace tcx;
@@ -1062,6 +1256,21 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   // own increment rounds phi(K) to bf16, which a sum from a zero state over
   // random-sign v leaves at ~2% on the state's significant elements.
   const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
+  // a plain forward of sequences of at most 8 segments: one launch, a cluster per sequence
+  if (!direct && !identity && io.S == nullptr && io.lens == nullptr && io.cu == nullptr &&
+      fault == nullptr && g.n_seg <= kMaxFusedSegments) {
+    auto fused = [&](auto kern) -> cudaError_t {
+      if (!fused_fits(kern, g.n_seg)) return cudaErrorNotSupported;
+      const cudaError_t err = launch_cluster_pdl(kern, dim3(g.n_items()), dim3(kAttThreads), kAttSmem,
+                                                 st, g.n_seg, tq, tk, tv, to, g, prefix, StateIO{},
+                                                 false, hdr);
+      count_launches(1);
+      return err != cudaSuccess ? err : cudaGetLastError();
+    };
+    const cudaError_t fe = causal ? fused(tc_attend_kernel<true, false, false, true>)
+                                  : fused(tc_attend_kernel<false, false, false, true>);
+    if (fe != cudaErrorNotSupported) return fe;
+  }
   cudaError_t e = cudaSuccess;
   if (!direct) {
     // causal with no state to write back: the last segment's sums would only feed the
@@ -1083,18 +1292,18 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
     if (err != cudaSuccess) return err;
     const int ctas = min(g.n_items(), resident_ctas(kern, kAttSmem, kAttThreads) * sms);
     err = launch_pdl(kern, dim3(ctas), dim3(kAttThreads), kAttSmem, st, tq, tk, tv, to, g,
-                     (const float*)prefix, kio, kdirect, hdr);
+                     prefix, kio, kdirect, hdr);
     count_launches(1);
     return err != cudaSuccess ? err : cudaGetLastError();
   };
   if (io.lens != nullptr || io.cu != nullptr)  // per-stream lengths: causal, elu + 1 only
-    return causal && !identity ? attend(tc_attend_kernel<true, false, true>, io, direct)
+    return causal && !identity ? attend(tc_attend_kernel<true, false, true, false>, io, direct)
                                : cudaErrorInvalidValue;
   if (causal)
-    return identity ? attend(tc_attend_kernel<true, true, false>, io, direct)
-                    : attend(tc_attend_kernel<true, false, false>, io, direct);
-  return identity ? attend(tc_attend_kernel<false, true, false>, StateIO{}, false)
-                  : attend(tc_attend_kernel<false, false, false>, StateIO{}, false);
+    return identity ? attend(tc_attend_kernel<true, true, false, false>, io, direct)
+                    : attend(tc_attend_kernel<true, false, false, false>, io, direct);
+  return identity ? attend(tc_attend_kernel<false, true, false, false>, StateIO{}, false)
+                  : attend(tc_attend_kernel<false, false, false, false>, StateIO{}, false);
 }
 
 }  // namespace la

@@ -497,6 +497,39 @@ def test_full_size_decode_sampled(la):
         assert_close(_np(outs[:, s, h]), want, w.dtype, f"decode[{s},{h}]")
 
 
+# --------------------------------------- one-launch forward for short sequences
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("shape", [(2, 3, 1000), (8, 8, 3072), (4, 8, 4096), (1, 1, 1100),
+                                   (3, 2, 200)], ids=lambda s: "b%dh%dn%d" % s)
+def test_fused_forward_matches_three_kernel_path(la, causal, shape):
+    """Sequences of at most 8 segments run the forward as one launch, a thread-block
+    cluster per sequence whose CTAs exchange their segment sums through shared memory.
+    Those sums are the segment-state kernel's and are added in the scan kernel's order,
+    so the output equals the three-kernel forward's bit for bit (that path forced here
+    through the failure hook with nothing withheld) and matches the oracle."""
+    import ctypes
+    B, H, N = shape
+    q, k, v = inputs.qkv(1700 + N, B, H, N, 64, 64, 0.125, inputs.BF16)
+    tq, tk, tv = (_t(x, inputs.BF16) for x in (q, k, v))
+    fused = la.la_forward(tq, tk, tv, causal=causal)
+    lib = la.load_library()
+    nbytes = la.la_forward_workspace_bytes(B, H, N, 64, 64, causal, la.LA_BF16)
+    ws = torch.zeros((nbytes,), dtype=torch.uint8, device=DEV)
+    three = torch.empty_like(fused)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = lib.la_debug_forward_fault(p(tq), p(tk), p(tv), p(three), B, H, N, 64, 64, int(causal),
+                                    la.LA_BF16, p(ws), nbytes, 1 << 30, 2_000_000_000,
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == la.LA_OK
+    torch.cuda.synchronize()
+    assert la.la_workspace_status(ws) == la.LA_OK
+    assert torch.equal(fused, three)
+    idx = list(range(B))[:2]
+    assert_close(fused[idx].float().cpu().numpy(), oracle.forward(q[idx], k[idx], v[idx], causal),
+                 "bf16", "out")
+
+
 # ------------------------------------------- backward reusing the forward's states
 
 @pytest.mark.parametrize("case", [(2, 3, 1000, 64, 64, inputs.BF16, True),
