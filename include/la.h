@@ -377,6 +377,8 @@ int la_workspace_status(void* workspace, size_t workspace_bytes, void* stream);
  */
 enum la_wait_site {
   LA_SITE_FORWARD_LOAD = 11,  /* forward chunk-attention kernel, waiting for a chunk's tiles */
+  LA_SITE_FORWARD_FUSED_LOAD = 16, /* one-launch forward, waiting for a chunk's K, V tiles
+                                      while it sums its segment's states */
   LA_SITE_BACKWARD_LOAD = 21  /* backward forward-direction kernel, waiting for a chunk's tiles */
 };
 int la_workspace_wait_site(void* workspace, size_t workspace_bytes, void* stream);
@@ -403,6 +405,19 @@ int la_debug_forward_fault(const void* q, const void* k, const void* v, void* ou
                            int B, int H, int N, int D, int M, int causal, int dtype,
                            void* workspace, size_t workspace_bytes, int withhold_load,
                            unsigned long long wait_limit_ns, void* stream);
+/*
+ * la_debug_forward_fused_fault: la_debug_forward_fault on the one-launch forward
+ * (a thread-block cluster per sequence; la_forward takes it when a sequence has at
+ * most 8 segments, and so does this hook; otherwise it is la_debug_forward_fault).
+ * CTA 0, the first segment's CTA of the first sequence, withholds its load number
+ * `withhold_load` (its loads of K, V while it sums the segment's states come first),
+ * so its wait runs out (LA_SITE_FORWARD_FUSED_LOAD for those); the CTA still
+ * reaches both of its cluster's barriers, so the cluster's other CTAs finish.
+ */
+int la_debug_forward_fused_fault(const void* q, const void* k, const void* v, void* out,
+                                 int B, int H, int N, int D, int M, int causal, int dtype,
+                                 void* workspace, size_t workspace_bytes, int withhold_load,
+                                 unsigned long long wait_limit_ns, void* stream);
 int la_debug_backward_fault(const void* q, const void* k, const void* v, const void* dout,
                             float* dq, float* dk, float* dv,
                             int B, int H, int N, int D, int M, int causal, int dtype,

@@ -28,7 +28,7 @@ __all__ = [
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_WORKSPACE, LA_ERR_CUDA, LA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 LA_ERR_TOO_LARGE = 5
 LA_F32, LA_BF16 = 0, 1
-LA_SITE_FORWARD_LOAD, LA_SITE_BACKWARD_LOAD = 11, 21
+LA_SITE_FORWARD_LOAD, LA_SITE_FORWARD_FUSED_LOAD, LA_SITE_BACKWARD_LOAD = 11, 16, 21
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "liblagb300.so")
@@ -65,6 +65,8 @@ _SIGNATURES = {
     "la_workspace_wait_site": (_c_int, [_vp, _c_size, _vp]),
     "la_debug_forward_fault": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _c_int,
                                                                     ctypes.c_ulonglong, _vp]),
+    "la_debug_forward_fused_fault": (_c_int, [_vp] * 4 + [_c_int] * 7 + [_vp, _c_size, _c_int,
+                                                                          ctypes.c_ulonglong, _vp]),
     "la_debug_backward_fault": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_vp, _c_size, _c_int,
                                                                      ctypes.c_ulonglong, _vp]),
 }

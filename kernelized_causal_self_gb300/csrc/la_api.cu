@@ -444,6 +444,26 @@ int la_debug_forward_fault(const void* q, const void* k, const void* v, void* ou
                                   st, &fh));
 }
 
+int la_debug_forward_fused_fault(const void* q, const void* k, const void* v, void* out, int B,
+                                 int H, int N, int D, int M, int causal, int dtype,
+                                 void* workspace, size_t workspace_bytes, int withhold_load,
+                                 unsigned long long wait_limit_ns, void* stream) {
+  if (!valid_dims(B, H, N, D, M) || !valid_dtype(dtype) || N == 0) return LA_ERR_INVALID_ARG;
+  if (!fault_args_ok(D, M, dtype, withhold_load, wait_limit_ns)) return LA_ERR_INVALID_ARG;
+  if (!ptrs_ok({q, k, v, out})) return LA_ERR_INVALID_ARG;
+  const size_t need = la_forward_workspace_bytes(B, H, N, D, M, causal, dtype);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need)
+    return LA_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  if (clear_header(workspace, st) != cudaSuccess) return LA_ERR_CUDA;
+  la::FaultHook fh;
+  fh.load = withhold_load;
+  fh.wait_ns = wait_limit_ns;
+  fh.fused = true;
+  return from_cuda(la::tc_forward(q, k, v, out, la::StateIO{}, B * H, N, causal != 0, workspace,
+                                  st, &fh));
+}
+
 int la_debug_backward_fault(const void* q, const void* k, const void* v, const void* dout,
                             float* dq, float* dk, float* dv, int B, int H, int N, int D, int M,
                             int causal, int dtype, void* workspace, size_t workspace_bytes,

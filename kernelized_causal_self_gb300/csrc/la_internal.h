@@ -42,6 +42,9 @@ struct StateIO {
 struct FaultHook {
   int load = -1;
   unsigned long long wait_ns = 0;
+  // run the one-launch (cluster) forward where the shape allows it, rather than the
+  // segment-state, scan and attention kernels
+  bool fused = false;
 };
 
 // Adds n to the process-wide kernel launch count reported by la_kernel_launches().

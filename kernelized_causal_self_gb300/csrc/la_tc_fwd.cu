@@ -640,6 +640,10 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // causal: nobody reads the last segment's sums
     if (!CAUSAL || seg + 1 < nseg) {
       auto load_kv = [&](int c) {
+        if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
+          ++issued;
+          return;
+        }
         const int st = issued % kAttStages;
         uint8_t* base = stages + st * 3 * kTile;
         mbar_arrive_expect_tx(&full[st], 2 * kTile);
@@ -1258,7 +1262,7 @@ cudaError_t tc_forward(const void* q, const void* k, const void* v, void* out, c
   const bool direct = causal && g.n_chunks == 1 && !(io.S != nullptr && !io.read_init);
   // a plain forward of sequences of at most 8 segments: one launch, a cluster per sequence
   if (!direct && !identity && io.S == nullptr && io.lens == nullptr && io.cu == nullptr &&
-      fault == nullptr && g.n_seg <= kMaxFusedSegments) {
+      (fault == nullptr || fault->fused) && g.n_seg <= kMaxFusedSegments) {
     auto fused = [&](auto kern) -> cudaError_t {
       if (!fused_fits(kern, g.n_seg)) return cudaErrorNotSupported;
       const cudaError_t err = launch_cluster_pdl(kern, dim3(g.n_items()), dim3(kAttThreads), kAttSmem,

@@ -173,20 +173,22 @@ def test_fault_hooks_reject_bad_arguments(lib):
     ok = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, H=2, N=1000, D=64, M=64, causal=1, dtype=1,
               ws=FAKE, wsb=1 << 24, load=1, ns=100_000)
 
-    def fwd(**kw):
-        a = dict(ok, **kw)
-        return lib.la_debug_forward_fault(a["q"], a["k"], a["v"], a["out"], a["B"], a["H"], a["N"],
-                                          a["D"], a["M"], a["causal"], a["dtype"], a["ws"], a["wsb"],
-                                          a["load"], a["ns"], None)
-    assert fwd(dtype=0) == la.LA_ERR_INVALID_ARG        # float32: not the tensor-core path
-    assert fwd(D=32, M=32) == la.LA_ERR_INVALID_ARG     # D = M = 64 only
-    assert fwd(load=-1) == la.LA_ERR_INVALID_ARG
-    assert fwd(ns=10) == la.LA_ERR_INVALID_ARG          # below 1 us
-    assert fwd(ns=3_000_000_000) == la.LA_ERR_INVALID_ARG
-    assert fwd(N=0) == la.LA_ERR_INVALID_ARG
-    assert fwd(q=0) == la.LA_ERR_INVALID_ARG
-    assert fwd(ws=0) == la.LA_ERR_WORKSPACE
-    assert fwd(wsb=16) == la.LA_ERR_WORKSPACE
+    for hook in (lib.la_debug_forward_fault, lib.la_debug_forward_fused_fault):
+        hook.restype = ctypes.c_int
+
+        def fwd(**kw):
+            a = dict(ok, **kw)
+            return hook(a["q"], a["k"], a["v"], a["out"], a["B"], a["H"], a["N"], a["D"], a["M"],
+                        a["causal"], a["dtype"], a["ws"], a["wsb"], a["load"], a["ns"], None)
+        assert fwd(dtype=0) == la.LA_ERR_INVALID_ARG        # float32: not the tensor-core path
+        assert fwd(D=32, M=32) == la.LA_ERR_INVALID_ARG     # D = M = 64 only
+        assert fwd(load=-1) == la.LA_ERR_INVALID_ARG
+        assert fwd(ns=10) == la.LA_ERR_INVALID_ARG          # below 1 us
+        assert fwd(ns=3_000_000_000) == la.LA_ERR_INVALID_ARG
+        assert fwd(N=0) == la.LA_ERR_INVALID_ARG
+        assert fwd(q=0) == la.LA_ERR_INVALID_ARG
+        assert fwd(ws=0) == la.LA_ERR_WORKSPACE
+        assert fwd(wsb=16) == la.LA_ERR_WORKSPACE
     args = [FAKE] * 7 + [1, 2, 1000, 64, 64, 1, 0, FAKE, 1 << 24, 1, 100_000, None]
     assert lib.la_debug_backward_fault(*args) == la.LA_ERR_INVALID_ARG   # dtype float32
     args[13] = 1

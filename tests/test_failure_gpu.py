@@ -50,6 +50,34 @@ def _case():
     return (B, H, N), (q, k, v, g)
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_fused_forward_load_wait_runs_out_and_the_cluster_finishes(la, causal):
+    """The one-launch forward (a thread-block cluster per sequence; this shape has 8
+    segments of one chunk): CTA 0 withholds its first load, the one of its segment-sum
+    phase, so its wait runs out after 100 us; it still reaches both of its cluster's
+    barriers, so the kernel returns on its own, the status names the site, and the next
+    ordinary call is exact."""
+    (B, H, N), (q, k, v, g) = _case()
+    tq, tk, tv = (inputs.to_torch(x, inputs.BF16, DEV) for x in (q, k, v))
+    out = torch.empty_like(tv)
+    nbytes = la.la_forward_workspace_bytes(B, H, N, 64, 64, causal, la.LA_BF16)
+    ws = torch.empty((nbytes,), dtype=torch.uint8, device=DEV)
+    lib = la.load_library()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    t0 = time.perf_counter()
+    rc = lib.la_debug_forward_fused_fault(_p(tq), _p(tk), _p(tv), _p(out), B, H, N, 64, 64,
+                                          int(causal), la.LA_BF16, _p(ws), nbytes, 0, LIMIT_NS, st)
+    assert rc == la.LA_OK
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 1.0          # returned on its own, well inside 2 s
+    assert la.la_workspace_wait_site(ws) == la.LA_SITE_FORWARD_FUSED_LOAD
+    assert la.la_workspace_status(ws) == la.LA_ERR_TIMEOUT
+    assert la.la_workspace_status(ws) == la.LA_OK   # read and cleared
+    la.la_forward(tq, tk, tv, causal=causal, out=out, workspace=ws)
+    assert la.la_workspace_status(ws) == la.LA_OK
+    assert_close(out.float().cpu().numpy(), oracle.forward(q, k, v, causal), "bf16", "out after")
+
+
 def test_forward_load_wait_runs_out_and_the_next_call_is_exact(la):
     (B, H, N), (q, k, v, g) = _case()
     tq, tk, tv = (inputs.to_torch(x, inputs.BF16, DEV) for x in (q, k, v))
