@@ -42,7 +42,7 @@ constexpr int kBwdStages = 2;
 constexpr int kSnapB = 2 * kDim * 128;  // state snapshot, hi and lo, 64 rows each
 constexpr int kGnB = 2 * kTile;         // gN hi and lo, 128 rows each
 constexpr int kArr = 8192;              // small float arrays
-constexpr int kLoB = 2 * kTile;         // phi(Q), phi(K) lo parts
+constexpr int kLoB = kTile;             // phi(Q) lo part
 constexpr int kBwdSmem =
     1024 + kBwdStages * 4 * kTile + kSnapB + kGnB + kLoB + kArr + 2048;
 
@@ -72,7 +72,6 @@ struct BwdSmem {
   uint8_t* gn_hi;
   uint8_t* gn_lo;
   uint8_t* qlo;
-  uint8_t* klo;
   float* arr;
   uint64_t* full;
   uint64_t* mma_bar;
@@ -88,8 +87,7 @@ struct BwdSmem {
     gn_hi = s_lo + kDim * 128;
     gn_lo = gn_hi + kTile;
     qlo = gn_lo + kTile;
-    klo = qlo + kTile;
-    arr = reinterpret_cast<float*>(klo + kTile);
+    arr = reinterpret_cast<float*>(qlo + kTile);
     uint8_t* misc = reinterpret_cast<uint8_t*>(arr) + kArr;
     full = reinterpret_cast<uint64_t*>(misc);
     mma_bar = full + kBwdStages;
