@@ -100,6 +100,14 @@ struct BwdSmem {
 
 enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 
+// Named barrier 1 over the dk/dv kernel's 512 threads: the threads that hand data
+// over arrive without waiting, the ones that take it wait.
+__device__ __forceinline__ void named_arrive_all() { asm volatile("bar.arrive 1, 512;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_all() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// The dk/dv kernel's second MMA group is issued by the first thread of warp 2 (TMEM
+// lanes 64-95, whose R exchange only hands data over), thread 0 issues the rest.
+constexpr int kG2Issuer = 64;
+
 // The reverse-direction kernel runs 512 threads: warp w covers TMEM lane quarter
 // w % 4 (rows 32 (w % 4) .. + 31) and column quarter qc = w / 4 (16 of the 64
 // state columns, the 32-column slice qc of the chunk's 128), so every row is
@@ -949,7 +957,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int s = 0; s < kBwdStages; ++s) mbar_init(&sm.full[s], 1);
     mbar_init(sm.mma_bar, 1);
     mbar_init(&sm.sbar[1], 1);
-    mbar_init(sm.drain, 1);
+    mbar_init(sm.drain, 2);  // thread 0's and the second group's issuer's MMAs
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -1147,25 +1155,11 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_st16(tl + kRH + 16 * qc, pth);
       tmem_st16(tl + kRL + 16 * qc, ptl);
       sync_tc();
-      if (tid == 0) {
-        const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
-        const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
-        issue_state_terms(smem_u32(kt), smem_u32(vt), smem_u32(sm.s_hi), smem_u32(sm.s_lo));
-        const uint32_t idV2 = idesc_bf16(128, 128, false, true), idV = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T [gN_hi | gN_lo] (N blocks gla - gha apart)
-          mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gha + k * 2048, gla - gha, 1024), idV2, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // dphiK += T_hi^T [phi(Q)_hi | phi(Q)_lo]
-          mma_ts(tbase + kRK, tbase + kRH + k * 8, sdesc(qa + k * 2048, ql - qa, 1024), idV2, 1);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)  // + T_lo^T phi(Q)_hi
-          mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
-        mma_commit(sm.mma_bar);
-      }
-      {  // R_run += this chunk's phi(Q)^T gN and r += sum gd phi(Q), while the second
-         // group runs; the lo-part rows (lanes 64-127) pass through the chunk's G
-         // tile (no MMA reads it any more)
+      {  // R_run += this chunk's phi(Q)^T gN and r += sum gd phi(Q) (the sums were
+         // issued with the first group); the lo-part rows (lanes 64-127) pass through
+         // the chunk's G tile (no MMA reads it any more). Their threads hand them over
+         // through named barrier 1 without waiting, and one of them then issues the
+         // second group, so the hi-part threads' update runs under that issue.
         if (!wait_uniform(&sm.sbar[1], sph, hdr, 34)) break;
         sph ^= 1;
         fence_after_sync();
@@ -1178,8 +1172,26 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             xs[drow * 16 + ((4 * qc + j) ^ (drow & 15))] =
                 make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          named_arrive_all();
+          if (tid == kG2Issuer) {
+            const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
+            const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+            issue_state_terms(smem_u32(kt), smem_u32(vt), smem_u32(sm.s_hi), smem_u32(sm.s_lo));
+            const uint32_t idV2 = idesc_bf16(128, 128, false, true), idV = idesc_bf16(128, 64, false, true);
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T [gN_hi | gN_lo] (N blocks gla - gha apart)
+              mma_ts(tbase + kRV, tbase + kRP + k * 8, sdesc(gha + k * 2048, gla - gha, 1024), idV2, 1);
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)  // dphiK += T_hi^T [phi(Q)_hi | phi(Q)_lo]
+              mma_ts(tbase + kRK, tbase + kRH + k * 8, sdesc(qa + k * 2048, ql - qa, 1024), idV2, 1);
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)  // + T_lo^T phi(Q)_hi
+              mma_ts(tbase + kRK, tbase + kRL + k * 8, sdesc(qa + k * 2048, 1024, 1024), idV, 1);
+            mma_commit(sm.mma_bar);
+          }
+        } else {
+          named_sync_all();
         }
-        __syncthreads();
         if (dthread) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -1248,7 +1260,9 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     bulk_wait_all<0>();
   }
-  drain_mmas(sm.drain, hdr, 35);
+  // every MMA of both issuing threads completes before TMEM is freed (time-bounded only)
+  if (tid == 0 || tid == kG2Issuer) mma_commit(sm.drain);
+  if (tid == 0 && !mbar_wait(sm.drain, 0)) record_timeout(hdr, 35);
   sync_tc();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
