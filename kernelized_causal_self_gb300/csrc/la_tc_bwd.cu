@@ -75,7 +75,7 @@ struct BwdSmem {
   float* arr;
   uint64_t* full;
   uint64_t* mma_bar;
-  uint64_t* sbar;  // sbar[1]: the deferred state MMAs (and all the issuer issued before them)
+  uint64_t* sbar;  // sbar[1]: the chunk's R sums (and all their issuer issued before them)
   uint64_t* drain;  // every MMA of the CTA is done (end of the kernel)
   uint32_t* tslot;
   __device__ explicit BwdSmem(uint8_t* raw) {
@@ -104,14 +104,16 @@ enum { kQ = 0, kK = 1, kV = 2, kG = 3 };
 // over arrive without waiting, the ones that take it wait.
 __device__ __forceinline__ void named_arrive_all() { asm volatile("bar.arrive 1, 512;" ::: "memory"); }
 __device__ __forceinline__ void named_sync_all() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
-// The dk/dv kernel's second MMA group is issued by the first thread of warp 2 (TMEM
-// lanes 64-95, whose R exchange only hands data over), thread 0 issues the rest.
+// The dk/dv kernel's per-chunk R sums and its second MMA group are issued by the
+// first thread of warp 2 (TMEM lanes 64-95: its slice of the P / T epilogue is
+// masked out entirely and its R exchange only hands data over); thread 0 issues
+// the first group (P, W).
 constexpr int kG2Issuer = 64;
 
 // The reverse-direction kernel runs 512 threads: warp w covers TMEM lane quarter
 // w % 4 (rows 32 (w % 4) .. + 31) and column quarter qc = w / 4 (16 of the 64
 // state columns, the 32-column slice qc of the chunk's 128), so every row is
-// handled by four threads; thread 0 issues its MMAs. Where a TMEM region is
+// handled by four threads; threads 0 and 64 issue its MMAs. Where a TMEM region is
 // compacted in place (fp32 P into bf16 P_L), all reads finish before a barrier
 // and the writes follow it.
 constexpr int kBTQ = 512;
@@ -949,8 +951,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // R carry: row d = 32 (lq % 2) + lane, held by the threads of TMEM lanes 0-63
   const int drow = 32 * (lq & 1) + lane;
   const bool dthread = lq < 2;
-  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
-  // stores) belong to warp 1's first thread, so that the two issue in parallel
+  // threads 0 and 64 issue the MMAs; the TMA loads and stores (and the waits on
+  // the stores) belong to warp 1's first thread, so that they issue in parallel
   const bool tma_thread = tid == 32;
 
   if (tid == 0) {
@@ -1078,7 +1080,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     if (tid == 0) {
       const uint32_t qa = smem_u32(qt), ka = smem_u32(kt), va = smem_u32(vt);
-      const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo), ql = smem_u32(sm.qlo);
       const uint32_t ha = smem_u32(sm.s_hi), la = smem_u32(sm.s_lo);
       if (CAUSAL) {
         const uint32_t idP = idesc_bf16(128, 128, false, false);
@@ -1092,22 +1093,6 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (!CAUSAL) issue_state_terms(ka, va, ha, la);  // causal: in the second group
       mma_commit(sm.mma_bar);
-      if (CAUSAL) {  // this chunk's phi(Q)^T gN, awaited when the state is updated:
-        // phi(Q)^T hi and lo stacked as one M = 128 MN-major operand (ql - qa
-        // bytes apart) times gN hi, then gN lo; rows d of the hi part in TMEM
-        // lanes 0-63, of the lo part in lanes 64-127
-        const uint32_t idR = idesc_bf16(128, 64, true, true);
-        const uint32_t lbo = ql - qa;
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024),
-                 idR, k);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024),
-                 idR, 1);
-        mma_commit(&sm.sbar[1]);
-      }
     }
     {  // the next chunk's den, gd: their latency hides behind the first MMA group
       RevCursor nx = cc;
@@ -1123,6 +1108,26 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
 
     if (CAUSAL) {
+      if (tid == kG2Issuer) {
+        // this chunk's phi(Q)^T gN, awaited when the state is updated, issued while
+        // the other warps run the epilogue below (warp 2's slice of it, query
+        // columns 0-31 of key rows 64-95, is masked out entirely): phi(Q)^T hi
+        // and lo stacked as one M = 128 MN-major operand (ql - qa bytes apart)
+        // times gN hi, then gN lo; rows d of the hi part in TMEM lanes 0-63, of
+        // the lo part in lanes 64-127
+        const uint32_t qa = smem_u32(qt), lbo = smem_u32(sm.qlo) - qa;
+        const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
+        const uint32_t idR = idesc_bf16(128, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gha + k * 2048, 1024, 1024),
+                 idR, k);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024),
+                 idR, 1);
+        mma_commit(&sm.sbar[1]);
+      }
       // key row keeps query columns i >= row; slice qc of P^T and of T^T
       uint32_t pph[16], pth[16], ptl[16];
       masked_pack_slice<false>(tl + kRP, qc, lq, row, pph);  // P_L^T enters the MMA as bf16
@@ -1156,7 +1161,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_st16(tl + kRL + 16 * qc, ptl);
       sync_tc();
       {  // R_run += this chunk's phi(Q)^T gN and r += sum gd phi(Q) (the sums were
-         // issued with the first group); the lo-part rows (lanes 64-127) pass through
+         // issued under the epilogue above); the lo-part rows (lanes 64-127) pass through
          // the chunk's G tile (no MMA reads it any more). Their threads hand them over
          // through named barrier 1 without waiting, and one of them then issues the
          // second group, so the hi-part threads' update runs under that issue.
