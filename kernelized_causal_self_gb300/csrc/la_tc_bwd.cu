@@ -994,11 +994,14 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // the state terms, first into the gradient accumulators: dV = phi(K) [R_hi | R_lo]
   // (B = R rows d read MN-major, n = m contiguous; hi and lo tiles la - ha apart)
   // and dphiK = V [R_hi; R_lo]^T (B = R rows d read K-major, the lo rows after the hi)
-  auto issue_state_terms = [&](uint32_t ka, uint32_t va, uint32_t ha, uint32_t la) {
-    const uint32_t idVn = idesc_bf16(128, 128, false, true), idKn = idesc_bf16(128, 128, false, false);
+  auto issue_state_dv = [&](uint32_t ka, uint32_t ha, uint32_t la) {
+    const uint32_t idVn = idesc_bf16(128, 128, false, true);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       mma_ss(tbase + kRV, sdesc(ka + k * 32, 16, 1024), sdesc(ha + k * 2048, la - ha, 1024), idVn, k);
+  };
+  auto issue_state_dk = [&](uint32_t va, uint32_t ha) {
+    const uint32_t idKn = idesc_bf16(128, 128, false, false);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       mma_ss(tbase + kRK, sdesc(va + k * 32, 16, 1024), sdesc(ha + k * 32, 16, 1024), idKn, k);
@@ -1091,7 +1094,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int k = 0; k < 4; ++k)  // W^T = V G^T
           mma_ss(tbase + kRT, sdesc(va + k * 32, 16, 1024), sdesc(ga + k * 32, 16, 1024), idP, k);
       }
-      if (!CAUSAL) issue_state_terms(ka, va, ha, la);  // causal: in the second group
+      if (!CAUSAL) {  // causal: dphiK's after the R sums, dV's in the second group
+        issue_state_dv(ka, ha, la);
+        issue_state_dk(va, ha);
+      }
       mma_commit(sm.mma_bar);
     }
     {  // the next chunk's den, gd: their latency hides behind the first MMA group
@@ -1127,6 +1133,8 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mma_ss(tbase + kRR, sdesc(qa + k * 2048, lbo, 1024), sdesc(gla + k * 2048, 1024, 1024),
                  idR, 1);
         mma_commit(&sm.sbar[1]);
+        // dphiK's state term (its accumulator is free: the previous chunk's dk was read)
+        issue_state_dk(smem_u32(vt), smem_u32(sm.s_hi));
       }
       // key row keeps query columns i >= row; slice qc of P^T and of T^T
       uint32_t pph[16], pth[16], ptl[16];
@@ -1181,7 +1189,7 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (tid == kG2Issuer) {
             const uint32_t qa = smem_u32(qt), ql = smem_u32(sm.qlo);
             const uint32_t gha = smem_u32(sm.gn_hi), gla = smem_u32(sm.gn_lo);
-            issue_state_terms(smem_u32(kt), smem_u32(vt), smem_u32(sm.s_hi), smem_u32(sm.s_lo));
+            issue_state_dv(smem_u32(kt), smem_u32(sm.s_hi), smem_u32(sm.s_lo));
             const uint32_t idV2 = idesc_bf16(128, 128, false, true), idV = idesc_bf16(128, 64, false, true);
 #pragma unroll
             for (int k = 0; k < kC / 16; ++k)  // dV += P_L^T [gN_hi | gN_lo] (N blocks gla - gha apart)
