@@ -482,11 +482,12 @@ constexpr int kAttStages = 2;  // 2 CTAs per SM
 constexpr int kSnapBytes = kDim * 128 + 16 * 128 + 16 * 128;
 constexpr int kAttSmem = 1024 + kAttStages * 3 * kTile + kSnapBytes + 2048;
 
-// TMEM columns (256 per CTA, two CTAs per SM). The first MMA group writes P
-// and the state increment; the second, issued once both are read, writes the
-// output over P's dead upper half and the spent increment.
+// TMEM columns (256 per CTA, two CTAs per SM). P is written first, and the
+// second group, issued once P is read, writes the output over P's dead upper
+// half; the state increment has columns of its own, so that it can be formed
+// while P is read and read while the second group runs.
 constexpr uint32_t kColP = 0;     // 128: phi(Q) phi(K)^T; then bf16 P_L in [0, 64)
-constexpr uint32_t kColS = 128;   // 64: dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+constexpr uint32_t kColS = 192;   // 64: dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
 constexpr uint32_t kColO = 64;    // 80: numerator in [64, 128), denominator in column 128
 constexpr uint32_t kTmemCols = 256;
 
@@ -526,7 +527,8 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);  // kAttStages
   uint64_t* mma_bar = full + kAttStages;
   uint64_t* drain = mma_bar + 1;  // every MMA of the CTA is done (end of the kernel)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sbar = drain + 1;     // the chunk's state increment
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sbar + 1);
   volatile int* ring = reinterpret_cast<volatile int*>(tslot + 1);  // kRing items (tickets)
 
   constexpr bool TICKETS = VARLEN;  // items dealt by tickets (else round robin)
@@ -537,13 +539,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // of quarter 2 holds Z (the TMEM lanes the stacked increment lands in)
   const bool sthread = q4 < 2;
   const bool zthread = q4 == 2 && lane == 0;
-  // thread 0 issues the MMAs; the TMA loads and stores (and the waits on the
-  // stores) belong to warp 1's first thread, so that the two issue in parallel
+  // thread 0 issues the MMAs but the state increment's, which warp 4's first
+  // thread issues while the others read P (warp 4's share of that epilogue, key
+  // columns 64-127 of query rows 0-31, is masked out entirely); the TMA loads
+  // and stores (and the waits on the stores) belong to warp 1's first thread
   const bool tma_thread = tid == 32;
+  constexpr int kSIssuer = 128;
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
-    mbar_init(drain, 1);
+    mbar_init(sbar, 1);
+    mbar_init(drain, 2);  // the MMAs of both issuing threads
     fence_mbar_init();
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_o);
@@ -627,7 +633,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   bool ok = true;
   long long consumed = 0;
-  uint32_t mma_phase = 0;
+  uint32_t mma_phase = 0, s_phase = 0;
   if constexpr (FUSED) {
     // ---------------------------------------------------------------- fused
     const int nseg = g.n_seg, seg = (int)cluster_ctarank(), bh = blockIdx.x / nseg;
@@ -875,13 +881,6 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // P = phi(Q) phi(K)^T
           mma_ss(tbase + kColP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
-        // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
-        // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
-        const uint32_t idS = idesc_bf16(128, 64, true, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kColS, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
-                 sdesc(ka + k * 2048, 1024, 1024), idS, k);
       } else {  // num and den = phi(Q) [S^T; Z; 0]^T, the state being the total
         const uint32_t idO = idesc_bf16(128, 80, false, false);
 #pragma unroll
@@ -906,6 +905,17 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
 
     if (CAUSAL) {
+      if (tid == kSIssuer) {
+        // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
+        // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+        const uint32_t va = smem_u32(vt), ka = smem_u32(kt), oa = smem_u32(ones);
+        const uint32_t idS = idesc_bf16(128, 64, true, true);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_ss(tbase + kColS, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+                 sdesc(ka + k * 2048, 1024, 1024), idS, k);
+        mma_commit(sbar);
+      }
       // masked P row -> bf16, written back over the first 64 TMEM columns; its
       // row sums (the intra-chunk part of den) come from an MMA with ones
       uint32_t pk[2][16];
@@ -932,17 +942,8 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 16; ++c) pk[t][c] = 0u;
         }
       }
-      // state update: S^T += dS^T (row `row`), Z += dZ (TMEM lane 64), this half's columns
-      if (q4 <= 2) {
-        uint32_t r[32];
-        tmem_ld32(tl + kColS + 32 * h, r);
-        if (sthread || zthread) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
-        }
-      }
       fence_before_sync();
-      __syncthreads();  // every read of fp32 P and of the increment is done before they are overwritten
+      __syncthreads();  // every read of fp32 P is done before P_L overwrites it
       fence_after_sync();
 #pragma unroll
       for (int t = 0; t < 2; ++t) tmem_st16(tl + kColP + 16 * (2 * h + t), pk[t]);
@@ -966,7 +967,26 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  idPV, 1);
         mma_commit(mma_bar);
       }
-      if (!wait_uniform(mma_bar, mma_phase, hdr, 13, wlim)) {
+      // state update while the second group runs: S^T += dS^T (row `row`), Z += dZ
+      // (TMEM lane 64), this half's columns; a warp whose wait runs out leaves the
+      // loop at the barrier below with the others
+      bool sok = true;
+      if (q4 <= 2) {  // warp-uniform
+        sok = __all_sync(0xffffffffu, mbar_wait(sbar, s_phase, wlim));
+        if (sok) {
+          fence_after_sync();
+          uint32_t r[32];
+          tmem_ld32(tl + kColS + 32 * h, r);
+          if (sthread || zthread) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
+          }
+        }
+      }
+      s_phase ^= 1;
+      const bool gok = mbar_wait(mma_bar, mma_phase, wlim);
+      if (!__syncthreads_and(sok && gok ? 1 : 0)) {
+        if (tid == 0) record_timeout(hdr, sok ? 13 : 18);
         ok = false;
         break;
       }
@@ -1036,7 +1056,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     bulk_wait_all<0>();
   }
-  drain_mmas(drain, hdr, 15);
+  // every MMA of both issuing threads completes before TMEM is freed (time-bounded only)
+  if (tid == 0 || tid == kSIssuer) mma_commit(drain);
+  if (tid == 0 && !mbar_wait(drain, 0)) record_timeout(hdr, 15);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
