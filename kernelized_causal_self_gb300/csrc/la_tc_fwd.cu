@@ -545,6 +545,9 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // and stores (and the waits on the stores) belong to warp 1's first thread
   const bool tma_thread = tid == 32;
   constexpr int kSIssuer = 128;
+  // the per-stream-length kernels keep the increment in thread 0's first group
+  // and read it with P (the later read costs them registers they do not have)
+  constexpr bool kLateS = !VARLEN;
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_bar, 1);
@@ -597,6 +600,15 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     cc.start(g, true);
     cp.start(g, true);
   }
+  // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times phi(K)
+  // (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
+  auto issue_ds = [&](uint32_t va, uint32_t ka, uint32_t oa) {
+    const uint32_t idS = idesc_bf16(128, 64, true, true);
+#pragma unroll
+    for (int k = 0; k < kC / 16; ++k)
+      mma_ss(tbase + kColS, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
+             sdesc(ka + k * 2048, 1024, 1024), idS, k);
+  };
   long long issued = 0;
   auto issue = [&](CursorT<VARLEN>& c) {
     if (g.faulty() && issued == g.fault_load) {  // test hook: this load is withheld
@@ -881,6 +893,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // P = phi(Q) phi(K)^T
           mma_ss(tbase + kColP, sdesc(qa + k * 32, 16, 1024), sdesc(ka + k * 32, 16, 1024), idP, k);
+        if (!kLateS) issue_ds(va, ka, oa);
       } else {  // num and den = phi(Q) [S^T; Z; 0]^T, the state being the total
         const uint32_t idO = idesc_bf16(128, 80, false, false);
 #pragma unroll
@@ -905,15 +918,8 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     fence_after_sync();
 
     if (CAUSAL) {
-      if (tid == kSIssuer) {
-        // [V^T; 1^T] (M = 128 MN-major, rows 64.. from the ones block) times
-        // phi(K) (N = 64 MN-major): dS^T [m][d] in lanes 0-63, dZ[d] in lanes 64-127
-        const uint32_t va = smem_u32(vt), ka = smem_u32(kt), oa = smem_u32(ones);
-        const uint32_t idS = idesc_bf16(128, 64, true, true);
-#pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_ss(tbase + kColS, sdesc(va + k * 2048, oa - (va + k * 2048), 1024),
-                 sdesc(ka + k * 2048, 1024, 1024), idS, k);
+      if (kLateS && tid == kSIssuer) {
+        issue_ds(smem_u32(vt), smem_u32(kt), smem_u32(ones));
         mma_commit(sbar);
       }
       // masked P row -> bf16, written back over the first 64 TMEM columns; its
@@ -942,8 +948,16 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 16; ++c) pk[t][c] = 0u;
         }
       }
+      if (!kLateS && q4 <= 2) {  // state update: S^T += dS^T (row `row`), Z += dZ (TMEM lane 64)
+        uint32_t r[32];
+        tmem_ld32(tl + kColS + 32 * h, r);
+        if (sthread || zthread) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) srun[j] += __uint_as_float(r[j]);
+        }
+      }
       fence_before_sync();
-      __syncthreads();  // every read of fp32 P is done before P_L overwrites it
+      __syncthreads();  // every read of fp32 P (and of the increment) is done before P_L overwrites it
       fence_after_sync();
 #pragma unroll
       for (int t = 0; t < 2; ++t) tmem_st16(tl + kColP + 16 * (2 * h + t), pk[t]);
@@ -971,7 +985,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // (TMEM lane 64), this half's columns; a warp whose wait runs out leaves the
       // loop at the barrier below with the others
       bool sok = true;
-      if (q4 <= 2) {  // warp-uniform
+      if (kLateS && q4 <= 2) {  // warp-uniform
         sok = __all_sync(0xffffffffu, mbar_wait(sbar, s_phase, wlim));
         if (sok) {
           fence_after_sync();
@@ -983,7 +997,7 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
         }
       }
-      s_phase ^= 1;
+      if (kLateS) s_phase ^= 1;
       const bool gok = mbar_wait(mma_bar, mma_phase, wlim);
       if (!__syncthreads_and(sok && gok ? 1 : 0)) {
         if (tid == 0) record_timeout(hdr, sok ? 13 : 18);
