@@ -46,9 +46,27 @@ constexpr int kLoB = kTile;             // phi(Q) lo part
 constexpr int kBwdSmem =
     1024 + kBwdStages * 4 * kTile + kSnapB + kGnB + kLoB + kArr + 2048;
 
+// Two float32 lanes at once (one packed instruction, each lane rounded as alone).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
-  lo = pack_bf16(a - bf16_lo_f(hi), b - bf16_hi_f(hi));
+  const float2 r = sub2(make_float2(a, b), make_float2(bf16_lo_f(hi), bf16_hi_f(hi)));
+  lo = pack_bf16(r.x, r.y);
 }
 
 // 16 consecutive bf16 of row `row`, logical 16-byte chunks c0, c0+1 -> float.
@@ -1147,8 +1165,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int i0 = 32 * qc + 2 * c;
-            split_bf16(__uint_as_float(r[2 * c]) * invs[i0] + gds[i0],
-                       __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1], pth[c], ptl[c]);
+            const float2 t = fma2(make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
+                                  *reinterpret_cast<const float2*>(invs + i0),
+                                  *reinterpret_cast<const float2*>(gds + i0));
+            split_bf16(t.x, t.y, pth[c], ptl[c]);
           }
         } else {
 #pragma unroll
