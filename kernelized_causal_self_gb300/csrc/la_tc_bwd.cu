@@ -55,6 +55,20 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
         "l"(*reinterpret_cast<uint64_t*>(&c)));
   return *reinterpret_cast<float2*>(&d);
 }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
 __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;"
@@ -167,7 +181,8 @@ __device__ __forceinline__ void phi_quarter_split_impl(uint8_t* tile, uint8_t* l
       const float a = valid ? phi_fast(bf16_lo_f(u[q])) : 0.f;
       const float b = valid ? phi_fast(bf16_hi_f(u[q])) : 0.f;
       u[q] = pack_bf16(a, b);
-      l[q] = pack_bf16(a - bf16_lo_f(u[q]), b - bf16_hi_f(u[q]));
+      const float2 e = sub2(make_float2(a, b), make_float2(bf16_lo_f(u[q]), bf16_hi_f(u[q])));
+      l[q] = pack_bf16(e.x, e.y);
       z[8 * c + 2 * q] = a;
       z[8 * c + 2 * q + 1] = b;
     }
@@ -708,7 +723,11 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           float gn[16];
           load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) gn[q] *= inv;
+          for (int q = 0; q < 16; q += 2) {
+            const float2 x = mul2(make_float2(gn[q], gn[q + 1]), make_float2(inv, inv));
+            gn[q] = x.x;
+            gn[q + 1] = x.y;
+          }
           store_split_quarter(gt, vt, row, qc, gn);
           fence_proxy_async_smem();
           fence_before_sync();
@@ -722,7 +741,12 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           load_row16(qt, row, 2 * qc, qv);
           load_row16(qlt, row, 2 * qc, ql);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) z[q] = gd * (qv[q] + ql[q]);
+          for (int q = 0; q < 16; q += 2) {
+            const float2 x = mul2(make_float2(gd, gd), add2(make_float2(qv[q], qv[q + 1]),
+                                                            make_float2(ql[q], ql[q + 1])));
+            z[q] = x.x;
+            z[q + 1] = x.y;
+          }
           const float cs = warp_column_sums16(z);
           if (lane < 16) dzr[lq * 64 + 16 * qc + lane] = cs;
         } else {
@@ -790,8 +814,14 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
         float qv[16], o[16];
         load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + gd * zs[16 * qc + q]) * fminf(qv[q], 1.f);
+        for (int q = 0; q < 16; q += 2) {
+          const float2 t = fma2(make_float2(gd, gd), *reinterpret_cast<const float2*>(zs + 16 * qc + q),
+                                add2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])),
+                                     make_float2(__uint_as_float(r2[q]), __uint_as_float(r2[q + 1]))));
+          const float2 x = mul2(t, make_float2(fminf(qv[q], 1.f), fminf(qv[q + 1], 1.f)));
+          o[q] = x.x;
+          o[q + 1] = x.y;
+        }
         uint8_t* sq = qc < 2 ? kt : klt;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -1083,9 +1113,13 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       float gn[16];
       load_row16(gt, row, 2 * qc, gn);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        gn[q] *= inv;
-        z[q] *= gdr;
+      for (int q = 0; q < 16; q += 2) {
+        const float2 x = mul2(make_float2(gn[q], gn[q + 1]), make_float2(inv, inv));
+        const float2 y = mul2(make_float2(z[q], z[q + 1]), make_float2(gdr, gdr));
+        gn[q] = x.x;
+        gn[q + 1] = x.y;
+        z[q] = y.x;
+        z[q + 1] = y.y;
       }
       store_split_quarter(sm.gn_hi, sm.gn_lo, row, qc, gn);
       const float cs = warp_column_sums16(z);
@@ -1265,8 +1299,14 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_ld16x2(tl + kRK + 16 * qc, r, tl + kRK + 64 + 16 * qc, r2);
       float o[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        o[q] = ((__uint_as_float(r[q]) + __uint_as_float(r2[q])) + rsnap[16 * qc + q]) * fminf(kv[q], 1.f);
+      for (int q = 0; q < 16; q += 2) {
+        const float2 t = add2(add2(make_float2(__uint_as_float(r[q]), __uint_as_float(r[q + 1])),
+                                   make_float2(__uint_as_float(r2[q]), __uint_as_float(r2[q + 1]))),
+                              *reinterpret_cast<const float2*>(rsnap + 16 * qc + q));
+        const float2 x = mul2(t, make_float2(fminf(kv[q], 1.f), fminf(kv[q + 1], 1.f)));
+        o[q] = x.x;
+        o[q + 1] = x.y;
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         *reinterpret_cast<float4*>(sk + sw128(row, (qc & 1) * 64 + c * 16)) =
