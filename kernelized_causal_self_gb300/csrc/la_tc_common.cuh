@@ -232,6 +232,37 @@ struct RevCursor {
   }
 };
 
+// Two float32 lanes at once (one packed instruction, each lane rounded as alone).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 __device__ __forceinline__ float bf16_lo_f(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
@@ -316,7 +347,8 @@ __device__ __forceinline__ uint32_t psi2_bf16(uint32_t u) {
   const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
   const float2 m = __bfloat1622float2(__hmin2(x, zero));
   const float2 p = __bfloat1622float2(__hmax2(x, zero));
-  const __nv_bfloat162 r = __floats2bfloat162_rn(__expf(m.x) - 1.f + p.x, __expf(m.y) - 1.f + p.y);
+  const float2 e = add2(sub2(make_float2(__expf(m.x), __expf(m.y)), make_float2(1.f, 1.f)), p);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(e.x, e.y);
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 

@@ -1028,9 +1028,12 @@ tc_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int c = 0; c < 4; ++c) {
         uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          o[q] = pack_bf16(__uint_as_float(r[8 * c + 2 * q]) * inv,
-                           __uint_as_float(r[8 * c + 2 * q + 1]) * inv);
+        for (int q = 0; q < 4; ++q) {
+          const float2 x = mul2(make_float2(__uint_as_float(r[8 * c + 2 * q]),
+                                            __uint_as_float(r[8 * c + 2 * q + 1])),
+                                make_float2(inv, inv));
+          o[q] = pack_bf16(x.x, x.y);
+        }
         *reinterpret_cast<uint4*>(qt + sw128(row, (4 * h + c) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
