@@ -676,10 +676,11 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int j0 = 32 * qc + 2 * c;
-              const float w0 = __uint_as_float(c < 8 ? rw[2 * c] : rw2[2 * c - 16]);
-              const float w1 = __uint_as_float(c < 8 ? rw[2 * c + 1] : rw2[2 * c - 15]);
-              split_bf16(qc < lq || j0 <= row ? w0 * inv + gd : 0.f,
-                         qc < lq || j0 + 1 <= row ? w1 * inv + gd : 0.f, th[c], tlo[c]);
+              const float2 t = fma2(make_float2(__uint_as_float(c < 8 ? rw[2 * c] : rw2[2 * c - 16]),
+                                                __uint_as_float(c < 8 ? rw[2 * c + 1] : rw2[2 * c - 15])),
+                                    make_float2(inv, inv), make_float2(gd, gd));
+              split_bf16(qc < lq || j0 <= row ? t.x : 0.f, qc < lq || j0 + 1 <= row ? t.y : 0.f, th[c],
+                         tlo[c]);
             }
           } else {
 #pragma unroll
@@ -1177,9 +1178,10 @@ tc_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int i0 = 32 * qc + 2 * c;
-            split_bf16(i0 >= row ? __uint_as_float(r[2 * c]) * invs[i0] + gds[i0] : 0.f,
-                       i0 + 1 >= row ? __uint_as_float(r[2 * c + 1]) * invs[i0 + 1] + gds[i0 + 1] : 0.f,
-                       pth[c], ptl[c]);
+            const float2 t = fma2(make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
+                                  *reinterpret_cast<const float2*>(invs + i0),
+                                  *reinterpret_cast<const float2*>(gds + i0));
+            split_bf16(i0 >= row ? t.x : 0.f, i0 + 1 >= row ? t.y : 0.f, pth[c], ptl[c]);
           }
         }
       } else {
