@@ -616,7 +616,8 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
       // ---- epilogue of the first group: den, G.num
       if (!bad && warp_wait(sm.bar(QSmem::kG1Done), ph, abort, hdr, 22)) {
         fence_after_sync();
-        float dpart = 0.f, npart = 0.f;
+        // the partial sums run in two lanes (even and odd columns), added at the end
+        float2 dp = make_float2(0.f, 0.f), np = make_float2(0.f, 0.f);
         if (CAUSAL && qc <= lq) {  // warp-uniform; slice qc of P and W in two 16-column halves
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -624,17 +625,19 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
             tmem_ld16x2(tl + kFP + 32 * qc + 16 * h, rp, tl + kFW + 32 * qc + 16 * h, rw);
             if (qc < lq) {  // below the diagonal block: nothing is masked
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float p = __uint_as_float(rp[c]);
-                dpart += p;
-                npart += p * __uint_as_float(rw[c]);
+              for (int c = 0; c < 16; c += 2) {
+                const float2 pp = make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1]));
+                dp = add2(dp, pp);
+                np = fma2(pp, make_float2(__uint_as_float(rw[c]), __uint_as_float(rw[c + 1])), np);
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float p = 32 * qc + 16 * h + c <= row ? __uint_as_float(rp[c]) : 0.f;
-                dpart += p;
-                npart += p * __uint_as_float(rw[c]);
+              for (int c = 0; c < 16; c += 2) {
+                const int j = 32 * qc + 16 * h + c;
+                const float2 pp = make_float2(j <= row ? __uint_as_float(rp[c]) : 0.f,
+                                              j + 1 <= row ? __uint_as_float(rp[c + 1]) : 0.f);
+                dp = add2(dp, pp);
+                np = fma2(pp, make_float2(__uint_as_float(rw[c]), __uint_as_float(rw[c + 1])), np);
               }
             }
           }
@@ -648,11 +651,14 @@ __device__ __forceinline__ void bwd_q_workers(QSmem& sm, const Geometry& g, uint
           load_row16(gt, row, 2 * qc, gv);
           load_row16(qt, row, 2 * qc, qv);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            npart += gv[q] * (__uint_as_float(ro[q]) + __uint_as_float(ro2[q]));
-            dpart += qv[q] * zs[16 * qc + q];
+          for (int q = 0; q < 16; q += 2) {
+            const float2 o = add2(make_float2(__uint_as_float(ro[q]), __uint_as_float(ro[q + 1])),
+                                  make_float2(__uint_as_float(ro2[q]), __uint_as_float(ro2[q + 1])));
+            np = fma2(make_float2(gv[q], gv[q + 1]), o, np);
+            dp = fma2(make_float2(qv[q], qv[q + 1]), *reinterpret_cast<const float2*>(zs + 16 * qc + q), dp);
           }
         }
+        const float dpart = dp.x + dp.y, npart = np.x + np.y;
         rsum[qc * 128 + row] = dpart;
         gnum[qc * 128 + row] = npart;
         fence_before_sync();
